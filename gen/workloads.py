@@ -1,0 +1,104 @@
+"""The five synthetic workloads of the CSA2 decode path, as input recipes.
+
+Only shapes, seeds and which generator stream feeds which tensor live here; no
+packing, scoring or attention arithmetic.  Sizes follow the pages:
+
+* 512-wide k=v latent per cache entry, 64 query heads (DeepSeek-V4.1-Flash
+  study, reading notes on the attention enclosure);
+* 32 indexer heads of 128 dims, top-512, candidate pool of 2,048 blocks of 8
+  (same study, lightning-indexer note; perchy.ai "Full. Reindex. Reuse." card);
+* 128-token sliding window (helix.ml, "CSA2 makes long context cheaper to retain");
+* m=2 gated pooling for encoder caches (study, Full-layer global KV note).
+
+Config index = seed.  Per-sequence tensors use the sequence index as sub-stream,
+per-query tensors the query index.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import inputs as G
+
+H, D, HI, DI = 64, 512, 32, 128
+TOPK, SWA, BLOCK, POOL_BLOCKS = 512, 128, 8, 2048
+
+
+@dataclass
+class Workload:
+    name: str
+    seed: int
+    n_seq: int              # B: independent caches
+    n_entries: int          # N: cache entries per sequence (after m-pooling)
+    n_q: int                # queries in one step
+    m: int = 1              # tokens pooled per entry
+    zipf: bool = False      # Zipf-skewed indexer key norms
+    pool: bool = False      # Reindex layer over a 16,384-position pool
+    prefill: bool = False   # causal prefill: all queries on sequence 0
+    swa_cap: int = SWA      # SWA ring capacity per sequence
+    extra: dict = field(default_factory=dict)
+
+    # ---- per-query descriptors (host int32 arrays) ----
+    def q_seq(self) -> np.ndarray:
+        if self.prefill:
+            return np.zeros(self.n_q, np.int32)
+        return (np.arange(self.n_q) % self.n_seq).astype(np.int32)
+
+    def pos(self) -> np.ndarray:
+        if self.prefill:
+            return np.arange(self.n_q, dtype=np.int32)
+        return np.full(self.n_q, self.n_entries * self.m - 1, np.int32)
+
+    def n_vis(self) -> np.ndarray:
+        if self.prefill:   # entry j (tokens 2j, 2j+1) visible to query t iff 2j+1 <= t
+            t = np.arange(self.n_q, dtype=np.int64)
+            return ((t + 1) // self.m).astype(np.int32)
+        return np.full(self.n_q, self.n_entries, np.int32)
+
+    def swa_first(self) -> np.ndarray:
+        p = self.pos().astype(np.int64)
+        return (np.maximum(0, p - (SWA - 1)) % self.swa_cap).astype(np.int32)
+
+    def swa_cnt(self) -> np.ndarray:
+        return np.minimum(SWA, self.pos().astype(np.int64) + 1).astype(np.int32)
+
+    # ---- tensors (bf16 as uint16 bit patterns, fp32 as float32) ----
+    def latent_rows(self, seq: int, rows) -> np.ndarray:
+        """[len(rows), 512] bf16: cache latents (m=1) or token latents (m=2)."""
+        return G.normal_rows_bf16(self.seed, G.S_LATENT, seq, rows, D)
+
+    def gate_rows(self, seq: int, rows) -> np.ndarray:
+        return G.gate_logits_f32(self.seed, seq, rows, D)
+
+    def key_rows(self, seq: int, rows) -> np.ndarray:
+        """[len(rows), 128] bf16 indexer keys."""
+        if self.zipf:
+            return G.zipf_keys_bf16(self.seed, seq, self.n_entries, rows, DI)
+        return G.normal_rows_bf16(self.seed, G.S_IDX_KEY, seq, rows, DI)
+
+    def swa_rows(self, seq: int, slots) -> np.ndarray:
+        return G.normal_rows_bf16(self.seed, G.S_SWA, seq, slots, D)
+
+    def q(self, qi: int) -> np.ndarray:
+        return G.normal_block_bf16(self.seed, G.S_Q, qi, 0, H, D)
+
+    def qidx(self, qi: int, reindex: bool = False) -> np.ndarray:
+        return G.normal_block_bf16(self.seed, G.S_QIDX_RE if reindex else G.S_QIDX, qi, 0, HI, DI)
+
+    def w(self, qi: int, reindex: bool = False) -> np.ndarray:
+        return G.weights_f32(self.seed, G.S_W_RE if reindex else G.S_W, qi, [0], HI)[0]
+
+
+CONFIGS = {
+    0: Workload("tiny_full_decode_N4096_B1", 0, 1, 4096, 1),
+    1: Workload("full_decode_N65536_B32", 1, 32, 65536, 32),
+    2: Workload("m2_prefill_T8192", 2, 1, 4096, 8192, m=2, prefill=True, swa_cap=8192),
+    3: Workload("reindex_decode_N1M_B64", 3, 64, 1 << 20, 64, pool=True),
+    4: Workload("long_full_decode_N1M_B8_zipf", 4, 8, 1 << 20, 8, zipf=True),
+}
+
+
+def small(n_seq=2, n_entries=1000, zipf=False, pool=False, seed=100) -> Workload:
+    """A small decode workload for tests (ragged N allowed)."""
+    return Workload(f"small_N{n_entries}_B{n_seq}", seed, n_seq, n_entries, n_seq, zipf=zipf, pool=pool)
