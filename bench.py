@@ -1,0 +1,331 @@
+"""Benchmark of the CSA2 decode hot path on GB300.
+
+One step = one Full-layer decode of a batch: lightning-indexer scores over
+every cache entry -> top-512 -> sparse MQA attention over the 512 selected FP4
+entries plus the 128-entry FP8 window.  Default workload: 8 sequences x
+1,048,576-entry m=1 caches with Zipf-skewed indexer keys, one query token per
+sequence (the 1M-context decode the metric is quoted on).
+
+Prints ONE JSON line (rank 0).  Timing: W untimed warm-up steps, then K steps
+between CUDA events on the launching stream, barrier + synchronize on both
+sides, max over ranks.  Each step streams 573 MB of cache (far more than the
+129 MB L2), so no extra L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config 4] [--no-cpu-baseline]
+
+--impl reference times the CPU oracle (plain C, fp64) on the host cores on a
+bounded sample of the same workload; under torchrun only rank 0 runs it.
+Multi-GPU (torchrun): every rank decodes its own batch on its own GPU (the
+batches are independent, no data-path collective): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode query-tokens/s for CSA2 (score+top512+attn) at 1M ctx; HBM GB/s vs peak"
+UNIT = "query-tokens/s"
+FIXED_BYTES_PER_QUERY = 348_416      # 512x288 + 128x528 + q 64 KiB + out 64 KiB + q_idx 2176 + w 128
+IDX_BYTES = 68
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_decode_sample(wl, qi=0):
+    """Time the oracle's decode of one query (score all entries, top-512,
+    attention) with its packed caches prepared beforehand (they are resident
+    state, not step work)."""
+    import numpy as np
+    import oracle
+    from oracle.compose import packed_keys, kv_records, swa_records, query_inputs
+    seq, n = int(wl.q_seq()[qi]), int(wl.n_vis()[qi])
+    keys = packed_keys(wl, seq, n)
+    qidx, w = query_inputs(wl, qi)
+    q = wl.q(qi)
+    t0 = time.perf_counter()
+    s = oracle.index_score(keys, qidx, w)
+    sel = oracle.topk(s, 512)
+    t1 = time.perf_counter()
+    kv = kv_records(wl, seq, sel[sel >= 0])            # record fetch = the gather of the selected entries
+    sw = swa_records(wl, seq, int(wl.swa_first()[qi]), int(wl.swa_cnt()[qi]))
+    t2 = time.perf_counter()
+    oracle.sparse_attn(q, kv, sw, int(wl.pos()[qi]))
+    t3 = time.perf_counter()
+    # record generation (t1..t2) is input synthesis, not oracle work
+    return (t1 - t0) + (t3 - t2)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, n_samples=1):
+    secs = [oracle_decode_sample(wl, qi) for qi in range(n_samples)]
+    per_q = sum(secs) / len(secs)
+    threads = int(os.environ.get("OMP_NUM_THREADS", cpu_cores()))
+    return {"value": 1.0 / per_q, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n_samples} of {wl.n_q} queries (sequence 0), full {wl.n_entries}-entry cache: "
+                      f"fp64 score of every entry + top-512 sort + attention, {per_q:.2f} s per query"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import compressed_sparse_attention_index_gb300 as C
+    from compressed_sparse_attention_index_gb300 import decode
+    from gen.device import build_device_workload
+    from gen.workloads import CONFIGS
+
+    torch.cuda.set_device(local_rank)
+    wl = CONFIGS[args.config]
+    assert not wl.pool and not wl.prefill, "the benchmark times the Full-layer decode configs (0, 1, 4)"
+    dw = build_device_workload(wl)
+    n_q, n_max = dw.q.shape[0], dw.n_max
+    buf = decode.DecodeBuffers(n_q, n_max, out_dtype=C.CSA2_OUT_BF16)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    def step():
+        decode.full_decode(dw, buf)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert C.csa2_get_device_status() == 0
+
+    # device-timed region: K steps, score kernel bracketed by its own events
+    ev_s = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_index = local_rank
+    if os.environ.get("CUDA_VISIBLE_DEVICES"):
+        try:
+            gpu_index = int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank])
+        except ValueError:
+            pass
+    clocks = ClockSampler(gpu_index)
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev_s[i][0].record(stream)
+        C.csa2_index_score(dw.key_nib, dw.key_scale, n_max, dw.kv.shape[0], dw.q_nib, dw.q_scale, dw.w, dw.q_seq,
+                           dw.n_vis, n_q, None, buf.scores, n_max, None, stream)
+        ev_s[i][1].record(stream)
+        C.csa2_topk(buf.scores, n_max, n_q, dw.n_vis, n_max, 512, 1, None, buf.sel, buf.ws, buf.ws_topk_bytes,
+                    stream)
+        decode.attend(dw, buf, None, stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    score_ms = sum(a.elapsed_time(b) for a, b in ev_s) / args.steps
+    assert C.csa2_get_device_status() == 0
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public API: host (pinned) inputs in, host output back
+    q_h = dw.q.cpu().pin_memory()
+    w_h = dw.w.cpu().pin_memory()
+    from gen import inputs as G
+    import numpy as np
+    qidx_bits = np.concatenate([G.normal_block_bf16(wl.seed, G.S_QIDX, qi, 0, 32, 128) for qi in range(n_q)])
+    qidx_h = torch.from_numpy(qidx_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    desc_h = torch.stack([dw.q_seq, dw.n_vis, dw.pos, dw.swa_first, dw.swa_cnt]).cpu().pin_memory()
+    out_h = torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory()
+    qidx_d = torch.empty(qidx_h.shape, dtype=torch.bfloat16, device="cuda")
+    desc_d = torch.empty(desc_h.shape, dtype=torch.int32, device="cuda")
+
+    def e2e_step():
+        dw.q.copy_(q_h, non_blocking=True)
+        dw.w.copy_(w_h, non_blocking=True)
+        qidx_d.copy_(qidx_h, non_blocking=True)
+        desc_d.copy_(desc_h, non_blocking=True)
+        C.csa2_fp4_pack(C.CSA2_IDX_MXFP4, qidx_d, n_q * 32, 1, None, dw.q_nib, dw.q_scale)
+        dw.q_seq, dw.n_vis, dw.pos, dw.swa_first, dw.swa_cnt = desc_d[0], desc_d[1], desc_d[2], desc_d[3], desc_d[4]
+        decode.full_decode(dw, buf)
+        out_h.copy_(buf.out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = q_h.numel() * 2 + w_h.numel() * 4 + qidx_h.numel() * 2 + desc_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size()
+
+    if rank != 0:
+        return None
+    units = n_q * args.steps * world
+    value = units / (ms / 1e3)
+    peak, peak_kind = peaks()
+    score_bytes = n_q * wl.n_entries * IDX_BYTES           # algorithmic bytes of one score launch
+    achieved = score_bytes / (score_ms / 1e3) / 1e9
+    step_bytes = n_q * (wl.n_entries * IDX_BYTES + FIXED_BYTES_PER_QUERY)
+    launches_per_step = 1 + (3 if n_max > 16384 else 1) + 2
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e2m1xe2m1->f32 (score), bf16xbf16->f32 (attention)",
+        "data": "synthetic (seeded counter-based generator; no trained weights)",
+        "config": {"workload": wl.name, "n_seq": wl.n_seq, "n_entries": wl.n_entries, "queries_per_step": n_q,
+                   "zipf_keys": wl.zipf, "topk": 512, "swa": 128, "heads": 64, "latent": 512,
+                   "l2": "inputs larger than L2 (%.0f MB streamed per step)" % (step_bytes / 1e6),
+                   "parallelism": f"replicas x{world} (independent batches)"},
+        "path_hbm_gbs": step_bytes / (ms / args.steps / 1e3) / 1e9,
+        "path_frac_of_measured_peak": step_bytes / (ms / args.steps / 1e3) / 1e9 / peak,
+        "roofline": {"kernel": "index_score", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": score_bytes, "avg_launch_ms": score_ms},
+        "clocks": clk,
+        "e2e": {"value": units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "impl": "ours",
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    return line
+
+
+def run_reference(args):
+    from gen.workloads import CONFIGS
+    import oracle
+    oracle.build()
+    wl = CONFIGS[args.config]
+    for _ in range(args.warmup):
+        pass                       # the oracle has no state to warm; its packed keys are built once below
+    t_total = 0.0
+    for i in range(args.steps):
+        t_total += oracle_decode_sample(wl, qi=i % wl.n_q if wl.n_q <= 1 else 0)
+    per_q = t_total / args.steps
+    value = 1.0 / per_q
+    cores = int(os.environ.get("OMP_NUM_THREADS", cpu_cores()))
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_q * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "n_seq": wl.n_seq, "n_entries": wl.n_entries,
+                   "queries_per_step": 1, "sample": "one query of sequence 0 per step"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"one query (sequence 0) per step, full {wl.n_entries}-entry cache"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+// C ABI of the CSA2 library: argument checks, workspace sizing, launches.
+// The declarations and the contract of every entry point are in include/csa2.h.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace csa2 {
+cudaError_t launch_pack(int kind, const void *src, int64_t rows, int m, const float *gate, void *dst,
+                        void *dst_scales, cudaStream_t st);
+cudaError_t launch_index_score_simt(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
+                                    const uint8_t *q_nib, const uint8_t *q_scale, const float *w,
+                                    const int32_t *q_seq, const int32_t *n_vis, int n_q, const int32_t *pool,
+                                    float *scores, int64_t stride, int *status, cudaStream_t st);
+size_t topk_workspace_bytes(int n_q, int64_t n_items);
+cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max, int k,
+                        int block, const int32_t *pool, int32_t *out, void *ws, int *status, cudaStream_t st);
+size_t attn_workspace_bytes(int n_q, int sel_stride);
+cudaError_t launch_attn_simt(const void *q, const void *kv, int64_t n_max, int n_seq, const int32_t *sel,
+                             int sel_stride, const void *swa, int swa_cap, const int32_t *q_seq, const int32_t *pos,
+                             const int32_t *swa_first, const int32_t *swa_cnt, int n_q, void *out, int out_dtype,
+                             float sm_scale, double rope_base, void *ws, int *status, cudaStream_t st);
+
+// The sticky status word of each device (a file-scope device variable: the
+// library makes no allocation for it).
+__device__ int g_status_word;
+
+static int *status_ptr() {
+  static int *ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (ptrs[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int *>(p);
+  }
+  return ptrs[dev];
+}
+
+static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+static bool params_ok(const csa2_params *p) {
+  if (p == nullptr) return true;   // null = the pages' constants
+  return p->heads == kHeads && p->dim == kDim && p->rope_dim == kRopeDim && p->rope_off == kRopeOff &&
+         p->idx_heads == kIdxHeads && p->idx_dim == kIdxDim && p->topk == kTopK && p->swa == kSwa &&
+         p->block == kBlock && p->pool_blocks == kPoolBlocks && p->rope_base > 0.0 && p->sm_scale > 0.f &&
+         isfinite(p->sm_scale) && isfinite(p->rope_base);
+}
+
+static csa2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+
+}  // namespace csa2
+
+using namespace csa2;
+
+extern "C" {
+
+csa2_status csa2_default_params(csa2_params *p) {
+  if (p == nullptr) return CSA2_ERR_INVALID_ARG;
+  p->heads = kHeads;
+  p->dim = kDim;
+  p->rope_dim = kRopeDim;
+  p->rope_off = kRopeOff;
+  p->rope_base = 10000.0;
+  p->sm_scale = 1.0f / sqrtf((float)kDim);
+  p->idx_heads = kIdxHeads;
+  p->idx_dim = kIdxDim;
+  p->topk = kTopK;
+  p->swa = kSwa;
+  p->block = kBlock;
+  p->pool_blocks = kPoolBlocks;
+  return CSA2_OK;
+}
+
+size_t csa2_entry_bytes(int kind) {
+  switch (kind) {
+    case CSA2_KV_NVFP4: return kKvBytes;
+    case CSA2_IDX_MXFP4: return kIdxNibBytes + kIdxScaleBytes;
+    case CSA2_SWA_MXFP8: return kSwaBytes;
+    default: return 0;
+  }
+}
+
+const char *csa2_status_string(csa2_status s) {
+  switch (s) {
+    case CSA2_OK: return "ok";
+    case CSA2_ERR_INVALID_ARG: return "invalid argument";
+    case CSA2_ERR_UNSUPPORTED: return "unsupported parameters";
+    case CSA2_ERR_CUDA: return "CUDA runtime error";
+    case CSA2_ERR_BOUNDS: return "device-side index out of range";
+    case CSA2_ERR_TIMEOUT: return "device-side bounded wait ran out";
+    case CSA2_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+csa2_status csa2_fp4_pack(int kind, const void *src, int64_t rows, int m, const float *gate_logits, void *dst,
+                          void *dst_scales, csa2_stream_t stream) {
+  if (kind != CSA2_KV_NVFP4 && kind != CSA2_IDX_MXFP4 && kind != CSA2_SWA_MXFP8) return CSA2_ERR_INVALID_ARG;
+  if (rows < 0 || (m != 1 && m != 2)) return CSA2_ERR_INVALID_ARG;
+  if (m == 2 && (kind != CSA2_KV_NVFP4 || gate_logits == nullptr || rows % 2 != 0)) return CSA2_ERR_INVALID_ARG;
+  if (m == 1 && gate_logits != nullptr) return CSA2_ERR_INVALID_ARG;
+  if ((kind == CSA2_IDX_MXFP4) != (dst_scales != nullptr)) return CSA2_ERR_INVALID_ARG;
+  if (rows == 0) return CSA2_OK;
+  if (src == nullptr || dst == nullptr) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(src, 16) || !aligned(dst, 16) || (gate_logits && !aligned(gate_logits, 16)))
+    return CSA2_ERR_INVALID_ARG;
+  return from_cuda(launch_pack(kind, src, rows, m, gate_logits, dst, dst_scales, (cudaStream_t)stream));
+}
+
+csa2_status csa2_index_score(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq, const void *q_nib,
+                             const void *q_scale, const float *w, const int32_t *q_seq, const int32_t *n_vis, int n_q,
+                             const int32_t *pool_blocks, float *scores, int64_t score_stride,
+                             const csa2_params *params, csa2_stream_t stream) {
+  if (!params_ok(params)) return CSA2_ERR_UNSUPPORTED;
+  if (n_q < 0 || n_seq < 1 || n_max <= 0 || n_max % 128 != 0 || n_max > ((int64_t)1 << 31) - 128)
+    return CSA2_ERR_INVALID_ARG;
+  if (n_q > 65535) return CSA2_ERR_UNSUPPORTED;
+  if (score_stride < (pool_blocks ? (int64_t)kPoolSlots : n_max)) return CSA2_ERR_INVALID_ARG;
+  if (n_q == 0) return CSA2_OK;
+  if (!key_nib || !key_scale || !q_nib || !q_scale || !w || !q_seq || !n_vis || !scores)
+    return CSA2_ERR_INVALID_ARG;
+  if (!aligned(key_nib, 16) || !aligned(key_scale, 4) || !aligned(q_nib, 16) || !aligned(q_scale, 4) ||
+      !aligned(scores, 4))
+    return CSA2_ERR_INVALID_ARG;
+  int *st = status_ptr();
+  if (st == nullptr) return CSA2_ERR_CUDA;
+  return from_cuda(launch_index_score_simt(
+      static_cast<const uint8_t *>(key_nib), static_cast<const uint8_t *>(key_scale), n_max, n_seq,
+      static_cast<const uint8_t *>(q_nib), static_cast<const uint8_t *>(q_scale), w, q_seq, n_vis, n_q, pool_blocks,
+      scores, score_stride, st, (cudaStream_t)stream));
+}
+
+csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t *bytes) {
+  (void)k;
+  if (bytes == nullptr || n_q < 0 || n_items < 0) return CSA2_ERR_INVALID_ARG;
+  if (op == CSA2_OP_TOPK) {
+    *bytes = topk_workspace_bytes(n_q, n_items);
+    return CSA2_OK;
+  }
+  if (op == CSA2_OP_SPARSE_ATTN) {
+    const int64_t sel_stride = n_items - kSwa;
+    if (sel_stride < 1 || sel_stride > kTopK) return CSA2_ERR_INVALID_ARG;
+    *bytes = attn_workspace_bytes(n_q, (int)sel_stride);
+    return CSA2_OK;
+  }
+  return CSA2_ERR_INVALID_ARG;
+}
+
+csa2_status csa2_topk(const float *scores, int64_t score_stride, int n_q, const int32_t *n_valid, int64_t n_max,
+                      int k, int block, const int32_t *pool_blocks, int32_t *out, void *workspace,
+                      size_t workspace_bytes, csa2_stream_t stream) {
+  if (k < 1 || k > 2048) return CSA2_ERR_UNSUPPORTED;
+  if (n_q < 0 || n_max <= 0 || n_max > ((int64_t)1 << 31) - 8 || (block != 1 && block != kBlock))
+    return CSA2_ERR_INVALID_ARG;
+  if (block != 1 && pool_blocks != nullptr) return CSA2_ERR_INVALID_ARG;
+  if (n_q > 65535) return CSA2_ERR_UNSUPPORTED;
+  const int64_t row_len = pool_blocks ? (int64_t)kPoolSlots : n_max;
+  if (score_stride < row_len) return CSA2_ERR_INVALID_ARG;
+  if (n_q == 0) return CSA2_OK;
+  if (!scores || !n_valid || !out) return CSA2_ERR_INVALID_ARG;
+  const int64_t items = pool_blocks ? (int64_t)kPoolSlots : (block == 1 ? n_max : (n_max + kBlock - 1) / kBlock);
+  const size_t need = topk_workspace_bytes(n_q, items);
+  if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned(workspace, 256))))
+    return CSA2_ERR_WORKSPACE;
+  int *st = status_ptr();
+  if (st == nullptr) return CSA2_ERR_CUDA;
+  return from_cuda(launch_topk(scores, score_stride, n_q, n_valid, n_max, k, block, pool_blocks, out, workspace, st,
+                               (cudaStream_t)stream));
+}
+
+csa2_status csa2_sparse_attn(const void *q, const void *kv_cache, int64_t n_max, int n_seq, const int32_t *sel,
+                             int sel_stride, const void *swa_cache, int swa_cap, const int32_t *q_seq,
+                             const int32_t *pos, const int32_t *swa_first, const int32_t *swa_cnt, int n_q, void *out,
+                             int out_dtype, const csa2_params *params, void *workspace, size_t workspace_bytes,
+                             csa2_stream_t stream) {
+  if (!params_ok(params)) return CSA2_ERR_UNSUPPORTED;
+  if (n_q < 0 || n_seq < 1 || n_max <= 0 || swa_cap < 0 || sel_stride < 1 || sel_stride > kTopK)
+    return CSA2_ERR_INVALID_ARG;
+  if (out_dtype != CSA2_OUT_BF16 && out_dtype != CSA2_OUT_F32) return CSA2_ERR_INVALID_ARG;
+  if (n_q > 65535) return CSA2_ERR_UNSUPPORTED;
+  if (n_q == 0) return CSA2_OK;
+  if (!q || !kv_cache || !sel || !q_seq || !pos || !swa_first || !swa_cnt || !out) return CSA2_ERR_INVALID_ARG;
+  if (swa_cap > 0 && swa_cache == nullptr) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || (swa_cache && !aligned(swa_cache, 16)) || !aligned(out, 16))
+    return CSA2_ERR_INVALID_ARG;
+  const size_t need = attn_workspace_bytes(n_q, sel_stride);
+  if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned(workspace, 256))))
+    return CSA2_ERR_WORKSPACE;
+  int *st = status_ptr();
+  if (st == nullptr) return CSA2_ERR_CUDA;
+  const float sm_scale = params ? params->sm_scale : 1.0f / sqrtf((float)kDim);
+  const double rope_base = params ? params->rope_base : 10000.0;
+  return from_cuda(launch_attn_simt(q, kv_cache, n_max, n_seq, sel, sel_stride, swa_cache, swa_cap, q_seq, pos,
+                                    swa_first, swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, workspace, st,
+                                    (cudaStream_t)stream));
+}
+
+csa2_status csa2_get_device_status(csa2_stream_t stream, csa2_status *out) {
+  if (out == nullptr) return CSA2_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CSA2_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return CSA2_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return CSA2_ERR_CUDA;
+  *out = (csa2_status)v;
+  return CSA2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,226 @@
+// Cache-write kernels: bf16 rows -> FP4 / FP8 cache records (csa2_fp4_pack).
+//
+// Formats ("An infra-oriented diagram of the DeepSeek-V4.1-Flash architecture",
+// reading notes and section "The KV cache"):
+//   KV  : 512 FP4 E2M1 + one E4M3 scale per 16 channels   (288 B)
+//   IDX : 128 FP4 E2M1 + one E8M0 scale per 32 channels    (68 B, two planes)
+//   SWA : 512 E4M3 + one E8M0 scale per 32 channels        (528 B)
+// m=2 entries pool two tokens with a per-channel softmax gate (same notes).
+//
+// Rounding is done by the hardware converters (cvt.rn.satfinite to e2m1x2 /
+// e4m3x2: nearest-even, saturating).  Each converter input is a correctly
+// rounded fp32 quotient or an exact power-of-two scaling of a bf16 value, and a
+// tie of the exact quotient cannot move under fp32 rounding (the quotient of an
+// 8-bit by a 4-bit significand is either exact or at least 2^-12 relative away
+// from every tie point), so the codes equal those of the exact real quotient.
+//
+// All three kernels are HBM-bound streams: one warp per row (KV, SWA) or eight
+// lanes per row (IDX), 16-B vector loads of the bf16 row, 8- or 16-B stores.
+#include "common.cuh"
+
+namespace csa2 {
+
+// Eight floats -> four bytes of E2M1 pairs; byte i = code(v[2i+1]) << 4 | code(v[2i]).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float v0, float v1, float v2, float v3, float v4, float v5,
+                                               float v6, float v7) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+
+// fp64 -> bf16 bits, one rounding (nearest-even), for finite values of bf16 range.
+__device__ __forceinline__ uint32_t bf16_from_f64(double v) {
+  unsigned long long u = (unsigned long long)__double_as_longlong(v);
+  uint32_t sign = (uint32_t)(u >> 63) << 15;
+  unsigned long long a = u & 0x7FFFFFFFFFFFFFFFull;
+  if (a == 0) return sign;
+  int ex = (int)(a >> 52) - 1023;                 // unbiased exponent of a normal double
+  uint32_t bits;
+  if (ex >= -126) {
+    // keep 7 of the 52 fraction bits: round away 45 bits, nearest-even
+    unsigned long long r = a + ((1ull << 44) - 1) + ((a >> 45) & 1ull);
+    r >>= 45;                                     // (exponent_d << 7) | frac7, may carry
+    int e_bf = (int)(r >> 7) - 1023 + 127;
+    bits = ((uint32_t)e_bf << 7) | (uint32_t)(r & 0x7F);
+  } else {
+    // bf16 subnormal: multiple of 2^-133; |v| < 2^-126 so the count is <= 128
+    double m = fabs(v) * 0x1p133;                 // exact power-of-two scaling
+    bits = (uint32_t)__double2ull_rn(m);          // nearest-even to an integer
+  }
+  return sign | bits;
+}
+
+// ------------------------------------------------------------------ KV (S1)
+// One warp per output row; lane g packs channels [16g, 16g+16).
+template <int M>
+__global__ void __launch_bounds__(256) pack_kv_kernel(const uint16_t *__restrict__ src,
+                                                       const float *__restrict__ gate, int64_t rows_out,
+                                                       uint8_t *__restrict__ dst) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows_out) return;
+  float x[16];
+  if (M == 1) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(src + row * kDim + lane * 16);
+    uint4 a = __ldg(p), b = __ldg(p + 1);
+    uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; i++) { x[2 * i] = bf16_lo(w[i]); x[2 * i + 1] = bf16_hi(w[i]); }
+  } else {
+    // gated pooling of tokens 2*row and 2*row+1, in fp64, rounded once to bf16
+    const uint4 *p0 = reinterpret_cast<const uint4 *>(src + (2 * row) * kDim + lane * 16);
+    const uint4 *p1 = reinterpret_cast<const uint4 *>(src + (2 * row + 1) * kDim + lane * 16);
+    const float *z0 = gate + (2 * row) * kDim + lane * 16;
+    const float *z1 = gate + (2 * row + 1) * kDim + lane * 16;
+    uint4 a0 = __ldg(p0), b0 = __ldg(p0 + 1), a1 = __ldg(p1), b1 = __ldg(p1 + 1);
+    uint32_t w0[8] = {a0.x, a0.y, a0.z, a0.w, b0.x, b0.y, b0.z, b0.w};
+    uint32_t w1[8] = {a1.x, a1.y, a1.z, a1.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      float t0 = (i & 1) ? bf16_hi(w0[i >> 1]) : bf16_lo(w0[i >> 1]);
+      float t1 = (i & 1) ? bf16_hi(w1[i >> 1]) : bf16_lo(w1[i >> 1]);
+      double za = (double)__ldg(z0 + i), zb = (double)__ldg(z1 + i);
+      double mz = za > zb ? za : zb;
+      double ea = exp(za - mz), eb = exp(zb - mz);
+      double v = (ea * (double)t0 + eb * (double)t1) / (ea + eb);
+      x[i] = __uint_as_float(bf16_from_f64(v) << 16);
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; i++) amax = fmaxf(amax, fabsf(x[i]));
+  const uint32_t sc = cvt_e4m3x2(0.f, __fdiv_rn(amax, 6.0f)) & 0xFFu;
+  const float s = e4m3_to_float(sc);
+  uint32_t nib[2] = {0u, 0u};
+  if (s != 0.f) {
+    float y[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) y[i] = __fdiv_rn(x[i], s);
+    nib[0] = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+    nib[1] = cvt_e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
+  }
+  uint8_t *rec = dst + row * kKvBytes;
+  *reinterpret_cast<uint2 *>(rec + lane * 8) = make_uint2(nib[0], nib[1]);
+  rec[256 + lane] = (uint8_t)sc;
+}
+
+// smallest e with lim * 2^e >= amax (amax > 0), for lim = 1.5 * 2^p, 1.75 * 2^p
+__device__ __forceinline__ int pow2_exp_fp4(float amax) {   // lim = 6 = 1.5 * 2^2
+  int ex;
+  frexpf(amax, &ex);                     // amax in [2^(ex-1), 2^ex)
+  int e0 = ex - 1;
+  int e = (amax <= ldexpf(6.0f, e0 - 2)) ? e0 - 2 : e0 - 1;
+  return max(-127, min(127, e));
+}
+__device__ __forceinline__ int pow2_exp_fp8(float amax) {   // lim = 448 = 1.75 * 2^8
+  int ex;
+  frexpf(amax, &ex);
+  int e0 = ex - 1;
+  int e = (amax <= ldexpf(448.0f, e0 - 8)) ? e0 - 8 : e0 - 7;
+  return max(-127, min(127, e));
+}
+
+// ------------------------------------------------------------------ IDX (S2, S4)
+// Eight lanes per 128-wide row; lane part p packs channels [16p, 16p+16), the
+// lane pair (2g, 2g+1) shares E8M0 group g.
+__global__ void __launch_bounds__(256) pack_idx_kernel(const uint16_t *__restrict__ src, int64_t rows,
+                                                        uint8_t *__restrict__ nib_out,
+                                                        uint8_t *__restrict__ sc_out) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t row = t >> 3;
+  const int part = (int)(t & 7);
+  const bool live = row < rows;
+  float x[16];
+  float amax = 0.f;
+  if (live) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(src + row * kIdxDim + part * 16);
+    uint4 a = __ldg(p), b = __ldg(p + 1);
+    uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; i++) { x[2 * i] = bf16_lo(w[i]); x[2 * i + 1] = bf16_hi(w[i]); }
+#pragma unroll
+    for (int i = 0; i < 16; i++) amax = fmaxf(amax, fabsf(x[i]));
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  if (!live) return;
+  uint32_t scale_byte = 0, nib[2] = {0u, 0u};
+  if (amax > 0.f) {
+    const int e = pow2_exp_fp4(amax);
+    scale_byte = (uint32_t)(e + 127);
+    float y[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) y[i] = ldexpf(x[i], -e);
+    nib[0] = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+    nib[1] = cvt_e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
+  }
+  *reinterpret_cast<uint2 *>(nib_out + row * kIdxNibBytes + part * 8) = make_uint2(nib[0], nib[1]);
+  if ((part & 1) == 0) sc_out[row * kIdxScaleBytes + (part >> 1)] = (uint8_t)scale_byte;
+}
+
+// ------------------------------------------------------------------ SWA (S3)
+// One warp per row; lane l packs channels [16l, 16l+16), lanes (2g, 2g+1) share group g.
+__global__ void __launch_bounds__(256) pack_swa_kernel(const uint16_t *__restrict__ src, int64_t rows,
+                                                        uint8_t *__restrict__ dst) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const uint4 *p = reinterpret_cast<const uint4 *>(src + row * kDim + lane * 16);
+  uint4 a = __ldg(p), b = __ldg(p + 1);
+  uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float x[16];
+#pragma unroll
+  for (int i = 0; i < 8; i++) { x[2 * i] = bf16_lo(w[i]); x[2 * i + 1] = bf16_hi(w[i]); }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; i++) amax = fmaxf(amax, fabsf(x[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  uint32_t scale_byte = 0, v[4] = {0u, 0u, 0u, 0u};
+  if (amax > 0.f) {
+    const int e = pow2_exp_fp8(amax);
+    scale_byte = (uint32_t)(e + 127);
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      uint32_t two = cvt_e4m3x2(ldexpf(x[2 * i + 1], -e), ldexpf(x[2 * i], -e));
+      v[i >> 1] |= two << (16 * (i & 1));
+    }
+  }
+  uint8_t *rec = dst + row * kSwaBytes;
+  *reinterpret_cast<uint4 *>(rec + lane * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+  if ((lane & 1) == 0) rec[512 + (lane >> 1)] = (uint8_t)scale_byte;
+}
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_pack(int kind, const void *src, int64_t rows, int m, const float *gate, void *dst,
+                        void *dst_scales, cudaStream_t st) {
+  const uint16_t *s = static_cast<const uint16_t *>(src);
+  if (kind == CSA2_KV_NVFP4) {
+    const int64_t out_rows = rows / m;
+    const int64_t blocks = (out_rows + 7) / 8;
+    if (m == 1)
+      pack_kv_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(s, nullptr, out_rows, (uint8_t *)dst);
+    else
+      pack_kv_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(s, gate, out_rows, (uint8_t *)dst);
+  } else if (kind == CSA2_IDX_MXFP4) {
+    const int64_t blocks = (rows * 8 + 255) / 256;
+    pack_idx_kernel<<<(unsigned)blocks, 256, 0, st>>>(s, rows, (uint8_t *)dst, (uint8_t *)dst_scales);
+  } else {
+    const int64_t blocks = (rows + 7) / 8;
+    pack_swa_kernel<<<(unsigned)blocks, 256, 0, st>>>(s, rows, (uint8_t *)dst);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

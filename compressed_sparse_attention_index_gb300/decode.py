@@ -1,0 +1,73 @@
+"""Decode-step compositions over the C ABI (one CUDA stream, no host sync).
+
+* Full layer: csa2_index_score over every visible entry -> csa2_topk (k=512)
+  -> csa2_sparse_attn over the selected entries + the SWA window.
+* Reindex layer: Full-layer scores -> csa2_topk in block mode (2,048 blocks of
+  8) -> csa2_index_score over the 16,384 pool slots with the Reindex layer's
+  own indexer query -> csa2_topk over the pool -> csa2_sparse_attn.
+  ("Reindex layers in the decoder only score a 16,384-entry candidate pool that
+  layer 20 chose by blocks of 8", DeepSeek-V4.1-Flash study, lightning-indexer
+  note; perchy.ai "shared KV -> candidate pool -> top 512 -> attention".)
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib as L
+
+TOPK, POOL_BLOCKS, POOL_SLOTS, SWA = 512, 2048, 16384, 128
+
+
+class DecodeBuffers:
+    """Device buffers of one decode step for n_q queries over caches of n_max entries."""
+
+    def __init__(self, n_q: int, n_max: int, pool: bool = False, out_dtype=L.CSA2_OUT_BF16, device="cuda"):
+        self.n_q, self.n_max, self.pool, self.out_dtype = n_q, n_max, pool, out_dtype
+        self.scores = torch.empty((n_q, n_max), dtype=torch.float32, device=device)
+        self.sel = torch.empty((n_q, TOPK), dtype=torch.int32, device=device)
+        odt = torch.bfloat16 if out_dtype == L.CSA2_OUT_BF16 else torch.float32
+        self.out = torch.empty((n_q, 64, 512), dtype=odt, device=device)
+        ws_t = L.csa2_workspace_size(L.CSA2_OP_TOPK, n_q, n_max, TOPK)
+        if pool:
+            self.blocks = torch.empty((n_q, POOL_BLOCKS), dtype=torch.int32, device=device)
+            self.pool_scores = torch.empty((n_q, POOL_SLOTS), dtype=torch.float32, device=device)
+            ws_t = max(ws_t, L.csa2_workspace_size(L.CSA2_OP_TOPK, n_q, (n_max + 7) // 8, POOL_BLOCKS),
+                       L.csa2_workspace_size(L.CSA2_OP_TOPK, n_q, POOL_SLOTS, TOPK))
+        self.ws_topk_bytes = ws_t
+        self.ws_attn_bytes = L.csa2_workspace_size(L.CSA2_OP_SPARSE_ATTN, n_q, TOPK + SWA)
+        self.ws = torch.empty(max(1, max(ws_t, self.ws_attn_bytes)), dtype=torch.uint8, device=device)
+
+
+def full_decode(dw, buf: DecodeBuffers, params=None, stream=None):
+    """Full-layer decode step of every query of a device workload (see gen.device)."""
+    n_q = buf.n_q
+    L.csa2_index_score(dw.key_nib, dw.key_scale, dw.n_max, dw.kv.shape[0], dw.q_nib, dw.q_scale, dw.w, dw.q_seq,
+                       dw.n_vis, n_q, None, buf.scores, buf.n_max, params, stream)
+    L.csa2_topk(buf.scores, buf.n_max, n_q, dw.n_vis, dw.n_max, TOPK, 1, None, buf.sel, buf.ws, buf.ws_topk_bytes,
+                stream)
+    attend(dw, buf, params, stream)
+    return buf.out
+
+
+def reindex_decode(dw, buf: DecodeBuffers, params=None, stream=None, build_pool: bool = True):
+    """Reindex-layer decode step.  With build_pool=False the candidate pool in
+    buf.blocks (chosen earlier by the Full layer) is reused as it is."""
+    n_q = buf.n_q
+    if build_pool:
+        L.csa2_index_score(dw.key_nib, dw.key_scale, dw.n_max, dw.kv.shape[0], dw.q_nib, dw.q_scale, dw.w,
+                           dw.q_seq, dw.n_vis, n_q, None, buf.scores, buf.n_max, params, stream)
+        L.csa2_topk(buf.scores, buf.n_max, n_q, dw.n_vis, dw.n_max, POOL_BLOCKS, 8, None, buf.blocks, buf.ws,
+                    buf.ws_topk_bytes, stream)
+    L.csa2_index_score(dw.key_nib, dw.key_scale, dw.n_max, dw.kv.shape[0], dw.q_nib_re, dw.q_scale_re, dw.w_re,
+                       dw.q_seq, dw.n_vis, n_q, buf.blocks, buf.pool_scores, POOL_SLOTS, params, stream)
+    L.csa2_topk(buf.pool_scores, POOL_SLOTS, n_q, dw.n_vis, dw.n_max, TOPK, 1, buf.blocks, buf.sel, buf.ws,
+                buf.ws_topk_bytes, stream)
+    attend(dw, buf, params, stream)
+    return buf.out
+
+
+def attend(dw, buf: DecodeBuffers, params=None, stream=None):
+    L.csa2_sparse_attn(dw.q, dw.kv, dw.n_max, dw.kv.shape[0], buf.sel, TOPK, dw.swa, dw.swa.shape[1], dw.q_seq,
+                       dw.pos, dw.swa_first, dw.swa_cnt, buf.n_q, buf.out, buf.out_dtype, params, buf.ws,
+                       buf.ws_attn_bytes, stream)
+    return buf.out

@@ -1,0 +1,242 @@
+/*
+ * csa2.h -- C ABI of the CSA2 global-attention decode path on GB300 (sm_103a).
+ *
+ * The path (DeepSeek-V4.1-Flash, "An infra-oriented diagram of the
+ * DeepSeek-V4.1-Flash architecture", reading notes; perchy.ai card
+ * "Full. Reindex. Reuse."):
+ *   1. lightning-indexer score of every visible cache entry      csa2_index_score
+ *   2. top-512 selection (or a 2,048-block candidate pool first)  csa2_topk
+ *   3. dequantisation of the selected FP4 latents + 64-head MQA
+ *      attention over them and the 128-token FP8 window          csa2_sparse_attn
+ *   0. cache write: FP4 / FP8 packing (m=1 or gated m=2)          csa2_fp4_pack
+ *
+ * Conventions (every entry point):
+ *   - Returns a csa2_status.  Nothing aborts, prints or allocates device memory.
+ *   - Pointers marked (device) are caller-owned device buffers; the library
+ *     never frees or retains them.  Scratch space is passed in by the caller;
+ *     csa2_workspace_size() says how much.
+ *   - All work is enqueued on `stream` and is asynchronous.  Host-side argument
+ *     checks happen before anything is launched; on a failed check nothing is
+ *     launched and CSA2_ERR_INVALID_ARG / CSA2_ERR_UNSUPPORTED is returned.
+ *   - Values held in device arrays (sequence ids, lengths, selected indices,
+ *     pool block ids) are checked by the kernels: an out-of-range value is
+ *     skipped and records CSA2_ERR_BOUNDS in a sticky device status word, read
+ *     (and cleared) with csa2_get_device_status().  No kernel traps or spins
+ *     without a bound.
+ *   - Errors from the CUDA runtime (launch failures) return CSA2_ERR_CUDA.
+ *
+ * Cache record formats (logical bytes per record are fixed by the pages; the
+ * physical arrangement below is this library's choice):
+ *   KV  (S1) 288 B per entry, array of records [n_seq][n_max][288]: bytes 0..255
+ *            hold 512 FP4 E2M1 codes (low nibble = even channel), bytes
+ *            256..287 hold 32 E4M3 scales, one per 16 channels
+ *            ("512 FP4 values with one E4M3 scale per 16 channels (288 bytes)",
+ *            study, "The KV cache").
+ *   IDX (S2) 68 B per entry as two planes, so that every row is 16-B aligned:
+ *            nibbles [rows][64] (128 E2M1 codes) and scales [rows][4] (E8M0, one
+ *            per 32 channels) ("128 FP4 values with one E8M0 scale per 32
+ *            (68 bytes)", same section).  The indexer query heads (S4) use the
+ *            same format with rows = n_q * 32.
+ *   SWA (S3) 528 B per entry [n_seq][swa_cap][528]: 512 E4M3 values then 16
+ *            E8M0 scales, one per 32 channels (reading of "128 entries of 528
+ *            FP8 bytes each", same section).
+ *
+ * Rounding (shared by every packer): round to nearest, ties to even, saturating
+ * at the format's largest finite value; the sign of x is kept when the magnitude
+ * rounds to zero.  E4M3 latent scale = E4M3(amax/6); a group whose scale is zero
+ * stores zero codes.  E8M0 scale = the smallest power of two >= amax/6 (FP4) or
+ * >= amax/448 (FP8), exponent clamped to [-127, 127]; amax = 0 stores byte 0 and
+ * zero codes.
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *csa2_stream_t;   /* == cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID_ARG = 1,   /* a null pointer, a negative or misaligned size, an unknown kind */
+  CSA2_ERR_UNSUPPORTED = 2,   /* parameters other than the pages' constants, k above the limit */
+  CSA2_ERR_CUDA = 3,          /* the CUDA runtime reported an error                           */
+  CSA2_ERR_BOUNDS = 4,        /* (device) an index or length in a device array was out of range */
+  CSA2_ERR_TIMEOUT = 5,       /* (device) a bounded wait ran out                               */
+  CSA2_ERR_WORKSPACE = 6      /* the workspace passed in is smaller than required             */
+} csa2_status;
+
+/* Record kinds for csa2_entry_bytes / csa2_fp4_pack. */
+enum { CSA2_KV_NVFP4 = 0, CSA2_IDX_MXFP4 = 1, CSA2_SWA_MXFP8 = 2 };
+/* Output dtypes for csa2_sparse_attn. */
+enum { CSA2_OUT_BF16 = 0, CSA2_OUT_F32 = 1 };
+/* Operations for csa2_workspace_size. */
+enum { CSA2_OP_TOPK = 0, CSA2_OP_SPARSE_ATTN = 1 };
+
+/* Model constants.  The kernels are built for the pages' values only
+ * (study, reading notes: 64 heads, 512-wide latent, RoPE on 64 of the 512
+ * dims; lightning indexer 32 x 128, top-512; pool of 2,048 blocks of 8;
+ * helix.ml: 128-token window).  rope_base and sm_scale are free. */
+typedef struct {
+  int heads;        /* 64                      */
+  int dim;          /* 512                     */
+  int rope_dim;     /* 64                      */
+  int rope_off;     /* 448 (dims 448..511)     */
+  double rope_base; /* 10000                   */
+  float sm_scale;   /* 1/sqrt(512)             */
+  int idx_heads;    /* 32                      */
+  int idx_dim;      /* 128                     */
+  int topk;         /* 512                     */
+  int swa;          /* 128                     */
+  int block;        /* 8                       */
+  int pool_blocks;  /* 2048                    */
+} csa2_params;
+
+/* Fills *p with the pages' constants.  Never fails for a non-null p. */
+csa2_status csa2_default_params(csa2_params *p);
+
+/* Bytes per logical record: KV 288, IDX 68, SWA 528; 0 for an unknown kind. */
+size_t csa2_entry_bytes(int kind);
+
+/* Human-readable name of a status code (static string). */
+const char *csa2_status_string(csa2_status s);
+
+/*
+ * csa2_fp4_pack -- cache write: quantise bf16 rows into cache records.
+ * (study, reading notes: "In the encoder (m=2) two consecutive tokens are
+ * pooled into one entry with a learned softmax gate ... the main cache is stored
+ * in FP4 (E2M1, one E4M3 scale per 16 channels)"; section "The KV cache".)
+ *
+ *   kind         CSA2_KV_NVFP4 (src rows of 512), CSA2_IDX_MXFP4 (rows of 128),
+ *                CSA2_SWA_MXFP8 (rows of 512).
+ *   src          (device) bf16 [rows][width], row-major, 16-B aligned.
+ *   rows         number of source rows (tokens); >= 0.  0 launches nothing.
+ *   m            1, or 2 (KV only): rows must be even; output row r pools
+ *                source rows 2r and 2r+1 per channel with weights
+ *                softmax(gate_logits[2r][c], gate_logits[2r+1][c]), computed
+ *                in fp64 and rounded to bf16 before packing.
+ *   gate_logits  (device) fp32 [rows][512] when m == 2, else must be NULL.
+ *   dst          (device) KV/SWA: rows/m records of 288/528 B; IDX: the nibble
+ *                plane [rows][64].  16-B aligned.
+ *   dst_scales   (device) IDX only: the scale plane [rows][4]; NULL otherwise.
+ */
+csa2_status csa2_fp4_pack(int kind, const void *src, int64_t rows, int m, const float *gate_logits,
+                          void *dst, void *dst_scales, csa2_stream_t stream);
+
+/*
+ * csa2_index_score -- lightning-indexer scores.
+ * (study, reading notes: "32 FP4 query heads of 128 dims against one shared key
+ * per entry, ReLU'd scores summed with per-head weights"):
+ *     s_j = sum_{h<32} w_h * max(0, qhat_h . khat_j)
+ * with qhat, khat the dequantised FP4 values (E2M1 x E8M0), fp32 accumulation.
+ *
+ *   key_nib, key_scale  (device) IDX cache planes of n_seq * n_max entries;
+ *                       entry j of sequence b is row b*n_max + j.
+ *   n_max               entries per sequence; a positive multiple of 128.
+ *   n_seq               number of sequences (>= 1).
+ *   q_nib, q_scale      (device) indexer queries, IDX format, rows = n_q*32.
+ *   w                   (device) fp32 [n_q][32] per-head weights.
+ *   q_seq               (device) int32 [n_q] sequence of each query.
+ *   n_vis               (device) int32 [n_q]: entries [0, n_vis) are visible.
+ *   n_q                 number of queries (0 launches nothing).
+ *   pool_blocks         NULL: Full mode, scores[q][j] for j < n_vis[q] (other
+ *                       columns untouched).  Non-NULL (device) int32 [n_q][2048]
+ *                       block ids (-1 = none): Reindex mode, scores[q][s] for the
+ *                       16,384 pool slots s (entry 8*pool_blocks[q][s/8] + s%8),
+ *                       -inf for a slot whose block is -1 or whose entry is not
+ *                       visible (study: Reindex layers "only score a 16,384-entry
+ *                       candidate pool ... chose by blocks of 8").
+ *   scores              (device) fp32, row stride score_stride (>= n_max in Full
+ *                       mode, >= 16384 in Reindex mode).
+ */
+csa2_status csa2_index_score(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq,
+                             const void *q_nib, const void *q_scale, const float *w,
+                             const int32_t *q_seq, const int32_t *n_vis, int n_q,
+                             const int32_t *pool_blocks, float *scores, int64_t score_stride,
+                             const csa2_params *params, csa2_stream_t stream);
+
+/*
+ * csa2_topk -- top-k selection by (score descending, index ascending): the lower
+ * index wins ties; -0.0 equals +0.0.  Output indices ascending, padded with -1
+ * when fewer than k items are valid.
+ * (perchy.ai: "Main sparse selection: 512 entries"; "Later decoder indexers use
+ * at most 16,384 candidate positions"; study: "a 16,384-entry candidate pool
+ * that layer 20 chose by blocks of 8".)
+ *
+ *   scores        (device) fp32 [n_q][score_stride].
+ *   n_valid       (device) int32 [n_q]: number of visible entries.
+ *   n_max         entries per row considered (Full mode: columns [0, n_max);
+ *                 <= score_stride).
+ *   k             1 .. 2048.
+ *   block         1: items are entries j < n_valid.
+ *                 8: items are blocks b of 8 entries (b*8 < n_valid), scored by
+ *                    the max over their visible entries (reading of "by blocks
+ *                    of 8"); the output holds block ids.  pool_blocks must be NULL.
+ *   pool_blocks   NULL, or (device) int32 [n_q][2048] when the scores are Reindex
+ *                 pool slots (row length 16384): item s is entry
+ *                 8*pool_blocks[q][s/8] + s%8, valid if the block id is >= 0 and
+ *                 the entry < n_valid; the output holds those entry indices.
+ *   out           (device) int32 [n_q][k].
+ *   workspace     (device) scratch of at least csa2_workspace_size(CSA2_OP_TOPK,..)
+ *                 bytes, 256-B aligned; contents need no initialisation.
+ */
+csa2_status csa2_topk(const float *scores, int64_t score_stride, int n_q, const int32_t *n_valid,
+                      int64_t n_max, int k, int block, const int32_t *pool_blocks, int32_t *out,
+                      void *workspace, size_t workspace_bytes, csa2_stream_t stream);
+
+/*
+ * csa2_sparse_attn -- 64-head MQA attention over the selected entries plus the
+ * sliding window, k = v.
+ * (study, reading notes: "one KV latent per token and it is shared by all 64
+ * query heads (k = v, 512-wide)"; "Every other layer attends over that window
+ * plus 512 selected entries"; "RoPE touches 64 of the 512 dims, and is
+ * un-rotated on the attention output"; helix.ml: SWA "covers the latest 128
+ * tokens".)  For each query and head h:
+ *     l_i = sm_scale * q_h . khat_i  over i in {selected} + {window}
+ *     o_h = sum_i softmax(l)_i khat_i
+ * then the pairs (rope_off + 2i, rope_off + 2i + 1), i < 32, are rotated by
+ * -pos:  (a, b) <- (a cos t + b sin t, -a sin t + b cos t),
+ * t = pos * rope_base^(-2i/64).  A query with no entry at all gets zeros.
+ *
+ *   q            (device) bf16 [n_q][64][512] (already rotated by upstream).
+ *   kv_cache     (device) KV records [n_seq][n_max][288].
+ *   sel          (device) int32 [n_q][sel_stride]: entry indices (< n_max) or -1;
+ *                sel_stride in 1 .. 512.
+ *   swa_cache    (device) SWA records [n_seq][swa_cap][528]; may be NULL when
+ *                swa_cap == 0.
+ *   q_seq, pos   (device) int32 [n_q]: sequence id, RoPE position of the query.
+ *   swa_first, swa_cnt  (device) int32 [n_q]: the window is ring slots
+ *                (swa_first + t) % swa_cap, t < swa_cnt (swa_cnt <= 128).
+ *   out          (device) [n_q][64][512], bf16 or fp32 per out_dtype.
+ *   workspace    (device) >= csa2_workspace_size(CSA2_OP_SPARSE_ATTN, ..) bytes.
+ */
+csa2_status csa2_sparse_attn(const void *q, const void *kv_cache, int64_t n_max, int n_seq,
+                             const int32_t *sel, int sel_stride, const void *swa_cache, int swa_cap,
+                             const int32_t *q_seq, const int32_t *pos, const int32_t *swa_first,
+                             const int32_t *swa_cnt, int n_q, void *out, int out_dtype,
+                             const csa2_params *params, void *workspace, size_t workspace_bytes,
+                             csa2_stream_t stream);
+
+/*
+ * csa2_workspace_size -- scratch bytes needed by an operation.
+ *   op = CSA2_OP_TOPK:        n_q queries, n_items = items per row (entries,
+ *                             blocks, or 16384 pool slots), k.
+ *   op = CSA2_OP_SPARSE_ATTN: n_q queries, n_items = sel_stride + 128, k unused.
+ */
+csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t *bytes);
+
+/*
+ * csa2_get_device_status -- synchronises `stream`, returns in *out the first
+ * device-side error recorded by any kernel of this library on the current
+ * device since the last call (CSA2_OK if none), and clears it.
+ */
+csa2_status csa2_get_device_status(csa2_stream_t stream, csa2_status *out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H */

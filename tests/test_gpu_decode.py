@@ -1,0 +1,186 @@
+"""GPU parity of the decode path (indexer score -> top-512 -> sparse attention)
+against the CPU oracle, through the C ABI, on the pages' workload shapes."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from gen.workloads import CONFIGS, Workload, small  # noqa: E402
+from tests.parity import (ATTN_TOL_BF16, ATTN_TOL_F32, check_scores, check_selection,  # noqa: E402
+                          row_norm_err)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import compressed_sparse_attention_index_gb300 as c
+    return c
+
+
+def _dw(wl, n_q=None):
+    from gen.device import build_device_workload
+    return build_device_workload(wl, n_q=n_q)
+
+
+def _bufs(dw, pool=False, out_dtype=None):
+    from compressed_sparse_attention_index_gb300 import decode, CSA2_OUT_F32
+    return decode.DecodeBuffers(dw.q.shape[0], dw.n_max, pool=pool,
+                                out_dtype=CSA2_OUT_F32 if out_dtype is None else out_dtype)
+
+
+@pytest.mark.parametrize("zipf", [False, True])
+def test_index_score_full_parity(lib, oracle_lib, zipf):
+    wl = small(n_seq=2, n_entries=1000, zipf=zipf, seed=200 + zipf)
+    dw = _dw(wl)
+    buf = _bufs(dw)
+    lib.csa2_index_score(dw.key_nib, dw.key_scale, dw.n_max, 2, dw.q_nib, dw.q_scale, dw.w, dw.q_seq, dw.n_vis, 2,
+                         None, buf.scores, dw.n_max)
+    s = buf.scores.cpu().numpy()
+    assert lib.csa2_get_device_status() == 0
+    for qi in range(2):
+        check_scores(s[qi, :1000], oracle_lib.full_scores(wl, qi))
+
+
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_sparse_attn_parity_on_oracle_selection(lib, oracle_lib, out_f32):
+    from compressed_sparse_attention_index_gb300 import decode, CSA2_OUT_F32, CSA2_OUT_BF16
+    wl = small(n_seq=3, n_entries=3000, seed=210)
+    dw = _dw(wl)
+    buf = _bufs(dw, out_dtype=CSA2_OUT_F32 if out_f32 else CSA2_OUT_BF16)
+    refs = [oracle_lib.decode_query(wl, qi) for qi in range(3)]
+    sel = np.stack([r["sel"] for r in refs])
+    sel[1, 100:] = -1                                   # ragged selection with holes
+    sel[1, 40:60] = -1
+    buf.sel.copy_(torch.from_numpy(sel))
+    decode.attend(dw, buf)
+    out = buf.out.float().cpu().numpy()
+    tol = ATTN_TOL_F32 if out_f32 else ATTN_TOL_BF16
+    from oracle.compose import kv_records, swa_records
+    for qi in range(3):
+        s = sel[qi][sel[qi] >= 0]
+        ref = oracle_lib.sparse_attn(wl.q(qi), kv_records(wl, qi, s),
+                                     swa_records(wl, qi, int(wl.swa_first()[qi]), int(wl.swa_cnt()[qi])),
+                                     int(wl.pos()[qi]))
+        assert row_norm_err(out[qi], ref) <= tol
+
+
+def _check_full(lib, oracle_lib, wl, dw, buf, queries):
+    from compressed_sparse_attention_index_gb300 import decode
+    decode.full_decode(dw, buf)
+    sel = buf.sel.cpu().numpy()
+    out = buf.out.float().cpu().numpy()
+    assert lib.csa2_get_device_status() == 0
+    worst = 0.0
+    for qi in queries:
+        r = oracle_lib.decode_query(wl, qi)
+        check_selection(sel[qi], r["sel"], r["scores"])
+        # attention is compared on the GPU's own selection (equal up to near-ties)
+        from oracle.compose import kv_records, swa_records
+        s = sel[qi][sel[qi] >= 0]
+        ref = oracle_lib.sparse_attn(wl.q(qi), kv_records(wl, int(wl.q_seq()[qi]), s),
+                                     swa_records(wl, int(wl.q_seq()[qi]), int(wl.swa_first()[qi]),
+                                                 int(wl.swa_cnt()[qi])), int(wl.pos()[qi]))
+        worst = max(worst, row_norm_err(out[qi], ref))
+    assert worst <= ATTN_TOL_F32, worst
+    return worst
+
+
+def test_full_decode_config0(lib, oracle_lib):
+    wl = CONFIGS[0]
+    dw = _dw(wl)
+    _check_full(lib, oracle_lib, wl, dw, _bufs(dw), [0])
+
+
+@pytest.mark.parametrize("n_entries", [300, 1000, 5003])
+def test_full_decode_small_ragged(lib, oracle_lib, n_entries):
+    wl = small(n_seq=2, n_entries=n_entries, seed=220 + n_entries)
+    dw = _dw(wl)
+    _check_full(lib, oracle_lib, wl, dw, _bufs(dw), [0, 1])
+
+
+def test_full_decode_config1_sampled(lib, oracle_lib):
+    wl = CONFIGS[1]
+    dw = _dw(wl)
+    _check_full(lib, oracle_lib, wl, dw, _bufs(dw), [0, 17, 31])
+
+
+def test_full_decode_config4_full_size_sampled(lib, oracle_lib):
+    wl = CONFIGS[4]
+    dw = _dw(wl)
+    _check_full(lib, oracle_lib, wl, dw, _bufs(dw), [0, 7])
+
+
+def test_reindex_decode_small(lib, oracle_lib):
+    from compressed_sparse_attention_index_gb300 import decode
+    wl = small(n_seq=2, n_entries=40_000, pool=True, seed=230)
+    dw = _dw(wl)
+    buf = _bufs(dw, pool=True)
+    decode.reindex_decode(dw, buf)
+    blocks, sel, out = buf.blocks.cpu().numpy(), buf.sel.cpu().numpy(), buf.out.float().cpu().numpy()
+    assert lib.csa2_get_device_status() == 0
+    from oracle.compose import kv_records, swa_records
+    for qi in range(2):
+        r = oracle_lib.reindex_query(wl, qi)
+        bscore = lambda b: max(r["scores_full"][8 * b:min(40_000, 8 * b + 8)])
+        check_selection(blocks[qi], r["blocks"], None, pos_to_score=bscore)
+        if np.array_equal(blocks[qi], r["blocks"]):
+            pos_score = dict(zip(r["pool_pos"].tolist(), r["scores_pool"].tolist()))
+            check_selection(sel[qi], r["sel"], None, pos_to_score=lambda p: pos_score[p])
+        s = sel[qi][sel[qi] >= 0]
+        ref = oracle_lib.sparse_attn(wl.q(qi), kv_records(wl, qi, s),
+                                     swa_records(wl, qi, int(wl.swa_first()[qi]), int(wl.swa_cnt()[qi])),
+                                     int(wl.pos()[qi]))
+        assert row_norm_err(out[qi], ref) <= ATTN_TOL_F32
+
+
+def test_reindex_decode_config3_full_size_sampled(lib, oracle_lib):
+    from compressed_sparse_attention_index_gb300 import decode
+    wl = CONFIGS[3]
+    dw = _dw(wl)
+    buf = _bufs(dw, pool=True)
+    decode.reindex_decode(dw, buf)
+    blocks, sel = buf.blocks.cpu().numpy(), buf.sel.cpu().numpy()
+    assert lib.csa2_get_device_status() == 0
+    r = oracle_lib.reindex_query(wl, 5)
+    n = wl.n_entries
+    bscore = lambda b: max(r["scores_full"][8 * b:min(n, 8 * b + 8)])
+    check_selection(blocks[5], r["blocks"], None, pos_to_score=bscore)
+    if np.array_equal(blocks[5], r["blocks"]):
+        pos_score = dict(zip(r["pool_pos"].tolist(), r["scores_pool"].tolist()))
+        check_selection(sel[5], r["sel"], None, pos_to_score=lambda p: pos_score[p])
+
+
+def test_prefill_m2_config2_sampled(lib, oracle_lib):
+    wl = CONFIGS[2]
+    dw = _dw(wl)
+    buf = _bufs(dw)
+    _check_full(lib, oracle_lib, wl, dw, buf, [0, 1, 2, 3, 127, 128, 1023, 1024, 4095, 8191])
+
+
+def test_out_of_range_selection_is_skipped_and_reported(lib, oracle_lib):
+    from compressed_sparse_attention_index_gb300 import decode
+    wl = small(n_seq=1, n_entries=1000, seed=240)
+    dw = _dw(wl)
+    buf = _bufs(dw)
+    sel = np.full((1, 512), -1, np.int32)
+    sel[0, :3] = [5, 10**7, 7]                          # 10**7 is beyond the cache
+    buf.sel.copy_(torch.from_numpy(sel))
+    decode.attend(dw, buf)
+    assert lib.csa2_get_device_status() == 4
+    from oracle.compose import kv_records, swa_records
+    ref = oracle_lib.sparse_attn(wl.q(0), kv_records(wl, 0, [5, 7]), swa_records(wl, 0, int(wl.swa_first()[0]),
+                                                                                 int(wl.swa_cnt()[0])),
+                                 int(wl.pos()[0]))
+    assert row_norm_err(buf.out.float().cpu().numpy()[0], ref) <= ATTN_TOL_F32
+
+
+def test_empty_query_gives_zeros(lib):
+    from compressed_sparse_attention_index_gb300 import decode
+    wl = small(n_seq=1, n_entries=256, seed=241)
+    dw = _dw(wl)
+    buf = _bufs(dw)
+    buf.sel.fill_(-1)
+    dw.swa_cnt.zero_()
+    decode.attend(dw, buf)
+    assert lib.csa2_get_device_status() == 0
+    assert torch.count_nonzero(buf.out).item() == 0
