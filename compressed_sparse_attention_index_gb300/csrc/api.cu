@@ -9,10 +9,10 @@
 namespace csa2 {
 cudaError_t launch_pack(int kind, const void *src, int64_t rows, int m, const float *gate, void *dst,
                         void *dst_scales, cudaStream_t st);
-cudaError_t launch_index_score_simt(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
-                                    const uint8_t *q_nib, const uint8_t *q_scale, const float *w,
-                                    const int32_t *q_seq, const int32_t *n_vis, int n_q, const int32_t *pool,
-                                    float *scores, int64_t stride, int *status, cudaStream_t st);
+cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
+                                  const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
+                                  const int32_t *n_vis, int n_q, const int32_t *pool, float *scores, int64_t stride,
+                                  int *status, cudaStream_t st);
 size_t topk_workspace_bytes(int n_q, int64_t n_items);
 cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max, int k,
                         int block, const int32_t *pool, int32_t *out, void *ws, int *status, cudaStream_t st);
@@ -121,12 +121,12 @@ csa2_status csa2_index_score(const void *key_nib, const void *key_scale, int64_t
   if (n_q == 0) return CSA2_OK;
   if (!key_nib || !key_scale || !q_nib || !q_scale || !w || !q_seq || !n_vis || !scores)
     return CSA2_ERR_INVALID_ARG;
-  if (!aligned(key_nib, 16) || !aligned(key_scale, 4) || !aligned(q_nib, 16) || !aligned(q_scale, 4) ||
-      !aligned(scores, 4))
+  if (!aligned(key_nib, 16) || !aligned(key_scale, 16) || !aligned(q_nib, 16) || !aligned(q_scale, 16) ||
+      !aligned(w, 16) || !aligned(scores, 4))
     return CSA2_ERR_INVALID_ARG;
   int *st = status_ptr();
   if (st == nullptr) return CSA2_ERR_CUDA;
-  return from_cuda(launch_index_score_simt(
+  return from_cuda(launch_index_score_tc(
       static_cast<const uint8_t *>(key_nib), static_cast<const uint8_t *>(key_scale), n_max, n_seq,
       static_cast<const uint8_t *>(q_nib), static_cast<const uint8_t *>(q_scale), w, q_seq, n_vis, n_q, pool_blocks,
       scores, score_stride, st, (cudaStream_t)stream));

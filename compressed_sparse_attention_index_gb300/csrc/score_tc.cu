@@ -1,0 +1,335 @@
+// Lightning-indexer scores on the 5th-generation tensor cores (csa2_index_score).
+//
+// "32 FP4 query heads of 128 dims against one shared key per entry, ReLU'd
+// scores summed with per-head weights" and the keys are "128 FP4 values with one
+// E8M0 scale per 32" ("An infra-oriented diagram of the DeepSeek-V4.1-Flash
+// architecture", lightning-indexer note and section "The KV cache").  That is
+// exactly the MXFP4 block-scaled format the tcgen05 MMA consumes, so
+//     D[entry][head] = sum_c khat[entry][c] * qhat[head][c]
+// is one  M=128 (entries) x N=32 (heads) x K=128  product per tile, issued as two
+// tcgen05.mma.kind::mxf4.block_scale.scale_vec::2X (K=64 each) into TMEM, and the
+// epilogue computes s = sum_h w_h * max(0, D[entry][h]) per row.
+//
+// The kernel is HBM-bound (68 B of key per entry, 8 FLOP/B of FP4 MMA): a
+// persistent CTA per SM streams tiles through a 12-stage shared-memory ring.
+// Warp roles (192 threads):
+//   warp 0      producer: TMA of the 128 x 64 B nibble tile (or 16 gathered
+//               8-entry blocks in pool mode), TMA of the query's 32 x 64 B, bulk
+//               copies of the key and query E8M0 scales;
+//   warp 1      TMEM owner + MMA issuer: rearranges the scales in shared memory
+//               into the 32-lane x 16-B layout tcgen05.cp expects, copies them
+//               into TMEM, issues the two MMAs, commits to the stage's "empty"
+//               barrier and to the accumulator's "full" barrier;
+//   warps 2..5  epilogue: one TMEM lane (= one entry) per thread, 32 columns
+//               (= heads) per tcgen05.ld, ReLU + weighted sum, coalesced store.
+// Two TMEM accumulators let the epilogue of tile i overlap the MMA of tile i+1.
+// Every mbarrier wait is bounded (CSA2_ERR_TIMEOUT instead of a hang).
+#include <cuda.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace csa2 {
+
+constexpr int kScStages = 12;
+constexpr int kScStageBytes = 12288;
+constexpr int kOffA = 0;          // 128 rows x 64 B, 64B-swizzled (TMA writes it, MMA reads it)
+constexpr int kOffB = 8192;       // 32 rows x 64 B query nibbles, 64B-swizzled
+constexpr int kOffSFA = 10240;    // 512 B key scales: staged [row][4], rearranged in place
+constexpr int kOffSFB = 10752;    // 512 B query scales: staged [head][4] in the first 128 B
+constexpr int kScThreads = 192;
+constexpr uint32_t kScTmemCols = 128;   // 2 x 32 accumulator columns + 2 x 4 SFA + 2 x 4 SFB
+constexpr uint32_t kColSFA = 64, kColSFB = 72;
+
+// Instruction descriptor of kind::mxf4 block-scaled MMA, M=128, N=32, both
+// operands E2M1 and K-major, UE8M0 scales; sf_id picks the scale byte pair.
+__host__ __device__ constexpr uint32_t idesc_mxf4_m128n32(uint32_t sf_id) {
+  return (sf_id << 4)            // B scale-factor id
+         | (1u << 7)             // A format: E2M1
+         | (1u << 10)            // B format: E2M1
+         | ((32u >> 3) << 17)    // N / 8
+         | (1u << 23)            // scale format UE8M0
+         | ((128u >> 4) << 24)   // M / 16
+         | (sf_id << 29);        // A scale-factor id
+}
+
+struct ScoreTcArgs {
+  const uint8_t *key_scale;
+  const uint8_t *q_scale;
+  const float *w;
+  const int32_t *q_seq;
+  const int32_t *n_vis;
+  const int32_t *pool;
+  float *scores;
+  int64_t stride;
+  int64_t n_max;
+  int n_seq;
+  int n_q;
+  int tiles_per_q;
+  int64_t total_tiles;
+  int *status;
+};
+
+struct TileInfo {
+  int q, tile, seq, nv;
+};
+
+// Shared tile schedule of every role: tile T = blockIdx.x + k * gridDim.x over
+// (query, 128-entry tile); tiles past a query's visible length are skipped.
+__device__ __forceinline__ bool next_tile(const ScoreTcArgs &P, int64_t &T, TileInfo &t) {
+  for (; T < P.total_tiles; T += gridDim.x) {
+    t.q = (int)(T / P.tiles_per_q);
+    t.tile = (int)(T % P.tiles_per_q);
+    t.seq = __ldg(P.q_seq + t.q);
+    t.nv = __ldg(P.n_vis + t.q);
+    if (t.seq < 0 || t.seq >= P.n_seq || t.nv < 0 || (int64_t)t.nv > P.n_max) {
+      if (t.tile == 0 && threadIdx.x == 0) record_error(P.status, CSA2_ERR_BOUNDS);
+      continue;
+    }
+    if (P.pool == nullptr && (int64_t)t.tile * 128 >= t.nv) continue;
+    T += gridDim.x;
+    return true;
+  }
+  return false;
+}
+
+__global__ void __launch_bounds__(kScThreads, 1)
+    index_score_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a8,
+                          const __grid_constant__ CUtensorMap map_b, ScoreTcArgs P) {
+  extern __shared__ __align__(1024) unsigned char sc_smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(sc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full_bar[kScStages], empty_bar[kScStages], acc_full[2], acc_empty[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kScStages; s++) {
+      ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; a++) {
+      ptx::mbar_init(&acc_full[a], 1);
+      ptx::mbar_init(&acc_empty[a], 4);
+    }
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&map_a);
+    ptx::prefetch_tensormap(&map_a8);
+    ptx::prefetch_tensormap(&map_b);
+  }
+  if (warp == 1) ptx::tmem_alloc(&tmem_base_sh, kScTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  auto fail = [&]() {
+    record_error(P.status, CSA2_ERR_TIMEOUT);
+    abort_flag = 1;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t policy = ptx::policy_evict_first();
+    int64_t T = blockIdx.x;
+    TileInfo t;
+    for (uint32_t it = 0; next_tile(P, T, t); it++) {
+      if (abort_flag) break;
+      const uint32_t s = it % kScStages, r = it / kScStages;
+      if (!ptx::mbar_wait(&empty_bar[s], (r & 1) ^ 1)) { fail(); break; }
+      unsigned char *st = smem + s * kScStageBytes;
+      const int64_t row0 = (int64_t)t.seq * P.n_max;
+      if (P.pool == nullptr) {
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&full_bar[s], 8192 + 2048 + 512 + 128);
+          const int64_t r0 = row0 + (int64_t)t.tile * 128;
+          ptx::tma_load_2d_hint(st + kOffA, &map_a, 0, (int32_t)r0, &full_bar[s], policy);
+          ptx::tma_load_2d(st + kOffB, &map_b, 0, t.q * kIdxHeads, &full_bar[s]);
+          ptx::bulk_load(st + kOffSFA, P.key_scale + r0 * 4, 512, &full_bar[s]);
+          ptx::bulk_load(st + kOffSFB, P.q_scale + (int64_t)t.q * kIdxHeads * 4, 128, &full_bar[s]);
+        }
+      } else {
+        int blk = -1;
+        bool ok = false;
+        if (lane < 16) {
+          blk = __ldg(P.pool + (int64_t)t.q * kPoolBlocks + t.tile * 16 + lane);
+          ok = blk >= 0 && (int64_t)blk * kBlock < P.n_max;
+          if (blk >= 0 && !ok) record_error(P.status, CSA2_ERR_BOUNDS);
+        }
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, ok);
+        if (lane == 0)
+          ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)__popc(m) * (512 + 32) + 2048 + 128);
+        __syncwarp();
+        if (ok) {
+          const int64_t r0 = row0 + (int64_t)blk * kBlock;
+          ptx::tma_load_2d_hint(st + kOffA + lane * 512, &map_a8, 0, (int32_t)r0, &full_bar[s], policy);
+          ptx::bulk_load(st + kOffSFA + lane * 32, P.key_scale + r0 * 4, 32, &full_bar[s]);
+        }
+        if (lane == 0) {
+          ptx::tma_load_2d(st + kOffB, &map_b, 0, t.q * kIdxHeads, &full_bar[s]);
+          ptx::bulk_load(st + kOffSFB, P.q_scale + (int64_t)t.q * kIdxHeads * 4, 128, &full_bar[s]);
+        }
+      }
+      __syncwarp();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int64_t T = blockIdx.x;
+    TileInfo t;
+    const uint32_t idesc0 = idesc_mxf4_m128n32(0), idesc1 = idesc_mxf4_m128n32(2);
+    for (uint32_t it = 0; next_tile(P, T, t); it++) {
+      if (abort_flag) break;
+      const uint32_t s = it % kScStages, r = it / kScStages, a = it & 1, ra = it >> 1;
+      if (!ptx::mbar_wait(&full_bar[s], r & 1)) { fail(); break; }
+      unsigned char *st = smem + s * kScStageBytes;
+      // scales -> tcgen05.cp layout: 16-B line m0 holds rows m0, m0+32, m0+64, m0+96
+      uint32_t *sfa = reinterpret_cast<uint32_t *>(st + kOffSFA);
+      uint32_t *sfb = reinterpret_cast<uint32_t *>(st + kOffSFB);
+      uint32_t va[4];
+#pragma unroll
+      for (int i = 0; i < 4; i++) va[i] = sfa[i * 32 + lane];
+      const uint32_t vb = sfb[lane];
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; i++) sfa[lane * 4 + i] = va[i];
+      sfb[lane * 4 + 0] = vb;
+      sfb[lane * 4 + 1] = 0u;
+      sfb[lane * 4 + 2] = 0u;
+      sfb[lane * 4 + 3] = 0u;
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (!ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) {
+          fail();
+        } else {
+          ptx::tc_fence_after();
+          const uint32_t t_sfa = tmem + kColSFA + a * 4, t_sfb = tmem + kColSFB + a * 4;
+          ptx::tc_cp_32x128b_warpx4(t_sfa, ptx::smem_desc(ptx::smem_u32(sfa), 0, 128, 0));
+          ptx::tc_cp_32x128b_warpx4(t_sfb, ptx::smem_desc(ptx::smem_u32(sfb), 0, 128, 0));
+          const uint64_t ad = ptx::smem_desc(ptx::smem_u32(st + kOffA), 16, 512, 4);
+          const uint64_t bd = ptx::smem_desc(ptx::smem_u32(st + kOffB), 16, 512, 4);
+          ptx::tc_mma_mxf4(tmem + a * 32, ad, bd, idesc0, t_sfa, t_sfb, 0u);
+          ptx::tc_mma_mxf4(tmem + a * 32, ad + 2, bd + 2, idesc1, t_sfa, t_sfb, 1u);   // +32 B along K
+          ptx::tc_commit(&empty_bar[s]);
+          ptx::tc_commit(&acc_full[a]);
+        }
+      }
+      __syncwarp();
+      if (abort_flag) break;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int64_t T = blockIdx.x;
+    TileInfo t;
+    int cur_q = -1;
+    float wv[kIdxHeads];
+    for (uint32_t it = 0; next_tile(P, T, t); it++) {
+      if (abort_flag) break;
+      const uint32_t a = it & 1, ra = it >> 1;
+      if (t.q != cur_q) {
+        const float4 *wp = reinterpret_cast<const float4 *>(P.w + (int64_t)t.q * kIdxHeads);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+          const float4 v = __ldg(wp + i);
+          wv[4 * i] = v.x;
+          wv[4 * i + 1] = v.y;
+          wv[4 * i + 2] = v.z;
+          wv[4 * i + 3] = v.w;
+        }
+        cur_q = t.q;
+      }
+      if (!ptx::mbar_wait(&acc_full[a], ra & 1)) { fail(); break; }
+      ptx::tc_fence_after();
+      uint32_t d[32];
+      ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + a * 32, d);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&acc_empty[a]);
+      float s = 0.f;
+#pragma unroll
+      for (int h = 0; h < kIdxHeads; h++) s = fmaf(wv[h], fmaxf(__uint_as_float(d[h]), 0.f), s);
+      const int64_t item = (int64_t)t.tile * 128 + row;
+      if (P.pool == nullptr) {
+        if (item < t.nv) P.scores[(int64_t)t.q * P.stride + item] = s;
+      } else {
+        const int blk = __ldg(P.pool + (int64_t)t.q * kPoolBlocks + (item >> 3));
+        const int64_t j = (int64_t)blk * kBlock + (item & 7);
+        const bool ok = blk >= 0 && (int64_t)blk * kBlock < P.n_max && j < t.nv;
+        P.scores[(int64_t)t.q * P.stride + item] = ok ? s : -INFINITY;
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kScTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+static bool encode_rows64(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+  cuuint64_t dims[2] = {64, rows};
+  cuuint64_t strides[1] = {64};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = cuTensorMapEncodeTiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+                                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static int sm_count() {
+  static int counts[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (counts[dev] == 0) cudaDeviceGetAttribute(&counts[dev], cudaDevAttrMultiProcessorCount, dev);
+  return counts[dev] > 0 ? counts[dev] : 148;
+}
+
+cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
+                                  const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
+                                  const int32_t *n_vis, int n_q, const int32_t *pool, float *scores, int64_t stride,
+                                  int *status, cudaStream_t st) {
+  CUtensorMap ma, ma8, mb;
+  if (!encode_rows64(&ma, key_nib, (uint64_t)n_seq * n_max, 128) ||
+      !encode_rows64(&ma8, key_nib, (uint64_t)n_seq * n_max, 8) || !encode_rows64(&mb, q_nib, (uint64_t)n_q * 32, 32))
+    return cudaErrorInvalidValue;
+  ScoreTcArgs P;
+  P.key_scale = key_scale;
+  P.q_scale = q_scale;
+  P.w = w;
+  P.q_seq = q_seq;
+  P.n_vis = n_vis;
+  P.pool = pool;
+  P.scores = scores;
+  P.stride = stride;
+  P.n_max = n_max;
+  P.n_seq = n_seq;
+  P.n_q = n_q;
+  P.tiles_per_q = pool ? kPoolSlots / 128 : (int)(n_max / 128);
+  P.total_tiles = (int64_t)n_q * P.tiles_per_q;
+  P.status = status;
+  const size_t smem = (size_t)kScStages * kScStageBytes + 1024;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_done[64] = {};
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const int64_t grid = P.total_tiles < sm_count() ? P.total_tiles : sm_count();
+  index_score_tc_kernel<<<(unsigned)grid, kScThreads, smem, st>>>(ma, ma8, mb, P);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

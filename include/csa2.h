@@ -135,11 +135,12 @@ csa2_status csa2_fp4_pack(int kind, const void *src, int64_t rows, int m, const 
  * with qhat, khat the dequantised FP4 values (E2M1 x E8M0), fp32 accumulation.
  *
  *   key_nib, key_scale  (device) IDX cache planes of n_seq * n_max entries;
- *                       entry j of sequence b is row b*n_max + j.
+ *                       entry j of sequence b is row b*n_max + j.  16-B aligned.
  *   n_max               entries per sequence; a positive multiple of 128.
  *   n_seq               number of sequences (>= 1).
- *   q_nib, q_scale      (device) indexer queries, IDX format, rows = n_q*32.
- *   w                   (device) fp32 [n_q][32] per-head weights.
+ *   q_nib, q_scale      (device) indexer queries, IDX format, rows = n_q*32;
+ *                       16-B aligned.
+ *   w                   (device) fp32 [n_q][32] per-head weights, 16-B aligned.
  *   q_seq               (device) int32 [n_q] sequence of each query.
  *   n_vis               (device) int32 [n_q]: entries [0, n_vis) are visible.
  *   n_q                 number of queries (0 launches nothing).
