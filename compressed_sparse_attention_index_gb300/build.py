@@ -62,7 +62,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
         raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
     if force or procs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        subprocess.check_call([nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcuda"])
+        subprocess.check_call([nvcc()] + ARCH + ["-shared", "-o", tmp] + objs)
         os.replace(tmp, LIB)
     return LIB
 

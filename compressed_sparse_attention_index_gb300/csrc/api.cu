@@ -13,12 +13,13 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
                                   const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
                                   const int32_t *n_vis, int n_q, const int32_t *pool, float *scores, int64_t stride,
                                   int *status, cudaStream_t st);
-size_t topk_workspace_bytes(int n_q, int64_t n_items);
+size_t topk_workspace_bytes(int n_q, int64_t n_items, int k);
+bool topk_items_supported(int64_t n_items, int k);
 cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max, int k,
                         int block, const int32_t *pool, int32_t *out, void *ws, int *status, cudaStream_t st);
 size_t attn_workspace_bytes(int n_q, int sel_stride);
-cudaError_t launch_attn_simt(const void *q, const void *kv, int64_t n_max, int n_seq, const int32_t *sel,
-                             int sel_stride, const void *swa, int swa_cap, const int32_t *q_seq, const int32_t *pos,
+cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_seq, const int32_t *sel,
+                           int sel_stride, const void *swa, int swa_cap, const int32_t *q_seq, const int32_t *pos,
                              const int32_t *swa_first, const int32_t *swa_cnt, int n_q, void *out, int out_dtype,
                              float sm_scale, double rope_base, void *ws, int *status, cudaStream_t st);
 
@@ -133,10 +134,10 @@ csa2_status csa2_index_score(const void *key_nib, const void *key_scale, int64_t
 }
 
 csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t *bytes) {
-  (void)k;
   if (bytes == nullptr || n_q < 0 || n_items < 0) return CSA2_ERR_INVALID_ARG;
   if (op == CSA2_OP_TOPK) {
-    *bytes = topk_workspace_bytes(n_q, n_items);
+    if (k < 1 || k > 2048) return CSA2_ERR_UNSUPPORTED;
+    *bytes = topk_workspace_bytes(n_q, n_items, k);
     return CSA2_OK;
   }
   if (op == CSA2_OP_SPARSE_ATTN) {
@@ -161,7 +162,8 @@ csa2_status csa2_topk(const float *scores, int64_t score_stride, int n_q, const 
   if (n_q == 0) return CSA2_OK;
   if (!scores || !n_valid || !out) return CSA2_ERR_INVALID_ARG;
   const int64_t items = pool_blocks ? (int64_t)kPoolSlots : (block == 1 ? n_max : (n_max + kBlock - 1) / kBlock);
-  const size_t need = topk_workspace_bytes(n_q, items);
+  if (!topk_items_supported(items, k)) return CSA2_ERR_UNSUPPORTED;
+  const size_t need = topk_workspace_bytes(n_q, items, k);
   if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned(workspace, 256))))
     return CSA2_ERR_WORKSPACE;
   int *st = status_ptr();
@@ -192,7 +194,7 @@ csa2_status csa2_sparse_attn(const void *q, const void *kv_cache, int64_t n_max,
   if (st == nullptr) return CSA2_ERR_CUDA;
   const float sm_scale = params ? params->sm_scale : 1.0f / sqrtf((float)kDim);
   const double rope_base = params ? params->rope_base : 10000.0;
-  return from_cuda(launch_attn_simt(q, kv_cache, n_max, n_seq, sel, sel_stride, swa_cache, swa_cap, q_seq, pos,
+  return from_cuda(launch_attn_tc(q, kv_cache, n_max, n_seq, sel, sel_stride, swa_cache, swa_cap, q_seq, pos,
                                     swa_first, swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, workspace, st,
                                     (cudaStream_t)stream));
 }

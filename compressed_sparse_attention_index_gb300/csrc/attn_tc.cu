@@ -1,0 +1,546 @@
+// Sparse MQA attention on the 5th-generation tensor cores (csa2_sparse_attn).
+//
+// "There is one KV latent per token and it is shared by all 64 query heads
+// (k = v, 512-wide)"; "Every other layer attends over that window plus 512
+// selected entries"; "RoPE touches 64 of the 512 dims, and is un-rotated on the
+// attention output" ("An infra-oriented diagram of the DeepSeek-V4.1-Flash
+// architecture", reading notes).
+//
+// The entry slots of a query (sel_stride selected entries, -1 = empty, then the
+// swa_cnt window entries) are processed in chunks of 128.  Per chunk:
+//   1. gather + dequantise the 128 records to bf16 in shared memory (exact: an
+//      E2M1 x E4M3 product has <= 6 significant bits, E4M3 x 2^e fits bf16);
+//   2. S^T[entry][head] = Khat . Q^T     tcgen05 kind::f16, M=128 entries, N=64
+//      heads, K=512 (both operands K-major, 128B-swizzled);
+//   3. softmax numerators p = 2^(l*log2e - m_ref) per (entry, head), stored as
+//      bf16 hi + lo parts (together ~16 significant bits);
+//   4. O^T[dim][head] += Vhat^T . P^T     M=128 dims (4 blocks), N=64, K=128
+//      entries; Vhat^T is the same shared-memory chunk read MN-major (k = v).
+//      A fifth block multiplies an all-ones tile, so its rows accumulate the
+//      softmax denominator sum_e p[e][h] with exactly the same weights.
+// m_ref is the running per-head maximum, raised lazily: the accumulators in
+// TMEM are rescaled only when a chunk's maximum exceeds m_ref by more than 8
+// (factor 256), otherwise the larger numerators are simply accumulated.
+// A CTA handles a range of chunks of one query; with a single range it
+// finishes the output (normalise, un-rotate, store), otherwise it writes
+// (O, m, l) partials that attn_merge_kernel combines.
+//
+// 256 threads: all of them gather/dequantise; warps 0-3 (TMEM lane quarters)
+// run the softmax on S^T rows; thread 0 issues the MMAs; all 8 warps share the
+// final read-out of the 5 x 64 accumulator columns.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace csa2 {
+
+constexpr int kTcChunk = 128;
+constexpr int kTcThreads = 256;
+// shared-memory layout (bytes; the big regions are 1024-aligned)
+constexpr int kSmK = 0;                         // 128 entries x 512 dims bf16  (128 KB)
+constexpr int kSmQ = kSmK + 128 * 1024;         // 64 heads  x 512 dims bf16    (64 KB)
+constexpr int kSmPhi = kSmQ + 64 * 1024;        // 64 heads  x 128 entries bf16 (16 KB)
+constexpr int kSmPlo = kSmPhi + 16 * 1024;      //                              (16 KB)
+constexpr int kSmOnes = kSmPlo + 16 * 1024;     // one 8 x 16-B core matrix of bf16 ones (128 B)
+constexpr int kSmMref = kSmOnes + 128;          // float[64] running maxima
+constexpr int kSmAlpha = kSmMref + 256;         // float[64] rescale factors
+constexpr int kSmValid = kSmAlpha + 256;        // uint8[128] slot validity
+constexpr int kSmBars = kSmValid + 128;         // 2 mbarriers, tmem base, flags
+constexpr int kSmTotal = kSmBars + 32;
+constexpr int kSmAlloc = kSmTotal + 1024;       // + alignment slack (<= 227 KB)
+constexpr uint32_t kAttTmemCols = 512;
+constexpr uint32_t kColS = 0;                   // S^T: 64 columns
+constexpr uint32_t kColO = 64;                  // O^T: 5 blocks x 64 columns (block 4 = denominators)
+constexpr float kRescaleLog2 = 8.0f;
+
+// byte offset of 16-B chunk `ch` (0..7) in row r of a 128B-swizzled 1024-B atom
+__device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t ch) { return r * 128u + ((ch ^ (r & 7u)) << 4); }
+
+// kind::f16 instruction descriptor: bf16 x bf16 -> f32, M=128, N=64, A K- or MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_m128n64(uint32_t a_mn_major) {
+  return (1u << 4)               // D format f32
+         | (1u << 7)             // A bf16
+         | (1u << 10)            // B bf16
+         | (a_mn_major << 15)    // A major-ness
+         | ((64u >> 3) << 17)    // N / 8
+         | ((128u >> 4) << 24);  // M / 16
+}
+
+struct AttnTcArgs {
+  const uint16_t *q;
+  const uint8_t *kv;
+  int64_t n_max;
+  int n_seq;
+  const int32_t *sel;
+  int sel_stride;
+  const uint8_t *swa;
+  int swa_cap;
+  const int32_t *q_seq, *pos, *swa_first, *swa_cnt;
+  void *out;
+  int out_f32;
+  float scale_log2;
+  double rope_base;
+  int nsplit, chunks_per_split;
+  float *part;      // [n_q][nsplit][64][512]
+  float *part_ml;   // [n_q][nsplit][2][64]
+  int *status;
+};
+
+__device__ __forceinline__ void unrotate_pair_tc(float &a, float &b, int pair, int pos, double base) {
+  const double th = (double)pos * pow(base, -2.0 * (double)pair / (double)kRopeDim);
+  double sn, cs;
+  sincos(th, &sn, &cs);
+  const float c = (float)cs, s = (float)sn;
+  const float x = a, y = b;
+  a = x * c + y * s;
+  b = -x * s + y * c;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
+  extern __shared__ __align__(1024) unsigned char at_smem_raw[];
+  unsigned char *sm = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(at_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float *m_ref = reinterpret_cast<float *>(sm + kSmMref);
+  float *alpha_sh = reinterpret_cast<float *>(sm + kSmAlpha);
+  float(*red)[kHeads] = reinterpret_cast<float(*)[kHeads]>(sm + kSmPhi);   // [4][64], during the max only
+  uint8_t *valid_sh = sm + kSmValid;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kSmBars);
+  uint64_t &bar_s = bars[0], &bar_o = bars[1];
+  uint32_t &tmem_sh = *reinterpret_cast<uint32_t *>(sm + kSmBars + 16);
+  volatile int &need_rescale = *reinterpret_cast<volatile int *>(sm + kSmBars + 20);
+  volatile int &bad_sh = *reinterpret_cast<volatile int *>(sm + kSmBars + 24);
+
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int qi = blockIdx.y, split = blockIdx.x;
+  const int seq = __ldg(A.q_seq + qi);
+  const int swa_cnt = __ldg(A.swa_cnt + qi), swa_first = __ldg(A.swa_first + qi);
+  const bool bad = seq < 0 || seq >= A.n_seq || swa_cnt < 0 || swa_cnt > kSwa ||
+                   (swa_cnt > 0 && (swa_first < 0 || swa_first >= A.swa_cap));
+  if (bad && t == 0 && split == 0) record_error(A.status, CSA2_ERR_BOUNDS);
+  const int n_slots = A.sel_stride + (bad ? 0 : swa_cnt);
+  const int c0 = split * A.chunks_per_split;
+  const int c1 = bad ? c0 : min((n_slots + kTcChunk - 1) / kTcChunk, c0 + A.chunks_per_split);
+
+  if (t == 0) {
+    ptx::mbar_init(&bar_s, 1);
+    ptx::mbar_init(&bar_o, 1);
+    bad_sh = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) ptx::tmem_alloc(&tmem_sh, kAttTmemCols);
+  if (t < kHeads) m_ref[t] = -INFINITY;
+  // stage Q (K-major, 128B swizzle: [head/8][dim/64][head%8][128 B])
+  {
+    const uint4 *src = reinterpret_cast<const uint4 *>(A.q + (int64_t)qi * kHeads * kDim);
+    for (int i = t; i < kHeads * kDim / 8; i += kTcThreads) {
+      const int h = i >> 6, ch = i & 63;               // 16-B chunk ch of row h (8 dims)
+      const uint32_t off = (h >> 3) * 8192 + (ch >> 3) * 1024 + sw128(h & 7, ch & 7);
+      *reinterpret_cast<uint4 *>(sm + kSmQ + off) = __ldg(src + i);
+    }
+    // all-ones A operand: one 8 x 16-B core matrix of bf16 1.0, read for every
+    // row group and K chunk (both descriptor strides 0)
+    if (t < 8)
+      *reinterpret_cast<uint4 *>(sm + kSmOnes + t * 16) = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_sh;
+  const uint32_t sK = ptx::smem_u32(sm + kSmK), sQ = ptx::smem_u32(sm + kSmQ);
+  const uint32_t sPhi = ptx::smem_u32(sm + kSmPhi), sPlo = ptx::smem_u32(sm + kSmPlo);
+  const uint32_t sOnes = ptx::smem_u32(sm + kSmOnes);
+  const uint32_t id_qk = idesc_bf16_m128n64(0), id_pv = idesc_bf16_m128n64(1);
+  uint32_t phase = 0;
+  bool any_chunk = false;
+
+  for (int c = c0; c < c1; c++) {
+    // ---------------------------------------------------------- gather + dequantise
+    {
+      const int e = t >> 1, half = t & 1;             // entry slot e, dims [256*half, 256*half+256)
+      const int slot = c * kTcChunk + e;
+      const uint32_t rowbase = (e >> 3) * 8192;        // 8-entry group
+      int ok = 0;
+      if (slot < A.sel_stride) {
+        const int j = __ldg(A.sel + (int64_t)qi * A.sel_stride + slot);
+        if (j >= 0 && (int64_t)j < A.n_max) {
+          ok = 1;
+          const uint8_t *rec = A.kv + ((int64_t)seq * A.n_max + j) * kKvBytes;
+          const uint32_t sc4[4] = {__ldg(reinterpret_cast<const uint32_t *>(rec + 256 + half * 16)),
+                                   __ldg(reinterpret_cast<const uint32_t *>(rec + 256 + half * 16 + 4)),
+                                   __ldg(reinterpret_cast<const uint32_t *>(rec + 256 + half * 16 + 8)),
+                                   __ldg(reinterpret_cast<const uint32_t *>(rec + 256 + half * 16 + 12))};
+#pragma unroll
+          for (int v = 0; v < 8; v++) {               // 16-B nibble load = 32 dims
+            const uint4 nb = __ldg(reinterpret_cast<const uint4 *>(rec + half * 128 + v * 16));
+            const uint32_t nw[4] = {nb.x, nb.y, nb.z, nb.w};
+#pragma unroll
+            for (int u = 0; u < 4; u++) {             // 8 dims per word -> one 16-B smem chunk
+              const int d0 = half * 256 + v * 32 + u * 8;
+              const int g = (d0 >> 4) - half * 16;    // scale group within this half (0..15)
+              const float s = e4m3_to_float((sc4[g >> 2] >> (8 * (g & 3))) & 0xFFu) * 0.5f;
+              uint32_t pk[4];
+#pragma unroll
+              for (int b = 0; b < 4; b++) {
+                const float lo = (float)e2m1_x2((nw[u] >> (8 * b)) & 15u) * s;
+                const float hi = (float)e2m1_x2((nw[u] >> (8 * b + 4)) & 15u) * s;
+                pk[b] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+              }
+              const uint32_t off = rowbase + (d0 >> 6) * 1024 + sw128(e & 7, (d0 >> 3) & 7);
+              *reinterpret_cast<uint4 *>(sm + kSmK + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          }
+        } else if (j >= 0) {
+          record_error(A.status, CSA2_ERR_BOUNDS);
+        }
+      } else if (slot < n_slots) {
+        ok = 1;
+        const int ring = (swa_first + (slot - A.sel_stride)) % A.swa_cap;
+        const uint8_t *rec = A.swa + ((int64_t)seq * A.swa_cap + ring) * kSwaBytes;
+        const uint2 scw = __ldg(reinterpret_cast<const uint2 *>(rec + 512 + half * 8));
+        const uint32_t sc2[2] = {scw.x, scw.y};
+#pragma unroll
+        for (int v = 0; v < 16; v++) {                // 16 B = 16 dims per load
+          const uint4 b = __ldg(reinterpret_cast<const uint4 *>(rec + half * 256 + v * 16));
+          const int g = v >> 1;                       // E8M0 group (32 dims) within this half
+          const float s = e8m0_to_float((sc2[g >> 2] >> (8 * (g & 3))) & 0xFFu);
+          const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int hf = 0; hf < 2; hf++) {            // two 8-dim smem chunks
+            uint32_t pk[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+              const uint32_t word = bw[hf * 2 + (u >> 1)];
+              const uint32_t sh = 16 * (u & 1);
+              const float lo = e4m3_to_float((word >> sh) & 0xFFu) * s;
+              const float hi = e4m3_to_float((word >> (sh + 8)) & 0xFFu) * s;
+              pk[u] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+            }
+            const int d0 = half * 256 + v * 16 + hf * 8;
+            const uint32_t off = rowbase + (d0 >> 6) * 1024 + sw128(e & 7, (d0 >> 3) & 7);
+            *reinterpret_cast<uint4 *>(sm + kSmK + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+      }
+      if (!ok) {
+#pragma unroll 4
+        for (int ch = 0; ch < 32; ch++) {
+          const int d0 = half * 256 + ch * 8;
+          const uint32_t off = rowbase + (d0 >> 6) * 1024 + sw128(e & 7, (d0 >> 3) & 7);
+          *reinterpret_cast<uint4 *>(sm + kSmK + off) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (half == 0) valid_sh[e] = (uint8_t)ok;
+    }
+    ptx::fence_proxy_async_smem();
+    __syncthreads();
+    // ---------------------------------------------------------- S^T = Khat Q^T
+    if (t == 0) {
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int kk = 0; kk < kDim / 16; kk++) {
+        const uint32_t koff = (kk >> 2) * 1024 + (kk & 3) * 32;
+        const uint64_t ad = ptx::smem_desc(sK + koff, 16, 8192, 2);
+        const uint64_t bd = ptx::smem_desc(sQ + koff, 16, 8192, 2);
+        ptx::tc_mma_bf16(tmem + kColS, ad, bd, id_qk, kk > 0 ? 1u : 0u);
+      }
+      ptx::tc_commit(&bar_s);
+    }
+    // ---------------------------------------------------------- softmax (warps 0-3)
+    if (warp < 4) {
+      if (!ptx::mbar_wait(&bar_s, phase)) { record_error(A.status, CSA2_ERR_TIMEOUT); bad_sh = 1; }
+      ptx::tc_fence_after();
+      const int e = warp * 32 + lane;                  // TMEM lane = entry
+      const uint32_t s_addr = tmem + ((uint32_t)(warp * 32) << 16) + kColS;
+      const bool ev = valid_sh[e] != 0;
+      // per-head max over the warp's 32 entries: transpose-reduce, 62 shuffles;
+      // afterwards lane L holds the max of heads base(L) and base(L)+1 in v[0], v[1]
+      float v[64];
+      {
+        uint32_t r0[32], r1[32];
+        ptx::tmem_ld_32x32b_x32(s_addr, r0);
+        ptx::tmem_ld_32x32b_x32(s_addr + 32, r1);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 32; h++) {
+          v[h] = ev ? __uint_as_float(r0[h]) * A.scale_log2 : -INFINITY;
+          v[h + 32] = ev ? __uint_as_float(r1[h]) * A.scale_log2 : -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int w = 32; w >= 2; w >>= 1) {              // w = values kept after this step
+        const int o = w >> 1;                           // partner distance in lanes: 16, 8, 4, 2, 1
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < 64; i++) {
+          if (i < w) {
+            // keep the half of indices selected by this lane's bit; send the other half
+            const float mine = upper ? v[i + w] : v[i];
+            const float send = upper ? v[i] : v[i + w];
+            const float got = __shfl_xor_sync(0xFFFFFFFFu, send, o);
+            v[i] = fmaxf(mine, got);
+          }
+        }
+      }
+      // lane L now holds, for i in {0, 1}, the max over the warp of head
+      // index  h = (bits of L reversed into the halving order) -- computed below
+      {
+        // recover the head indices kept by this lane: at step with partner
+        // distance o (16..1) the upper lane kept the upper half of the w values
+        int base = 0, w = 64;
+        for (int o = 16; o >= 1; o >>= 1) {
+          w >>= 1;
+          if (lane & o) base += w;
+        }
+        red[warp][base] = v[0];
+        red[warp][base + 1] = v[1];
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (t < kHeads) {
+        const float cm = fmaxf(fmaxf(red[0][t], red[1][t]), fmaxf(red[2][t], red[3][t]));
+        const float mo = m_ref[t];
+        float al = 1.f;
+        if (cm != -INFINITY && (mo == -INFINITY || cm > mo + kRescaleLog2)) {
+          al = (mo == -INFINITY) ? 0.f : exp2f(mo - cm);
+          m_ref[t] = cm;
+        }
+        alpha_sh[t] = al;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (t == 0) {
+        int rs = 0;
+        for (int h = 0; h < kHeads; h++) rs |= (alpha_sh[h] != 1.f && alpha_sh[h] != 0.f) ? 1 : 0;
+        need_rescale = rs;
+      }
+      // numerators, bf16 hi + lo, into P[head][entry] (K-major, 128B swizzle);
+      // S is read from TMEM again rather than kept live through the reduction
+      const uint32_t pe = (e >> 6) * 1024;             // entry atom
+      const uint32_t pcol = (uint32_t)(e & 63) * 2;    // byte within the 128-B row
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(s_addr + hh * 32, r);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+          const int h = hh * 32 + i;
+          const float l2 = __uint_as_float(r[i]) * A.scale_log2;
+          const float p = ev ? exp2f(l2 - m_ref[h]) : 0.f;
+          const __nv_bfloat16 ph = __float2bfloat16_rn(p);
+          const __nv_bfloat16 pl = __float2bfloat16_rn(p - __bfloat162float(ph));
+          const uint32_t off = (h >> 3) * 2048 + pe + sw128(h & 7, pcol >> 4) + (pcol & 15);
+          *reinterpret_cast<__nv_bfloat16 *>(sm + kSmPhi + off) = ph;
+          *reinterpret_cast<__nv_bfloat16 *>(sm + kSmPlo + off) = pl;
+        }
+      }
+      ptx::tc_fence_before();
+    }
+    ptx::fence_proxy_async_smem();
+    __syncthreads();
+    // ---------------------------------------------------------- lazy rescale of O^T
+    if (need_rescale && any_chunk) {
+      ptx::tc_fence_after();
+      // warp w: lane quarter w%4, blocks {w/4, w/4 + 2} (+ block 4 for warps 0-3)
+      const int quarter = warp & 3;
+      for (int blk = warp >> 2; blk < 5; blk += 2) {
+        if (blk == 4 && warp >= 4) break;
+        for (int half = 0; half < 2; half++) {
+          uint32_t r[32];
+          const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + kColO + blk * 64 + half * 32;
+          ptx::tmem_ld_32x32b_x32(ta, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i++) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha_sh[half * 32 + i]);
+          ptx::tmem_st_32x32b_x32(ta, r);
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncthreads();
+    }
+    // ---------------------------------------------------------- O^T += Vhat^T P^T
+    if (t == 0) {
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int ks = 0; ks < kTcChunk / 16; ks++) {
+        const uint32_t poff = (ks >> 2) * 1024 + (ks & 3) * 32;
+        const uint64_t bhi = ptx::smem_desc(sPhi + poff, 16, 2048, 2);
+        const uint64_t blo = ptx::smem_desc(sPlo + poff, 16, 2048, 2);
+        const uint32_t acc0 = (any_chunk || ks > 0) ? 1u : 0u;
+#pragma unroll 1
+        for (int mb = 0; mb < 4; mb++) {
+          // Vhat^T block: dims [128 mb, 128 mb + 128), entries [16 ks, 16 ks + 16), MN-major
+          const uint64_t ad = ptx::smem_desc(sK + (2 * ks) * 8192 + (2 * mb) * 1024, 1024, 8192, 2);
+          ptx::tc_mma_bf16(tmem + kColO + mb * 64, ad, bhi, id_pv, acc0);
+          ptx::tc_mma_bf16(tmem + kColO + mb * 64, ad, blo, id_pv, 1u);
+        }
+        const uint64_t ones = ptx::smem_desc(sOnes, 0, 0, 0);
+        ptx::tc_mma_bf16(tmem + kColO + 4 * 64, ones, bhi, id_qk, acc0);
+        ptx::tc_mma_bf16(tmem + kColO + 4 * 64, ones, blo, id_qk, 1u);
+      }
+      ptx::tc_commit(&bar_o);
+    }
+    if (!ptx::mbar_wait(&bar_o, phase)) { record_error(A.status, CSA2_ERR_TIMEOUT); bad_sh = 1; }
+    ptx::tc_fence_after();
+    phase ^= 1;
+    any_chunk = true;
+    __syncthreads();
+    if (bad_sh) break;
+  }
+
+  // ---------------------------------------------------------- read-out
+  {
+    const int quarter = warp & 3;
+    const int pos = __ldg(A.pos + qi);
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    for (int blk = warp >> 2; blk < 4; blk += 2) {
+      const int d = blk * 128 + quarter * 32 + lane;   // TMEM lane = dim within block
+      float rc = 1.f, rs = 0.f;                        // rotation by -pos of the pair holding d
+      if (d >= kRopeOff && A.nsplit == 1) {
+        float a = 1.f, b = 0.f;                        // unit vector e_a through the rotation
+        unrotate_pair_tc(a, b, (d - kRopeOff) >> 1, pos, A.rope_base);
+        rc = a;                                        // cos t
+        rs = b;                                        // -sin t
+      }
+#pragma unroll
+      for (int half = 0; half < 2; half++) {
+        uint32_t r[32], lr[32];
+        if (any_chunk) {
+          ptx::tmem_ld_32x32b_x32(lane_base + kColO + blk * 64 + half * 32, r);
+          ptx::tmem_ld_32x32b_x32(lane_base + kColO + 4 * 64 + half * 32, lr);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i++) r[i] = lr[i] = 0u;
+        }
+        if (A.nsplit == 1) {
+#pragma unroll
+          for (int i = 0; i < 32; i++) {
+            const int h = half * 32 + i;
+            const float l = __uint_as_float(lr[i]);
+            float x = l > 0.f ? __uint_as_float(r[i]) / l : 0.f;
+            if (d >= kRopeOff) {
+              // partner dim d^1 lives in the neighbouring lane; with c = cos t,
+              // s = sin t (rc = c, rs = -s):  a' = a c + b s,  b' = -a s + b c
+              const float y = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+              x = (d & 1) ? (x * rc + y * rs) : (x * rc - y * rs);
+            }
+            const int64_t off = ((int64_t)qi * kHeads + h) * kDim + d;
+            if (A.out_f32) static_cast<float *>(A.out)[off] = x;
+            else reinterpret_cast<__nv_bfloat16 *>(A.out)[off] = __float2bfloat16_rn(x);
+          }
+        } else {
+          float *P = A.part + ((int64_t)qi * A.nsplit + split) * kHeads * kDim;
+#pragma unroll
+          for (int i = 0; i < 32; i++) P[(half * 32 + i) * kDim + d] = __uint_as_float(r[i]);
+          if (blk == (warp >> 2) && quarter == 0 && lane == 0 && warp < 4) {
+            float *ml = A.part_ml + ((int64_t)qi * A.nsplit + split) * 2 * kHeads;
+#pragma unroll
+            for (int i = 0; i < 32; i++) ml[kHeads + half * 32 + i] = __uint_as_float(lr[i]);
+          }
+        }
+      }
+    }
+    if (A.nsplit > 1 && t < kHeads) {
+      // (the denominators, replicated over all 128 lanes, were written by lane 0 of warp 0)
+      float *ml = A.part_ml + ((int64_t)qi * A.nsplit + split) * 2 * kHeads;
+      ml[t] = any_chunk ? m_ref[t] : -INFINITY;
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kAttTmemCols);
+  }
+}
+
+// Combine the split partials of one (query, head) row: 256 threads, one dim pair each.
+__global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnTcArgs A) {
+  const int qi = blockIdx.y, h = blockIdx.x, t = threadIdx.x;
+  const float *ml = A.part_ml + (int64_t)qi * A.nsplit * 2 * kHeads;
+  float M = -INFINITY;
+  for (int s = 0; s < A.nsplit; s++) M = fmaxf(M, ml[s * 2 * kHeads + h]);
+  float L = 0.f, x = 0.f, y = 0.f;
+  const int d = 2 * t;
+  if (M != -INFINITY) {
+    for (int s = 0; s < A.nsplit; s++) {
+      const float m = ml[s * 2 * kHeads + h];
+      if (m == -INFINITY) continue;
+      const float wgt = exp2f(m - M);
+      L += wgt * ml[s * 2 * kHeads + kHeads + h];
+      const float2 v =
+          *reinterpret_cast<const float2 *>(A.part + (((int64_t)qi * A.nsplit + s) * kHeads + h) * kDim + d);
+      x += wgt * v.x;
+      y += wgt * v.y;
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  x *= inv;
+  y *= inv;
+  if (d >= kRopeOff) unrotate_pair_tc(x, y, (d - kRopeOff) >> 1, __ldg(A.pos + qi), A.rope_base);
+  const int64_t off = ((int64_t)qi * kHeads + h) * kDim + d;
+  if (A.out_f32)
+    *reinterpret_cast<float2 *>(static_cast<float *>(A.out) + off) = make_float2(x, y);
+  else
+    *reinterpret_cast<__nv_bfloat162 *>(static_cast<uint16_t *>(A.out) + off) = __floats2bfloat162_rn(x, y);
+}
+
+static int attn_chunks(int sel_stride) { return (sel_stride + kSwa + kTcChunk - 1) / kTcChunk; }
+
+// Split the chunks of a query over CTAs when the batch alone cannot fill the GPU.
+int attn_nsplit(int n_q, int sel_stride) {
+  const int chunks = attn_chunks(sel_stride);
+  const int ns = (2 * 152 + n_q - 1) / n_q;
+  return ns < 1 ? 1 : (ns > chunks ? chunks : ns);
+}
+
+size_t attn_workspace_bytes(int n_q, int sel_stride) {
+  const int ns = attn_nsplit(n_q, sel_stride);
+  if (ns == 1) return 0;
+  return (size_t)n_q * ns * (kHeads * kDim + 2 * kHeads) * sizeof(float);
+}
+
+cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_seq, const int32_t *sel, int sel_stride,
+                           const void *swa, int swa_cap, const int32_t *q_seq, const int32_t *pos,
+                           const int32_t *swa_first, const int32_t *swa_cnt, int n_q, void *out, int out_dtype,
+                           float sm_scale, double rope_base, void *ws, int *status, cudaStream_t st) {
+  AttnTcArgs A;
+  A.q = static_cast<const uint16_t *>(q);
+  A.kv = static_cast<const uint8_t *>(kv);
+  A.n_max = n_max;
+  A.n_seq = n_seq;
+  A.sel = sel;
+  A.sel_stride = sel_stride;
+  A.swa = static_cast<const uint8_t *>(swa);
+  A.swa_cap = swa_cap;
+  A.q_seq = q_seq;
+  A.pos = pos;
+  A.swa_first = swa_first;
+  A.swa_cnt = swa_cnt;
+  A.out = out;
+  A.out_f32 = out_dtype == CSA2_OUT_F32;
+  A.scale_log2 = sm_scale * 1.4426950408889634f;
+  A.rope_base = rope_base;
+  const int chunks = attn_chunks(sel_stride);
+  A.nsplit = attn_nsplit(n_q, sel_stride);
+  A.chunks_per_split = (chunks + A.nsplit - 1) / A.nsplit;
+  A.nsplit = (chunks + A.chunks_per_split - 1) / A.chunks_per_split;
+  A.part = static_cast<float *>(ws);
+  A.part_ml = A.part + (size_t)n_q * A.nsplit * kHeads * kDim;
+  A.status = status;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_done[64] = {};
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  attn_tc_kernel<<<dim3(A.nsplit, n_q), kTcThreads, kSmAlloc, st>>>(A);
+  if (A.nsplit > 1) attn_tc_merge_kernel<<<dim3(kHeads, n_q), 256, 0, st>>>(A);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

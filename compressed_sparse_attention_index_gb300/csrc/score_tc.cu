@@ -12,7 +12,7 @@
 //
 // The kernel is HBM-bound (68 B of key per entry, 8 FLOP/B of FP4 MMA): a
 // persistent CTA per SM streams tiles through a 12-stage shared-memory ring.
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      producer: TMA of the 128 x 64 B nibble tile (or 16 gathered
 //               8-entry blocks in pool mode), TMA of the query's 32 x 64 B, bulk
 //               copies of the key and query E8M0 scales;
@@ -20,9 +20,11 @@
 //               into the 32-lane x 16-B layout tcgen05.cp expects, copies them
 //               into TMEM, issues the two MMAs, commits to the stage's "empty"
 //               barrier and to the accumulator's "full" barrier;
-//   warps 2..5  epilogue: one TMEM lane (= one entry) per thread, 32 columns
-//               (= heads) per tcgen05.ld, ReLU + weighted sum, coalesced store.
-// Two TMEM accumulators let the epilogue of tile i overlap the MMA of tile i+1.
+//   warps 2..9  epilogue, two groups of four warps taking alternate tiles: one
+//               TMEM lane (= one entry) per thread, 32 columns (= heads) per
+//               tcgen05.ld, ReLU + weighted sum, coalesced store.
+// Four TMEM accumulators let the epilogue of earlier tiles overlap the MMAs of
+// later ones.
 // Every mbarrier wait is bounded (CSA2_ERR_TIMEOUT instead of a hang).
 #include <cuda.h>
 
@@ -37,9 +39,10 @@ constexpr int kOffA = 0;          // 128 rows x 64 B, 64B-swizzled (TMA writes i
 constexpr int kOffB = 8192;       // 32 rows x 64 B query nibbles, 64B-swizzled
 constexpr int kOffSFA = 10240;    // 512 B key scales: staged [row][4], rearranged in place
 constexpr int kOffSFB = 10752;    // 512 B query scales: staged [head][4] in the first 128 B
-constexpr int kScThreads = 192;
-constexpr uint32_t kScTmemCols = 128;   // 2 x 32 accumulator columns + 2 x 4 SFA + 2 x 4 SFB
-constexpr uint32_t kColSFA = 64, kColSFB = 72;
+constexpr int kScThreads = 320;
+constexpr int kScAcc = 4;               // TMEM accumulator stages
+constexpr uint32_t kScTmemCols = 256;   // 4 x 32 accumulator columns + 4 x 4 SFA + 4 x 4 SFB
+constexpr uint32_t kColSFA = 128, kColSFB = 144;
 
 // Instruction descriptor of kind::mxf4 block-scaled MMA, M=128, N=32, both
 // operands E2M1 and K-major, UE8M0 scales; sf_id picks the scale byte pair.
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
   extern __shared__ __align__(1024) unsigned char sc_smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(sc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t full_bar[kScStages], empty_bar[kScStages], acc_full[2], acc_empty[2];
+  __shared__ __align__(8) uint64_t full_bar[kScStages], empty_bar[kScStages], acc_full[kScAcc], acc_empty[kScAcc];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
       ptx::mbar_init(&full_bar[s], 1);
       ptx::mbar_init(&empty_bar[s], 1);
     }
-    for (int a = 0; a < 2; a++) {
+    for (int a = 0; a < kScAcc; a++) {
       ptx::mbar_init(&acc_full[a], 1);
       ptx::mbar_init(&acc_empty[a], 4);
     }
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
     const uint32_t idesc0 = idesc_mxf4_m128n32(0), idesc1 = idesc_mxf4_m128n32(2);
     for (uint32_t it = 0; next_tile(P, T, t); it++) {
       if (abort_flag) break;
-      const uint32_t s = it % kScStages, r = it / kScStages, a = it & 1, ra = it >> 1;
+      const uint32_t s = it % kScStages, r = it / kScStages, a = it % kScAcc, ra = it / kScAcc;
       if (!ptx::mbar_wait(&full_bar[s], r & 1)) { fail(); break; }
       unsigned char *st = smem + s * kScStageBytes;
       // scales -> tcgen05.cp layout: 16-B line m0 holds rows m0, m0+32, m0+64, m0+96
@@ -224,6 +227,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
+    const uint32_t group = (uint32_t)(warp - 2) >> 2;     // warps 2..5 -> 0, 6..9 -> 1
     const int row = quarter * 32 + lane;
     int64_t T = blockIdx.x;
     TileInfo t;
@@ -231,7 +235,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
     float wv[kIdxHeads];
     for (uint32_t it = 0; next_tile(P, T, t); it++) {
       if (abort_flag) break;
-      const uint32_t a = it & 1, ra = it >> 1;
+      if ((it & 1) != group) continue;
+      const uint32_t a = it % kScAcc, ra = it / kScAcc;
       if (t.q != cur_q) {
         const float4 *wp = reinterpret_cast<const float4 *>(P.w + (int64_t)t.q * kIdxHeads);
 #pragma unroll
@@ -275,14 +280,35 @@ __global__ void __launch_bounds__(kScThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
+// The driver's tensor-map encoder, fetched through the runtime so that the
+// library does not link libcuda directly (it still loads on a machine without
+// a driver, e.g. to read its exports).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tensor_map_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
 static bool encode_rows64(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
   cuuint64_t dims[2] = {64, rows};
   cuuint64_t strides[1] = {64};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = cuTensorMapEncodeTiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
-                                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

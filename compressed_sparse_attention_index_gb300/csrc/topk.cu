@@ -9,18 +9,21 @@
 // these keys needs no separate tie pass.
 //
 // Rows of up to kDirectCap items are selected by one CTA from shared memory.
-// Longer rows (1M-entry Full-layer rows, 131,072-block pool rows) first go
-// through a multi-CTA filter: a 4,096-bin histogram of the top 12 key bits finds
-// the bin that holds the k-th key, and only items in that bin or above are kept
-// as candidates (usually a few thousand).  A row whose candidates overflow the
-// buffer falls back to an exact radix select straight over the score row.
+// Longer rows (1M-entry Full-layer rows, 131,072-block pool rows) take two
+// launches: a bandwidth pass writes the maximum key of every group of 128 items;
+// then one CTA per row finds T, the k-th largest group maximum (a lower bound of
+// the k-th best key), rescans only the groups whose maximum reaches T, and runs
+// the exact selection on those candidates (usually about 2k items).  A row whose
+// candidates overflow the buffer falls back to an exact radix select straight
+// over the score row.
 #include "common.cuh"
 
 namespace csa2 {
 
 constexpr int kDirectCap = 16384;   // items held in shared memory by one CTA
-constexpr int kCandCap = 16384;     // candidate buffer per query (filter path)
-constexpr int kHistBins = 4096;     // top 12 bits of the 32-bit score key
+constexpr int kMaxGroup = 128;      // largest group of items per group maximum (long rows)
+constexpr int kMaxGroups = 8192;    // groups a long row may have
+constexpr int kCandCap = 8192;      // candidates kept in shared memory (long rows)
 constexpr int kMaxK = 2048;
 constexpr int kTopkThreads = 1024;
 
@@ -204,119 +207,138 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
   select_and_write(get, n, n, k, out + (int64_t)q * k, sh, sel);
 }
 
-// ---------------------------------------------------------------- filter path
-__global__ void __launch_bounds__(kTopkThreads) topk_hist_kernel(TopkSrc S, int slices, uint32_t *__restrict__ ghist,
-                                                                  int *status) {
-  __shared__ uint32_t h[kHistBins];
+// ---------------------------------------------------------------- long rows
+// Group maxima: the max key over each group of G consecutive items (0 if the
+// group holds no valid item), G a power of two in [8, 128].  A warp covers
+// 32 * ipl items (ipl = max(1, G/32) per lane) and reduces within groups.
+__global__ void __launch_bounds__(256) topk_groupmax_kernel(TopkSrc S, int G, int n_groups,
+                                                             uint32_t *__restrict__ gmax, int *status) {
   const int q = blockIdx.y;
   const int nv = query_nv(S, q, status);
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = 0;
-  __syncthreads();
-  const int64_t per = (S.n_items + slices - 1) / slices;
-  const int64_t i0 = (int64_t)blockIdx.x * per, i1 = min(S.n_items, i0 + per);
-  for (int64_t i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
-    uint64_t key;
-    if (item_key(S, q, i, nv, key, status)) atomicAdd(&h[(uint32_t)(key >> 52)], 1u);
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  const int ipl = G >= 32 ? G / 32 : 1;          // items per lane
+  const int lpg = G >= 32 ? 32 : G;              // lanes per group
+  const int64_t span = 32 * ipl;                 // items per warp step
+  const int64_t n_steps = ((int64_t)n_groups * G + span - 1) / span;
+  for (int64_t w = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); w < n_steps; w += (int64_t)gridDim.x * warps) {
+    uint32_t m = 0;
+    const int64_t i0 = w * span + (int64_t)lane * ipl;
+    if (ipl == 4 && S.block == 1 && S.pool == nullptr && i0 + 4 <= nv) {
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(S.scores + (int64_t)q * S.stride + i0));
+      m = max(max(order_key(v.x), order_key(v.y)), max(order_key(v.z), order_key(v.w)));
+    } else {
+      for (int u = 0; u < ipl; u++) {
+        uint64_t key;
+        if (i0 + u < S.n_items && item_key(S, q, i0 + u, nv, key, status)) m = max(m, (uint32_t)(key >> 32));
+      }
+    }
+    for (int o = lpg >> 1; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const int64_t g = i0 / G;
+    if ((lane & (lpg - 1)) == 0 && g < n_groups) gmax[(int64_t)q * n_groups + g] = m;
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
-    if (h[i]) atomicAdd(ghist + (int64_t)q * kHistBins + i, h[i]);
 }
 
-// Lowest bin b* such that the bins >= b* hold at least k items (0 if fewer).
-__device__ int find_bin(const uint32_t *__restrict__ hist, int k, int *sh_scan) {
-  // each thread owns 4 consecutive bins; block-wide suffix sums
-  const int t = threadIdx.x;
-  uint32_t c[4];
-  uint32_t part = 0;
-#pragma unroll
-  for (int b = 0; b < 4; b++) { c[b] = __ldg(hist + 4 * t + b); part += c[b]; }
-  sh_scan[t] = (int)part;
+// One CTA per query.  T = the k-th largest group maximum: at least k groups
+// reach T, so at least k items do, so the k-th best item key is >= T and every
+// item of the top-k lies in a group whose maximum is >= T.  Those groups are
+// scanned for items with key >= T (a superset of the top-k, usually ~2k items),
+// and the exact selection runs on that candidate set.
+__global__ void __launch_bounds__(kTopkThreads) topk_group_select_kernel(TopkSrc S, int G, int n_groups, int k,
+                                                                          const uint32_t *__restrict__ gmax,
+                                                                          int32_t *__restrict__ out, int *status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  uint64_t *gk = reinterpret_cast<uint64_t *>(smem_raw);                 // [kMaxGroups]
+  uint64_t *cand = gk + kMaxGroups;                                      // [kCandCap]
+  int32_t *sel = reinterpret_cast<int32_t *>(cand + kCandCap);           // [kMaxK]
+  __shared__ SelectShared sh;
+  __shared__ int n_cand, n_valid_groups;
+  __shared__ uint32_t thr_sh;
+  const int q = blockIdx.x;
+  const int nv = query_nv(S, q, status);
+  const uint32_t *gm = gmax + (int64_t)q * n_groups;
+  if (threadIdx.x == 0) { n_cand = 0; n_valid_groups = 0; }
   __syncthreads();
-  for (int o = 1; o < kTopkThreads; o <<= 1) {   // inclusive suffix scan (Hillis-Steele)
-    const int v = (t + o < kTopkThreads) ? sh_scan[t + o] : 0;
-    __syncthreads();
-    sh_scan[t] += v;
-    __syncthreads();
+  int live_groups = 0;
+  for (int g = threadIdx.x; g < n_groups; g += blockDim.x) {
+    const uint32_t m = gm[g];
+    gk[g] = ((uint64_t)m << 32) | (uint32_t)(~(uint32_t)g);
+    live_groups += m != 0;
   }
-  __shared__ int bin;
-  if (t == 0) bin = 0;
+  atomicAdd(&n_valid_groups, live_groups);
   __syncthreads();
-  const int incl = sh_scan[t];
-  const int above = incl - (int)part;
-  if (above < k && k <= incl) {
-    int run = above;
-    for (int b = 3; b >= 0; b--) {
-      run += (int)c[b];
-      if (run >= k) { bin = 4 * t + b; break; }
+  uint32_t T = 0;
+  if (n_valid_groups > k) {
+    auto get = [&](int64_t i, uint64_t &key) { key = gk[i]; return (key >> 32) != 0; };
+    T = (uint32_t)(radix_threshold(get, n_groups, k, sh) >> 32);
+  }
+  if (threadIdx.x == 0) thr_sh = T;
+  __syncthreads();
+  T = thr_sh;
+  // scan the groups whose maximum reaches T; one warp per group
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int g = warp; g < n_groups; g += blockDim.x >> 5) {
+    const uint32_t m = gm[g];
+    if (m == 0 || m < T) continue;
+    for (int u = 0; u < G; u += 32) {
+      const int64_t i = (int64_t)g * G + u + lane;
+      uint64_t key = 0;
+      const bool v = u + lane < G && i < S.n_items && item_key(S, q, i, nv, key, status) &&
+                     (uint32_t)(key >> 32) >= T;
+      const unsigned b = __ballot_sync(0xFFFFFFFFu, v);
+      int base = 0;
+      if (lane == 0 && b) base = atomicAdd(&n_cand, __popc(b));
+      base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(b & ((1u << lane) - 1u));
+      if (v && base < kCandCap) cand[base] = key;
     }
   }
   __syncthreads();
-  return bin;
-}
-
-__global__ void __launch_bounds__(kTopkThreads) topk_filter_kernel(TopkSrc S, int slices, int k,
-                                                                    const uint32_t *__restrict__ ghist,
-                                                                    uint32_t *__restrict__ gcount,
-                                                                    uint64_t *__restrict__ cand, int *status) {
-  __shared__ int scan[kTopkThreads];
-  const int q = blockIdx.y;
-  const int nv = query_nv(S, q, status);
-  const int bstar = find_bin(ghist + (int64_t)q * kHistBins, k, scan);
-  const int64_t per = (S.n_items + slices - 1) / slices;
-  const int64_t i0 = (int64_t)blockIdx.x * per, i1 = min(S.n_items, i0 + per);
-  const int lane = threadIdx.x & 31;
-  for (int64_t base = i0; base < i1; base += blockDim.x) {
-    const int64_t i = base + threadIdx.x;
-    uint64_t key = 0;
-    const bool v = i < i1 && item_key(S, q, i, nv, key, status) && (int)(key >> 52) >= bstar;
-    const unsigned ballot = __ballot_sync(0xFFFFFFFFu, v);
-    uint32_t pos = 0;
-    if (lane == 0 && ballot) pos = atomicAdd(gcount + q, (uint32_t)__popc(ballot));
-    pos = __shfl_sync(0xFFFFFFFFu, pos, 0) + __popc(ballot & ((1u << lane) - 1u));
-    if (v && pos < (uint32_t)kCandCap) cand[(int64_t)q * kCandCap + pos] = key;
-  }
-}
-
-__global__ void __launch_bounds__(kTopkThreads) topk_final_kernel(TopkSrc S, int k, const uint32_t *__restrict__ gcount,
-                                                                   const uint64_t *__restrict__ cand,
-                                                                   const uint32_t *__restrict__ ghist,
-                                                                   int32_t *__restrict__ out, int *status) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint64_t *keys = reinterpret_cast<uint64_t *>(smem_raw);
-  int32_t *sel = reinterpret_cast<int32_t *>(keys + kCandCap);
-  __shared__ SelectShared sh;
-  const int q = blockIdx.x;
-  const uint32_t cnt = gcount[q];
-  // number of valid items = histogram total
-  __shared__ int total;
-  if (threadIdx.x == 0) total = 0;
-  __syncthreads();
-  int part = 0;
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) part += (int)ghist[(int64_t)q * kHistBins + i];
-  atomicAdd(&total, part);
-  __syncthreads();
-  const int n_valid_items = total;
-  if (cnt <= (uint32_t)kCandCap) {
-    for (uint32_t i = threadIdx.x; i < cnt; i += blockDim.x) keys[i] = cand[(int64_t)q * kCandCap + i];
-    __syncthreads();
-    auto get = [&](int64_t i, uint64_t &key) { key = keys[i]; return true; };
-    // candidates hold every item at or above the k-th key's bin, so the top-k of
-    // the candidates is the top-k of the row
-    select_and_write(get, (int64_t)cnt, min((int)cnt, n_valid_items), k, out + (int64_t)q * k, sh, sel);
+  const int nc = n_cand;
+  if (nc <= kCandCap) {
+    auto get = [&](int64_t i, uint64_t &key) { key = cand[i]; return true; };
+    select_and_write(get, nc, nc, k, out + (int64_t)q * k, sh, sel);
   } else {
-    const int nv = query_nv(S, q, status);
+    // too many ties at T for the buffer: exact selection straight over the row
+    __shared__ int nvi;
+    if (threadIdx.x == 0) nvi = 0;
+    __syncthreads();
+    int c = 0;
+    for (int64_t i = threadIdx.x; i < S.n_items; i += blockDim.x) {
+      uint64_t key;
+      c += item_key(S, q, i, nv, key, status) ? 1 : 0;
+    }
+    atomicAdd(&nvi, c);
+    __syncthreads();
     auto get = [&](int64_t i, uint64_t &key) { return item_key(S, q, i, nv, key, status); };
-    select_and_write(get, S.n_items, n_valid_items, k, out + (int64_t)q * k, sh, sel);
+    select_and_write(get, S.n_items, nvi, k, out + (int64_t)q * k, sh, sel);
   }
 }
 
 // ---------------------------------------------------------------- host side
-size_t topk_workspace_bytes(int n_q, int64_t n_items) {
+static int64_t topk_items(int64_t n_max, int block, bool pool) {
+  return pool ? (int64_t)kPoolSlots : (block == 1 ? n_max : (n_max + kBlock - 1) / kBlock);
+}
+
+// Group size for long rows: the smallest power of two >= 8 that keeps the
+// groups within kMaxGroups, doubled while at least 4k groups remain.
+static int topk_group(int64_t n_items, int k) {
+  int G = 8;
+  while (G <= kMaxGroup && ((n_items + G - 1) / G > kMaxGroups || n_items / (2 * G) >= 4 * (int64_t)k) &&
+         !(G == kMaxGroup && (n_items + G - 1) / G <= kMaxGroups))
+    G <<= 1;
+  return G;
+}
+
+size_t topk_workspace_bytes(int n_q, int64_t n_items, int k) {
   if (n_items <= kDirectCap) return 0;
-  size_t b = (size_t)n_q * kHistBins * 4 + (size_t)n_q * 4;
-  b = (b + 255) & ~(size_t)255;
-  return b + (size_t)n_q * kCandCap * 8;
+  const int G = topk_group(n_items, k);
+  return (size_t)n_q * ((n_items + G - 1) / G) * 4;
+}
+
+bool topk_items_supported(int64_t n_items, int k) {
+  if (n_items <= kDirectCap) return true;
+  const int G = topk_group(n_items, k);
+  return G <= kMaxGroup && (n_items + G - 1) / G <= kMaxGroups;
 }
 
 cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max, int k,
@@ -328,31 +350,30 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
   S.pool = pool;
   S.block = block;
   S.n_max = n_max;
-  S.n_items = pool ? (int64_t)kPoolSlots : (block == 1 ? n_max : (n_max + kBlock - 1) / kBlock);
-  const size_t dsm = (size_t)kDirectCap * 8 + (size_t)kMaxK * 4;
+  S.n_items = topk_items(n_max, block, pool != nullptr);
+  const size_t dsm_direct = (size_t)kDirectCap * 8 + (size_t)kMaxK * 4;
+  const size_t dsm_group = (size_t)(kMaxGroups + kCandCap) * 8 + (size_t)kMaxK * 4;
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_done[64] = {};
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaFuncSetAttribute(topk_direct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm);
-    cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm);
+    cudaFuncSetAttribute(topk_direct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm_direct);
+    cudaFuncSetAttribute(topk_group_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm_group);
     attr_done[dev] = true;
   }
   if (S.n_items <= kDirectCap) {
-    topk_direct_kernel<<<n_q, kTopkThreads, dsm, st>>>(S, k, out, status);
+    topk_direct_kernel<<<n_q, kTopkThreads, dsm_direct, st>>>(S, k, out, status);
     return cudaGetLastError();
   }
-  uint32_t *ghist = static_cast<uint32_t *>(ws);
-  uint32_t *gcount = ghist + (size_t)n_q * kHistBins;
-  size_t off = ((size_t)n_q * kHistBins * 4 + (size_t)n_q * 4 + 255) & ~(size_t)255;
-  uint64_t *cand = reinterpret_cast<uint64_t *>(static_cast<char *>(ws) + off);
-  cudaError_t e = cudaMemsetAsync(ghist, 0, (size_t)n_q * kHistBins * 4 + (size_t)n_q * 4, st);
-  if (e != cudaSuccess) return e;
-  int slices = (int)max((int64_t)1, min((S.n_items + 4095) / 4096, (int64_t)((2 * 152 + n_q - 1) / n_q)));
-  dim3 grid(slices, n_q);
-  topk_hist_kernel<<<grid, kTopkThreads, 0, st>>>(S, slices, ghist, status);
-  topk_filter_kernel<<<grid, kTopkThreads, 0, st>>>(S, slices, k, ghist, gcount, cand, status);
-  topk_final_kernel<<<n_q, kTopkThreads, dsm, st>>>(S, k, gcount, cand, ghist, out, status);
+  const int G = topk_group(S.n_items, k);
+  const int n_groups = (int)((S.n_items + G - 1) / G);
+  uint32_t *gmax = static_cast<uint32_t *>(ws);
+  const int64_t warp_steps = ((int64_t)n_groups * G + 32 * (G >= 32 ? G / 32 : 1) - 1) / (32 * (G >= 32 ? G / 32 : 1));
+  int64_t gx = (warp_steps + 7) / 8;
+  const int64_t cap = (4 * 152 + n_q - 1) / n_q;
+  if (gx > cap) gx = cap;
+  topk_groupmax_kernel<<<dim3((unsigned)gx, n_q), 256, 0, st>>>(S, G, n_groups, gmax, status);
+  topk_group_select_kernel<<<n_q, kTopkThreads, dsm_group, st>>>(S, G, n_groups, k, gmax, out, status);
   return cudaGetLastError();
 }
 
