@@ -122,7 +122,7 @@ csa2_status csa2_index_score(const void *key_nib, const void *key_scale, int64_t
   if (n_q == 0) return CSA2_OK;
   if (!key_nib || !key_scale || !q_nib || !q_scale || !w || !q_seq || !n_vis || !scores)
     return CSA2_ERR_INVALID_ARG;
-  if (!aligned(key_nib, 16) || !aligned(key_scale, 16) || !aligned(q_nib, 16) || !aligned(q_scale, 16) ||
+  if (!aligned(key_nib, 512) || !aligned(key_scale, 16) || !aligned(q_nib, 512) || !aligned(q_scale, 16) ||
       !aligned(w, 16) || !aligned(scores, 4))
     return CSA2_ERR_INVALID_ARG;
   int *st = status_ptr();

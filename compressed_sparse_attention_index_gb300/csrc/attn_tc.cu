@@ -29,6 +29,7 @@
 // run the softmax on S^T rows; thread 0 issues the MMAs; all 8 warps share the
 // final read-out of the 5 x 64 accumulator columns.
 #include <cuda_bf16.h>
+#include <math.h>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -80,21 +81,22 @@ struct AttnTcArgs {
   void *out;
   int out_f32;
   float scale_log2;
-  double rope_base;
+  double inv_freq[kRopeDim / 2];   // rope_base^(-2i/64)
   int nsplit, chunks_per_split;
   float *part;      // [n_q][nsplit][64][512]
   float *part_ml;   // [n_q][nsplit][2][64]
   int *status;
 };
 
-__device__ __forceinline__ void unrotate_pair_tc(float &a, float &b, int pair, int pos, double base) {
-  const double th = (double)pos * pow(base, -2.0 * (double)pair / (double)kRopeDim);
-  double sn, cs;
-  sincos(th, &sn, &cs);
-  const float c = (float)cs, s = (float)sn;
-  const float x = a, y = b;
-  a = x * c + y * s;
-  b = -x * s + y * c;
+// cos and sin of theta = pos * inv_freq (inv_freq = rope_base^(-2i/64), computed
+// on the host in fp64): the product and its reduction modulo 2 pi are done in
+// fp64 (pos reaches 2^20, so theta reaches ~1e6 rad), the sine and cosine of the
+// reduced angle in fp32.
+__device__ __forceinline__ void rope_cs(double inv_freq, int pos, float &c, float &s) {
+  const double th = (double)pos * inv_freq;
+  const double k = rint(th * 0.15915494309189535);            // 1 / (2 pi)
+  const double r = fma(-k, 6.283185307179586, th);
+  sincosf((float)r, &s, &c);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
@@ -133,10 +135,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   // stage Q (K-major, 128B swizzle: [head/8][dim/64][head%8][128 B])
   {
     const uint4 *src = reinterpret_cast<const uint4 *>(A.q + (int64_t)qi * kHeads * kDim);
-    for (int i = t; i < kHeads * kDim / 8; i += kTcThreads) {
+    uint4 qv[kHeads * kDim / 8 / kTcThreads];        // all 16 loads in flight before any store
+#pragma unroll
+    for (int j = 0; j < kHeads * kDim / 8 / kTcThreads; j++) qv[j] = __ldg(src + t + j * kTcThreads);
+#pragma unroll
+    for (int j = 0; j < kHeads * kDim / 8 / kTcThreads; j++) {
+      const int i = t + j * kTcThreads;
       const int h = i >> 6, ch = i & 63;               // 16-B chunk ch of row h (8 dims)
       const uint32_t off = (h >> 3) * 8192 + (ch >> 3) * 1024 + sw128(h & 7, ch & 7);
-      *reinterpret_cast<uint4 *>(sm + kSmQ + off) = __ldg(src + i);
+      *reinterpret_cast<uint4 *>(sm + kSmQ + off) = qv[j];
     }
     // all-ones A operand: one 8 x 16-B core matrix of bf16 1.0, read for every
     // row group and K chunk (both descriptor strides 0)
@@ -171,9 +178,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
                                    __ldg(reinterpret_cast<const uint32_t *>(rec + 256 + half * 16 + 4)),
                                    __ldg(reinterpret_cast<const uint32_t *>(rec + 256 + half * 16 + 8)),
                                    __ldg(reinterpret_cast<const uint32_t *>(rec + 256 + half * 16 + 12))};
+          uint4 nbv[8];
+#pragma unroll
+          for (int v = 0; v < 8; v++) nbv[v] = __ldg(reinterpret_cast<const uint4 *>(rec + half * 128 + v * 16));
 #pragma unroll
           for (int v = 0; v < 8; v++) {               // 16-B nibble load = 32 dims
-            const uint4 nb = __ldg(reinterpret_cast<const uint4 *>(rec + half * 128 + v * 16));
+            const uint4 nb = nbv[v];
             const uint32_t nw[4] = {nb.x, nb.y, nb.z, nb.w};
 #pragma unroll
             for (int u = 0; u < 4; u++) {             // 8 dims per word -> one 16-B smem chunk
@@ -200,9 +210,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
         const uint8_t *rec = A.swa + ((int64_t)seq * A.swa_cap + ring) * kSwaBytes;
         const uint2 scw = __ldg(reinterpret_cast<const uint2 *>(rec + 512 + half * 8));
         const uint32_t sc2[2] = {scw.x, scw.y};
+        uint4 bv[16];
+#pragma unroll
+        for (int v = 0; v < 16; v++) bv[v] = __ldg(reinterpret_cast<const uint4 *>(rec + half * 256 + v * 16));
 #pragma unroll
         for (int v = 0; v < 16; v++) {                // 16 B = 16 dims per load
-          const uint4 b = __ldg(reinterpret_cast<const uint4 *>(rec + half * 256 + v * 16));
+          const uint4 b = bv[v];
           const int g = v >> 1;                       // E8M0 group (32 dims) within this half
           const float s = e8m0_to_float((sc2[g >> 2] >> (8 * (g & 3))) & 0xFFu);
           const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
@@ -396,13 +409,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     for (int blk = warp >> 2; blk < 4; blk += 2) {
       const int d = blk * 128 + quarter * 32 + lane;   // TMEM lane = dim within block
-      float rc = 1.f, rs = 0.f;                        // rotation by -pos of the pair holding d
-      if (d >= kRopeOff && A.nsplit == 1) {
-        float a = 1.f, b = 0.f;                        // unit vector e_a through the rotation
-        unrotate_pair_tc(a, b, (d - kRopeOff) >> 1, pos, A.rope_base);
-        rc = a;                                        // cos t
-        rs = b;                                        // -sin t
-      }
+      float rc = 1.f, rs = 0.f;                        // cos t, sin t of the pair holding d
+      if (d >= kRopeOff && A.nsplit == 1) rope_cs(A.inv_freq[(d - kRopeOff) >> 1], pos, rc, rs);
 #pragma unroll
       for (int half = 0; half < 2; half++) {
         uint32_t r[32], lr[32];
@@ -421,10 +429,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
             const float l = __uint_as_float(lr[i]);
             float x = l > 0.f ? __uint_as_float(r[i]) / l : 0.f;
             if (d >= kRopeOff) {
-              // partner dim d^1 lives in the neighbouring lane; with c = cos t,
-              // s = sin t (rc = c, rs = -s):  a' = a c + b s,  b' = -a s + b c
+              // rotate the pair (a, b) = (o[d & ~1], o[d | 1]) by -pos:
+              // a' = a c + b s,  b' = -a s + b c; the partner lives in the next lane
               const float y = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
-              x = (d & 1) ? (x * rc + y * rs) : (x * rc - y * rs);
+              x = (d & 1) ? (x * rc - y * rs) : (x * rc + y * rs);
             }
             const int64_t off = ((int64_t)qi * kHeads + h) * kDim + d;
             if (A.out_f32) static_cast<float *>(A.out)[off] = x;
@@ -479,7 +487,13 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnTcArgs A) {
   const float inv = L > 0.f ? 1.f / L : 0.f;
   x *= inv;
   y *= inv;
-  if (d >= kRopeOff) unrotate_pair_tc(x, y, (d - kRopeOff) >> 1, __ldg(A.pos + qi), A.rope_base);
+  if (d >= kRopeOff) {
+    float c, sn;
+    rope_cs(A.inv_freq[(d - kRopeOff) >> 1], __ldg(A.pos + qi), c, sn);
+    const float a = x, b = y;
+    x = a * c + b * sn;
+    y = -a * sn + b * c;
+  }
   const int64_t off = ((int64_t)qi * kHeads + h) * kDim + d;
   if (A.out_f32)
     *reinterpret_cast<float2 *>(static_cast<float *>(A.out) + off) = make_float2(x, y);
@@ -522,7 +536,7 @@ cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_s
   A.out = out;
   A.out_f32 = out_dtype == CSA2_OUT_F32;
   A.scale_log2 = sm_scale * 1.4426950408889634f;
-  A.rope_base = rope_base;
+  for (int i = 0; i < kRopeDim / 2; i++) A.inv_freq[i] = pow(rope_base, -2.0 * i / (double)kRopeDim);
   const int chunks = attn_chunks(sel_stride);
   A.nsplit = attn_nsplit(n_q, sel_stride);
   A.chunks_per_split = (chunks + A.nsplit - 1) / A.nsplit;

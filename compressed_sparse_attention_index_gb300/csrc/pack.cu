@@ -135,7 +135,9 @@ __device__ __forceinline__ int pow2_exp_fp8(float amax) {   // lim = 448 = 1.75 
 
 // ------------------------------------------------------------------ IDX (S2, S4)
 // Eight lanes per 128-wide row; lane part p packs channels [16p, 16p+16), the
-// lane pair (2g, 2g+1) shares E8M0 group g.
+// lane pair (2g, 2g+1) shares E8M0 group g.  The nibble row is stored in the
+// 64-byte swizzled order (see include/csa2.h) so that the indexer can move
+// whole tiles with one bulk copy.
 __global__ void __launch_bounds__(256) pack_idx_kernel(const uint16_t *__restrict__ src, int64_t rows,
                                                         uint8_t *__restrict__ nib_out,
                                                         uint8_t *__restrict__ sc_out) {
@@ -166,7 +168,11 @@ __global__ void __launch_bounds__(256) pack_idx_kernel(const uint16_t *__restric
     nib[0] = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
     nib[1] = cvt_e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
   }
-  *reinterpret_cast<uint2 *>(nib_out + row * kIdxNibBytes + part * 8) = make_uint2(nib[0], nib[1]);
+  // 64-byte-swizzled row: 16-B chunk c of the row at address A goes to chunk
+  // c ^ ((A >> 7) & 3), the order the tensor-core operand reads it in
+  uint8_t *rowp = nib_out + row * kIdxNibBytes;
+  const uint32_t chunk = ((uint32_t)part >> 1) ^ (uint32_t)((reinterpret_cast<uintptr_t>(rowp) >> 7) & 3u);
+  *reinterpret_cast<uint2 *>(rowp + chunk * 16 + (part & 1) * 8) = make_uint2(nib[0], nib[1]);
   if ((part & 1) == 0) sc_out[row * kIdxScaleBytes + (part >> 1)] = (uint8_t)scale_byte;
 }
 

@@ -13,9 +13,11 @@
 // The kernel is HBM-bound (68 B of key per entry, 8 FLOP/B of FP4 MMA): a
 // persistent CTA per SM streams tiles through a 12-stage shared-memory ring.
 // Warp roles (320 threads):
-//   warp 0      producer: TMA of the 128 x 64 B nibble tile (or 16 gathered
-//               8-entry blocks in pool mode), TMA of the query's 32 x 64 B, bulk
-//               copies of the key and query E8M0 scales;
+//   warp 0      producer: bulk copies (cp.async.bulk) of the 128 x 64 B nibble
+//               tile (or 16 gathered 8-entry blocks of 512 B in pool mode), of the
+//               query's 32 x 64 B, and of the key and query E8M0 scales.  The
+//               nibble planes are stored 64B-swizzled, so a plain contiguous copy
+//               lands in the layout the MMA reads;
 //   warp 1      TMEM owner + MMA issuer: rearranges the scales in shared memory
 //               into the 32-lane x 16-B layout tcgen05.cp expects, copies them
 //               into TMEM, issues the two MMAs, commits to the stage's "empty"
@@ -26,8 +28,6 @@
 // Four TMEM accumulators let the epilogue of earlier tiles overlap the MMAs of
 // later ones.
 // Every mbarrier wait is bounded (CSA2_ERR_TIMEOUT instead of a hang).
-#include <cuda.h>
-
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -57,6 +57,8 @@ __host__ __device__ constexpr uint32_t idesc_mxf4_m128n32(uint32_t sf_id) {
 }
 
 struct ScoreTcArgs {
+  const uint8_t *key_nib;
+  const uint8_t *q_nib;
   const uint8_t *key_scale;
   const uint8_t *q_scale;
   const float *w;
@@ -96,9 +98,7 @@ __device__ __forceinline__ bool next_tile(const ScoreTcArgs &P, int64_t &T, Tile
   return false;
 }
 
-__global__ void __launch_bounds__(kScThreads, 1)
-    index_score_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a8,
-                          const __grid_constant__ CUtensorMap map_b, ScoreTcArgs P) {
+__global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcArgs P) {
   extern __shared__ __align__(1024) unsigned char sc_smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(sc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -118,11 +118,6 @@ __global__ void __launch_bounds__(kScThreads, 1)
     }
     abort_flag = 0;
     ptx::fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    ptx::prefetch_tensormap(&map_a);
-    ptx::prefetch_tensormap(&map_a8);
-    ptx::prefetch_tensormap(&map_b);
   }
   if (warp == 1) ptx::tmem_alloc(&tmem_base_sh, kScTmemCols);
   ptx::tc_fence_before();
@@ -150,8 +145,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(&full_bar[s], 8192 + 2048 + 512 + 128);
           const int64_t r0 = row0 + (int64_t)t.tile * 128;
-          ptx::tma_load_2d_hint(st + kOffA, &map_a, 0, (int32_t)r0, &full_bar[s], policy);
-          ptx::tma_load_2d(st + kOffB, &map_b, 0, t.q * kIdxHeads, &full_bar[s]);
+          ptx::bulk_load_hint(st + kOffA, P.key_nib + r0 * 64, 8192, &full_bar[s], policy);
+          ptx::bulk_load(st + kOffB, P.q_nib + (int64_t)t.q * kIdxHeads * 64, 2048, &full_bar[s]);
           ptx::bulk_load(st + kOffSFA, P.key_scale + r0 * 4, 512, &full_bar[s]);
           ptx::bulk_load(st + kOffSFB, P.q_scale + (int64_t)t.q * kIdxHeads * 4, 128, &full_bar[s]);
         }
@@ -169,11 +164,11 @@ __global__ void __launch_bounds__(kScThreads, 1)
         __syncwarp();
         if (ok) {
           const int64_t r0 = row0 + (int64_t)blk * kBlock;
-          ptx::tma_load_2d_hint(st + kOffA + lane * 512, &map_a8, 0, (int32_t)r0, &full_bar[s], policy);
+          ptx::bulk_load_hint(st + kOffA + lane * 512, P.key_nib + r0 * 64, 512, &full_bar[s], policy);
           ptx::bulk_load(st + kOffSFA + lane * 32, P.key_scale + r0 * 4, 32, &full_bar[s]);
         }
         if (lane == 0) {
-          ptx::tma_load_2d(st + kOffB, &map_b, 0, t.q * kIdxHeads, &full_bar[s]);
+          ptx::bulk_load(st + kOffB, P.q_nib + (int64_t)t.q * kIdxHeads * 64, 2048, &full_bar[s]);
           ptx::bulk_load(st + kOffSFB, P.q_scale + (int64_t)t.q * kIdxHeads * 4, 128, &full_bar[s]);
         }
       }
@@ -280,38 +275,6 @@ __global__ void __launch_bounds__(kScThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-// The driver's tensor-map encoder, fetched through the runtime so that the
-// library does not link libcuda directly (it still loads on a machine without
-// a driver, e.g. to read its exports).
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn tensor_map_encoder() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-static bool encode_rows64(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
-  EncodeTiledFn enc = tensor_map_encoder();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[2] = {64, rows};
-  cuuint64_t strides[1] = {64};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 static int sm_count() {
   static int counts[64] = {};
   int dev = 0;
@@ -325,11 +288,9 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
                                   const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
                                   const int32_t *n_vis, int n_q, const int32_t *pool, float *scores, int64_t stride,
                                   int *status, cudaStream_t st) {
-  CUtensorMap ma, ma8, mb;
-  if (!encode_rows64(&ma, key_nib, (uint64_t)n_seq * n_max, 128) ||
-      !encode_rows64(&ma8, key_nib, (uint64_t)n_seq * n_max, 8) || !encode_rows64(&mb, q_nib, (uint64_t)n_q * 32, 32))
-    return cudaErrorInvalidValue;
   ScoreTcArgs P;
+  P.key_nib = key_nib;
+  P.q_nib = q_nib;
   P.key_scale = key_scale;
   P.q_scale = q_scale;
   P.w = w;
@@ -354,7 +315,7 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
     attr_done[dev] = true;
   }
   const int64_t grid = P.total_tiles < sm_count() ? P.total_tiles : sm_count();
-  index_score_tc_kernel<<<(unsigned)grid, kScThreads, smem, st>>>(ma, ma8, mb, P);
+  index_score_tc_kernel<<<(unsigned)grid, kScThreads, smem, st>>>(P);
   return cudaGetLastError();
 }
 

@@ -117,9 +117,16 @@ __device__ uint64_t radix_threshold(Get get, int64_t n, int k, SelectShared &sh)
   for (int shift = 56; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist[i] = 0;
     __syncthreads();
-    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
-      uint64_t key;
-      if (get(i, key) && (key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
+    // warp-aggregated counting: lanes with equal digits add once (heavily skewed
+    // score distributions otherwise serialise on a few bins)
+    const int lane = threadIdx.x & 31;
+    for (int64_t b0 = 0; b0 < n; b0 += blockDim.x) {
+      const int64_t i = b0 + threadIdx.x;
+      uint64_t key = 0;
+      const bool v = i < n && get(i, key) && (key & mask) == prefix;
+      const uint32_t dig = v ? (uint32_t)((key >> shift) & 255u) : 256u + (uint32_t)lane;
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, dig);
+      if (v && (__ffs(peers) - 1) == lane) atomicAdd(&sh.hist[dig], (uint32_t)__popc(peers));
     }
     __syncthreads();
     find_digit(sh, rem);
@@ -369,9 +376,7 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
   const int n_groups = (int)((S.n_items + G - 1) / G);
   uint32_t *gmax = static_cast<uint32_t *>(ws);
   const int64_t warp_steps = ((int64_t)n_groups * G + 32 * (G >= 32 ? G / 32 : 1) - 1) / (32 * (G >= 32 ? G / 32 : 1));
-  int64_t gx = (warp_steps + 7) / 8;
-  const int64_t cap = (4 * 152 + n_q - 1) / n_q;
-  if (gx > cap) gx = cap;
+  const int64_t gx = (warp_steps + 7) / 8;            // one warp step per warp: every load in flight at once
   topk_groupmax_kernel<<<dim3((unsigned)gx, n_q), 256, 0, st>>>(S, G, n_groups, gmax, status);
   topk_group_select_kernel<<<n_q, kTopkThreads, dsm_group, st>>>(S, G, n_groups, k, gmax, out, status);
   return cudaGetLastError();

@@ -35,8 +35,13 @@
  *   IDX (S2) 68 B per entry as two planes, so that every row is 16-B aligned:
  *            nibbles [rows][64] (128 E2M1 codes) and scales [rows][4] (E8M0, one
  *            per 32 channels) ("128 FP4 values with one E8M0 scale per 32
- *            (68 bytes)", same section).  The indexer query heads (S4) use the
- *            same format with rows = n_q * 32.
+ *            (68 bytes)", same section).  The nibble plane is stored in the
+ *            64-byte swizzled order of the tensor cores: the 16-byte chunk c
+ *            (channels 32c .. 32c+31) of a row at byte address A is stored at
+ *            chunk c ^ ((A >> 7) & 3) of that row; with a 512-B aligned plane
+ *            that is c ^ ((row >> 1) & 3).  csa2_fp4_pack writes this order, so
+ *            any 8-row-aligned range can be packed independently.  The indexer
+ *            query heads (S4) use the same format with rows = n_q * 32.
  *   SWA (S3) 528 B per entry [n_seq][swa_cap][528]: 512 E4M3 values then 16
  *            E8M0 scales, one per 32 channels (reading of "128 entries of 528
  *            FP8 bytes each", same section).
@@ -135,11 +140,12 @@ csa2_status csa2_fp4_pack(int kind, const void *src, int64_t rows, int m, const 
  * with qhat, khat the dequantised FP4 values (E2M1 x E8M0), fp32 accumulation.
  *
  *   key_nib, key_scale  (device) IDX cache planes of n_seq * n_max entries;
- *                       entry j of sequence b is row b*n_max + j.  16-B aligned.
+ *                       entry j of sequence b is row b*n_max + j.  key_nib
+ *                       512-B aligned, key_scale 16-B aligned.
  *   n_max               entries per sequence; a positive multiple of 128.
  *   n_seq               number of sequences (>= 1).
  *   q_nib, q_scale      (device) indexer queries, IDX format, rows = n_q*32;
- *                       16-B aligned.
+ *                       q_nib 512-B aligned, q_scale 16-B aligned.
  *   w                   (device) fp32 [n_q][32] per-head weights, 16-B aligned.
  *   q_seq               (device) int32 [n_q] sequence of each query.
  *   n_vis               (device) int32 [n_q]: entries [0, n_vis) are visible.

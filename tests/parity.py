@@ -52,3 +52,15 @@ def check_scores(s_gpu, s_orc, tol=SCORE_TOL):
     err = np.abs(s_gpu - s_orc).max() if s_orc.size else 0.0
     assert err <= tol * m + 1e-30, (err, m)
     return err / m if m else 0.0
+
+
+def unswizzle_idx_nibbles(nib):
+    """Logical order of IDX nibble rows stored 64B-swizzled (include/csa2.h):
+    16-B chunk c of row r (row 0 at a 512-B aligned address) sits at chunk
+    c ^ ((r >> 1) & 3).  The permutation is its own inverse."""
+    nib = np.asarray(nib, np.uint8).reshape(-1, 4, 16)
+    r = np.arange(nib.shape[0])
+    out = np.empty_like(nib)
+    for c in range(4):
+        out[:, c] = nib[r, c ^ ((r >> 1) & 3)]
+    return out.reshape(-1, 64)

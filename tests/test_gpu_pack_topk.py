@@ -75,7 +75,8 @@ def test_pack_idx_bit_exact(lib, oracle_lib, rows):
     nib = torch.zeros((n, 64), dtype=torch.uint8, device="cuda")
     sc = torch.zeros((n, 4), dtype=torch.uint8, device="cuda")
     lib.csa2_fp4_pack(lib.CSA2_IDX_MXFP4, _dev_bf16(x), n, 1, None, nib, sc)
-    got = np.concatenate([nib.cpu().numpy(), sc.cpu().numpy()], axis=1)
+    from tests.parity import unswizzle_idx_nibbles
+    got = np.concatenate([unswizzle_idx_nibbles(nib.cpu().numpy()), sc.cpu().numpy()], axis=1)
     assert np.array_equal(got, oracle_lib.pack_idx(x))
 
 
