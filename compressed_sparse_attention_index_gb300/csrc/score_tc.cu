@@ -11,13 +11,15 @@
 // epilogue computes s = sum_h w_h * max(0, D[entry][h]) per row.
 //
 // The kernel is HBM-bound (68 B of key per entry, 8 FLOP/B of FP4 MMA): a
-// persistent CTA per SM streams tiles through a 12-stage shared-memory ring.
+// persistent CTA per SM streams tiles through a 20-stage shared-memory ring.
 // Warp roles (320 threads):
 //   warp 0      producer: bulk copies (cp.async.bulk) of the 128 x 64 B nibble
-//               tile (or 16 gathered 8-entry blocks of 512 B in pool mode), of the
-//               query's 32 x 64 B, and of the key and query E8M0 scales.  The
-//               nibble planes are stored 64B-swizzled, so a plain contiguous copy
-//               lands in the layout the MMA reads;
+//               tile (or 16 gathered 8-entry blocks of 512 B in pool mode) and of
+//               its E8M0 scales into the stage ring; the query's 32 x 64 B and its
+//               scales only when the CTA moves to another query (two query slots),
+//               so that 152 CTAs do not re-read the same few L2 lines per tile.
+//               The nibble planes are stored 64B-swizzled, so a plain contiguous
+//               copy lands in the layout the MMA reads;
 //   warp 1      TMEM owner + MMA issuer: rearranges the scales in shared memory
 //               into the 32-lane x 16-B layout tcgen05.cp expects, copies them
 //               into TMEM, issues the two MMAs, commits to the stage's "empty"
@@ -33,15 +35,16 @@
 
 namespace csa2 {
 
-constexpr int kScStages = 12;
-constexpr int kScStageBytes = 12288;
-constexpr int kOffA = 0;          // 128 rows x 64 B, 64B-swizzled (TMA writes it, MMA reads it)
-constexpr int kOffB = 8192;       // 32 rows x 64 B query nibbles, 64B-swizzled
-constexpr int kOffSFA = 10240;    // 512 B key scales: staged [row][4], rearranged in place
-constexpr int kOffSFB = 10752;    // 512 B query scales: staged [head][4] in the first 128 B
+constexpr int kScStages = 20;
+constexpr int kScStageBytes = 9216;
+constexpr int kOffA = 0;          // 128 rows x 64 B nibble tile, 64B-swizzled as stored
+constexpr int kOffSFA = 8192;     // 512 B key scales: staged [row][4], rearranged in place
+constexpr int kScQBytes = 2560;   // per query slot: 32 x 64 B nibbles + 512 B scales
+constexpr int kQOffB = 0, kQOffSFB = 2048;
+constexpr int kScSmem = kScStages * kScStageBytes + 2 * kScQBytes;
 constexpr int kScThreads = 320;
 constexpr int kScAcc = 4;               // TMEM accumulator stages
-constexpr uint32_t kScTmemCols = 256;   // 4 x 32 accumulator columns + 4 x 4 SFA + 4 x 4 SFB
+constexpr uint32_t kScTmemCols = 256;   // 4 x 32 accumulator columns + 4 x 4 SFA + 2 x 4 SFB
 constexpr uint32_t kColSFA = 128, kColSFB = 144;
 
 // Instruction descriptor of kind::mxf4 block-scaled MMA, M=128, N=32, both
@@ -102,7 +105,9 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   extern __shared__ __align__(1024) unsigned char sc_smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(sc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char *qslots = smem + kScStages * kScStageBytes;
   __shared__ __align__(8) uint64_t full_bar[kScStages], empty_bar[kScStages], acc_full[kScAcc], acc_empty[kScAcc];
+  __shared__ __align__(8) uint64_t qfull[2], qempty[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
@@ -115,6 +120,10 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     for (int a = 0; a < kScAcc; a++) {
       ptx::mbar_init(&acc_full[a], 1);
       ptx::mbar_init(&acc_empty[a], 4);
+    }
+    for (int q = 0; q < 2; q++) {
+      ptx::mbar_init(&qfull[q], 1);
+      ptx::mbar_init(&qempty[q], 1);
     }
     abort_flag = 0;
     ptx::fence_mbar_init();
@@ -135,20 +144,32 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     const uint64_t policy = ptx::policy_evict_first();
     int64_t T = blockIdx.x;
     TileInfo t;
+    int cur_q = -1;
+    uint32_t qsw = 0;                                   // query switches so far
     for (uint32_t it = 0; next_tile(P, T, t); it++) {
       if (abort_flag) break;
+      if (t.q != cur_q) {
+        const uint32_t slot = qsw & 1, rnd = qsw >> 1;
+        if (!ptx::mbar_wait(&qempty[slot], (rnd & 1) ^ 1)) { fail(); break; }
+        if (lane == 0) {
+          unsigned char *qs = qslots + slot * kScQBytes;
+          ptx::mbar_arrive_expect_tx(&qfull[slot], 2048 + 128);
+          ptx::bulk_load(qs + kQOffB, P.q_nib + (int64_t)t.q * kIdxHeads * 64, 2048, &qfull[slot]);
+          ptx::bulk_load(qs + kQOffSFB, P.q_scale + (int64_t)t.q * kIdxHeads * 4, 128, &qfull[slot]);
+        }
+        cur_q = t.q;
+        qsw++;
+      }
       const uint32_t s = it % kScStages, r = it / kScStages;
       if (!ptx::mbar_wait(&empty_bar[s], (r & 1) ^ 1)) { fail(); break; }
       unsigned char *st = smem + s * kScStageBytes;
       const int64_t row0 = (int64_t)t.seq * P.n_max;
       if (P.pool == nullptr) {
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&full_bar[s], 8192 + 2048 + 512 + 128);
+          ptx::mbar_arrive_expect_tx(&full_bar[s], 8192 + 512);
           const int64_t r0 = row0 + (int64_t)t.tile * 128;
           ptx::bulk_load_hint(st + kOffA, P.key_nib + r0 * 64, 8192, &full_bar[s], policy);
-          ptx::bulk_load(st + kOffB, P.q_nib + (int64_t)t.q * kIdxHeads * 64, 2048, &full_bar[s]);
           ptx::bulk_load(st + kOffSFA, P.key_scale + r0 * 4, 512, &full_bar[s]);
-          ptx::bulk_load(st + kOffSFB, P.q_scale + (int64_t)t.q * kIdxHeads * 4, 128, &full_bar[s]);
         }
       } else {
         int blk = -1;
@@ -159,17 +180,13 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
           if (blk >= 0 && !ok) record_error(P.status, CSA2_ERR_BOUNDS);
         }
         const unsigned m = __ballot_sync(0xFFFFFFFFu, ok);
-        if (lane == 0)
-          ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)__popc(m) * (512 + 32) + 2048 + 128);
+        // an all-empty tile still arrives once, so its phase completes
+        if (lane == 0) ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)__popc(m) * (512 + 32));
         __syncwarp();
         if (ok) {
           const int64_t r0 = row0 + (int64_t)blk * kBlock;
           ptx::bulk_load_hint(st + kOffA + lane * 512, P.key_nib + r0 * 64, 512, &full_bar[s], policy);
           ptx::bulk_load(st + kOffSFA + lane * 32, P.key_scale + r0 * 4, 32, &full_bar[s]);
-        }
-        if (lane == 0) {
-          ptx::bulk_load(st + kOffB, P.q_nib + (int64_t)t.q * kIdxHeads * 64, 2048, &full_bar[s]);
-          ptx::bulk_load(st + kOffSFB, P.q_scale + (int64_t)t.q * kIdxHeads * 4, 128, &full_bar[s]);
         }
       }
       __syncwarp();
@@ -178,26 +195,44 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     // ------------------------------------------------------------ MMA issuer
     int64_t T = blockIdx.x;
     TileInfo t;
+    int cur_q = -1;
+    uint32_t qsw = 0, slot = 0;
     const uint32_t idesc0 = idesc_mxf4_m128n32(0), idesc1 = idesc_mxf4_m128n32(2);
     for (uint32_t it = 0; next_tile(P, T, t); it++) {
       if (abort_flag) break;
+      if (t.q != cur_q) {
+        // release the previous query slot once every MMA issued so far is done
+        if (qsw > 0 && lane == 0) ptx::tc_commit(&qempty[(qsw - 1) & 1]);
+        slot = qsw & 1;
+        const uint32_t rnd = qsw >> 1;
+        if (!ptx::mbar_wait(&qfull[slot], rnd & 1)) { fail(); break; }
+        uint32_t *sfb = reinterpret_cast<uint32_t *>(qslots + slot * kScQBytes + kQOffSFB);
+        const uint32_t vb = sfb[lane];
+        __syncwarp();
+        sfb[lane * 4 + 0] = vb;          // head `lane` -> 16-B line `lane` (tcgen05.cp layout)
+        sfb[lane * 4 + 1] = 0u;
+        sfb[lane * 4 + 2] = 0u;
+        sfb[lane * 4 + 3] = 0u;
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tc_fence_after();
+          ptx::tc_cp_32x128b_warpx4(tmem + kColSFB + slot * 4, ptx::smem_desc(ptx::smem_u32(sfb), 0, 128, 0));
+        }
+        cur_q = t.q;
+        qsw++;
+      }
       const uint32_t s = it % kScStages, r = it / kScStages, a = it % kScAcc, ra = it / kScAcc;
       if (!ptx::mbar_wait(&full_bar[s], r & 1)) { fail(); break; }
       unsigned char *st = smem + s * kScStageBytes;
-      // scales -> tcgen05.cp layout: 16-B line m0 holds rows m0, m0+32, m0+64, m0+96
+      // key scales -> tcgen05.cp layout: 16-B line m0 holds rows m0, m0+32, m0+64, m0+96
       uint32_t *sfa = reinterpret_cast<uint32_t *>(st + kOffSFA);
-      uint32_t *sfb = reinterpret_cast<uint32_t *>(st + kOffSFB);
       uint32_t va[4];
 #pragma unroll
       for (int i = 0; i < 4; i++) va[i] = sfa[i * 32 + lane];
-      const uint32_t vb = sfb[lane];
       __syncwarp();
 #pragma unroll
       for (int i = 0; i < 4; i++) sfa[lane * 4 + i] = va[i];
-      sfb[lane * 4 + 0] = vb;
-      sfb[lane * 4 + 1] = 0u;
-      sfb[lane * 4 + 2] = 0u;
-      sfb[lane * 4 + 3] = 0u;
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -205,11 +240,10 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
           fail();
         } else {
           ptx::tc_fence_after();
-          const uint32_t t_sfa = tmem + kColSFA + a * 4, t_sfb = tmem + kColSFB + a * 4;
+          const uint32_t t_sfa = tmem + kColSFA + a * 4, t_sfb = tmem + kColSFB + slot * 4;
           ptx::tc_cp_32x128b_warpx4(t_sfa, ptx::smem_desc(ptx::smem_u32(sfa), 0, 128, 0));
-          ptx::tc_cp_32x128b_warpx4(t_sfb, ptx::smem_desc(ptx::smem_u32(sfb), 0, 128, 0));
           const uint64_t ad = ptx::smem_desc(ptx::smem_u32(st + kOffA), 16, 512, 4);
-          const uint64_t bd = ptx::smem_desc(ptx::smem_u32(st + kOffB), 16, 512, 4);
+          const uint64_t bd = ptx::smem_desc(ptx::smem_u32(qslots + slot * kScQBytes + kQOffB), 16, 512, 4);
           ptx::tc_mma_mxf4(tmem + a * 32, ad, bd, idesc0, t_sfa, t_sfb, 0u);
           ptx::tc_mma_mxf4(tmem + a * 32, ad + 2, bd + 2, idesc1, t_sfa, t_sfb, 1u);   // +32 B along K
           ptx::tc_commit(&empty_bar[s]);
@@ -305,7 +339,7 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
   P.tiles_per_q = pool ? kPoolSlots / 128 : (int)(n_max / 128);
   P.total_tiles = (int64_t)n_q * P.tiles_per_q;
   P.status = status;
-  const size_t smem = (size_t)kScStages * kScStageBytes + 1024;
+  const size_t smem = (size_t)kScSmem + 1024;
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_done[64] = {};

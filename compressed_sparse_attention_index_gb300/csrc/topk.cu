@@ -246,58 +246,94 @@ __global__ void __launch_bounds__(256) topk_groupmax_kernel(TopkSrc S, int G, in
   }
 }
 
+// k-th largest of n 32-bit values (counted with multiplicity; requires at
+// least k valid values): four 8-bit radix passes narrowing a prefix.
+template <class Get>
+__device__ uint32_t radix_kth_u32(Get get, int n, int k, SelectShared &sh) {
+  uint32_t prefix = 0, mask = 0;
+  int rem = k;
+  const int lane = threadIdx.x & 31;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist[i] = 0;
+    __syncthreads();
+    for (int b0 = 0; b0 < n; b0 += blockDim.x) {
+      const int i = b0 + threadIdx.x;
+      uint32_t v = 0;
+      const bool ok = i < n && get(i, v) && (v & mask) == prefix;
+      const uint32_t dig = ok ? ((v >> shift) & 255u) : 256u + (uint32_t)lane;
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, dig);
+      if (ok && (__ffs(peers) - 1) == lane) atomicAdd(&sh.hist[dig], (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    find_digit(sh, rem);
+    __syncthreads();
+    prefix |= (uint32_t)sh.digit << shift;
+    mask |= 0xFFu << shift;
+    rem -= sh.above;
+    __syncthreads();
+  }
+  return prefix;
+}
+
 // One CTA per query.  T = the k-th largest group maximum: at least k groups
 // reach T, so at least k items do, so the k-th best item key is >= T and every
 // item of the top-k lies in a group whose maximum is >= T.  Those groups are
-// scanned for items with key >= T (a superset of the top-k, usually ~2k items),
-// and the exact selection runs on that candidate set.
+// listed, their items scanned by all threads at once for keys >= T (a superset
+// of the top-k, usually ~2k items), and the exact selection runs on that set.
 __global__ void __launch_bounds__(kTopkThreads) topk_group_select_kernel(TopkSrc S, int G, int n_groups, int k,
                                                                           const uint32_t *__restrict__ gmax,
                                                                           int32_t *__restrict__ out, int *status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint64_t *gk = reinterpret_cast<uint64_t *>(smem_raw);                 // [kMaxGroups]
-  uint64_t *cand = gk + kMaxGroups;                                      // [kCandCap]
-  int32_t *sel = reinterpret_cast<int32_t *>(cand + kCandCap);           // [kMaxK]
+  uint64_t *cand = reinterpret_cast<uint64_t *>(smem_raw);               // [kCandCap]
+  uint32_t *gm = reinterpret_cast<uint32_t *>(cand + kCandCap);          // [kMaxGroups] group maxima
+  int32_t *glist = reinterpret_cast<int32_t *>(gm + kMaxGroups);         // [kMaxGroups] groups to scan
+  int32_t *sel = glist + kMaxGroups;                                     // [kMaxK]
   __shared__ SelectShared sh;
-  __shared__ int n_cand, n_valid_groups;
-  __shared__ uint32_t thr_sh;
+  __shared__ int n_cand, n_valid_groups, n_list;
   const int q = blockIdx.x;
   const int nv = query_nv(S, q, status);
-  const uint32_t *gm = gmax + (int64_t)q * n_groups;
-  if (threadIdx.x == 0) { n_cand = 0; n_valid_groups = 0; }
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) { n_cand = 0; n_valid_groups = 0; n_list = 0; }
   __syncthreads();
   int live_groups = 0;
   for (int g = threadIdx.x; g < n_groups; g += blockDim.x) {
-    const uint32_t m = gm[g];
-    gk[g] = ((uint64_t)m << 32) | (uint32_t)(~(uint32_t)g);
+    const uint32_t m = gmax[(int64_t)q * n_groups + g];
+    gm[g] = m;
     live_groups += m != 0;
   }
   atomicAdd(&n_valid_groups, live_groups);
   __syncthreads();
-  uint32_t T = 0;
+  uint32_t T = 1;                                    // nonzero keys: every valid item
   if (n_valid_groups > k) {
-    auto get = [&](int64_t i, uint64_t &key) { key = gk[i]; return (key >> 32) != 0; };
-    T = (uint32_t)(radix_threshold(get, n_groups, k, sh) >> 32);
+    auto get = [&](int i, uint32_t &v) { v = gm[i]; return v != 0; };
+    T = radix_kth_u32(get, n_groups, k, sh);
   }
-  if (threadIdx.x == 0) thr_sh = T;
+  // list the groups whose maximum reaches T
+  for (int b0 = 0; b0 < n_groups; b0 += blockDim.x) {
+    const int g = b0 + threadIdx.x;
+    const bool v = g < n_groups && gm[g] >= T;
+    const unsigned b = __ballot_sync(0xFFFFFFFFu, v);
+    int base = 0;
+    if (lane == 0 && b) base = atomicAdd(&n_list, __popc(b));
+    base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(b & ((1u << lane) - 1u));
+    if (v) glist[base] = g;
+  }
   __syncthreads();
-  T = thr_sh;
-  // scan the groups whose maximum reaches T; one warp per group
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int g = warp; g < n_groups; g += blockDim.x >> 5) {
-    const uint32_t m = gm[g];
-    if (m == 0 || m < T) continue;
-    for (int u = 0; u < G; u += 32) {
-      const int64_t i = (int64_t)g * G + u + lane;
-      uint64_t key = 0;
-      const bool v = u + lane < G && i < S.n_items && item_key(S, q, i, nv, key, status) &&
-                     (uint32_t)(key >> 32) >= T;
-      const unsigned b = __ballot_sync(0xFFFFFFFFu, v);
-      int base = 0;
-      if (lane == 0 && b) base = atomicAdd(&n_cand, __popc(b));
-      base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(b & ((1u << lane) - 1u));
-      if (v && base < kCandCap) cand[base] = key;
+  // scan their items, all loads of the block in flight together
+  const int64_t total = (int64_t)n_list * G;
+  for (int64_t b0 = 0; b0 < total; b0 += blockDim.x) {
+    const int64_t f = b0 + threadIdx.x;
+    uint64_t key = 0;
+    bool v = false;
+    if (f < total) {
+      const int64_t i = (int64_t)glist[f / G] * G + f % G;
+      v = i < S.n_items && item_key(S, q, i, nv, key, status) && (uint32_t)(key >> 32) >= T;
     }
+    const unsigned b = __ballot_sync(0xFFFFFFFFu, v);
+    int base = 0;
+    if (lane == 0 && b) base = atomicAdd(&n_cand, __popc(b));
+    base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(b & ((1u << lane) - 1u));
+    if (v && base < kCandCap) cand[base] = key;
   }
   __syncthreads();
   const int nc = n_cand;
@@ -359,7 +395,7 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
   S.n_max = n_max;
   S.n_items = topk_items(n_max, block, pool != nullptr);
   const size_t dsm_direct = (size_t)kDirectCap * 8 + (size_t)kMaxK * 4;
-  const size_t dsm_group = (size_t)(kMaxGroups + kCandCap) * 8 + (size_t)kMaxK * 4;
+  const size_t dsm_group = (size_t)kCandCap * 8 + (size_t)kMaxGroups * 8 + (size_t)kMaxK * 4;
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_done[64] = {};
