@@ -3,7 +3,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/csa2.h"
+#include "csa2.h"
 
 namespace csa2 {
 

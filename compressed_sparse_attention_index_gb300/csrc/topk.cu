@@ -78,10 +78,33 @@ __device__ __forceinline__ int query_nv(const TopkSrc &S, int q, int *status) {
 // ---- block-wide pieces (blockDim.x == kTopkThreads) ----
 struct SelectShared {
   uint32_t hist[256];
+  uint32_t *whist;   // [32 warps][256] private histograms (dynamic shared memory)
   int digit;
   int above;
   int count;
 };
+
+// sh.hist[d] = number of items i < n with digit_of(i, d) true.  Each warp counts
+// into its own histogram (no cross-warp contention on the few busy bins of a
+// skewed distribution), then the 32 histograms are summed.
+template <class F>
+__device__ void block_hist(SelectShared &sh, int64_t n, F digit_of) {
+  uint32_t *wh = sh.whist + (threadIdx.x >> 5) * 256;
+  for (int i = threadIdx.x; i < 32 * 256; i += blockDim.x) sh.whist[i] = 0;
+  __syncthreads();
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    uint32_t d;
+    if (digit_of(i, d)) atomicAdd(&wh[d], 1u);
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < 256; b += blockDim.x) {
+    uint32_t c = 0;
+#pragma unroll 8
+    for (int w = 0; w < 32; w++) c += sh.whist[w * 256 + b];
+    sh.hist[b] = c;
+  }
+  __syncthreads();
+}
 
 // Warp 0 finds digit d with (#keys above d) < rem <= (#keys above d) + hist[d].
 __device__ __forceinline__ void find_digit(SelectShared &sh, int rem) {
@@ -115,20 +138,12 @@ __device__ uint64_t radix_threshold(Get get, int64_t n, int k, SelectShared &sh)
   uint64_t prefix = 0, mask = 0;
   int rem = k;
   for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist[i] = 0;
-    __syncthreads();
-    // warp-aggregated counting: lanes with equal digits add once (heavily skewed
-    // score distributions otherwise serialise on a few bins)
-    const int lane = threadIdx.x & 31;
-    for (int64_t b0 = 0; b0 < n; b0 += blockDim.x) {
-      const int64_t i = b0 + threadIdx.x;
-      uint64_t key = 0;
-      const bool v = i < n && get(i, key) && (key & mask) == prefix;
-      const uint32_t dig = v ? (uint32_t)((key >> shift) & 255u) : 256u + (uint32_t)lane;
-      const unsigned peers = __match_any_sync(0xFFFFFFFFu, dig);
-      if (v && (__ffs(peers) - 1) == lane) atomicAdd(&sh.hist[dig], (uint32_t)__popc(peers));
-    }
-    __syncthreads();
+    block_hist(sh, n, [&](int64_t i, uint32_t &d) {
+      uint64_t key;
+      if (!get(i, key) || (key & mask) != prefix) return false;
+      d = (uint32_t)((key >> shift) & 255u);
+      return true;
+    });
     find_digit(sh, rem);
     __syncthreads();
     const int d = sh.digit;
@@ -193,6 +208,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
   uint64_t *keys = reinterpret_cast<uint64_t *>(smem_raw);                       // [kDirectCap]
   int32_t *sel = reinterpret_cast<int32_t *>(keys + kDirectCap);                 // [kMaxK]
   __shared__ SelectShared sh;
+  sh.whist = reinterpret_cast<uint32_t *>(sel + kMaxK);                          // [32][256]
   __shared__ int n_keys;
   const int q = blockIdx.x;
   const int nv = query_nv(S, q, status);
@@ -241,7 +257,7 @@ __global__ void __launch_bounds__(256) topk_groupmax_kernel(TopkSrc S, int G, in
       }
     }
     for (int o = lpg >> 1; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    const int64_t g = i0 / G;
+    const int64_t g = i0 >> (__ffs(G) - 1);
     if ((lane & (lpg - 1)) == 0 && g < n_groups) gmax[(int64_t)q * n_groups + g] = m;
   }
 }
@@ -252,19 +268,13 @@ template <class Get>
 __device__ uint32_t radix_kth_u32(Get get, int n, int k, SelectShared &sh) {
   uint32_t prefix = 0, mask = 0;
   int rem = k;
-  const int lane = threadIdx.x & 31;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist[i] = 0;
-    __syncthreads();
-    for (int b0 = 0; b0 < n; b0 += blockDim.x) {
-      const int i = b0 + threadIdx.x;
-      uint32_t v = 0;
-      const bool ok = i < n && get(i, v) && (v & mask) == prefix;
-      const uint32_t dig = ok ? ((v >> shift) & 255u) : 256u + (uint32_t)lane;
-      const unsigned peers = __match_any_sync(0xFFFFFFFFu, dig);
-      if (ok && (__ffs(peers) - 1) == lane) atomicAdd(&sh.hist[dig], (uint32_t)__popc(peers));
-    }
-    __syncthreads();
+    block_hist(sh, n, [&](int64_t i, uint32_t &d) {
+      uint32_t v;
+      if (!get((int)i, v) || (v & mask) != prefix) return false;
+      d = (v >> shift) & 255u;
+      return true;
+    });
     find_digit(sh, rem);
     __syncthreads();
     prefix |= (uint32_t)sh.digit << shift;
@@ -289,6 +299,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_group_select_kernel(TopkSrc
   int32_t *glist = reinterpret_cast<int32_t *>(gm + kMaxGroups);         // [kMaxGroups] groups to scan
   int32_t *sel = glist + kMaxGroups;                                     // [kMaxK]
   __shared__ SelectShared sh;
+  sh.whist = reinterpret_cast<uint32_t *>(sel + kMaxK);                  // [32][256]
   __shared__ int n_cand, n_valid_groups, n_list;
   const int q = blockIdx.x;
   const int nv = query_nv(S, q, status);
@@ -296,10 +307,19 @@ __global__ void __launch_bounds__(kTopkThreads) topk_group_select_kernel(TopkSrc
   if (threadIdx.x == 0) { n_cand = 0; n_valid_groups = 0; n_list = 0; }
   __syncthreads();
   int live_groups = 0;
-  for (int g = threadIdx.x; g < n_groups; g += blockDim.x) {
-    const uint32_t m = gmax[(int64_t)q * n_groups + g];
-    gm[g] = m;
-    live_groups += m != 0;
+  for (int b0 = 0; b0 < n_groups; b0 += 8 * blockDim.x) {     // eight loads in flight per thread
+    uint32_t m[8];
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      const int g = b0 + u * blockDim.x + threadIdx.x;
+      m[u] = g < n_groups ? __ldg(gmax + (int64_t)q * n_groups + g) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      const int g = b0 + u * blockDim.x + threadIdx.x;
+      if (g < n_groups) gm[g] = m[u];
+      live_groups += m[u] != 0;
+    }
   }
   atomicAdd(&n_valid_groups, live_groups);
   __syncthreads();
@@ -319,21 +339,39 @@ __global__ void __launch_bounds__(kTopkThreads) topk_group_select_kernel(TopkSrc
     if (v) glist[base] = g;
   }
   __syncthreads();
-  // scan their items, all loads of the block in flight together
-  const int64_t total = (int64_t)n_list * G;
-  for (int64_t b0 = 0; b0 < total; b0 += blockDim.x) {
-    const int64_t f = b0 + threadIdx.x;
-    uint64_t key = 0;
-    bool v = false;
-    if (f < total) {
-      const int64_t i = (int64_t)glist[f / G] * G + f % G;
-      v = i < S.n_items && item_key(S, q, i, nv, key, status) && (uint32_t)(key >> 32) >= T;
+  // scan their items: every thread keeps kScanU item loads in flight
+  constexpr int kScanU = 8;
+  const int lg = __ffs(G) - 1;                      // G is a power of two
+  const int total = n_list << lg;
+  const bool plain = S.pool == nullptr && S.block == 1;
+  const float *row = S.scores + (int64_t)q * S.stride;
+  for (int b0 = 0; b0 < total; b0 += kScanU * blockDim.x) {
+    uint64_t key[kScanU];
+    bool v[kScanU];
+#pragma unroll
+    for (int u = 0; u < kScanU; u++) {
+      const int f = b0 + u * blockDim.x + threadIdx.x;
+      key[u] = 0;
+      v[u] = false;
+      if (f < total) {
+        const int64_t i = ((int64_t)glist[f >> lg] << lg) + (f & (G - 1));
+        if (plain) {
+          v[u] = i < nv;
+          if (v[u]) key[u] = ((uint64_t)order_key(__ldg(row + i)) << 32) | (uint32_t)(~(uint32_t)i);
+        } else {
+          v[u] = i < S.n_items && item_key(S, q, i, nv, key[u], status);
+        }
+      }
     }
-    const unsigned b = __ballot_sync(0xFFFFFFFFu, v);
-    int base = 0;
-    if (lane == 0 && b) base = atomicAdd(&n_cand, __popc(b));
-    base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(b & ((1u << lane) - 1u));
-    if (v && base < kCandCap) cand[base] = key;
+#pragma unroll
+    for (int u = 0; u < kScanU; u++) {
+      const bool ok = v[u] && (uint32_t)(key[u] >> 32) >= T;
+      const unsigned b = __ballot_sync(0xFFFFFFFFu, ok);
+      int base = 0;
+      if (lane == 0 && b) base = atomicAdd(&n_cand, __popc(b));
+      base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(b & ((1u << lane) - 1u));
+      if (ok && base < kCandCap) cand[base] = key[u];
+    }
   }
   __syncthreads();
   const int nc = n_cand;
@@ -394,8 +432,8 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
   S.block = block;
   S.n_max = n_max;
   S.n_items = topk_items(n_max, block, pool != nullptr);
-  const size_t dsm_direct = (size_t)kDirectCap * 8 + (size_t)kMaxK * 4;
-  const size_t dsm_group = (size_t)kCandCap * 8 + (size_t)kMaxGroups * 8 + (size_t)kMaxK * 4;
+  const size_t dsm_direct = (size_t)kDirectCap * 8 + (size_t)kMaxK * 4 + 32 * 256 * 4;
+  const size_t dsm_group = (size_t)kCandCap * 8 + (size_t)kMaxGroups * 8 + (size_t)kMaxK * 4 + 32 * 256 * 4;
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_done[64] = {};
