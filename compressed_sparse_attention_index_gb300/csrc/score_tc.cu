@@ -6,46 +6,50 @@
 // architecture", lightning-indexer note and section "The KV cache").  That is
 // exactly the MXFP4 block-scaled format the tcgen05 MMA consumes, so
 //     D[entry][head] = sum_c khat[entry][c] * qhat[head][c]
-// is one  M=128 (entries) x N=32 (heads) x K=128  product per tile, issued as two
-// tcgen05.mma.kind::mxf4.block_scale.scale_vec::2X (K=64 each) into TMEM, and the
-// epilogue computes s = sum_h w_h * max(0, D[entry][h]) per row.
+// is one  M=128 (entries) x N=32 (heads) x K=128  product per 128 entries,
+// issued as two tcgen05.mma.kind::mxf4.block_scale.scale_vec::2X (K=64 each)
+// into TMEM; the epilogue computes s = sum_h w_h * max(0, D[entry][h]) per row.
 //
 // The kernel is HBM-bound (68 B of key per entry, 8 FLOP/B of FP4 MMA): a
-// persistent CTA per SM streams tiles through a 20-stage shared-memory ring.
-// Warp roles (320 threads):
-//   warp 0      producer: bulk copies (cp.async.bulk) of the 128 x 64 B nibble
-//               tile (or 16 gathered 8-entry blocks of 512 B in pool mode) and of
-//               its E8M0 scales into the stage ring; the query's 32 x 64 B and its
-//               scales only when the CTA moves to another query (two query slots),
-//               so that 152 CTAs do not re-read the same few L2 lines per tile.
-//               The nibble planes are stored 64B-swizzled, so a plain contiguous
-//               copy lands in the layout the MMA reads;
-//   warp 1      TMEM owner + MMA issuer: rearranges the scales in shared memory
-//               into the 32-lane x 16-B layout tcgen05.cp expects, copies them
-//               into TMEM, issues the two MMAs, commits to the stage's "empty"
-//               barrier and to the accumulator's "full" barrier;
-//   warps 2..9  epilogue, two groups of four warps taking alternate tiles: one
-//               TMEM lane (= one entry) per thread, 32 columns (= heads) per
-//               tcgen05.ld, ReLU + weighted sum, coalesced store.
-// Four TMEM accumulators let the epilogue of earlier tiles overlap the MMAs of
-// later ones.
-// Every mbarrier wait is bounded (CSA2_ERR_TIMEOUT instead of a hang).
+// persistent CTA per SM streams work units of 256 entries (two 128-row
+// sub-tiles) through a 12-stage shared-memory ring.  Warp roles (352 threads):
+//   warp 0      producer: one bulk copy (cp.async.bulk) of the unit's 16 KB of
+//               nibbles and one of its 1 KB of E8M0 scales (pool mode: 32
+//               gathered 8-entry blocks of 512 B + 32 B); the query's 2 KB of
+//               nibbles and 128 B of scales only when the CTA moves to another
+//               query (two query slots).  The nibble planes are stored
+//               64B-swizzled, so a plain contiguous copy lands in the layout the
+//               MMA reads;
+//   warp 2      scale-factor warp: rearranges the unit's key scales in shared
+//               memory into the 32-lane x 16-B layout tcgen05.cp expects, copies
+//               them into TMEM and signals the MMA warp through tcgen05.commit;
+//   warp 1      TMEM owner + MMA issuer: four MMAs per unit, then commits to the
+//               stage's "empty" barrier and to the accumulator's "full" barrier;
+//   warps 3..10 epilogue, two groups of four warps taking alternate units: one
+//               TMEM lane (= one entry of each sub-tile) per thread, 32 columns
+//               (= heads) per tcgen05.ld, ReLU + weighted sum, coalesced store.
+// The tile schedule is advanced incrementally (no division per unit) and the
+// per-query sequence id / visible length are cached, so the issuing warps spend
+// their time on the pipeline, not on bookkeeping.  Every mbarrier wait is
+// bounded (CSA2_ERR_TIMEOUT instead of a hang).
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
 namespace csa2 {
 
-constexpr int kScStages = 20;
-constexpr int kScStageBytes = 9216;
-constexpr int kOffA = 0;          // 128 rows x 64 B nibble tile, 64B-swizzled as stored
-constexpr int kOffSFA = 8192;     // 512 B key scales: staged [row][4], rearranged in place
-constexpr int kScQBytes = 2560;   // per query slot: 32 x 64 B nibbles + 512 B scales
+constexpr int kScStages = 12;
+constexpr int kUnit = 256;                // entries per work unit (two 128-row sub-tiles)
+constexpr int kScStageBytes = 17408;      // 16 KB nibbles + 1 KB scales
+constexpr int kOffA = 0;                  // sub-tile j at j * 8192: 128 rows x 64 B, 64B-swizzled as stored
+constexpr int kOffSFA = 16384;            // 2 x 512 B key scales: staged [row][4], rearranged in place
+constexpr int kScQBytes = 2560;           // per query slot: 32 x 64 B nibbles + 512 B scales
 constexpr int kQOffB = 0, kQOffSFB = 2048;
 constexpr int kScSmem = kScStages * kScStageBytes + 2 * kScQBytes;
-constexpr int kScThreads = 320;
-constexpr int kScAcc = 4;               // TMEM accumulator stages
-constexpr uint32_t kScTmemCols = 256;   // 4 x 32 accumulator columns + 4 x 4 SFA + 2 x 4 SFB
-constexpr uint32_t kColSFA = 128, kColSFB = 144;
+constexpr int kScThreads = 352;
+constexpr int kScAcc = 4;                 // TMEM accumulator stages (64 columns each)
+constexpr uint32_t kScTmemCols = 512;
+constexpr uint32_t kColSFA = 256;         // per stage: 2 sub-tiles x 4 columns
+constexpr uint32_t kColSFB = 256 + kScStages * 8;   // per query slot: 4 columns
 
 // Instruction descriptor of kind::mxf4 block-scaled MMA, M=128, N=32, both
 // operands E2M1 and K-major, UE8M0 scales; sf_id picks the scale byte pair.
@@ -73,41 +77,57 @@ struct ScoreTcArgs {
   int64_t n_max;
   int n_seq;
   int n_q;
-  int tiles_per_q;
-  int64_t total_tiles;
+  int units_per_q;
   int *status;
 };
 
-struct TileInfo {
-  int q, tile, seq, nv;
-};
-
-// Shared tile schedule of every role: tile T = blockIdx.x + k * gridDim.x over
-// (query, 128-entry tile); tiles past a query's visible length are skipped.
-__device__ __forceinline__ bool next_tile(const ScoreTcArgs &P, int64_t &T, TileInfo &t) {
-  for (; T < P.total_tiles; T += gridDim.x) {
-    t.q = (int)(T / P.tiles_per_q);
-    t.tile = (int)(T % P.tiles_per_q);
-    t.seq = __ldg(P.q_seq + t.q);
-    t.nv = __ldg(P.n_vis + t.q);
-    if (t.seq < 0 || t.seq >= P.n_seq || t.nv < 0 || (int64_t)t.nv > P.n_max) {
-      if (t.tile == 0 && threadIdx.x == 0) record_error(P.status, CSA2_ERR_BOUNDS);
-      continue;
-    }
-    if (P.pool == nullptr && (int64_t)t.tile * 128 >= t.nv) continue;
-    T += gridDim.x;
-    return true;
+// Work schedule shared by every role: unit index T = blockIdx.x + k * gridDim.x
+// over (query, 256-entry unit), advanced without division; units past a query's
+// visible length are skipped.  seq / nv are re-read only when the query changes.
+struct Schedule {
+  int q, u, seq, nv;
+  bool started;
+  __device__ void init(const ScoreTcArgs &P) {
+    q = (int)(blockIdx.x / (unsigned)P.units_per_q);
+    u = (int)(blockIdx.x % (unsigned)P.units_per_q);
+    started = false;
+    load(P);
   }
-  return false;
-}
+  __device__ void load(const ScoreTcArgs &P) {
+    if (q < P.n_q) {
+      seq = __ldg(P.q_seq + q);
+      nv = __ldg(P.n_vis + q);
+      if (seq < 0 || seq >= P.n_seq || nv < 0 || (int64_t)nv > P.n_max) {
+        if (u == 0 && threadIdx.x == 0) record_error(P.status, CSA2_ERR_BOUNDS);
+        nv = -1;                                      // marks a query to skip
+      }
+    }
+  }
+  // Advance to the next unit this CTA processes; false when done.
+  __device__ bool next(const ScoreTcArgs &P) {
+    for (;;) {
+      if (started) {
+        u += gridDim.x;
+        bool moved = false;
+        while (u >= P.units_per_q) { u -= P.units_per_q; q++; moved = true; }
+        if (moved) load(P);
+      }
+      started = true;
+      if (q >= P.n_q) return false;
+      if (nv < 0) continue;
+      if (P.pool == nullptr && u * kUnit >= nv) continue;
+      return true;
+    }
+  }
+};
 
 __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcArgs P) {
   extern __shared__ __align__(1024) unsigned char sc_smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(sc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char *qslots = smem + kScStages * kScStageBytes;
-  __shared__ __align__(8) uint64_t full_bar[kScStages], empty_bar[kScStages], acc_full[kScAcc], acc_empty[kScAcc];
-  __shared__ __align__(8) uint64_t qfull[2], qempty[2];
+  __shared__ __align__(8) uint64_t full_bar[kScStages], sf_bar[kScStages], empty_bar[kScStages];
+  __shared__ __align__(8) uint64_t acc_full[kScAcc], acc_empty[kScAcc], qfull[2], qempty[2], qsf[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
@@ -115,6 +135,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   if (threadIdx.x == 0) {
     for (int s = 0; s < kScStages; s++) {
       ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&sf_bar[s], 1);
       ptx::mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < kScAcc; a++) {
@@ -124,6 +145,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     for (int q = 0; q < 2; q++) {
       ptx::mbar_init(&qfull[q], 1);
       ptx::mbar_init(&qempty[q], 1);
+      ptx::mbar_init(&qsf[q], 1);
     }
     abort_flag = 0;
     ptx::fence_mbar_init();
@@ -139,48 +161,46 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     abort_flag = 1;
   };
 
+  Schedule sc;
+  sc.init(P);
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = ptx::policy_evict_first();
-    int64_t T = blockIdx.x;
-    TileInfo t;
     int cur_q = -1;
     uint32_t qsw = 0;                                   // query switches so far
-    for (uint32_t it = 0; next_tile(P, T, t); it++) {
+    for (uint32_t it = 0; sc.next(P); it++) {
       if (abort_flag) break;
-      if (t.q != cur_q) {
+      if (sc.q != cur_q) {
         const uint32_t slot = qsw & 1, rnd = qsw >> 1;
         if (!ptx::mbar_wait(&qempty[slot], (rnd & 1) ^ 1)) { fail(); break; }
         if (lane == 0) {
           unsigned char *qs = qslots + slot * kScQBytes;
           ptx::mbar_arrive_expect_tx(&qfull[slot], 2048 + 128);
-          ptx::bulk_load(qs + kQOffB, P.q_nib + (int64_t)t.q * kIdxHeads * 64, 2048, &qfull[slot]);
-          ptx::bulk_load(qs + kQOffSFB, P.q_scale + (int64_t)t.q * kIdxHeads * 4, 128, &qfull[slot]);
+          ptx::bulk_load(qs + kQOffB, P.q_nib + (int64_t)sc.q * kIdxHeads * 64, 2048, &qfull[slot]);
+          ptx::bulk_load(qs + kQOffSFB, P.q_scale + (int64_t)sc.q * kIdxHeads * 4, 128, &qfull[slot]);
         }
-        cur_q = t.q;
+        cur_q = sc.q;
         qsw++;
       }
       const uint32_t s = it % kScStages, r = it / kScStages;
       if (!ptx::mbar_wait(&empty_bar[s], (r & 1) ^ 1)) { fail(); break; }
       unsigned char *st = smem + s * kScStageBytes;
-      const int64_t row0 = (int64_t)t.seq * P.n_max;
+      const int64_t row0 = (int64_t)sc.seq * P.n_max;
       if (P.pool == nullptr) {
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&full_bar[s], 8192 + 512);
-          const int64_t r0 = row0 + (int64_t)t.tile * 128;
-          ptx::bulk_load_hint(st + kOffA, P.key_nib + r0 * 64, 8192, &full_bar[s], policy);
-          ptx::bulk_load(st + kOffSFA, P.key_scale + r0 * 4, 512, &full_bar[s]);
+          // sub-tiles that start before n_vis end within n_max (n_max % 128 == 0)
+          const int nsub = (sc.u * kUnit + 128 < sc.nv) ? 2 : 1;
+          ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)nsub * (8192 + 512));
+          const int64_t r0 = row0 + (int64_t)sc.u * kUnit;
+          ptx::bulk_load_hint(st + kOffA, P.key_nib + r0 * 64, (uint32_t)nsub * 8192, &full_bar[s], policy);
+          ptx::bulk_load(st + kOffSFA, P.key_scale + r0 * 4, (uint32_t)nsub * 512, &full_bar[s]);
         }
       } else {
-        int blk = -1;
-        bool ok = false;
-        if (lane < 16) {
-          blk = __ldg(P.pool + (int64_t)t.q * kPoolBlocks + t.tile * 16 + lane);
-          ok = blk >= 0 && (int64_t)blk * kBlock < P.n_max;
-          if (blk >= 0 && !ok) record_error(P.status, CSA2_ERR_BOUNDS);
-        }
+        const int blk = __ldg(P.pool + (int64_t)sc.q * kPoolBlocks + sc.u * 32 + lane);
+        const bool ok = blk >= 0 && (int64_t)blk * kBlock < P.n_max;
+        if (blk >= 0 && !ok) record_error(P.status, CSA2_ERR_BOUNDS);
         const unsigned m = __ballot_sync(0xFFFFFFFFu, ok);
-        // an all-empty tile still arrives once, so its phase completes
+        // an all-empty unit still arrives once, so its phase completes
         if (lane == 0) ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)__popc(m) * (512 + 32));
         __syncwarp();
         if (ok) {
@@ -191,20 +211,14 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       }
       __syncwarp();
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    int64_t T = blockIdx.x;
-    TileInfo t;
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ scale-factor warp
     int cur_q = -1;
-    uint32_t qsw = 0, slot = 0;
-    const uint32_t idesc0 = idesc_mxf4_m128n32(0), idesc1 = idesc_mxf4_m128n32(2);
-    for (uint32_t it = 0; next_tile(P, T, t); it++) {
+    uint32_t qsw = 0;
+    for (uint32_t it = 0; sc.next(P); it++) {
       if (abort_flag) break;
-      if (t.q != cur_q) {
-        // release the previous query slot once every MMA issued so far is done
-        if (qsw > 0 && lane == 0) ptx::tc_commit(&qempty[(qsw - 1) & 1]);
-        slot = qsw & 1;
-        const uint32_t rnd = qsw >> 1;
+      if (sc.q != cur_q) {
+        const uint32_t slot = qsw & 1, rnd = qsw >> 1;
         if (!ptx::mbar_wait(&qfull[slot], rnd & 1)) { fail(); break; }
         uint32_t *sfb = reinterpret_cast<uint32_t *>(qslots + slot * kScQBytes + kQOffSFB);
         const uint32_t vb = sfb[lane];
@@ -218,36 +232,69 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         if (lane == 0) {
           ptx::tc_fence_after();
           ptx::tc_cp_32x128b_warpx4(tmem + kColSFB + slot * 4, ptx::smem_desc(ptx::smem_u32(sfb), 0, 128, 0));
+          ptx::tc_commit(&qsf[slot]);
         }
-        cur_q = t.q;
+        cur_q = sc.q;
         qsw++;
       }
-      const uint32_t s = it % kScStages, r = it / kScStages, a = it % kScAcc, ra = it / kScAcc;
+      const uint32_t s = it % kScStages, r = it / kScStages;
       if (!ptx::mbar_wait(&full_bar[s], r & 1)) { fail(); break; }
-      unsigned char *st = smem + s * kScStageBytes;
-      // key scales -> tcgen05.cp layout: 16-B line m0 holds rows m0, m0+32, m0+64, m0+96
-      uint32_t *sfa = reinterpret_cast<uint32_t *>(st + kOffSFA);
-      uint32_t va[4];
+      // key scales -> tcgen05.cp layout: 16-B line m0 of sub-tile j holds rows
+      // m0, m0+32, m0+64, m0+96 of that sub-tile
+      uint32_t *sfa = reinterpret_cast<uint32_t *>(smem + s * kScStageBytes + kOffSFA);
+      uint32_t va[8];
 #pragma unroll
-      for (int i = 0; i < 4; i++) va[i] = sfa[i * 32 + lane];
+      for (int i = 0; i < 8; i++) va[i] = sfa[i * 32 + lane];
       __syncwarp();
 #pragma unroll
-      for (int i = 0; i < 4; i++) sfa[lane * 4 + i] = va[i];
+      for (int j = 0; j < 2; j++)
+#pragma unroll
+        for (int i = 0; i < 4; i++) sfa[j * 128 + lane * 4 + i] = va[j * 4 + i];
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        if (!ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) {
-          fail();
-        } else {
+        ptx::tc_fence_after();
+        const uint32_t sa = ptx::smem_u32(sfa);
+        ptx::tc_cp_32x128b_warpx4(tmem + kColSFA + s * 8, ptx::smem_desc(sa, 0, 128, 0));
+        ptx::tc_cp_32x128b_warpx4(tmem + kColSFA + s * 8 + 4, ptx::smem_desc(sa + 512, 0, 128, 0));
+        ptx::tc_commit(&sf_bar[s]);
+      }
+      __syncwarp();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int cur_q = -1;
+    uint32_t qsw = 0, slot = 0;
+    const uint32_t idesc0 = idesc_mxf4_m128n32(0), idesc1 = idesc_mxf4_m128n32(2);
+    for (uint32_t it = 0; sc.next(P); it++) {
+      if (abort_flag) break;
+      if (lane == 0) {
+        if (sc.q != cur_q) {
+          // release the previous query slot once every MMA issued so far is done
+          if (qsw > 0) ptx::tc_commit(&qempty[(qsw - 1) & 1]);
+          slot = qsw & 1;
+          if (!ptx::mbar_wait(&qsf[slot], (qsw >> 1) & 1)) { fail(); }
+          cur_q = sc.q;
+          qsw++;
+        }
+        const uint32_t s = it % kScStages, r = it / kScStages, a = it % kScAcc, ra = it / kScAcc;
+        if (!abort_flag && ptx::mbar_wait(&sf_bar[s], r & 1) && ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) {
           ptx::tc_fence_after();
-          const uint32_t t_sfa = tmem + kColSFA + a * 4, t_sfb = tmem + kColSFB + slot * 4;
-          ptx::tc_cp_32x128b_warpx4(t_sfa, ptx::smem_desc(ptx::smem_u32(sfa), 0, 128, 0));
-          const uint64_t ad = ptx::smem_desc(ptx::smem_u32(st + kOffA), 16, 512, 4);
+          const uint32_t sa = ptx::smem_u32(smem + s * kScStageBytes + kOffA);
           const uint64_t bd = ptx::smem_desc(ptx::smem_u32(qslots + slot * kScQBytes + kQOffB), 16, 512, 4);
-          ptx::tc_mma_mxf4(tmem + a * 32, ad, bd, idesc0, t_sfa, t_sfb, 0u);
-          ptx::tc_mma_mxf4(tmem + a * 32, ad + 2, bd + 2, idesc1, t_sfa, t_sfb, 1u);   // +32 B along K
+          const uint32_t t_sfb = tmem + kColSFB + slot * 4;
+#pragma unroll
+          for (int j = 0; j < 2; j++) {
+            const uint64_t ad = ptx::smem_desc(sa + j * 8192, 16, 512, 4);
+            const uint32_t t_sfa = tmem + kColSFA + s * 8 + j * 4;
+            const uint32_t d = tmem + a * 64 + j * 32;
+            ptx::tc_mma_mxf4(d, ad, bd, idesc0, t_sfa, t_sfb, 0u);
+            ptx::tc_mma_mxf4(d, ad + 2, bd + 2, idesc1, t_sfa, t_sfb, 1u);   // +32 B along K
+          }
           ptx::tc_commit(&empty_bar[s]);
           ptx::tc_commit(&acc_full[a]);
+        } else if (!abort_flag) {
+          fail();
         }
       }
       __syncwarp();
@@ -256,18 +303,16 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
-    const uint32_t group = (uint32_t)(warp - 2) >> 2;     // warps 2..5 -> 0, 6..9 -> 1
+    const uint32_t group = (uint32_t)(warp - 3) >> 2;     // warps 3..6 -> 0, 7..10 -> 1
     const int row = quarter * 32 + lane;
-    int64_t T = blockIdx.x;
-    TileInfo t;
     int cur_q = -1;
     float wv[kIdxHeads];
-    for (uint32_t it = 0; next_tile(P, T, t); it++) {
+    for (uint32_t it = 0; sc.next(P); it++) {
       if (abort_flag) break;
       if ((it & 1) != group) continue;
       const uint32_t a = it % kScAcc, ra = it / kScAcc;
-      if (t.q != cur_q) {
-        const float4 *wp = reinterpret_cast<const float4 *>(P.w + (int64_t)t.q * kIdxHeads);
+      if (sc.q != cur_q) {
+        const float4 *wp = reinterpret_cast<const float4 *>(P.w + (int64_t)sc.q * kIdxHeads);
 #pragma unroll
         for (int i = 0; i < 8; i++) {
           const float4 v = __ldg(wp + i);
@@ -276,27 +321,36 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
           wv[4 * i + 2] = v.z;
           wv[4 * i + 3] = v.w;
         }
-        cur_q = t.q;
+        cur_q = sc.q;
       }
       if (!ptx::mbar_wait(&acc_full[a], ra & 1)) { fail(); break; }
       ptx::tc_fence_after();
-      uint32_t d[32];
-      ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + a * 32, d);
+      uint32_t d0[32], d1[32];
+      const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + a * 64;
+      ptx::tmem_ld_32x32b_x32(ta, d0);
+      ptx::tmem_ld_32x32b_x32(ta + 32, d1);
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&acc_empty[a]);
-      float s = 0.f;
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-      for (int h = 0; h < kIdxHeads; h++) s = fmaf(wv[h], fmaxf(__uint_as_float(d[h]), 0.f), s);
-      const int64_t item = (int64_t)t.tile * 128 + row;
+      for (int h = 0; h < kIdxHeads; h++) {
+        s0 = fmaf(wv[h], fmaxf(__uint_as_float(d0[h]), 0.f), s0);
+        s1 = fmaf(wv[h], fmaxf(__uint_as_float(d1[h]), 0.f), s1);
+      }
+      float *out = P.scores + (int64_t)sc.q * P.stride;
+      const int64_t i0 = (int64_t)sc.u * kUnit + row, i1 = i0 + 128;
       if (P.pool == nullptr) {
-        if (item < t.nv) P.scores[(int64_t)t.q * P.stride + item] = s;
+        if (i0 < sc.nv) out[i0] = s0;
+        if (i1 < sc.nv) out[i1] = s1;
       } else {
-        const int blk = __ldg(P.pool + (int64_t)t.q * kPoolBlocks + (item >> 3));
-        const int64_t j = (int64_t)blk * kBlock + (item & 7);
-        const bool ok = blk >= 0 && (int64_t)blk * kBlock < P.n_max && j < t.nv;
-        P.scores[(int64_t)t.q * P.stride + item] = ok ? s : -INFINITY;
+        const int32_t *pl = P.pool + (int64_t)sc.q * kPoolBlocks;
+        const int b0 = __ldg(pl + (i0 >> 3)), b1 = __ldg(pl + (i1 >> 3));
+        const bool ok0 = b0 >= 0 && (int64_t)b0 * kBlock < P.n_max && (int64_t)b0 * kBlock + (i0 & 7) < sc.nv;
+        const bool ok1 = b1 >= 0 && (int64_t)b1 * kBlock < P.n_max && (int64_t)b1 * kBlock + (i1 & 7) < sc.nv;
+        out[i0] = ok0 ? s0 : -INFINITY;
+        out[i1] = ok1 ? s1 : -INFINITY;
       }
     }
   }
@@ -336,8 +390,8 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
   P.n_max = n_max;
   P.n_seq = n_seq;
   P.n_q = n_q;
-  P.tiles_per_q = pool ? kPoolSlots / 128 : (int)(n_max / 128);
-  P.total_tiles = (int64_t)n_q * P.tiles_per_q;
+  P.units_per_q = pool ? kPoolSlots / kUnit : (int)((n_max + kUnit - 1) / kUnit);
+  const int64_t total_units = (int64_t)n_q * P.units_per_q;
   P.status = status;
   const size_t smem = (size_t)kScSmem + 1024;
   int dev = 0;
@@ -348,7 +402,7 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const int64_t grid = P.total_tiles < sm_count() ? P.total_tiles : sm_count();
+  const int64_t grid = total_units < sm_count() ? total_units : sm_count();
   index_score_tc_kernel<<<(unsigned)grid, kScThreads, smem, st>>>(P);
   return cudaGetLastError();
 }
