@@ -22,7 +22,7 @@ STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED", 3:
 
 EXPORTS = ["csa2_default_params", "csa2_entry_bytes", "csa2_status_string", "csa2_fp4_pack",
            "csa2_index_score", "csa2_topk", "csa2_sparse_attn", "csa2_workspace_size",
-           "csa2_get_device_status"]
+           "csa2_get_device_status", "csa2_topk_noalloc"]
 
 
 class CSA2Error(RuntimeError):
@@ -58,6 +58,7 @@ def load(path: str = LIB_PATH):
         "csa2_fp4_pack": (i32, [i32, P, i64, i32, P, P, P, P]),
         "csa2_index_score": (i32, [P, P, i64, i32, P, P, P, P, P, i32, P, P, i64, PP, P]),
         "csa2_topk": (i32, [P, i64, i32, P, i64, i32, i32, P, P, P, sz, P]),
+        "csa2_topk_noalloc": (i32, [P, i64, i32, P, i64, i32, i32, P, P, P]),
         "csa2_sparse_attn": (i32, [P, P, i64, i32, P, i32, P, i32, P, P, P, P, i32, P, i32, PP, P, sz, P]),
         "csa2_workspace_size": (i32, [i32, i32, i64, i32, ctypes.POINTER(sz)]),
         "csa2_get_device_status": (i32, [P, ctypes.POINTER(i32)]),
@@ -125,6 +126,13 @@ def csa2_topk(scores, score_stride, n_q, n_valid, n_max, k, block, pool_blocks, 
     _check("csa2_topk", load().csa2_topk(_ptr(scores), int(score_stride), int(n_q), _ptr(n_valid), int(n_max), int(k),
                                          int(block), _ptr(pool_blocks), _ptr(out), _ptr(workspace),
                                          int(workspace_bytes), _stream(stream)))
+
+
+def csa2_topk_noalloc(scores, score_stride, n_q, n_valid, n_max, k, block, pool_blocks, out, stream=None):
+    """csa2_topk without a workspace argument (scratch is a fixed array inside the library)."""
+    _check("csa2_topk_noalloc", load().csa2_topk_noalloc(_ptr(scores), int(score_stride), int(n_q), _ptr(n_valid),
+                                                         int(n_max), int(k), int(block), _ptr(pool_blocks), _ptr(out),
+                                                         _stream(stream)))
 
 
 def csa2_sparse_attn(q, kv_cache, n_max, n_seq, sel, sel_stride, swa_cache, swa_cap, q_seq, pos, swa_first, swa_cnt,

@@ -39,6 +39,9 @@ static int *status_ptr() {
   return ptrs[dev];
 }
 
+// The status word's device address for entry points defined in other files.
+int *status_word_ptr() { return status_ptr(); }
+
 static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 static bool params_ok(const csa2_params *p) {

@@ -237,6 +237,33 @@ csa2_status csa2_sparse_attn(const void *q, const void *kv_cache, int64_t n_max,
 csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t *bytes);
 
 /*
+ * csa2_topk_noalloc -- csa2_topk for callers that cannot allocate device
+ * memory: code running where cudaMalloc is not available or not allowed (inside
+ * a host callback or another library's allocation-free region, a plugin whose
+ * host owns all device memory, a process that must not grow its footprint after
+ * start-up).  The pages have no counterpart of this call: it exists only for
+ * the library's users.
+ *
+ * Same arguments, results and errors as csa2_topk, without the workspace.  The
+ * scratch it needs (4 bytes per group of scores, for rows longer than 16,384
+ * items; for 1,048,576-entry rows and k = 512 that is 32 KiB per query) lives in
+ * one fixed device array of CSA2_TOPK_NOALLOC_SCRATCH_BYTES (1 MiB) that every
+ * GPU which loads the library holds until the process exits.  A call whose
+ * scratch would exceed it returns CSA2_ERR_WORKSPACE and launches nothing (use
+ * csa2_topk with a workspace instead).  The call allocates nothing and calls no
+ * allocating routine.  The first call on a device looks up the array's device
+ * address on that device; make that first call before any stream capture.
+ * All calls share the one array: calls that can run at the same time on the
+ * GPU (other streams, other host threads) race and must be serialised by the
+ * caller.  Nothing has to be cleared between calls: every scratch value a call
+ * reads is written earlier in that same call.
+ */
+#define CSA2_TOPK_NOALLOC_SCRATCH_BYTES (1u << 20)
+csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stride, int n_q, const int32_t *n_valid,
+                              int64_t n_max, int k, int block, const int32_t *pool_blocks, int32_t *out,
+                              csa2_stream_t stream);
+
+/*
  * csa2_get_device_status -- synchronises `stream`, returns in *out the first
  * device-side error recorded by any kernel of this library on the current
  * device since the last call (CSA2_OK if none), and clears it.
