@@ -25,9 +25,9 @@
 // finishes the output (normalise, un-rotate, store), otherwise it writes
 // (O, m, l) partials that attn_merge_kernel combines.
 //
-// 256 threads: all of them gather/dequantise; warps 0-3 (TMEM lane quarters)
-// run the softmax on S^T rows; thread 0 issues the MMAs; all 8 warps share the
-// final read-out of the 5 x 64 accumulator columns.
+// 256 threads: all of them gather/dequantise and run the softmax (warp w reads
+// TMEM lane quarter w%4, heads 32*(w/4) ..); thread 0 issues the MMAs; all 8
+// warps share the final read-out of the 5 x 64 accumulator columns.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -54,6 +54,25 @@ constexpr uint32_t kAttTmemCols = 512;
 constexpr uint32_t kColS = 0;                   // S^T: 64 columns
 constexpr uint32_t kColO = 64;                  // O^T: 5 blocks x 64 columns (block 4 = denominators)
 constexpr float kRescaleLog2 = 8.0f;
+
+// Eight E2M1 codes (one per nibble of w, channel i in nibble i) -> eight bf16
+// values as four bf16x2 words, by table lookups with __byte_perm: the high and
+// low bytes of the bf16 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}, then the sign.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t (&out)[4]) {
+#pragma unroll
+  for (int hw = 0; hw < 2; hw++) {
+    const uint32_t n = w >> (16 * hw);               // nibbles of channels 4hw .. 4hw+3
+    const uint32_t sel = n & 0x7777u;
+    const uint32_t hi = __byte_perm(0x3F3F3F00u, 0x40404040u, sel);
+    const uint32_t lo = __byte_perm(0xC0800000u, 0xC0804000u, sel);
+    uint32_t a = __byte_perm(lo, hi, 0x5140u);       // channels 4hw, 4hw+1
+    uint32_t b = __byte_perm(lo, hi, 0x7362u);       // channels 4hw+2, 4hw+3
+    a |= ((n << 12) & 0x8000u) | ((n << 24) & 0x80000000u);
+    b |= ((n << 4) & 0x8000u) | ((n << 16) & 0x80000000u);
+    out[2 * hw] = a;
+    out[2 * hw + 1] = b;
+  }
+}
 
 // byte offset of 16-B chunk `ch` (0..7) in row r of a 128B-swizzled 1024-B atom
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t ch) { return r * 128u + ((ch ^ (r & 7u)) << 4); }
@@ -183,19 +202,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
           for (int v = 0; v < 8; v++) nbv[v] = __ldg(reinterpret_cast<const uint4 *>(rec + half * 128 + v * 16));
 #pragma unroll
           for (int v = 0; v < 8; v++) {               // 16-B nibble load = 32 dims
-            const uint4 nb = nbv[v];
-            const uint32_t nw[4] = {nb.x, nb.y, nb.z, nb.w};
+            const uint32_t nw[4] = {nbv[v].x, nbv[v].y, nbv[v].z, nbv[v].w};
 #pragma unroll
             for (int u = 0; u < 4; u++) {             // 8 dims per word -> one 16-B smem chunk
               const int d0 = half * 256 + v * 32 + u * 8;
               const int g = (d0 >> 4) - half * 16;    // scale group within this half (0..15)
-              const float s = e4m3_to_float((sc4[g >> 2] >> (8 * (g & 3))) & 0xFFu) * 0.5f;
+              const __nv_bfloat16 sb = __float2bfloat16_rn(e4m3_to_float((sc4[g >> 2] >> (8 * (g & 3))) & 0xFFu));
+              const __nv_bfloat162 s2 = __halves2bfloat162(sb, sb);
               uint32_t pk[4];
+              e2m1x8_to_bf16(nw[u], pk);
 #pragma unroll
               for (int b = 0; b < 4; b++) {
-                const float lo = (float)e2m1_x2((nw[u] >> (8 * b)) & 15u) * s;
-                const float hi = (float)e2m1_x2((nw[u] >> (8 * b + 4)) & 15u) * s;
-                pk[b] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+                __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&pk[b]);
+                x = __hmul2(x, s2);                   // exact: <= 6 significant bits, in range
+                pk[b] = *reinterpret_cast<uint32_t *>(&x);
               }
               const uint32_t off = rowbase + (d0 >> 6) * 1024 + sw128(e & 7, (d0 >> 3) & 7);
               *reinterpret_cast<uint4 *>(sm + kSmK + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -260,56 +280,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       }
       ptx::tc_commit(&bar_s);
     }
-    // ---------------------------------------------------------- softmax (warps 0-3)
-    if (warp < 4) {
+    // ---------------------------------------------------------- softmax (all 8 warps)
+    // warp w: TMEM lane quarter w%4 (entries 32*(w%4) ..), heads 32*(w/4) .. +31
+    {
+      const int quarter = warp & 3, hb = (warp >> 2) * 32;
       if (!ptx::mbar_wait(&bar_s, phase)) { record_error(A.status, CSA2_ERR_TIMEOUT); bad_sh = 1; }
       ptx::tc_fence_after();
-      const int e = warp * 32 + lane;                  // TMEM lane = entry
-      const uint32_t s_addr = tmem + ((uint32_t)(warp * 32) << 16) + kColS;
+      const int e = quarter * 32 + lane;               // TMEM lane = entry
+      const uint32_t s_addr = tmem + ((uint32_t)(quarter * 32) << 16) + kColS + hb;
       const bool ev = valid_sh[e] != 0;
-      // per-head max over the warp's 32 entries: transpose-reduce, 62 shuffles;
-      // afterwards lane L holds the max of heads base(L) and base(L)+1 in v[0], v[1]
-      float v[64];
+      // per-head max over the warp's 32 entries: transpose-reduce in 31
+      // shuffles; afterwards lane L holds the max of head hb + L
+      float v[32];
       {
-        uint32_t r0[32], r1[32];
-        ptx::tmem_ld_32x32b_x32(s_addr, r0);
-        ptx::tmem_ld_32x32b_x32(s_addr + 32, r1);
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(s_addr, r);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; h++) {
-          v[h] = ev ? __uint_as_float(r0[h]) * A.scale_log2 : -INFINITY;
-          v[h + 32] = ev ? __uint_as_float(r1[h]) * A.scale_log2 : -INFINITY;
-        }
+        for (int h = 0; h < 32; h++) v[h] = ev ? __uint_as_float(r[h]) * A.scale_log2 : -INFINITY;
       }
 #pragma unroll
-      for (int w = 32; w >= 2; w >>= 1) {              // w = values kept after this step
-        const int o = w >> 1;                           // partner distance in lanes: 16, 8, 4, 2, 1
-        const bool upper = (lane & o) != 0;
+      for (int w = 16; w >= 1; w >>= 1) {              // w = values kept, partner distance w
+        const bool upper = (lane & w) != 0;
 #pragma unroll
-        for (int i = 0; i < 64; i++) {
+        for (int i = 0; i < 16; i++) {
           if (i < w) {
-            // keep the half of indices selected by this lane's bit; send the other half
             const float mine = upper ? v[i + w] : v[i];
             const float send = upper ? v[i] : v[i + w];
-            const float got = __shfl_xor_sync(0xFFFFFFFFu, send, o);
-            v[i] = fmaxf(mine, got);
+            v[i] = fmaxf(mine, __shfl_xor_sync(0xFFFFFFFFu, send, w));
           }
         }
       }
-      // lane L now holds, for i in {0, 1}, the max over the warp of head
-      // index  h = (bits of L reversed into the halving order) -- computed below
-      {
-        // recover the head indices kept by this lane: at step with partner
-        // distance o (16..1) the upper lane kept the upper half of the w values
-        int base = 0, w = 64;
-        for (int o = 16; o >= 1; o >>= 1) {
-          w >>= 1;
-          if (lane & o) base += w;
-        }
-        red[warp][base] = v[0];
-        red[warp][base + 1] = v[1];
-      }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      red[quarter][hb + lane] = v[0];
+      __syncthreads();
       if (t < kHeads) {
         const float cm = fmaxf(fmaxf(red[0][t], red[1][t]), fmaxf(red[2][t], red[3][t]));
         const float mo = m_ref[t];
@@ -320,7 +323,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
         }
         alpha_sh[t] = al;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      __syncthreads();
       if (t == 0) {
         int rs = 0;
         for (int h = 0; h < kHeads; h++) rs |= (alpha_sh[h] != 1.f && alpha_sh[h] != 0.f) ? 1 : 0;
@@ -330,22 +333,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       // S is read from TMEM again rather than kept live through the reduction
       const uint32_t pe = (e >> 6) * 1024;             // entry atom
       const uint32_t pcol = (uint32_t)(e & 63) * 2;    // byte within the 128-B row
+      uint32_t r[32];
+      ptx::tmem_ld_32x32b_x32(s_addr, r);
+      ptx::tmem_wait_ld();
 #pragma unroll
-      for (int hh = 0; hh < 2; hh++) {
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(s_addr + hh * 32, r);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; i++) {
-          const int h = hh * 32 + i;
-          const float l2 = __uint_as_float(r[i]) * A.scale_log2;
-          const float p = ev ? exp2f(l2 - m_ref[h]) : 0.f;
-          const __nv_bfloat16 ph = __float2bfloat16_rn(p);
-          const __nv_bfloat16 pl = __float2bfloat16_rn(p - __bfloat162float(ph));
-          const uint32_t off = (h >> 3) * 2048 + pe + sw128(h & 7, pcol >> 4) + (pcol & 15);
-          *reinterpret_cast<__nv_bfloat16 *>(sm + kSmPhi + off) = ph;
-          *reinterpret_cast<__nv_bfloat16 *>(sm + kSmPlo + off) = pl;
-        }
+      for (int i = 0; i < 32; i++) {
+        const int h = hb + i;
+        const float l2 = __uint_as_float(r[i]) * A.scale_log2;
+        const float p = ev ? exp2f(l2 - m_ref[h]) : 0.f;
+        const __nv_bfloat16 ph = __float2bfloat16_rn(p);
+        const __nv_bfloat16 pl = __float2bfloat16_rn(p - __bfloat162float(ph));
+        const uint32_t off = (h >> 3) * 2048 + pe + sw128(h & 7, pcol >> 4) + (pcol & 15);
+        *reinterpret_cast<__nv_bfloat16 *>(sm + kSmPhi + off) = ph;
+        *reinterpret_cast<__nv_bfloat16 *>(sm + kSmPlo + off) = pl;
       }
       ptx::tc_fence_before();
     }

@@ -201,6 +201,69 @@ __device__ void select_and_write(Get get, int64_t n, int n_valid_items, int k, i
   for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < take ? sel[i] : -1;
 }
 
+// Descending bitonic sort of n_pow2 64-bit keys in shared memory.
+__device__ void bitonic_sort_desc_u64(uint64_t *a, int n_pow2) {
+  for (int size = 2; size <= n_pow2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n_pow2; i += blockDim.x) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool desc = (i & size) == 0;
+          const uint64_t x = a[i], y = a[j];
+          if ((x < y) == desc) { a[i] = y; a[j] = x; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Exact top-k of n unique keys already in shared memory (capacity >= the next
+// power of two of n), by sorting them: cheaper than radix passes for small n.
+// The keys array is reordered.
+__device__ void select_small(uint64_t *keys, int n, int k, int32_t *out, int32_t *sel) {
+  int np2 = 1;
+  while (np2 < n) np2 <<= 1;
+  for (int i = n + threadIdx.x; i < np2; i += blockDim.x) keys[i] = 0;   // below every valid key
+  __syncthreads();
+  bitonic_sort_desc_u64(keys, np2);
+  const int take = min(k, n);
+  int sp2 = 1;
+  while (sp2 < take) sp2 <<= 1;
+  for (int i = threadIdx.x; i < sp2; i += blockDim.x)
+    sel[i] = i < take ? (int32_t)(~(uint32_t)(keys[i] & 0xFFFFFFFFu)) : INT32_MAX;
+  __syncthreads();
+  bitonic_sort(sel, sp2);
+  for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < take ? sel[i] : -1;
+}
+
+constexpr int kSortMax = 4096;     // sets up to this size are selected by sorting
+constexpr int kRankMax = 1536;     // sets up to this size are selected by ranking
+
+// Exact top-k of n unique keys in shared memory by counting: a key is selected
+// iff fewer than k keys are larger; its output slot is the number of selected
+// keys with a smaller index.  O(n^2) comparisons, two barriers.
+__device__ void select_rank(const uint64_t *keys, int n, int k, int32_t *out, int32_t *sel) {
+  const int take = min(k, n);
+  __shared__ int n_sel;
+  if (threadIdx.x == 0) n_sel = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint64_t ki = keys[i];
+    int above = 0;
+    for (int j = 0; j < n; j++) above += keys[j] > ki;
+    if (above < take) sel[atomicAdd(&n_sel, 1)] = (int32_t)(~(uint32_t)(ki & 0xFFFFFFFFu));
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < take; i += blockDim.x) {
+    const int32_t xi = sel[i];
+    int before = 0;
+    for (int j = 0; j < take; j++) before += sel[j] < xi;
+    out[before] = xi;
+  }
+  for (int i = take + threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
+}
+
 // ---------------------------------------------------------------- direct path
 __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, int k, int32_t *__restrict__ out,
                                                                     int *status) {
@@ -226,8 +289,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
   }
   __syncthreads();
   const int n = n_keys;
-  auto get = [&](int64_t i, uint64_t &key) { key = keys[i]; return true; };
-  select_and_write(get, n, n, k, out + (int64_t)q * k, sh, sel);
+  if (n <= kRankMax) {
+    select_rank(keys, n, k, out + (int64_t)q * k, sel);
+  } else if (n <= kSortMax) {
+    select_small(keys, n, k, out + (int64_t)q * k, sel);
+  } else {
+    auto get = [&](int64_t i, uint64_t &key) { key = keys[i]; return true; };
+    select_and_write(get, n, n, k, out + (int64_t)q * k, sh, sel);
+  }
 }
 
 // ---------------------------------------------------------------- long rows
@@ -247,8 +316,10 @@ __global__ void __launch_bounds__(256) topk_groupmax_kernel(TopkSrc S, int G, in
   for (int64_t w = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); w < n_steps; w += (int64_t)gridDim.x * warps) {
     uint32_t m = 0;
     const int64_t i0 = w * span + (int64_t)lane * ipl;
-    if (ipl == 4 && S.block == 1 && S.pool == nullptr && i0 + 4 <= nv) {
-      const float4 v = __ldg(reinterpret_cast<const float4 *>(S.scores + (int64_t)q * S.stride + i0));
+    const float *rowp = S.scores + (int64_t)q * S.stride;
+    if (ipl == 4 && S.block == 1 && S.pool == nullptr && i0 + 4 <= nv &&
+        ((reinterpret_cast<uintptr_t>(rowp + i0) & 15u) == 0)) {
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(rowp + i0));
       m = max(max(order_key(v.x), order_key(v.y)), max(order_key(v.z), order_key(v.w)));
     } else {
       for (int u = 0; u < ipl; u++) {
@@ -263,12 +334,13 @@ __global__ void __launch_bounds__(256) topk_groupmax_kernel(TopkSrc S, int G, in
 }
 
 // k-th largest of n 32-bit values (counted with multiplicity; requires at
-// least k valid values): four 8-bit radix passes narrowing a prefix.
+// least k valid values): 8-bit radix passes narrowing a prefix, down to bit
+// min_shift (the lower bits of the result are zero).
 template <class Get>
-__device__ uint32_t radix_kth_u32(Get get, int n, int k, SelectShared &sh) {
+__device__ uint32_t radix_kth_u32(Get get, int n, int k, SelectShared &sh, int min_shift = 0) {
   uint32_t prefix = 0, mask = 0;
   int rem = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  for (int shift = 24; shift >= min_shift; shift -= 8) {
     block_hist(sh, n, [&](int64_t i, uint32_t &d) {
       uint32_t v;
       if (!get((int)i, v) || (v & mask) != prefix) return false;
@@ -326,7 +398,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_group_select_kernel(TopkSrc
   uint32_t T = 1;                                    // nonzero keys: every valid item
   if (n_valid_groups > k) {
     auto get = [&](int i, uint32_t &v) { v = gm[i]; return v != 0; };
-    T = radix_kth_u32(get, n_groups, k, sh);
+    // the k-th largest group maximum to 16-bit resolution: its upper 16 bits
+    // (lower bits zero) are still a lower bound of the k-th best key
+    T = radix_kth_u32(get, n_groups, k, sh, 16);
   }
   // list the groups whose maximum reaches T
   for (int b0 = 0; b0 < n_groups; b0 += blockDim.x) {
@@ -345,6 +419,49 @@ __global__ void __launch_bounds__(kTopkThreads) topk_group_select_kernel(TopkSrc
   const int total = n_list << lg;
   const bool plain = S.pool == nullptr && S.block == 1;
   const float *row = S.scores + (int64_t)q * S.stride;
+  const bool row16 = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  if (plain) {
+    // four consecutive items per thread and load (G is a multiple of 4)
+    constexpr int kV = 4;
+    for (int b0 = 0; b0 < total; b0 += 4 * kV * blockDim.x) {
+      float4 sc[kV];
+      int64_t base[kV];
+#pragma unroll
+      for (int u = 0; u < kV; u++) {
+        const int f = b0 + 4 * (u * blockDim.x + threadIdx.x);
+        base[u] = -1;
+        sc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (f < total) {
+          base[u] = ((int64_t)glist[f >> lg] << lg) + (f & (G - 1));
+          if (row16 && base[u] + 4 <= nv) {
+            sc[u] = __ldg(reinterpret_cast<const float4 *>(row + base[u]));
+          } else {                                   // ragged end or unaligned row: element loads
+            const int64_t b = base[u];
+            if (b < nv) sc[u].x = __ldg(row + b);
+            if (b + 1 < nv) sc[u].y = __ldg(row + b + 1);
+            if (b + 2 < nv) sc[u].z = __ldg(row + b + 2);
+            if (b + 3 < nv) sc[u].w = __ldg(row + b + 3);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kV; u++) {
+        const float vals[4] = {sc[u].x, sc[u].y, sc[u].z, sc[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const int64_t i = base[u] + e;
+          uint32_t kk = 0;
+          const bool ok = base[u] >= 0 && i < nv && (kk = order_key(vals[e])) >= T;
+          if (!__any_sync(0xFFFFFFFFu, ok)) continue;   // most rounds have no candidate
+          const unsigned b = __ballot_sync(0xFFFFFFFFu, ok);
+          int pos0 = 0;
+          if (lane == 0 && b) pos0 = atomicAdd(&n_cand, __popc(b));
+          pos0 = __shfl_sync(0xFFFFFFFFu, pos0, 0) + __popc(b & ((1u << lane) - 1u));
+          if (ok && pos0 < kCandCap) cand[pos0] = ((uint64_t)kk << 32) | (uint32_t)(~(uint32_t)i);
+        }
+      }
+    }
+  } else
   for (int b0 = 0; b0 < total; b0 += kScanU * blockDim.x) {
     uint64_t key[kScanU];
     bool v[kScanU];
@@ -366,6 +483,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_group_select_kernel(TopkSrc
 #pragma unroll
     for (int u = 0; u < kScanU; u++) {
       const bool ok = v[u] && (uint32_t)(key[u] >> 32) >= T;
+      if (!__any_sync(0xFFFFFFFFu, ok)) continue;
       const unsigned b = __ballot_sync(0xFFFFFFFFu, ok);
       int base = 0;
       if (lane == 0 && b) base = atomicAdd(&n_cand, __popc(b));
@@ -375,7 +493,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_group_select_kernel(TopkSrc
   }
   __syncthreads();
   const int nc = n_cand;
-  if (nc <= kCandCap) {
+  if (nc <= kRankMax) {
+    select_rank(cand, nc, k, out + (int64_t)q * k, sel);
+  } else if (nc <= kSortMax) {
+    select_small(cand, nc, k, out + (int64_t)q * k, sel);
+  } else if (nc <= kCandCap) {
     auto get = [&](int64_t i, uint64_t &key) { key = cand[i]; return true; };
     select_and_write(get, nc, nc, k, out + (int64_t)q * k, sh, sel);
   } else {

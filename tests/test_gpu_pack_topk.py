@@ -117,6 +117,22 @@ def test_topk_bit_exact(lib, oracle_lib, n, levels, k):
         assert np.array_equal(got[i], want), i
 
 
+def test_topk_long_rows_odd_stride(lib, oracle_lib):
+    """Row starts not 16-B aligned and ragged lengths: element-wise loads."""
+    n, stride = 70_001, 70_003
+    base = np.stack([G.uniform_f32_scores(95 + i, 1, stride, 0) for i in range(3)])
+    scores = torch.from_numpy(np.ascontiguousarray(base, np.float32)).cuda()
+    nv = torch.tensor([n, n - 2, 65_537], dtype=torch.int32, device="cuda")
+    out = torch.empty((3, 512), dtype=torch.int32, device="cuda")
+    wsb = lib.csa2_workspace_size(lib.CSA2_OP_TOPK, 3, n, 512)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+    lib.csa2_topk(scores, stride, 3, nv, n, 512, 1, None, out, ws, wsb)
+    assert lib.csa2_get_device_status() == 0
+    got = out.cpu().numpy()
+    for i, m in enumerate([n, n - 2, 65_537]):
+        assert np.array_equal(got[i], oracle_lib.topk(base[i, :m].astype(np.float64), 512))
+
+
 def test_topk_all_equal_row_uses_exact_fallback(lib, oracle_lib):
     n = 200_000                                            # candidates overflow the filter buffer
     rows = np.zeros((2, n), np.float32)
