@@ -37,19 +37,22 @@
 
 namespace csa2 {
 
-constexpr int kScStages = 12;
-constexpr int kUnit = 256;                // entries per work unit (two 128-row sub-tiles)
-constexpr int kScStageBytes = 17408;      // 16 KB nibbles + 1 KB scales
+constexpr int kScStages = 6;
+constexpr int kSub = 4;                   // 128-row sub-tiles per work unit
+constexpr int kUnit = kSub * 128;         // entries per work unit
+constexpr int kScStageBytes = kSub * (8192 + 512);   // nibbles + scales
 constexpr int kOffA = 0;                  // sub-tile j at j * 8192: 128 rows x 64 B, 64B-swizzled as stored
-constexpr int kOffSFA = 16384;            // 2 x 512 B key scales: staged [row][4], rearranged in place
+constexpr int kOffSFA = kSub * 8192;      // kSub x 512 B key scales: staged [row][4], rearranged in place
 constexpr int kScQBytes = 2560;           // per query slot: 32 x 64 B nibbles + 512 B scales
 constexpr int kQOffB = 0, kQOffSFB = 2048;
 constexpr int kScSmem = kScStages * kScStageBytes + 2 * kScQBytes;
 constexpr int kScThreads = 352;
-constexpr int kScAcc = 4;                 // TMEM accumulator stages (64 columns each)
+constexpr int kScAcc = 2;                 // TMEM accumulators (kSub x 32 columns each), one per epilogue group
 constexpr uint32_t kScTmemCols = 512;
-constexpr uint32_t kColSFA = 256;         // per stage: 2 sub-tiles x 4 columns
-constexpr uint32_t kColSFB = 256 + kScStages * 8;   // per query slot: 4 columns
+constexpr uint32_t kColSFA = kScAcc * kSub * 32;              // per stage: kSub x 4 columns
+constexpr uint32_t kColSFB = kColSFA + kScStages * kSub * 4;  // per query slot: 4 columns
+static_assert(kColSFB + 8 <= kScTmemCols, "TMEM columns");
+static_assert(kScStages % kScAcc == 0, "a stage's done barrier also marks its accumulator full");
 
 // Instruction descriptor of kind::mxf4 block-scaled MMA, M=128, N=32, both
 // operands E2M1 and K-major, UE8M0 scales; sf_id picks the scale byte pair.
@@ -126,8 +129,10 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(sc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char *qslots = smem + kScStages * kScStageBytes;
-  __shared__ __align__(8) uint64_t full_bar[kScStages], sf_bar[kScStages], empty_bar[kScStages];
-  __shared__ __align__(8) uint64_t acc_full[kScAcc], acc_empty[kScAcc], qfull[2], qempty[2], qsf[2];
+  // done_bar[s]: the MMAs of the unit in stage s have completed, so the stage
+  // may be refilled and the unit's accumulator may be read (one commit serves both)
+  __shared__ __align__(8) uint64_t full_bar[kScStages], sf_bar[kScStages], done_bar[kScStages];
+  __shared__ __align__(8) uint64_t acc_empty[kScAcc], qfull[2], qempty[2], qsf[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
@@ -136,12 +141,9 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     for (int s = 0; s < kScStages; s++) {
       ptx::mbar_init(&full_bar[s], 1);
       ptx::mbar_init(&sf_bar[s], 1);
-      ptx::mbar_init(&empty_bar[s], 1);
+      ptx::mbar_init(&done_bar[s], 1);
     }
-    for (int a = 0; a < kScAcc; a++) {
-      ptx::mbar_init(&acc_full[a], 1);
-      ptx::mbar_init(&acc_empty[a], 4);
-    }
+    for (int a = 0; a < kScAcc; a++) ptx::mbar_init(&acc_empty[a], 4);
     for (int q = 0; q < 2; q++) {
       ptx::mbar_init(&qfull[q], 1);
       ptx::mbar_init(&qempty[q], 1);
@@ -183,30 +185,39 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         qsw++;
       }
       const uint32_t s = it % kScStages, r = it / kScStages;
-      if (!ptx::mbar_wait(&empty_bar[s], (r & 1) ^ 1)) { fail(); break; }
+      if (!ptx::mbar_wait(&done_bar[s], (r & 1) ^ 1)) { fail(); break; }
       unsigned char *st = smem + s * kScStageBytes;
       const int64_t row0 = (int64_t)sc.seq * P.n_max;
       if (P.pool == nullptr) {
         if (lane == 0) {
           // sub-tiles that start before n_vis end within n_max (n_max % 128 == 0)
-          const int nsub = (sc.u * kUnit + 128 < sc.nv) ? 2 : 1;
+          const int left = sc.nv - sc.u * kUnit;
+          const int nsub = left >= kUnit ? kSub : (left + 127) >> 7;
           ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)nsub * (8192 + 512));
           const int64_t r0 = row0 + (int64_t)sc.u * kUnit;
           ptx::bulk_load_hint(st + kOffA, P.key_nib + r0 * 64, (uint32_t)nsub * 8192, &full_bar[s], policy);
           ptx::bulk_load(st + kOffSFA, P.key_scale + r0 * 4, (uint32_t)nsub * 512, &full_bar[s]);
         }
       } else {
-        const int blk = __ldg(P.pool + (int64_t)sc.q * kPoolBlocks + sc.u * 32 + lane);
-        const bool ok = blk >= 0 && (int64_t)blk * kBlock < P.n_max;
-        if (blk >= 0 && !ok) record_error(P.status, CSA2_ERR_BOUNDS);
-        const unsigned m = __ballot_sync(0xFFFFFFFFu, ok);
+        // kUnit / 8 gathered 8-entry blocks, two per lane
+        const int32_t *pl = P.pool + (int64_t)sc.q * kPoolBlocks + sc.u * (kUnit / kBlock);
+        const int blk0 = __ldg(pl + lane), blk1 = __ldg(pl + 32 + lane);
+        const bool ok0 = blk0 >= 0 && (int64_t)blk0 * kBlock < P.n_max;
+        const bool ok1 = blk1 >= 0 && (int64_t)blk1 * kBlock < P.n_max;
+        if ((blk0 >= 0 && !ok0) || (blk1 >= 0 && !ok1)) record_error(P.status, CSA2_ERR_BOUNDS);
+        const int n_ok = __popc(__ballot_sync(0xFFFFFFFFu, ok0)) + __popc(__ballot_sync(0xFFFFFFFFu, ok1));
         // an all-empty unit still arrives once, so its phase completes
-        if (lane == 0) ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)__popc(m) * (512 + 32));
+        if (lane == 0) ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)n_ok * (512 + 32));
         __syncwarp();
-        if (ok) {
-          const int64_t r0 = row0 + (int64_t)blk * kBlock;
+        if (ok0) {
+          const int64_t r0 = row0 + (int64_t)blk0 * kBlock;
           ptx::bulk_load_hint(st + kOffA + lane * 512, P.key_nib + r0 * 64, 512, &full_bar[s], policy);
           ptx::bulk_load(st + kOffSFA + lane * 32, P.key_scale + r0 * 4, 32, &full_bar[s]);
+        }
+        if (ok1) {
+          const int64_t r0 = row0 + (int64_t)blk1 * kBlock;
+          ptx::bulk_load_hint(st + kOffA + (32 + lane) * 512, P.key_nib + r0 * 64, 512, &full_bar[s], policy);
+          ptx::bulk_load(st + kOffSFA + (32 + lane) * 32, P.key_scale + r0 * 4, 32, &full_bar[s]);
         }
       }
       __syncwarp();
@@ -242,12 +253,12 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       // key scales -> tcgen05.cp layout: 16-B line m0 of sub-tile j holds rows
       // m0, m0+32, m0+64, m0+96 of that sub-tile
       uint32_t *sfa = reinterpret_cast<uint32_t *>(smem + s * kScStageBytes + kOffSFA);
-      uint32_t va[8];
+      uint32_t va[4 * kSub];
 #pragma unroll
-      for (int i = 0; i < 8; i++) va[i] = sfa[i * 32 + lane];
+      for (int i = 0; i < 4 * kSub; i++) va[i] = sfa[i * 32 + lane];
       __syncwarp();
 #pragma unroll
-      for (int j = 0; j < 2; j++)
+      for (int j = 0; j < kSub; j++)
 #pragma unroll
         for (int i = 0; i < 4; i++) sfa[j * 128 + lane * 4 + i] = va[j * 4 + i];
       ptx::fence_proxy_async_smem();
@@ -255,53 +266,55 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       if (lane == 0) {
         ptx::tc_fence_after();
         const uint32_t sa = ptx::smem_u32(sfa);
-        ptx::tc_cp_32x128b_warpx4(tmem + kColSFA + s * 8, ptx::smem_desc(sa, 0, 128, 0));
-        ptx::tc_cp_32x128b_warpx4(tmem + kColSFA + s * 8 + 4, ptx::smem_desc(sa + 512, 0, 128, 0));
+#pragma unroll
+        for (int j = 0; j < kSub; j++)
+          ptx::tc_cp_32x128b_warpx4(tmem + kColSFA + s * (kSub * 4) + j * 4, ptx::smem_desc(sa + j * 512, 0, 128, 0));
         ptx::tc_commit(&sf_bar[s]);
       }
       __syncwarp();
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    int cur_q = -1;
-    uint32_t qsw = 0, slot = 0;
-    const uint32_t idesc0 = idesc_mxf4_m128n32(0), idesc1 = idesc_mxf4_m128n32(2);
-    for (uint32_t it = 0; sc.next(P); it++) {
-      if (abort_flag) break;
-      if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (lane 0)
+    // One commit per unit: tcgen05 instructions cost the issuing thread tens of
+    // cycles each, so the loop issues only the 2 x kSub MMAs and that commit.
+    if (lane == 0) {
+      int cur_q = -1;
+      uint32_t qsw = 0, slot = 0;
+      const uint32_t idesc0 = idesc_mxf4_m128n32(0), idesc1 = idesc_mxf4_m128n32(2);
+      for (uint32_t it = 0; sc.next(P); it++) {
+        if (abort_flag) break;
         if (sc.q != cur_q) {
           // release the previous query slot once every MMA issued so far is done
           if (qsw > 0) ptx::tc_commit(&qempty[(qsw - 1) & 1]);
           slot = qsw & 1;
-          if (!ptx::mbar_wait(&qsf[slot], (qsw >> 1) & 1)) { fail(); }
+          if (!ptx::mbar_wait(&qsf[slot], (qsw >> 1) & 1)) { fail(); break; }
           cur_q = sc.q;
           qsw++;
         }
         const uint32_t s = it % kScStages, r = it / kScStages, a = it % kScAcc, ra = it / kScAcc;
-        if (!abort_flag && ptx::mbar_wait(&sf_bar[s], r & 1) && ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) {
-          ptx::tc_fence_after();
-          const uint32_t sa = ptx::smem_u32(smem + s * kScStageBytes + kOffA);
-          const uint64_t bd = ptx::smem_desc(ptx::smem_u32(qslots + slot * kScQBytes + kQOffB), 16, 512, 4);
-          const uint32_t t_sfb = tmem + kColSFB + slot * 4;
+        if (!ptx::mbar_wait(&sf_bar[s], r & 1) || !ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) { fail(); break; }
+        ptx::tc_fence_after();
+        const uint32_t sa = ptx::smem_u32(smem + s * kScStageBytes + kOffA);
+        const uint64_t bd = ptx::smem_desc(ptx::smem_u32(qslots + slot * kScQBytes + kQOffB), 16, 512, 4);
+        const uint32_t t_sfb = tmem + kColSFB + slot * 4;
 #pragma unroll
-          for (int j = 0; j < 2; j++) {
-            const uint64_t ad = ptx::smem_desc(sa + j * 8192, 16, 512, 4);
-            const uint32_t t_sfa = tmem + kColSFA + s * 8 + j * 4;
-            const uint32_t d = tmem + a * 64 + j * 32;
-            ptx::tc_mma_mxf4(d, ad, bd, idesc0, t_sfa, t_sfb, 0u);
-            ptx::tc_mma_mxf4(d, ad + 2, bd + 2, idesc1, t_sfa, t_sfb, 1u);   // +32 B along K
-          }
-          ptx::tc_commit(&empty_bar[s]);
-          ptx::tc_commit(&acc_full[a]);
-        } else if (!abort_flag) {
-          fail();
+        for (int j = 0; j < kSub; j++) {
+          const uint64_t ad = ptx::smem_desc(sa + j * 8192, 16, 512, 4);
+          const uint32_t t_sfa = tmem + kColSFA + s * (kSub * 4) + j * 4;
+          const uint32_t d = tmem + a * (kSub * 32) + j * 32;
+          ptx::tc_mma_mxf4(d, ad, bd, idesc0, t_sfa, t_sfb, 0u);
+          ptx::tc_mma_mxf4(d, ad + 2, bd + 2, idesc1, t_sfa, t_sfb, 1u);   // +32 B along K
         }
+        ptx::tc_commit(&done_bar[s]);
       }
-      __syncwarp();
-      if (abort_flag) break;
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    // group g (warps 3+4g .. 6+4g) takes the units with it % 2 == g and owns
+    // accumulator g.  Waiting on done_bar is unambiguous: the stage's next
+    // phase needs the MMA of unit it+kScStages, which needs this group to have
+    // released unit it+kScStages-2, i.e. to have passed unit it.
     const int quarter = warp & 3;
     const uint32_t group = (uint32_t)(warp - 3) >> 2;     // warps 3..6 -> 0, 7..10 -> 1
     const int row = quarter * 32 + lane;
@@ -310,7 +323,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     for (uint32_t it = 0; sc.next(P); it++) {
       if (abort_flag) break;
       if ((it & 1) != group) continue;
-      const uint32_t a = it % kScAcc, ra = it / kScAcc;
+      const uint32_t s = it % kScStages, r = it / kScStages;
       if (sc.q != cur_q) {
         const float4 *wp = reinterpret_cast<const float4 *>(P.w + (int64_t)sc.q * kIdxHeads);
 #pragma unroll
@@ -323,34 +336,40 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         }
         cur_q = sc.q;
       }
-      if (!ptx::mbar_wait(&acc_full[a], ra & 1)) { fail(); break; }
+      if (!ptx::mbar_wait(&done_bar[s], r & 1)) { fail(); break; }
       ptx::tc_fence_after();
-      uint32_t d0[32], d1[32];
-      const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + a * 64;
-      ptx::tmem_ld_32x32b_x32(ta, d0);
-      ptx::tmem_ld_32x32b_x32(ta + 32, d1);
-      ptx::tmem_wait_ld();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&acc_empty[a]);
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int h = 0; h < kIdxHeads; h++) {
-        s0 = fmaf(wv[h], fmaxf(__uint_as_float(d0[h]), 0.f), s0);
-        s1 = fmaf(wv[h], fmaxf(__uint_as_float(d1[h]), 0.f), s1);
-      }
+      const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + group * (kSub * 32);
       float *out = P.scores + (int64_t)sc.q * P.stride;
-      const int64_t i0 = (int64_t)sc.u * kUnit + row, i1 = i0 + 128;
-      if (P.pool == nullptr) {
-        if (i0 < sc.nv) out[i0] = s0;
-        if (i1 < sc.nv) out[i1] = s1;
-      } else {
-        const int32_t *pl = P.pool + (int64_t)sc.q * kPoolBlocks;
-        const int b0 = __ldg(pl + (i0 >> 3)), b1 = __ldg(pl + (i1 >> 3));
-        const bool ok0 = b0 >= 0 && (int64_t)b0 * kBlock < P.n_max && (int64_t)b0 * kBlock + (i0 & 7) < sc.nv;
-        const bool ok1 = b1 >= 0 && (int64_t)b1 * kBlock < P.n_max && (int64_t)b1 * kBlock + (i1 & 7) < sc.nv;
-        out[i0] = ok0 ? s0 : -INFINITY;
-        out[i1] = ok1 ? s1 : -INFINITY;
+      const int32_t *pl = P.pool + (int64_t)sc.q * kPoolBlocks;
+      auto store = [&](int64_t i, float v) {
+        if (P.pool == nullptr) {
+          if (i < sc.nv) out[i] = v;
+        } else {
+          const int b = __ldg(pl + (i >> 3));
+          const bool ok = b >= 0 && (int64_t)b * kBlock < P.n_max && (int64_t)b * kBlock + (i & 7) < sc.nv;
+          out[i] = ok ? v : -INFINITY;
+        }
+      };
+      const int64_t i0 = (int64_t)sc.u * kUnit + row;
+#pragma unroll 1
+      for (int h2 = 0; h2 < kSub / 2; h2++) {         // two sub-tiles (64 columns) at a time
+        uint32_t d0[32], d1[32];
+        ptx::tmem_ld_32x32b_x32(ta + h2 * 64, d0);
+        ptx::tmem_ld_32x32b_x32(ta + h2 * 64 + 32, d1);
+        ptx::tmem_wait_ld();
+        if (h2 == kSub / 2 - 1) {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&acc_empty[group]);
+        }
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int h = 0; h < kIdxHeads; h++) {
+          s0 = fmaf(wv[h], fmaxf(__uint_as_float(d0[h]), 0.f), s0);
+          s1 = fmaf(wv[h], fmaxf(__uint_as_float(d1[h]), 0.f), s1);
+        }
+        store(i0 + h2 * 256, s0);
+        store(i0 + h2 * 256 + 128, s1);
       }
     }
   }
