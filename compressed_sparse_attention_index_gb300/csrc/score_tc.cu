@@ -11,10 +11,13 @@
 // into TMEM; the epilogue computes s = sum_h w_h * max(0, D[entry][h]) per row.
 //
 // The kernel is HBM-bound (68 B of key per entry, 8 FLOP/B of FP4 MMA): a
-// persistent CTA per SM streams work units of 256 entries (two 128-row
-// sub-tiles) through a 12-stage shared-memory ring.  Warp roles (352 threads):
-//   warp 0      producer: one bulk copy (cp.async.bulk) of the unit's 16 KB of
-//               nibbles and one of its 1 KB of E8M0 scales (pool mode: 32
+// persistent CTA per SM streams work units of 512 entries (four 128-row
+// sub-tiles, 34 KB) through a 6-stage shared-memory ring.  Every tcgen05
+// instruction and every barrier wait costs its issuing thread tens of cycles,
+// so the design keeps those per byte low: big units, one commit per unit, and
+// two MMA issuers.  Warp roles (384 threads):
+//   warp 0      producer: one bulk copy (cp.async.bulk) of the unit's 32 KB of
+//               nibbles and one of its 2 KB of E8M0 scales (pool mode: 64
 //               gathered 8-entry blocks of 512 B + 32 B); the query's 2 KB of
 //               nibbles and 128 B of scales only when the CTA moves to another
 //               query (two query slots).  The nibble planes are stored
@@ -22,15 +25,16 @@
 //               MMA reads;
 //   warp 2      scale-factor warp: rearranges the unit's key scales in shared
 //               memory into the 32-lane x 16-B layout tcgen05.cp expects, copies
-//               them into TMEM and signals the MMA warp through tcgen05.commit;
-//   warp 1      TMEM owner + MMA issuer: four MMAs per unit, then commits to the
-//               stage's "empty" barrier and to the accumulator's "full" barrier;
+//               them into TMEM and signals the MMA issuers through tcgen05.commit;
+//   warps 1, 11 MMA issuers (lane 0; warp 1 also owns TMEM), even and odd
+//               units: eight MMAs per unit into the unit's accumulator, then one
+//               commit to the stage's done barrier, which both frees the stage
+//               and marks the accumulator full;
 //   warps 3..10 epilogue, two groups of four warps taking alternate units: one
 //               TMEM lane (= one entry of each sub-tile) per thread, 32 columns
-//               (= heads) per tcgen05.ld, ReLU + weighted sum, coalesced store.
+//               (= heads) per sub-tile, ReLU + weighted sum, coalesced store.
 // The tile schedule is advanced incrementally (no division per unit) and the
-// per-query sequence id / visible length are cached, so the issuing warps spend
-// their time on the pipeline, not on bookkeeping.  Every mbarrier wait is
+// per-query sequence id / visible length are cached.  Every mbarrier wait is
 // bounded (CSA2_ERR_TIMEOUT instead of a hang).
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -46,7 +50,8 @@ constexpr int kOffSFA = kSub * 8192;      // kSub x 512 B key scales: staged [ro
 constexpr int kScQBytes = 2560;           // per query slot: 32 x 64 B nibbles + 512 B scales
 constexpr int kQOffB = 0, kQOffSFB = 2048;
 constexpr int kScSmem = kScStages * kScStageBytes + 2 * kScQBytes;
-constexpr int kScThreads = 352;
+constexpr int kScThreads = 384;
+constexpr int kScMmaWarp2 = 11;          // second MMA issuer (odd units)
 constexpr int kScAcc = 2;                 // TMEM accumulators (kSub x 32 columns each), one per epilogue group
 constexpr uint32_t kScTmemCols = 512;
 constexpr uint32_t kColSFA = kScAcc * kSub * 32;              // per stage: kSub x 4 columns
@@ -146,7 +151,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     for (int a = 0; a < kScAcc; a++) ptx::mbar_init(&acc_empty[a], 4);
     for (int q = 0; q < 2; q++) {
       ptx::mbar_init(&qfull[q], 1);
-      ptx::mbar_init(&qempty[q], 1);
+      ptx::mbar_init(&qempty[q], 2);                 // both MMA issuers release the slot
       ptx::mbar_init(&qsf[q], 1);
     }
     abort_flag = 0;
@@ -273,11 +278,13 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       }
       __syncwarp();
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (lane 0)
-    // One commit per unit: tcgen05 instructions cost the issuing thread tens of
-    // cycles each, so the loop issues only the 2 x kSub MMAs and that commit.
+  } else if (warp == 1 || warp == kScMmaWarp2) {
+    // ------------------------------------------------------------ MMA issuers (lane 0 of warps 1, 11)
+    // A lone issuing thread spends most of a unit's time on its own instruction
+    // latency (waits, descriptors, schedule), so two warps issue alternate units,
+    // each into its own accumulator, with one commit per unit.
     if (lane == 0) {
+      const uint32_t par = warp == 1 ? 0u : 1u;
       int cur_q = -1;
       uint32_t qsw = 0, slot = 0;
       const uint32_t idesc0 = idesc_mxf4_m128n32(0), idesc1 = idesc_mxf4_m128n32(2);
@@ -291,6 +298,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
           cur_q = sc.q;
           qsw++;
         }
+        if ((it & 1) != par) continue;
         const uint32_t s = it % kScStages, r = it / kScStages, a = it % kScAcc, ra = it / kScAcc;
         if (!ptx::mbar_wait(&sf_bar[s], r & 1) || !ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) { fail(); break; }
         ptx::tc_fence_after();
