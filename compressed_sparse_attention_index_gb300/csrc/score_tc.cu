@@ -18,9 +18,10 @@
 // two MMA issuers.  Warp roles (384 threads):
 //   warp 0      producer: one bulk copy (cp.async.bulk) of the unit's 32 KB of
 //               nibbles and one of its 2 KB of E8M0 scales (pool mode: 64
-//               gathered 8-entry blocks of 512 B + 32 B); the query's 2 KB of
-//               nibbles and 128 B of scales only when the CTA moves to another
-//               query (two query slots).  The nibble planes are stored
+//               gathered 8-entry blocks of 512 B + 32 B); with the first unit
+//               of each run of one query, its 2 KB of nibbles and 128 B of
+//               scales into the next of six query slots (so a CTA may switch
+//               query on every unit without a stall).  The nibble planes are stored
 //               64B-swizzled, so a plain contiguous copy lands in the layout the
 //               MMA reads;
 //   warp 2      scale-factor warp: rearranges the unit's key scales in shared
@@ -44,19 +45,21 @@ namespace csa2 {
 constexpr int kScStages = 6;
 constexpr int kSub = 4;                   // 128-row sub-tiles per work unit
 constexpr int kUnit = kSub * 128;         // entries per work unit
-constexpr int kScStageBytes = kSub * (8192 + 512);   // nibbles + scales
 constexpr int kOffA = 0;                  // sub-tile j at j * 8192: 128 rows x 64 B, 64B-swizzled as stored
 constexpr int kOffSFA = kSub * 8192;      // kSub x 512 B key scales: staged [row][4], rearranged in place
-constexpr int kScQBytes = 2560;           // per query slot: 32 x 64 B nibbles + 512 B scales
+constexpr int kScStageBytes = kOffSFA + kSub * 512;
+constexpr int kQSlots = 6;                // query slots, used round-robin, one per run of units of a query
+constexpr int kScQBytes = 2560;           // per slot: 32 heads x 64 B nibbles + 128 B scales spread to 512 B
 constexpr int kQOffB = 0, kQOffSFB = 2048;
-constexpr int kScSmem = kScStages * kScStageBytes + 2 * kScQBytes;
+constexpr int kScSmem = kScStages * kScStageBytes + kQSlots * kScQBytes;
+static_assert(kScStageBytes % 1024 == 0, "64B-swizzled tiles need 512-B aligned stages and slots");
 constexpr int kScThreads = 384;
 constexpr int kScMmaWarp2 = 11;          // second MMA issuer (odd units)
 constexpr int kScAcc = 2;                 // TMEM accumulators (kSub x 32 columns each), one per epilogue group
 constexpr uint32_t kScTmemCols = 512;
 constexpr uint32_t kColSFA = kScAcc * kSub * 32;              // per stage: kSub x 4 columns
 constexpr uint32_t kColSFB = kColSFA + kScStages * kSub * 4;  // per query slot: 4 columns
-static_assert(kColSFB + 8 <= kScTmemCols, "TMEM columns");
+static_assert(kColSFB + kQSlots * 4 <= kScTmemCols, "TMEM columns");
 static_assert(kScStages % kScAcc == 0, "a stage's done barrier also marks its accumulator full");
 
 // Instruction descriptor of kind::mxf4 block-scaled MMA, M=128, N=32, both
@@ -129,6 +132,32 @@ struct Schedule {
   }
 };
 
+// Query slots as seen by one role walking the schedule.  A run of consecutive
+// units of one query (an epoch) takes the next slot round-robin; the slot's
+// previous user was the last unit of the epoch kQSlots earlier.  Registers
+// only: the ring of epoch starts is shifted, never indexed.
+struct QuerySlots {
+  int cur_q = -1;
+  uint32_t slot = kQSlots - 1;
+  int start[kQSlots];                    // first unit of the last kQSlots epochs, oldest first
+  __device__ QuerySlots() {
+#pragma unroll
+    for (int i = 0; i < kQSlots; i++) start[i] = -1;
+  }
+  // call once per unit in schedule order; true when unit `it` starts an epoch
+  __device__ bool step(int q, int it) {
+    if (q == cur_q) return false;
+    cur_q = q;
+    slot = slot + 1 == (uint32_t)kQSlots ? 0u : slot + 1;
+#pragma unroll
+    for (int i = 0; i + 1 < kQSlots; i++) start[i] = start[i + 1];
+    start[kQSlots - 1] = it;
+    return true;
+  }
+  // after step() returned true: the last unit that used this slot (< 0 if none)
+  __device__ int prev_user() const { return start[0] - 1; }
+};
+
 __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcArgs P) {
   extern __shared__ __align__(1024) unsigned char sc_smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -137,7 +166,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   // done_bar[s]: the MMAs of the unit in stage s have completed, so the stage
   // may be refilled and the unit's accumulator may be read (one commit serves both)
   __shared__ __align__(8) uint64_t full_bar[kScStages], sf_bar[kScStages], done_bar[kScStages];
-  __shared__ __align__(8) uint64_t acc_empty[kScAcc], qfull[2], qempty[2], qsf[2];
+  __shared__ __align__(8) uint64_t acc_empty[kScAcc];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
@@ -149,11 +178,6 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       ptx::mbar_init(&done_bar[s], 1);
     }
     for (int a = 0; a < kScAcc; a++) ptx::mbar_init(&acc_empty[a], 4);
-    for (int q = 0; q < 2; q++) {
-      ptx::mbar_init(&qfull[q], 1);
-      ptx::mbar_init(&qempty[q], 2);                 // both MMA issuers release the slot
-      ptx::mbar_init(&qsf[q], 1);
-    }
     abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -173,32 +197,40 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = ptx::policy_evict_first();
-    int cur_q = -1;
-    uint32_t qsw = 0;                                   // query switches so far
+    QuerySlots qs;
     for (uint32_t it = 0; sc.next(P); it++) {
       if (abort_flag) break;
-      if (sc.q != cur_q) {
-        const uint32_t slot = qsw & 1, rnd = qsw >> 1;
-        if (!ptx::mbar_wait(&qempty[slot], (rnd & 1) ^ 1)) { fail(); break; }
-        if (lane == 0) {
-          unsigned char *qs = qslots + slot * kScQBytes;
-          ptx::mbar_arrive_expect_tx(&qfull[slot], 2048 + 128);
-          ptx::bulk_load(qs + kQOffB, P.q_nib + (int64_t)sc.q * kIdxHeads * 64, 2048, &qfull[slot]);
-          ptx::bulk_load(qs + kQOffSFB, P.q_scale + (int64_t)sc.q * kIdxHeads * 4, 128, &qfull[slot]);
-        }
-        cur_q = sc.q;
-        qsw++;
-      }
       const uint32_t s = it % kScStages, r = it / kScStages;
+      const bool fresh = qs.step(sc.q, (int)it);
       if (!ptx::mbar_wait(&done_bar[s], (r & 1) ^ 1)) { fail(); break; }
+      if (fresh) {
+        // the slot's previous users must be done: its last unit and the one
+        // before (the two issuers complete independently; each in order).
+        // Units up to it - kScStages are (the wait above); a later one is
+        // waited for on its own stage barrier, whose next phase needs a unit
+        // not yet loaded, so the parity is unambiguous.
+        bool ok = true;
+        for (int u = qs.prev_user(), k = 0; k < 2 && ok; k++, u--)
+          if (u >= 0 && u + kScStages > (int)it)
+            ok = ptx::mbar_wait(&done_bar[u % kScStages], (uint32_t)(u / kScStages) & 1);
+        if (!ok) { fail(); break; }
+      }
       unsigned char *st = smem + s * kScStageBytes;
+      // a new run of units of one query: its data travel with this unit
+      const uint32_t qbytes = fresh ? 2048 + 128 : 0;
+      unsigned char *qd = qslots + qs.slot * kScQBytes;
+      auto load_query = [&]() {
+        ptx::bulk_load(qd + kQOffB, P.q_nib + (int64_t)sc.q * kIdxHeads * 64, 2048, &full_bar[s]);
+        ptx::bulk_load(qd + kQOffSFB, P.q_scale + (int64_t)sc.q * kIdxHeads * 4, 128, &full_bar[s]);
+      };
       const int64_t row0 = (int64_t)sc.seq * P.n_max;
       if (P.pool == nullptr) {
         if (lane == 0) {
           // sub-tiles that start before n_vis end within n_max (n_max % 128 == 0)
           const int left = sc.nv - sc.u * kUnit;
           const int nsub = left >= kUnit ? kSub : (left + 127) >> 7;
-          ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)nsub * (8192 + 512));
+          ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)nsub * (8192 + 512) + qbytes);
+          if (fresh) load_query();
           const int64_t r0 = row0 + (int64_t)sc.u * kUnit;
           ptx::bulk_load_hint(st + kOffA, P.key_nib + r0 * 64, (uint32_t)nsub * 8192, &full_bar[s], policy);
           ptx::bulk_load(st + kOffSFA, P.key_scale + r0 * 4, (uint32_t)nsub * 512, &full_bar[s]);
@@ -212,7 +244,10 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         if ((blk0 >= 0 && !ok0) || (blk1 >= 0 && !ok1)) record_error(P.status, CSA2_ERR_BOUNDS);
         const int n_ok = __popc(__ballot_sync(0xFFFFFFFFu, ok0)) + __popc(__ballot_sync(0xFFFFFFFFu, ok1));
         // an all-empty unit still arrives once, so its phase completes
-        if (lane == 0) ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)n_ok * (512 + 32));
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)n_ok * (512 + 32) + qbytes);
+          if (fresh) load_query();
+        }
         __syncwarp();
         if (ok0) {
           const int64_t r0 = row0 + (int64_t)blk0 * kBlock;
@@ -229,35 +264,26 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ scale-factor warp
-    int cur_q = -1;
-    uint32_t qsw = 0;
+    QuerySlots qs;
     for (uint32_t it = 0; sc.next(P); it++) {
       if (abort_flag) break;
-      if (sc.q != cur_q) {
-        const uint32_t slot = qsw & 1, rnd = qsw >> 1;
-        if (!ptx::mbar_wait(&qfull[slot], rnd & 1)) { fail(); break; }
-        uint32_t *sfb = reinterpret_cast<uint32_t *>(qslots + slot * kScQBytes + kQOffSFB);
+      const uint32_t s = it % kScStages, r = it / kScStages;
+      const bool fresh = qs.step(sc.q, (int)it);
+      if (!ptx::mbar_wait(&full_bar[s], r & 1)) { fail(); break; }
+      unsigned char *st = smem + s * kScStageBytes;
+      unsigned char *qd = qslots + qs.slot * kScQBytes;
+      if (fresh) {
+        uint32_t *sfb = reinterpret_cast<uint32_t *>(qd + kQOffSFB);
         const uint32_t vb = sfb[lane];
         __syncwarp();
         sfb[lane * 4 + 0] = vb;          // head `lane` -> 16-B line `lane` (tcgen05.cp layout)
         sfb[lane * 4 + 1] = 0u;
         sfb[lane * 4 + 2] = 0u;
         sfb[lane * 4 + 3] = 0u;
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::tc_fence_after();
-          ptx::tc_cp_32x128b_warpx4(tmem + kColSFB + slot * 4, ptx::smem_desc(ptx::smem_u32(sfb), 0, 128, 0));
-          ptx::tc_commit(&qsf[slot]);
-        }
-        cur_q = sc.q;
-        qsw++;
       }
-      const uint32_t s = it % kScStages, r = it / kScStages;
-      if (!ptx::mbar_wait(&full_bar[s], r & 1)) { fail(); break; }
       // key scales -> tcgen05.cp layout: 16-B line m0 of sub-tile j holds rows
       // m0, m0+32, m0+64, m0+96 of that sub-tile
-      uint32_t *sfa = reinterpret_cast<uint32_t *>(smem + s * kScStageBytes + kOffSFA);
+      uint32_t *sfa = reinterpret_cast<uint32_t *>(st + kOffSFA);
       uint32_t va[4 * kSub];
 #pragma unroll
       for (int i = 0; i < 4 * kSub; i++) va[i] = sfa[i * 32 + lane];
@@ -270,6 +296,8 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       __syncwarp();
       if (lane == 0) {
         ptx::tc_fence_after();
+        if (fresh)
+          ptx::tc_cp_32x128b_warpx4(tmem + kColSFB + qs.slot * 4, ptx::smem_desc(ptx::smem_u32(qd + kQOffSFB), 0, 128, 0));
         const uint32_t sa = ptx::smem_u32(sfa);
 #pragma unroll
         for (int j = 0; j < kSub; j++)
@@ -285,26 +313,18 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     // each into its own accumulator, with one commit per unit.
     if (lane == 0) {
       const uint32_t par = warp == 1 ? 0u : 1u;
-      int cur_q = -1;
-      uint32_t qsw = 0, slot = 0;
       const uint32_t idesc0 = idesc_mxf4_m128n32(0), idesc1 = idesc_mxf4_m128n32(2);
+      QuerySlots qs;
       for (uint32_t it = 0; sc.next(P); it++) {
         if (abort_flag) break;
-        if (sc.q != cur_q) {
-          // release the previous query slot once every MMA issued so far is done
-          if (qsw > 0) ptx::tc_commit(&qempty[(qsw - 1) & 1]);
-          slot = qsw & 1;
-          if (!ptx::mbar_wait(&qsf[slot], (qsw >> 1) & 1)) { fail(); break; }
-          cur_q = sc.q;
-          qsw++;
-        }
+        qs.step(sc.q, (int)it);
         if ((it & 1) != par) continue;
         const uint32_t s = it % kScStages, r = it / kScStages, a = it % kScAcc, ra = it / kScAcc;
         if (!ptx::mbar_wait(&sf_bar[s], r & 1) || !ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) { fail(); break; }
         ptx::tc_fence_after();
         const uint32_t sa = ptx::smem_u32(smem + s * kScStageBytes + kOffA);
-        const uint64_t bd = ptx::smem_desc(ptx::smem_u32(qslots + slot * kScQBytes + kQOffB), 16, 512, 4);
-        const uint32_t t_sfb = tmem + kColSFB + slot * 4;
+        const uint64_t bd = ptx::smem_desc(ptx::smem_u32(qslots + qs.slot * kScQBytes + kQOffB), 16, 512, 4);
+        const uint32_t t_sfb = tmem + kColSFB + qs.slot * 4;
 #pragma unroll
         for (int j = 0; j < kSub; j++) {
           const uint64_t ad = ptx::smem_desc(sa + j * 8192, 16, 512, 4);
