@@ -10,19 +10,19 @@
 //
 // Rows of up to kDirectCap items are selected by one CTA from shared memory.
 // Longer rows (1M-entry Full-layer rows, 131,072-block pool rows) take two
-// launches: a bandwidth pass writes the maximum key of every group of 128 items;
-// then one CTA per row finds T, the k-th largest group maximum (a lower bound of
-// the k-th best key), rescans only the groups whose maximum reaches T, and runs
-// the exact selection on those candidates (usually about 2k items).  A row whose
-// candidates overflow the buffer falls back to an exact radix select straight
-// over the score row.
+// launches: a bandwidth pass writes the maximum key of every group of G items
+// (G = 32 for k = 512 over 1M entries); then one CTA per row finds a threshold
+// T from the group maxima alone (two 12-bit histogram digits), rescans only the
+// groups whose maximum reaches T (about k groups), and runs the exact
+// selection on those candidates (about k items).  A row whose lists overflow
+// shared memory falls back to an exact radix select straight over the row.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace csa2 {
 
 constexpr int kDirectCap = 16384;   // items held in shared memory by one CTA
-constexpr int kMaxGroup = 128;      // largest group of items per group maximum (long rows)
-constexpr int kMaxGroups = 8192;    // groups a long row may have
 constexpr int kCandCap = 8192;      // candidates kept in shared memory (long rows)
 constexpr int kMaxK = 2048;
 constexpr int kTopkThreads = 1024;
@@ -264,6 +264,120 @@ __device__ void select_rank(const uint64_t *keys, int n, int k, int32_t *out, in
   for (int i = take + threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
 }
 
+// Block-wide exclusive scans over nb counters in shared memory (nb a multiple
+// of blockDim.x, blockDim.x a multiple of 32): suffix (counts of the bins
+// above) and prefix (counts of the bins below).
+template <bool kSuffix>
+__device__ void block_offsets(uint32_t *h, int nb) {
+  __shared__ uint32_t wsum[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int per = nb / blockDim.x;
+  const int b0 = threadIdx.x * per;
+  uint32_t part = 0;
+  for (int j = 0; j < per; j++) part += h[b0 + j];
+  uint32_t incl = part;                              // inclusive scan toward this thread
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = kSuffix ? __shfl_down_sync(0xFFFFFFFFu, incl, o) : __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (kSuffix ? lane + o < 32 : lane >= o) incl += v;
+  }
+  if (lane == 0) wsum[warp] = 0;
+  __syncthreads();
+  if (kSuffix ? lane == 0 : lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  uint32_t run = incl - part;
+  for (int w = 0; w < nw; w++)
+    if (kSuffix ? w > warp : w < warp) run += wsum[w];
+  if (kSuffix) {
+    for (int j = per - 1; j >= 0; j--) { const uint32_t v = h[b0 + j]; h[b0 + j] = run; run += v; }
+  } else {
+    for (int j = 0; j < per; j++) { const uint32_t v = h[b0 + j]; h[b0 + j] = run; run += v; }
+  }
+  __syncthreads();
+}
+
+// Exact top-k of n unique keys in shared memory (n <= kCandCap) in O(n) work
+// and a few barriers, for candidate sets a little larger than k.  The keys
+// are bucketed by value (4,096 buckets of power-of-two width over the range
+// present) and scattered bucket by bucket from the top; a key's rank is the
+// number of keys in the buckets above plus the larger keys in its own.  The
+// k selected indices are placed in ascending order the same way, bucketed by
+// index.  tmp: n 64-bit slots; bins: 8,192 counters.  out[0..k): ascending
+// indices, -1 padding.  Heavily tied buckets cost up to their size squared.
+constexpr int kBuckets = 4096;
+
+__device__ void select_bucket(const uint64_t *keys, int n, int k, int32_t *out, uint64_t *tmp, uint32_t *bins) {
+  __shared__ unsigned long long lo_sh, hi_sh;
+  __shared__ int max_idx_sh;
+  uint32_t *hist = bins, *cur = bins + kBuckets;
+  const int take = min(k, n);
+  if (threadIdx.x == 0) { lo_sh = ~0ull; hi_sh = 0ull; max_idx_sh = 0; }
+  for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) { hist[i] = 0; cur[i] = 0; }
+  __syncthreads();
+  // ---- value range -> bucket width 2^sh
+  unsigned long long lo = ~0ull, hi = 0ull;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    lo = min(lo, (unsigned long long)keys[i]);
+    hi = max(hi, (unsigned long long)keys[i]);
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
+  }
+  if ((threadIdx.x & 31) == 0) { atomicMin(&lo_sh, lo); atomicMax(&hi_sh, hi); }
+  __syncthreads();
+  lo = lo_sh;
+  const unsigned long long range = n > 0 ? hi_sh - lo : 0ull;
+  const int sh = range == 0 ? 0 : max(0, 64 - __clzll((long long)range) - 12);   // (range >> sh) < 4096
+  // ---- scatter by value bucket, buckets in descending order
+  for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&hist[(uint32_t)((keys[i] - lo) >> sh)], 1u);
+  __syncthreads();
+  block_offsets<true>(hist, kBuckets);               // hist[b] <- keys in the buckets above b
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint32_t b = (uint32_t)((keys[i] - lo) >> sh);
+    tmp[hist[b] + atomicAdd(&cur[b], 1u)] = keys[i];
+  }
+  __syncthreads();
+  // ---- rank = keys above the bucket + larger keys inside it; keep rank < take
+  // (the cursors are no longer read: their space holds the selection by rank)
+  int32_t *sel = reinterpret_cast<int32_t *>(cur);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint64_t x = tmp[i];
+    const uint32_t b = (uint32_t)((x - lo) >> sh);
+    int rank = (int)hist[b];
+    for (int j = (int)hist[b]; j < n && (uint32_t)((tmp[j] - lo) >> sh) == b; j++) rank += tmp[j] > x;
+    if (rank < take) sel[rank] = (int32_t)(~(uint32_t)(x & 0xFFFFFFFFu));
+  }
+  __syncthreads();
+  // ---- ascending index order: 2,048 index buckets (hist halves: counts, cursors)
+  uint32_t *h2 = hist, *c2 = hist + 2048;
+  for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) hist[i] = 0;
+  int mx = 0;
+  for (int i = threadIdx.x; i < take; i += blockDim.x) mx = max(mx, sel[i]);
+  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+  if ((threadIdx.x & 31) == 0) atomicMax(&max_idx_sh, mx);
+  __syncthreads();
+  const int sh2 = max(0, 32 - __clz(max_idx_sh) - 11);  // (max index >> sh2) < 2048
+  for (int i = threadIdx.x; i < take; i += blockDim.x) atomicAdd(&h2[sel[i] >> sh2], 1u);
+  __syncthreads();
+  block_offsets<false>(h2, 2048);                    // h2[b] <- indices in the buckets below b
+  int32_t *by_idx = reinterpret_cast<int32_t *>(tmp);
+  for (int i = threadIdx.x; i < take; i += blockDim.x) {
+    const int b = sel[i] >> sh2;
+    by_idx[h2[b] + atomicAdd(&c2[b], 1u)] = sel[i];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < take; i += blockDim.x) {
+    const int32_t x = by_idx[i];
+    const int b = x >> sh2;
+    int before = (int)h2[b];
+    for (int j = (int)h2[b]; j < take && (by_idx[j] >> sh2) == b; j++) before += by_idx[j] < x;
+    out[before] = x;
+  }
+  for (int i = take + threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------- direct path
 __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, int k, int32_t *__restrict__ out,
                                                                     int *status) {
@@ -300,206 +414,289 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
 }
 
 // ---------------------------------------------------------------- long rows
-// Group maxima: the max key over each group of G consecutive items (0 if the
-// group holds no valid item), G a power of two in [8, 128].  A warp covers
-// 32 * ipl items (ipl = max(1, G/32) per lane) and reduces within groups.
-__global__ void __launch_bounds__(256) topk_groupmax_kernel(TopkSrc S, int G, int n_groups,
-                                                             uint32_t *__restrict__ gmax, int *status) {
+// Two streaming passes over the row.  Pass 1 writes the maximum key of every
+// supergroup of SGI consecutive items (SGI a power of two, so that a row has
+// about 4k supergroups).  Pass 2 (P CTAs per row) takes T = the k-th largest
+// supergroup maximum with its low 16 bits cleared: at least k supergroups
+// reach T, so at least k items do, so the k-th best item key is >= T and every
+// top-k item has a key >= T.  Each CTA streams its share of the row and
+// appends the items with key >= T (a small superset of the top-k) to the
+// row's candidate buffer; the last CTA of the row to finish (a counter; no CTA
+// ever waits for another) runs the exact selection on the candidates, or on
+// the whole row if the buffer overflowed.
+//
+// Workspace, per row q: smax[q][sstride] (the supergroup maxima, 0 = no valid
+// item), ctr[q][4] (candidates appended, CTAs done), cand[q][kCandCap] (keys).
+// Pass 1 clears ctr; slots past a row's valid length are never read.
+constexpr int kCollectThreads = 1024;
+constexpr int kSuperCap = 16384;    // supergroups per row (held in shared memory by pass 2)
+
+struct LongRowWs {
+  uint32_t *smax, *ctr;
+  uint64_t *cand;
+  int64_t sstride;
+};
+
+// Items per supergroup: the largest power of two in [8, 512] that leaves at
+// least 4k supergroups, doubled further while a row has more than kSuperCap.
+__host__ __device__ inline int64_t long_row_sgi(int64_t n_items, int k) {
+  int64_t sgi = 512;
+  while (sgi > 8 && n_items / sgi < 4 * (int64_t)k) sgi >>= 1;
+  while ((n_items + sgi - 1) / sgi > kSuperCap) sgi <<= 1;
+  return sgi;
+}
+
+__host__ __device__ inline LongRowWs long_row_ws(void *ws, int n_q, int64_t n_items, int k) {
+  LongRowWs w;
+  const int64_t sgi = long_row_sgi(n_items, k);
+  w.sstride = ((n_items + sgi - 1) / sgi + 3) / 4 * 4;
+  w.smax = static_cast<uint32_t *>(ws);
+  w.ctr = w.smax + (int64_t)n_q * w.sstride;
+  w.cand = reinterpret_cast<uint64_t *>(w.ctr + (int64_t)n_q * 4);   // 16-B aligned: parts are multiples of 4 words
+  return w;
+}
+
+__host__ __device__ inline size_t long_row_ws_bytes(int n_q, int64_t n_items, int k) {
+  const LongRowWs w = long_row_ws(nullptr, n_q, n_items, k);
+  return (size_t)n_q * ((size_t)(w.sstride + 4) * 4 + (size_t)kCandCap * 8);
+}
+
+// Pass 1.  A warp step covers 32 x IPL items: plain rows one float4 (IPL = 4)
+// per lane, block rows one item per lane.  A warp takes four steps at a time
+// (four loads in flight per lane) and a pass of max(sgi, 4 steps) items, so
+// no two warps share a supergroup.  Supergroups smaller than a step reduce
+// over sgi / IPL lanes; larger ones over the whole warp and over steps.
+// Block (0, q) clears row q's counters.
+template <bool kPlain>
+__global__ void __launch_bounds__(256) topk_smax_kernel(TopkSrc S, int64_t sgi, LongRowWs W, int *status) {
+  constexpr int IPL = kPlain ? 4 : 1;
+  constexpr int64_t kStep = 32 * IPL;
   const int q = blockIdx.y;
   const int nv = query_nv(S, q, status);
   const int lane = threadIdx.x & 31;
-  const int warps = blockDim.x >> 5;
-  const int ipl = G >= 32 ? G / 32 : 1;          // items per lane
-  const int lpg = G >= 32 ? 32 : G;              // lanes per group
-  const int64_t span = 32 * ipl;                 // items per warp step
-  const int64_t n_steps = ((int64_t)n_groups * G + span - 1) / span;
-  for (int64_t w = (int64_t)blockIdx.x * warps + (threadIdx.x >> 5); w < n_steps; w += (int64_t)gridDim.x * warps) {
-    uint32_t m = 0;
-    const int64_t i0 = w * span + (int64_t)lane * ipl;
-    const float *rowp = S.scores + (int64_t)q * S.stride;
-    if (ipl == 4 && S.block == 1 && S.pool == nullptr && i0 + 4 <= nv &&
-        ((reinterpret_cast<uintptr_t>(rowp + i0) & 15u) == 0)) {
-      const float4 v = __ldg(reinterpret_cast<const float4 *>(rowp + i0));
-      m = max(max(order_key(v.x), order_key(v.y)), max(order_key(v.z), order_key(v.w)));
-    } else {
-      for (int u = 0; u < ipl; u++) {
-        uint64_t key;
-        if (i0 + u < S.n_items && item_key(S, q, i0 + u, nv, key, status)) m = max(m, (uint32_t)(key >> 32));
-      }
-    }
-    for (int o = lpg >> 1; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    const int64_t g = i0 >> (__ffs(G) - 1);
-    if ((lane & (lpg - 1)) == 0 && g < n_groups) gmax[(int64_t)q * n_groups + g] = m;
-  }
-}
-
-// k-th largest of n 32-bit values (counted with multiplicity; requires at
-// least k valid values): 8-bit radix passes narrowing a prefix, down to bit
-// min_shift (the lower bits of the result are zero).
-template <class Get>
-__device__ uint32_t radix_kth_u32(Get get, int n, int k, SelectShared &sh, int min_shift = 0) {
-  uint32_t prefix = 0, mask = 0;
-  int rem = k;
-  for (int shift = 24; shift >= min_shift; shift -= 8) {
-    block_hist(sh, n, [&](int64_t i, uint32_t &d) {
-      uint32_t v;
-      if (!get((int)i, v) || (v & mask) != prefix) return false;
-      d = (v >> shift) & 255u;
-      return true;
-    });
-    find_digit(sh, rem);
-    __syncthreads();
-    prefix |= (uint32_t)sh.digit << shift;
-    mask |= 0xFFu << shift;
-    rem -= sh.above;
-    __syncthreads();
-  }
-  return prefix;
-}
-
-// One CTA per query.  T = the k-th largest group maximum: at least k groups
-// reach T, so at least k items do, so the k-th best item key is >= T and every
-// item of the top-k lies in a group whose maximum is >= T.  Those groups are
-// listed, their items scanned by all threads at once for keys >= T (a superset
-// of the top-k, usually ~2k items), and the exact selection runs on that set.
-__global__ void __launch_bounds__(kTopkThreads) topk_group_select_kernel(TopkSrc S, int G, int n_groups, int k,
-                                                                          const uint32_t *__restrict__ gmax,
-                                                                          int32_t *__restrict__ out, int *status) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint64_t *cand = reinterpret_cast<uint64_t *>(smem_raw);               // [kCandCap]
-  uint32_t *gm = reinterpret_cast<uint32_t *>(cand + kCandCap);          // [kMaxGroups] group maxima
-  int32_t *glist = reinterpret_cast<int32_t *>(gm + kMaxGroups);         // [kMaxGroups] groups to scan
-  int32_t *sel = glist + kMaxGroups;                                     // [kMaxK]
-  __shared__ SelectShared sh;
-  sh.whist = reinterpret_cast<uint32_t *>(sel + kMaxK);                  // [32][256]
-  __shared__ int n_cand, n_valid_groups, n_list;
-  const int q = blockIdx.x;
-  const int nv = query_nv(S, q, status);
-  const int lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) { n_cand = 0; n_valid_groups = 0; n_list = 0; }
-  __syncthreads();
-  int live_groups = 0;
-  for (int b0 = 0; b0 < n_groups; b0 += 8 * blockDim.x) {     // eight loads in flight per thread
-    uint32_t m[8];
-#pragma unroll
-    for (int u = 0; u < 8; u++) {
-      const int g = b0 + u * blockDim.x + threadIdx.x;
-      m[u] = g < n_groups ? __ldg(gmax + (int64_t)q * n_groups + g) : 0u;
-    }
-#pragma unroll
-    for (int u = 0; u < 8; u++) {
-      const int g = b0 + u * blockDim.x + threadIdx.x;
-      if (g < n_groups) gm[g] = m[u];
-      live_groups += m[u] != 0;
-    }
-  }
-  atomicAdd(&n_valid_groups, live_groups);
-  __syncthreads();
-  uint32_t T = 1;                                    // nonzero keys: every valid item
-  if (n_valid_groups > k) {
-    auto get = [&](int i, uint32_t &v) { v = gm[i]; return v != 0; };
-    // the k-th largest group maximum to 16-bit resolution: its upper 16 bits
-    // (lower bits zero) are still a lower bound of the k-th best key
-    T = radix_kth_u32(get, n_groups, k, sh, 16);
-  }
-  // list the groups whose maximum reaches T
-  for (int b0 = 0; b0 < n_groups; b0 += blockDim.x) {
-    const int g = b0 + threadIdx.x;
-    const bool v = g < n_groups && gm[g] >= T;
-    const unsigned b = __ballot_sync(0xFFFFFFFFu, v);
-    int base = 0;
-    if (lane == 0 && b) base = atomicAdd(&n_list, __popc(b));
-    base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(b & ((1u << lane) - 1u));
-    if (v) glist[base] = g;
-  }
-  __syncthreads();
-  // scan their items: every thread keeps kScanU item loads in flight
-  constexpr int kScanU = 8;
-  const int lg = __ffs(G) - 1;                      // G is a power of two
-  const int total = n_list << lg;
-  const bool plain = S.pool == nullptr && S.block == 1;
+  if (blockIdx.x == 0 && threadIdx.x < 4) W.ctr[(int64_t)q * 4 + threadIdx.x] = 0u;
+  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int lsg = __ffsll(sgi) - 1;
+  uint32_t *sq = W.smax + (int64_t)q * W.sstride;
   const float *row = S.scores + (int64_t)q * S.stride;
   const bool row16 = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-  if (plain) {
-    // four consecutive items per thread and load (G is a multiple of 4)
-    constexpr int kV = 4;
-    for (int b0 = 0; b0 < total; b0 += 4 * kV * blockDim.x) {
-      float4 sc[kV];
-      int64_t base[kV];
+  const int64_t span = sgi > 4 * kStep ? sgi : 4 * kStep;
+  const int64_t n_pass = (S.n_items + span - 1) / span;
+  for (int64_t w = wid; w < n_pass; w += n_warps) {
+    uint32_t acc = 0;
+    for (int64_t c0 = w * span; c0 < (w + 1) * span; c0 += 4 * kStep) {
+      uint32_t m[4];
 #pragma unroll
-      for (int u = 0; u < kV; u++) {
-        const int f = b0 + 4 * (u * blockDim.x + threadIdx.x);
-        base[u] = -1;
-        sc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (f < total) {
-          base[u] = ((int64_t)glist[f >> lg] << lg) + (f & (G - 1));
-          if (row16 && base[u] + 4 <= nv) {
-            sc[u] = __ldg(reinterpret_cast<const float4 *>(row + base[u]));
-          } else {                                   // ragged end or unaligned row: element loads
-            const int64_t b = base[u];
-            if (b < nv) sc[u].x = __ldg(row + b);
-            if (b + 1 < nv) sc[u].y = __ldg(row + b + 1);
-            if (b + 2 < nv) sc[u].z = __ldg(row + b + 2);
-            if (b + 3 < nv) sc[u].w = __ldg(row + b + 3);
+      for (int u = 0; u < 4; u++) {
+        const int64_t i0 = c0 + u * kStep + lane * IPL;
+        m[u] = 0;
+        if (kPlain) {
+          if (i0 < nv) {
+            if (row16 && i0 + 4 <= nv) {
+              const float4 v = __ldg(reinterpret_cast<const float4 *>(row + i0));
+              m[u] = order_key(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));   // order_key is monotonic
+            } else {                                 // ragged end or unaligned row
+              for (int j = 0; j < 4; j++)
+                if (i0 + j < nv) m[u] = max(m[u], order_key(__ldg(row + i0 + j)));
+            }
           }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kV; u++) {
-        const float vals[4] = {sc[u].x, sc[u].y, sc[u].z, sc[u].w};
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-          const int64_t i = base[u] + e;
-          uint32_t kk = 0;
-          const bool ok = base[u] >= 0 && i < nv && (kk = order_key(vals[e])) >= T;
-          if (!__any_sync(0xFFFFFFFFu, ok)) continue;   // most rounds have no candidate
-          const unsigned b = __ballot_sync(0xFFFFFFFFu, ok);
-          int pos0 = 0;
-          if (lane == 0 && b) pos0 = atomicAdd(&n_cand, __popc(b));
-          pos0 = __shfl_sync(0xFFFFFFFFu, pos0, 0) + __popc(b & ((1u << lane) - 1u));
-          if (ok && pos0 < kCandCap) cand[pos0] = ((uint64_t)kk << 32) | (uint32_t)(~(uint32_t)i);
-        }
-      }
-    }
-  } else
-  for (int b0 = 0; b0 < total; b0 += kScanU * blockDim.x) {
-    uint64_t key[kScanU];
-    bool v[kScanU];
-#pragma unroll
-    for (int u = 0; u < kScanU; u++) {
-      const int f = b0 + u * blockDim.x + threadIdx.x;
-      key[u] = 0;
-      v[u] = false;
-      if (f < total) {
-        const int64_t i = ((int64_t)glist[f >> lg] << lg) + (f & (G - 1));
-        if (plain) {
-          v[u] = i < nv;
-          if (v[u]) key[u] = ((uint64_t)order_key(__ldg(row + i)) << 32) | (uint32_t)(~(uint32_t)i);
         } else {
-          v[u] = i < S.n_items && item_key(S, q, i, nv, key[u], status);
+          uint64_t key;
+          if (i0 < S.n_items && item_key(S, q, i0, nv, key, status)) m[u] = (uint32_t)(key >> 32);
+        }
+      }
+      if (sgi < kStep) {
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+          uint32_t x = m[u];
+          for (int o = 1; o < sgi / IPL; o <<= 1) x = max(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+          const int64_t i0 = c0 + u * kStep + lane * IPL;
+          if ((lane & (sgi / IPL - 1)) == 0 && i0 < S.n_items) sq[i0 >> lsg] = x;
+        }
+      } else {
+        uint32_t xs[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) xs[u] = __reduce_max_sync(0xFFFFFFFFu, m[u]);
+        if (sgi <= 2 * kStep) {                      // one or two steps per supergroup
+#pragma unroll
+          for (int u = 0; u < 4; u++) {
+            if (sgi == 2 * kStep && (u & 1)) continue;
+            const uint32_t x = sgi == 2 * kStep ? max(xs[u], xs[u | 1]) : xs[u];
+            const int64_t i0 = c0 + u * kStep;
+            if (lane == 0 && i0 < S.n_items) sq[i0 >> lsg] = x;
+          }
+        } else {
+          acc = max(acc, max(max(xs[0], xs[1]), max(xs[2], xs[3])));
         }
       }
     }
+    if (sgi > 2 * kStep && lane == 0 && w * span < S.n_items) sq[(w * span) >> lsg] = acc;
+  }
+}
+
+// Pass 2: grid (P, n_q).
+__global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S, int64_t sgi, int k, LongRowWs W,
+                                                                       int32_t *__restrict__ out, int *status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  uint64_t *keys = reinterpret_cast<uint64_t *>(smem_raw);               // [kCandCap] (last CTA)
+  int32_t *sel = reinterpret_cast<int32_t *>(keys + kCandCap);           // [kMaxK]
+  uint32_t *sv = reinterpret_cast<uint32_t *>(sel + kMaxK);              // [kSuperCap] supergroup maxima
+  __shared__ SelectShared sh;
+  sh.whist = sv + kSuperCap;                                             // [32][256]
+  __shared__ uint32_t T_sh, cnt[2];
+  __shared__ int n_vs, is_last;
+  const int q = blockIdx.y, P = gridDim.x, part = blockIdx.x;
+  const int nv = query_nv(S, q, status);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t *ctr = W.ctr + (int64_t)q * 4;
+  uint64_t *cq = W.cand + (int64_t)q * kCandCap;
+  const bool plain = S.pool == nullptr && S.block == 1;
+  const int64_t valid_items = plain ? nv : (S.pool != nullptr ? S.n_items : ((int64_t)nv + kBlock - 1) / kBlock);
+  const int ns = (int)((valid_items + sgi - 1) / sgi);                   // supergroups that may hold a valid item
+  if (threadIdx.x == 0) { n_vs = 0; T_sh = 1u; }                         // T = 1: every valid item
+  __syncthreads();
+  // ---- the supergroup maxima (16-B loads; slots past ns are never used)
+  {
+    const uint4 *src = reinterpret_cast<const uint4 *>(W.smax + (int64_t)q * W.sstride);
+    int vs = 0;
+    for (int i = threadIdx.x; 4 * i < ns; i += blockDim.x) {
+      const uint4 v = __ldcg(src + i);
+      const uint32_t e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int u = 0; u < kScanU; u++) {
-      const bool ok = v[u] && (uint32_t)(key[u] >> 32) >= T;
-      if (!__any_sync(0xFFFFFFFFu, ok)) continue;
-      const unsigned b = __ballot_sync(0xFFFFFFFFu, ok);
-      int base = 0;
-      if (lane == 0 && b) base = atomicAdd(&n_cand, __popc(b));
-      base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(b & ((1u << lane) - 1u));
-      if (ok && base < kCandCap) cand[base] = key[u];
+      for (int j = 0; j < 4; j++) {
+        const uint32_t x = 4 * i + j < ns ? e[j] : 0u;
+        sv[4 * i + j] = x;
+        vs += x != 0u;
+      }
+    }
+    vs = __reduce_add_sync(0xFFFFFFFFu, vs);
+    if (lane == 0 && vs) atomicAdd(&n_vs, vs);
+  }
+  __syncthreads();
+  // ---- T: the largest multiple of 2^16 that at least k supergroup maxima reach
+  if (n_vs > k) {
+    if (ns <= 4096) {
+      // one warp, no block barriers
+      if (warp == 0) {
+        uint32_t prefix = 0;
+        for (int bit = 31; bit >= 16; bit--) {
+          const uint32_t t = prefix | (1u << bit);
+          int c = 0;
+          for (int i = lane; 4 * i < ns; i += 32) {
+            const uint4 v = reinterpret_cast<const uint4 *>(sv)[i];
+            c += (v.x >= t) + (v.y >= t) + (v.z >= t) + (v.w >= t);
+          }
+          if (__reduce_add_sync(0xFFFFFFFFu, c) >= k) prefix = t;
+        }
+        if (lane == 0) T_sh = prefix;
+      }
+    } else {
+      uint32_t prefix = 0;
+      for (int bit = 31, it = 0; bit >= 16; bit--, it++) {
+        const uint32_t t = prefix | (1u << bit);
+        int c = 0;
+        for (int i = threadIdx.x; 4 * i < ns; i += blockDim.x) {
+          const uint4 v = reinterpret_cast<const uint4 *>(sv)[i];
+          c += (v.x >= t) + (v.y >= t) + (v.z >= t) + (v.w >= t);
+        }
+        c = __reduce_add_sync(0xFFFFFFFFu, c);
+        if (threadIdx.x == 0) cnt[it & 1] = 0;      // the other slot may still be read
+        __syncthreads();
+        if (lane == 0 && c) atomicAdd(&cnt[it & 1], (uint32_t)c);
+        __syncthreads();
+        if (cnt[it & 1] >= (uint32_t)k) prefix = t;
+      }
+      if (threadIdx.x == 0) T_sh = prefix;
     }
   }
   __syncthreads();
-  const int nc = n_cand;
-  if (nc <= kRankMax) {
-    select_rank(cand, nc, k, out + (int64_t)q * k, sel);
-  } else if (nc <= kSortMax) {
-    select_small(cand, nc, k, out + (int64_t)q * k, sel);
-  } else if (nc <= kCandCap) {
-    auto get = [&](int64_t i, uint64_t &key) { key = cand[i]; return true; };
-    select_and_write(get, nc, nc, k, out + (int64_t)q * k, sh, sel);
+  const uint32_t T = T_sh;
+  // ---- stream this CTA's share of the row, appending keys >= T
+  {
+    const int64_t per = ((valid_items + P - 1) / P + 15) / 16 * 16;
+    const int64_t i_lo = (int64_t)part * per, i_hi = min(valid_items, i_lo + per);
+    const float *row = S.scores + (int64_t)q * S.stride;
+    const bool row16 = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+    constexpr int kU = 4;
+    const int64_t step = plain ? 4 : 1;
+    for (int64_t b0 = i_lo; b0 < i_hi; b0 += kU * step * blockDim.x) {
+      float4 sc[kU];
+      uint64_t gk[kU];
+#pragma unroll
+      for (int u = 0; u < kU; u++) {
+        const int64_t i0 = b0 + (u * (int64_t)blockDim.x + threadIdx.x) * step;
+        sc[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        gk[u] = 0;
+        if (plain) {
+          if (i0 < i_hi) {
+            if (row16 && i0 + 4 <= i_hi) {
+              sc[u] = __ldcg(reinterpret_cast<const float4 *>(row + i0));
+            } else {
+              if (i0 < i_hi) sc[u].x = __ldcg(row + i0);
+              if (i0 + 1 < i_hi) sc[u].y = __ldcg(row + i0 + 1);
+              if (i0 + 2 < i_hi) sc[u].z = __ldcg(row + i0 + 2);
+              if (i0 + 3 < i_hi) sc[u].w = __ldcg(row + i0 + 3);
+            }
+          }
+        } else if (i0 < i_hi) {
+          uint64_t key;
+          if (item_key(S, q, i0, nv, key, status)) gk[u] = key;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; u++) {
+        const int64_t i0 = b0 + (u * (int64_t)blockDim.x + threadIdx.x) * step;
+#pragma unroll
+        for (int e = 0; e < (plain ? 4 : 1); e++) {
+          uint64_t key;
+          bool ok;
+          if (plain) {
+            const float x = e == 0 ? sc[u].x : e == 1 ? sc[u].y : e == 2 ? sc[u].z : sc[u].w;
+            const uint32_t kk = order_key(x);
+            ok = i0 + e < i_hi && kk >= T;
+            key = ((uint64_t)kk << 32) | (uint32_t)(~(uint32_t)(i0 + e));
+          } else {
+            key = gk[u];
+            ok = key != 0 && (uint32_t)(key >> 32) >= T;
+          }
+          if (!__any_sync(0xFFFFFFFFu, ok)) continue;   // most rounds have no candidate
+          const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
+          uint32_t base = 0;
+          if (lane == 0) base = atomicAdd(ctr + 0, (uint32_t)__popc(bal));
+          base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(bal & ((1u << lane) - 1u));
+          if (ok && base < (uint32_t)kCandCap) cq[base] = key;
+        }
+      }
+    }
+  }
+  // ---- the last CTA of this row selects
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(ctr + 1, 1u) == (uint32_t)(P - 1);
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  const uint32_t nc_all = atomicAdd(ctr + 0, 0u);
+  int32_t *oq = out + (int64_t)q * k;
+  if (nc_all <= (uint32_t)kCandCap) {
+    const int nc = (int)nc_all;
+    for (int i0 = 0; i0 < nc; i0 += 4 * blockDim.x) {
+      uint64_t v[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int i = i0 + u * blockDim.x + threadIdx.x;
+        v[u] = i < nc ? __ldcg(cq + i) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int i = i0 + u * blockDim.x + threadIdx.x;
+        if (i < nc) keys[i] = v[u];
+      }
+    }
+    __syncthreads();
+    // sv (64 KB) holds the bucket scatter, whist (32 KB) the bucket counters
+    select_bucket(keys, nc, k, oq, reinterpret_cast<uint64_t *>(sv), sh.whist);
   } else {
     // too many ties at T for the buffer: exact selection straight over the row
     __shared__ int nvi;
@@ -513,7 +710,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_group_select_kernel(TopkSrc
     atomicAdd(&nvi, c);
     __syncthreads();
     auto get = [&](int64_t i, uint64_t &key) { return item_key(S, q, i, nv, key, status); };
-    select_and_write(get, S.n_items, nvi, k, out + (int64_t)q * k, sh, sel);
+    select_and_write(get, S.n_items, nvi, k, oq, sh, sel);
   }
 }
 
@@ -522,26 +719,14 @@ static int64_t topk_items(int64_t n_max, int block, bool pool) {
   return pool ? (int64_t)kPoolSlots : (block == 1 ? n_max : (n_max + kBlock - 1) / kBlock);
 }
 
-// Group size for long rows: the smallest power of two >= 8 that keeps the
-// groups within kMaxGroups, doubled while at least 4k groups remain.
-static int topk_group(int64_t n_items, int k) {
-  int G = 8;
-  while (G <= kMaxGroup && ((n_items + G - 1) / G > kMaxGroups || n_items / (2 * G) >= 4 * (int64_t)k) &&
-         !(G == kMaxGroup && (n_items + G - 1) / G <= kMaxGroups))
-    G <<= 1;
-  return G;
-}
-
 size_t topk_workspace_bytes(int n_q, int64_t n_items, int k) {
   if (n_items <= kDirectCap) return 0;
-  const int G = topk_group(n_items, k);
-  return (size_t)n_q * ((n_items + G - 1) / G) * 4;
+  return long_row_ws_bytes(n_q, n_items, k);
 }
 
 bool topk_items_supported(int64_t n_items, int k) {
-  if (n_items <= kDirectCap) return true;
-  const int G = topk_group(n_items, k);
-  return G <= kMaxGroup && (n_items + G - 1) / G <= kMaxGroups;
+  (void)k;
+  return n_items < ((int64_t)1 << 31) - 64;          // int32 item indices
 }
 
 cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max, int k,
@@ -555,26 +740,34 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
   S.n_max = n_max;
   S.n_items = topk_items(n_max, block, pool != nullptr);
   const size_t dsm_direct = (size_t)kDirectCap * 8 + (size_t)kMaxK * 4 + 32 * 256 * 4;
-  const size_t dsm_group = (size_t)kCandCap * 8 + (size_t)kMaxGroups * 8 + (size_t)kMaxK * 4 + 32 * 256 * 4;
+  const size_t dsm_collect = (size_t)kCandCap * 8 + (size_t)kMaxK * 4 + (size_t)kSuperCap * 4 + 32 * 256 * 4;
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_done[64] = {};
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
     cudaFuncSetAttribute(topk_direct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm_direct);
-    cudaFuncSetAttribute(topk_group_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm_group);
+    cudaFuncSetAttribute(topk_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm_collect);
     attr_done[dev] = true;
   }
   if (S.n_items <= kDirectCap) {
     topk_direct_kernel<<<n_q, kTopkThreads, dsm_direct, st>>>(S, k, out, status);
     return cudaGetLastError();
   }
-  const int G = topk_group(S.n_items, k);
-  const int n_groups = (int)((S.n_items + G - 1) / G);
-  uint32_t *gmax = static_cast<uint32_t *>(ws);
-  const int64_t warp_steps = ((int64_t)n_groups * G + 32 * (G >= 32 ? G / 32 : 1) - 1) / (32 * (G >= 32 ? G / 32 : 1));
-  const int64_t gx = (warp_steps + 7) / 8;            // one warp step per warp: every load in flight at once
-  topk_groupmax_kernel<<<dim3((unsigned)gx, n_q), 256, 0, st>>>(S, G, n_groups, gmax, status);
-  topk_group_select_kernel<<<n_q, kTopkThreads, dsm_group, st>>>(S, G, n_groups, k, gmax, out, status);
+  const int64_t sgi = long_row_sgi(S.n_items, k);
+  const LongRowWs W = long_row_ws(ws, n_q, S.n_items, k);
+  const bool plain = pool == nullptr && block == 1;
+  const int64_t span = std::max<int64_t>(sgi, plain ? 4 * 128 : 4 * 32);
+  const int64_t n_pass = (S.n_items + span - 1) / span;
+  const int64_t gx = std::min<int64_t>((n_pass + 7) / 8, 65535);       // one warp pass per warp
+  if (plain)
+    topk_smax_kernel<true><<<dim3((unsigned)gx, n_q), 256, 0, st>>>(S, sgi, W, status);
+  else
+    topk_smax_kernel<false><<<dim3((unsigned)gx, n_q), 256, 0, st>>>(S, sgi, W, status);
+  int sms = 148;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // one CTA per SM (shared memory): a single wave over all rows
+  const int64_t P = std::max<int64_t>(1, std::min<int64_t>(sms / n_q, S.n_items / 4096));
+  topk_collect_kernel<<<dim3((unsigned)P, n_q), kCollectThreads, dsm_collect, st>>>(S, sgi, k, W, out, status);
   return cudaGetLastError();
 }
 

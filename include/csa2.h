@@ -245,10 +245,11 @@ csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t 
  * the library's users.
  *
  * Same arguments, results and errors as csa2_topk, without the workspace.  The
- * scratch it needs (4 bytes per group of scores, for rows longer than 16,384
- * items; for 1,048,576-entry rows and k = 512 that is 32 KiB per query) lives in
- * one fixed device array of CSA2_TOPK_NOALLOC_SCRATCH_BYTES (1 MiB) that every
- * GPU which loads the library holds until the process exits.  A call whose
+ * scratch it needs (rows longer than 16,384 items only: 4 bytes per group of
+ * scores plus 80 KiB per query; for 1,048,576-entry rows and k = 512 that is
+ * 208 KiB per query) lives in one fixed device array of
+ * CSA2_TOPK_NOALLOC_SCRATCH_BYTES (4 MiB) that every GPU which loads the
+ * library holds until the process exits.  A call whose
  * scratch would exceed it returns CSA2_ERR_WORKSPACE and launches nothing (use
  * csa2_topk with a workspace instead).  The call allocates nothing and calls no
  * allocating routine.  The first call on a device looks up the array's device
@@ -256,9 +257,9 @@ csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t 
  * All calls share the one array: calls that can run at the same time on the
  * GPU (other streams, other host threads) race and must be serialised by the
  * caller.  Nothing has to be cleared between calls: every scratch value a call
- * reads is written earlier in that same call.
+ * reads is written (or cleared) earlier in that same call.
  */
-#define CSA2_TOPK_NOALLOC_SCRATCH_BYTES (1u << 20)
+#define CSA2_TOPK_NOALLOC_SCRATCH_BYTES (4u << 20)
 csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stride, int n_q, const int32_t *n_valid,
                               int64_t n_max, int k, int block, const int32_t *pool_blocks, int32_t *out,
                               csa2_stream_t stream);

@@ -39,7 +39,7 @@ def _both(lib, rows, n_valid, k, block=1):
 
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls(lib):
-    # call 1: eight 1,048,576-entry rows (256 KiB of scratch), Zipf-like skew and ties
+    # call 1: eight 1,048,576-entry rows (1.6 MiB of scratch), Zipf-like skew and ties
     n = 1 << 20
     rows = np.stack([G.uniform_f32_scores(300 + i, i, n, 0 if i % 2 else 97) for i in range(8)])
     rows[1] = np.sign(rows[1]) * np.abs(rows[1]) ** 9
@@ -56,8 +56,12 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(lib):
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(lib):
-    n = 1 << 20                              # 8,192 groups x 4 B per query
-    too_many = (1 << 20) // (8192 * 4) + 1   # one query more than the 1 MiB array holds
+    n = 1 << 20
+    scratch = 4 << 20                        # CSA2_TOPK_NOALLOC_SCRATCH_BYTES
+    per_query = lib.csa2_workspace_size(lib.CSA2_OP_TOPK, 1, n, 512)
+    too_many = scratch // per_query + 1      # one query more than the array holds
+    assert lib.csa2_workspace_size(lib.CSA2_OP_TOPK, too_many, n, 512) > scratch
+    assert lib.csa2_workspace_size(lib.CSA2_OP_TOPK, too_many - 1, n, 512) <= scratch
     dummy = 1 << 20                          # never dereferenced: the call is rejected first
     with pytest.raises(lib.CSA2Error) as e:
         lib.csa2_topk_noalloc(dummy, n, too_many, dummy, n, 512, 1, None, dummy)
