@@ -201,69 +201,6 @@ __device__ void select_and_write(Get get, int64_t n, int n_valid_items, int k, i
   for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < take ? sel[i] : -1;
 }
 
-// Descending bitonic sort of n_pow2 64-bit keys in shared memory.
-__device__ void bitonic_sort_desc_u64(uint64_t *a, int n_pow2) {
-  for (int size = 2; size <= n_pow2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < n_pow2; i += blockDim.x) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool desc = (i & size) == 0;
-          const uint64_t x = a[i], y = a[j];
-          if ((x < y) == desc) { a[i] = y; a[j] = x; }
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
-
-// Exact top-k of n unique keys already in shared memory (capacity >= the next
-// power of two of n), by sorting them: cheaper than radix passes for small n.
-// The keys array is reordered.
-__device__ void select_small(uint64_t *keys, int n, int k, int32_t *out, int32_t *sel) {
-  int np2 = 1;
-  while (np2 < n) np2 <<= 1;
-  for (int i = n + threadIdx.x; i < np2; i += blockDim.x) keys[i] = 0;   // below every valid key
-  __syncthreads();
-  bitonic_sort_desc_u64(keys, np2);
-  const int take = min(k, n);
-  int sp2 = 1;
-  while (sp2 < take) sp2 <<= 1;
-  for (int i = threadIdx.x; i < sp2; i += blockDim.x)
-    sel[i] = i < take ? (int32_t)(~(uint32_t)(keys[i] & 0xFFFFFFFFu)) : INT32_MAX;
-  __syncthreads();
-  bitonic_sort(sel, sp2);
-  for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < take ? sel[i] : -1;
-}
-
-constexpr int kSortMax = 4096;     // sets up to this size are selected by sorting
-constexpr int kRankMax = 1536;     // sets up to this size are selected by ranking
-
-// Exact top-k of n unique keys in shared memory by counting: a key is selected
-// iff fewer than k keys are larger; its output slot is the number of selected
-// keys with a smaller index.  O(n^2) comparisons, two barriers.
-__device__ void select_rank(const uint64_t *keys, int n, int k, int32_t *out, int32_t *sel) {
-  const int take = min(k, n);
-  __shared__ int n_sel;
-  if (threadIdx.x == 0) n_sel = 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const uint64_t ki = keys[i];
-    int above = 0;
-    for (int j = 0; j < n; j++) above += keys[j] > ki;
-    if (above < take) sel[atomicAdd(&n_sel, 1)] = (int32_t)(~(uint32_t)(ki & 0xFFFFFFFFu));
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < take; i += blockDim.x) {
-    const int32_t xi = sel[i];
-    int before = 0;
-    for (int j = 0; j < take; j++) before += sel[j] < xi;
-    out[before] = xi;
-  }
-  for (int i = take + threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
-}
-
 // Block-wide exclusive scans over nb counters in shared memory (nb a multiple
 // of blockDim.x, blockDim.x a multiple of 32): suffix (counts of the bins
 // above) and prefix (counts of the bins below).
@@ -285,9 +222,8 @@ __device__ void block_offsets(uint32_t *h, int nb) {
   __syncthreads();
   if (kSuffix ? lane == 0 : lane == 31) wsum[warp] = incl;
   __syncthreads();
-  uint32_t run = incl - part;
-  for (int w = 0; w < nw; w++)
-    if (kSuffix ? w > warp : w < warp) run += wsum[w];
+  const bool other = lane < nw && (kSuffix ? lane > warp : lane < warp);
+  uint32_t run = incl - part + __reduce_add_sync(0xFFFFFFFFu, other ? wsum[lane] : 0u);
   if (kSuffix) {
     for (int j = per - 1; j >= 0; j--) { const uint32_t v = h[b0 + j]; h[b0 + j] = run; run += v; }
   } else {
@@ -296,83 +232,155 @@ __device__ void block_offsets(uint32_t *h, int nb) {
   __syncthreads();
 }
 
-// Exact top-k of n unique keys in shared memory (n <= kCandCap) in O(n) work
-// and a few barriers, for candidate sets a little larger than k.  The keys
-// are bucketed by value (4,096 buckets of power-of-two width over the range
-// present) and scattered bucket by bucket from the top; a key's rank is the
-// number of keys in the buckets above plus the larger keys in its own.  The
-// k selected indices are placed in ascending order the same way, bucketed by
-// index.  tmp: n 64-bit slots; bins: 8,192 counters.  out[0..k): ascending
-// indices, -1 padding.  Heavily tied buckets cost up to their size squared.
-constexpr int kBuckets = 4096;
+// Warp-wide sum of one int per lane (shuffles; every lane gets it).
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
 
-__device__ void select_bucket(const uint64_t *keys, int n, int k, int32_t *out, uint64_t *tmp, uint32_t *bins) {
-  __shared__ unsigned long long lo_sh, hi_sh;
-  __shared__ int max_idx_sh;
-  uint32_t *hist = bins, *cur = bins + kBuckets;
+// Block-wide: the rem-th largest (with multiplicity) of the values v[i] with
+// sel(i), i < n (shared memory), found eight bits per step from bit 31 down to
+// bit `low` (a multiple of 8); the result has its bits below `low` cleared, so
+// at least rem selected values reach it.  Each step: a 256-bin histogram of
+// the next digit (shared-memory atomics), then warp 0 locates the digit by a
+// suffix scan over the bins.  hist: 256 counters of shared memory.
+template <class Sel>
+__device__ uint32_t block_kth256(const uint32_t *v, int n, int rem, int low, Sel sel, uint32_t *hist) {
+  __shared__ uint32_t prefix_sh, pmask_sh;
+  __shared__ int rem_sh;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) { prefix_sh = 0u; pmask_sh = 0u; rem_sh = rem; }
+  for (int shift = 24; shift >= low; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
+    __syncthreads();
+    const uint32_t prefix = prefix_sh, pmask = pmask_sh;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint32_t x = v[i];
+      if ((x & pmask) == prefix && sel(i)) atomicAdd(&hist[(x >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // lane l owns digits 8l .. 8l+7; suffix sums over the lanes above
+      uint32_t c[8], part = 0u;
+#pragma unroll
+      for (int j = 0; j < 8; j++) { c[j] = hist[8 * lane + j]; part += c[j]; }
+      uint32_t incl = part;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+        if (lane + o < 32) incl += t;
+      }
+      const int r = rem_sh;
+      uint32_t above = incl - part;                  // values in the digits of the lanes above
+      if (above < (uint32_t)r && (uint32_t)r <= incl) {
+#pragma unroll
+        for (int j = 7; j >= 0; j--) {
+          if (above + c[j] >= (uint32_t)r) {
+            prefix_sh = prefix | ((uint32_t)(8 * lane + j) << shift);
+            pmask_sh = pmask | (255u << shift);
+            rem_sh = r - (int)above;
+            break;
+          }
+          above += c[j];
+        }
+      }
+    }
+    __syncthreads();
+  }
+  return prefix_sh;
+}
+
+// Block-wide min / max of one value per thread; every thread gets the result.
+// The two slot rows alternate, so back-to-back calls need one barrier each.
+struct BlockReduce {
+  uint32_t (*slots)[32];
+  int parity;
+  template <bool kMax>
+  __device__ uint32_t run(uint32_t v) {
+    const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    v = kMax ? __reduce_max_sync(0xFFFFFFFFu, v) : __reduce_min_sync(0xFFFFFFFFu, v);
+    if (lane == 0) slots[parity][threadIdx.x >> 5] = v;
+    __syncthreads();
+    const uint32_t w = lane < nw ? slots[parity][lane] : (kMax ? 0u : ~0u);
+    parity ^= 1;
+    return kMax ? __reduce_max_sync(0xFFFFFFFFu, w) : __reduce_min_sync(0xFFFFFFFFu, w);
+  }
+};
+
+// Exact top-k of n unique nonzero keys in shared memory (n <= kCandCap), for
+// candidate sets a little larger than k.  The k-th largest key is found on
+// the score halves (sk[i] = keys[i] >> 32) by a radix-256 search, then, among
+// the keys tied on that score, on the index halves.  The block then compacts
+// the selected indices and places them in ascending order by bucketing them
+// by index (buckets of power-of-two width; a few indices per bucket).  keys
+// and sk are reused as scratch.  sel: >= k ints; bins: >= 4096 counters.
+// out[0..k): ascending indices, -1 padding.
+__device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t *out, int32_t *sel, uint32_t *bins) {
+  __shared__ int cnt_sh[2];
+  __shared__ int n_sel;
+  __shared__ uint32_t red_slots[2][32];
+  BlockReduce br{red_slots, 0};
   const int take = min(k, n);
-  if (threadIdx.x == 0) { lo_sh = ~0ull; hi_sh = 0ull; max_idx_sh = 0; }
-  for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) { hist[i] = 0; cur[i] = 0; }
-  __syncthreads();
-  // ---- value range -> bucket width 2^sh
-  unsigned long long lo = ~0ull, hi = 0ull;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    lo = min(lo, (unsigned long long)keys[i]);
-    hi = max(hi, (unsigned long long)keys[i]);
-  }
-  for (int o = 16; o > 0; o >>= 1) {
-    lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
-    hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
-  }
-  if ((threadIdx.x & 31) == 0) { atomicMin(&lo_sh, lo); atomicMax(&hi_sh, hi); }
-  __syncthreads();
-  lo = lo_sh;
-  const unsigned long long range = n > 0 ? hi_sh - lo : 0ull;
-  const int sh = range == 0 ? 0 : max(0, 64 - __clzll((long long)range) - 12);   // (range >> sh) < 4096
-  // ---- scatter by value bucket, buckets in descending order
-  for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&hist[(uint32_t)((keys[i] - lo) >> sh)], 1u);
-  __syncthreads();
-  block_offsets<true>(hist, kBuckets);               // hist[b] <- keys in the buckets above b
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const uint32_t b = (uint32_t)((keys[i] - lo) >> sh);
-    tmp[hist[b] + atomicAdd(&cur[b], 1u)] = keys[i];
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) { n_sel = 0; cnt_sh[0] = 0; cnt_sh[1] = 0; }
+  uint64_t K = 1;                                    // keys >= K are selected
+  if (take < n) {
+    const uint32_t t32 = block_kth256(sk, n, take, 0, [](int) { return true; }, bins);
+    int c_gt = 0, c_eq = 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) { c_gt += sk[i] > t32; c_eq += sk[i] == t32; }
+    c_gt = warp_sum(c_gt);
+    c_eq = warp_sum(c_eq);
+    if (lane == 0) { atomicAdd(&cnt_sh[0], c_gt); atomicAdd(&cnt_sh[1], c_eq); }
+    __syncthreads();
+    const int need = take - cnt_sh[0];
+    uint32_t tlo = 0u;
+    if (need < cnt_sh[1]) {
+      // several keys tie on the score: the `need` largest index halves among them
+      for (int i = threadIdx.x; i < n; i += blockDim.x) sk[i] = sk[i] == t32 ? (uint32_t)keys[i] : 0u;
+      __syncthreads();
+      tlo = block_kth256(sk, n, need, 0, [](int) { return true; }, bins);
+    }
+    K = ((uint64_t)t32 << 32) | tlo;
   }
   __syncthreads();
-  // ---- rank = keys above the bucket + larger keys inside it; keep rank < take
-  // (the cursors are no longer read: their space holds the selection by rank)
-  int32_t *sel = reinterpret_cast<int32_t *>(cur);
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const uint64_t x = tmp[i];
-    const uint32_t b = (uint32_t)((x - lo) >> sh);
-    int rank = (int)hist[b];
-    for (int j = (int)hist[b]; j < n && (uint32_t)((tmp[j] - lo) >> sh) == b; j++) rank += tmp[j] > x;
-    if (rank < take) sel[rank] = (int32_t)(~(uint32_t)(x & 0xFFFFFFFFu));
+  // ---- compact the selected indices
+  for (int b0 = 0; b0 < n; b0 += blockDim.x) {
+    const int i = b0 + threadIdx.x;
+    const uint64_t x = i < n ? keys[i] : 0ull;
+    const bool ok = x != 0ull && x >= K;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
+    if (!bal) continue;
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&n_sel, __popc(bal));
+    base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(bal & ((1u << lane) - 1u));
+    if (ok) sel[base] = (int32_t)(~(uint32_t)(x & 0xFFFFFFFFu));
   }
   __syncthreads();
-  // ---- ascending index order: 2,048 index buckets (hist halves: counts, cursors)
-  uint32_t *h2 = hist, *c2 = hist + 2048;
-  for (int i = threadIdx.x; i < kBuckets; i += blockDim.x) hist[i] = 0;
+  // ---- ascending index order: 2,048 index buckets (counts, cursors); the
+  // key buffer (the keys are in registers now) receives them bucket by bucket
+  uint32_t *h2 = bins, *c2 = bins + 2048;
+  for (int i = threadIdx.x; i < 4096; i += blockDim.x) bins[i] = 0;
   int mx = 0;
   for (int i = threadIdx.x; i < take; i += blockDim.x) mx = max(mx, sel[i]);
-  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-  if ((threadIdx.x & 31) == 0) atomicMax(&max_idx_sh, mx);
-  __syncthreads();
-  const int sh2 = max(0, 32 - __clz(max_idx_sh) - 11);  // (max index >> sh2) < 2048
+  const int max_idx = (int)br.run<true>((uint32_t)mx);  // its barrier also orders the clearing above
+  const int sh2 = max(0, 32 - __clz(max_idx) - 11);    // (max index >> sh2) < 2048
   for (int i = threadIdx.x; i < take; i += blockDim.x) atomicAdd(&h2[sel[i] >> sh2], 1u);
   __syncthreads();
-  block_offsets<false>(h2, 2048);                    // h2[b] <- indices in the buckets below b
-  int32_t *by_idx = reinterpret_cast<int32_t *>(tmp);
+  block_offsets<false>(h2, 2048);                      // h2[b] <- indices in the buckets below b
+  int32_t *by = reinterpret_cast<int32_t *>(keys);
   for (int i = threadIdx.x; i < take; i += blockDim.x) {
     const int b = sel[i] >> sh2;
-    by_idx[h2[b] + atomicAdd(&c2[b], 1u)] = sel[i];
+    by[h2[b] + atomicAdd(&c2[b], 1u)] = sel[i];
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < take; i += blockDim.x) {
-    const int32_t x = by_idx[i];
-    const int b = x >> sh2;
-    int before = (int)h2[b];
-    for (int j = (int)h2[b]; j < take && (by_idx[j] >> sh2) == b; j++) before += by_idx[j] < x;
-    out[before] = x;
+  for (int p = threadIdx.x; p < take; p += blockDim.x) {
+    const int32_t v = by[p];
+    const int b = v >> sh2;
+    const int start = (int)h2[b], cnt = (int)c2[b];
+    int r = 0;
+    for (int j = start; j < start + cnt; j++) r += by[j] < v;   // buckets hold very few indices
+    out[start + r] = v;
   }
   for (int i = take + threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
   __syncthreads();
@@ -403,13 +411,67 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
   }
   __syncthreads();
   const int n = n_keys;
-  if (n <= kRankMax) {
-    select_rank(keys, n, k, out + (int64_t)q * k, sel);
-  } else if (n <= kSortMax) {
-    select_small(keys, n, k, out + (int64_t)q * k, sel);
-  } else {
+  int32_t *oq = out + (int64_t)q * k;
+  uint32_t *sk = sh.whist + 32 * 256;                                            // [kCandCap]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (n <= 2048) {
+    for (int i = threadIdx.x; i < ((n + 3) & ~3); i += blockDim.x) sk[i] = i < n ? (uint32_t)(keys[i] >> 32) : 0u;
+    __syncthreads();
+    select_block(keys, sk, n, k, oq, sel, sh.whist);
+    return;
+  }
+  // Larger sets: a threshold from the maxima of groups of gsz keys (the
+  // largest power of two <= 32 leaving >= 4k groups): at least k groups reach
+  // the k-th largest maximum T, so the top-k keys all have scores >= T; those
+  // candidates go to select_warp.
+  int gsz = 32;
+  while (gsz > 1 && n / gsz < 4 * k) gsz >>= 1;
+  bool done = false;
+  if (gsz >= 2) {
+    __shared__ uint32_t T_sh;
+    __shared__ int n_c;
+    const int ng = (n + gsz - 1) / gsz;
+    // group maxima of the score halves: gsz lanes per group
+    for (int b0 = warp * 32; b0 < ng * gsz; b0 += nw * 32) {
+      const int i = b0 + lane;
+      uint32_t v = i < n ? (uint32_t)(keys[i] >> 32) : 0u;
+      for (int o = 1; o < gsz; o <<= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+      if ((lane & (gsz - 1)) == 0 && i / gsz < ng) sk[i / gsz] = v;
+    }
+    for (int i = ng + threadIdx.x; i < ((ng + 3) & ~3); i += blockDim.x) sk[i] = 0u;
+    if (threadIdx.x == 0) { T_sh = 1u; n_c = 0; }
+    __syncthreads();
+    if (ng > k) {
+      const uint32_t t = block_kth256(sk, ng, k, 16, [](int) { return true; }, reinterpret_cast<uint32_t *>(sel));
+      if (threadIdx.x == 0) T_sh = t;
+    }
+    __syncthreads();
+    const uint32_t T = T_sh;
+    uint64_t *cand = reinterpret_cast<uint64_t *>(sh.whist);                     // [kCandCap / 2]
+    constexpr int kDirCand = kCandCap / 2;
+    for (int b0 = 0; b0 < n; b0 += blockDim.x) {
+      const int i = b0 + threadIdx.x;
+      const uint64_t x = i < n ? keys[i] : 0ull;
+      const bool ok = i < n && (uint32_t)(x >> 32) >= T;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
+      if (!bal) continue;
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&n_c, __popc(bal));
+      base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(bal & ((1u << lane) - 1u));
+      if (ok && base < kDirCand) cand[base] = x;
+    }
+    __syncthreads();
+    const int nc = n_c;
+    if (nc <= kDirCand) {
+      for (int i = threadIdx.x; i < ((nc + 3) & ~3); i += blockDim.x) sk[i] = i < nc ? (uint32_t)(cand[i] >> 32) : 0u;
+      __syncthreads();
+      select_block(cand, sk, nc, k, oq, sel, reinterpret_cast<uint32_t *>(keys));  // keys is free: bucket counters
+      done = true;
+    }
+  }
+  if (!done) {
     auto get = [&](int64_t i, uint64_t &key) { key = keys[i]; return true; };
-    select_and_write(get, n, n, k, out + (int64_t)q * k, sh, sel);
+    select_and_write(get, n, n, k, oq, sh, sel);
   }
 }
 
@@ -574,79 +636,72 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
     if (lane == 0 && vs) atomicAdd(&n_vs, vs);
   }
   __syncthreads();
-  // ---- T: the largest multiple of 2^16 that at least k supergroup maxima reach
+  // ---- T: the largest multiple of 2^16 that at least k supergroup maxima
+  // reach, bit by bit from the top, by warp 0 alone (sv is zero-padded)
   if (n_vs > k) {
-    if (ns <= 4096) {
-      // one warp, no block barriers
-      if (warp == 0) {
-        uint32_t prefix = 0;
-        for (int bit = 31; bit >= 16; bit--) {
-          const uint32_t t = prefix | (1u << bit);
-          int c = 0;
-          for (int i = lane; 4 * i < ns; i += 32) {
-            const uint4 v = reinterpret_cast<const uint4 *>(sv)[i];
-            c += (v.x >= t) + (v.y >= t) + (v.z >= t) + (v.w >= t);
-          }
-          if (__reduce_add_sync(0xFFFFFFFFu, c) >= k) prefix = t;
-        }
-        if (lane == 0) T_sh = prefix;
-      }
-    } else {
-      uint32_t prefix = 0;
-      for (int bit = 31, it = 0; bit >= 16; bit--, it++) {
-        const uint32_t t = prefix | (1u << bit);
-        int c = 0;
-        for (int i = threadIdx.x; 4 * i < ns; i += blockDim.x) {
-          const uint4 v = reinterpret_cast<const uint4 *>(sv)[i];
-          c += (v.x >= t) + (v.y >= t) + (v.z >= t) + (v.w >= t);
-        }
-        c = __reduce_add_sync(0xFFFFFFFFu, c);
-        if (threadIdx.x == 0) cnt[it & 1] = 0;      // the other slot may still be read
-        __syncthreads();
-        if (lane == 0 && c) atomicAdd(&cnt[it & 1], (uint32_t)c);
-        __syncthreads();
-        if (cnt[it & 1] >= (uint32_t)k) prefix = t;
-      }
-      if (threadIdx.x == 0) T_sh = prefix;
-    }
+    const uint32_t t = block_kth256(sv, ns, k, 16, [](int) { return true; }, sh.whist);
+    if (threadIdx.x == 0) T_sh = t;
   }
   __syncthreads();
   const uint32_t T = T_sh;
-  // ---- stream this CTA's share of the row, appending keys >= T
+  // ---- stream the supergroups of this CTA's share that reach T, appending keys >= T
   {
-    const int64_t per = ((valid_items + P - 1) / P + 15) / 16 * 16;
-    const int64_t i_lo = (int64_t)part * per, i_hi = min(valid_items, i_lo + per);
+    const int per = (ns + P - 1) / P;
+    const int s_lo = part * per, s_hi = min(ns, s_lo + per);
     const float *row = S.scores + (int64_t)q * S.stride;
     const bool row16 = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+    // list them (order irrelevant)
+    int32_t *slist = reinterpret_cast<int32_t *>(keys);     // keys is used by the last CTA only after this
+    __shared__ int n_sl;
+    if (threadIdx.x == 0) n_sl = 0;
+    __syncthreads();
+    for (int b0 = s_lo; b0 < s_hi; b0 += blockDim.x) {
+      const int i = b0 + threadIdx.x;
+      const bool ok = i < s_hi && sv[i] >= T && sv[i] != 0u;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
+      if (!bal) continue;
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&n_sl, __popc(bal));
+      base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(bal & ((1u << lane) - 1u));
+      if (ok) slist[base] = i;
+    }
+    __syncthreads();
+    const int nsl = n_sl;
+    const int64_t total = (int64_t)nsl * sgi;                 // items of the listed supergroups
     constexpr int kU = 4;
     const int64_t step = plain ? 4 : 1;
-    for (int64_t b0 = i_lo; b0 < i_hi; b0 += kU * step * blockDim.x) {
+    const int lsg = __ffsll(sgi) - 1;
+    for (int64_t b0 = 0; b0 < total; b0 += kU * step * blockDim.x) {
       float4 sc[kU];
       uint64_t gk[kU];
+      int64_t base_i[kU];
 #pragma unroll
       for (int u = 0; u < kU; u++) {
-        const int64_t i0 = b0 + (u * (int64_t)blockDim.x + threadIdx.x) * step;
+        const int64_t f = b0 + (u * (int64_t)blockDim.x + threadIdx.x) * step;   // flat position
         sc[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         gk[u] = 0;
-        if (plain) {
-          if (i0 < i_hi) {
-            if (row16 && i0 + 4 <= i_hi) {
+        base_i[u] = -1;
+        if (f < total) {
+          const int64_t i0 = ((int64_t)slist[f >> lsg] << lsg) + (f & (sgi - 1));
+          base_i[u] = i0;
+          if (plain) {
+            if (row16 && i0 + 4 <= nv) {
               sc[u] = __ldcg(reinterpret_cast<const float4 *>(row + i0));
             } else {
-              if (i0 < i_hi) sc[u].x = __ldcg(row + i0);
-              if (i0 + 1 < i_hi) sc[u].y = __ldcg(row + i0 + 1);
-              if (i0 + 2 < i_hi) sc[u].z = __ldcg(row + i0 + 2);
-              if (i0 + 3 < i_hi) sc[u].w = __ldcg(row + i0 + 3);
+              if (i0 < nv) sc[u].x = __ldcg(row + i0);
+              if (i0 + 1 < nv) sc[u].y = __ldcg(row + i0 + 1);
+              if (i0 + 2 < nv) sc[u].z = __ldcg(row + i0 + 2);
+              if (i0 + 3 < nv) sc[u].w = __ldcg(row + i0 + 3);
             }
+          } else {
+            uint64_t key;
+            if (i0 < S.n_items && item_key(S, q, i0, nv, key, status)) gk[u] = key;
           }
-        } else if (i0 < i_hi) {
-          uint64_t key;
-          if (item_key(S, q, i0, nv, key, status)) gk[u] = key;
         }
       }
 #pragma unroll
       for (int u = 0; u < kU; u++) {
-        const int64_t i0 = b0 + (u * (int64_t)blockDim.x + threadIdx.x) * step;
+        const int64_t i0 = base_i[u];
 #pragma unroll
         for (int e = 0; e < (plain ? 4 : 1); e++) {
           uint64_t key;
@@ -654,7 +709,7 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
           if (plain) {
             const float x = e == 0 ? sc[u].x : e == 1 ? sc[u].y : e == 2 ? sc[u].z : sc[u].w;
             const uint32_t kk = order_key(x);
-            ok = i0 + e < i_hi && kk >= T;
+            ok = i0 >= 0 && i0 + e < nv && kk >= T;
             key = ((uint64_t)kk << 32) | (uint32_t)(~(uint32_t)(i0 + e));
           } else {
             key = gk[u];
@@ -669,15 +724,23 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
         }
       }
     }
+    __syncthreads();                                   // slist (in keys) is dead from here
   }
-  // ---- the last CTA of this row selects
-  __threadfence();
+  // ---- the last CTA of this row selects (barrier, then one thread fences
+  // and counts: the block's candidate stores are ordered before the count)
   __syncthreads();
-  if (threadIdx.x == 0) is_last = atomicAdd(ctr + 1, 1u) == (uint32_t)(P - 1);
+  __shared__ uint32_t nc_sh;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    is_last = atomicAdd(ctr + 1, 1u) == (uint32_t)(P - 1);
+    if (is_last) {
+      __threadfence();
+      nc_sh = atomicAdd(ctr + 0, 0u);
+    }
+  }
   __syncthreads();
   if (!is_last) return;
-  __threadfence();
-  const uint32_t nc_all = atomicAdd(ctr + 0, 0u);
+  const uint32_t nc_all = nc_sh;
   int32_t *oq = out + (int64_t)q * k;
   if (nc_all <= (uint32_t)kCandCap) {
     const int nc = (int)nc_all;
@@ -692,11 +755,11 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
       for (int u = 0; u < 4; u++) {
         const int i = i0 + u * blockDim.x + threadIdx.x;
         if (i < nc) keys[i] = v[u];
+        if (i < ((nc + 3) & ~3)) sv[i] = (uint32_t)(v[u] >> 32);   // score halves, zero-padded
       }
     }
     __syncthreads();
-    // sv (64 KB) holds the bucket scatter, whist (32 KB) the bucket counters
-    select_bucket(keys, nc, k, oq, reinterpret_cast<uint64_t *>(sv), sh.whist);
+    select_block(keys, sv, nc, k, oq, sel, sh.whist);
   } else {
     // too many ties at T for the buffer: exact selection straight over the row
     __shared__ int nvi;
@@ -739,7 +802,7 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
   S.block = block;
   S.n_max = n_max;
   S.n_items = topk_items(n_max, block, pool != nullptr);
-  const size_t dsm_direct = (size_t)kDirectCap * 8 + (size_t)kMaxK * 4 + 32 * 256 * 4;
+  const size_t dsm_direct = (size_t)kDirectCap * 8 + (size_t)kMaxK * 4 + 32 * 256 * 4 + (size_t)kCandCap * 4;
   const size_t dsm_collect = (size_t)kCandCap * 8 + (size_t)kMaxK * 4 + (size_t)kSuperCap * 4 + 32 * 256 * 4;
   int dev = 0;
   cudaGetDevice(&dev);
