@@ -1,10 +1,10 @@
 // Sparse MQA attention on the 5th-generation tensor cores (csa2_sparse_attn).
 //
-// "There is one KV latent per token and it is shared by all 64 query heads
-// (k = v, 512-wide)"; "Every other layer attends over that window plus 512
-// selected entries"; "RoPE touches 64 of the 512 dims, and is un-rotated on the
-// attention output" ("An infra-oriented diagram of the DeepSeek-V4.1-Flash
-// architecture", reading notes).
+// Each token keeps one 512-wide latent that serves as key and value for all 64
+// query heads; a query attends over its 512 selected entries plus the sliding
+// window; RoPE acts on 64 of the 512 dimensions and is undone on the output
+// (An infra-oriented diagram of the DeepSeek-V4.1-Flash architecture, reading
+// notes).
 //
 // The entry slots of a query (sel_stride selected entries, -1 = empty, then the
 // swa_cnt window entries) are processed in chunks of 128.  Per chunk:

@@ -1,9 +1,10 @@
 // Lightning-indexer scores on the 5th-generation tensor cores (csa2_index_score).
 //
-// "32 FP4 query heads of 128 dims against one shared key per entry, ReLU'd
-// scores summed with per-head weights" and the keys are "128 FP4 values with one
-// E8M0 scale per 32" ("An infra-oriented diagram of the DeepSeek-V4.1-Flash
-// architecture", lightning-indexer note and section "The KV cache").  That is
+// The indexer compares 32 FP4 query heads of width 128 with one key per entry,
+// clamps each head's dot product at zero and sums them with per-head weights;
+// a key is 128 FP4 values with one E8M0 scale per 32 (An infra-oriented diagram
+// of the DeepSeek-V4.1-Flash architecture, lightning-indexer note and section
+// "The KV cache").  That is
 // exactly the MXFP4 block-scaled format the tcgen05 MMA consumes, so
 //     D[entry][head] = sum_c khat[entry][c] * qhat[head][c]
 // is one  M=128 (entries) x N=32 (heads) x K=128  product per 128 entries,

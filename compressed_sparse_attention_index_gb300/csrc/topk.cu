@@ -1,7 +1,8 @@
-// Top-k selection (csa2_topk): "Main sparse selection: 512 entries"
-// (perchy.ai, card "Full. Reindex. Reuse."); the candidate pool of 2,048 blocks
-// of 8 ("a 16,384-entry candidate pool that layer 20 chose by blocks of 8",
-// DeepSeek-V4.1-Flash study, lightning-indexer note).
+// Top-k selection (csa2_topk): the 512 entries each query attends to
+// (perchy.ai/models/deepseek, card "Full. Reindex. Reuse."), and the candidate
+// pool of 2,048 blocks of 8 entries that Reindex layers score (An
+// infra-oriented diagram of the DeepSeek-V4.1-Flash architecture,
+// lightning-indexer note).
 //
 // Every item gets a unique 64-bit key  (order_key(score) << 32) | ~index :
 // larger key = higher score, then lower index.  Selecting the k largest keys

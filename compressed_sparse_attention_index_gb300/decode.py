@@ -5,9 +5,10 @@
 * Reindex layer: Full-layer scores -> csa2_topk in block mode (2,048 blocks of
   8) -> csa2_index_score over the 16,384 pool slots with the Reindex layer's
   own indexer query -> csa2_topk over the pool -> csa2_sparse_attn.
-  ("Reindex layers in the decoder only score a 16,384-entry candidate pool that
-  layer 20 chose by blocks of 8", DeepSeek-V4.1-Flash study, lightning-indexer
-  note; perchy.ai "shared KV -> candidate pool -> top 512 -> attention".)
+  (An infra-oriented diagram of the DeepSeek-V4.1-Flash architecture,
+  lightning-indexer note: decoder Reindex layers score only a 16,384-position
+  pool picked earlier as blocks of 8; perchy.ai/models/deepseek, card "Full.
+  Reindex. Reuse.": the pool feeds the top-512 that attention reads.)
 """
 from __future__ import annotations
 

@@ -112,9 +112,10 @@ const char *csa2_status_string(csa2_status s);
 
 /*
  * csa2_fp4_pack -- cache write: quantise bf16 rows into cache records.
- * (study, reading notes: "In the encoder (m=2) two consecutive tokens are
- * pooled into one entry with a learned softmax gate ... the main cache is stored
- * in FP4 (E2M1, one E4M3 scale per 16 channels)"; section "The KV cache".)
+ * (An infra-oriented diagram of the DeepSeek-V4.1-Flash architecture, reading
+ * notes and section "The KV cache": the encoder pools each pair of tokens into
+ * one entry through a learned softmax gate, and the latent cache holds E2M1
+ * values with an E4M3 scale for every 16 channels.)
  *
  *   kind         CSA2_KV_NVFP4 (src rows of 512), CSA2_IDX_MXFP4 (rows of 128),
  *                CSA2_SWA_MXFP8 (rows of 512).
@@ -134,8 +135,10 @@ csa2_status csa2_fp4_pack(int kind, const void *src, int64_t rows, int m, const 
 
 /*
  * csa2_index_score -- lightning-indexer scores.
- * (study, reading notes: "32 FP4 query heads of 128 dims against one shared key
- * per entry, ReLU'd scores summed with per-head weights"):
+ * (An infra-oriented diagram of the DeepSeek-V4.1-Flash architecture, reading
+ * notes: the indexer compares 32 FP4 query heads of width 128 with the single
+ * key of each entry, clamps each head's dot product at zero and adds them up
+ * with one weight per head):
  *     s_j = sum_{h<32} w_h * max(0, qhat_h . khat_j)
  * with qhat, khat the dequantised FP4 values (E2M1 x E8M0), fp32 accumulation.
  *
@@ -155,8 +158,9 @@ csa2_status csa2_fp4_pack(int kind, const void *src, int64_t rows, int m, const 
  *                       block ids (-1 = none): Reindex mode, scores[q][s] for the
  *                       16,384 pool slots s (entry 8*pool_blocks[q][s/8] + s%8),
  *                       -inf for a slot whose block is -1 or whose entry is not
- *                       visible (study: Reindex layers "only score a 16,384-entry
- *                       candidate pool ... chose by blocks of 8").
+ *                       visible (same page, lightning-indexer note: decoder
+ *                       Reindex layers score only the 16,384 positions of the
+ *                       pool an earlier layer picked as 2,048 blocks of 8).
  *   scores              (device) fp32, row stride score_stride (>= n_max in Full
  *                       mode, >= 16384 in Reindex mode).
  */
@@ -170,9 +174,10 @@ csa2_status csa2_index_score(const void *key_nib, const void *key_scale, int64_t
  * csa2_topk -- top-k selection by (score descending, index ascending): the lower
  * index wins ties; -0.0 equals +0.0.  Output indices ascending, padded with -1
  * when fewer than k items are valid.
- * (perchy.ai: "Main sparse selection: 512 entries"; "Later decoder indexers use
- * at most 16,384 candidate positions"; study: "a 16,384-entry candidate pool
- * that layer 20 chose by blocks of 8".)
+ * (perchy.ai/models/deepseek, card "Full. Reindex. Reuse.": the main selection
+ * keeps 512 entries and later decoder indexers look at no more than 16,384
+ * candidates; An infra-oriented diagram of the DeepSeek-V4.1-Flash architecture,
+ * lightning-indexer note: those candidates are 2,048 blocks of 8 entries.)
  *
  *   scores        (device) fp32 [n_q][score_stride].
  *   n_valid       (device) int32 [n_q]: number of visible entries.
@@ -198,11 +203,13 @@ csa2_status csa2_topk(const float *scores, int64_t score_stride, int n_q, const 
 /*
  * csa2_sparse_attn -- 64-head MQA attention over the selected entries plus the
  * sliding window, k = v.
- * (study, reading notes: "one KV latent per token and it is shared by all 64
- * query heads (k = v, 512-wide)"; "Every other layer attends over that window
- * plus 512 selected entries"; "RoPE touches 64 of the 512 dims, and is
- * un-rotated on the attention output"; helix.ml: SWA "covers the latest 128
- * tokens".)  For each query and head h:
+ * (An infra-oriented diagram of the DeepSeek-V4.1-Flash architecture, reading
+ * notes: each token has one 512-wide latent serving as both key and value for
+ * all 64 query heads; attention covers the selected 512 entries plus the
+ * window; RoPE acts on 64 of the 512 dimensions and is undone on the output.
+ * DeepSeek V4.1 Flash: Why Its Encoder, Engram and KV Cache Matter, section
+ * "CSA2 makes long context cheaper to retain": the window is the last 128
+ * tokens.)  For each query and head h:
  *     l_i = sm_scale * q_h . khat_i  over i in {selected} + {window}
  *     o_h = sum_i softmax(l)_i khat_i
  * then the pairs (rope_off + 2i, rope_off + 2i + 1), i < 32, are rotated by

@@ -6,8 +6,8 @@ the oracle steps in the pages' order:
 
 * Full layer [study, lightning-indexer note]: score every visible entry,
   take the top-512, attend over those entries plus the SWA window.
-* Reindex layer [study: "Reindex layers in the decoder only score a 16,384-entry
-  candidate pool that layer 20 chose by blocks of 8"]: the Full layer's scores
+* Reindex layer [study, lightning-indexer note: decoder Reindex layers score
+  only a 16,384-position pool picked earlier as blocks of 8]: the Full layer's scores
   pick 2,048 blocks of 8; the Reindex layer's own indexer query scores only
   those positions and takes the top-512 among them.
 

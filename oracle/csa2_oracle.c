@@ -289,7 +289,7 @@ void orc_index_score(const uint8_t *keys, int64_t n, const uint8_t *qidx, const 
 /* ---------------------------------------------------------------- top-k */
 /* Top-k by (score descending, index ascending): lower index wins ties.  The
  * selected indices are returned in ascending order and padded with -1.
- * [perchy "Main sparse selection: 512 entries"; study, lightning indexer] */
+ * [perchy: the main selection keeps 512 entries; study, lightning indexer] */
 static const double *g_sort_keys;
 static int cmp_desc_then_idx(const void *a, const void *b) {
     int64_t i = *(const int64_t *)a, j = *(const int64_t *)b;
@@ -316,8 +316,8 @@ int orc_topk(const double *s, int64_t n, int k, int32_t *out) {
     return m;
 }
 
-/* Candidate pool [study: "a 16,384-entry candidate pool that layer 20 chose by
- * blocks of 8"]: block score = max of the Full-layer scores of the block's
+/* Candidate pool [study, lightning-indexer note: 16,384 positions chosen as
+ * 2,048 blocks of 8 by an earlier layer]: block score = max of the Full-layer scores of the block's
  * entries j < n (reading: max), top `nb` blocks by (block score desc, block id
  * asc), returned ascending and padded with -1.  Returns the number selected. */
 int orc_pool_blocks(const double *s, int64_t n, int block, int nb, int32_t *out) {
@@ -336,8 +336,8 @@ int orc_pool_blocks(const double *s, int64_t n, int block, int nb, int32_t *out)
 
 /* ------------------------------------------------------- sparse attention */
 /* One query, all 64 heads [study: k = v, one 512-wide latent shared by all
- * heads; "every other layer attends over that window plus 512 selected
- * entries"; RoPE on 64 of 512 dims, un-rotated on the output]:
+ * heads; attention covers the SWA window and the 512 selected entries; RoPE
+ * on 64 of 512 dims, un-rotated on the output]:
  *   l_i  = sm_scale * q_h . khat_i     over the selected entries and the SWA
  *                                      window (no dedup, no sink)
  *   p    = softmax(l)                  (fp64)
