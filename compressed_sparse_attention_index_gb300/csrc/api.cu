@@ -5,23 +5,9 @@
 #include <string.h>
 
 #include "common.cuh"
+#include "launch.cuh"
 
 namespace csa2 {
-cudaError_t launch_pack(int kind, const void *src, int64_t rows, int m, const float *gate, void *dst,
-                        void *dst_scales, cudaStream_t st);
-cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
-                                  const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
-                                  const int32_t *n_vis, int n_q, const int32_t *pool, float *scores, int64_t stride,
-                                  int *status, cudaStream_t st);
-size_t topk_workspace_bytes(int n_q, int64_t n_items, int k);
-bool topk_items_supported(int64_t n_items, int k);
-cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max, int k,
-                        int block, const int32_t *pool, int32_t *out, void *ws, int *status, cudaStream_t st);
-size_t attn_workspace_bytes(int n_q, int sel_stride);
-cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_seq, const int32_t *sel,
-                           int sel_stride, const void *swa, int swa_cap, const int32_t *q_seq, const int32_t *pos,
-                             const int32_t *swa_first, const int32_t *swa_cnt, int n_q, void *out, int out_dtype,
-                             float sm_scale, double rope_base, void *ws, int *status, cudaStream_t st);
 
 // The sticky status word of each device (a file-scope device variable: the
 // library makes no allocation for it).
@@ -53,6 +39,15 @@ static bool params_ok(const csa2_params *p) {
 }
 
 static csa2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+
+static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+// csa2_decode's workspace: scores [n_q][n_max] fp32, then the top-k scratch,
+// then the attention scratch, each 256-B aligned.
+static size_t decode_workspace_bytes(int n_q, int64_t n_max) {
+  return round256((size_t)n_q * (size_t)n_max * 4) + round256(topk_fused_bytes(n_q, n_max, kTopK)) +
+         round256(attn_workspace_bytes(n_q, kTopK));
+}
 
 }  // namespace csa2
 
@@ -143,6 +138,11 @@ csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t 
     *bytes = topk_workspace_bytes(n_q, n_items, k);
     return CSA2_OK;
   }
+  if (op == CSA2_OP_DECODE) {
+    if (n_items <= 0) return CSA2_ERR_INVALID_ARG;
+    *bytes = decode_workspace_bytes(n_q, n_items);
+    return CSA2_OK;
+  }
   if (op == CSA2_OP_SPARSE_ATTN) {
     const int64_t sel_stride = n_items - kSwa;
     if (sel_stride < 1 || sel_stride > kTopK) return CSA2_ERR_INVALID_ARG;
@@ -200,6 +200,51 @@ csa2_status csa2_sparse_attn(const void *q, const void *kv_cache, int64_t n_max,
   return from_cuda(launch_attn_tc(q, kv_cache, n_max, n_seq, sel, sel_stride, swa_cache, swa_cap, q_seq, pos,
                                     swa_first, swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, workspace, st,
                                     (cudaStream_t)stream));
+}
+
+csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq, const void *q_nib,
+                        const void *q_scale, const float *w, const int32_t *q_seq, const int32_t *n_vis, int n_q,
+                        const void *q, const void *kv_cache, const void *swa_cache, int swa_cap, const int32_t *pos,
+                        const int32_t *swa_first, const int32_t *swa_cnt, int32_t *sel, void *out, int out_dtype,
+                        const csa2_params *params, void *workspace, size_t workspace_bytes, csa2_stream_t stream) {
+  if (!params_ok(params)) return CSA2_ERR_UNSUPPORTED;
+  if (n_q < 0 || n_seq < 1 || n_max <= 0 || n_max % 128 != 0 || n_max > ((int64_t)1 << 31) - 128 || swa_cap < 0)
+    return CSA2_ERR_INVALID_ARG;
+  if (out_dtype != CSA2_OUT_BF16 && out_dtype != CSA2_OUT_F32) return CSA2_ERR_INVALID_ARG;
+  if (n_q > 65535) return CSA2_ERR_UNSUPPORTED;
+  if (n_q == 0) return CSA2_OK;
+  if (!key_nib || !key_scale || !q_nib || !q_scale || !w || !q_seq || !n_vis || !q || !kv_cache || !pos ||
+      !swa_first || !swa_cnt || !sel || !out)
+    return CSA2_ERR_INVALID_ARG;
+  if (swa_cap > 0 && swa_cache == nullptr) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(key_nib, 512) || !aligned(key_scale, 16) || !aligned(q_nib, 512) || !aligned(q_scale, 16) ||
+      !aligned(w, 16) || !aligned(q, 16) || !aligned(kv_cache, 16) || (swa_cache && !aligned(swa_cache, 16)) ||
+      !aligned(out, 16) || !aligned(sel, 4))
+    return CSA2_ERR_INVALID_ARG;
+  if (!topk_items_supported(n_max, kTopK)) return CSA2_ERR_UNSUPPORTED;
+  if (workspace_bytes < decode_workspace_bytes(n_q, n_max) || workspace == nullptr || !aligned(workspace, 256))
+    return CSA2_ERR_WORKSPACE;
+  int *st = status_ptr();
+  if (st == nullptr) return CSA2_ERR_CUDA;
+  const cudaStream_t s = (cudaStream_t)stream;
+  unsigned char *base = static_cast<unsigned char *>(workspace);
+  float *scores = reinterpret_cast<float *>(base);
+  void *ws_topk = base + round256((size_t)n_q * (size_t)n_max * 4);
+  void *ws_attn = static_cast<unsigned char *>(ws_topk) + round256(topk_fused_bytes(n_q, n_max, kTopK));
+  const FusedTopk F = topk_fused_plan(ws_topk, n_q, n_max, kTopK);
+  const bool fused = F.mode > 0;
+  cudaError_t e = launch_index_score_tc(
+      static_cast<const uint8_t *>(key_nib), static_cast<const uint8_t *>(key_scale), n_max, n_seq,
+      static_cast<const uint8_t *>(q_nib), static_cast<const uint8_t *>(q_scale), w, q_seq, n_vis, n_q, nullptr, scores,
+      n_max, st, s, fused ? F.W.smax : nullptr, fused ? F.W.sstride : 0, fused ? F.mode : 0,
+      fused ? F.W.ctr : nullptr, fused ? n_q * 4 : 0);
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  e = launch_topk_fused(scores, n_max, n_q, n_vis, n_max, kTopK, F, sel, ws_topk, st, s);
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  const float sm_scale = params ? params->sm_scale : 1.0f / sqrtf((float)kDim);
+  const double rope_base = params ? params->rope_base : 10000.0;
+  return from_cuda(launch_attn_tc(q, kv_cache, n_max, n_seq, sel, kTopK, swa_cache, swa_cap, q_seq, pos, swa_first,
+                                  swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, ws_attn, st, s));
 }
 
 csa2_status csa2_get_device_status(csa2_stream_t stream, csa2_status *out) {

@@ -32,6 +32,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "launch.cuh"
 #include "tc_ptx.cuh"
 
 namespace csa2 {

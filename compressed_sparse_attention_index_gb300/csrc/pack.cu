@@ -17,6 +17,7 @@
 // All three kernels are HBM-bound streams: one warp per row (KV, SWA) or eight
 // lanes per row (IDX), 16-B vector loads of the bf16 row, 8- or 16-B stores.
 #include "common.cuh"
+#include "launch.cuh"
 
 namespace csa2 {
 

@@ -40,6 +40,7 @@
 // bounded (CSA2_ERR_TIMEOUT instead of a hang).
 #include "common.cuh"
 #include "tc_ptx.cuh"
+#include "launch.cuh"
 
 namespace csa2 {
 
@@ -91,6 +92,16 @@ struct ScoreTcArgs {
   int n_q;
   int units_per_q;
   int *status;
+  // optional, Full mode only: maxima of the order keys of the scores, for the
+  // top-k that follows.  smax_mode 1: per work unit, four partial maxima (one
+  // per TMEM lane quarter, over its rows of the four sub-tiles) at
+  // smax[q * sstride + 4u + quarter]; smax_mode 2: per 32 consecutive entries
+  // at smax[q * sstride + entry / 32].  Invalid entries count as key 0.
+  uint32_t *smax;
+  int64_t sstride;
+  int smax_mode;
+  uint32_t *clear;         // n_clear words zeroed by block 0 before anything else
+  int n_clear;
 };
 
 // Work schedule shared by every role: unit index T = blockIdx.x + k * gridDim.x
@@ -172,6 +183,8 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < P.n_clear; i += blockDim.x) P.clear[i] = 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kScStages; s++) {
       ptx::mbar_init(&full_bar[s], 1);
@@ -380,6 +393,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         }
       };
       const int64_t i0 = (int64_t)sc.u * kUnit + row;
+      uint32_t umax = 0u;                             // smax_mode 1: this lane's maximum key
 #pragma unroll 1
       for (int h2 = 0; h2 < kSub / 2; h2++) {         // two sub-tiles (64 columns) at a time
         uint32_t d0[32], d1[32];
@@ -399,6 +413,27 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         }
         store(i0 + h2 * 256, s0);
         store(i0 + h2 * 256 + 128, s1);
+        if (P.smax_mode != 0) {
+          // order keys of this lane's two entries (0 if not visible)
+          const uint32_t k0 = i0 + h2 * 256 < sc.nv ? order_key(s0) : 0u;
+          const uint32_t k1 = i0 + h2 * 256 + 128 < sc.nv ? order_key(s1) : 0u;
+          uint32_t *sm = P.smax + (int64_t)sc.q * P.sstride;
+          if (P.smax_mode == 2) {
+            // 32 consecutive entries per warp and sub-tile
+            const uint32_t g0 = __reduce_max_sync(0xFFFFFFFFu, k0), g1 = __reduce_max_sync(0xFFFFFFFFu, k1);
+            if (lane == 0) {
+              const int64_t e0 = (int64_t)sc.u * kUnit + h2 * 256 + quarter * 32;
+              sm[e0 >> 5] = g0;
+              sm[(e0 + 128) >> 5] = g1;
+            }
+          } else {
+            umax = max(umax, max(k0, k1));
+          }
+        }
+      }
+      if (P.smax_mode == 1) {
+        umax = __reduce_max_sync(0xFFFFFFFFu, umax);
+        if (lane == 0) P.smax[(int64_t)sc.q * P.sstride + (int64_t)sc.u * 4 + quarter] = umax;
       }
     }
   }
@@ -423,8 +458,14 @@ static int sm_count() {
 cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
                                   const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
                                   const int32_t *n_vis, int n_q, const int32_t *pool, float *scores, int64_t stride,
-                                  int *status, cudaStream_t st) {
+                                  int *status, cudaStream_t st, uint32_t *smax, int64_t sstride, int smax_mode,
+                                  uint32_t *clear, int n_clear) {
   ScoreTcArgs P;
+  P.smax = smax;
+  P.sstride = sstride;
+  P.smax_mode = pool == nullptr ? smax_mode : 0;
+  P.clear = clear;
+  P.n_clear = clear != nullptr ? n_clear : 0;
   P.key_nib = key_nib;
   P.q_nib = q_nib;
   P.key_scale = key_scale;

@@ -20,6 +20,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "launch.cuh"
 
 namespace csa2 {
 
@@ -494,11 +495,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
 constexpr int kCollectThreads = 1024;
 constexpr int kSuperCap = 16384;    // supergroups per row (held in shared memory by pass 2)
 
-struct LongRowWs {
-  uint32_t *smax, *ctr;
-  uint64_t *cand;
-  int64_t sstride;
-};
 
 // Items per supergroup: the largest power of two in [8, 512] that leaves at
 // least 4k supergroups, doubled further while a row has more than kSuperCap.
@@ -599,8 +595,9 @@ __global__ void __launch_bounds__(256) topk_smax_kernel(TopkSrc S, int64_t sgi, 
 }
 
 // Pass 2: grid (P, n_q).
-__global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S, int64_t sgi, int k, LongRowWs W,
-                                                                       int32_t *__restrict__ out, int *status) {
+__global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S, int64_t sgi, int parts, int k,
+                                                                       LongRowWs W, int32_t *__restrict__ out,
+                                                                       int *status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint64_t *keys = reinterpret_cast<uint64_t *>(smem_raw);               // [kCandCap] (last CTA)
   int32_t *sel = reinterpret_cast<int32_t *>(keys + kCandCap);           // [kMaxK]
@@ -619,18 +616,28 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
   const int ns = (int)((valid_items + sgi - 1) / sgi);                   // supergroups that may hold a valid item
   if (threadIdx.x == 0) { n_vs = 0; T_sh = 1u; }                         // T = 1: every valid item
   __syncthreads();
-  // ---- the supergroup maxima (16-B loads; slots past ns are never used)
+  // ---- the supergroup maxima (16-B loads; slots past ns are never used).
+  // parts == 4: each supergroup's maximum is stored as four partial maxima.
   {
     const uint4 *src = reinterpret_cast<const uint4 *>(W.smax + (int64_t)q * W.sstride);
     int vs = 0;
-    for (int i = threadIdx.x; 4 * i < ns; i += blockDim.x) {
-      const uint4 v = __ldcg(src + i);
-      const uint32_t e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; j++) {
-        const uint32_t x = 4 * i + j < ns ? e[j] : 0u;
-        sv[4 * i + j] = x;
+    if (parts == 4) {
+      for (int i = threadIdx.x; i < ns; i += blockDim.x) {
+        const uint4 v = __ldcg(src + i);
+        const uint32_t x = max(max(v.x, v.y), max(v.z, v.w));
+        sv[i] = x;
         vs += x != 0u;
+      }
+    } else {
+      for (int i = threadIdx.x; 4 * i < ns; i += blockDim.x) {
+        const uint4 v = __ldcg(src + i);
+        const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+          const uint32_t x = 4 * i + j < ns ? e[j] : 0u;
+          sv[4 * i + j] = x;
+          vs += x != 0u;
+        }
       }
     }
     vs = __reduce_add_sync(0xFFFFFFFFu, vs);
@@ -831,7 +838,67 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   // one CTA per SM (shared memory): a single wave over all rows
   const int64_t P = std::max<int64_t>(1, std::min<int64_t>(sms / n_q, S.n_items / 4096));
-  topk_collect_kernel<<<dim3((unsigned)P, n_q), kCollectThreads, dsm_collect, st>>>(S, sgi, k, W, out, status);
+  topk_collect_kernel<<<dim3((unsigned)P, n_q), kCollectThreads, dsm_collect, st>>>(S, sgi, 1, k, W, out, status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- fused decode
+// When the indexer's epilogue writes the supergroup maxima (csa2_decode), the
+// selection runs only the collection pass.  mode 1: supergroups are the
+// indexer's 512-entry work units, each stored as four partial maxima; mode 2:
+// supergroups of 32 entries; 0: the maxima pass runs (other supergroup sizes);
+// -1: rows short enough for one CTA (no scratch).
+FusedTopk topk_fused_plan(void *ws, int n_q, int64_t n_max, int k) {
+  FusedTopk F;
+  F.mode = 0;
+  F.sgi = 0;
+  F.parts = 1;
+  F.W = LongRowWs{};
+  if (n_max <= kDirectCap) { F.mode = -1; return F; }
+  const int64_t sgi = long_row_sgi(n_max, k);
+  if (sgi != 512 && sgi != 32) return F;
+  F.mode = sgi == 512 ? 1 : 2;
+  F.sgi = sgi;
+  F.parts = sgi == 512 ? 4 : 1;
+  LongRowWs &W = F.W;
+  W.sstride = sgi == 512 ? (n_max + 511) / 512 * 4 : ((n_max + 31) / 32 + 3) / 4 * 4;
+  W.smax = static_cast<uint32_t *>(ws);
+  W.ctr = W.smax + (int64_t)n_q * W.sstride;
+  W.cand = reinterpret_cast<uint64_t *>(W.ctr + (int64_t)n_q * 4);
+  return F;
+}
+
+size_t topk_fused_bytes(int n_q, int64_t n_max, int k) {
+  const FusedTopk F = topk_fused_plan(nullptr, n_q, n_max, k);
+  if (F.mode == -1) return 0;
+  if (F.mode == 0) return topk_workspace_bytes(n_q, n_max, k);
+  return (size_t)n_q * ((size_t)(F.W.sstride + 4) * 4 + (size_t)kCandCap * 8);
+}
+
+cudaError_t launch_topk_fused(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max,
+                              int k, const FusedTopk &F, int32_t *out, void *ws, int *status, cudaStream_t st) {
+  if (F.mode <= 0) return launch_topk(scores, stride, n_q, n_valid, n_max, k, 1, nullptr, out, ws, status, st);
+  TopkSrc S;
+  S.scores = scores;
+  S.stride = stride;
+  S.n_valid = n_valid;
+  S.pool = nullptr;
+  S.block = 1;
+  S.n_max = n_max;
+  S.n_items = n_max;
+  const size_t dsm_collect = (size_t)kCandCap * 8 + (size_t)kMaxK * 4 + (size_t)kSuperCap * 4 + 32 * 256 * 4;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_done[64] = {};
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    cudaFuncSetAttribute(topk_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm_collect);
+    attr_done[dev] = true;
+  }
+  int sms = 148;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t P = std::max<int64_t>(1, std::min<int64_t>(sms / n_q, n_max / 4096));
+  topk_collect_kernel<<<dim3((unsigned)P, n_q), kCollectThreads, dsm_collect, st>>>(S, F.sgi, F.parts, k, F.W, out,
+                                                                                    status);
   return cudaGetLastError();
 }
 

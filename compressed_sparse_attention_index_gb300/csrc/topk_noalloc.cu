@@ -5,13 +5,9 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "launch.cuh"
 
 namespace csa2 {
-size_t topk_workspace_bytes(int n_q, int64_t n_items, int k);
-bool topk_items_supported(int64_t n_items, int k);
-cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max, int k,
-                        int block, const int32_t *pool, int32_t *out, void *ws, int *status, cudaStream_t st);
-int *status_word_ptr();
 
 // Fixed scratch of CSA2_TOPK_NOALLOC_SCRATCH_BYTES (1 MiB) on every device that
 // loads the library, held until the process exits.

@@ -36,7 +36,9 @@ class DecodeBuffers:
                        L.csa2_workspace_size(L.CSA2_OP_TOPK, n_q, POOL_SLOTS, TOPK))
         self.ws_topk_bytes = ws_t
         self.ws_attn_bytes = L.csa2_workspace_size(L.CSA2_OP_SPARSE_ATTN, n_q, TOPK + SWA)
-        self.ws = torch.empty(max(1, max(ws_t, self.ws_attn_bytes)), dtype=torch.uint8, device=device)
+        self.ws_decode_bytes = 0 if pool else L.csa2_workspace_size(L.CSA2_OP_DECODE, n_q, n_max, TOPK)
+        self.ws = torch.empty(max(1, ws_t, self.ws_attn_bytes, self.ws_decode_bytes), dtype=torch.uint8,
+                              device=device)
 
 
 def full_decode(dw, buf: DecodeBuffers, params=None, stream=None):
@@ -47,6 +49,15 @@ def full_decode(dw, buf: DecodeBuffers, params=None, stream=None):
     L.csa2_topk(buf.scores, buf.n_max, n_q, dw.n_vis, dw.n_max, TOPK, 1, None, buf.sel, buf.ws, buf.ws_topk_bytes,
                 stream)
     attend(dw, buf, params, stream)
+    return buf.out
+
+
+def fused_decode(dw, buf: DecodeBuffers, params=None, stream=None):
+    """The same Full-layer step as full_decode, as the single call csa2_decode
+    (scores stay in the workspace; buf.sel and buf.out are written)."""
+    L.csa2_decode(dw.key_nib, dw.key_scale, dw.n_max, dw.kv.shape[0], dw.q_nib, dw.q_scale, dw.w, dw.q_seq,
+                  dw.n_vis, buf.n_q, dw.q, dw.kv, dw.swa, dw.swa.shape[1], dw.pos, dw.swa_first, dw.swa_cnt,
+                  buf.sel, buf.out, buf.out_dtype, params, buf.ws, buf.ws_decode_bytes, stream)
     return buf.out
 
 

@@ -80,7 +80,7 @@ enum { CSA2_KV_NVFP4 = 0, CSA2_IDX_MXFP4 = 1, CSA2_SWA_MXFP8 = 2 };
 /* Output dtypes for csa2_sparse_attn. */
 enum { CSA2_OUT_BF16 = 0, CSA2_OUT_F32 = 1 };
 /* Operations for csa2_workspace_size. */
-enum { CSA2_OP_TOPK = 0, CSA2_OP_SPARSE_ATTN = 1 };
+enum { CSA2_OP_TOPK = 0, CSA2_OP_SPARSE_ATTN = 1, CSA2_OP_DECODE = 2 };
 
 /* Model constants.  The kernels are built for the pages' values only
  * (study, reading notes: 64 heads, 512-wide latent, RoPE on 64 of the 512
@@ -236,10 +236,35 @@ csa2_status csa2_sparse_attn(const void *q, const void *kv_cache, int64_t n_max,
                              csa2_stream_t stream);
 
 /*
+ * csa2_decode -- one Full-layer decode step: csa2_index_score over every
+ * visible entry, top-512 selection, csa2_sparse_attn over the selection and
+ * the window, issued as one call.  The pages give no such call; it composes
+ * the three steps above (same arguments, same meaning, same results as the
+ * chain csa2_index_score -> csa2_topk(k = 512, block = 1) ->
+ * csa2_sparse_attn(sel_stride = 512)), and lets the indexer's epilogue also
+ * write the maxima the selection starts from, which saves the selection's
+ * first pass over the scores.
+ *
+ *   key_nib .. n_q      as csa2_index_score (Full mode; scores are kept in the
+ *                       workspace).
+ *   q .. swa_cnt, out, out_dtype, params   as csa2_sparse_attn.
+ *   sel                 (device) int32 [n_q][512]: the selected entries
+ *                       (ascending, -1 padding), as csa2_topk writes them.
+ *   workspace           (device) >= csa2_workspace_size(CSA2_OP_DECODE, n_q,
+ *                       n_max, 512) bytes, 256-B aligned; no initialisation.
+ */
+csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq, const void *q_nib,
+                        const void *q_scale, const float *w, const int32_t *q_seq, const int32_t *n_vis, int n_q,
+                        const void *q, const void *kv_cache, const void *swa_cache, int swa_cap, const int32_t *pos,
+                        const int32_t *swa_first, const int32_t *swa_cnt, int32_t *sel, void *out, int out_dtype,
+                        const csa2_params *params, void *workspace, size_t workspace_bytes, csa2_stream_t stream);
+
+/*
  * csa2_workspace_size -- scratch bytes needed by an operation.
  *   op = CSA2_OP_TOPK:        n_q queries, n_items = items per row (entries,
  *                             blocks, or 16384 pool slots), k.
  *   op = CSA2_OP_SPARSE_ATTN: n_q queries, n_items = sel_stride + 128, k unused.
+ *   op = CSA2_OP_DECODE:      n_q queries, n_items = n_max, k unused (512).
  */
 csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t *bytes);
 

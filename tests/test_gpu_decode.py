@@ -184,3 +184,26 @@ def test_empty_query_gives_zeros(lib):
     decode.attend(dw, buf)
     assert lib.csa2_get_device_status() == 0
     assert torch.count_nonzero(buf.out).item() == 0
+
+
+@pytest.mark.parametrize("case", ["small_direct", "ragged_standalone", "config1_groups", "config4_units"])
+def test_fused_decode_equals_call_chain(lib, case):
+    """csa2_decode (score epilogue feeds the selection) gives exactly the
+    results of csa2_index_score -> csa2_topk -> csa2_sparse_attn, for each of
+    its selection plans: one CTA per row, the standalone passes, 32-entry
+    groups and 512-entry units."""
+    from compressed_sparse_attention_index_gb300 import decode
+    wl = {"small_direct": small(n_seq=2, n_entries=1000, seed=250),
+          "ragged_standalone": small(n_seq=3, n_entries=20_000, seed=251),
+          "config1_groups": CONFIGS[1], "config4_units": CONFIGS[4]}[case]
+    dw = _dw(wl)
+    chain, fused = _bufs(dw), _bufs(dw)
+    decode.full_decode(dw, chain)
+    fused.sel.fill_(-7)
+    fused.out.fill_(7)
+    decode.fused_decode(dw, fused)
+    assert lib.csa2_get_device_status() == 0
+    assert torch.equal(chain.sel, fused.sel)
+    assert torch.equal(chain.out.view(torch.int32), fused.out.view(torch.int32))
+    decode.fused_decode(dw, fused)                       # second call: nothing left over from the first
+    assert torch.equal(chain.sel, fused.sel)
