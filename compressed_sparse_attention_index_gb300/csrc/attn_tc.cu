@@ -29,6 +29,7 @@
 // TMEM lane quarter w%4, heads 32*(w/4) ..); thread 0 issues the MMAs; all 8
 // warps share the final read-out of the 5 x 64 accumulator columns.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -52,8 +53,9 @@ constexpr int kSmBars = kSmValid + 128;         // 2 mbarriers, tmem base, flags
 constexpr int kSmTotal = kSmBars + 32;
 constexpr int kSmAlloc = kSmTotal + 1024;       // + alignment slack (<= 227 KB)
 constexpr uint32_t kAttTmemCols = 512;
-constexpr uint32_t kColS = 0;                   // S^T: 64 columns
+constexpr uint32_t kColS = 0;                   // S^T, dims 0..255 of the dot products: 64 columns
 constexpr uint32_t kColO = 64;                  // O^T: 5 blocks x 64 columns (block 4 = denominators)
+constexpr uint32_t kColS2 = 384;                // S^T, dims 256..511: 64 columns (a second issuer)
 constexpr float kRescaleLog2 = 8.0f;
 
 // Eight E2M1 codes (one per nibble of w, channel i in nibble i) -> eight bf16
@@ -73,6 +75,14 @@ __device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t (&out)[4]) {
     out[2 * hw] = a;
     out[2 * hw + 1] = b;
   }
+}
+
+// Two E4M3 codes (low byte first) -> their values as f16x2 (exact: E4M3 is a
+// subset of f16), by the hardware converter.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)two));
+  return __half22float2(*reinterpret_cast<__half2 *>(&h));
 }
 
 // byte offset of 16-B chunk `ch` (0..7) in row r of a 128B-swizzled 1024-B atom
@@ -145,13 +155,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   const int c1 = bad ? c0 : min((n_slots + kTcChunk - 1) / kTcChunk, c0 + A.chunks_per_split);
 
   if (t == 0) {
-    ptx::mbar_init(&bar_s, 1);
-    ptx::mbar_init(&bar_o, 1);
+    ptx::mbar_init(&bar_s, 2);                       // two S issuers
+    ptx::mbar_init(&bar_o, 5);                       // five O issuers
     bad_sh = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0) ptx::tmem_alloc(&tmem_sh, kAttTmemCols);
   if (t < kHeads) m_ref[t] = -INFINITY;
+  // start the first chunk's record reads (L2 prefetch) while Q is staged
+  if (c0 < c1) {
+    const int e = t >> 1, half = t & 1, slot = c0 * kTcChunk + e;
+    const uint8_t *rec = nullptr;
+    int bytes = 0;
+    if (slot < A.sel_stride) {
+      const int j = __ldg(A.sel + (int64_t)qi * A.sel_stride + slot);
+      if (j >= 0 && (int64_t)j < A.n_max) { rec = A.kv + ((int64_t)seq * A.n_max + j) * kKvBytes; bytes = kKvBytes; }
+    } else if (slot < n_slots) {
+      const int ring = (swa_first + (slot - A.sel_stride)) % A.swa_cap;
+      rec = A.swa + ((int64_t)seq * A.swa_cap + ring) * kSwaBytes;
+      bytes = kSwaBytes;
+    }
+    for (int o = half * 128; rec != nullptr && o < bytes; o += 256)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + o));
+  }
   // stage Q (K-major, 128B swizzle: [head/8][dim/64][head%8][128 B])
   {
     const uint4 *src = reinterpret_cast<const uint4 *>(A.q + (int64_t)qi * kHeads * kDim);
@@ -246,10 +272,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
 #pragma unroll
             for (int u = 0; u < 4; u++) {
               const uint32_t word = bw[hf * 2 + (u >> 1)];
-              const uint32_t sh = 16 * (u & 1);
-              const float lo = e4m3_to_float((word >> sh) & 0xFFu) * s;
-              const float hi = e4m3_to_float((word >> (sh + 8)) & 0xFFu) * s;
-              pk[u] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+              const float2 f = e4m3x2_to_float2(word >> (16 * (u & 1)));   // exact; x the power-of-two scale: exact
+              const __nv_bfloat162 bb = __floats2bfloat162_rn(f.x * s, f.y * s);
+              pk[u] = *reinterpret_cast<const uint32_t *>(&bb);
             }
             const int d0 = half * 256 + v * 16 + hf * 8;
             const uint32_t off = rowbase + (d0 >> 6) * 1024 + sw128(e & 7, (d0 >> 3) & 7);
@@ -270,14 +295,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     ptx::fence_proxy_async_smem();
     __syncthreads();
     // ---------------------------------------------------------- S^T = Khat Q^T
-    if (t == 0) {
+    // two issuers (lane 0 of warps 0 and 1), dims 0..255 and 256..511 into two
+    // tiles that the softmax adds: tcgen05 issue cost is per thread
+    if (lane == 0 && warp < 2) {
       ptx::tc_fence_after();
+      const uint32_t col = warp == 0 ? kColS : kColS2;
 #pragma unroll 1
-      for (int kk = 0; kk < kDim / 16; kk++) {
+      for (int k2 = 0; k2 < kDim / 32; k2++) {
+        const int kk = warp * (kDim / 32) + k2;
         const uint32_t koff = (kk >> 2) * 1024 + (kk & 3) * 32;
         const uint64_t ad = ptx::smem_desc(sK + koff, 16, 8192, 2);
         const uint64_t bd = ptx::smem_desc(sQ + koff, 16, 8192, 2);
-        ptx::tc_mma_bf16(tmem + kColS, ad, bd, id_qk, kk > 0 ? 1u : 0u);
+        ptx::tc_mma_bf16(tmem + col, ad, bd, id_qk, k2 > 0 ? 1u : 0u);
       }
       ptx::tc_commit(&bar_s);
     }
@@ -294,11 +323,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       // shuffles; afterwards lane L holds the max of head hb + L
       float v[32];
       {
-        uint32_t r[32];
+        uint32_t r[32], r2[32];
         ptx::tmem_ld_32x32b_x32(s_addr, r);
+        ptx::tmem_ld_32x32b_x32(s_addr + (kColS2 - kColS), r2);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; h++) v[h] = ev ? __uint_as_float(r[h]) * A.scale_log2 : -INFINITY;
+        for (int h = 0; h < 32; h++)
+          v[h] = ev ? (__uint_as_float(r[h]) + __uint_as_float(r2[h])) * A.scale_log2 : -INFINITY;
       }
 #pragma unroll
       for (int w = 16; w >= 1; w >>= 1) {              // w = values kept, partner distance w
@@ -334,13 +365,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       // S is read from TMEM again rather than kept live through the reduction
       const uint32_t pe = (e >> 6) * 1024;             // entry atom
       const uint32_t pcol = (uint32_t)(e & 63) * 2;    // byte within the 128-B row
-      uint32_t r[32];
+      uint32_t r[32], r2[32];
       ptx::tmem_ld_32x32b_x32(s_addr, r);
+      ptx::tmem_ld_32x32b_x32(s_addr + (kColS2 - kColS), r2);
       ptx::tmem_wait_ld();
 #pragma unroll
       for (int i = 0; i < 32; i++) {
         const int h = hb + i;
-        const float l2 = __uint_as_float(r[i]) * A.scale_log2;
+        const float l2 = (__uint_as_float(r[i]) + __uint_as_float(r2[i])) * A.scale_log2;
         const float p = ev ? exp2f(l2 - m_ref[h]) : 0.f;
         const __nv_bfloat16 ph = __float2bfloat16_rn(p);
         const __nv_bfloat16 pl = __float2bfloat16_rn(p - __bfloat162float(ph));
@@ -374,24 +406,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       __syncthreads();
     }
     // ---------------------------------------------------------- O^T += Vhat^T P^T
-    if (t == 0) {
+    // five issuers (lane 0 of warps 0..4): dim blocks 0..3, then the
+    // denominators (ones x P^T)
+    if (lane == 0 && warp < 5) {
       ptx::tc_fence_after();
+      const int mb = warp;
 #pragma unroll 1
       for (int ks = 0; ks < kTcChunk / 16; ks++) {
         const uint32_t poff = (ks >> 2) * 1024 + (ks & 3) * 32;
         const uint64_t bhi = ptx::smem_desc(sPhi + poff, 16, 2048, 2);
         const uint64_t blo = ptx::smem_desc(sPlo + poff, 16, 2048, 2);
         const uint32_t acc0 = (any_chunk || ks > 0) ? 1u : 0u;
-#pragma unroll 1
-        for (int mb = 0; mb < 4; mb++) {
+        if (mb < 4) {
           // Vhat^T block: dims [128 mb, 128 mb + 128), entries [16 ks, 16 ks + 16), MN-major
           const uint64_t ad = ptx::smem_desc(sK + (2 * ks) * 8192 + (2 * mb) * 1024, 1024, 8192, 2);
           ptx::tc_mma_bf16(tmem + kColO + mb * 64, ad, bhi, id_pv, acc0);
           ptx::tc_mma_bf16(tmem + kColO + mb * 64, ad, blo, id_pv, 1u);
+        } else {
+          const uint64_t ones = ptx::smem_desc(sOnes, 0, 0, 0);
+          ptx::tc_mma_bf16(tmem + kColO + 4 * 64, ones, bhi, id_qk, acc0);
+          ptx::tc_mma_bf16(tmem + kColO + 4 * 64, ones, blo, id_qk, 1u);
         }
-        const uint64_t ones = ptx::smem_desc(sOnes, 0, 0, 0);
-        ptx::tc_mma_bf16(tmem + kColO + 4 * 64, ones, bhi, id_qk, acc0);
-        ptx::tc_mma_bf16(tmem + kColO + 4 * 64, ones, blo, id_qk, 1u);
       }
       ptx::tc_commit(&bar_o);
     }
