@@ -38,6 +38,12 @@ FIXED_BYTES_PER_QUERY = 348_416      # 512x288 + 128x528 + q 64 KiB + out 64 KiB
 IDX_BYTES = 68
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum of one index_score_tc_kernel launch, from an ncu
+# capture of this kernel version on the named workload (profiles/index_score_tc_32x64K.md gives
+# the command); workloads without a capture report null.
+INDEX_SCORE_TRAFFIC = {"long_full_decode_N1M_B8_zipf": 570552064 + 3530496}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -286,7 +292,8 @@ def run_ours(args, rank, world, local_rank):
         "path_hbm_gbs": step_bytes / (ms / args.steps / 1e3) / 1e9,
         "path_frac_of_measured_peak": step_bytes / (ms / args.steps / 1e3) / 1e9 / peak,
         "roofline": {"kernel": "index_score", "bound": "hbm", "achieved": achieved, "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": INDEX_SCORE_TRAFFIC.get(wl.name),
                      "algorithmic_bytes_per_launch": score_bytes, "avg_launch_ms": score_ms,
                      "measured_in": "K steps of the three-call chain after the timed region, same kernel"},
         "clocks": clk,
