@@ -246,27 +246,29 @@ __device__ __forceinline__ int warp_sum(int v) {
 // bit `low` (a multiple of 8); the result has its bits below `low` cleared, so
 // at least rem selected values reach it.  Each step: a 256-bin histogram of
 // the next digit (shared-memory atomics), then warp 0 locates the digit by a
-// suffix scan over the bins.  hist: 256 counters of shared memory.
+// suffix scan over the bins while the other threads clear the next step's
+// histogram (two alternate): two barriers per step.  hist: 512 counters.
 template <class Sel>
 __device__ uint32_t block_kth256(const uint32_t *v, int n, int rem, int low, Sel sel, uint32_t *hist) {
   __shared__ uint32_t prefix_sh, pmask_sh;
   __shared__ int rem_sh;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) { prefix_sh = 0u; pmask_sh = 0u; rem_sh = rem; }
-  for (int shift = 24; shift >= low; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
-    __syncthreads();
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
+  __syncthreads();
+  for (int shift = 24, buf = 0; shift >= low; shift -= 8, buf ^= 1) {
+    uint32_t *h = hist + buf * 256;
     const uint32_t prefix = prefix_sh, pmask = pmask_sh;
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
       const uint32_t x = v[i];
-      if ((x & pmask) == prefix && sel(i)) atomicAdd(&hist[(x >> shift) & 255u], 1u);
+      if ((x & pmask) == prefix && sel(i)) atomicAdd(&h[(x >> shift) & 255u], 1u);
     }
     __syncthreads();
     if (threadIdx.x < 32) {
       // lane l owns digits 8l .. 8l+7; suffix sums over the lanes above
       uint32_t c[8], part = 0u;
 #pragma unroll
-      for (int j = 0; j < 8; j++) { c[j] = hist[8 * lane + j]; part += c[j]; }
+      for (int j = 0; j < 8; j++) { c[j] = h[8 * lane + j]; part += c[j]; }
       uint32_t incl = part;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -287,6 +289,8 @@ __device__ uint32_t block_kth256(const uint32_t *v, int n, int rem, int low, Sel
           above += c[j];
         }
       }
+    } else {
+      for (int i = threadIdx.x - 32; i < 256; i += blockDim.x - 32) hist[(buf ^ 1) * 256 + i] = 0u;
     }
     __syncthreads();
   }
@@ -660,8 +664,9 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
     const bool row16 = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
     // list them (order irrelevant)
     int32_t *slist = reinterpret_cast<int32_t *>(keys);     // keys is used by the last CTA only after this
-    __shared__ int n_sl;
-    if (threadIdx.x == 0) n_sl = 0;
+    __shared__ int n_sl, n_lc;
+    __shared__ uint32_t g_base;
+    if (threadIdx.x == 0) { n_sl = 0; n_lc = 0; }
     __syncthreads();
     for (int b0 = s_lo; b0 < s_hi; b0 += blockDim.x) {
       const int i = b0 + threadIdx.x;
@@ -676,7 +681,11 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
     __syncthreads();
     const int nsl = n_sl;
     const int64_t total = (int64_t)nsl * sgi;                 // items of the listed supergroups
-    constexpr int kU = 4;
+    // candidates gather in shared memory (sv is free now), then go out with
+    // one global reservation per CTA
+    uint64_t *lc = reinterpret_cast<uint64_t *>(sv);
+    constexpr int kLocalCap = kSuperCap / 2;
+    constexpr int kU = 6;
     const int64_t step = plain ? 4 : 1;
     const int lsg = __ffsll(sgi) - 1;
     for (int64_t b0 = 0; b0 < total; b0 += kU * step * blockDim.x) {
@@ -725,14 +734,20 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
           }
           if (!__any_sync(0xFFFFFFFFu, ok)) continue;   // most rounds have no candidate
           const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
-          uint32_t base = 0;
-          if (lane == 0) base = atomicAdd(ctr + 0, (uint32_t)__popc(bal));
+          int base = 0;
+          if (lane == 0) base = atomicAdd(&n_lc, __popc(bal));
           base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(bal & ((1u << lane) - 1u));
-          if (ok && base < (uint32_t)kCandCap) cq[base] = key;
+          if (ok && base < kLocalCap) lc[base] = key;
         }
       }
     }
     __syncthreads();                                   // slist (in keys) is dead from here
+    const int nl = n_lc;
+    if (threadIdx.x == 0 && nl > 0)                    // more than kLocalCap: force the overflow path
+      g_base = atomicAdd(ctr + 0, nl <= kLocalCap ? (uint32_t)nl : (uint32_t)kCandCap + 1u);
+    __syncthreads();
+    for (int i = threadIdx.x; i < min(nl, kLocalCap); i += blockDim.x)
+      if (g_base + (uint32_t)i < (uint32_t)kCandCap) cq[g_base + i] = lc[i];
   }
   // ---- the last CTA of this row selects (barrier, then one thread fences
   // and counts: the block's candidate stores are ordered before the count)
