@@ -231,20 +231,24 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
   float *scores = reinterpret_cast<float *>(base);
   void *ws_topk = base + round256((size_t)n_q * (size_t)n_max * 4);
   void *ws_attn = static_cast<unsigned char *>(ws_topk) + round256(topk_fused_bytes(n_q, n_max, kTopK));
-  const FusedTopk F = topk_fused_plan(ws_topk, n_q, n_max, kTopK);
+  FusedTopk F = topk_fused_plan(ws_topk, n_q, n_max, kTopK);
+  F.kv = static_cast<const uint8_t *>(kv_cache);
+  F.q_seq = q_seq;
+  F.n_seq = n_seq;
   const bool fused = F.mode > 0;
   cudaError_t e = launch_index_score_tc(
       static_cast<const uint8_t *>(key_nib), static_cast<const uint8_t *>(key_scale), n_max, n_seq,
       static_cast<const uint8_t *>(q_nib), static_cast<const uint8_t *>(q_scale), w, q_seq, n_vis, n_q, nullptr, scores,
-      n_max, st, s, fused ? F.W.smax : nullptr, fused ? F.W.sstride : 0, fused ? F.mode : 0,
-      fused ? F.W.ctr : nullptr, fused ? n_q * 4 : 0);
+      n_max, st, s, fused ? F.W.smax : nullptr, fused ? F.W.sstride : 0, fused ? F.mode : 0);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
   e = launch_topk_fused(scores, n_max, n_q, n_vis, n_max, kTopK, F, sel, ws_topk, st, s);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
   const float sm_scale = params ? params->sm_scale : 1.0f / sqrtf((float)kDim);
   const double rope_base = params ? params->rope_base : 10000.0;
+  // the attention inputs were final before the indexer started (it waits for
+  // every earlier grid), so the attention may stage them during the top-k
   return from_cuda(launch_attn_tc(q, kv_cache, n_max, n_seq, sel, kTopK, swa_cache, swa_cap, q_seq, pos, swa_first,
-                                  swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, ws_attn, st, s));
+                                  swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, ws_attn, st, s, true));
 }
 
 csa2_status csa2_get_device_status(csa2_stream_t stream, csa2_status *out) {

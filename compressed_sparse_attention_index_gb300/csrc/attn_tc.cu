@@ -32,6 +32,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.cuh"
 #include "tc_ptx.cuh"
@@ -113,9 +115,10 @@ struct AttnTcArgs {
   float scale_log2;
   double inv_freq[kRopeDim / 2];   // rope_base^(-2i/64)
   int nsplit, chunks_per_split;
-  float *part;      // [n_q][nsplit][64][512]
+  float *part;      // [n_q][nsplit][64][512]: unnormalised O
   float *part_ml;   // [n_q][nsplit][2][64]
   int *status;
+  int settled;      // q, the window cache and the per-query arrays may be read before the grid ahead completes
 };
 
 // cos and sin of theta = pos * inv_freq (inv_freq = rope_base^(-2i/64), computed
@@ -140,11 +143,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kSmBars);
   uint64_t &bar_s = bars[0], &bar_o = bars[1];
   uint32_t &tmem_sh = *reinterpret_cast<uint32_t *>(sm + kSmBars + 16);
-  volatile int &need_rescale = *reinterpret_cast<volatile int *>(sm + kSmBars + 20);
   volatile int &bad_sh = *reinterpret_cast<volatile int *>(sm + kSmBars + 24);
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int qi = blockIdx.y, split = blockIdx.x;
+  // grid (n_q, nsplit), the last split first: the window-only chunks, which
+  // need no selection, are the first CTAs to be placed
+  const int qi = blockIdx.x, split = A.nsplit - 1 - (int)blockIdx.y;
+  // The selection (sel) comes from the grid ahead.  With settled inputs the
+  // wait is put off until the first chunk that holds selected entries: Q is
+  // staged and window-only chunks run while the selection finishes.  (TMEM is
+  // taken before the wait only then, when the grid ahead is the top-k, which
+  // holds no TMEM.)
+  bool waited = false;
+  if (!A.settled) {
+    griddep_wait();
+    griddep_launch();
+    waited = true;
+  }
   const int seq = __ldg(A.q_seq + qi);
   const int swa_cnt = __ldg(A.swa_cnt + qi), swa_first = __ldg(A.swa_first + qi);
   const bool bad = seq < 0 || seq >= A.n_seq || swa_cnt < 0 || swa_cnt > kSwa ||
@@ -163,7 +178,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   if (warp == 0) ptx::tmem_alloc(&tmem_sh, kAttTmemCols);
   if (t < kHeads) m_ref[t] = -INFINITY;
   // start the first chunk's record reads (L2 prefetch) while Q is staged
-  if (c0 < c1) {
+  if (waited && c0 < c1) {
     const int e = t >> 1, half = t & 1, slot = c0 * kTcChunk + e;
     const uint8_t *rec = nullptr;
     int bytes = 0;
@@ -209,6 +224,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   bool any_chunk = false;
 
   for (int c = c0; c < c1; c++) {
+    if (!waited && c * kTcChunk < A.sel_stride) {     // the chunk holds selected entries
+      griddep_wait();
+      griddep_launch();
+      waited = true;
+    }
     // ---------------------------------------------------------- gather + dequantise
     {
       const int e = t >> 1, half = t & 1;             // entry slot e, dims [256*half, 256*half+256)
@@ -311,6 +331,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       ptx::tc_commit(&bar_s);
     }
     // ---------------------------------------------------------- softmax (all 8 warps)
+    int need_rescale = 0;
     // warp w: TMEM lane quarter w%4 (entries 32*(w%4) ..), heads 32*(w/4) .. +31
     {
       const int quarter = warp & 3, hb = (warp >> 2) * 32;
@@ -345,6 +366,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       }
       red[quarter][hb + lane] = v[0];
       __syncthreads();
+      int rs = 0;                                      // some head's accumulators need rescaling
       if (t < kHeads) {
         const float cm = fmaxf(fmaxf(red[0][t], red[1][t]), fmaxf(red[2][t], red[3][t]));
         const float mo = m_ref[t];
@@ -354,13 +376,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
           m_ref[t] = cm;
         }
         alpha_sh[t] = al;
+        rs = al != 1.f && al != 0.f;
       }
-      __syncthreads();
-      if (t == 0) {
-        int rs = 0;
-        for (int h = 0; h < kHeads; h++) rs |= (alpha_sh[h] != 1.f && alpha_sh[h] != 0.f) ? 1 : 0;
-        need_rescale = rs;
-      }
+      need_rescale = __syncthreads_or(rs);
       // numerators, bf16 hi + lo, into P[head][entry] (K-major, 128B swizzle);
       // S is read from TMEM again rather than kept live through the reduction
       const uint32_t pe = (e >> 6) * 1024;             // entry atom
@@ -438,6 +456,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     if (bad_sh) break;
   }
 
+  if (!waited) {
+    griddep_wait();
+    griddep_launch();
+  }
   // ---------------------------------------------------------- read-out
   {
     const int quarter = warp & 3;
@@ -475,6 +497,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
             else reinterpret_cast<__nv_bfloat16 *>(A.out)[off] = __float2bfloat16_rn(x);
           }
         } else {
+          // partial O[head][dim]: for each head the warp writes one 128-B line
           float *P = A.part + ((int64_t)qi * A.nsplit + split) * kHeads * kDim;
 #pragma unroll
           for (int i = 0; i < 32; i++) P[(half * 32 + i) * kDim + d] = __uint_as_float(r[i]);
@@ -500,63 +523,106 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   }
 }
 
-// Combine the split partials of one (query, head) row: 256 threads, one dim pair each.
+// Combine the split partials of one query over 32 output dims: grid
+// (kDim / 32, n_q), 256 threads, thread = (head, 8 consecutive dims).
+// Weights w_s = 2^(m_s - max_s m_s) per head, O = sum_s w_s O_s / sum_s w_s l_s,
+// then the RoPE pairs are rotated by -pos.
+constexpr int kMaxSplit = 8;
 __global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnTcArgs A) {
-  const int qi = blockIdx.y, h = blockIdx.x, t = threadIdx.x;
-  const float *ml = A.part_ml + (int64_t)qi * A.nsplit * 2 * kHeads;
+  griddep_wait();
+  griddep_launch();
+  const int qi = blockIdx.y, t = threadIdx.x, ns = A.nsplit;
+  const int h = t >> 2, d = blockIdx.x * 32 + (t & 3) * 8;
+  const float *ml = A.part_ml + (int64_t)qi * ns * 2 * kHeads;
+  float4 v[kMaxSplit][2];                            // every split's loads in flight at once
+  float m[kMaxSplit], l[kMaxSplit];
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; s++) {
+    if (s < ns) {
+      const float4 *src = reinterpret_cast<const float4 *>(A.part + (((int64_t)qi * ns + s) * kHeads + h) * kDim + d);
+      v[s][0] = src[0];
+      v[s][1] = src[1];
+      m[s] = ml[s * 2 * kHeads + h];
+      l[s] = ml[s * 2 * kHeads + kHeads + h];
+    }
+  }
   float M = -INFINITY;
-  for (int s = 0; s < A.nsplit; s++) M = fmaxf(M, ml[s * 2 * kHeads + h]);
-  float L = 0.f, x = 0.f, y = 0.f;
-  const int d = 2 * t;
-  if (M != -INFINITY) {
-    for (int s = 0; s < A.nsplit; s++) {
-      const float m = ml[s * 2 * kHeads + h];
-      if (m == -INFINITY) continue;
-      const float wgt = exp2f(m - M);
-      L += wgt * ml[s * 2 * kHeads + kHeads + h];
-      const float2 v =
-          *reinterpret_cast<const float2 *>(A.part + (((int64_t)qi * A.nsplit + s) * kHeads + h) * kDim + d);
-      x += wgt * v.x;
-      y += wgt * v.y;
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; s++)
+    if (s < ns) M = fmaxf(M, m[s]);
+  float L = 0.f, y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; s++) {
+    if (s < ns && M != -INFINITY && m[s] != -INFINITY) {
+      const float w = exp2f(m[s] - M);
+      L += w * l[s];
+      const float e[8] = {v[s][0].x, v[s][0].y, v[s][0].z, v[s][0].w, v[s][1].x, v[s][1].y, v[s][1].z, v[s][1].w};
+#pragma unroll
+      for (int j = 0; j < 8; j++) y[j] += w * e[j];
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  x *= inv;
-  y *= inv;
+#pragma unroll
+  for (int j = 0; j < 8; j++) y[j] *= inv;
   if (d >= kRopeOff) {
-    float c, sn;
-    rope_cs(A.inv_freq[(d - kRopeOff) >> 1], __ldg(A.pos + qi), c, sn);
-    const float a = x, b = y;
-    x = a * c + b * sn;
-    y = -a * sn + b * c;
+    const int pos = __ldg(A.pos + qi);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      float c, sn;
+      rope_cs(A.inv_freq[(d + j - kRopeOff) >> 1], pos, c, sn);
+      const float a = y[j], b = y[j + 1];
+      y[j] = a * c + b * sn;
+      y[j + 1] = -a * sn + b * c;
+    }
   }
   const int64_t off = ((int64_t)qi * kHeads + h) * kDim + d;
-  if (A.out_f32)
-    *reinterpret_cast<float2 *>(static_cast<float *>(A.out) + off) = make_float2(x, y);
-  else
-    *reinterpret_cast<__nv_bfloat162 *>(static_cast<uint16_t *>(A.out) + off) = __floats2bfloat162_rn(x, y);
+  if (A.out_f32) {
+    float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(A.out) + off);
+    o[0] = make_float4(y[0], y[1], y[2], y[3]);
+    o[1] = make_float4(y[4], y[5], y[6], y[7]);
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(y[2 * j], y[2 * j + 1]);
+      w[j] = *reinterpret_cast<const uint32_t *>(&b2);
+    }
+    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(A.out) + off) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 }
 
 static int attn_chunks(int sel_stride) { return (sel_stride + kSwa + kTcChunk - 1) / kTcChunk; }
 
-// Split the chunks of a query over CTAs when the batch alone cannot fill the GPU.
-int attn_nsplit(int n_q, int sel_stride) {
+// How the chunks of a query are spread over CTAs: one chunk per CTA while the
+// CTAs whose chunks hold selected entries fit one wave on a 152-SM GPU (the
+// window-only chunks are placed first and run while the selection finishes);
+// else contiguous runs of chunks, at least one CTA per query.
+struct AttnPlan {
+  int nsplit, cps;
+};
+static AttnPlan attn_plan(int n_q, int sel_stride) {
+  constexpr int kSms = 152;
   const int chunks = attn_chunks(sel_stride);
-  const int ns = (2 * 152 + n_q - 1) / n_q;
-  return ns < 1 ? 1 : (ns > chunks ? chunks : ns);
+  const int sel_ch = (sel_stride + kTcChunk - 1) / kTcChunk;
+  if (n_q * sel_ch <= kSms) return AttnPlan{chunks, 1};
+  const int ns = std::max(1, std::min(chunks, kSms / n_q));
+  const int cps = (chunks + ns - 1) / ns;
+  return AttnPlan{(chunks + cps - 1) / cps, cps};
 }
 
 size_t attn_workspace_bytes(int n_q, int sel_stride) {
-  const int ns = attn_nsplit(n_q, sel_stride);
-  if (ns == 1) return 0;
-  return (size_t)n_q * ns * (kHeads * kDim + 2 * kHeads) * sizeof(float);
+  const AttnPlan p = attn_plan(n_q, sel_stride);
+  if (p.nsplit == 1) return 0;
+  return (size_t)n_q * p.nsplit * (kHeads * kDim + 2 * kHeads) * sizeof(float);
 }
 
 cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_seq, const int32_t *sel, int sel_stride,
                            const void *swa, int swa_cap, const int32_t *q_seq, const int32_t *pos,
                            const int32_t *swa_first, const int32_t *swa_cnt, int n_q, void *out, int out_dtype,
-                           float sm_scale, double rope_base, void *ws, int *status, cudaStream_t st) {
+                           float sm_scale, double rope_base, void *ws, int *status, cudaStream_t st,
+                           bool inputs_settled) {
   AttnTcArgs A;
+  A.settled = inputs_settled ? 1 : 0;
   A.q = static_cast<const uint16_t *>(q);
   A.kv = static_cast<const uint8_t *>(kv);
   A.n_max = n_max;
@@ -573,10 +639,9 @@ cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_s
   A.out_f32 = out_dtype == CSA2_OUT_F32;
   A.scale_log2 = sm_scale * 1.4426950408889634f;
   for (int i = 0; i < kRopeDim / 2; i++) A.inv_freq[i] = pow(rope_base, -2.0 * i / (double)kRopeDim);
-  const int chunks = attn_chunks(sel_stride);
-  A.nsplit = attn_nsplit(n_q, sel_stride);
-  A.chunks_per_split = (chunks + A.nsplit - 1) / A.nsplit;
-  A.nsplit = (chunks + A.chunks_per_split - 1) / A.chunks_per_split;
+  const AttnPlan plan = attn_plan(n_q, sel_stride);
+  A.nsplit = plan.nsplit;
+  A.chunks_per_split = plan.cps;
   A.part = static_cast<float *>(ws);
   A.part_ml = A.part + (size_t)n_q * A.nsplit * kHeads * kDim;
   A.status = status;
@@ -588,9 +653,9 @@ cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_s
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  attn_tc_kernel<<<dim3(A.nsplit, n_q), kTcThreads, kSmAlloc, st>>>(A);
-  if (A.nsplit > 1) attn_tc_merge_kernel<<<dim3(kHeads, n_q), 256, 0, st>>>(A);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(attn_tc_kernel, dim3(n_q, A.nsplit), dim3(kTcThreads), kSmAlloc, st, 1u, A);
+  if (e != cudaSuccess || A.nsplit == 1) return e;
+  return launch_pdl(attn_tc_merge_kernel, dim3(kDim / 32, n_q), dim3(256), 0, st, 1u, A);
 }
 
 }  // namespace csa2

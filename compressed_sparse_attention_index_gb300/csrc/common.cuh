@@ -48,7 +48,15 @@ __device__ __forceinline__ uint32_t order_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Bounded spin helper for any cross-CTA wait (none used yet).
-constexpr long long kSpinLimit = 1LL << 26;
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialisation attribute may start before the grid ahead of it on the
+// stream has finished; griddep_wait() returns once that grid has completed and
+// its memory is visible (at once when there is no such grid).  griddep_launch()
+// lets the next grid on the stream start early.  Every kernel of this library
+// waits before it reads anything that a grid still running may write, and
+// signals only after its own wait, so a grid that starts early finds every
+// grid two or more places ahead of it complete.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 }  // namespace csa2

@@ -7,14 +7,40 @@
 
 namespace csa2 {
 
-// Scratch of a long-row top-k, per row q: smax[q][sstride] (supergroup maxima,
-// or partial maxima), ctr[q][4] (candidates appended, collecting CTAs done),
-// cand[q][8192] (64-bit candidate keys).
+// Scratch of a long-row top-k: smax[q][sstride], the supergroup maxima (or
+// partial maxima) of row q.
 struct LongRowWs {
-  uint32_t *smax, *ctr;
-  uint64_t *cand;
+  uint32_t *smax;
   int64_t sstride;
 };
+
+// Launch `kern` with programmatic stream serialisation (the kernel calls
+// griddep_wait before it reads what an earlier grid wrote) and, when
+// cluster_x > 1, thread-block clusters of cluster_x CTAs along x.
+template <class... Params, class... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       unsigned cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  unsigned na = 0;
+  at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[na].val.programmaticStreamSerializationAllowed = 1;
+  na++;
+  if (cluster_x > 1) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = cluster_x;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    na++;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // Top-k plan of the fused decode: mode -1 one CTA per row (no scratch); 0 the
 // standalone passes; 1 / 2 the indexer's epilogue writes the maxima (512-entry
@@ -24,18 +50,22 @@ struct FusedTopk {
   int64_t sgi;
   int parts;
   LongRowWs W;
+  // optional: the latent cache [n_seq][n_max][288] and the queries' sequences,
+  // for an L2 prefetch of the selected records (modes 1 and 2)
+  const uint8_t *kv;
+  const int32_t *q_seq;
+  int n_seq;
 };
 
 cudaError_t launch_pack(int kind, const void *src, int64_t rows, int m, const float *gate, void *dst,
                         void *dst_scales, cudaStream_t st);
 
-// smax / sstride / smax_mode: maxima for a fused top-k (smax_mode 0: none);
-// clear / n_clear: words zeroed by the kernel before anything else.
+// smax / sstride / smax_mode: maxima for a fused top-k (smax_mode 0: none).
 cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
                                   const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
                                   const int32_t *n_vis, int n_q, const int32_t *pool, float *scores, int64_t stride,
                                   int *status, cudaStream_t st, uint32_t *smax = nullptr, int64_t sstride = 0,
-                                  int smax_mode = 0, uint32_t *clear = nullptr, int n_clear = 0);
+                                  int smax_mode = 0);
 
 size_t topk_workspace_bytes(int n_q, int64_t n_items, int k);
 bool topk_items_supported(int64_t n_items, int k);
@@ -47,10 +77,15 @@ cudaError_t launch_topk_fused(const float *scores, int64_t stride, int n_q, cons
                               int k, const FusedTopk &F, int32_t *out, void *ws, int *status, cudaStream_t st);
 
 size_t attn_workspace_bytes(int n_q, int sel_stride);
+// inputs_settled: q, the window cache and the per-query arrays were final
+// before the grid ahead of this one on the stream started (so inside
+// csa2_decode): the kernel then stages Q and runs its window-only chunks before
+// it waits for the selection.
 cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_seq, const int32_t *sel,
                            int sel_stride, const void *swa, int swa_cap, const int32_t *q_seq, const int32_t *pos,
                            const int32_t *swa_first, const int32_t *swa_cnt, int n_q, void *out, int out_dtype,
-                           float sm_scale, double rope_base, void *ws, int *status, cudaStream_t st);
+                           float sm_scale, double rope_base, void *ws, int *status, cudaStream_t st,
+                           bool inputs_settled = false);
 
 int *status_word_ptr();
 

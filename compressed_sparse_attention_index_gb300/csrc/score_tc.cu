@@ -100,8 +100,6 @@ struct ScoreTcArgs {
   uint32_t *smax;
   int64_t sstride;
   int smax_mode;
-  uint32_t *clear;         // n_clear words zeroed by block 0 before anything else
-  int n_clear;
 };
 
 // Work schedule shared by every role: unit index T = blockIdx.x + k * gridDim.x
@@ -183,8 +181,9 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < P.n_clear; i += blockDim.x) P.clear[i] = 0u;
+  // everything below reads inputs or allocates TMEM: after the grid ahead
+  griddep_wait();
+  griddep_launch();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kScStages; s++) {
       ptx::mbar_init(&full_bar[s], 1);
@@ -458,14 +457,11 @@ static int sm_count() {
 cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
                                   const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
                                   const int32_t *n_vis, int n_q, const int32_t *pool, float *scores, int64_t stride,
-                                  int *status, cudaStream_t st, uint32_t *smax, int64_t sstride, int smax_mode,
-                                  uint32_t *clear, int n_clear) {
+                                  int *status, cudaStream_t st, uint32_t *smax, int64_t sstride, int smax_mode) {
   ScoreTcArgs P;
   P.smax = smax;
   P.sstride = sstride;
   P.smax_mode = pool == nullptr ? smax_mode : 0;
-  P.clear = clear;
-  P.n_clear = clear != nullptr ? n_clear : 0;
   P.key_nib = key_nib;
   P.q_nib = q_nib;
   P.key_scale = key_scale;
@@ -492,8 +488,7 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
     attr_done[dev] = true;
   }
   const int64_t grid = total_units < sm_count() ? total_units : sm_count();
-  index_score_tc_kernel<<<(unsigned)grid, kScThreads, smem, st>>>(P);
-  return cudaGetLastError();
+  return launch_pdl(index_score_tc_kernel, dim3((unsigned)grid), dim3(kScThreads), smem, st, 1u, P);
 }
 
 }  // namespace csa2

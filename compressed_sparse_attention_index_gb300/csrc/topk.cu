@@ -37,6 +37,11 @@ struct TopkSrc {
   int block;              // 1 or 8
   int64_t n_max;          // entries per row (Full) or 16384 (pool)
   int64_t n_items;        // items per row
+  // optional (plain rows): latent cache records [n_seq][n_max][288] that the
+  // attention reads next; the selected ones are prefetched into L2
+  const uint8_t *kv_pf;
+  const int32_t *q_seq;
+  int n_seq;
 };
 
 // Key of item i of query q; false if the item is not valid.
@@ -241,12 +246,32 @@ __device__ __forceinline__ int warp_sum(int v) {
   return v;
 }
 
+// Block-wide exclusive prefix sum of one int per thread, in thread order;
+// *total receives the sum.  Two barriers.
+__device__ int block_excl_scan(int c, int *total) {
+  __shared__ int wsum[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  __syncthreads();                                   // an earlier call's readers are done with wsum
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  const int w = lane < nw ? wsum[lane] : 0;
+  *total = __reduce_add_sync(0xFFFFFFFFu, w);
+  return __reduce_add_sync(0xFFFFFFFFu, lane < warp ? w : 0) + incl - c;
+}
+
 // Block-wide: the rem-th largest (with multiplicity) of the values v[i] with
 // sel(i), i < n (shared memory), found eight bits per step from bit 31 down to
 // bit `low` (a multiple of 8); the result has its bits below `low` cleared, so
 // at least rem selected values reach it.  Each step: a 256-bin histogram of
-// the next digit (shared-memory atomics), then warp 0 locates the digit by a
-// suffix scan over the bins while the other threads clear the next step's
+// the next digit (shared-memory atomics; a warp whose values all share the
+// digit, as leading digits often do, adds them with one), then warp 0 locates the digit
+// by a suffix scan over the bins while the other threads clear the next step's
 // histogram (two alternate): two barriers per step.  hist: 512 counters.
 template <class Sel>
 __device__ uint32_t block_kth256(const uint32_t *v, int n, int rem, int low, Sel sel, uint32_t *hist) {
@@ -259,9 +284,21 @@ __device__ uint32_t block_kth256(const uint32_t *v, int n, int rem, int low, Sel
   for (int shift = 24, buf = 0; shift >= low; shift -= 8, buf ^= 1) {
     uint32_t *h = hist + buf * 256;
     const uint32_t prefix = prefix_sh, pmask = pmask_sh;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const uint32_t x = v[i];
-      if ((x & pmask) == prefix && sel(i)) atomicAdd(&h[(x >> shift) & 255u], 1u);
+    for (int b0 = 0; b0 < n; b0 += blockDim.x) {      // uniform trip count: whole warps
+      const int i = b0 + threadIdx.x;
+      const uint32_t x = i < n ? v[i] : 0u;
+      const bool ok = i < n && (x & pmask) == prefix && sel(i);
+      const unsigned act = __ballot_sync(0xFFFFFFFFu, ok);
+      if (ok) {
+        const uint32_t d = (x >> shift) & 255u;
+        const int first = __ffs(act) - 1;
+        const uint32_t d0 = __shfl_sync(act, d, first);
+        if (__all_sync(act, d == d0)) {
+          if (lane == first) atomicAdd(&h[d], (uint32_t)__popc(act));
+        } else {
+          atomicAdd(&h[d], 1u);
+        }
+      }
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -321,8 +358,12 @@ struct BlockReduce {
 // the selected indices and places them in ascending order by bucketing them
 // by index (buckets of power-of-two width; a few indices per bucket).  keys
 // and sk are reused as scratch.  sel: >= k ints; bins: >= 4096 counters.
-// out[0..k): ascending indices, -1 padding.
-__device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t *out, int32_t *sel, uint32_t *bins) {
+// out[0..k): ascending indices, -1 padding.  pf: null, or the base of records
+// of kKvBytes per index, which are prefetched into L2 once the set is known.
+// by_index: keys[] is already in ascending index order; the selected keys are
+// then written out by one order-keeping compaction.
+__device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t *out, int32_t *sel, uint32_t *bins,
+                             const uint8_t *pf = nullptr, bool by_index = false) {
   __shared__ int cnt_sh[2];
   __shared__ int n_sel;
   __shared__ uint32_t red_slots[2][32];
@@ -350,6 +391,31 @@ __device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t
     K = ((uint64_t)t32 << 32) | tlo;
   }
   __syncthreads();
+  if (by_index) {
+    // thread t keeps keys [t * per, t * per + per) in order
+    const int per = (n + blockDim.x - 1) / blockDim.x, i0 = threadIdx.x * per;
+    int c = 0;
+    for (int j = 0; j < per; j++) c += (i0 + j < n && keys[i0 + j] >= K) ? 1 : 0;
+    int total;
+    int pos = block_excl_scan(c, &total);
+    for (int j = 0; j < per; j++) {
+      const int i = i0 + j;
+      if (i < n && keys[i] >= K) {
+        const int32_t idx = (int32_t)(~(uint32_t)(keys[i] & 0xFFFFFFFFu));
+        out[pos++] = idx;
+        if (pf != nullptr) {
+          const uint8_t *rec = pf + (int64_t)idx * kKvBytes;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(rec));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + 128));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + 256));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + kKvBytes - 1));
+        }
+      }
+    }
+    for (int i = take + threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
+    __syncthreads();
+    return;
+  }
   // ---- compact the selected indices
   for (int b0 = 0; b0 < n; b0 += blockDim.x) {
     const int i = b0 + threadIdx.x;
@@ -363,6 +429,12 @@ __device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t
     if (ok) sel[base] = (int32_t)(~(uint32_t)(x & 0xFFFFFFFFu));
   }
   __syncthreads();
+  if (pf != nullptr)
+    for (int i = threadIdx.x; i < 4 * take; i += blockDim.x) {   // a record spans at most four 128-B lines
+      const uint8_t *rec = pf + (int64_t)sel[i >> 2] * kKvBytes;
+      const int o = (i & 3) == 3 ? kKvBytes - 1 : (i & 3) * 128;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + o));
+    }
   // ---- ascending index order: 2,048 index buckets (counts, cursors); the
   // key buffer (the keys are in registers now) receives them bucket by bucket
   uint32_t *h2 = bins, *c2 = bins + 2048;
@@ -401,6 +473,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
   __shared__ SelectShared sh;
   sh.whist = reinterpret_cast<uint32_t *>(sel + kMaxK);                          // [32][256]
   __shared__ int n_keys;
+  griddep_wait();
+  griddep_launch();
   const int q = blockIdx.x;
   const int nv = query_nv(S, q, status);
   if (threadIdx.x == 0) n_keys = 0;
@@ -487,15 +561,16 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
 // about 4k supergroups).  Pass 2 (P CTAs per row) takes T = the k-th largest
 // supergroup maximum with its low 16 bits cleared: at least k supergroups
 // reach T, so at least k items do, so the k-th best item key is >= T and every
-// top-k item has a key >= T.  Each CTA streams its share of the row and
-// appends the items with key >= T (a small superset of the top-k) to the
-// row's candidate buffer; the last CTA of the row to finish (a counter; no CTA
-// ever waits for another) runs the exact selection on the candidates, or on
-// the whole row if the buffer overflowed.
+// top-k item has a key >= T.  The P CTAs of a row form one thread-block
+// cluster.  Each streams its share of the row and gathers the items with key
+// >= T (a small superset of the top-k) in its own shared memory; after a
+// cluster barrier, CTA 0 reads every CTA's candidates through distributed
+// shared memory and runs the exact selection on them, or on the whole row if
+// they overflow its buffer.  A second cluster barrier keeps the other CTAs
+// (and their shared memory) alive until CTA 0 has read them.
 //
 // Workspace, per row q: smax[q][sstride] (the supergroup maxima, 0 = no valid
-// item), ctr[q][4] (candidates appended, CTAs done), cand[q][kCandCap] (keys).
-// Pass 1 clears ctr; slots past a row's valid length are never read.
+// item); slots past a row's valid length are never read.
 constexpr int kCollectThreads = 1024;
 constexpr int kSuperCap = 16384;    // supergroups per row (held in shared memory by pass 2)
 
@@ -514,14 +589,12 @@ __host__ __device__ inline LongRowWs long_row_ws(void *ws, int n_q, int64_t n_it
   const int64_t sgi = long_row_sgi(n_items, k);
   w.sstride = ((n_items + sgi - 1) / sgi + 3) / 4 * 4;
   w.smax = static_cast<uint32_t *>(ws);
-  w.ctr = w.smax + (int64_t)n_q * w.sstride;
-  w.cand = reinterpret_cast<uint64_t *>(w.ctr + (int64_t)n_q * 4);   // 16-B aligned: parts are multiples of 4 words
   return w;
 }
 
 __host__ __device__ inline size_t long_row_ws_bytes(int n_q, int64_t n_items, int k) {
   const LongRowWs w = long_row_ws(nullptr, n_q, n_items, k);
-  return (size_t)n_q * ((size_t)(w.sstride + 4) * 4 + (size_t)kCandCap * 8);
+  return (size_t)n_q * (size_t)w.sstride * 4;
 }
 
 // Pass 1.  A warp step covers 32 x IPL items: plain rows one float4 (IPL = 4)
@@ -529,15 +602,15 @@ __host__ __device__ inline size_t long_row_ws_bytes(int n_q, int64_t n_items, in
 // (four loads in flight per lane) and a pass of max(sgi, 4 steps) items, so
 // no two warps share a supergroup.  Supergroups smaller than a step reduce
 // over sgi / IPL lanes; larger ones over the whole warp and over steps.
-// Block (0, q) clears row q's counters.
 template <bool kPlain>
 __global__ void __launch_bounds__(256) topk_smax_kernel(TopkSrc S, int64_t sgi, LongRowWs W, int *status) {
   constexpr int IPL = kPlain ? 4 : 1;
   constexpr int64_t kStep = 32 * IPL;
+  griddep_wait();
+  griddep_launch();
   const int q = blockIdx.y;
   const int nv = query_nv(S, q, status);
   const int lane = threadIdx.x & 31;
-  if (blockIdx.x == 0 && threadIdx.x < 4) W.ctr[(int64_t)q * 4 + threadIdx.x] = 0u;
   const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int lsg = __ffsll(sgi) - 1;
@@ -598,27 +671,57 @@ __global__ void __launch_bounds__(256) topk_smax_kernel(TopkSrc S, int64_t sgi, 
   }
 }
 
-// Pass 2: grid (P, n_q).
+// Distributed shared memory of the cluster: the address of this CTA's
+// shared-memory location p in the CTA of cluster rank r, and loads from it.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t r) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(a)
+               : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(r));
+  return a;
+}
+__device__ __forceinline__ uint32_t dsmem_ld32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t dsmem_ld64(uint32_t a) {
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  return v;
+}
+// Every thread of every CTA of the cluster; orders shared-memory writes before
+// the barrier with reads after it, across the cluster.
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+constexpr int kMaxCluster = 16;
+
+// Pass 2: grid (P, n_q), clusters of P CTAs along x (P <= kMaxCluster): the
+// cluster rank of a CTA is blockIdx.x.  No thread returns before the second
+// cluster barrier.
 __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S, int64_t sgi, int parts, int k,
                                                                        LongRowWs W, int32_t *__restrict__ out,
                                                                        int *status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint64_t *keys = reinterpret_cast<uint64_t *>(smem_raw);               // [kCandCap] (last CTA)
+  uint64_t *keys = reinterpret_cast<uint64_t *>(smem_raw);               // [kCandCap] (CTA 0)
   int32_t *sel = reinterpret_cast<int32_t *>(keys + kCandCap);           // [kMaxK]
   uint32_t *sv = reinterpret_cast<uint32_t *>(sel + kMaxK);              // [kSuperCap] supergroup maxima
   __shared__ SelectShared sh;
   sh.whist = sv + kSuperCap;                                             // [32][256]
-  __shared__ uint32_t T_sh, cnt[2];
-  __shared__ int n_vs, is_last;
+  __shared__ uint32_t T_sh;
+  __shared__ int n_vs, n_lc, lc_sorted;
+  __shared__ int c_off[kMaxCluster + 1], c_bad, c_sorted;
+  griddep_wait();
+  griddep_launch();
   const int q = blockIdx.y, P = gridDim.x, part = blockIdx.x;
   const int nv = query_nv(S, q, status);
+  const int pf_seq = (S.kv_pf != nullptr && part == 0) ? __ldg(S.q_seq + q) : -1;   // used at the end
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t *ctr = W.ctr + (int64_t)q * 4;
-  uint64_t *cq = W.cand + (int64_t)q * kCandCap;
   const bool plain = S.pool == nullptr && S.block == 1;
   const int64_t valid_items = plain ? nv : (S.pool != nullptr ? S.n_items : ((int64_t)nv + kBlock - 1) / kBlock);
   const int ns = (int)((valid_items + sgi - 1) / sgi);                   // supergroups that may hold a valid item
-  if (threadIdx.x == 0) { n_vs = 0; T_sh = 1u; }                         // T = 1: every valid item
+  if (threadIdx.x == 0) { n_vs = 0; T_sh = 1u; n_lc = 0; }             // T = 1: every valid item
   __syncthreads();
   // ---- the supergroup maxima (16-B loads; slots past ns are never used).
   // parts == 4: each supergroup's maximum is stored as four partial maxima.
@@ -648,43 +751,47 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
     if (lane == 0 && vs) atomicAdd(&n_vs, vs);
   }
   __syncthreads();
-  // ---- T: the largest multiple of 2^16 that at least k supergroup maxima
-  // reach, bit by bit from the top, by warp 0 alone (sv is zero-padded)
+  // ---- T: the largest multiple of 2^16 that at least k supergroup maxima reach
   if (n_vs > k) {
     const uint32_t t = block_kth256(sv, ns, k, 16, [](int) { return true; }, sh.whist);
     if (threadIdx.x == 0) T_sh = t;
   }
   __syncthreads();
   const uint32_t T = T_sh;
-  // ---- stream the supergroups of this CTA's share that reach T, appending keys >= T
+  // ---- list the supergroups that reach T in index order; this CTA takes a
+  // contiguous, equal share of that list (ranks [r_lo, r_hi)), so that the
+  // CTAs' candidates follow one another in index order and every CTA streams
+  // the same number of supergroups however they bunch together
+  uint64_t *lc = reinterpret_cast<uint64_t *>(sv);    // this CTA's keys >= T (over sv, once listed)
+  constexpr int kLocalCap = kSuperCap / 2;
   {
-    const int per = (ns + P - 1) / P;
-    const int s_lo = part * per, s_hi = min(ns, s_lo + per);
     const float *row = S.scores + (int64_t)q * S.stride;
     const bool row16 = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-    // list them (order irrelevant)
-    int32_t *slist = reinterpret_cast<int32_t *>(keys);     // keys is used by the last CTA only after this
-    __shared__ int n_sl, n_lc;
-    __shared__ uint32_t g_base;
-    if (threadIdx.x == 0) { n_sl = 0; n_lc = 0; }
-    __syncthreads();
-    for (int b0 = s_lo; b0 < s_hi; b0 += blockDim.x) {
-      const int i = b0 + threadIdx.x;
-      const bool ok = i < s_hi && sv[i] >= T && sv[i] != 0u;
-      const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
-      if (!bal) continue;
-      int base = 0;
-      if (lane == 0) base = atomicAdd(&n_sl, __popc(bal));
-      base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(bal & ((1u << lane) - 1u));
-      if (ok) slist[base] = i;
+    int32_t *slist = reinterpret_cast<int32_t *>(keys);
+    const int run = (ns + blockDim.x - 1) / blockDim.x, g0 = threadIdx.x * run;   // this thread's supergroups
+    int c = 0;
+    for (int j = 0; j < run; j++) {
+      const int i = g0 + j;
+      c += (i < ns && sv[i] >= T && sv[i] != 0u) ? 1 : 0;
+    }
+    int n_listed;
+    int rank = block_excl_scan(c, &n_listed);
+    const int r_lo = (int)((int64_t)part * n_listed / P), r_hi = (int)((int64_t)(part + 1) * n_listed / P);
+    for (int j = 0; j < run && rank < r_hi; j++) {
+      const int i = g0 + j;
+      if (i < ns && sv[i] >= T && sv[i] != 0u) {
+        if (rank >= r_lo) slist[rank - r_lo] = i;
+        rank++;
+      }
     }
     __syncthreads();
-    const int nsl = n_sl;
+    const int nsl = r_hi - r_lo;
     const int64_t total = (int64_t)nsl * sgi;                 // items of the listed supergroups
-    // candidates gather in shared memory (sv is free now), then go out with
-    // one global reservation per CTA
-    uint64_t *lc = reinterpret_cast<uint64_t *>(sv);
-    constexpr int kLocalCap = kSuperCap / 2;
+    // Plain rows with T above the key of +0: key(x) >= T exactly when the raw
+    // bits of x, read as a signed integer, are >= those of T's float (NaN,
+    // -0 and the -inf of missing items included).
+    const bool fast = plain && T > 0x80000000u;
+    const int tb = (int)(T & 0x7FFFFFFFu);
     constexpr int kU = 6;
     const int64_t step = plain ? 4 : 1;
     const int lsg = __ffsll(sgi) - 1;
@@ -716,73 +823,148 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
           }
         }
       }
+      if (fast) {
+        // one integer compare per item; then one reservation per warp, each
+        // thread writing its own candidates in a run
+        int c = 0;
+#pragma unroll
+        for (int u = 0; u < kU; u++)
+          c += (__float_as_int(sc[u].x) >= tb) + (__float_as_int(sc[u].y) >= tb) + (__float_as_int(sc[u].z) >= tb) +
+               (__float_as_int(sc[u].w) >= tb);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int wtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        if (wtot == 0) continue;                       // most warps of most rounds
+        int base = 0;
+        if (lane == 31) base = atomicAdd(&n_lc, wtot);
+        base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - c;
+        if (c > 0) {
+#pragma unroll
+          for (int u = 0; u < kU; u++) {
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+              const float x = e == 0 ? sc[u].x : e == 1 ? sc[u].y : e == 2 ? sc[u].z : sc[u].w;
+              if (__float_as_int(x) >= tb) {
+                if (base < kLocalCap)
+                  lc[base] = ((uint64_t)order_key(x) << 32) | (uint32_t)(~(uint32_t)(base_i[u] + e));
+                base++;
+              }
+            }
+          }
+        }
+        continue;
+      }
+      // the round's keys >= T: ballots first, then one reservation per warp
+      constexpr int kE = 4;                            // items per load (plain rows; block rows use e = 0)
+      unsigned bal[kU * kE];
+      int cnt = 0;
 #pragma unroll
       for (int u = 0; u < kU; u++) {
-        const int64_t i0 = base_i[u];
 #pragma unroll
-        for (int e = 0; e < (plain ? 4 : 1); e++) {
-          uint64_t key;
-          bool ok;
+        for (int e = 0; e < kE; e++) {
+          bool ok = false;
           if (plain) {
             const float x = e == 0 ? sc[u].x : e == 1 ? sc[u].y : e == 2 ? sc[u].z : sc[u].w;
-            const uint32_t kk = order_key(x);
-            ok = i0 >= 0 && i0 + e < nv && kk >= T;
-            key = ((uint64_t)kk << 32) | (uint32_t)(~(uint32_t)(i0 + e));
-          } else {
-            key = gk[u];
-            ok = key != 0 && (uint32_t)(key >> 32) >= T;
+            ok = base_i[u] >= 0 && base_i[u] + e < nv && order_key(x) >= T;
+          } else if (e == 0) {
+            ok = gk[u] != 0 && (uint32_t)(gk[u] >> 32) >= T;
           }
-          if (!__any_sync(0xFFFFFFFFu, ok)) continue;   // most rounds have no candidate
-          const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
-          int base = 0;
-          if (lane == 0) base = atomicAdd(&n_lc, __popc(bal));
-          base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(bal & ((1u << lane) - 1u));
-          if (ok && base < kLocalCap) lc[base] = key;
+          bal[u * kE + e] = __ballot_sync(0xFFFFFFFFu, ok);
+          cnt += __popc(bal[u * kE + e]);
+        }
+      }
+      if (cnt == 0) continue;                          // most rounds of most warps
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&n_lc, cnt);
+      base = __shfl_sync(0xFFFFFFFFu, base, 0);
+      const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+      for (int u = 0; u < kU; u++) {
+#pragma unroll
+        for (int e = 0; e < kE; e++) {
+          const unsigned b = bal[u * kE + e];
+          if (b & (1u << lane)) {
+            const int pos = base + __popc(b & below);
+            uint64_t key;
+            if (plain) {
+              const float x = e == 0 ? sc[u].x : e == 1 ? sc[u].y : e == 2 ? sc[u].z : sc[u].w;
+              key = ((uint64_t)order_key(x) << 32) | (uint32_t)(~(uint32_t)(base_i[u] + e));
+            } else {
+              key = gk[u];
+            }
+            if (pos < kLocalCap) lc[pos] = key;
+          }
+          base += __popc(b);
         }
       }
     }
-    __syncthreads();                                   // slist (in keys) is dead from here
+  }
+  // ---- a short list is put in index order (rank = number of larger index
+  // halves, the index halves being ~index): the lists of the CTAs, taken in
+  // cluster order, then run in index order
+  constexpr int kSortCap = 256;
+  __syncthreads();                                     // lc and n_lc are final
+  {
     const int nl = n_lc;
-    if (threadIdx.x == 0 && nl > 0)                    // more than kLocalCap: force the overflow path
-      g_base = atomicAdd(ctr + 0, nl <= kLocalCap ? (uint32_t)nl : (uint32_t)kCandCap + 1u);
-    __syncthreads();
-    for (int i = threadIdx.x; i < min(nl, kLocalCap); i += blockDim.x)
-      if (g_base + (uint32_t)i < (uint32_t)kCandCap) cq[g_base + i] = lc[i];
+    if (nl <= kSortCap) {
+      uint64_t mine = 0;
+      int r = 0;
+      if ((int)threadIdx.x < nl) {
+        mine = lc[threadIdx.x];
+        const uint32_t lo = (uint32_t)mine;
+        for (int j = 0; j < nl; j++) r += (uint32_t)lc[j] > lo ? 1 : 0;
+      }
+      __syncthreads();
+      if ((int)threadIdx.x < nl) lc[r] = mine;
+    }
+    if (threadIdx.x == 0) lc_sorted = nl <= kSortCap ? 1 : 0;
   }
-  // ---- the last CTA of this row selects (barrier, then one thread fences
-  // and counts: the block's candidate stores are ordered before the count)
-  __syncthreads();
-  __shared__ uint32_t nc_sh;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    is_last = atomicAdd(ctr + 1, 1u) == (uint32_t)(P - 1);
-    if (is_last) {
-      __threadfence();
-      nc_sh = atomicAdd(ctr + 0, 0u);
+  // ---- CTA 0 gathers the cluster's candidates into keys
+  cluster_barrier();                                   // every CTA's lc, n_lc and lc_sorted are final
+  if (part == 0) {
+    if (warp == 0) {
+      const int c = lane < P ? (int)dsmem_ld32(dsmem_addr(&n_lc, (uint32_t)lane)) : 0;
+      const int srt = lane < P ? (int)dsmem_ld32(dsmem_addr(&lc_sorted, (uint32_t)lane)) : 1;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane <= kMaxCluster) c_off[lane] = incl - c;   // c_off[P] = the total
+      const bool over = __any_sync(0xFFFFFFFFu, c > kLocalCap) || __shfl_sync(0xFFFFFFFFu, incl, 31) > kCandCap;
+      const bool all_sorted = __all_sync(0xFFFFFFFFu, srt != 0);
+      if (lane == 0) {
+        c_bad = over ? 1 : 0;
+        c_sorted = all_sorted ? 1 : 0;
+      }
+    }
+    __syncthreads();
+    if (!c_bad) {
+      const int nc = c_off[P];
+      for (int i = threadIdx.x; i < nc; i += blockDim.x) {
+        int r = 0;
+        while (i >= c_off[r + 1]) r++;
+        keys[i] = dsmem_ld64(dsmem_addr(lc + (i - c_off[r]), (uint32_t)r));
+      }
     }
   }
-  __syncthreads();
-  if (!is_last) return;
-  const uint32_t nc_all = nc_sh;
+  cluster_barrier();                                   // the other CTAs' shared memory is no longer read
+  if (part != 0) return;
   int32_t *oq = out + (int64_t)q * k;
-  if (nc_all <= (uint32_t)kCandCap) {
-    const int nc = (int)nc_all;
-    for (int i0 = 0; i0 < nc; i0 += 4 * blockDim.x) {
-      uint64_t v[4];
-#pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const int i = i0 + u * blockDim.x + threadIdx.x;
-        v[u] = i < nc ? __ldcg(cq + i) : 0;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const int i = i0 + u * blockDim.x + threadIdx.x;
-        if (i < nc) keys[i] = v[u];
-        if (i < ((nc + 3) & ~3)) sv[i] = (uint32_t)(v[u] >> 32);   // score halves, zero-padded
-      }
-    }
+  if (!c_bad) {
+    const int nc = c_off[P];
+    for (int i = threadIdx.x; i < ((nc + 3) & ~3); i += blockDim.x)
+      sv[i] = i < nc ? (uint32_t)(keys[i] >> 32) : 0u;   // score halves, zero-padded
     __syncthreads();
-    select_block(keys, sv, nc, k, oq, sel, sh.whist);
+    const uint8_t *pf =
+        (pf_seq >= 0 && pf_seq < S.n_seq) ? S.kv_pf + (int64_t)pf_seq * S.n_max * kKvBytes : nullptr;
+    // pool items run in slot order, not index order: only plain and block rows keep order
+    select_block(keys, sv, nc, k, oq, sel, sh.whist, pf, c_sorted != 0 && S.pool == nullptr);
   } else {
     // too many ties at T for the buffer: exact selection straight over the row
     __shared__ int nvi;
@@ -815,6 +997,54 @@ bool topk_items_supported(int64_t n_items, int k) {
   return n_items < ((int64_t)1 << 31) - 64;          // int32 item indices
 }
 
+static size_t collect_smem_bytes() {
+  return (size_t)kCandCap * 8 + (size_t)kMaxK * 4 + (size_t)kSuperCap * 4 + 32 * 256 * 4;
+}
+
+// Collecting CTAs per row (the cluster size P): one CTA per SM over all rows
+// (the shared memory allows one), at most one per 4,096 items, at most 16,
+// and no larger than lets all n_q clusters be resident at once (a second wave
+// of clusters would double the kernel's time).  Sets the kernel's attributes
+// on first use on a device.
+static unsigned collect_ctas(int dev, int n_q, int64_t n_items) {
+  static int fit[64][kMaxCluster + 1];                // resident clusters of each size (-1: unknown)
+  static int sms[64] = {};
+  static bool init[64] = {};
+  if (dev < 0 || dev >= 64) return 1;
+  const size_t dsm = collect_smem_bytes();
+  if (!init[dev]) {
+    cudaFuncSetAttribute(topk_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm);
+    cudaFuncSetAttribute(topk_collect_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaGetLastError();                                // a refused attribute leaves no error behind
+    cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    for (int c = 0; c <= kMaxCluster; c++) fit[dev][c] = -1;
+    init[dev] = true;
+  }
+  const int m = sms[dev] > 0 ? sms[dev] : 148;
+  int p = (int)std::min<int64_t>(std::min<int64_t>(m / std::max(n_q, 1), n_items / 4096), kMaxCluster);
+  for (; p > 1; p--) {
+    if (fit[dev][p] < 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(p, 1);
+      cfg.blockDim = dim3(kCollectThreads);
+      cfg.dynamicSmemBytes = dsm;
+      cudaLaunchAttribute at;
+      at.id = cudaLaunchAttributeClusterDimension;
+      at.val.clusterDim.x = p;
+      at.val.clusterDim.y = 1;
+      at.val.clusterDim.z = 1;
+      cfg.attrs = &at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, topk_collect_kernel, &cfg) != cudaSuccess) n = 0;
+      cudaGetLastError();
+      fit[dev][p] = n;
+    }
+    if (fit[dev][p] >= n_q) break;
+  }
+  return (unsigned)std::max(p, 1);
+}
+
 cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max, int k,
                         int block, const int32_t *pool, int32_t *out, void *ws, int *status, cudaStream_t st) {
   TopkSrc S;
@@ -825,36 +1055,34 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
   S.block = block;
   S.n_max = n_max;
   S.n_items = topk_items(n_max, block, pool != nullptr);
+  S.kv_pf = nullptr;
+  S.q_seq = nullptr;
+  S.n_seq = 0;
   const size_t dsm_direct = (size_t)kDirectCap * 8 + (size_t)kMaxK * 4 + 32 * 256 * 4 + (size_t)kCandCap * 4;
-  const size_t dsm_collect = (size_t)kCandCap * 8 + (size_t)kMaxK * 4 + (size_t)kSuperCap * 4 + 32 * 256 * 4;
+  const size_t dsm_collect = collect_smem_bytes();
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_done[64] = {};
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
     cudaFuncSetAttribute(topk_direct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm_direct);
-    cudaFuncSetAttribute(topk_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm_collect);
     attr_done[dev] = true;
   }
-  if (S.n_items <= kDirectCap) {
-    topk_direct_kernel<<<n_q, kTopkThreads, dsm_direct, st>>>(S, k, out, status);
-    return cudaGetLastError();
-  }
+  if (S.n_items <= kDirectCap)
+    return launch_pdl(topk_direct_kernel, dim3(n_q), dim3(kTopkThreads), dsm_direct, st, 1u, S, k, out, status);
   const int64_t sgi = long_row_sgi(S.n_items, k);
   const LongRowWs W = long_row_ws(ws, n_q, S.n_items, k);
   const bool plain = pool == nullptr && block == 1;
   const int64_t span = std::max<int64_t>(sgi, plain ? 4 * 128 : 4 * 32);
   const int64_t n_pass = (S.n_items + span - 1) / span;
   const int64_t gx = std::min<int64_t>((n_pass + 7) / 8, 65535);       // one warp pass per warp
-  if (plain)
-    topk_smax_kernel<true><<<dim3((unsigned)gx, n_q), 256, 0, st>>>(S, sgi, W, status);
-  else
-    topk_smax_kernel<false><<<dim3((unsigned)gx, n_q), 256, 0, st>>>(S, sgi, W, status);
-  int sms = 148;
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // one CTA per SM (shared memory): a single wave over all rows
-  const int64_t P = std::max<int64_t>(1, std::min<int64_t>(sms / n_q, S.n_items / 4096));
-  topk_collect_kernel<<<dim3((unsigned)P, n_q), kCollectThreads, dsm_collect, st>>>(S, sgi, 1, k, W, out, status);
-  return cudaGetLastError();
+  cudaError_t e = plain ? launch_pdl(topk_smax_kernel<true>, dim3((unsigned)gx, n_q), dim3(256), 0, st, 1u, S, sgi,
+                                     W, status)
+                        : launch_pdl(topk_smax_kernel<false>, dim3((unsigned)gx, n_q), dim3(256), 0, st, 1u, S, sgi,
+                                     W, status);
+  if (e != cudaSuccess) return e;
+  const unsigned P = collect_ctas(dev, n_q, S.n_items);
+  return launch_pdl(topk_collect_kernel, dim3(P, n_q), dim3(kCollectThreads), dsm_collect, st, P, S, sgi, 1, k, W,
+                    out, status);
 }
 
 // ---------------------------------------------------------------- fused decode
@@ -869,6 +1097,9 @@ FusedTopk topk_fused_plan(void *ws, int n_q, int64_t n_max, int k) {
   F.sgi = 0;
   F.parts = 1;
   F.W = LongRowWs{};
+  F.kv = nullptr;
+  F.q_seq = nullptr;
+  F.n_seq = 0;
   if (n_max <= kDirectCap) { F.mode = -1; return F; }
   const int64_t sgi = long_row_sgi(n_max, k);
   if (sgi != 512 && sgi != 32) return F;
@@ -878,8 +1109,6 @@ FusedTopk topk_fused_plan(void *ws, int n_q, int64_t n_max, int k) {
   LongRowWs &W = F.W;
   W.sstride = sgi == 512 ? (n_max + 511) / 512 * 4 : ((n_max + 31) / 32 + 3) / 4 * 4;
   W.smax = static_cast<uint32_t *>(ws);
-  W.ctr = W.smax + (int64_t)n_q * W.sstride;
-  W.cand = reinterpret_cast<uint64_t *>(W.ctr + (int64_t)n_q * 4);
   return F;
 }
 
@@ -887,7 +1116,7 @@ size_t topk_fused_bytes(int n_q, int64_t n_max, int k) {
   const FusedTopk F = topk_fused_plan(nullptr, n_q, n_max, k);
   if (F.mode == -1) return 0;
   if (F.mode == 0) return topk_workspace_bytes(n_q, n_max, k);
-  return (size_t)n_q * ((size_t)(F.W.sstride + 4) * 4 + (size_t)kCandCap * 8);
+  return (size_t)n_q * (size_t)F.W.sstride * 4;
 }
 
 cudaError_t launch_topk_fused(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max,
@@ -901,20 +1130,15 @@ cudaError_t launch_topk_fused(const float *scores, int64_t stride, int n_q, cons
   S.block = 1;
   S.n_max = n_max;
   S.n_items = n_max;
-  const size_t dsm_collect = (size_t)kCandCap * 8 + (size_t)kMaxK * 4 + (size_t)kSuperCap * 4 + 32 * 256 * 4;
+  S.kv_pf = F.kv;
+  S.q_seq = F.q_seq;
+  S.n_seq = F.n_seq;
+  const size_t dsm_collect = collect_smem_bytes();
   int dev = 0;
   cudaGetDevice(&dev);
-  static bool attr_done[64] = {};
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaFuncSetAttribute(topk_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm_collect);
-    attr_done[dev] = true;
-  }
-  int sms = 148;
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t P = std::max<int64_t>(1, std::min<int64_t>(sms / n_q, n_max / 4096));
-  topk_collect_kernel<<<dim3((unsigned)P, n_q), kCollectThreads, dsm_collect, st>>>(S, F.sgi, F.parts, k, F.W, out,
-                                                                                    status);
-  return cudaGetLastError();
+  const unsigned P = collect_ctas(dev, n_q, n_max);
+  return launch_pdl(topk_collect_kernel, dim3(P, n_q), dim3(kCollectThreads), dsm_collect, st, P, S, F.sgi, F.parts,
+                    k, F.W, out, status);
 }
 
 }  // namespace csa2

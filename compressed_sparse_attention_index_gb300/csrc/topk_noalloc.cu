@@ -9,7 +9,7 @@
 
 namespace csa2 {
 
-// Fixed scratch of CSA2_TOPK_NOALLOC_SCRATCH_BYTES (1 MiB) on every device that
+// Fixed scratch of CSA2_TOPK_NOALLOC_SCRATCH_BYTES (4 MiB) on every device that
 // loads the library, held until the process exits.
 static __device__ __align__(256) uint32_t g_topk_scratch[CSA2_TOPK_NOALLOC_SCRATCH_BYTES / 4];
 

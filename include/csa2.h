@@ -29,13 +29,13 @@
  * physical arrangement below is this library's choice):
  *   KV  (S1) 288 B per entry, array of records [n_seq][n_max][288]: bytes 0..255
  *            hold 512 FP4 E2M1 codes (low nibble = even channel), bytes
- *            256..287 hold 32 E4M3 scales, one per 16 channels
- *            ("512 FP4 values with one E4M3 scale per 16 channels (288 bytes)",
- *            study, "The KV cache").
+ *            256..287 hold 32 E4M3 scales, one per 16 channels (the study's
+ *            section "The KV cache" sizes a main-cache entry at 288 bytes: 512
+ *            FP4 codes and one E4M3 scale for each 16 channels).
  *   IDX (S2) 68 B per entry as two planes, so that every row is 16-B aligned:
  *            nibbles [rows][64] (128 E2M1 codes) and scales [rows][4] (E8M0, one
- *            per 32 channels) ("128 FP4 values with one E8M0 scale per 32
- *            (68 bytes)", same section).  The nibble plane is stored in the
+ *            per 32 channels) (the same section sizes an indexer key at 68
+ *            bytes: 128 FP4 codes, an E8M0 scale for each 32).  The nibble plane is stored in the
  *            64-byte swizzled order of the tensor cores: the 16-byte chunk c
  *            (channels 32c .. 32c+31) of a row at byte address A is stored at
  *            chunk c ^ ((A >> 7) & 3) of that row; with a 512-B aligned plane
@@ -43,8 +43,8 @@
  *            any 8-row-aligned range can be packed independently.  The indexer
  *            query heads (S4) use the same format with rows = n_q * 32.
  *   SWA (S3) 528 B per entry [n_seq][swa_cap][528]: 512 E4M3 values then 16
- *            E8M0 scales, one per 32 channels (reading of "128 entries of 528
- *            FP8 bytes each", same section).
+ *            E8M0 scales, one per 32 channels (a reading of the same section,
+ *            which gives the window as 128 FP8 entries of 528 bytes).
  *
  * Rounding (shared by every packer): round to nearest, ties to even, saturating
  * at the format's largest finite value; the sign of x is kept when the magnitude
@@ -186,8 +186,9 @@ csa2_status csa2_index_score(const void *key_nib, const void *key_scale, int64_t
  *   k             1 .. 2048.
  *   block         1: items are entries j < n_valid.
  *                 8: items are blocks b of 8 entries (b*8 < n_valid), scored by
- *                    the max over their visible entries (reading of "by blocks
- *                    of 8"); the output holds block ids.  pool_blocks must be NULL.
+ *                    the max over their visible entries (a reading of the
+ *                    card's selection in 8-entry blocks); the output holds block
+ *                    ids.  pool_blocks must be NULL.
  *   pool_blocks   NULL, or (device) int32 [n_q][2048] when the scores are Reindex
  *                 pool slots (row length 16384): item s is entry
  *                 8*pool_blocks[q][s/8] + s%8, valid if the block id is >= 0 and
@@ -278,8 +279,8 @@ csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t 
  *
  * Same arguments, results and errors as csa2_topk, without the workspace.  The
  * scratch it needs (rows longer than 16,384 items only: 4 bytes per group of
- * scores plus 80 KiB per query; for 1,048,576-entry rows and k = 512 that is
- * 208 KiB per query) lives in one fixed device array of
+ * scores, 2,048 to 16,384 groups per row; for 1,048,576-entry rows and k = 512
+ * that is 8 KiB per query) lives in one fixed device array of
  * CSA2_TOPK_NOALLOC_SCRATCH_BYTES (4 MiB) that every GPU which loads the
  * library holds until the process exits.  A call whose
  * scratch would exceed it returns CSA2_ERR_WORKSPACE and launches nothing (use

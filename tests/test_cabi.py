@@ -76,8 +76,8 @@ def test_host_validation_rejects_before_launch(lib):
 
 def test_workspace_sizes(lib):
     assert lib.csa2_workspace_size(lib.CSA2_OP_TOPK, 8, 4096, 512) == 0          # one CTA per row
-    # per row: 2,048 maxima of 512-item supergroups, 4 counters, 8,192 candidate keys
-    assert lib.csa2_workspace_size(lib.CSA2_OP_TOPK, 8, 1 << 20, 512) == 8 * (2048 * 4 + 16 + 8192 * 8)
+    # per row: the 2,048 maxima of 512-item supergroups (candidates stay on chip)
+    assert lib.csa2_workspace_size(lib.CSA2_OP_TOPK, 8, 1 << 20, 512) == 8 * 2048 * 4
     assert lib.csa2_workspace_size(lib.CSA2_OP_SPARSE_ATTN, 8192, 640) == 0      # no split for big batches
     with pytest.raises(lib.CSA2Error):
         lib.csa2_workspace_size(lib.CSA2_OP_SPARSE_ATTN, 8, 100)

@@ -133,6 +133,22 @@ def test_topk_long_rows_odd_stride(lib, oracle_lib):
         assert np.array_equal(got[i], oracle_lib.topk(base[i, :m].astype(np.float64), 512))
 
 
+@pytest.mark.parametrize("n", [100_000, 1 << 20])
+def test_topk_long_rows_negative_and_zero_thresholds(lib, oracle_lib, n):
+    """Long rows whose threshold is a negative score or exactly zero (the
+    streaming pass then compares order keys, not raw bits), next to an
+    ordinary row; -0 and +0 tie and ties go to the smaller index."""
+    neg = G.uniform_f32_scores(97, 0, n, 0) * 0.5 - 1.5               # all in [-2, -1)
+    zero = np.zeros(n, np.float32)
+    zero[1::2] = -0.0
+    rng = np.random.default_rng(5)
+    zero[rng.choice(n, 300, replace=False)] = rng.random(300).astype(np.float32) + 0.5
+    rows = np.stack([neg, zero, G.uniform_f32_scores(98, 0, n, 0)])
+    got = _run_topk(lib, rows, [n, n, n], 512)
+    for i in range(3):
+        assert np.array_equal(got[i], oracle_lib.topk(rows[i].astype(np.float64), 512)), i
+
+
 def test_topk_all_equal_row_uses_exact_fallback(lib, oracle_lib):
     n = 200_000                                            # candidates overflow the filter buffer
     rows = np.zeros((2, n), np.float32)
