@@ -44,6 +44,7 @@ static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 // csa2_decode's workspace: scores [n_q][n_max] fp32, then the top-k scratch,
 // then the attention scratch, each 256-B aligned.
+// scores | top-k scratch | attention partials
 static size_t decode_workspace_bytes(int n_q, int64_t n_max) {
   return round256((size_t)n_q * (size_t)n_max * 4) + round256(topk_fused_bytes(n_q, n_max, kTopK)) +
          round256(attn_workspace_bytes(n_q, kTopK));
@@ -236,10 +237,11 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
   F.q_seq = q_seq;
   F.n_seq = n_seq;
   const bool fused = F.mode > 0;
-  cudaError_t e = launch_index_score_tc(
-      static_cast<const uint8_t *>(key_nib), static_cast<const uint8_t *>(key_scale), n_max, n_seq,
-      static_cast<const uint8_t *>(q_nib), static_cast<const uint8_t *>(q_scale), w, q_seq, n_vis, n_q, nullptr, scores,
-      n_max, st, s, fused ? F.W.smax : nullptr, fused ? F.W.sstride : 0, fused ? F.mode : 0);
+  cudaError_t e = launch_index_score_tc(static_cast<const uint8_t *>(key_nib), static_cast<const uint8_t *>(key_scale),
+                                        n_max, n_seq, static_cast<const uint8_t *>(q_nib),
+                                        static_cast<const uint8_t *>(q_scale), w, q_seq, n_vis, n_q, nullptr, scores,
+                                        n_max, st, s, fused ? F.W.smax : nullptr, fused ? F.W.sstride : 0,
+                                        fused ? F.mode : 0);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
   e = launch_topk_fused(scores, n_max, n_q, n_vis, n_max, kTopK, F, sel, ws_topk, st, s);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;

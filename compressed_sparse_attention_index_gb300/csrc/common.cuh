@@ -59,4 +59,7 @@ __device__ __forceinline__ uint32_t order_key(float s) {
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Iteration limit of a spin-wait on shared memory written by another warp.
+constexpr long long kSpinLimit = 1LL << 26;
+
 }  // namespace csa2

@@ -35,9 +35,10 @@
 //   warps 3..10 epilogue, two groups of four warps taking alternate units: one
 //               TMEM lane (= one entry of each sub-tile) per thread, 32 columns
 //               (= heads) per sub-tile, ReLU + weighted sum, coalesced store.
-// The tile schedule is advanced incrementally (no division per unit) and the
-// per-query sequence id / visible length are cached.  Every mbarrier wait is
-// bounded (CSA2_ERR_TIMEOUT instead of a hang).
+// The producer walks the CTA's units (a fixed stride over all of them) and
+// hands each to the other roles through a small shared-memory ring; the
+// per-query sequence id / visible length are cached.  Every wait is bounded (CSA2_ERR_TIMEOUT
+// instead of a hang).
 #include "common.cuh"
 #include "tc_ptx.cuh"
 #include "launch.cuh"
@@ -102,42 +103,43 @@ struct ScoreTcArgs {
   int smax_mode;
 };
 
-// Work schedule shared by every role: unit index T = blockIdx.x + k * gridDim.x
-// over (query, 256-entry unit), advanced without division; units past a query's
-// visible length are skipped.  seq / nv are re-read only when the query changes.
-struct Schedule {
-  int q, u, seq, nv;
-  bool started;
-  __device__ void init(const ScoreTcArgs &P) {
-    q = (int)(blockIdx.x / (unsigned)P.units_per_q);
-    u = (int)(blockIdx.x % (unsigned)P.units_per_q);
-    started = false;
-    load(P);
+// Work units are T = (query, unit) in query-major order, T < n_q * units_per_q;
+// a CTA takes T = blockIdx.x, blockIdx.x + gridDim.x, ...  The producer walks
+// that sequence, skips units past a query's visible length, and publishes the
+// unit of each of its iterations `it` in a ring of shared-memory words
+// (it << 32 | T; T = kDone after the last unit); every other role reads the
+// ring in iteration order instead of walking the sequence itself.  A slot is
+// rewritten 16 iterations later, which needs the MMA of iteration it + 10
+// done, so every role has read it by then.  (Units claimed from a global
+// counter, so that faster SMs take more, measured slower: the counter's
+// atomics queue up.)
+constexpr int kRing = 16;
+constexpr uint32_t kDone = 0xFFFFFFFFu;
+
+// Bounded wait for the ring entry of iteration it; false on timeout or abort.
+__device__ __forceinline__ bool ring_get(const volatile unsigned long long *ring, uint32_t it, uint32_t &T,
+                                         const volatile int &abort_flag) {
+  for (long long n = 0; n < kSpinLimit; n++) {
+    const unsigned long long e = ring[it % kRing];
+    if ((uint32_t)(e >> 32) == it) { T = (uint32_t)e; return true; }
+    if ((n & 63) == 63 && abort_flag) return false;
   }
-  __device__ void load(const ScoreTcArgs &P) {
-    if (q < P.n_q) {
-      seq = __ldg(P.q_seq + q);
-      nv = __ldg(P.n_vis + q);
-      if (seq < 0 || seq >= P.n_seq || nv < 0 || (int64_t)nv > P.n_max) {
-        if (u == 0 && threadIdx.x == 0) record_error(P.status, CSA2_ERR_BOUNDS);
-        nv = -1;                                      // marks a query to skip
-      }
-    }
-  }
-  // Advance to the next unit this CTA processes; false when done.
-  __device__ bool next(const ScoreTcArgs &P) {
-    for (;;) {
-      if (started) {
-        u += gridDim.x;
-        bool moved = false;
-        while (u >= P.units_per_q) { u -= P.units_per_q; q++; moved = true; }
-        if (moved) load(P);
-      }
-      started = true;
-      if (q >= P.n_q) return false;
-      if (nv < 0) continue;
-      if (P.pool == nullptr && u * kUnit >= nv) continue;
-      return true;
+  return false;
+}
+
+// Sequence id and visible length of a query, re-read when the query changes;
+// nv = -1 marks a query whose values are out of range (recorded once, by the
+// producer of its unit 0).
+struct QueryInfo {
+  int q = -1, seq = 0, nv = -1;
+  __device__ void set(const ScoreTcArgs &P, int nq, int u, bool record) {
+    if (nq == q) return;
+    q = nq;
+    seq = __ldg(P.q_seq + q);
+    nv = __ldg(P.n_vis + q);
+    if (seq < 0 || seq >= P.n_seq || nv < 0 || (int64_t)nv > P.n_max) {
+      if (record && u == 0) record_error(P.status, CSA2_ERR_BOUNDS);
+      nv = -1;
     }
   }
 };
@@ -179,6 +181,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   __shared__ __align__(8) uint64_t acc_empty[kScAcc];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
+  __shared__ volatile unsigned long long unit_ring[kRing];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // everything below reads inputs or allocates TMEM: after the grid ahead
@@ -191,6 +194,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       ptx::mbar_init(&done_bar[s], 1);
     }
     for (int a = 0; a < kScAcc; a++) ptx::mbar_init(&acc_empty[a], 4);
+    for (int i = 0; i < kRing; i++) unit_ring[i] = ~0ull;   // no iteration's tag
     abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -205,14 +209,28 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     abort_flag = 1;
   };
 
-  Schedule sc;
-  sc.init(P);
+  const uint32_t total_units = (uint32_t)P.n_q * (uint32_t)P.units_per_q;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = ptx::policy_evict_first();
     QuerySlots qs;
-    for (uint32_t it = 0; sc.next(P); it++) {
+    QueryInfo sc;
+    uint32_t T = blockIdx.x;
+    for (uint32_t it = 0;; it++) {
       if (abort_flag) break;
+      // this iteration's unit: the next one inside its query's visible length
+      int uq = 0;
+      for (;;) {
+        if (T >= total_units) { T = kDone; break; }
+        const int q = (int)(T / (uint32_t)P.units_per_q);
+        uq = (int)(T - (uint32_t)q * (uint32_t)P.units_per_q);
+        sc.set(P, q, uq, lane == 0);
+        if (sc.nv >= 0 && (P.pool != nullptr || uq * kUnit < sc.nv)) break;
+        T += gridDim.x;
+      }
+      if (lane == 0) unit_ring[it % kRing] = ((unsigned long long)it << 32) | T;
+      if (T == kDone) break;
+      const int cur_u = uq;
       const uint32_t s = it % kScStages, r = it / kScStages;
       const bool fresh = qs.step(sc.q, (int)it);
       if (!ptx::mbar_wait(&done_bar[s], (r & 1) ^ 1)) { fail(); break; }
@@ -240,17 +258,17 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       if (P.pool == nullptr) {
         if (lane == 0) {
           // sub-tiles that start before n_vis end within n_max (n_max % 128 == 0)
-          const int left = sc.nv - sc.u * kUnit;
+          const int left = sc.nv - cur_u * kUnit;
           const int nsub = left >= kUnit ? kSub : (left + 127) >> 7;
           ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)nsub * (8192 + 512) + qbytes);
           if (fresh) load_query();
-          const int64_t r0 = row0 + (int64_t)sc.u * kUnit;
+          const int64_t r0 = row0 + (int64_t)cur_u * kUnit;
           ptx::bulk_load_hint(st + kOffA, P.key_nib + r0 * 64, (uint32_t)nsub * 8192, &full_bar[s], policy);
           ptx::bulk_load(st + kOffSFA, P.key_scale + r0 * 4, (uint32_t)nsub * 512, &full_bar[s]);
         }
       } else {
         // kUnit / 8 gathered 8-entry blocks, two per lane
-        const int32_t *pl = P.pool + (int64_t)sc.q * kPoolBlocks + sc.u * (kUnit / kBlock);
+        const int32_t *pl = P.pool + (int64_t)sc.q * kPoolBlocks + cur_u * (kUnit / kBlock);
         const int blk0 = __ldg(pl + lane), blk1 = __ldg(pl + 32 + lane);
         const bool ok0 = blk0 >= 0 && (int64_t)blk0 * kBlock < P.n_max;
         const bool ok1 = blk1 >= 0 && (int64_t)blk1 * kBlock < P.n_max;
@@ -274,14 +292,18 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         }
       }
       __syncwarp();
+      T += gridDim.x;
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ scale-factor warp
     QuerySlots qs;
-    for (uint32_t it = 0; sc.next(P); it++) {
+    for (uint32_t it = 0;; it++) {
       if (abort_flag) break;
+      uint32_t T;
+      if (!ring_get(unit_ring, it, T, abort_flag)) { fail(); break; }
+      if (T == kDone) break;
       const uint32_t s = it % kScStages, r = it / kScStages;
-      const bool fresh = qs.step(sc.q, (int)it);
+      const bool fresh = qs.step((int)(T / (uint32_t)P.units_per_q), (int)it);
       if (!ptx::mbar_wait(&full_bar[s], r & 1)) { fail(); break; }
       unsigned char *st = smem + s * kScStageBytes;
       unsigned char *qd = qslots + qs.slot * kScQBytes;
@@ -328,9 +350,12 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       const uint32_t par = warp == 1 ? 0u : 1u;
       const uint32_t idesc0 = idesc_mxf4_m128n32(0), idesc1 = idesc_mxf4_m128n32(2);
       QuerySlots qs;
-      for (uint32_t it = 0; sc.next(P); it++) {
+      for (uint32_t it = 0;; it++) {
         if (abort_flag) break;
-        qs.step(sc.q, (int)it);
+        uint32_t T;
+        if (!ring_get(unit_ring, it, T, abort_flag)) { fail(); break; }
+        if (T == kDone) break;
+        qs.step((int)(T / (uint32_t)P.units_per_q), (int)it);
         if ((it & 1) != par) continue;
         const uint32_t s = it % kScStages, r = it / kScStages, a = it % kScAcc, ra = it / kScAcc;
         if (!ptx::mbar_wait(&sf_bar[s], r & 1) || !ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) { fail(); break; }
@@ -361,9 +386,15 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     const int row = quarter * 32 + lane;
     int cur_q = -1;
     float wv[kIdxHeads];
-    for (uint32_t it = 0; sc.next(P); it++) {
+    QueryInfo sc;
+    for (uint32_t it = 0;; it++) {
       if (abort_flag) break;
+      uint32_t T;
+      if (!ring_get(unit_ring, it, T, abort_flag)) { fail(); break; }   // every entry: the last may be either parity
+      if (T == kDone) break;
       if ((it & 1) != group) continue;
+      const int cur_u = (int)(T % (uint32_t)P.units_per_q);
+      sc.set(P, (int)(T / (uint32_t)P.units_per_q), cur_u, false);
       const uint32_t s = it % kScStages, r = it / kScStages;
       if (sc.q != cur_q) {
         const float4 *wp = reinterpret_cast<const float4 *>(P.w + (int64_t)sc.q * kIdxHeads);
@@ -391,7 +422,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
           out[i] = ok ? v : -INFINITY;
         }
       };
-      const int64_t i0 = (int64_t)sc.u * kUnit + row;
+      const int64_t i0 = (int64_t)cur_u * kUnit + row;
       uint32_t umax = 0u;                             // smax_mode 1: this lane's maximum key
 #pragma unroll 1
       for (int h2 = 0; h2 < kSub / 2; h2++) {         // two sub-tiles (64 columns) at a time
@@ -421,7 +452,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
             // 32 consecutive entries per warp and sub-tile
             const uint32_t g0 = __reduce_max_sync(0xFFFFFFFFu, k0), g1 = __reduce_max_sync(0xFFFFFFFFu, k1);
             if (lane == 0) {
-              const int64_t e0 = (int64_t)sc.u * kUnit + h2 * 256 + quarter * 32;
+              const int64_t e0 = (int64_t)cur_u * kUnit + h2 * 256 + quarter * 32;
               sm[e0 >> 5] = g0;
               sm[(e0 + 128) >> 5] = g1;
             }
@@ -432,7 +463,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       }
       if (P.smax_mode == 1) {
         umax = __reduce_max_sync(0xFFFFFFFFu, umax);
-        if (lane == 0) P.smax[(int64_t)sc.q * P.sstride + (int64_t)sc.u * 4 + quarter] = umax;
+        if (lane == 0) P.smax[(int64_t)sc.q * P.sstride + (int64_t)cur_u * 4 + quarter] = umax;
       }
     }
   }

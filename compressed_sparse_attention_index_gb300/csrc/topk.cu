@@ -265,29 +265,53 @@ __device__ int block_excl_scan(int c, int *total) {
   return __reduce_add_sync(0xFFFFFFFFu, lane < warp ? w : 0) + incl - c;
 }
 
-// Block-wide: the rem-th largest (with multiplicity) of the values v[i] with
-// sel(i), i < n (shared memory), found eight bits per step from bit 31 down to
-// bit `low` (a multiple of 8); the result has its bits below `low` cleared, so
-// at least rem selected values reach it.  Each step: a 256-bin histogram of
-// the next digit (shared-memory atomics; a warp whose values all share the
-// digit, as leading digits often do, adds them with one), then warp 0 locates the digit
-// by a suffix scan over the bins while the other threads clear the next step's
-// histogram (two alternate): two barriers per step.  hist: 512 counters.
-template <class Sel>
-__device__ uint32_t block_kth256(const uint32_t *v, int n, int rem, int low, Sel sel, uint32_t *hist) {
-  __shared__ uint32_t prefix_sh, pmask_sh;
+// Block-wide: a lower bound of the rem-th largest (with multiplicity) of the
+// values v[0..n) in shared memory, 0 meaning "no value" (1 <= rem <= the
+// number of nonzero values), exact in its bits from 31 down to `low`, with
+// the bits below `low` cleared, so at least rem values reach it.  The bits
+// every nonzero value shares (those above the highest bit where the maximum
+// and the smallest nonzero value differ) are taken from the maximum; the rest go
+// eight bits per step: a 256-bin histogram of the next digit among the values
+// that match the prefix so far (shared-memory atomics; a warp whose values all
+// share the digit adds them with one), then warp 0 finds the digit by a suffix
+// scan while the other threads clear the next step's histogram (two
+// alternate).  With max_steps set, the search stops after that many steps and
+// returns the prefix found (a coarser, still valid, lower bound).  hist: 512
+// counters.  Not inlined: every call site shares one copy of the code.
+__device__ __noinline__ uint32_t block_kth256(const uint32_t *v, int n, int rem, int low, uint32_t *hist,
+                                             int max_steps = 32) {
+  __shared__ uint32_t prefix_sh, ext_sh[2][32];
   __shared__ int rem_sh;
-  const int lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) { prefix_sh = 0u; pmask_sh = 0u; rem_sh = rem; }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  uint32_t mx = 0u, mn = ~0u;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint32_t x = v[i];
+    mx = max(mx, x);
+    if (x != 0u) mn = min(mn, x);
+  }
+  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+  mn = __reduce_min_sync(0xFFFFFFFFu, mn);
+  if (lane == 0) { ext_sh[0][warp] = mx; ext_sh[1][warp] = mn; }
   for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
+  if (threadIdx.x == 0) rem_sh = rem;
   __syncthreads();
-  for (int shift = 24, buf = 0; shift >= low; shift -= 8, buf ^= 1) {
+  mx = __reduce_max_sync(0xFFFFFFFFu, lane < nw ? ext_sh[0][lane] : 0u);
+  mn = __reduce_min_sync(0xFFFFFFFFu, lane < nw ? ext_sh[1][lane] : ~0u);
+  const uint32_t lowmask = low >= 32 ? ~0u : (1u << low) - 1u;
+  const int hb = (mx ^ mn) == 0u ? -1 : 31 - __clz(mx ^ mn);   // highest differing bit
+  uint32_t pmask = hb >= 31 ? 0u : ~((2u << hb) - 1u);
+  uint32_t prefix = mx & pmask;
+  if (hb < low) {                                              // the bits from `low` up are common
+    __syncthreads();                                           // ext_sh is read; the next call may rewrite it
+    return mx & ~lowmask;
+  }
+  int shift = max(hb - 7, low);
+  for (int step = 0, buf = 0;; step++, buf ^= 1) {
     uint32_t *h = hist + buf * 256;
-    const uint32_t prefix = prefix_sh, pmask = pmask_sh;
     for (int b0 = 0; b0 < n; b0 += blockDim.x) {      // uniform trip count: whole warps
       const int i = b0 + threadIdx.x;
       const uint32_t x = i < n ? v[i] : 0u;
-      const bool ok = i < n && (x & pmask) == prefix && sel(i);
+      const bool ok = i < n && (x & pmask) == prefix;
       const unsigned act = __ballot_sync(0xFFFFFFFFu, ok);
       if (ok) {
         const uint32_t d = (x >> shift) & 255u;
@@ -319,7 +343,6 @@ __device__ uint32_t block_kth256(const uint32_t *v, int n, int rem, int low, Sel
         for (int j = 7; j >= 0; j--) {
           if (above + c[j] >= (uint32_t)r) {
             prefix_sh = prefix | ((uint32_t)(8 * lane + j) << shift);
-            pmask_sh = pmask | (255u << shift);
             rem_sh = r - (int)above;
             break;
           }
@@ -330,8 +353,13 @@ __device__ uint32_t block_kth256(const uint32_t *v, int n, int rem, int low, Sel
       for (int i = threadIdx.x - 32; i < 256; i += blockDim.x - 32) hist[(buf ^ 1) * 256 + i] = 0u;
     }
     __syncthreads();
+    prefix = prefix_sh;
+    pmask |= 255u << shift;
+    if (shift == low || step + 1 == max_steps) break;
+    shift = max(shift - 8, low);
   }
-  return prefix_sh;
+  __syncthreads();                                   // prefix_sh is read; the next call may rewrite it
+  return prefix & ~((1u << shift) - 1u);
 }
 
 // Block-wide min / max of one value per thread; every thread gets the result.
@@ -362,8 +390,8 @@ struct BlockReduce {
 // of kKvBytes per index, which are prefetched into L2 once the set is known.
 // by_index: keys[] is already in ascending index order; the selected keys are
 // then written out by one order-keeping compaction.
-__device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t *out, int32_t *sel, uint32_t *bins,
-                             const uint8_t *pf = nullptr, bool by_index = false) {
+__device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t *out, int32_t *sel,
+                                          uint32_t *bins, const uint8_t *pf = nullptr, bool by_index = false) {
   __shared__ int cnt_sh[2];
   __shared__ int n_sel;
   __shared__ uint32_t red_slots[2][32];
@@ -373,7 +401,7 @@ __device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t
   if (threadIdx.x == 0) { n_sel = 0; cnt_sh[0] = 0; cnt_sh[1] = 0; }
   uint64_t K = 1;                                    // keys >= K are selected
   if (take < n) {
-    const uint32_t t32 = block_kth256(sk, n, take, 0, [](int) { return true; }, bins);
+    const uint32_t t32 = block_kth256(sk, n, take, 0, bins);
     int c_gt = 0, c_eq = 0;
     for (int i = threadIdx.x; i < n; i += blockDim.x) { c_gt += sk[i] > t32; c_eq += sk[i] == t32; }
     c_gt = warp_sum(c_gt);
@@ -386,7 +414,7 @@ __device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t
       // several keys tie on the score: the `need` largest index halves among them
       for (int i = threadIdx.x; i < n; i += blockDim.x) sk[i] = sk[i] == t32 ? (uint32_t)keys[i] : 0u;
       __syncthreads();
-      tlo = block_kth256(sk, n, need, 0, [](int) { return true; }, bins);
+      tlo = block_kth256(sk, n, need, 0, bins);
     }
     K = ((uint64_t)t32 << 32) | tlo;
   }
@@ -522,7 +550,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
     if (threadIdx.x == 0) { T_sh = 1u; n_c = 0; }
     __syncthreads();
     if (ng > k) {
-      const uint32_t t = block_kth256(sk, ng, k, 16, [](int) { return true; }, reinterpret_cast<uint32_t *>(sel));
+      const uint32_t t = block_kth256(sk, ng, k, 16, reinterpret_cast<uint32_t *>(sel));
       if (threadIdx.x == 0) T_sh = t;
     }
     __syncthreads();
@@ -751,9 +779,10 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
     if (lane == 0 && vs) atomicAdd(&n_vs, vs);
   }
   __syncthreads();
-  // ---- T: the largest multiple of 2^16 that at least k supergroup maxima reach
+  // ---- T: a lower bound of the k-th largest supergroup maximum, exact in
+  // the 16 bits below the leading bits all maxima share
   if (n_vs > k) {
-    const uint32_t t = block_kth256(sv, ns, k, 16, [](int) { return true; }, sh.whist);
+    const uint32_t t = block_kth256(sv, ns, k, 16, sh.whist, 2);
     if (threadIdx.x == 0) T_sh = t;
   }
   __syncthreads();
