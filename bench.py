@@ -41,7 +41,7 @@ IDX_BYTES = 68
 # dram__bytes_read.sum + dram__bytes_write.sum of one index_score_tc_kernel launch, from an ncu
 # capture of this kernel version on the named workload (profiles/index_score_tc_32x64K.md gives
 # the command); workloads without a capture report null.
-INDEX_SCORE_TRAFFIC = {"long_full_decode_N1M_B8_zipf": 570552064 + 3530496}
+INDEX_SCORE_TRAFFIC = {"long_full_decode_N1M_B8_zipf": 570487040 + 5117184}
 
 
 def parse():
