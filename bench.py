@@ -14,6 +14,13 @@ sides, max over ranks.  Each step streams 573 MB of cache (far more than the
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--config 4] [--no-cpu-baseline]
 
+--config 0/1/4 time other Full-layer decode batches the same way.  --config 3
+(Reindex decode: 64 x 1,048,576 entries, pool of 2,048 blocks given) and
+--config 2 (m=2 chunked prefill: 8,192 causal queries over 4,096 pooled
+entries) time those steps and report the roofline of their dominant kernel
+(the pool-mode indexer against HBM; the attention against the bf16 tensor
+peak); they are measurements of those steps, not the headline line.
+
 --impl reference times the CPU oracle (plain C, fp64) on the host cores on a
 bounded sample of the same workload; under torchrun only rank 0 runs it.
 Multi-GPU (torchrun): every rank decodes its own batch on its own GPU (the
@@ -159,7 +166,8 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     wl = CONFIGS[args.config]
-    assert not wl.pool and not wl.prefill, "the benchmark times the Full-layer decode configs (0, 1, 4)"
+    if wl.pool or wl.prefill:
+        return run_rows(args, rank, world, local_rank, wl)
     dw = build_device_workload(wl)
     n_q, n_max = dw.q.shape[0], dw.n_max
     buf = decode.DecodeBuffers(n_q, n_max, out_dtype=C.CSA2_OUT_BF16)
@@ -305,6 +313,151 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     return line
+
+
+def run_rows(args, rank, world, local_rank, wl):
+    """Reindex decode (pool given) or m=2 prefill: event-timed steps, the
+    dominant kernel's roofline, and the step through pinned host inputs."""
+    import torch
+    import torch.distributed as dist
+    import compressed_sparse_attention_index_gb300 as C
+    from compressed_sparse_attention_index_gb300 import decode
+    from gen.device import build_device_workload
+
+    dw = build_device_workload(wl)
+    n_q, n_max = dw.q.shape[0], dw.n_max
+    buf = decode.DecodeBuffers(n_q, n_max, pool=wl.pool, out_dtype=C.CSA2_OUT_BF16)
+    stream = torch.cuda.current_stream()
+    if wl.pool:
+        decode.reindex_decode(dw, buf, None, stream, build_pool=True)     # the pool the step is given
+
+        def step():
+            decode.reindex_decode(dw, buf, None, stream, build_pool=False)
+    else:
+        def step():
+            decode.fused_decode(dw, buf, None, stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert C.csa2_get_device_status() == 0
+    clocks = ClockSampler(local_rank)
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    assert C.csa2_get_device_status() == 0
+
+    # the dominant kernel, alone in K further launches, bracketed by its own events
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        if wl.pool:
+            C.csa2_index_score(dw.key_nib, dw.key_scale, n_max, dw.kv.shape[0], dw.q_nib_re, dw.q_scale_re,
+                               dw.w_re, dw.q_seq, dw.n_vis, n_q, buf.blocks, buf.pool_scores, 16384, None, stream)
+        else:
+            decode.attend(dw, buf, None, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    k_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    assert C.csa2_get_device_status() == 0
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # the step through pinned host inputs: the attention query and the indexer
+    # inputs of the step in, the output back
+    import numpy as np
+    from gen import inputs as G
+    q_h = dw.q.cpu().pin_memory()
+    w_dev = dw.w_re if wl.pool else dw.w
+    w_h = w_dev.cpu().pin_memory()
+    s_qidx = G.S_QIDX_RE if wl.pool else G.S_QIDX
+    qidx_bits = np.concatenate([G.normal_block_bf16(wl.seed, s_qidx, qi, 0, 32, 128) for qi in range(n_q)])
+    qidx_h = torch.from_numpy(qidx_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    qidx_d = torch.empty(qidx_h.shape, dtype=torch.bfloat16, device="cuda")
+    out_h = torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory()
+    nib, scl = (dw.q_nib_re, dw.q_scale_re) if wl.pool else (dw.q_nib, dw.q_scale)
+
+    def e2e_step():
+        dw.q.copy_(q_h, non_blocking=True)
+        w_dev.copy_(w_h, non_blocking=True)
+        qidx_d.copy_(qidx_h, non_blocking=True)
+        C.csa2_fp4_pack(C.CSA2_IDX_MXFP4, qidx_d, n_q * 32, 1, None, nib, scl)
+        step()
+        out_h.copy_(buf.out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    h2d = q_h.numel() * 2 + w_h.numel() * 4 + qidx_h.numel() * 2
+    d2h = out_h.numel() * out_h.element_size()
+    if rank != 0:
+        return None
+
+    peaks_all = {}
+    pf = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pf):
+        with open(pf) as f:
+            peaks_all = json.load(f)
+    units = n_q * args.steps * world
+    n_vis = dw.n_vis.cpu().numpy().astype(np.int64)
+    swa_cnt = dw.swa_cnt.cpu().numpy().astype(np.int64)
+    if wl.pool:
+        # pool keys + block ids + the fixed per-query bytes
+        step_bytes = n_q * (16384 * IDX_BYTES + 2048 * 4 + FIXED_BYTES_PER_QUERY)
+        k_bytes = n_q * 16384 * IDX_BYTES
+        hbm, hbm_kind = peaks()
+        roof = {"kernel": "index_score (pool mode)", "bound": "hbm", "achieved": k_bytes / (k_ms / 1e3) / 1e9,
+                "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s",
+                "frac": k_bytes / (k_ms / 1e3) / 1e9 / hbm, "traffic": None,
+                "algorithmic_bytes_per_launch": k_bytes, "avg_launch_ms": k_ms}
+        dtype = "e2m1xe2m1->f32 (score), bf16xbf16->f32 (attention)"
+    else:
+        # (query, entry) pairs of the attention, 4 FLOP per pair, head and dim (QK and PV)
+        pairs = int(np.minimum(512, n_vis).sum() + swa_cnt.sum())
+        flop = pairs * 64 * 512 * 4
+        bf16 = float(peaks_all.get("bf16_tflops", 1900.0))
+        achieved = flop / (k_ms / 1e3) / 1e12
+        step_bytes = n_q * (65536 * 2 + 2176 + 128) + wl.n_entries * (288 + IDX_BYTES) + wl.swa_cap * 528
+        roof = {"kernel": "sparse_attn", "bound": "tensor", "achieved": achieved, "peak": bf16,
+                "peak_kind": "measured" if "bf16_tflops" in peaks_all else "fallback", "unit": "TFLOP/s",
+                "frac": achieved / bf16, "traffic": None, "algorithmic_flop_per_launch": flop,
+                "avg_launch_ms": k_ms}
+        dtype = "e2m1xe2m1->f32 (score), bf16xbf16->f32 (attention)"
+    launches = (1 + 1 + 2) if wl.pool else (1 + 1 + 1)
+    return {
+        "metric": ("Reindex decode" if wl.pool else "m=2 prefill") + " query-tokens/s for CSA2 (score+top512+attn)",
+        "value": units / (ms / 1e3), "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": dtype, "data": "synthetic (seeded counter-based generator; no trained weights)",
+        "config": {"workload": wl.name, "n_seq": wl.n_seq, "n_entries": wl.n_entries, "queries_per_step": n_q,
+                   "m": wl.m, "pool_given": bool(wl.pool), "topk": 512, "swa": 128, "heads": 64, "latent": 512,
+                   "parallelism": f"replicas x{world} (independent batches)"},
+        "path_hbm_gbs": step_bytes / (ms / args.steps / 1e3) / 1e9,
+        "roofline": roof, "clocks": clk,
+        "e2e": {"value": units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches * args.steps,
+        "impl": "ours",
+    }
 
 
 def run_reference(args):

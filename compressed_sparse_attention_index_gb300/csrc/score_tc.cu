@@ -16,10 +16,11 @@
 // sub-tiles, 34 KB) through a 6-stage shared-memory ring.  Every tcgen05
 // instruction and every barrier wait costs its issuing thread tens of cycles,
 // so the design keeps those per byte low: big units, one commit per unit, and
-// two MMA issuers.  Warp roles (384 threads):
+// two MMA issuers.  Warp roles (480 threads):
 //   warp 0      producer: one bulk copy (cp.async.bulk) of the unit's 32 KB of
-//               nibbles and one of its 2 KB of E8M0 scales (pool mode: 64
-//               gathered 8-entry blocks of 512 B + 32 B); with the first unit
+//               nibbles and one of its 2 KB of E8M0 scales (pool mode: 16 of
+//               the 64 gathered 8-entry blocks of 512 B + 32 B, by 16-B
+//               asynchronous copies; warps 12..14 gather the other 48); with the first unit
 //               of each run of one query, its 2 KB of nibbles and 128 B of
 //               scales into the next of six query slots (so a CTA may switch
 //               query on every unit without a stall).  The nibble planes are stored
@@ -56,7 +57,9 @@ constexpr int kScQBytes = 2560;           // per slot: 32 heads x 64 B nibbles +
 constexpr int kQOffB = 0, kQOffSFB = 2048;
 constexpr int kScSmem = kScStages * kScStageBytes + kQSlots * kScQBytes;
 static_assert(kScStageBytes % 1024 == 0, "64B-swizzled tiles need 512-B aligned stages and slots");
-constexpr int kScThreads = 384;
+constexpr int kScGather0 = 12;            // warps 12..14: extra gathering warps (pool mode)
+constexpr int kPoolGatherWarps = 4;       // warp 0 and warps 12..14, 16 of a unit's 64 blocks each
+constexpr int kScThreads = 480;
 constexpr int kScMmaWarp2 = 11;          // second MMA issuer (odd units)
 constexpr int kScAcc = 2;                 // TMEM accumulators (kSub x 32 columns each), one per epilogue group
 constexpr uint32_t kScTmemCols = 512;
@@ -132,11 +135,18 @@ __device__ __forceinline__ bool ring_get(const volatile unsigned long long *ring
 // producer of its unit 0).
 struct QueryInfo {
   int q = -1, seq = 0, nv = -1;
+  int pre_q = -1, pre_seq = 0, pre_nv = 0;   // values loaded ahead (prefetch)
+  __device__ void prefetch(const ScoreTcArgs &P, int nq) {
+    if (nq == q || nq == pre_q) return;
+    pre_q = nq;
+    pre_seq = __ldg(P.q_seq + nq);
+    pre_nv = __ldg(P.n_vis + nq);
+  }
   __device__ void set(const ScoreTcArgs &P, int nq, int u, bool record) {
     if (nq == q) return;
     q = nq;
-    seq = __ldg(P.q_seq + q);
-    nv = __ldg(P.n_vis + q);
+    seq = nq == pre_q ? pre_seq : __ldg(P.q_seq + q);
+    nv = nq == pre_q ? pre_nv : __ldg(P.n_vis + q);
     if (seq < 0 || seq >= P.n_seq || nv < 0 || (int64_t)nv > P.n_max) {
       if (record && u == 0) record_error(P.status, CSA2_ERR_BOUNDS);
       nv = -1;
@@ -170,6 +180,49 @@ struct QuerySlots {
   __device__ int prev_user() const { return start[0] - 1; }
 };
 
+// Pool mode: a unit is 64 gathered 8-entry blocks (512 B of nibbles + 32 B of
+// scales each).  Small bulk copies cost the copy engine more than their bytes,
+// and one warp's plain asynchronous copies are limited by how many it may have
+// in flight, so four warps each move 16 blocks in 16-B pieces: one block's
+// nibbles per instruction (16 B per lane), then the 16 blocks' scales in one.
+// Each lane arrives on the stage's barrier when its copies have landed (the
+// barrier expects 1 + 32 x 4 arrivals: the producer's lane 0, with the query
+// data's bytes, and every gathering lane).  Each warp loads the block ids of
+// its next unit (T + gridDim.x, the usual next one) while this one's copies go
+// out.
+struct PoolGather {
+  uint32_t pre_T = kDone;
+  int pre_b = -1;
+  __device__ void prefetch(const ScoreTcArgs &P, int g, uint32_t Tn, QueryInfo &qi, uint32_t total_units) {
+    if (Tn >= total_units) return;
+    const int lane = threadIdx.x & 31;
+    const int qn = (int)(Tn / (uint32_t)P.units_per_q), un = (int)(Tn - (uint32_t)qn * (uint32_t)P.units_per_q);
+    pre_b = __ldg(P.pool + (int64_t)qn * kPoolBlocks + un * (kUnit / kBlock) + g * 16 + (lane & 15));
+    pre_T = Tn;
+    qi.prefetch(P, qn);
+  }
+  __device__ void gather(const ScoreTcArgs &P, int g, uint32_t T, int q, int u, int64_t row0, unsigned char *st,
+                         uint64_t *full) {
+    const int lane = threadIdx.x & 31;
+    const int b = pre_T == T ? pre_b
+                             : __ldg(P.pool + (int64_t)q * kPoolBlocks + u * (kUnit / kBlock) + g * 16 + (lane & 15));
+    const bool ok = b >= 0 && (int64_t)b * kBlock < P.n_max;
+    if (lane < 16 && b >= 0 && !ok) record_error(P.status, CSA2_ERR_BOUNDS);
+#pragma unroll 4
+    for (int j = 0; j < 16; j++) {
+      const int bj = __shfl_sync(0xFFFFFFFFu, b, j);
+      if (bj >= 0 && (int64_t)bj * kBlock < P.n_max)
+        ptx::cp_async16(st + kOffA + (g * 16 + j) * 512 + lane * 16,
+                        P.key_nib + (row0 + (int64_t)bj * kBlock) * 64 + lane * 16);
+    }
+    const int bs = __shfl_sync(0xFFFFFFFFu, b, lane >> 1);
+    if (bs >= 0 && (int64_t)bs * kBlock < P.n_max)
+      ptx::cp_async16(st + kOffSFA + (g * 16 + (lane >> 1)) * 32 + (lane & 1) * 16,
+                      P.key_scale + (row0 + (int64_t)bs * kBlock) * 4 + (lane & 1) * 16);
+    ptx::cp_async_arrive_noinc(full);
+  }
+};
+
 __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcArgs P) {
   extern __shared__ __align__(1024) unsigned char sc_smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -189,7 +242,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   griddep_launch();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kScStages; s++) {
-      ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&full_bar[s], P.pool != nullptr ? 1 + 32 * kPoolGatherWarps : 1);   // pool: see PoolGather
       ptx::mbar_init(&sf_bar[s], 1);
       ptx::mbar_init(&done_bar[s], 1);
     }
@@ -216,6 +269,8 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     QuerySlots qs;
     QueryInfo sc;
     uint32_t T = blockIdx.x;
+    PoolGather pg;
+    if (P.pool != nullptr) pg.prefetch(P, 0, T, sc, total_units);
     for (uint32_t it = 0;; it++) {
       if (abort_flag) break;
       // this iteration's unit: the next one inside its query's visible length
@@ -267,29 +322,14 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
           ptx::bulk_load(st + kOffSFA, P.key_scale + r0 * 4, (uint32_t)nsub * 512, &full_bar[s]);
         }
       } else {
-        // kUnit / 8 gathered 8-entry blocks, two per lane
-        const int32_t *pl = P.pool + (int64_t)sc.q * kPoolBlocks + cur_u * (kUnit / kBlock);
-        const int blk0 = __ldg(pl + lane), blk1 = __ldg(pl + 32 + lane);
-        const bool ok0 = blk0 >= 0 && (int64_t)blk0 * kBlock < P.n_max;
-        const bool ok1 = blk1 >= 0 && (int64_t)blk1 * kBlock < P.n_max;
-        if ((blk0 >= 0 && !ok0) || (blk1 >= 0 && !ok1)) record_error(P.status, CSA2_ERR_BOUNDS);
-        const int n_ok = __popc(__ballot_sync(0xFFFFFFFFu, ok0)) + __popc(__ballot_sync(0xFFFFFFFFu, ok1));
-        // an all-empty unit still arrives once, so its phase completes
+        // pool: this warp gathers blocks 0..15 of the unit, warps 12..14 the
+        // rest (see PoolGather); lane 0 also brings the query data, if any
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)n_ok * (512 + 32) + qbytes);
+          ptx::mbar_arrive_expect_tx(&full_bar[s], qbytes);
           if (fresh) load_query();
         }
-        __syncwarp();
-        if (ok0) {
-          const int64_t r0 = row0 + (int64_t)blk0 * kBlock;
-          ptx::bulk_load_hint(st + kOffA + lane * 512, P.key_nib + r0 * 64, 512, &full_bar[s], policy);
-          ptx::bulk_load(st + kOffSFA + lane * 32, P.key_scale + r0 * 4, 32, &full_bar[s]);
-        }
-        if (ok1) {
-          const int64_t r0 = row0 + (int64_t)blk1 * kBlock;
-          ptx::bulk_load_hint(st + kOffA + (32 + lane) * 512, P.key_nib + r0 * 64, 512, &full_bar[s], policy);
-          ptx::bulk_load(st + kOffSFA + (32 + lane) * 32, P.key_scale + r0 * 4, 32, &full_bar[s]);
-        }
+        pg.gather(P, 0, T, sc.q, cur_u, row0, st, &full_bar[s]);
+        pg.prefetch(P, 0, T + gridDim.x, sc, total_units);
       }
       __syncwarp();
       T += gridDim.x;
@@ -359,6 +399,9 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         if ((it & 1) != par) continue;
         const uint32_t s = it % kScStages, r = it / kScStages, a = it % kScAcc, ra = it / kScAcc;
         if (!ptx::mbar_wait(&sf_bar[s], r & 1) || !ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) { fail(); break; }
+        // pool mode: the stage was filled by ordinary asynchronous copies, which
+        // the MMA (async proxy) reads only after a proxy fence
+        if (P.pool != nullptr) ptx::fence_proxy_async_smem();
         ptx::tc_fence_after();
         const uint32_t sa = ptx::smem_u32(smem + s * kScStageBytes + kOffA);
         const uint64_t bd = ptx::smem_desc(ptx::smem_u32(qslots + qs.slot * kScQBytes + kQOffB), 16, 512, 4);
@@ -375,6 +418,26 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       }
     }
     __syncwarp();
+  } else if (warp >= kScGather0) {
+    // ------------------------------------------------------------ gathering warps (pool mode only)
+    if (P.pool != nullptr) {
+      const int g = warp - kScGather0 + 1;
+      QueryInfo gq;
+      PoolGather pg;
+      pg.prefetch(P, g, blockIdx.x, gq, total_units);
+      for (uint32_t it = 0;; it++) {
+        if (abort_flag) break;
+        uint32_t T;
+        if (!ring_get(unit_ring, it, T, abort_flag)) { fail(); break; }
+        if (T == kDone) break;
+        const uint32_t s = it % kScStages, r = it / kScStages;
+        const int q = (int)(T / (uint32_t)P.units_per_q), u = (int)(T % (uint32_t)P.units_per_q);
+        gq.set(P, q, u, false);                       // published units are valid
+        if (!ptx::mbar_wait(&done_bar[s], (r & 1) ^ 1)) { fail(); break; }
+        pg.gather(P, g, T, q, u, (int64_t)gq.seq * P.n_max, smem + s * kScStageBytes, &full_bar[s]);
+        pg.prefetch(P, g, T + gridDim.x, gq, total_units);
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     // group g (warps 3+4g .. 6+4g) takes the units with it % 2 == g and owns
