@@ -41,6 +41,32 @@ def test_index_score_full_parity(lib, oracle_lib, zipf):
         check_scores(s[qi, :1000], oracle_lib.full_scores(wl, qi))
 
 
+def test_index_score_pool_mode_gather(lib, oracle_lib):
+    """Pool mode: each 512-entry unit is 64 gathered 8-entry blocks, moved by
+    four warps of 16 blocks each.  Empty slots (-1) fall in every warp's share,
+    the last block of the cache is ragged (entries past n_vis score -inf), and
+    a block beyond the cache is skipped and reported."""
+    wl = small(n_seq=2, n_entries=40_003, seed=240)
+    dw = _dw(wl)
+    n_blocks = (40_003 + 7) // 8
+    rng = np.random.default_rng(11)
+    pool = np.stack([np.sort(rng.choice(n_blocks, 2048, replace=False)) for _ in range(2)]).astype(np.int32)
+    pool[0, -1] = n_blocks - 1                          # the ragged last block
+    pool[1, 3::7] = -1                                  # holes in every 16-block share
+    pool[1, 2047] = n_blocks + 100                      # beyond the cache: skipped, reported
+    scores = torch.empty((2, 16384), dtype=torch.float32, device="cuda")
+    lib.csa2_index_score(dw.key_nib, dw.key_scale, dw.n_max, 2, dw.q_nib, dw.q_scale, dw.w, dw.q_seq, dw.n_vis, 2,
+                         torch.from_numpy(pool).cuda(), scores, 16384)
+    assert lib.csa2_get_device_status() == 4            # CSA2_ERR_BOUNDS, then cleared
+    got = scores.cpu().numpy()
+    for qi in range(2):
+        ref = oracle_lib.full_scores(wl, qi)
+        pos = (pool[qi].astype(np.int64)[:, None] * 8 + np.arange(8)).reshape(-1)
+        ok = (np.repeat(pool[qi], 8) >= 0) & (pos < 40_003)
+        assert np.all(np.isneginf(got[qi][~ok])), qi
+        check_scores(got[qi][ok], ref[pos[ok]])
+
+
 @pytest.mark.parametrize("out_f32", [True, False])
 def test_sparse_attn_parity_on_oracle_selection(lib, oracle_lib, out_f32):
     from compressed_sparse_attention_index_gb300 import decode, CSA2_OUT_F32, CSA2_OUT_BF16
