@@ -250,7 +250,8 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
   // the attention inputs were final before the indexer started (it waits for
   // every earlier grid), so the attention may stage them during the top-k
   return from_cuda(launch_attn_tc(q, kv_cache, n_max, n_seq, sel, kTopK, swa_cache, swa_cap, q_seq, pos, swa_first,
-                                  swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, ws_attn, st, s, true));
+                                  swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, ws_attn, st, s, true,
+                                  topk_fused_ctas(F, n_q, n_max)));
 }
 
 csa2_status csa2_get_device_status(csa2_stream_t stream, csa2_status *out) {

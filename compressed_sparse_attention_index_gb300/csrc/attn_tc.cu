@@ -48,7 +48,8 @@ constexpr int kSmQ = kSmK + 128 * 1024;         // 64 heads  x 512 dims bf16    
 constexpr int kSmPhi = kSmQ + 64 * 1024;        // 64 heads  x 128 entries bf16 (16 KB)
 constexpr int kSmPlo = kSmPhi + 16 * 1024;      //                              (16 KB)
 constexpr int kSmOnes = kSmPlo + 16 * 1024;     // one 8 x 16-B core matrix of bf16 ones (128 B)
-constexpr int kSmMref = kSmOnes + 128;          // float[64] running maxima
+constexpr int kSmOnes16 = kSmOnes + 128;        // the same of f16 ones (128 B)
+constexpr int kSmMref = kSmOnes16 + 128;        // float[64] running maxima
 constexpr int kSmAlpha = kSmMref + 256;         // float[64] rescale factors
 constexpr int kSmValid = kSmAlpha + 256;        // uint8[128] slot validity
 constexpr int kSmBars = kSmValid + 128;         // 2 mbarriers, tmem base, flags
@@ -90,14 +91,35 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
 // byte offset of 16-B chunk `ch` (0..7) in row r of a 128B-swizzled 1024-B atom
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t ch) { return r * 128u + ((ch ^ (r & 7u)) << 4); }
 
-// kind::f16 instruction descriptor: bf16 x bf16 -> f32, M=128, N=64, A K- or MN-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_m128n64(uint32_t a_mn_major) {
-  return (1u << 4)               // D format f32
-         | (1u << 7)             // A bf16
-         | (1u << 10)            // B bf16
-         | (a_mn_major << 15)    // A major-ness
-         | ((64u >> 3) << 17)    // N / 8
-         | ((128u >> 4) << 24);  // M / 16
+// kind::f16 instruction descriptor: bf16 x bf16 (or f16 x f16) -> f32, M=128,
+// N=64, A K- or MN-major.
+__host__ __device__ constexpr uint32_t idesc_m128n64(uint32_t a_mn_major, bool f16) {
+  return (1u << 4)                     // D format f32
+         | ((f16 ? 0u : 1u) << 7)      // A: f16 0, bf16 1
+         | ((f16 ? 0u : 1u) << 10)     // B: f16 0, bf16 1
+         | (a_mn_major << 15)          // A major-ness
+         | ((64u >> 3) << 17)          // N / 8
+         | ((128u >> 4) << 24);        // M / 16
+}
+
+// Eight E2M1 codes (channel i in nibble i of w) -> eight f16 values as four
+// f16x2 words, by the hardware converter (exact: E2M1 is a subset of f16).
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t (&out)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+      : "r"(w));
+}
+
+// Two E4M3 codes (low byte first) -> f16x2 bits (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)two));
+  return h;
 }
 
 struct AttnTcArgs {
@@ -119,6 +141,7 @@ struct AttnTcArgs {
   float *part_ml;   // [n_q][nsplit][2][64]
   int *status;
   int settled;      // q, the window cache and the per-query arrays may be read before the grid ahead completes
+  int warm;         // settled, one chunk per CTA, all CTAs resident beside the grid ahead: warm-up pass
 };
 
 // cos and sin of theta = pos * inv_freq (inv_freq = rope_base^(-2i/64), computed
@@ -193,12 +216,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     for (int o = half * 128; rec != nullptr && o < bytes; o += 256)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + o));
   }
-  // stage Q (K-major, 128B swizzle: [head/8][dim/64][head%8][128 B])
-  {
+  // Stage Q (K-major, 128B swizzle: [head/8][dim/64][head%8][128 B]) in the
+  // operand type of the chunk ahead: bf16, or f16 for a chunk of FP4 latents
+  // only (their dequantised values are exact in f16 and the hardware converts
+  // E2M1 straight to f16).  In f16, Q is scaled by 2^-qs, qs >= 0 the smallest
+  // shift that brings max |q| below 2^15: a power of two, so exact (but for
+  // underflow below 2^-24), folded back into the softmax scale.  Returns 2^qs.
+  __shared__ uint32_t qmax_sh[kTcThreads / 32];
+  auto stage_q = [&](bool f16) -> float {
     const uint4 *src = reinterpret_cast<const uint4 *>(A.q + (int64_t)qi * kHeads * kDim);
     uint4 qv[kHeads * kDim / 8 / kTcThreads];        // all 16 loads in flight before any store
 #pragma unroll
     for (int j = 0; j < kHeads * kDim / 8 / kTcThreads; j++) qv[j] = __ldg(src + t + j * kTcThreads);
+    float qscale = 1.f;
+    if (f16) {
+      uint32_t m = 0u;                               // max |q| as bf16 bits, two lanes per word
+#pragma unroll
+      for (int j = 0; j < kHeads * kDim / 8 / kTcThreads; j++) {
+        m = __vmaxu2(m, qv[j].x & 0x7FFF7FFFu);
+        m = __vmaxu2(m, qv[j].y & 0x7FFF7FFFu);
+        m = __vmaxu2(m, qv[j].z & 0x7FFF7FFFu);
+        m = __vmaxu2(m, qv[j].w & 0x7FFF7FFFu);
+      }
+      m = __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
+      if (lane == 0) qmax_sh[warp] = m;
+      __syncthreads();
+      uint32_t mm = 0u;
+#pragma unroll
+      for (int w = 0; w < kTcThreads / 32; w++) mm = max(mm, qmax_sh[w]);
+      const int ex = (int)((mm >> 7) & 0xFFu) - 127;  // max |q| < 2^(ex + 1)
+      const int qs = max(0, ex - 14);
+      qscale = ldexpf(1.f, qs);
+      const float inv = ldexpf(1.f, -qs);
+#pragma unroll
+      for (int j = 0; j < kHeads * kDim / 8 / kTcThreads; j++) {
+        uint32_t wd[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          const __half2 h2 = __floats2half2_rn(bf16_lo(wd[k]) * inv, bf16_hi(wd[k]) * inv);
+          wd[k] = *reinterpret_cast<const uint32_t *>(&h2);
+        }
+        qv[j] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      }
+    }
 #pragma unroll
     for (int j = 0; j < kHeads * kDim / 8 / kTcThreads; j++) {
       const int i = t + j * kTcThreads;
@@ -206,11 +266,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       const uint32_t off = (h >> 3) * 8192 + (ch >> 3) * 1024 + sw128(h & 7, ch & 7);
       *reinterpret_cast<uint4 *>(sm + kSmQ + off) = qv[j];
     }
-    // all-ones A operand: one 8 x 16-B core matrix of bf16 1.0, read for every
-    // row group and K chunk (both descriptor strides 0)
-    if (t < 8)
-      *reinterpret_cast<uint4 *>(sm + kSmOnes + t * 16) = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-  }
+    return qscale;
+  };
+  // the chunks of FP4 latents only (the first sel_stride / 128 ones) run in f16
+  auto chunk_f16 = [&](int c) { return (c + 1) * kTcChunk <= A.sel_stride; };
+  bool q16 = c0 < c1 && chunk_f16(c0);
+  float qscale = stage_q(q16);
+  // all-ones A operands: one 8 x 16-B core matrix of 1.0 in bf16 and in f16,
+  // read for every row group and K chunk (both descriptor strides 0)
+  if (t < 8)
+    *reinterpret_cast<uint4 *>(sm + kSmOnes + t * 16) = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  else if (t < 16)
+    *reinterpret_cast<uint4 *>(sm + kSmOnes16 + (t - 8) * 16) =
+        make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
@@ -218,17 +286,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   const uint32_t tmem = tmem_sh;
   const uint32_t sK = ptx::smem_u32(sm + kSmK), sQ = ptx::smem_u32(sm + kSmQ);
   const uint32_t sPhi = ptx::smem_u32(sm + kSmPhi), sPlo = ptx::smem_u32(sm + kSmPlo);
-  const uint32_t sOnes = ptx::smem_u32(sm + kSmOnes);
-  const uint32_t id_qk = idesc_bf16_m128n64(0), id_pv = idesc_bf16_m128n64(1);
+  const uint32_t sOnes = ptx::smem_u32(sm + kSmOnes), sOnes16 = ptx::smem_u32(sm + kSmOnes16);
   uint32_t phase = 0;
   bool any_chunk = false;
 
-  for (int c = c0; c < c1; c++) {
-    if (!waited && c * kTcChunk < A.sel_stride) {     // the chunk holds selected entries
+  // A CTA that has to wait for the selection first runs its first chunk's
+  // pipeline once over the sequence's first 128 entries (settled inputs) and
+  // discards the result (wp: the warm-up pass): the real pass then finds its
+  // instructions in the SM's caches instead of fetching each phase's code as
+  // it first runs.
+  const int warm = A.warm && !waited && c0 < c1 && c0 * kTcChunk < A.sel_stride ? 1 : 0;
+  for (int c = c0, wp = warm; c < c1; c += 1 - wp, wp = 0) {
+    if (!waited && !wp && c * kTcChunk < A.sel_stride) {   // the chunk holds selected entries
       griddep_wait();
       griddep_launch();
       waited = true;
     }
+    const bool f16c = chunk_f16(c);
+    if (f16c != q16) {                                // the last chunk's MMAs are complete
+      qscale = stage_q(f16c);
+      q16 = f16c;
+      ptx::fence_proxy_async_smem();
+      __syncthreads();
+    }
+    const uint32_t id_qk = idesc_m128n64(0, f16c), id_pv = idesc_m128n64(1, f16c);
+    const float sl2 = A.scale_log2 * (f16c ? qscale : 1.f);   // S was computed with Q x 2^-qs
     // ---------------------------------------------------------- gather + dequantise
     {
       const int e = t >> 1, half = t & 1;             // entry slot e, dims [256*half, 256*half+256)
@@ -236,7 +318,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       const uint32_t rowbase = (e >> 3) * 8192;        // 8-entry group
       int ok = 0;
       if (slot < A.sel_stride) {
-        const int j = __ldg(A.sel + (int64_t)qi * A.sel_stride + slot);
+        const int j = wp ? ((int64_t)e < A.n_max ? e : -1) : __ldg(A.sel + (int64_t)qi * A.sel_stride + slot);
         if (j >= 0 && (int64_t)j < A.n_max) {
           ok = 1;
           const uint8_t *rec = A.kv + ((int64_t)seq * A.n_max + j) * kKvBytes;
@@ -247,6 +329,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
           uint4 nbv[8];
 #pragma unroll
           for (int v = 0; v < 8; v++) nbv[v] = __ldg(reinterpret_cast<const uint4 *>(rec + half * 128 + v * 16));
+          if (f16c) {
+            // f16: E2M1 pairs and E4M3 scale pairs by the hardware converter
+            uint32_t sh[8];                           // the half-row's 16 scales as f16x2 pairs
+#pragma unroll
+            for (int k = 0; k < 8; k++) sh[k] = e4m3x2_to_f16x2(sc4[k >> 1] >> (16 * (k & 1)));
+#pragma unroll
+            for (int v = 0; v < 8; v++) {
+              const uint32_t nw[4] = {nbv[v].x, nbv[v].y, nbv[v].z, nbv[v].w};
+#pragma unroll
+              for (int u = 0; u < 4; u++) {
+                const int d0 = half * 256 + v * 32 + u * 8;
+                const int g = 2 * v + (u >> 1);       // scale group within this half (0..15)
+                const uint32_t sg = (sh[g >> 1] >> (16 * (g & 1))) & 0xFFFFu;
+                const uint32_t s2w = sg | (sg << 16);
+                uint32_t pk[4];
+                e2m1x8_to_f16(nw[u], pk);
+#pragma unroll
+                for (int b = 0; b < 4; b++) {
+                  __half2 x = *reinterpret_cast<__half2 *>(&pk[b]);
+                  x = __hmul2(x, *reinterpret_cast<const __half2 *>(&s2w));   // exact: <= 10 significant bits, <= 2688
+                  pk[b] = *reinterpret_cast<uint32_t *>(&x);
+                }
+                const uint32_t off = rowbase + (d0 >> 6) * 1024 + sw128(e & 7, (d0 >> 3) & 7);
+                *reinterpret_cast<uint4 *>(sm + kSmK + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              }
+            }
+          } else
 #pragma unroll
           for (int v = 0; v < 8; v++) {               // 16-B nibble load = 32 dims
             const uint32_t nw[4] = {nbv[v].x, nbv[v].y, nbv[v].z, nbv[v].w};
@@ -350,7 +459,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int h = 0; h < 32; h++)
-          v[h] = ev ? (__uint_as_float(r[h]) + __uint_as_float(r2[h])) * A.scale_log2 : -INFINITY;
+          v[h] = ev ? (__uint_as_float(r[h]) + __uint_as_float(r2[h])) * sl2 : -INFINITY;
       }
 #pragma unroll
       for (int w = 16; w >= 1; w >>= 1) {              // w = values kept, partner distance w
@@ -387,16 +496,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       ptx::tmem_ld_32x32b_x32(s_addr, r);
       ptx::tmem_ld_32x32b_x32(s_addr + (kColS2 - kColS), r2);
       ptx::tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; i++) {
+      // hi + lo parts in the chunk's operand type (one loop per type)
+      auto put = [&](int i, uint16_t hi, uint16_t lo) {
         const int h = hb + i;
-        const float l2 = (__uint_as_float(r[i]) + __uint_as_float(r2[i])) * A.scale_log2;
-        const float p = ev ? exp2f(l2 - m_ref[h]) : 0.f;
-        const __nv_bfloat16 ph = __float2bfloat16_rn(p);
-        const __nv_bfloat16 pl = __float2bfloat16_rn(p - __bfloat162float(ph));
         const uint32_t off = (h >> 3) * 2048 + pe + sw128(h & 7, pcol >> 4) + (pcol & 15);
-        *reinterpret_cast<__nv_bfloat16 *>(sm + kSmPhi + off) = ph;
-        *reinterpret_cast<__nv_bfloat16 *>(sm + kSmPlo + off) = pl;
+        *reinterpret_cast<uint16_t *>(sm + kSmPhi + off) = hi;
+        *reinterpret_cast<uint16_t *>(sm + kSmPlo + off) = lo;
+      };
+      if (f16c) {
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+          const float l2 = (__uint_as_float(r[i]) + __uint_as_float(r2[i])) * sl2;
+          const float p = ev ? exp2f(l2 - m_ref[hb + i]) : 0.f;
+          const __half ph = __float2half_rn(p);
+          put(i, __half_as_ushort(ph), __half_as_ushort(__float2half_rn(p - __half2float(ph))));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+          const float l2 = (__uint_as_float(r[i]) + __uint_as_float(r2[i])) * sl2;
+          const float p = ev ? exp2f(l2 - m_ref[hb + i]) : 0.f;
+          const __nv_bfloat16 ph = __float2bfloat16_rn(p);
+          put(i, __bfloat16_as_ushort(ph), __bfloat16_as_ushort(__float2bfloat16_rn(p - __bfloat162float(ph))));
+        }
       }
       ptx::tc_fence_before();
     }
@@ -441,7 +563,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
           ptx::tc_mma_bf16(tmem + kColO + mb * 64, ad, bhi, id_pv, acc0);
           ptx::tc_mma_bf16(tmem + kColO + mb * 64, ad, blo, id_pv, 1u);
         } else {
-          const uint64_t ones = ptx::smem_desc(sOnes, 0, 0, 0);
+          const uint64_t ones = ptx::smem_desc(f16c ? sOnes16 : sOnes, 0, 0, 0);
           ptx::tc_mma_bf16(tmem + kColO + 4 * 64, ones, bhi, id_qk, acc0);
           ptx::tc_mma_bf16(tmem + kColO + 4 * 64, ones, blo, id_qk, 1u);
         }
@@ -451,7 +573,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     if (!ptx::mbar_wait(&bar_o, phase)) { record_error(A.status, CSA2_ERR_TIMEOUT); bad_sh = 1; }
     ptx::tc_fence_after();
     phase ^= 1;
-    any_chunk = true;
+    if (wp) {
+      if (t < kHeads) m_ref[t] = -INFINITY;           // the real pass starts afresh (any_chunk stays false)
+    } else {
+      any_chunk = true;
+    }
     __syncthreads();
     if (bad_sh) break;
   }
@@ -620,7 +746,7 @@ cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_s
                            const void *swa, int swa_cap, const int32_t *q_seq, const int32_t *pos,
                            const int32_t *swa_first, const int32_t *swa_cnt, int n_q, void *out, int out_dtype,
                            float sm_scale, double rope_base, void *ws, int *status, cudaStream_t st,
-                           bool inputs_settled) {
+                           bool inputs_settled, int ahead_ctas) {
   AttnTcArgs A;
   A.settled = inputs_settled ? 1 : 0;
   A.q = static_cast<const uint16_t *>(q);
@@ -648,11 +774,16 @@ cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_s
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_done[64] = {};
+  static int sms[64] = {};
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
     if (e != cudaSuccess) return e;
+    cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
     attr_done[dev] = true;
   }
+  // the warm-up pays only where every CTA is resident while the grid ahead runs
+  const int n_sm = dev >= 0 && dev < 64 ? sms[dev] : 0;
+  A.warm = inputs_settled && plan.cps == 1 && ahead_ctas >= 0 && ahead_ctas + n_q * plan.nsplit <= n_sm ? 1 : 0;
   cudaError_t e = launch_pdl(attn_tc_kernel, dim3(n_q, A.nsplit), dim3(kTcThreads), kSmAlloc, st, 1u, A);
   if (e != cudaSuccess || A.nsplit == 1) return e;
   return launch_pdl(attn_tc_merge_kernel, dim3(kDim / 32, n_q), dim3(256), 0, st, 1u, A);

@@ -75,17 +75,22 @@ FusedTopk topk_fused_plan(void *ws, int n_q, int64_t n_max, int k);
 size_t topk_fused_bytes(int n_q, int64_t n_max, int k);
 cudaError_t launch_topk_fused(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max,
                               int k, const FusedTopk &F, int32_t *out, void *ws, int *status, cudaStream_t st);
+// CTAs (one per SM) that the fused plan's collection grid holds while it runs,
+// or -1 where that is not known (modes -1 and 0).
+int topk_fused_ctas(const FusedTopk &F, int n_q, int64_t n_max);
 
 size_t attn_workspace_bytes(int n_q, int sel_stride);
 // inputs_settled: q, the window cache and the per-query arrays were final
 // before the grid ahead of this one on the stream started (so inside
 // csa2_decode): the kernel then stages Q and runs its window-only chunks before
-// it waits for the selection.
+// it waits for the selection.  ahead_ctas: the SMs the grid ahead holds while
+// it runs (one CTA each), or -1; when this grid fits beside it and a CTA has
+// one chunk, CTAs that wait for the selection run a warm-up pass meanwhile.
 cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_seq, const int32_t *sel,
                            int sel_stride, const void *swa, int swa_cap, const int32_t *q_seq, const int32_t *pos,
                            const int32_t *swa_first, const int32_t *swa_cnt, int n_q, void *out, int out_dtype,
                            float sm_scale, double rope_base, void *ws, int *status, cudaStream_t st,
-                           bool inputs_settled = false);
+                           bool inputs_settled = false, int ahead_ctas = -1);
 
 int *status_word_ptr();
 

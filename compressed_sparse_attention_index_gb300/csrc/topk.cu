@@ -1141,6 +1141,13 @@ FusedTopk topk_fused_plan(void *ws, int n_q, int64_t n_max, int k) {
   return F;
 }
 
+int topk_fused_ctas(const FusedTopk &F, int n_q, int64_t n_max) {
+  if (F.mode <= 0) return -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return (int)collect_ctas(dev, n_q, n_max) * n_q;
+}
+
 size_t topk_fused_bytes(int n_q, int64_t n_max, int k) {
   const FusedTopk F = topk_fused_plan(nullptr, n_q, n_max, k);
   if (F.mode == -1) return 0;
