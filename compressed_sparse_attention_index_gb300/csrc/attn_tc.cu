@@ -219,9 +219,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   // Stage Q (K-major, 128B swizzle: [head/8][dim/64][head%8][128 B]) in the
   // operand type of the chunk ahead: bf16, or f16 for a chunk of FP4 latents
   // only (their dequantised values are exact in f16 and the hardware converts
-  // E2M1 straight to f16).  In f16, Q is scaled by 2^-qs, qs >= 0 the smallest
-  // shift that brings max |q| below 2^15: a power of two, so exact (but for
-  // underflow below 2^-24), folded back into the softmax scale.  Returns 2^qs.
+  // E2M1 straight to f16).  In f16, Q is scaled by 2^-qs, the power of two
+  // that brings max |q| into [2^14, 2^15) (qs >= -100): exact but for elements
+  // below 2^-24 of that range, and folded back into the softmax scale.
+  // Returns 2^qs.
   __shared__ uint32_t qmax_sh[kTcThreads / 32];
   auto stage_q = [&](bool f16) -> float {
     const uint4 *src = reinterpret_cast<const uint4 *>(A.q + (int64_t)qi * kHeads * kDim);
@@ -244,8 +245,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       uint32_t mm = 0u;
 #pragma unroll
       for (int w = 0; w < kTcThreads / 32; w++) mm = max(mm, qmax_sh[w]);
-      const int ex = (int)((mm >> 7) & 0xFFu) - 127;  // max |q| < 2^(ex + 1)
-      const int qs = max(0, ex - 14);
+      const int ex = (int)((mm >> 7) & 0xFFu) - 127;  // max |q| in [2^ex, 2^(ex + 1)) if normal
+      const int qs = mm == 0u ? 0 : max(ex - 14, -100);
       qscale = ldexpf(1.f, qs);
       const float inv = ldexpf(1.f, -qs);
 #pragma unroll

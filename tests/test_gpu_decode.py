@@ -90,6 +90,35 @@ def test_sparse_attn_parity_on_oracle_selection(lib, oracle_lib, out_f32):
         assert row_norm_err(out[qi], ref) <= tol
 
 
+@pytest.mark.parametrize("e", [-40, 40])
+def test_sparse_attn_query_scale_invariance(lib, oracle_lib, e):
+    """q x 2^e with sm_scale x 2^-e gives the same logits.  The selected
+    (FP4-only) chunks run in f16 with Q shifted by the power of two that puts
+    max |q| in [2^14, 2^15), the window chunk in bf16 with Q as given: both must
+    undo the shift, for huge and for tiny queries alike."""
+    from compressed_sparse_attention_index_gb300 import decode, default_params
+    wl = small(n_seq=2, n_entries=3000, seed=260)
+    dw = _dw(wl)
+    buf = _bufs(dw)
+    sel = np.stack([oracle_lib.decode_query(wl, qi)["sel"] for qi in range(2)])
+    buf.sel.copy_(torch.from_numpy(sel))
+    decode.attend(dw, buf)
+    base = buf.out.float().cpu().numpy()
+    dw.q.mul_(2.0 ** e)                                 # exact in bf16 at this range
+    p = default_params()
+    p.sm_scale = p.sm_scale * 2.0 ** -e
+    decode.attend(dw, buf, params=p)
+    out = buf.out.float().cpu().numpy()
+    assert lib.csa2_get_device_status() == 0
+    from oracle.compose import kv_records, swa_records
+    for qi in range(2):
+        ref = oracle_lib.sparse_attn(wl.q(qi), kv_records(wl, qi, sel[qi][sel[qi] >= 0]),
+                                     swa_records(wl, qi, int(wl.swa_first()[qi]), int(wl.swa_cnt()[qi])),
+                                     int(wl.pos()[qi]))
+        assert row_norm_err(out[qi], ref) <= ATTN_TOL_F32
+        assert row_norm_err(out[qi], base[qi]) <= 1e-6
+
+
 def _check_full(lib, oracle_lib, wl, dw, buf, queries):
     from compressed_sparse_attention_index_gb300 import decode
     decode.full_decode(dw, buf)
