@@ -653,13 +653,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
 // Combine the split partials of one query over 32 output dims: grid
 // (kDim / 32, n_q), 256 threads, thread = (head, 8 consecutive dims).
 // Weights w_s = 2^(m_s - max_s m_s) per head, O = sum_s w_s O_s / sum_s w_s l_s,
-// then the RoPE pairs are rotated by -pos.
+// then the RoPE pairs are rotated by -pos.  The rotation angles (fp64 range
+// reduction) depend on pos alone, an input of the call that no grid of it
+// writes, so they are computed before the wait, while the attention runs.
 constexpr int kMaxSplit = 8;
 __global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnTcArgs A) {
-  griddep_wait();
-  griddep_launch();
   const int qi = blockIdx.y, t = threadIdx.x, ns = A.nsplit;
   const int h = t >> 2, d = blockIdx.x * 32 + (t & 3) * 8;
+  float rc[4] = {1.f, 1.f, 1.f, 1.f}, rsn[4] = {0.f, 0.f, 0.f, 0.f};
+  if (d >= kRopeOff) {
+    const int pos = __ldg(A.pos + qi);
+#pragma unroll
+    for (int j = 0; j < 4; j++) rope_cs(A.inv_freq[(d + 2 * j - kRopeOff) >> 1], pos, rc[j], rsn[j]);
+  }
+  griddep_wait();
+  griddep_launch();
   const float *ml = A.part_ml + (int64_t)qi * ns * 2 * kHeads;
   float4 v[kMaxSplit][2];                            // every split's loads in flight at once
   float m[kMaxSplit], l[kMaxSplit];
@@ -692,12 +700,9 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnTcArgs A) {
 #pragma unroll
   for (int j = 0; j < 8; j++) y[j] *= inv;
   if (d >= kRopeOff) {
-    const int pos = __ldg(A.pos + qi);
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
-      float c, sn;
-      rope_cs(A.inv_freq[(d + j - kRopeOff) >> 1], pos, c, sn);
-      const float a = y[j], b = y[j + 1];
+      const float c = rc[j >> 1], sn = rsn[j >> 1], a = y[j], b = y[j + 1];
       y[j] = a * c + b * sn;
       y[j + 1] = -a * sn + b * c;
     }
