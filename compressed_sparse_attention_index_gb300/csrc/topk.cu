@@ -38,7 +38,8 @@ struct TopkSrc {
   int64_t n_max;          // entries per row (Full) or 16384 (pool)
   int64_t n_items;        // items per row
   // optional (plain rows): latent cache records [n_seq][n_max][288] that the
-  // attention reads next; the selected ones are prefetched into L2
+  // attention reads next; the collecting CTAs prefetch their candidates' ones
+  // into L2
   const uint8_t *kv_pf;
   const int32_t *q_seq;
   int n_seq;
@@ -386,12 +387,10 @@ struct BlockReduce {
 // the selected indices and places them in ascending order by bucketing them
 // by index (buckets of power-of-two width; a few indices per bucket).  keys
 // and sk are reused as scratch.  sel: >= k ints; bins: >= 4096 counters.
-// out[0..k): ascending indices, -1 padding.  pf: null, or the base of records
-// of kKvBytes per index, which are prefetched into L2 once the set is known.
-// by_index: keys[] is already in ascending index order; the selected keys are
+// out[0..k): ascending indices, -1 padding.  by_index: keys[] is already in ascending index order; the selected keys are
 // then written out by one order-keeping compaction.
 __device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t *out, int32_t *sel,
-                                          uint32_t *bins, const uint8_t *pf = nullptr, bool by_index = false) {
+                                          uint32_t *bins, bool by_index = false) {
   __shared__ int cnt_sh[2];
   __shared__ int n_sel;
   __shared__ uint32_t red_slots[2][32];
@@ -431,13 +430,6 @@ __device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t
       if (i < n && keys[i] >= K) {
         const int32_t idx = (int32_t)(~(uint32_t)(keys[i] & 0xFFFFFFFFu));
         out[pos++] = idx;
-        if (pf != nullptr) {
-          const uint8_t *rec = pf + (int64_t)idx * kKvBytes;
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(rec));
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + 128));
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + 256));
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + kKvBytes - 1));
-        }
       }
     }
     for (int i = take + threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
@@ -457,12 +449,6 @@ __device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t
     if (ok) sel[base] = (int32_t)(~(uint32_t)(x & 0xFFFFFFFFu));
   }
   __syncthreads();
-  if (pf != nullptr)
-    for (int i = threadIdx.x; i < 4 * take; i += blockDim.x) {   // a record spans at most four 128-B lines
-      const uint8_t *rec = pf + (int64_t)sel[i >> 2] * kKvBytes;
-      const int o = (i & 3) == 3 ? kKvBytes - 1 : (i & 3) * 128;
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + o));
-    }
   // ---- ascending index order: 2,048 index buckets (counts, cursors); the
   // key buffer (the keys are in registers now) receives them bucket by bucket
   uint32_t *h2 = bins, *c2 = bins + 2048;
@@ -744,7 +730,7 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
   griddep_launch();
   const int q = blockIdx.y, P = gridDim.x, part = blockIdx.x;
   const int nv = query_nv(S, q, status);
-  const int pf_seq = (S.kv_pf != nullptr && part == 0) ? __ldg(S.q_seq + q) : -1;   // used at the end
+  const int pf_seq = S.kv_pf != nullptr ? __ldg(S.q_seq + q) : -1;   // used at the end
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool plain = S.pool == nullptr && S.block == 1;
   const int64_t valid_items = plain ? nv : (S.pool != nullptr ? S.n_items : ((int64_t)nv + kBlock - 1) / kBlock);
@@ -983,17 +969,29 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
     }
   }
   cluster_barrier();                                   // the other CTAs' shared memory is no longer read
+  // L2 prefetch of the latent records of this CTA's candidates (a superset of
+  // the selected entries, which the attention gathers next): spread over the
+  // cluster, and out of CTA 0's selection, which follows
+  if (plain && pf_seq >= 0 && pf_seq < S.n_seq) {
+    const uint8_t *pf = S.kv_pf + (int64_t)pf_seq * S.n_max * kKvBytes;
+    const int nl = min(n_lc, kLocalCap);
+    for (int i = threadIdx.x; i < 4 * nl; i += blockDim.x) {   // a record spans at most four 128-B lines
+      const uint32_t idx = ~(uint32_t)lc[i >> 2];
+      if ((int64_t)idx >= S.n_max) continue;
+      const uint8_t *rec = pf + (int64_t)idx * kKvBytes;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + ((i & 3) == 3 ? kKvBytes - 1 : (i & 3) * 128)));
+    }
+  }
   if (part != 0) return;
   int32_t *oq = out + (int64_t)q * k;
   if (!c_bad) {
     const int nc = c_off[P];
+    __syncthreads();                                   // lc (over sv) is read above
     for (int i = threadIdx.x; i < ((nc + 3) & ~3); i += blockDim.x)
       sv[i] = i < nc ? (uint32_t)(keys[i] >> 32) : 0u;   // score halves, zero-padded
     __syncthreads();
-    const uint8_t *pf =
-        (pf_seq >= 0 && pf_seq < S.n_seq) ? S.kv_pf + (int64_t)pf_seq * S.n_max * kKvBytes : nullptr;
     // pool items run in slot order, not index order: only plain and block rows keep order
-    select_block(keys, sv, nc, k, oq, sel, sh.whist, pf, c_sorted != 0 && S.pool == nullptr);
+    select_block(keys, sv, nc, k, oq, sel, sh.whist, c_sorted != 0 && S.pool == nullptr);
   } else {
     // too many ties at T for the buffer: exact selection straight over the row
     __shared__ int nvi;
