@@ -262,3 +262,9 @@ def test_fused_decode_equals_call_chain(lib, case):
     assert torch.equal(chain.out.view(torch.int32), fused.out.view(torch.int32))
     decode.fused_decode(dw, fused)                       # second call: nothing left over from the first
     assert torch.equal(chain.sel, fused.sel)
+    fused.ws.fill_(0xA5)                                 # a workspace of garbage: nothing in it is
+    fused.out.fill_(7)                                   # read before this call writes it
+    decode.fused_decode(dw, fused)
+    assert lib.csa2_get_device_status() == 0
+    assert torch.equal(chain.sel, fused.sel)
+    assert torch.equal(chain.out.view(torch.int32), fused.out.view(torch.int32))
