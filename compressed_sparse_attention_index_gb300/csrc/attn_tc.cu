@@ -13,7 +13,8 @@
 //   2. S^T[entry][head] = Khat . Q^T     tcgen05 kind::f16, M=128 entries, N=64
 //      heads, K=512 (both operands K-major, 128B-swizzled);
 //   3. softmax numerators p = 2^(l*log2e - m_ref) per (entry, head), stored as
-//      bf16 hi + lo parts (together ~16 significant bits);
+//      f16 (chunks of FP4 latents, see below; 11 significant bits) or as bf16
+//      hi + lo parts (together ~16 significant bits);
 //   4. O^T[dim][head] += Vhat^T . P^T     M=128 dims (4 blocks), N=64, K=128
 //      entries; Vhat^T is the same shared-memory chunk read MN-major (k = v).
 //      A fifth block multiplies an all-ones tile, so its rows accumulate the
@@ -497,10 +498,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       ptx::tmem_ld_32x32b_x32(s_addr, r);
       ptx::tmem_ld_32x32b_x32(s_addr + (kColS2 - kColS), r2);
       ptx::tmem_wait_ld();
-      // hi + lo parts in the chunk's operand type (one loop per type)
-      auto put = [&](int i, uint16_t hi, uint16_t lo) {
+      // f16 chunks: the numerator rounded to f16 (11 significant bits); bf16
+      // chunks: bf16 hi + lo parts (~16 bits).  One loop per type.
+      auto off_of = [&](int i) {
         const int h = hb + i;
-        const uint32_t off = (h >> 3) * 2048 + pe + sw128(h & 7, pcol >> 4) + (pcol & 15);
+        return (h >> 3) * 2048 + pe + sw128(h & 7, pcol >> 4) + (pcol & 15);
+      };
+      auto put = [&](int i, uint16_t hi, uint16_t lo) {
+        const uint32_t off = off_of(i);
         *reinterpret_cast<uint16_t *>(sm + kSmPhi + off) = hi;
         *reinterpret_cast<uint16_t *>(sm + kSmPlo + off) = lo;
       };
@@ -509,8 +514,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
         for (int i = 0; i < 32; i++) {
           const float l2 = (__uint_as_float(r[i]) + __uint_as_float(r2[i])) * sl2;
           const float p = ev ? exp2f(l2 - m_ref[hb + i]) : 0.f;
-          const __half ph = __float2half_rn(p);
-          put(i, __half_as_ushort(ph), __half_as_ushort(__float2half_rn(p - __half2float(ph))));
+          *reinterpret_cast<__half *>(sm + kSmPhi + off_of(i)) = __float2half_rn(p);
         }
       } else {
 #pragma unroll
@@ -562,11 +566,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
           // Vhat^T block: dims [128 mb, 128 mb + 128), entries [16 ks, 16 ks + 16), MN-major
           const uint64_t ad = ptx::smem_desc(sK + (2 * ks) * 8192 + (2 * mb) * 1024, 1024, 8192, 2);
           ptx::tc_mma_bf16(tmem + kColO + mb * 64, ad, bhi, id_pv, acc0);
-          ptx::tc_mma_bf16(tmem + kColO + mb * 64, ad, blo, id_pv, 1u);
+          if (!f16c) ptx::tc_mma_bf16(tmem + kColO + mb * 64, ad, blo, id_pv, 1u);
         } else {
           const uint64_t ones = ptx::smem_desc(f16c ? sOnes16 : sOnes, 0, 0, 0);
           ptx::tc_mma_bf16(tmem + kColO + 4 * 64, ones, bhi, id_qk, acc0);
-          ptx::tc_mma_bf16(tmem + kColO + 4 * 64, ones, blo, id_qk, 1u);
+          if (!f16c) ptx::tc_mma_bf16(tmem + kColO + 4 * 64, ones, blo, id_qk, 1u);
         }
       }
       ptx::tc_commit(&bar_o);
