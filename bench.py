@@ -308,7 +308,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e2m1xe2m1->f32 (score), bf16xbf16->f32 (attention)",
+        "dtype": "e2m1xe2m1->f32 (score), f16xf16 + bf16xbf16->f32 (attention)",
         "data": "synthetic (seeded counter-based generator; no trained weights)",
         "config": {"workload": wl.name, "n_seq": wl.n_seq, "n_entries": wl.n_entries, "queries_per_step": n_q,
                    "zipf_keys": wl.zipf, "topk": 512, "swa": 128, "heads": 64, "latent": 512,
@@ -447,7 +447,7 @@ def run_rows(args, rank, world, local_rank, wl):
                 "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s",
                 "frac": k_bytes / (k_ms / 1e3) / 1e9 / hbm, "traffic": None,
                 "algorithmic_bytes_per_launch": k_bytes, "avg_launch_ms": k_ms}
-        dtype = "e2m1xe2m1->f32 (score), bf16xbf16->f32 (attention)"
+        dtype = "e2m1xe2m1->f32 (score), f16xf16 + bf16xbf16->f32 (attention)"
     else:
         # (query, entry) pairs of the attention, 4 FLOP per pair, head and dim (QK and PV)
         pairs = int(np.minimum(512, n_vis).sum() + swa_cnt.sum())
@@ -459,7 +459,7 @@ def run_rows(args, rank, world, local_rank, wl):
                 "peak_kind": "measured" if "bf16_tflops" in peaks_all else "fallback", "unit": "TFLOP/s",
                 "frac": achieved / bf16, "traffic": None, "algorithmic_flop_per_launch": flop,
                 "avg_launch_ms": k_ms}
-        dtype = "e2m1xe2m1->f32 (score), bf16xbf16->f32 (attention)"
+        dtype = "e2m1xe2m1->f32 (score), f16xf16 + bf16xbf16->f32 (attention)"
     launches = (1 + 1 + 2) if wl.pool else (1 + 1 + 1)
     return {
         "metric": ("Reindex decode" if wl.pool else "m=2 prefill") + " query-tokens/s for CSA2 (score+top512+attn)",
