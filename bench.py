@@ -184,8 +184,9 @@ def run_ours(args, rank, world, local_rank):
     from gen.device import build_device_workload
     from gen.workloads import CONFIGS
 
+    from compressed_sparse_attention_index_gb300 import ranks
     torch.cuda.set_device(local_rank)
-    wl = CONFIGS[args.config]
+    wl = ranks.rank_workload(CONFIGS[args.config], rank)    # each rank decodes its own batch
     if wl.pool or wl.prefill:
         return run_rows(args, rank, world, local_rank, wl)
     dw = build_device_workload(wl)
@@ -212,16 +213,14 @@ def run_ours(args, rank, world, local_rank):
             pass
     clocks = ClockSampler(gpu_index)
     time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
+    ranks.barrier()
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
         step()
     t_end.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    ranks.barrier()
     clk = clocks.stop()
     ms = t_start.elapsed_time(t_end)
     assert C.csa2_get_device_status() == 0
@@ -242,10 +241,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     score_ms = sum(a.elapsed_time(b) for a, b in ev_s) / args.steps
     assert C.csa2_get_device_status() == 0
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = ranks.max_over_ranks(ms, device="cuda")
 
     # end to end through the public API: the step's inputs (attention query,
     # indexer query in bf16, head weights, per-query descriptors) packed in one
@@ -276,17 +272,14 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = ranks.max_over_ranks(e2e_ms, device="cuda")
     h2d = stage_h.numel()
     d2h = out_h.numel() * out_h.element_size()
 
     if rank != 0:
         return None
     units = n_q * args.steps * world
-    value = units / (ms / 1e3)
+    value = ranks.whole_job_rate(n_q * args.steps, world, ms)
     peak, peak_kind = peaks()
     score_bytes = n_q * wl.n_entries * IDX_BYTES           # algorithmic bytes of one score launch
     achieved = score_bytes / (score_ms / 1e3) / 1e9
@@ -338,7 +331,7 @@ def run_rows(args, rank, world, local_rank, wl):
     import torch
     import torch.distributed as dist
     import compressed_sparse_attention_index_gb300 as C
-    from compressed_sparse_attention_index_gb300 import decode
+    from compressed_sparse_attention_index_gb300 import decode, ranks
     from gen.device import build_device_workload
 
     dw = build_device_workload(wl)
@@ -359,8 +352,7 @@ def run_rows(args, rank, world, local_rank, wl):
     assert C.csa2_get_device_status() == 0
     clocks = ClockSampler(local_rank)
     time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
+    ranks.barrier()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -368,8 +360,7 @@ def run_rows(args, rank, world, local_rank, wl):
         step()
     t1.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    ranks.barrier()
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
     assert C.csa2_get_device_status() == 0
@@ -387,10 +378,7 @@ def run_rows(args, rank, world, local_rank, wl):
     torch.cuda.synchronize()
     k_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     assert C.csa2_get_device_status() == 0
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = ranks.max_over_ranks(ms, device="cuda")
 
     # the step through pinned host inputs: the attention query and the indexer
     # inputs of the step in, the output back
@@ -424,7 +412,7 @@ def run_rows(args, rank, world, local_rank, wl):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = ranks.max_over_ranks(e0.elapsed_time(e1), device="cuda")
     h2d = stage_h.numel()
     d2h = out_h.numel() * out_h.element_size()
     if rank != 0:
