@@ -15,6 +15,8 @@ Parity status per function (the pins are the ``-m "not gpu"`` tests):
   topk, pool_blocks         pinned (brute-force sort, superset invariant)
   sparse_attn               pinned (dense softmax attention, single-entry and
                             RoPE closed forms, shift invariance)
+  sparse_attn_lse           pinned (outputs of parts of a softmax's entries,
+                            merged by their log-sum-exp, equal the whole)
 DeepSeek's own numerics are not published on the pages, so parity is pinned to
 the readings stated in the C source, not to DeepSeek's kernels.
 """
@@ -64,6 +66,7 @@ def lib():
             "orc_topk": (i32, [P, i64, i32, P]),
             "orc_pool_blocks": (i32, [P, i64, i32, i32, P]),
             "orc_sparse_attn": (None, [P, P, i32, P, i32, i64, f64, f64, i32, i32, P]),
+            "orc_sparse_attn_lse": (None, [P, P, i32, P, i32, i64, f64, f64, i32, i32, P, P]),
             "orc_kv_bytes": (i32, []), "orc_idx_bytes": (i32, []), "orc_swa_bytes": (i32, []),
         }
         for name, (res, args) in sig.items():
@@ -184,6 +187,19 @@ def sparse_attn(q_bf16, kv_rows, swa_rows, pos, sm_scale=1.0 / np.sqrt(512.0), r
     lib().orc_sparse_attn(_p(q), _p(kv), kv.shape[0], _p(sw), sw.shape[0], int(pos), float(sm_scale),
                           float(rope_base), rope_off, rope_dim, _p(out))
     return out
+
+
+def sparse_attn_lse(q_bf16, kv_rows, swa_rows, pos, sm_scale=1.0 / np.sqrt(512.0), rope_base=10000.0,
+                    rope_off=448, rope_dim=64):
+    """sparse_attn, and per head the log-sum-exp of the logits over the entries given."""
+    q = _c(q_bf16, np.uint16).reshape(H, D)
+    kv = _c(kv_rows, np.uint8).reshape(-1, KV_BYTES)
+    sw = _c(swa_rows, np.uint8).reshape(-1, SWA_BYTES)
+    out = np.zeros((H, D), np.float64)
+    lse = np.zeros(H, np.float64)
+    lib().orc_sparse_attn_lse(_p(q), _p(kv), kv.shape[0], _p(sw), sw.shape[0], int(pos), float(sm_scale),
+                              float(rope_base), rope_off, rope_dim, _p(out), _p(lse))
+    return out, lse
 
 
 from .compose import *  # noqa: E402,F401,F403  (workload-level compositions)

@@ -346,9 +346,9 @@ int orc_pool_blocks(const double *s, int64_t n, int block, int nb, int32_t *out)
  *   by -pos with theta_i = pos * rope_base^(-2i / rope_dim).
  * kv_rows: [n_sel][288] records of the selected entries, swa_rows: [n_swa][528].
  * q: [64][512] bf16.  out: [64][512]. */
-void orc_sparse_attn(const uint16_t *q, const uint8_t *kv_rows, int n_sel, const uint8_t *swa_rows,
-                     int n_swa, int64_t pos, double sm_scale, double rope_base, int rope_off,
-                     int rope_dim, double *out) {
+static void orc_sparse_attn_impl(const uint16_t *q, const uint8_t *kv_rows, int n_sel, const uint8_t *swa_rows,
+                                 int n_swa, int64_t pos, double sm_scale, double rope_base, int rope_off,
+                                 int rope_dim, double *out, double *lse) {
     int n = n_sel + n_swa;
     double *k = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * ORC_DIM);
     for (int i = 0; i < n_sel; i++) orc_dequant_kv(kv_rows + (size_t)i * ORC_KV_BYTES, k + (size_t)i * ORC_DIM);
@@ -358,6 +358,7 @@ void orc_sparse_attn(const uint16_t *q, const uint8_t *kv_rows, int n_sel, const
     for (int h = 0; h < ORC_HEADS; h++) {
         double *o = out + (size_t)h * ORC_DIM;
         for (int c = 0; c < ORC_DIM; c++) o[c] = 0.0;
+        if (lse) lse[h] = -INFINITY;
         if (n == 0) continue;
         double qh[ORC_DIM];
         for (int c = 0; c < ORC_DIM; c++) qh[c] = orc_bf16_value(q[h * ORC_DIM + c]);
@@ -371,6 +372,7 @@ void orc_sparse_attn(const uint16_t *q, const uint8_t *kv_rows, int n_sel, const
         }
         double den = 0.0;
         for (int i = 0; i < n; i++) { l[i] = exp(l[i] - mx); den += l[i]; }
+        if (lse) lse[h] = mx + log(den);   /* log sum_i exp(l_i) */
         for (int i = 0; i < n; i++) {
             double p = l[i] / den;
             for (int c = 0; c < ORC_DIM; c++) o[c] += p * k[(size_t)i * ORC_DIM + c];
@@ -385,4 +387,21 @@ void orc_sparse_attn(const uint16_t *q, const uint8_t *kv_rows, int n_sel, const
         }
     }
     free(k);
+}
+
+void orc_sparse_attn(const uint16_t *q, const uint8_t *kv_rows, int n_sel, const uint8_t *swa_rows,
+                     int n_swa, int64_t pos, double sm_scale, double rope_base, int rope_off,
+                     int rope_dim, double *out) {
+    orc_sparse_attn_impl(q, kv_rows, n_sel, swa_rows, n_swa, pos, sm_scale, rope_base, rope_off, rope_dim, out,
+                         NULL);
+}
+
+/* The same, also writing lse[h] = log sum_i exp(l_i) over the entries given
+ * (-inf when there are none): the weight with which this output enters a
+ * softmax over a larger set of entries (log-sum-exp merge of partial sets). */
+void orc_sparse_attn_lse(const uint16_t *q, const uint8_t *kv_rows, int n_sel, const uint8_t *swa_rows,
+                         int n_swa, int64_t pos, double sm_scale, double rope_base, int rope_off,
+                         int rope_dim, double *out, double *lse) {
+    orc_sparse_attn_impl(q, kv_rows, n_sel, swa_rows, n_swa, pos, sm_scale, rope_base, rope_off, rope_dim, out,
+                         lse);
 }
