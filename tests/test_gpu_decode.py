@@ -90,6 +90,37 @@ def test_sparse_attn_parity_on_oracle_selection(lib, oracle_lib, out_f32):
         assert row_norm_err(out[qi], ref) <= tol
 
 
+@pytest.mark.parametrize("n_seq,stride", [(3, 1), (3, 129), (3, 300), (48, 511)])
+def test_sparse_attn_ragged_selection_stride(lib, oracle_lib, n_seq, stride):
+    """sel_stride not a multiple of 128: the chunk that holds the last selected
+    entries and the first window entries dequantises its FP4 latents to bf16
+    (the chunks of FP4 latents only run in f16), and Q is staged in both types;
+    with 48 queries a CTA takes two chunks, f16 then that bf16 one, and
+    restages Q between them."""
+    import compressed_sparse_attention_index_gb300 as C
+    wl = small(n_seq=n_seq, n_entries=3000 if n_seq == 3 else 1500, seed=270 + stride)
+    dw = _dw(wl)
+    n_q = dw.q.shape[0]
+    full = np.stack([oracle_lib.decode_query(wl, qi)["sel"] for qi in range(n_q)])
+    sel = np.ascontiguousarray(full[:, :stride])
+    sel[1, ::3] = -1                                    # holes as well
+    out = torch.empty((n_q, 64, 512), dtype=torch.float32, device="cuda")
+    ws_bytes = C.csa2_workspace_size(C.CSA2_OP_SPARSE_ATTN, n_q, stride + 128)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    C.csa2_sparse_attn(dw.q, dw.kv, dw.n_max, dw.kv.shape[0], torch.from_numpy(sel).cuda(), stride, dw.swa,
+                       dw.swa.shape[1], dw.q_seq, dw.pos, dw.swa_first, dw.swa_cnt, n_q, out, C.CSA2_OUT_F32, None,
+                       ws, ws_bytes)
+    got = out.cpu().numpy()
+    assert lib.csa2_get_device_status() == 0
+    from oracle.compose import kv_records, swa_records
+    for qi in range(n_q):
+        s_ = sel[qi][sel[qi] >= 0]
+        ref = oracle_lib.sparse_attn(wl.q(qi), kv_records(wl, qi, s_),
+                                     swa_records(wl, qi, int(wl.swa_first()[qi]), int(wl.swa_cnt()[qi])),
+                                     int(wl.pos()[qi]))
+        assert row_norm_err(got[qi], ref) <= ATTN_TOL_F32
+
+
 @pytest.mark.parametrize("e", [-40, 40])
 def test_sparse_attn_query_scale_invariance(lib, oracle_lib, e):
     """q x 2^e with sm_scale x 2^-e gives the same logits.  The selected
