@@ -115,7 +115,8 @@ def cpu_baseline(wl, n_samples=1):
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     def __init__(self, gpu_index: int):
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        import tempfile
+        self.path = os.path.join(tempfile.gettempdir(), f"csa2_clocks_{os.getpid()}.csv")
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
