@@ -8,8 +8,10 @@
 //
 // The entry slots of a query (sel_stride selected entries, -1 = empty, then the
 // swa_cnt window entries) are processed in chunks of 128.  Per chunk:
-//   1. gather + dequantise the 128 records to bf16 in shared memory (exact: an
-//      E2M1 x E4M3 product has <= 6 significant bits, E4M3 x 2^e fits bf16);
+//   1. gather + dequantise the 128 records in shared memory, exactly: a chunk
+//      of FP4 latents only to f16 (an E2M1 x E4M3 product has <= 6 significant
+//      bits and lies in [2^-10, 2688] or is 0), a chunk holding window entries
+//      to bf16 (E4M3 x 2^e fits bf16); Q is staged in the chunk's type;
 //   2. S^T[entry][head] = Khat . Q^T     tcgen05 kind::f16, M=128 entries, N=64
 //      heads, K=512 (both operands K-major, 128B-swizzled);
 //   3. softmax numerators p = 2^(l*log2e - m_ref) per (entry, head), stored as
@@ -24,11 +26,14 @@
 // (factor 256), otherwise the larger numerators are simply accumulated.
 // A CTA handles a range of chunks of one query; with a single range it
 // finishes the output (normalise, un-rotate, store), otherwise it writes
-// (O, m, l) partials that attn_merge_kernel combines.
+// (O, m, l) partials that attn_tc_merge_kernel combines.  Started ahead of the
+// selection (settled inputs), a CTA stages Q, runs window-only chunks, and may
+// run a discarded warm-up pass of its first chunk before it waits.
 //
 // 256 threads: all of them gather/dequantise and run the softmax (warp w reads
-// TMEM lane quarter w%4, heads 32*(w/4) ..); thread 0 issues the MMAs; all 8
-// warps share the final read-out of the 5 x 64 accumulator columns.
+// TMEM lane quarter w%4, heads 32*(w/4) ..); lane 0 of warps 0-1 issues the QK
+// MMAs and lane 0 of warps 0-4 the PV MMAs; all 8 warps share the final
+// read-out of the 5 x 64 accumulator columns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
