@@ -11,11 +11,13 @@
 //
 // Rows of up to kDirectCap items are selected by one CTA from shared memory.
 // Longer rows (1M-entry Full-layer rows, 131,072-block pool rows) take two
-// launches: a bandwidth pass writes the maximum key of every group of G items
-// (G = 32 for k = 512 over 1M entries); then one CTA per row finds a threshold
-// T from the group maxima alone (two 12-bit histogram digits), rescans only the
-// groups whose maximum reaches T (about k groups), and runs the exact
-// selection on those candidates (about k items).  A row whose lists overflow
+// passes: the maximum key of every supergroup of items (512 items for k = 512
+// over 1M entries; written by a bandwidth pass, or by the indexer's epilogue
+// inside csa2_decode); then a thread-block cluster of P CTAs per row finds a
+// threshold T from the supergroup maxima alone (radix-256 steps below the
+// leading bits all maxima share), streams only the supergroups whose maximum
+// reaches T (about k), and CTA 0 runs the exact selection on the candidates
+// gathered from the cluster (about k items).  A row whose lists overflow
 // shared memory falls back to an exact radix select straight over the row.
 #include <algorithm>
 
