@@ -46,9 +46,11 @@ IDX_BYTES = 68
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one index_score_tc_kernel launch, from an ncu
-# capture of this kernel version on the named workload (profiles/index_score_tc_32x64K.md gives
-# the command); workloads without a capture report null.
-INDEX_SCORE_TRAFFIC = {"long_full_decode_N1M_B8_zipf": 570487040 + 5117184}
+# capture of the current kernel version on the named workload (profiles/index_score_tc_32x64K.md
+# gives the command); workloads without such a capture report null.  The last capture
+# (570,487,040 + 5,117,184 B at 8 x 1M) predates the kernel's pool-gathering warps, so none
+# is current.
+INDEX_SCORE_TRAFFIC = {}
 
 
 def parse():
