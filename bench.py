@@ -45,12 +45,10 @@ FIXED_BYTES_PER_QUERY = 348_416      # 512x288 + 128x528 + q 64 KiB + out 64 KiB
 IDX_BYTES = 68
 
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one index_score_tc_kernel launch, from an ncu
-# capture of the current kernel version on the named workload (profiles/index_score_tc_32x64K.md
-# gives the command); workloads without such a capture report null.  The last capture
-# (570,487,040 + 5,117,184 B at 8 x 1M) predates the kernel's pool-gathering warps, so none
-# is current.
-INDEX_SCORE_TRAFFIC = {}
+# dram__bytes_read.sum + dram__bytes_write.sum of one index_score_tc_kernel launch inside
+# csa2_decode, from an ncu capture (--metrics dram__bytes_read.sum,dram__bytes_write.sum) of the
+# current kernel on the named workload; workloads without such a capture report null.
+INDEX_SCORE_TRAFFIC = {"long_full_decode_N1M_B8_zipf": 570_497_024 + 4_925_184}
 
 
 def parse():

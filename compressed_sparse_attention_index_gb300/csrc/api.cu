@@ -14,15 +14,17 @@ namespace csa2 {
 __device__ int g_status_word;
 
 static int *status_ptr() {
-  static int *ptrs[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (ptrs[dev] == nullptr) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<int *>(p);
+  static std::atomic<int *> ptrs[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  int *p = ptrs[dev].load(std::memory_order_relaxed);
+  if (p == nullptr) {
+    void *a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_status_word) != cudaSuccess) return nullptr;
+    p = static_cast<int *>(a);
+    ptrs[dev].store(p, std::memory_order_relaxed);
   }
-  return ptrs[dev];
+  return p;
 }
 
 // The status word's device address for entry points defined in other files.

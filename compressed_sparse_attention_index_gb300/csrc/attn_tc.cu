@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   }
   const int seq = __ldg(A.q_seq + qi);
   const int swa_cnt = __ldg(A.swa_cnt + qi), swa_first = __ldg(A.swa_first + qi);
-  const bool bad = seq < 0 || seq >= A.n_seq || swa_cnt < 0 || swa_cnt > kSwa ||
+  const bool bad = seq < 0 || seq >= A.n_seq || swa_cnt < 0 || swa_cnt > kSwa || swa_cnt > A.swa_cap ||
                    (swa_cnt > 0 && (swa_first < 0 || swa_first >= A.swa_cap));
   if (bad && t == 0 && split == 0) record_error(A.status, CSA2_ERR_BOUNDS);
   const int n_slots = A.sel_stride + (bad ? 0 : swa_cnt);
@@ -734,25 +734,25 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnTcArgs A) {
 
 static int attn_chunks(int sel_stride) { return (sel_stride + kSwa + kTcChunk - 1) / kTcChunk; }
 
-// How the chunks of a query are spread over CTAs: one chunk per CTA while the
-// CTAs whose chunks hold selected entries fit one wave on a 152-SM GPU (the
-// window-only chunks are placed first and run while the selection finishes);
-// else contiguous runs of chunks, at least one CTA per query.
+// How the chunks of a query are spread over CTAs (one CTA per SM): one chunk
+// per CTA while the CTAs whose chunks hold selected entries fit one wave on the
+// current device's n_sm SMs (the window-only chunks are placed first and run
+// while the selection finishes); else contiguous runs of chunks, at least one
+// CTA per query.
 struct AttnPlan {
   int nsplit, cps;
 };
-static AttnPlan attn_plan(int n_q, int sel_stride) {
-  constexpr int kSms = 152;
+static AttnPlan attn_plan(int n_q, int sel_stride, int n_sm) {
   const int chunks = attn_chunks(sel_stride);
   const int sel_ch = (sel_stride + kTcChunk - 1) / kTcChunk;
-  if (n_q * sel_ch <= kSms) return AttnPlan{chunks, 1};
-  const int ns = std::max(1, std::min(chunks, kSms / n_q));
+  if (n_q * sel_ch <= n_sm) return AttnPlan{chunks, 1};
+  const int ns = std::max(1, std::min(chunks, n_sm / n_q));
   const int cps = (chunks + ns - 1) / ns;
   return AttnPlan{(chunks + cps - 1) / cps, cps};
 }
 
 size_t attn_workspace_bytes(int n_q, int sel_stride) {
-  const AttnPlan p = attn_plan(n_q, sel_stride);
+  const AttnPlan p = attn_plan(n_q, sel_stride, device_sm_count(current_device()));
   if (p.nsplit == 1) return 0;
   return (size_t)n_q * p.nsplit * (kHeads * kDim + 2 * kHeads) * sizeof(float);
 }
@@ -780,26 +780,22 @@ cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_s
   A.out_f32 = out_dtype == CSA2_OUT_F32;
   A.scale_log2 = sm_scale * 1.4426950408889634f;
   for (int i = 0; i < kRopeDim / 2; i++) A.inv_freq[i] = pow(rope_base, -2.0 * i / (double)kRopeDim);
-  const AttnPlan plan = attn_plan(n_q, sel_stride);
+  const int dev = current_device();
+  const int n_sm = device_sm_count(dev);
+  const AttnPlan plan = attn_plan(n_q, sel_stride, n_sm);
   A.nsplit = plan.nsplit;
   A.chunks_per_split = plan.cps;
   A.part = static_cast<float *>(ws);
   A.part_ml = A.part + (size_t)n_q * A.nsplit * kHeads * kDim;
   A.status = status;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  static bool attr_done[64] = {};
-  static int sms[64] = {};
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
-    if (e != cudaSuccess) return e;
-    cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    attr_done[dev] = true;
-  }
+  static std::atomic<int> attr_done[kMaxDevices];
+  cudaError_t e = once_per_device(attr_done, dev, [&] {
+    return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+  });
+  if (e != cudaSuccess) return e;
   // the warm-up pays only where every CTA is resident while the grid ahead runs
-  const int n_sm = dev >= 0 && dev < 64 ? sms[dev] : 0;
   A.warm = inputs_settled && plan.cps == 1 && ahead_ctas >= 0 && ahead_ctas + n_q * plan.nsplit <= n_sm ? 1 : 0;
-  cudaError_t e = launch_pdl(attn_tc_kernel, dim3(n_q, A.nsplit), dim3(kTcThreads), kSmAlloc, st, 1u, A);
+  e = launch_pdl(attn_tc_kernel, dim3(n_q, A.nsplit), dim3(kTcThreads), kSmAlloc, st, 1u, A);
   if (e != cudaSuccess || A.nsplit == 1) return e;
   return launch_pdl(attn_tc_merge_kernel, dim3(kDim / 32, n_q), dim3(256), 0, st, 1u, A);
 }

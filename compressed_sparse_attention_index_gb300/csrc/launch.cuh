@@ -5,7 +5,48 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace csa2 {
+
+// Host-side caches, one entry per device ordinal below kMaxDevices.  Host
+// threads may make their first calls at the same time, so every entry is an
+// atomic read and written with relaxed ordering: racing fillers store the same
+// value, and a reader sees either nothing yet (and fills it itself) or that value.
+constexpr int kMaxDevices = 64;
+
+// Runs init() (which returns a cudaError_t) on the first call for device dev
+// and remembers success; two threads racing on the first call may both run it,
+// which must be harmless (kernel attributes set twice to the same value).
+template <class F>
+cudaError_t once_per_device(std::atomic<int> (&done)[kMaxDevices], int dev, F init) {
+  if (dev < 0 || dev >= kMaxDevices) return init();
+  if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  const cudaError_t e = init();
+  if (e == cudaSuccess) done[dev].store(1, std::memory_order_relaxed);
+  return e;
+}
+
+// Number of SMs of device dev (cached), or `fallback` if it cannot be read.
+inline int device_sm_count(int dev, int fallback = 148) {
+  static std::atomic<int> counts[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return fallback;
+  int c = counts[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) {
+      cudaGetLastError();
+      return fallback;
+    }
+    counts[dev].store(c, std::memory_order_relaxed);
+  }
+  return c;
+}
+
+inline int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
 
 // Scratch of a long-row top-k: smax[q][sstride], the supergroup maxima (or
 // partial maxima) of row q.

@@ -539,15 +539,6 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
 }
 
 // ---------------------------------------------------------------- host side
-static int sm_count() {
-  static int counts[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return 148;
-  if (counts[dev] == 0) cudaDeviceGetAttribute(&counts[dev], cudaDevAttrMultiProcessorCount, dev);
-  return counts[dev] > 0 ? counts[dev] : 148;
-}
-
 cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
                                   const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
                                   const int32_t *n_vis, int n_q, const int32_t *pool, float *scores, int64_t stride,
@@ -573,15 +564,14 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
   const int64_t total_units = (int64_t)n_q * P.units_per_q;
   P.status = status;
   const size_t smem = (size_t)kScSmem + 1024;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  static bool attr_done[64] = {};
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
-  const int64_t grid = total_units < sm_count() ? total_units : sm_count();
+  const int dev = current_device();
+  static std::atomic<int> attr_done[kMaxDevices];
+  const cudaError_t e = once_per_device(attr_done, dev, [&] {
+    return cudaFuncSetAttribute(index_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (e != cudaSuccess) return e;
+  const int n_sm = device_sm_count(dev);
+  const int64_t grid = total_units < n_sm ? total_units : n_sm;
   return launch_pdl(index_score_tc_kernel, dim3((unsigned)grid), dim3(kScThreads), smem, st, 1u, P);
 }
 

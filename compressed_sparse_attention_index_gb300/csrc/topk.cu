@@ -1036,23 +1036,21 @@ static size_t collect_smem_bytes() {
 // of clusters would double the kernel's time).  Sets the kernel's attributes
 // on first use on a device.
 static unsigned collect_ctas(int dev, int n_q, int64_t n_items) {
-  static int fit[64][kMaxCluster + 1];                // resident clusters of each size (-1: unknown)
-  static int sms[64] = {};
-  static bool init[64] = {};
-  if (dev < 0 || dev >= 64) return 1;
+  static std::atomic<int> fit[kMaxDevices][kMaxCluster + 1];   // resident clusters of each size + 1 (0: unknown)
+  static std::atomic<int> attr_done[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return 1;
   const size_t dsm = collect_smem_bytes();
-  if (!init[dev]) {
+  once_per_device(attr_done, dev, [&] {
     cudaFuncSetAttribute(topk_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm);
     cudaFuncSetAttribute(topk_collect_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaGetLastError();                                // a refused attribute leaves no error behind
-    cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    for (int c = 0; c <= kMaxCluster; c++) fit[dev][c] = -1;
-    init[dev] = true;
-  }
-  const int m = sms[dev] > 0 ? sms[dev] : 148;
+    return cudaSuccess;
+  });
+  const int m = device_sm_count(dev);
   int p = (int)std::min<int64_t>(std::min<int64_t>(m / std::max(n_q, 1), n_items / 4096), kMaxCluster);
   for (; p > 1; p--) {
-    if (fit[dev][p] < 0) {
+    int f = fit[dev][p].load(std::memory_order_relaxed);
+    if (f == 0) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(p, 1);
       cfg.blockDim = dim3(kCollectThreads);
@@ -1067,9 +1065,10 @@ static unsigned collect_ctas(int dev, int n_q, int64_t n_items) {
       int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, topk_collect_kernel, &cfg) != cudaSuccess) n = 0;
       cudaGetLastError();
-      fit[dev][p] = n;
+      f = n + 1;
+      fit[dev][p].store(f, std::memory_order_relaxed);
     }
-    if (fit[dev][p] >= n_q) break;
+    if (f - 1 >= n_q) break;
   }
   return (unsigned)std::max(p, 1);
 }
@@ -1089,13 +1088,12 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
   S.n_seq = 0;
   const size_t dsm_direct = (size_t)kDirectCap * 8 + (size_t)kMaxK * 4 + 32 * 256 * 4 + (size_t)kCandCap * 4;
   const size_t dsm_collect = collect_smem_bytes();
-  int dev = 0;
-  cudaGetDevice(&dev);
-  static bool attr_done[64] = {};
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaFuncSetAttribute(topk_direct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm_direct);
-    attr_done[dev] = true;
-  }
+  const int dev = current_device();
+  static std::atomic<int> attr_done[kMaxDevices];
+  const cudaError_t ea = once_per_device(attr_done, dev, [&] {
+    return cudaFuncSetAttribute(topk_direct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm_direct);
+  });
+  if (ea != cudaSuccess) return ea;
   if (S.n_items <= kDirectCap)
     return launch_pdl(topk_direct_kernel, dim3(n_q), dim3(kTopkThreads), dsm_direct, st, 1u, S, k, out, status);
   const int64_t sgi = long_row_sgi(S.n_items, k);
@@ -1143,9 +1141,7 @@ FusedTopk topk_fused_plan(void *ws, int n_q, int64_t n_max, int k) {
 
 int topk_fused_ctas(const FusedTopk &F, int n_q, int64_t n_max) {
   if (F.mode <= 0) return -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  return (int)collect_ctas(dev, n_q, n_max) * n_q;
+  return (int)collect_ctas(current_device(), n_q, n_max) * n_q;
 }
 
 size_t topk_fused_bytes(int n_q, int64_t n_max, int k) {
@@ -1170,9 +1166,7 @@ cudaError_t launch_topk_fused(const float *scores, int64_t stride, int n_q, cons
   S.q_seq = F.q_seq;
   S.n_seq = F.n_seq;
   const size_t dsm_collect = collect_smem_bytes();
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const unsigned P = collect_ctas(dev, n_q, n_max);
+  const unsigned P = collect_ctas(current_device(), n_q, n_max);
   return launch_pdl(topk_collect_kernel, dim3(P, n_q), dim3(kCollectThreads), dsm_collect, st, P, S, F.sgi, F.parts,
                     k, F.W, out, status);
 }

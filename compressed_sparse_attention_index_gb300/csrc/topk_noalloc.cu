@@ -17,15 +17,15 @@ static __device__ __align__(256) uint32_t g_topk_scratch[CSA2_TOPK_NOALLOC_SCRAT
 // per device with that device current (the host-side name of a __device__
 // array is not a device address).  nullptr if the lookup failed.
 static void *topk_scratch_ptr() {
-  static void *ptrs[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (ptrs[dev] == nullptr) {
-    void *p = nullptr;
+  static std::atomic<void *> ptrs[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  void *p = ptrs[dev].load(std::memory_order_relaxed);
+  if (p == nullptr) {
     if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess) return nullptr;
-    ptrs[dev] = p;
+    ptrs[dev].store(p, std::memory_order_relaxed);
   }
-  return ptrs[dev];
+  return p;
 }
 
 }  // namespace csa2

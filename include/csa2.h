@@ -230,7 +230,10 @@ csa2_status csa2_topk(const float *scores, int64_t score_stride, int n_q, const 
  *                swa_cap == 0.
  *   q_seq, pos   (device) int32 [n_q]: sequence id, RoPE position of the query.
  *   swa_first, swa_cnt  (device) int32 [n_q]: the window is ring slots
- *                (swa_first + t) % swa_cap, t < swa_cnt (swa_cnt <= 128).
+ *                (swa_first + t) % swa_cap, t < swa_cnt, with
+ *                0 <= swa_cnt <= min(128, swa_cap) and 0 <= swa_first < swa_cap
+ *                when swa_cnt > 0; a query breaking this (or with q_seq out of
+ *                range) records CSA2_ERR_BOUNDS and gets zeros.
  *   out          (device) [n_q][64][512], bf16 or fp32 per out_dtype.
  *   workspace    (device) >= csa2_workspace_size(CSA2_OP_SPARSE_ATTN, ..) bytes.
  */
@@ -286,8 +289,12 @@ csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t 
  * scratch it needs (rows longer than 16,384 items only: 4 bytes per group of
  * scores, 2,048 to 16,384 groups per row; for 1,048,576-entry rows and k = 512
  * that is 8 KiB per query) lives in one fixed device array of
- * CSA2_TOPK_NOALLOC_SCRATCH_BYTES (4 MiB) that every GPU which loads the
- * library holds until the process exits.  A call whose
+ * CSA2_TOPK_NOALLOC_SCRATCH_BYTES (4 MiB), held on each GPU until the process
+ * exits.  With CUDA's default lazy module loading the array is mapped on a
+ * device only when its module is first loaded there, i.e. by the first call
+ * of this function on that device: that first call grows the device
+ * footprint by the 4 MiB.  Callers that need a fixed footprint after start-up
+ * make one call on each device (any size) during start-up.  A call whose
  * scratch would exceed it returns CSA2_ERR_WORKSPACE and launches nothing (use
  * csa2_topk with a workspace instead).  The call allocates nothing and calls no
  * allocating routine.  The first call on a device looks up the array's device

@@ -15,6 +15,8 @@ Parity status per function (the pins are the ``-m "not gpu"`` tests):
   topk, pool_blocks         pinned (brute-force sort, superset invariant)
   sparse_attn               pinned (dense softmax attention, single-entry and
                             RoPE closed forms, shift invariance)
+  attn_f64                  pinned (RoPE shift invariance, position 0 = no
+                            rotation; sparse_attn is this on dequantised records)
   sparse_attn_lse           pinned (outputs of parts of a softmax's entries,
                             merged by their log-sum-exp, equal the whole)
 DeepSeek's own numerics are not published on the pages, so parity is pinned to
@@ -67,6 +69,7 @@ def lib():
             "orc_pool_blocks": (i32, [P, i64, i32, i32, P]),
             "orc_sparse_attn": (None, [P, P, i32, P, i32, i64, f64, f64, i32, i32, P]),
             "orc_sparse_attn_lse": (None, [P, P, i32, P, i32, i64, f64, f64, i32, i32, P, P]),
+            "orc_attn_f64": (None, [P, P, i32, i64, f64, f64, i32, i32, P, P]),
             "orc_kv_bytes": (i32, []), "orc_idx_bytes": (i32, []), "orc_swa_bytes": (i32, []),
         }
         for name, (res, args) in sig.items():
@@ -200,6 +203,20 @@ def sparse_attn_lse(q_bf16, kv_rows, swa_rows, pos, sm_scale=1.0 / np.sqrt(512.0
     lib().orc_sparse_attn_lse(_p(q), _p(kv), kv.shape[0], _p(sw), sw.shape[0], int(pos), float(sm_scale),
                               float(rope_base), rope_off, rope_dim, _p(out), _p(lse))
     return out, lse
+
+
+def attn_f64(q, k, pos, sm_scale=1.0 / np.sqrt(512.0), rope_base=10000.0, rope_off=448, rope_dim=64,
+             with_lse=False):
+    """The attention arithmetic of sparse_attn on fp64 inputs (no cache
+    records): q [64][512], k [n][512] (keys = values).  Returns out [64][512]
+    (and the per-head log-sum-exp when with_lse)."""
+    q = _c(q, np.float64).reshape(H, D)
+    k = _c(k, np.float64).reshape(-1, D)
+    out = np.zeros((H, D), np.float64)
+    lse = np.zeros(H, np.float64)
+    lib().orc_attn_f64(_p(q), _p(k), k.shape[0], int(pos), float(sm_scale), float(rope_base), rope_off, rope_dim,
+                       _p(out), _p(lse))
+    return (out, lse) if with_lse else out
 
 
 from .compose import *  # noqa: E402,F401,F403  (workload-level compositions)

@@ -22,7 +22,7 @@ import numpy as np
 from gen.workloads import Workload, TOPK, SWA, BLOCK, POOL_BLOCKS
 
 __all__ = ["packed_keys", "kv_records", "swa_records", "query_inputs", "decode_query",
-           "full_scores", "reindex_query"]
+           "full_scores", "reindex_query", "reindex_on_pool"]
 
 
 def _o():
@@ -107,19 +107,30 @@ def decode_query(wl: Workload, qi: int, k: int = TOPK) -> dict:
     return {"scores": s, "sel": sel, "out": _attend(wl, qi, sel)}
 
 
-def reindex_query(wl: Workload, qi: int, k: int = TOPK) -> dict:
-    """Reindex-layer decode of query qi: Full-layer scores -> 2,048-block pool ->
-    Reindex scores over the pool's positions -> top-k -> attention."""
+def reindex_on_pool(wl: Workload, qi: int, blocks, k: int = TOPK) -> dict:
+    """The Reindex layer's own step for query qi over a given pool of 8-entry
+    blocks (block ids, -1 = none): its indexer query scores the pool's visible
+    positions, and the top-k of those scores (lower position first on ties,
+    positions ascending) is the selection."""
     o = _o()
     seq, n = int(wl.q_seq()[qi]), int(wl.n_vis()[qi])
-    s_full = full_scores(wl, qi)
-    blocks = o.pool_blocks(s_full, BLOCK, POOL_BLOCKS)
-    vb = blocks[blocks >= 0].astype(np.int64)
+    blocks = np.asarray(blocks)
+    vb = np.sort(blocks[blocks >= 0].astype(np.int64))
     pos = (vb[:, None] * BLOCK + np.arange(BLOCK)[None, :]).reshape(-1)
     pos = pos[pos < n]
     qidx, w = query_inputs(wl, qi, reindex=True)
     s_pool = o.index_score(packed_keys(wl, seq, n)[pos], qidx, w)
     loc = o.topk(s_pool, k)
     sel = np.where(loc >= 0, pos[np.maximum(loc, 0)], -1).astype(np.int32)
-    return {"scores_full": s_full, "blocks": blocks, "pool_pos": pos, "scores_pool": s_pool,
-            "sel": sel, "out": _attend(wl, qi, sel)}
+    return {"pool_pos": pos, "scores_pool": s_pool, "sel": sel}
+
+
+def reindex_query(wl: Workload, qi: int, k: int = TOPK) -> dict:
+    """Reindex-layer decode of query qi: Full-layer scores -> 2,048-block pool ->
+    Reindex scores over the pool's positions -> top-k -> attention."""
+    o = _o()
+    s_full = full_scores(wl, qi)
+    blocks = o.pool_blocks(s_full, BLOCK, POOL_BLOCKS)
+    r = reindex_on_pool(wl, qi, blocks, k)
+    return {"scores_full": s_full, "blocks": blocks, "pool_pos": r["pool_pos"], "scores_pool": r["scores_pool"],
+            "sel": r["sel"], "out": _attend(wl, qi, r["sel"])}

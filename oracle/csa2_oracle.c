@@ -338,30 +338,24 @@ int orc_pool_blocks(const double *s, int64_t n, int block, int nb, int32_t *out)
 /* One query, all 64 heads [study: k = v, one 512-wide latent shared by all
  * heads; attention covers the SWA window and the 512 selected entries; RoPE
  * on 64 of 512 dims, un-rotated on the output]:
- *   l_i  = sm_scale * q_h . khat_i     over the selected entries and the SWA
- *                                      window (no dedup, no sink)
+ *   l_i  = sm_scale * q_h . k_i        over the n entries given (the selected
+ *                                      entries and the SWA window; no dedup,
+ *                                      no sink)
  *   p    = softmax(l)                  (fp64)
- *   o_h  = sum_i p_i khat_i            (values are the keys)
+ *   o_h  = sum_i p_i k_i               (values are the keys)
  *   then dims (rope_off + 2i, rope_off + 2i + 1), i < rope_dim/2, are rotated
  *   by -pos with theta_i = pos * rope_base^(-2i / rope_dim).
- * kv_rows: [n_sel][288] records of the selected entries, swa_rows: [n_swa][528].
- * q: [64][512] bf16.  out: [64][512]. */
-static void orc_sparse_attn_impl(const uint16_t *q, const uint8_t *kv_rows, int n_sel, const uint8_t *swa_rows,
-                                 int n_swa, int64_t pos, double sm_scale, double rope_base, int rope_off,
-                                 int rope_dim, double *out, double *lse) {
-    int n = n_sel + n_swa;
-    double *k = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * ORC_DIM);
-    for (int i = 0; i < n_sel; i++) orc_dequant_kv(kv_rows + (size_t)i * ORC_KV_BYTES, k + (size_t)i * ORC_DIM);
-    for (int i = 0; i < n_swa; i++)
-        orc_dequant_swa(swa_rows + (size_t)i * ORC_SWA_BYTES, k + (size_t)(n_sel + i) * ORC_DIM);
+ * q: [64][512], k: [n][512], both already in fp64 (dequantised).  out:
+ * [64][512]; lse (optional): [64], log sum_i exp(l_i), -inf when n == 0. */
+void orc_attn_f64(const double *q, const double *k, int n, int64_t pos, double sm_scale, double rope_base,
+                  int rope_off, int rope_dim, double *out, double *lse) {
 #pragma omp parallel for schedule(static)
     for (int h = 0; h < ORC_HEADS; h++) {
         double *o = out + (size_t)h * ORC_DIM;
+        const double *qh = q + (size_t)h * ORC_DIM;
         for (int c = 0; c < ORC_DIM; c++) o[c] = 0.0;
         if (lse) lse[h] = -INFINITY;
         if (n == 0) continue;
-        double qh[ORC_DIM];
-        for (int c = 0; c < ORC_DIM; c++) qh[c] = orc_bf16_value(q[h * ORC_DIM + c]);
         double *l = (double *)malloc(sizeof(double) * (size_t)n);
         double mx = -INFINITY;
         for (int i = 0; i < n; i++) {
@@ -386,6 +380,23 @@ static void orc_sparse_attn_impl(const uint16_t *q, const uint8_t *kv_rows, int 
             o[rope_off + 2 * i + 1] = -a * sn + b * cs;
         }
     }
+}
+
+/* The cache-record form: q [64][512] bf16, kv_rows [n_sel][288] records of the
+ * selected entries, swa_rows [n_swa][528]; dequantised (exactly, in fp64) and
+ * passed to orc_attn_f64 in that order. */
+static void orc_sparse_attn_impl(const uint16_t *q, const uint8_t *kv_rows, int n_sel, const uint8_t *swa_rows,
+                                 int n_swa, int64_t pos, double sm_scale, double rope_base, int rope_off,
+                                 int rope_dim, double *out, double *lse) {
+    int n = n_sel + n_swa;
+    double *k = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * ORC_DIM);
+    double *qd = (double *)malloc(sizeof(double) * ORC_HEADS * ORC_DIM);
+    for (int i = 0; i < n_sel; i++) orc_dequant_kv(kv_rows + (size_t)i * ORC_KV_BYTES, k + (size_t)i * ORC_DIM);
+    for (int i = 0; i < n_swa; i++)
+        orc_dequant_swa(swa_rows + (size_t)i * ORC_SWA_BYTES, k + (size_t)(n_sel + i) * ORC_DIM);
+    for (int i = 0; i < ORC_HEADS * ORC_DIM; i++) qd[i] = orc_bf16_value(q[i]);
+    orc_attn_f64(qd, k, n, pos, sm_scale, rope_base, rope_off, rope_dim, out, lse);
+    free(qd);
     free(k);
 }
 

@@ -196,6 +196,27 @@ def test_full_decode_config4_full_size_sampled(lib, oracle_lib):
     _check_full(lib, oracle_lib, wl, dw, _bufs(dw), [0, 7])
 
 
+def _check_reindex(lib, oracle_lib, wl, blocks, sel, out, qi):
+    """The pool (blocks of 8) against the oracle's under the near-tie rule on
+    block scores; the Reindex selection against the oracle's Reindex step run
+    on the GPU's own pool (so a legal near-tie swap of a pool block cannot hide
+    the selection from the check); the attention on the GPU's selection."""
+    from oracle.compose import kv_records, swa_records
+    r = oracle_lib.reindex_query(wl, qi)
+    n = int(wl.n_vis()[qi])
+    bscore = lambda b: max(r["scores_full"][8 * b:min(n, 8 * b + 8)])
+    check_selection(blocks, r["blocks"], None, pos_to_score=bscore)
+    rp = r if np.array_equal(blocks, r["blocks"]) else oracle_lib.reindex_on_pool(wl, qi, blocks)
+    pos_score = dict(zip(rp["pool_pos"].tolist(), rp["scores_pool"].tolist()))
+    check_selection(sel, rp["sel"], None, pos_to_score=lambda p: pos_score[p])
+    if out is not None:
+        seq = int(wl.q_seq()[qi])
+        ref = oracle_lib.sparse_attn(wl.q(qi), kv_records(wl, seq, sel[sel >= 0]),
+                                     swa_records(wl, seq, int(wl.swa_first()[qi]), int(wl.swa_cnt()[qi])),
+                                     int(wl.pos()[qi]))
+        assert row_norm_err(out, ref) <= ATTN_TOL_F32
+
+
 def test_reindex_decode_small(lib, oracle_lib):
     from compressed_sparse_attention_index_gb300 import decode
     wl = small(n_seq=2, n_entries=40_000, pool=True, seed=230)
@@ -204,36 +225,55 @@ def test_reindex_decode_small(lib, oracle_lib):
     decode.reindex_decode(dw, buf)
     blocks, sel, out = buf.blocks.cpu().numpy(), buf.sel.cpu().numpy(), buf.out.float().cpu().numpy()
     assert lib.csa2_get_device_status() == 0
-    from oracle.compose import kv_records, swa_records
     for qi in range(2):
-        r = oracle_lib.reindex_query(wl, qi)
-        bscore = lambda b: max(r["scores_full"][8 * b:min(40_000, 8 * b + 8)])
-        check_selection(blocks[qi], r["blocks"], None, pos_to_score=bscore)
-        if np.array_equal(blocks[qi], r["blocks"]):
-            pos_score = dict(zip(r["pool_pos"].tolist(), r["scores_pool"].tolist()))
-            check_selection(sel[qi], r["sel"], None, pos_to_score=lambda p: pos_score[p])
-        s = sel[qi][sel[qi] >= 0]
-        ref = oracle_lib.sparse_attn(wl.q(qi), kv_records(wl, qi, s),
-                                     swa_records(wl, qi, int(wl.swa_first()[qi]), int(wl.swa_cnt()[qi])),
-                                     int(wl.pos()[qi]))
-        assert row_norm_err(out[qi], ref) <= ATTN_TOL_F32
+        _check_reindex(lib, oracle_lib, wl, blocks[qi], sel[qi], out[qi], qi)
+
+
+def test_reindex_on_a_pool_with_near_ties_swapped(lib, oracle_lib):
+    """The Reindex step is checked on whatever pool it is given: here the
+    GPU's pool with its last-ranked block replaced by another one, as a legal
+    near-tie swap would, and the selection still matches the oracle's Reindex
+    step on that same pool."""
+    from compressed_sparse_attention_index_gb300 import decode
+    wl = small(n_seq=2, n_entries=40_000, pool=True, seed=231)
+    dw = _dw(wl)
+    buf = _bufs(dw, pool=True)
+    decode.reindex_decode(dw, buf)
+    blocks = buf.blocks.cpu().numpy()
+    r = oracle_lib.reindex_query(wl, 1)
+    s_full = r["scores_full"]
+    bs = np.array([s_full[8 * b:8 * b + 8].max() for b in blocks[1]])
+    outside = np.setdiff1d(np.arange(5000), blocks[1])
+    swapped = blocks[1].copy()
+    swapped[int(np.argmin(bs))] = outside[0]
+    swapped = np.sort(swapped)
+    buf.blocks[1].copy_(torch.from_numpy(swapped))
+    decode.reindex_decode(dw, buf, build_pool=False)
+    sel, out = buf.sel.cpu().numpy(), buf.out.float().cpu().numpy()
+    assert lib.csa2_get_device_status() == 0
+    rp = oracle_lib.reindex_on_pool(wl, 1, swapped)
+    pos_score = dict(zip(rp["pool_pos"].tolist(), rp["scores_pool"].tolist()))
+    check_selection(sel[1], rp["sel"], None, pos_to_score=lambda p: pos_score[p])
+    from oracle.compose import kv_records, swa_records
+    ref = oracle_lib.sparse_attn(wl.q(1), kv_records(wl, 1, sel[1][sel[1] >= 0]),
+                                 swa_records(wl, 1, int(wl.swa_first()[1]), int(wl.swa_cnt()[1])), int(wl.pos()[1]))
+    assert row_norm_err(out[1], ref) <= ATTN_TOL_F32
 
 
 def test_reindex_decode_config3_full_size_sampled(lib, oracle_lib):
+    """64 x 1,048,576 Reindex decode: the pool, the Reindex selection and the
+    attention output (64 queries: the split plan with several chunks per CTA,
+    FP4-only chunks in f16 beside the window's chunk in bf16) for sampled
+    queries."""
     from compressed_sparse_attention_index_gb300 import decode
     wl = CONFIGS[3]
     dw = _dw(wl)
     buf = _bufs(dw, pool=True)
     decode.reindex_decode(dw, buf)
-    blocks, sel = buf.blocks.cpu().numpy(), buf.sel.cpu().numpy()
+    blocks, sel, out = buf.blocks.cpu().numpy(), buf.sel.cpu().numpy(), buf.out.float().cpu().numpy()
     assert lib.csa2_get_device_status() == 0
-    r = oracle_lib.reindex_query(wl, 5)
-    n = wl.n_entries
-    bscore = lambda b: max(r["scores_full"][8 * b:min(n, 8 * b + 8)])
-    check_selection(blocks[5], r["blocks"], None, pos_to_score=bscore)
-    if np.array_equal(blocks[5], r["blocks"]):
-        pos_score = dict(zip(r["pool_pos"].tolist(), r["scores_pool"].tolist()))
-        check_selection(sel[5], r["sel"], None, pos_to_score=lambda p: pos_score[p])
+    for qi in (5, 63):
+        _check_reindex(lib, oracle_lib, wl, blocks[qi], sel[qi], out[qi], qi)
 
 
 def test_prefill_m2_config2_sampled(lib, oracle_lib):
@@ -299,3 +339,30 @@ def test_fused_decode_equals_call_chain(lib, case):
     assert lib.csa2_get_device_status() == 0
     assert torch.equal(chain.sel, fused.sel)
     assert torch.equal(chain.out.view(torch.int32), fused.out.view(torch.int32))
+
+
+def test_window_longer_than_ring_is_rejected(lib, oracle_lib):
+    """A window count above the ring's capacity would wrap the ring and attend
+    to some window entries twice: the query is skipped (zeros) and reported,
+    while a query whose window fits the ring is served as usual."""
+    import compressed_sparse_attention_index_gb300 as C
+    wl = small(n_seq=2, n_entries=1000, seed=242)
+    dw = _dw(wl)
+    cap = 64
+    swa = dw.swa[:, :cap].contiguous()                  # a 64-slot ring
+    sel = np.stack([oracle_lib.decode_query(wl, qi)["sel"] for qi in range(2)])
+    swa_first = torch.tensor([0, 5], dtype=torch.int32, device="cuda")
+    swa_cnt = torch.tensor([128, 64], dtype=torch.int32, device="cuda")    # query 0: 128 > 64
+    out = torch.full((2, 64, 512), 7.0, dtype=torch.float32, device="cuda")
+    ws_bytes = C.csa2_workspace_size(C.CSA2_OP_SPARSE_ATTN, 2, 512 + 128)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    C.csa2_sparse_attn(dw.q, dw.kv, dw.n_max, 2, torch.from_numpy(sel).cuda(), 512, swa, cap, dw.q_seq, dw.pos,
+                       swa_first, swa_cnt, 2, out, C.CSA2_OUT_F32, None, ws, ws_bytes)
+    assert lib.csa2_get_device_status() == 4            # CSA2_ERR_BOUNDS
+    got = out.cpu().numpy()
+    assert np.count_nonzero(got[0]) == 0
+    from oracle.compose import kv_records
+    ring = oracle_lib.pack_swa(wl.swa_rows(1, np.arange(cap)))
+    win = ring[(5 + np.arange(64)) % cap]
+    ref = oracle_lib.sparse_attn(wl.q(1), kv_records(wl, 1, sel[1][sel[1] >= 0]), win, int(wl.pos()[1]))
+    assert row_norm_err(got[1], ref) <= ATTN_TOL_F32

@@ -205,3 +205,29 @@ def test_prefill_visibility_recipe():
     nv, pos, f, c = wl.n_vis(), wl.pos(), wl.swa_first(), wl.swa_cnt()
     assert nv[0] == 0 and nv[1] == 1 and nv[2] == 1 and nv[3] == 2 and nv[8191] == 4096
     assert c[0] == 1 and c[127] == 128 and c[8191] == 128 and f[8191] == 8191 - 127 and f[5] == 0
+
+
+@pytest.mark.parametrize("pos,delta", [(0, 1), (1000, 37), (4095, 1_000_000), (1_048_575, 123_457)])
+def test_rope_shift_invariance_fp64(oracle_lib, pos, delta):
+    """RoPE's relative-position property, on unquantised fp64 data: rotating
+    the query and every key forward by delta (textbook RoPE on dims 448..511)
+    and moving the query to pos + delta leaves every logit unchanged, so after
+    the output is rotated back by -(pos + delta) it equals the unshifted result.
+    A wrong rotation direction, pairing or frequency fails this."""
+    rng = np.random.default_rng(pos + delta)
+    q = rng.standard_normal((64, 512))
+    k = rng.standard_normal((200, 512))
+    base = oracle_lib.attn_f64(q, k, pos)
+    shifted = oracle_lib.attn_f64(_rope_forward(q, delta), _rope_forward(k, delta), pos + delta)
+    assert np.allclose(shifted, base, rtol=0, atol=1e-9 * np.abs(base).max())
+    # the rotation matters: shifting only the keys changes the output
+    other = oracle_lib.attn_f64(q, _rope_forward(k, delta), pos + delta)
+    assert np.abs(other - base).max() > 1e-6 * np.abs(base).max()
+
+
+def test_attn_f64_is_sparse_attn_on_dequantised_records(oracle_lib):
+    q, kv, sw = _attn_inputs(oracle_lib, 52, 90, 30)
+    K = np.concatenate([_decode_kv_np(kv), _decode_swa_np(sw)], axis=0)
+    a = oracle_lib.sparse_attn(q, kv, sw, 321)
+    b = oracle_lib.attn_f64(G.bf16_bits_to_f32(q).astype(np.float64), K, 321)
+    assert np.array_equal(a, b)
