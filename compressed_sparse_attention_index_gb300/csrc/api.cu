@@ -44,9 +44,8 @@ static csa2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA2_OK 
 
 static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
-// csa2_decode's workspace: scores [n_q][n_max] fp32, then the top-k scratch,
-// then the attention scratch, each 256-B aligned.
-// scores | top-k scratch | attention partials
+// csa2_decode's workspace, each part 256-B aligned:
+// scores [n_q][n_max] fp32 | top-k scratch | attention partials
 static size_t decode_workspace_bytes(int n_q, int64_t n_max) {
   return round256((size_t)n_q * (size_t)n_max * 4) + round256(topk_fused_bytes(n_q, n_max, kTopK)) +
          round256(attn_workspace_bytes(n_q, kTopK));
@@ -238,12 +237,12 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
   F.kv = static_cast<const uint8_t *>(kv_cache);
   F.q_seq = q_seq;
   F.n_seq = n_seq;
+  F.reserve = attn_ctas(n_q, kTopK);
   const bool fused = F.mode > 0;
   cudaError_t e = launch_index_score_tc(static_cast<const uint8_t *>(key_nib), static_cast<const uint8_t *>(key_scale),
                                         n_max, n_seq, static_cast<const uint8_t *>(q_nib),
                                         static_cast<const uint8_t *>(q_scale), w, q_seq, n_vis, n_q, nullptr, scores,
-                                        n_max, st, s, fused ? F.W.smax : nullptr, fused ? F.W.sstride : 0,
-                                        fused ? F.mode : 0);
+                                        n_max, st, s, fused ? &F.W : nullptr, fused ? F.mode : 0);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
   e = launch_topk_fused(scores, n_max, n_q, n_vis, n_max, kTopK, F, sel, ws_topk, st, s);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;

@@ -98,13 +98,13 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t ch) { return r * 128u + ((ch ^ (r & 7u)) << 4); }
 
 // kind::f16 instruction descriptor: bf16 x bf16 (or f16 x f16) -> f32, M=128,
-// N=64, A K- or MN-major.
-__host__ __device__ constexpr uint32_t idesc_m128n64(uint32_t a_mn_major, bool f16) {
+// N = n (a multiple of 16), A K- or MN-major.
+__host__ __device__ constexpr uint32_t idesc_m128(uint32_t a_mn_major, bool f16, uint32_t n) {
   return (1u << 4)                     // D format f32
          | ((f16 ? 0u : 1u) << 7)      // A: f16 0, bf16 1
          | ((f16 ? 0u : 1u) << 10)     // B: f16 0, bf16 1
          | (a_mn_major << 15)          // A major-ness
-         | ((64u >> 3) << 17)          // N / 8
+         | ((n >> 3) << 17)            // N / 8
          | ((128u >> 4) << 24);        // M / 16
 }
 
@@ -143,6 +143,7 @@ struct AttnTcArgs {
   float scale_log2;
   double inv_freq[kRopeDim / 2];   // rope_base^(-2i/64)
   int nsplit, chunks_per_split;
+  int hsplit;       // CTAs sharing a chunk, each with 64 / hsplit of the heads
   float *part;      // [n_q][nsplit][64][512]: unnormalised O
   float *part_ml;   // [n_q][nsplit][2][64]
   int *status;
@@ -161,7 +162,13 @@ __device__ __forceinline__ void rope_cs(double inv_freq, int pos, float &c, floa
   sincosf((float)r, &s, &c);
 }
 
+// NH: the heads one CTA handles (64, or 32 when two CTAs share each chunk:
+// the gather is repeated, the MMAs, the softmax and the read-out are halved).
+template <int NH>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
+  static_assert(NH == 64 || NH == 32, "heads per CTA");
+  constexpr int HS = kHeads / NH;                 // CTAs per chunk
+  constexpr int HW = NH / 2;                      // heads per softmax warp (two warps per TMEM lane quarter)
   extern __shared__ __align__(1024) unsigned char at_smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(at_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -175,9 +182,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   volatile int &bad_sh = *reinterpret_cast<volatile int *>(sm + kSmBars + 24);
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  // grid (n_q, nsplit), the last split first: the window-only chunks, which
-  // need no selection, are the first CTAs to be placed
-  const int qi = blockIdx.x, split = A.nsplit - 1 - (int)blockIdx.y;
+  // grid (n_q, nsplit x HS), the last split first: the window-only chunks,
+  // which need no selection, are the first CTAs to be placed; heads [h0, h0 + NH)
+  const int qi = blockIdx.x, split = A.nsplit - 1 - (int)blockIdx.y / HS, h0 = ((int)blockIdx.y % HS) * NH;
   // The selection (sel) comes from the grid ahead.  With settled inputs the
   // wait is put off until the first chunk that holds selected entries: Q is
   // staged and window-only chunks run while the selection finishes.  (TMEM is
@@ -193,7 +200,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   const int swa_cnt = __ldg(A.swa_cnt + qi), swa_first = __ldg(A.swa_first + qi);
   const bool bad = seq < 0 || seq >= A.n_seq || swa_cnt < 0 || swa_cnt > kSwa || swa_cnt > A.swa_cap ||
                    (swa_cnt > 0 && (swa_first < 0 || swa_first >= A.swa_cap));
-  if (bad && t == 0 && split == 0) record_error(A.status, CSA2_ERR_BOUNDS);
+  if (bad && t == 0 && split == 0 && h0 == 0) record_error(A.status, CSA2_ERR_BOUNDS);
   const int n_slots = A.sel_stride + (bad ? 0 : swa_cnt);
   const int c0 = split * A.chunks_per_split;
   const int c1 = bad ? c0 : min((n_slots + kTcChunk - 1) / kTcChunk, c0 + A.chunks_per_split);
@@ -205,7 +212,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     ptx::fence_mbar_init();
   }
   if (warp == 0) ptx::tmem_alloc(&tmem_sh, kAttTmemCols);
-  if (t < kHeads) m_ref[t] = -INFINITY;
+  if (t < NH) m_ref[t] = -INFINITY;
   // start the first chunk's record reads (L2 prefetch) while Q is staged
   if (waited && c0 < c1) {
     const int e = t >> 1, half = t & 1, slot = c0 * kTcChunk + e;
@@ -230,16 +237,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   // below 2^-24 of that range, and folded back into the softmax scale.
   // Returns 2^qs.
   __shared__ uint32_t qmax_sh[kTcThreads / 32];
+  constexpr int kQv = NH * kDim / 8 / kTcThreads;    // 16-B loads per thread
   auto stage_q = [&](bool f16) -> float {
-    const uint4 *src = reinterpret_cast<const uint4 *>(A.q + (int64_t)qi * kHeads * kDim);
-    uint4 qv[kHeads * kDim / 8 / kTcThreads];        // all 16 loads in flight before any store
+    const uint4 *src = reinterpret_cast<const uint4 *>(A.q + ((int64_t)qi * kHeads + h0) * kDim);
+    uint4 qv[kQv];                                   // all loads in flight before any store
 #pragma unroll
-    for (int j = 0; j < kHeads * kDim / 8 / kTcThreads; j++) qv[j] = __ldg(src + t + j * kTcThreads);
+    for (int j = 0; j < kQv; j++) qv[j] = __ldg(src + t + j * kTcThreads);
     float qscale = 1.f;
     if (f16) {
       uint32_t m = 0u;                               // max |q| as bf16 bits, two lanes per word
 #pragma unroll
-      for (int j = 0; j < kHeads * kDim / 8 / kTcThreads; j++) {
+      for (int j = 0; j < kQv; j++) {
         m = __vmaxu2(m, qv[j].x & 0x7FFF7FFFu);
         m = __vmaxu2(m, qv[j].y & 0x7FFF7FFFu);
         m = __vmaxu2(m, qv[j].z & 0x7FFF7FFFu);
@@ -256,7 +264,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       qscale = ldexpf(1.f, qs);
       const float inv = ldexpf(1.f, -qs);
 #pragma unroll
-      for (int j = 0; j < kHeads * kDim / 8 / kTcThreads; j++) {
+      for (int j = 0; j < kQv; j++) {
         uint32_t wd[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
 #pragma unroll
         for (int k = 0; k < 4; k++) {
@@ -267,7 +275,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       }
     }
 #pragma unroll
-    for (int j = 0; j < kHeads * kDim / 8 / kTcThreads; j++) {
+    for (int j = 0; j < kQv; j++) {
       const int i = t + j * kTcThreads;
       const int h = i >> 6, ch = i & 63;               // 16-B chunk ch of row h (8 dims)
       const uint32_t off = (h >> 3) * 8192 + (ch >> 3) * 1024 + sw128(h & 7, ch & 7);
@@ -316,7 +324,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       ptx::fence_proxy_async_smem();
       __syncthreads();
     }
-    const uint32_t id_qk = idesc_m128n64(0, f16c), id_pv = idesc_m128n64(1, f16c);
+    const uint32_t id_qk = idesc_m128(0, f16c, NH), id_pv = idesc_m128(1, f16c, NH);
     const float sl2 = A.scale_log2 * (f16c ? qscale : 1.f);   // S was computed with Q x 2^-qs
     // ---------------------------------------------------------- gather + dequantise
     {
@@ -325,7 +333,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       const uint32_t rowbase = (e >> 3) * 8192;        // 8-entry group
       int ok = 0;
       if (slot < A.sel_stride) {
-        const int j = wp ? ((int64_t)e < A.n_max ? e : -1) : __ldg(A.sel + (int64_t)qi * A.sel_stride + slot);
+        const int j = wp ? ((int64_t)e < A.n_max ? e : -1) : __ldcg(A.sel + (int64_t)qi * A.sel_stride + slot);
         if (j >= 0 && (int64_t)j < A.n_max) {
           ok = 1;
           const uint8_t *rec = A.kv + ((int64_t)seq * A.n_max + j) * kKvBytes;
@@ -448,31 +456,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     }
     // ---------------------------------------------------------- softmax (all 8 warps)
     int need_rescale = 0;
-    // warp w: TMEM lane quarter w%4 (entries 32*(w%4) ..), heads 32*(w/4) .. +31
+    // warp w: TMEM lane quarter w%4 (entries 32*(w%4) ..), heads HW*(w/4) .. +HW-1
     {
-      const int quarter = warp & 3, hb = (warp >> 2) * 32;
+      const int quarter = warp & 3, hb = (warp >> 2) * HW;
       if (!ptx::mbar_wait(&bar_s, phase)) { record_error(A.status, CSA2_ERR_TIMEOUT); bad_sh = 1; }
       ptx::tc_fence_after();
       const int e = quarter * 32 + lane;               // TMEM lane = entry
       const uint32_t s_addr = tmem + ((uint32_t)(quarter * 32) << 16) + kColS + hb;
       const bool ev = valid_sh[e] != 0;
-      // per-head max over the warp's 32 entries: transpose-reduce in 31
-      // shuffles; afterwards lane L holds the max of head hb + L
-      float v[32];
-      {
-        uint32_t r[32], r2[32];
-        ptx::tmem_ld_32x32b_x32(s_addr, r);
-        ptx::tmem_ld_32x32b_x32(s_addr + (kColS2 - kColS), r2);
-        ptx::tmem_wait_ld();
+      // S (two K halves, summed) for this warp's HW heads
+      auto load_s = [&](float (&x)[HW]) {
+        if constexpr (HW == 32) {
+          uint32_t r[32], r2[32];
+          ptx::tmem_ld_32x32b_x32(s_addr, r);
+          ptx::tmem_ld_32x32b_x32(s_addr + (kColS2 - kColS), r2);
+          ptx::tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; h++)
-          v[h] = ev ? (__uint_as_float(r[h]) + __uint_as_float(r2[h])) * sl2 : -INFINITY;
-      }
+          for (int h = 0; h < 32; h++) x[h] = (__uint_as_float(r[h]) + __uint_as_float(r2[h])) * sl2;
+        } else {
+          uint32_t r[16], r2[16];
+          ptx::tmem_ld_32x32b_x16(s_addr, r);
+          ptx::tmem_ld_32x32b_x16(s_addr + (kColS2 - kColS), r2);
+          ptx::tmem_wait_ld();
 #pragma unroll
-      for (int w = 16; w >= 1; w >>= 1) {              // w = values kept, partner distance w
+          for (int h = 0; h < 16; h++) x[h] = (__uint_as_float(r[h]) + __uint_as_float(r2[h])) * sl2;
+        }
+      };
+      // per-head max over the warp's 32 entries: transpose-reduce (HW - 1
+      // shuffles, one more when HW = 16); afterwards lane L holds the max of
+      // head hb + L % HW
+      float v[HW];
+      load_s(v);
+#pragma unroll
+      for (int h = 0; h < HW; h++) v[h] = ev ? v[h] : -INFINITY;
+#pragma unroll
+      for (int w = HW / 2; w >= 1; w >>= 1) {          // w = values kept, partner distance w
         const bool upper = (lane & w) != 0;
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
+        for (int i = 0; i < HW / 2; i++) {
           if (i < w) {
             const float mine = upper ? v[i + w] : v[i];
             const float send = upper ? v[i] : v[i + w];
@@ -480,10 +501,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
           }
         }
       }
-      red[quarter][hb + lane] = v[0];
+      if (HW == 16) v[0] = fmaxf(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], 16));
+      red[quarter][hb + (lane & (HW - 1))] = v[0];
       __syncthreads();
       int rs = 0;                                      // some head's accumulators need rescaling
-      if (t < kHeads) {
+      if (t < NH) {
         const float cm = fmaxf(fmaxf(red[0][t], red[1][t]), fmaxf(red[2][t], red[3][t]));
         const float mo = m_ref[t];
         float al = 1.f;
@@ -499,10 +521,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       // S is read from TMEM again rather than kept live through the reduction
       const uint32_t pe = (e >> 6) * 1024;             // entry atom
       const uint32_t pcol = (uint32_t)(e & 63) * 2;    // byte within the 128-B row
-      uint32_t r[32], r2[32];
-      ptx::tmem_ld_32x32b_x32(s_addr, r);
-      ptx::tmem_ld_32x32b_x32(s_addr + (kColS2 - kColS), r2);
-      ptx::tmem_wait_ld();
+      float l2v[HW];
+      load_s(l2v);
       // f16 chunks: the numerator rounded to f16 (11 significant bits); bf16
       // chunks: bf16 hi + lo parts (~16 bits).  One loop per type.
       auto off_of = [&](int i) {
@@ -516,16 +536,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       };
       if (f16c) {
 #pragma unroll
-        for (int i = 0; i < 32; i++) {
-          const float l2 = (__uint_as_float(r[i]) + __uint_as_float(r2[i])) * sl2;
-          const float p = ev ? exp2f(l2 - m_ref[hb + i]) : 0.f;
+        for (int i = 0; i < HW; i++) {
+          const float p = ev ? exp2f(l2v[i] - m_ref[hb + i]) : 0.f;
           *reinterpret_cast<__half *>(sm + kSmPhi + off_of(i)) = __float2half_rn(p);
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; i++) {
-          const float l2 = (__uint_as_float(r[i]) + __uint_as_float(r2[i])) * sl2;
-          const float p = ev ? exp2f(l2 - m_ref[hb + i]) : 0.f;
+        for (int i = 0; i < HW; i++) {
+          const float p = ev ? exp2f(l2v[i] - m_ref[hb + i]) : 0.f;
           const __nv_bfloat16 ph = __float2bfloat16_rn(p);
           put(i, __bfloat16_as_ushort(ph), __bfloat16_as_ushort(__float2bfloat16_rn(p - __bfloat162float(ph))));
         }
@@ -541,9 +559,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       const int quarter = warp & 3;
       for (int blk = warp >> 2; blk < 5; blk += 2) {
         if (blk == 4 && warp >= 4) break;
-        for (int half = 0; half < 2; half++) {
+        for (int half = 0; half < NH / 32; half++) {
           uint32_t r[32];
-          const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + kColO + blk * 64 + half * 32;
+          const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + kColO + blk * NH + half * 32;
           ptx::tmem_ld_32x32b_x32(ta, r);
           ptx::tmem_wait_ld();
 #pragma unroll
@@ -570,12 +588,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
         if (mb < 4) {
           // Vhat^T block: dims [128 mb, 128 mb + 128), entries [16 ks, 16 ks + 16), MN-major
           const uint64_t ad = ptx::smem_desc(sK + (2 * ks) * 8192 + (2 * mb) * 1024, 1024, 8192, 2);
-          ptx::tc_mma_bf16(tmem + kColO + mb * 64, ad, bhi, id_pv, acc0);
-          if (!f16c) ptx::tc_mma_bf16(tmem + kColO + mb * 64, ad, blo, id_pv, 1u);
+          ptx::tc_mma_bf16(tmem + kColO + mb * NH, ad, bhi, id_pv, acc0);
+          if (!f16c) ptx::tc_mma_bf16(tmem + kColO + mb * NH, ad, blo, id_pv, 1u);
         } else {
           const uint64_t ones = ptx::smem_desc(f16c ? sOnes16 : sOnes, 0, 0, 0);
-          ptx::tc_mma_bf16(tmem + kColO + 4 * 64, ones, bhi, id_qk, acc0);
-          if (!f16c) ptx::tc_mma_bf16(tmem + kColO + 4 * 64, ones, blo, id_qk, 1u);
+          ptx::tc_mma_bf16(tmem + kColO + 4 * NH, ones, bhi, id_qk, acc0);
+          if (!f16c) ptx::tc_mma_bf16(tmem + kColO + 4 * NH, ones, blo, id_qk, 1u);
         }
       }
       ptx::tc_commit(&bar_o);
@@ -584,7 +602,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     ptx::tc_fence_after();
     phase ^= 1;
     if (wp) {
-      if (t < kHeads) m_ref[t] = -INFINITY;           // the real pass starts afresh (any_chunk stays false)
+      if (t < NH) m_ref[t] = -INFINITY;               // the real pass starts afresh (any_chunk stays false)
     } else {
       any_chunk = true;
     }
@@ -606,11 +624,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       float rc = 1.f, rs = 0.f;                        // cos t, sin t of the pair holding d
       if (d >= kRopeOff && A.nsplit == 1) rope_cs(A.inv_freq[(d - kRopeOff) >> 1], pos, rc, rs);
 #pragma unroll
-      for (int half = 0; half < 2; half++) {
+      for (int half = 0; half < NH / 32; half++) {
         uint32_t r[32], lr[32];
         if (any_chunk) {
-          ptx::tmem_ld_32x32b_x32(lane_base + kColO + blk * 64 + half * 32, r);
-          ptx::tmem_ld_32x32b_x32(lane_base + kColO + 4 * 64 + half * 32, lr);
+          ptx::tmem_ld_32x32b_x32(lane_base + kColO + blk * NH + half * 32, r);
+          ptx::tmem_ld_32x32b_x32(lane_base + kColO + 4 * NH + half * 32, lr);
           ptx::tmem_wait_ld();
         } else {
 #pragma unroll
@@ -619,7 +637,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
         if (A.nsplit == 1) {
 #pragma unroll
           for (int i = 0; i < 32; i++) {
-            const int h = half * 32 + i;
+            const int h = h0 + half * 32 + i;
             const float l = __uint_as_float(lr[i]);
             float x = l > 0.f ? __uint_as_float(r[i]) / l : 0.f;
             if (d >= kRopeOff) {
@@ -636,19 +654,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
           // partial O[head][dim]: for each head the warp writes one 128-B line
           float *P = A.part + ((int64_t)qi * A.nsplit + split) * kHeads * kDim;
 #pragma unroll
-          for (int i = 0; i < 32; i++) P[(half * 32 + i) * kDim + d] = __uint_as_float(r[i]);
+          for (int i = 0; i < 32; i++) P[(h0 + half * 32 + i) * kDim + d] = __uint_as_float(r[i]);
           if (blk == (warp >> 2) && quarter == 0 && lane == 0 && warp < 4) {
             float *ml = A.part_ml + ((int64_t)qi * A.nsplit + split) * 2 * kHeads;
 #pragma unroll
-            for (int i = 0; i < 32; i++) ml[kHeads + half * 32 + i] = __uint_as_float(lr[i]);
+            for (int i = 0; i < 32; i++) ml[kHeads + h0 + half * 32 + i] = __uint_as_float(lr[i]);
           }
         }
       }
     }
-    if (A.nsplit > 1 && t < kHeads) {
+    if (A.nsplit > 1 && t < NH) {
       // (the denominators, replicated over all 128 lanes, were written by lane 0 of warp 0)
       float *ml = A.part_ml + ((int64_t)qi * A.nsplit + split) * 2 * kHeads;
-      ml[t] = any_chunk ? m_ref[t] : -INFINITY;
+      ml[h0 + t] = any_chunk ? m_ref[t] : -INFINITY;
     }
   }
   ptx::tc_fence_before();
@@ -684,10 +702,10 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(AttnTcArgs A) {
   for (int s = 0; s < kMaxSplit; s++) {
     if (s < ns) {
       const float4 *src = reinterpret_cast<const float4 *>(A.part + (((int64_t)qi * ns + s) * kHeads + h) * kDim + d);
-      v[s][0] = src[0];
-      v[s][1] = src[1];
-      m[s] = ml[s * 2 * kHeads + h];
-      l[s] = ml[s * 2 * kHeads + kHeads + h];
+      v[s][0] = __ldcg(src);
+      v[s][1] = __ldcg(src + 1);
+      m[s] = __ldcg(ml + s * 2 * kHeads + h);
+      l[s] = __ldcg(ml + s * 2 * kHeads + kHeads + h);
     }
   }
   float M = -INFINITY;
@@ -740,15 +758,24 @@ static int attn_chunks(int sel_stride) { return (sel_stride + kSwa + kTcChunk - 
 // while the selection finishes); else contiguous runs of chunks, at least one
 // CTA per query.
 struct AttnPlan {
-  int nsplit, cps;
+  int nsplit, cps, hs;   // splits of a query's chunks, chunks per split, CTAs per chunk (head halves)
 };
 static AttnPlan attn_plan(int n_q, int sel_stride, int n_sm) {
   const int chunks = attn_chunks(sel_stride);
   const int sel_ch = (sel_stride + kTcChunk - 1) / kTcChunk;
-  if (n_q * sel_ch <= n_sm) return AttnPlan{chunks, 1};
+  if (n_q * sel_ch <= n_sm) {
+    // one chunk per CTA; two CTAs per chunk (32 heads each) while all of them
+    // fit one wave: the gather is repeated, the rest of the chunk is halved
+    return AttnPlan{chunks, 1, n_q * chunks * 2 <= n_sm ? 2 : 1};
+  }
   const int ns = std::max(1, std::min(chunks, n_sm / n_q));
   const int cps = (chunks + ns - 1) / ns;
-  return AttnPlan{(chunks + cps - 1) / cps, cps};
+  return AttnPlan{(chunks + cps - 1) / cps, cps, 1};
+}
+
+int attn_ctas(int n_q, int sel_stride) {
+  const AttnPlan p = attn_plan(n_q, sel_stride, device_sm_count(current_device()));
+  return n_q * p.nsplit * p.hs;
 }
 
 size_t attn_workspace_bytes(int n_q, int sel_stride) {
@@ -785,17 +812,23 @@ cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_s
   const AttnPlan plan = attn_plan(n_q, sel_stride, n_sm);
   A.nsplit = plan.nsplit;
   A.chunks_per_split = plan.cps;
+  A.hsplit = plan.hs;
   A.part = static_cast<float *>(ws);
   A.part_ml = A.part + (size_t)n_q * A.nsplit * kHeads * kDim;
   A.status = status;
   static std::atomic<int> attr_done[kMaxDevices];
   cudaError_t e = once_per_device(attr_done, dev, [&] {
-    return cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+    cudaError_t e1 = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+    cudaError_t e2 = cudaFuncSetAttribute(attn_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+    return e1 != cudaSuccess ? e1 : e2;
   });
   if (e != cudaSuccess) return e;
   // the warm-up pays only where every CTA is resident while the grid ahead runs
-  A.warm = inputs_settled && plan.cps == 1 && ahead_ctas >= 0 && ahead_ctas + n_q * plan.nsplit <= n_sm ? 1 : 0;
-  e = launch_pdl(attn_tc_kernel, dim3(n_q, A.nsplit), dim3(kTcThreads), kSmAlloc, st, 1u, A);
+  const int n_ctas = n_q * plan.nsplit * plan.hs;
+  A.warm = inputs_settled && plan.cps == 1 && ahead_ctas >= 0 && ahead_ctas + n_ctas <= n_sm ? 1 : 0;
+  const dim3 grid(n_q, A.nsplit * plan.hs);
+  e = plan.hs == 2 ? launch_pdl(attn_tc_kernel<32>, grid, dim3(kTcThreads), kSmAlloc, st, 1u, A)
+                   : launch_pdl(attn_tc_kernel<64>, grid, dim3(kTcThreads), kSmAlloc, st, 1u, A);
   if (e != cudaSuccess || A.nsplit == 1) return e;
   return launch_pdl(attn_tc_merge_kernel, dim3(kDim / 32, n_q), dim3(256), 0, st, 1u, A);
 }

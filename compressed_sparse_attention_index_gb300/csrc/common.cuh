@@ -62,4 +62,5 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 // Iteration limit of a spin-wait on shared memory written by another warp.
 constexpr long long kSpinLimit = 1LL << 26;
 
+
 }  // namespace csa2

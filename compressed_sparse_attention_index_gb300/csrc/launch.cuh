@@ -53,6 +53,10 @@ inline int current_device() {
 struct LongRowWs {
   uint32_t *smax;
   int64_t sstride;
+  // optional (plain rows): the maxima of every 32 consecutive entries,
+  // gmax[q][gstride] (entry j in group j / 32), or null
+  uint32_t *gmax = nullptr;
+  int64_t gstride = 0;
 };
 
 // Launch `kern` with programmatic stream serialisation (the kernel calls
@@ -84,29 +88,33 @@ cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t sm
 }
 
 // Top-k plan of the fused decode: mode -1 one CTA per row (no scratch); 0 the
-// standalone passes; 1 / 2 the indexer's epilogue writes the maxima (512-entry
-// units as four partials / 32-entry groups) and only the collection runs.
+// standalone passes; 2 / 3 the indexer's epilogue writes the maxima (32-entry
+// groups / 512-entry units as four partials and their 32-entry groups) and
+// only the collection runs.
 struct FusedTopk {
   int mode;
   int64_t sgi;
   int parts;
   LongRowWs W;
   // optional: the latent cache [n_seq][n_max][288] and the queries' sequences,
-  // for an L2 prefetch of the selected records (modes 1 and 2)
+  // for an L2 prefetch of the selected records (modes 2 and 3)
   const uint8_t *kv;
   const int32_t *q_seq;
   int n_seq;
+  // SMs to leave to the grid that follows (the attention, whose CTAs are
+  // placed while the collection runs), when that still leaves the collection
+  // at least four CTAs per row
+  int reserve;
 };
 
 cudaError_t launch_pack(int kind, const void *src, int64_t rows, int m, const float *gate, void *dst,
                         void *dst_scales, cudaStream_t st);
 
-// smax / sstride / smax_mode: maxima for a fused top-k (smax_mode 0: none).
+// W / smax_mode: maxima for a fused top-k (smax_mode 0: none).
 cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
                                   const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
                                   const int32_t *n_vis, int n_q, const int32_t *pool, float *scores, int64_t stride,
-                                  int *status, cudaStream_t st, uint32_t *smax = nullptr, int64_t sstride = 0,
-                                  int smax_mode = 0);
+                                  int *status, cudaStream_t st, const LongRowWs *W = nullptr, int smax_mode = 0);
 
 size_t topk_workspace_bytes(int n_q, int64_t n_items, int k);
 bool topk_items_supported(int64_t n_items, int k);
@@ -121,6 +129,8 @@ cudaError_t launch_topk_fused(const float *scores, int64_t stride, int n_q, cons
 int topk_fused_ctas(const FusedTopk &F, int n_q, int64_t n_max);
 
 size_t attn_workspace_bytes(int n_q, int sel_stride);
+// CTAs of the attention grid (one per SM) for n_q queries
+int attn_ctas(int n_q, int sel_stride);
 // inputs_settled: q, the window cache and the per-query arrays were final
 // before the grid ahead of this one on the stream started (so inside
 // csa2_decode): the kernel then stages Q and runs its window-only chunks before

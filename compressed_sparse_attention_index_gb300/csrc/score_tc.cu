@@ -97,12 +97,15 @@ struct ScoreTcArgs {
   int units_per_q;
   int *status;
   // optional, Full mode only: maxima of the order keys of the scores, for the
-  // top-k that follows.  smax_mode 1: per work unit, four partial maxima (one
-  // per TMEM lane quarter, over its rows of the four sub-tiles) at
-  // smax[q * sstride + 4u + quarter]; smax_mode 2: per 32 consecutive entries
-  // at smax[q * sstride + entry / 32].  Invalid entries count as key 0.
+  // top-k that follows.  smax_mode 2: per 32 consecutive entries at
+  // smax[q * sstride + entry / 32]; smax_mode 3: per work unit u, four partial
+  // maxima (one per TMEM lane quarter, over its rows of the four sub-tiles) at
+  // smax[q * sstride + 4u + quarter], and per 32 consecutive entries at
+  // gmax[q * gstride + entry / 32].  Invalid entries count as key 0.
   uint32_t *smax;
   int64_t sstride;
+  uint32_t *gmax;
+  int64_t gstride;
   int smax_mode;
 };
 
@@ -486,7 +489,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         }
       };
       const int64_t i0 = (int64_t)cur_u * kUnit + row;
-      uint32_t umax = 0u;                             // smax_mode 1: this lane's maximum key
+      uint32_t umax = 0u;                             // smax_mode 3: the quarter's maximum key
 #pragma unroll 1
       for (int h2 = 0; h2 < kSub / 2; h2++) {         // two sub-tiles (64 columns) at a time
         uint32_t d0[32], d1[32];
@@ -510,24 +513,18 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
           // order keys of this lane's two entries (0 if not visible)
           const uint32_t k0 = i0 + h2 * 256 < sc.nv ? order_key(s0) : 0u;
           const uint32_t k1 = i0 + h2 * 256 + 128 < sc.nv ? order_key(s1) : 0u;
-          uint32_t *sm = P.smax + (int64_t)sc.q * P.sstride;
-          if (P.smax_mode == 2) {
-            // 32 consecutive entries per warp and sub-tile
-            const uint32_t g0 = __reduce_max_sync(0xFFFFFFFFu, k0), g1 = __reduce_max_sync(0xFFFFFFFFu, k1);
-            if (lane == 0) {
-              const int64_t e0 = (int64_t)cur_u * kUnit + h2 * 256 + quarter * 32;
-              sm[e0 >> 5] = g0;
-              sm[(e0 + 128) >> 5] = g1;
-            }
-          } else {
-            umax = max(umax, max(k0, k1));
+          // 32 consecutive entries per warp and sub-tile
+          uint32_t *gm = P.smax_mode == 2 ? P.smax + (int64_t)sc.q * P.sstride : P.gmax + (int64_t)sc.q * P.gstride;
+          const uint32_t g0 = __reduce_max_sync(0xFFFFFFFFu, k0), g1 = __reduce_max_sync(0xFFFFFFFFu, k1);
+          if (lane == 0) {
+            const int64_t e0 = (int64_t)cur_u * kUnit + h2 * 256 + quarter * 32;
+            gm[e0 >> 5] = g0;
+            gm[(e0 + 128) >> 5] = g1;
           }
+          umax = max(umax, max(g0, g1));
         }
       }
-      if (P.smax_mode == 1) {
-        umax = __reduce_max_sync(0xFFFFFFFFu, umax);
-        if (lane == 0) P.smax[(int64_t)sc.q * P.sstride + (int64_t)cur_u * 4 + quarter] = umax;
-      }
+      if (P.smax_mode == 3 && lane == 0) P.smax[(int64_t)sc.q * P.sstride + (int64_t)cur_u * 4 + quarter] = umax;
     }
   }
   ptx::tc_fence_before();
@@ -542,11 +539,14 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
 cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
                                   const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
                                   const int32_t *n_vis, int n_q, const int32_t *pool, float *scores, int64_t stride,
-                                  int *status, cudaStream_t st, uint32_t *smax, int64_t sstride, int smax_mode) {
+                                  int *status, cudaStream_t st, const LongRowWs *W, int smax_mode) {
   ScoreTcArgs P;
-  P.smax = smax;
-  P.sstride = sstride;
-  P.smax_mode = pool == nullptr ? smax_mode : 0;
+  P.smax = W ? W->smax : nullptr;
+  P.sstride = W ? W->sstride : 0;
+  P.gmax = W ? W->gmax : nullptr;
+  P.gstride = W ? W->gstride : 0;
+  P.smax_mode = pool == nullptr && W != nullptr && (smax_mode == 2 || (smax_mode == 3 && W->gmax != nullptr))
+                    ? smax_mode : 0;
   P.key_nib = key_nib;
   P.q_nib = q_nib;
   P.key_scale = key_scale;

@@ -382,6 +382,172 @@ struct BlockReduce {
   }
 };
 
+// Block-wide exclusive suffix sum of one value per thread (threads with a
+// larger index come first); *total receives the sum.  Two barriers.
+__device__ uint32_t block_excl_suffix(uint32_t c, uint32_t *total) {
+  __shared__ uint32_t wsum[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  uint32_t incl = c;                                 // inclusive suffix within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+    if (lane + o < 32) incl += v;
+  }
+  __syncthreads();                                   // an earlier call's readers are done with wsum
+  if (lane == 0) wsum[warp] = incl;
+  __syncthreads();
+  const uint32_t w = lane < nw ? wsum[lane] : 0u;
+  *total = __reduce_add_sync(0xFFFFFFFFu, w);
+  return __reduce_add_sync(0xFFFFFFFFu, lane > warp ? w : 0u) + incl - c;
+}
+
+constexpr int kWideBins = 4096;                      // 12-bit digits
+
+// Common-prefix split of the nonzero values v[0..n): the bits above the
+// highest bit where the largest and the smallest nonzero value differ are
+// shared by every nonzero value; the 12-bit digit just below them orders the
+// values.  Block-wide; every thread gets the same result.  Clears hist
+// (kWideBins counters) on the way (the first barrier orders it).
+struct WideDigit {
+  uint32_t prefix, pmask;
+  int sh;        // digit = (x >> sh) & 4095; -1: all nonzero values are equal (or none)
+  uint32_t mx;
+};
+template <class Get>
+__device__ WideDigit wide_digit(Get get, int n, uint32_t *hist) {
+  __shared__ uint32_t ext_sh[2][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  uint32_t mx = 0u, mn = ~0u;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint32_t x = get(i);
+    mx = max(mx, x);
+    if (x != 0u) mn = min(mn, x);
+  }
+  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+  mn = __reduce_min_sync(0xFFFFFFFFu, mn);
+  __syncthreads();                                   // an earlier call's readers are done with ext_sh
+  if (lane == 0) { ext_sh[0][warp] = mx; ext_sh[1][warp] = mn; }
+  for (int i = threadIdx.x; i < kWideBins; i += blockDim.x) hist[i] = 0u;
+  __syncthreads();
+  WideDigit d;
+  d.mx = __reduce_max_sync(0xFFFFFFFFu, lane < nw ? ext_sh[0][lane] : 0u);
+  mn = __reduce_min_sync(0xFFFFFFFFu, lane < nw ? ext_sh[1][lane] : ~0u);
+  const uint32_t diff = mn == ~0u ? 0u : (d.mx ^ mn);
+  const int hb = diff == 0u ? -1 : 31 - __clz(diff);
+  d.sh = hb < 0 ? -1 : max(hb - 11, 0);
+  d.pmask = hb < 0 ? ~0u : (hb >= 31 ? 0u : ~((2u << hb) - 1u));
+  d.prefix = d.mx & d.pmask;
+  return d;
+}
+
+// After the digits' histogram: the digit D that holds the rem-th largest
+// value (values in digits above D: *above < rem <= *above + hist[D]).  Four
+// bins per thread (blockDim.x * 4 == kWideBins).  Three barriers.
+__device__ int wide_find(const uint32_t *hist, int rem, uint32_t *above_out) {
+  __shared__ int d_sh;
+  __shared__ uint32_t a_sh;
+  const int b0 = threadIdx.x * 4;
+  const uint32_t c0 = hist[b0], c1 = hist[b0 + 1], c2 = hist[b0 + 2], c3 = hist[b0 + 3];
+  uint32_t total;
+  uint32_t above = block_excl_suffix(c0 + c1 + c2 + c3, &total);
+  const uint32_t c[4] = {c0, c1, c2, c3};
+#pragma unroll
+  for (int j = 3; j >= 0; j--) {
+    if (above < (uint32_t)rem && (uint32_t)rem <= above + c[j]) { d_sh = b0 + j; a_sh = above; }
+    above += c[j];
+  }
+  __syncthreads();
+  *above_out = a_sh;
+  return d_sh;
+}
+
+// Block-wide: a lower bound L of the rem-th largest (with multiplicity) of the
+// values v[0..n) in shared memory, 0 meaning "no value" (1 <= rem <= the
+// number of nonzero values), such that at least rem values are >= L: exact in
+// the bits every nonzero value shares and in the 12 bits below them, and in
+// 12 more when more than 64 values share the digit found, lower bits cleared.
+// Each step is one 4,096-bin histogram and a block-wide scan (blockDim.x ==
+// 1024).  hist: kWideBins counters.
+__device__ __noinline__ uint32_t block_kth_bound12(const uint32_t *v, int n, int rem, uint32_t *hist) {
+  const WideDigit wd = wide_digit([&](int i) { return v[i]; }, n, hist);
+  if (wd.sh < 0) {
+    __syncthreads();
+    return wd.mx;
+  }
+  uint32_t prefix = wd.prefix, pmask = wd.pmask;
+  int sh = wd.sh;
+  for (int step = 0;; step++) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint32_t x = v[i];
+      if (x != 0u && (x & pmask) == prefix) atomicAdd(&hist[(x >> sh) & (kWideBins - 1)], 1u);
+    }
+    __syncthreads();
+    uint32_t above;
+    const int D = wide_find(hist, rem, &above);
+    // digits above D hold `above` < rem of the values matching the prefix,
+    // digit D the rest: at least rem values are >= prefix | D << sh
+    prefix |= (uint32_t)D << sh;
+    pmask |= (uint32_t)(kWideBins - 1) << sh;
+    rem -= (int)above;
+    const uint32_t cnt = hist[D];
+    if (step == 1 || sh == 0 || cnt <= 64u) break;     // uniform
+    __syncthreads();                                    // hist[D] is read everywhere
+    for (int i = threadIdx.x; i < kWideBins; i += blockDim.x) hist[i] = 0u;
+    sh = max(sh - 12, 0);
+    __syncthreads();
+  }
+  __syncthreads();                                      // hist is read; the caller may reuse it
+  return prefix & ~((1u << sh) - 1u);
+}
+
+// Exact top-k of n unique nonzero 64-bit keys held in shared memory in
+// ascending index order, k < n <= blockDim.x (one key per thread): the digit
+// of the k-th largest key is found by one 4,096-bin histogram of the 12 bits
+// below the common prefix of the score halves, the keys in that digit (at
+// most kBinCap) are ranked among themselves, and the selected keys are
+// written out by one order-keeping compaction: out[0..k) ascending indices.
+// Returns false, having written nothing, when that digit holds more than
+// kBinCap keys (many equal scores); the caller then runs select_block.
+// hist: kWideBins counters; bin_keys: kBinCap keys of scratch.
+constexpr int kBinCap = 256;
+__device__ __noinline__ bool select_small(const uint64_t *keys, int n, int k, int32_t *out, uint32_t *hist,
+                                          uint64_t *bin_keys) {
+  __shared__ int n_bin;
+  const int t = threadIdx.x;
+  const uint64_t x = t < n ? keys[t] : 0ull;
+  const uint32_t hi = (uint32_t)(x >> 32);
+  if (t == 0) n_bin = 0;
+  const WideDigit wd = wide_digit([&](int i) { return (uint32_t)(keys[i] >> 32); }, n, hist);
+  const int sh = wd.sh < 0 ? 0 : wd.sh;
+  const int d = wd.sh < 0 ? 0 : (int)((hi >> sh) & (kWideBins - 1));
+  if (t < n) atomicAdd(&hist[d], 1u);
+  __syncthreads();
+  uint32_t above;
+  const int D = wide_find(hist, k, &above);
+  const int in_d = (int)hist[D], take_d = k - (int)above;   // keys of digit D, and how many of them are kept
+  if (in_d > kBinCap) {                                      // uniform: every thread read the same counts
+    __syncthreads();                                         // hist is read; the caller may reuse it
+    return false;
+  }
+  if (t < n && d == D) bin_keys[atomicAdd(&n_bin, 1)] = x;
+  __syncthreads();
+  int selected = 0;
+  if (t < n) {
+    if (d > D) {
+      selected = 1;
+    } else if (d == D) {
+      int r = 0;                                             // keys of digit D larger than this one
+      for (int j = 0; j < in_d; j++) r += bin_keys[j] > x ? 1 : 0;
+      selected = r < take_d;
+    }
+  }
+  int total;
+  const int pos = block_excl_scan(selected, &total);
+  if (selected) out[pos] = (int32_t)(~(uint32_t)(x & 0xFFFFFFFFu));
+  __syncthreads();
+  return true;
+}
+
 // Exact top-k of n unique nonzero keys in shared memory (n <= kCandCap), for
 // candidate sets a little larger than k.  The k-th largest key is found on
 // the score halves (sk[i] = keys[i] >> 32) by a radix-256 search, then, among
@@ -701,6 +867,12 @@ __device__ __forceinline__ uint32_t dsmem_ld32(uint32_t a) {
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
   return v;
 }
+__device__ __forceinline__ void dsmem_st32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void dsmem_st64(uint32_t a, uint64_t v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
 __device__ __forceinline__ uint64_t dsmem_ld64(uint32_t a) {
   uint64_t v;
   asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
@@ -726,40 +898,70 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
   __shared__ SelectShared sh;
   sh.whist = sv + kSuperCap;                                             // [32][256]
   __shared__ uint32_t T_sh;
-  __shared__ int n_vs, n_lc, lc_sorted;
+  __shared__ int n_vs, n_lc, lc_sorted, n_g;
   __shared__ int c_off[kMaxCluster + 1], c_bad, c_sorted;
+  __shared__ int c_cnt[kMaxCluster], c_srt[kMaxCluster];   // (CTA 0) pushed by every CTA of the cluster
   griddep_wait();
   griddep_launch();
   const int q = blockIdx.y, P = gridDim.x, part = blockIdx.x;
-  const int nv = query_nv(S, q, status);
-  const int pf_seq = S.kv_pf != nullptr ? __ldg(S.q_seq + q) : -1;   // used at the end
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool plain = S.pool == nullptr && S.block == 1;
+  // Plain rows with the maxima of their 32-entry groups as well (written by
+  // the indexer's epilogue, parts == 4): CTA p of the cluster takes the groups
+  // [g_lo, g_hi) of the row and streams only those reaching T, about one per
+  // listed supergroup, instead of listing supergroups and streaming all of
+  // their entries.  Its groups' maxima are loaded up front, with the
+  // supergroup maxima, before the row's length is known (slots past it hold
+  // stale values and are masked once it is).
+  const bool by_groups = plain && parts == 4 && W.gmax != nullptr;
+  const int gps = (int)(sgi >> 5);                                       // groups per supergroup
+  const int64_t g_all = (W.sstride / 4) * gps;                           // group slots of a row
+  const int64_t g_lo = part * g_all / P, g_hi = (part + 1) * g_all / P;
+  constexpr int kGPre = 4;
+  uint32_t gpre[kGPre];
+  const uint32_t *gq = W.gmax + (int64_t)q * W.gstride;
+  if (by_groups) {
+#pragma unroll
+    for (int j = 0; j < kGPre; j++) {
+      const int64_t gid = g_lo + threadIdx.x + (int64_t)j * blockDim.x;
+      gpre[j] = gid < g_hi ? __ldcg(gq + gid) : 0u;
+    }
+  }
+  // the supergroup maxima: 16-B loads over every slot of the row
+  const uint4 *src = reinterpret_cast<const uint4 *>(W.smax + (int64_t)q * W.sstride);
+  const int n_vec = (int)(W.sstride / 4);
+  uint4 vpre[2];
+#pragma unroll
+  for (int j = 0; j < 2; j++) {
+    const int i = threadIdx.x + j * blockDim.x;
+    vpre[j] = i < n_vec ? __ldcg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  const int nv = query_nv(S, q, status);
+  const int pf_seq = S.kv_pf != nullptr ? __ldg(S.q_seq + q) : -1;   // used at the end
   const int64_t valid_items = plain ? nv : (S.pool != nullptr ? S.n_items : ((int64_t)nv + kBlock - 1) / kBlock);
   const int ns = (int)((valid_items + sgi - 1) / sgi);                   // supergroups that may hold a valid item
-  if (threadIdx.x == 0) { n_vs = 0; T_sh = 1u; n_lc = 0; }             // T = 1: every valid item
+  if (threadIdx.x == 0) { n_vs = 0; T_sh = 1u; n_lc = 0; n_g = 0; }    // T = 1: every valid item
   __syncthreads();
-  // ---- the supergroup maxima (16-B loads; slots past ns are never used).
   // parts == 4: each supergroup's maximum is stored as four partial maxima.
   {
-    const uint4 *src = reinterpret_cast<const uint4 *>(W.smax + (int64_t)q * W.sstride);
     int vs = 0;
-    if (parts == 4) {
-      for (int i = threadIdx.x; i < ns; i += blockDim.x) {
-        const uint4 v = __ldcg(src + i);
-        const uint32_t x = max(max(v.x, v.y), max(v.z, v.w));
-        sv[i] = x;
-        vs += x != 0u;
-      }
-    } else {
-      for (int i = threadIdx.x; 4 * i < ns; i += blockDim.x) {
-        const uint4 v = __ldcg(src + i);
+    for (int i = threadIdx.x; i < n_vec; i += blockDim.x) {
+      const int j = (i - threadIdx.x) / blockDim.x;
+      const uint4 v = j < 2 ? vpre[j] : __ldcg(src + i);
+      if (parts == 4) {
+        if (i < ns) {
+          const uint32_t x = max(max(v.x, v.y), max(v.z, v.w));
+          sv[i] = x;
+          vs += x != 0u;
+        }
+      } else {
         const uint32_t e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-          const uint32_t x = 4 * i + j < ns ? e[j] : 0u;
-          sv[4 * i + j] = x;
-          vs += x != 0u;
+        for (int jj = 0; jj < 4; jj++) {
+          if (4 * i + jj < ns) {
+            sv[4 * i + jj] = e[jj];
+            vs += e[jj] != 0u;
+          }
         }
       }
     }
@@ -768,42 +970,101 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
   }
   __syncthreads();
   // ---- T: a lower bound of the k-th largest supergroup maximum, exact in
-  // the 16 bits below the leading bits all maxima share
+  // the 12 (or 24) bits below the leading bits all maxima share
   if (n_vs > k) {
-    const uint32_t t = block_kth256(sv, ns, k, 16, sh.whist, 2);
+    const uint32_t t = block_kth_bound12(sv, ns, k, sh.whist);
     if (threadIdx.x == 0) T_sh = t;
   }
   __syncthreads();
   const uint32_t T = T_sh;
-  // ---- list the supergroups that reach T in index order; this CTA takes a
-  // contiguous, equal share of that list (ranks [r_lo, r_hi)), so that the
-  // CTAs' candidates follow one another in index order and every CTA streams
-  // the same number of supergroups however they bunch together
-  uint64_t *lc = reinterpret_cast<uint64_t *>(sv);    // this CTA's keys >= T (over sv, once listed)
+  uint64_t *lc = reinterpret_cast<uint64_t *>(sv);    // this CTA's keys >= T (over sv, once T is known)
   constexpr int kLocalCap = kSuperCap / 2;
   {
     const float *row = S.scores + (int64_t)q * S.stride;
     const bool row16 = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
     int32_t *slist = reinterpret_cast<int32_t *>(keys);
-    const int run = (ns + blockDim.x - 1) / blockDim.x, g0 = threadIdx.x * run;   // this thread's supergroups
-    int c = 0;
-    for (int j = 0; j < run; j++) {
-      const int i = g0 + j;
-      c += (i < ns && sv[i] >= T && sv[i] != 0u) ? 1 : 0;
+    int nsl = 0;
+    if (!by_groups) {
+      // ---- list the supergroups that reach T in index order; this CTA takes a
+      // contiguous, equal share of that list (ranks [r_lo, r_hi)), so that the
+      // CTAs' candidates follow one another in index order and every CTA streams
+      // the same number of supergroups however they bunch together
+      const int run = (ns + blockDim.x - 1) / blockDim.x, g0 = threadIdx.x * run;   // this thread's supergroups
+      int c = 0;
+      for (int j = 0; j < run; j++) {
+        const int i = g0 + j;
+        c += (i < ns && sv[i] >= T && sv[i] != 0u) ? 1 : 0;
+      }
+      int n_listed;
+      int rank = block_excl_scan(c, &n_listed);
+      const int r_lo = (int)((int64_t)part * n_listed / P), r_hi = (int)((int64_t)(part + 1) * n_listed / P);
+      for (int j = 0; j < run && rank < r_hi; j++) {
+        const int i = g0 + j;
+        if (i < ns && sv[i] >= T && sv[i] != 0u) {
+          if (rank >= r_lo) slist[rank - r_lo] = i;
+          rank++;
+        }
+      }
+      __syncthreads();
+      nsl = r_hi - r_lo;
     }
-    int n_listed;
-    int rank = block_excl_scan(c, &n_listed);
-    const int r_lo = (int)((int64_t)part * n_listed / P), r_hi = (int)((int64_t)(part + 1) * n_listed / P);
-    for (int j = 0; j < run && rank < r_hi; j++) {
-      const int i = g0 + j;
-      if (i < ns && sv[i] >= T && sv[i] != 0u) {
-        if (rank >= r_lo) slist[rank - r_lo] = i;
-        rank++;
+    const int64_t total = (int64_t)nsl * sgi;                 // items of the listed supergroups
+    if (by_groups) {
+      // ---- this CTA's groups that reach T (their maxima were loaded up front)
+      constexpr int kGCap = 32 * 256;
+      int32_t *glist = reinterpret_cast<int32_t *>(sh.whist);   // [kGCap]: free since T was found
+      const int64_t g_valid = (int64_t)ns * gps;                 // groups of the supergroups holding valid entries
+      for (int64_t b0 = g_lo, j = 0; b0 < g_hi; b0 += blockDim.x, j++) {   // uniform trip count
+        const int64_t gid = b0 + threadIdx.x;
+        const uint32_t m0 = gpre[0];                             // this round's prefetched maximum
+#pragma unroll
+        for (int t = 0; t + 1 < kGPre; t++) gpre[t] = gpre[t + 1];
+        gpre[kGPre - 1] = 0u;
+        bool ok = false;
+        if (gid < g_hi && gid < g_valid) {
+          const uint32_t m = j < kGPre ? m0 : __ldcg(gq + gid);
+          ok = m >= T && m != 0u;
+        }
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
+        if (bal == 0u) continue;
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&n_g, __popc(bal));
+        base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(bal & ((1u << lane) - 1u));
+        if (ok && base < kGCap) glist[base] = (int32_t)gid;
+      }
+      __syncthreads();
+      // too many groups for the list: report an overflowing candidate list,
+      // so that the row is selected exactly from its scores instead
+      const int ng = n_g <= kGCap ? n_g : 0;
+      if (n_g > kGCap && threadIdx.x == 0) n_lc = kLocalCap + 1;
+      for (int b0 = 0; b0 < ng * 8; b0 += blockDim.x) {        // 8 threads per group, a float4 each
+        const int j = b0 + threadIdx.x;
+        float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        int64_t e0 = -1;
+        if (j < ng * 8) {
+          e0 = (int64_t)glist[j >> 3] * 32 + (j & 7) * 4;
+          if (row16 && e0 + 4 <= nv) {
+            v = __ldcg(reinterpret_cast<const float4 *>(row + e0));
+          } else {
+            if (e0 < nv) v.x = __ldcg(row + e0);
+            if (e0 + 1 < nv) v.y = __ldcg(row + e0 + 1);
+            if (e0 + 2 < nv) v.z = __ldcg(row + e0 + 2);
+            if (e0 + 3 < nv) v.w = __ldcg(row + e0 + 3);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const float x = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+          const bool ok = e0 >= 0 && e0 + e < nv && order_key(x) >= T;
+          const unsigned bal = __ballot_sync(0xFFFFFFFFu, ok);
+          if (bal == 0u) continue;
+          int base = 0;
+          if (lane == 0) base = atomicAdd(&n_lc, __popc(bal));
+          base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(bal & ((1u << lane) - 1u));
+          if (ok && base < kLocalCap) lc[base] = ((uint64_t)order_key(x) << 32) | (uint32_t)(~(uint32_t)(e0 + e));
+        }
       }
     }
-    __syncthreads();
-    const int nsl = r_hi - r_lo;
-    const int64_t total = (int64_t)nsl * sgi;                 // items of the listed supergroups
     // Plain rows with T above the key of +0: key(x) >= T exactly when the raw
     // bits of x, read as a signed integer, are >= those of T's float (NaN,
     // -0 and the -inf of missing items included).
@@ -812,7 +1073,7 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
     constexpr int kU = 6;
     const int64_t step = plain ? 4 : 1;
     const int lsg = __ffsll(sgi) - 1;
-    for (int64_t b0 = 0; b0 < total; b0 += kU * step * blockDim.x) {
+    for (int64_t b0 = 0; !by_groups && b0 < total; b0 += kU * step * blockDim.x) {
       float4 sc[kU];
       uint64_t gk[kU];
       int64_t base_i[kU];
@@ -940,12 +1201,26 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
     }
     if (threadIdx.x == 0) lc_sorted = nl <= kSortCap ? 1 : 0;
   }
-  // ---- CTA 0 gathers the cluster's candidates into keys
-  cluster_barrier();                                   // every CTA's lc, n_lc and lc_sorted are final
+  // ---- every CTA pushes its list into CTA 0's shared memory: slot `part`
+  // of keys (slot_cap keys each), with its length and sorted flag; after the
+  // cluster barrier CTA 0 holds the cluster's candidates and nobody reads
+  // another CTA's shared memory, so the others may leave
+  const int slot_cap = kCandCap / P;
+  __syncthreads();                                     // the sorted lc is written
+  {
+    const int nl = n_lc;
+    const int np = min(nl, min(kLocalCap, slot_cap));
+    for (int i = threadIdx.x; i < np; i += blockDim.x) dsmem_st64(dsmem_addr(keys + part * slot_cap + i, 0u), lc[i]);
+    if (threadIdx.x == 0) {
+      dsmem_st32(dsmem_addr(&c_cnt[part], 0u), (uint32_t)nl);
+      dsmem_st32(dsmem_addr(&c_srt[part], 0u), (uint32_t)lc_sorted);
+    }
+  }
+  cluster_barrier();                                   // the pushed lists are in CTA 0
   if (part == 0) {
     if (warp == 0) {
-      const int c = lane < P ? (int)dsmem_ld32(dsmem_addr(&n_lc, (uint32_t)lane)) : 0;
-      const int srt = lane < P ? (int)dsmem_ld32(dsmem_addr(&lc_sorted, (uint32_t)lane)) : 1;
+      const int c = lane < P ? c_cnt[lane] : 0;
+      const int srt = lane < P ? c_srt[lane] : 1;
       int incl = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -953,7 +1228,7 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
         if (lane >= o) incl += y;
       }
       if (lane <= kMaxCluster) c_off[lane] = incl - c;   // c_off[P] = the total
-      const bool over = __any_sync(0xFFFFFFFFu, c > kLocalCap) || __shfl_sync(0xFFFFFFFFu, incl, 31) > kCandCap;
+      const bool over = __any_sync(0xFFFFFFFFu, c > kLocalCap || c > slot_cap);
       const bool all_sorted = __all_sync(0xFFFFFFFFu, srt != 0);
       if (lane == 0) {
         c_bad = over ? 1 : 0;
@@ -962,15 +1237,27 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
     }
     __syncthreads();
     if (!c_bad) {
+      // close the gaps between the slots: read every key, then write it
+      constexpr int kPer = kCandCap / kCollectThreads;
       const int nc = c_off[P];
-      for (int i = threadIdx.x; i < nc; i += blockDim.x) {
-        int r = 0;
-        while (i >= c_off[r + 1]) r++;
-        keys[i] = dsmem_ld64(dsmem_addr(lc + (i - c_off[r]), (uint32_t)r));
+      uint64_t tmp[kPer];
+#pragma unroll
+      for (int j = 0; j < kPer; j++) {
+        const int i = threadIdx.x + j * kCollectThreads;
+        if (i < nc) {
+          int r = 0;
+          while (i >= c_off[r + 1]) r++;
+          tmp[j] = keys[r * slot_cap + (i - c_off[r])];
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < kPer; j++) {
+        const int i = threadIdx.x + j * kCollectThreads;
+        if (i < nc) keys[i] = tmp[j];
       }
     }
   }
-  cluster_barrier();                                   // the other CTAs' shared memory is no longer read
   // L2 prefetch of the latent records of this CTA's candidates (a superset of
   // the selected entries, which the attention gathers next): spread over the
   // cluster, and out of CTA 0's selection, which follows
@@ -993,7 +1280,10 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
       sv[i] = i < nc ? (uint32_t)(keys[i] >> 32) : 0u;   // score halves, zero-padded
     __syncthreads();
     // pool items run in slot order, not index order: only plain and block rows keep order
-    select_block(keys, sv, nc, k, oq, sel, sh.whist, c_sorted != 0 && S.pool == nullptr);
+    const bool by_index = c_sorted != 0 && S.pool == nullptr;
+    if (!(by_index && nc > k && nc <= (int)blockDim.x &&
+          select_small(keys, nc, k, oq, sh.whist, reinterpret_cast<uint64_t *>(sel))))
+      select_block(keys, sv, nc, k, oq, sel, sh.whist, by_index);
   } else {
     // too many ties at T for the buffer: exact selection straight over the row
     __shared__ int nvi;
@@ -1035,7 +1325,7 @@ static size_t collect_smem_bytes() {
 // and no larger than lets all n_q clusters be resident at once (a second wave
 // of clusters would double the kernel's time).  Sets the kernel's attributes
 // on first use on a device.
-static unsigned collect_ctas(int dev, int n_q, int64_t n_items) {
+static unsigned collect_ctas(int dev, int n_q, int64_t n_items, int reserve = 0) {
   static std::atomic<int> fit[kMaxDevices][kMaxCluster + 1];   // resident clusters of each size + 1 (0: unknown)
   static std::atomic<int> attr_done[kMaxDevices];
   if (dev < 0 || dev >= kMaxDevices) return 1;
@@ -1048,6 +1338,7 @@ static unsigned collect_ctas(int dev, int n_q, int64_t n_items) {
   });
   const int m = device_sm_count(dev);
   int p = (int)std::min<int64_t>(std::min<int64_t>(m / std::max(n_q, 1), n_items / 4096), kMaxCluster);
+  if (reserve > 0 && (m - reserve) / std::max(n_q, 1) >= 4) p = std::min(p, (m - reserve) / std::max(n_q, 1));
   for (; p > 1; p--) {
     int f = fit[dev][p].load(std::memory_order_relaxed);
     if (f == 0) {
@@ -1114,10 +1405,11 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
 
 // ---------------------------------------------------------------- fused decode
 // When the indexer's epilogue writes the supergroup maxima (csa2_decode), the
-// selection runs only the collection pass.  mode 1: supergroups are the
-// indexer's 512-entry work units, each stored as four partial maxima; mode 2:
-// supergroups of 32 entries; 0: the maxima pass runs (other supergroup sizes);
-// -1: rows short enough for one CTA (no scratch).
+// selection runs only the collection pass.  mode 3: supergroups are the
+// indexer's 512-entry work units, each stored as four partial maxima, plus the
+// maxima of their 32-entry groups (only the groups that reach the threshold
+// are streamed); mode 2: supergroups of 32 entries; 0: the maxima pass runs
+// (other supergroup sizes); -1: rows short enough for one CTA (no scratch).
 FusedTopk topk_fused_plan(void *ws, int n_q, int64_t n_max, int k) {
   FusedTopk F;
   F.mode = 0;
@@ -1127,28 +1419,37 @@ FusedTopk topk_fused_plan(void *ws, int n_q, int64_t n_max, int k) {
   F.kv = nullptr;
   F.q_seq = nullptr;
   F.n_seq = 0;
+  F.reserve = 0;
   if (n_max <= kDirectCap) { F.mode = -1; return F; }
   const int64_t sgi = long_row_sgi(n_max, k);
   if (sgi != 512 && sgi != 32) return F;
-  F.mode = sgi == 512 ? 1 : 2;
+  F.mode = sgi == 512 ? 3 : 2;
   F.sgi = sgi;
   F.parts = sgi == 512 ? 4 : 1;
   LongRowWs &W = F.W;
   W.sstride = sgi == 512 ? (n_max + 511) / 512 * 4 : ((n_max + 31) / 32 + 3) / 4 * 4;
   W.smax = static_cast<uint32_t *>(ws);
+  if (F.mode == 3) {
+    // then the maxima of the 32-entry groups, [n_q][n_max / 32], 256-B aligned
+    W.gstride = (n_max + 511) / 512 * 16;
+    const size_t off = ((size_t)n_q * (size_t)W.sstride * 4 + 255) / 256 * 256;
+    W.gmax = ws == nullptr ? nullptr : reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(ws) + off);
+  }
   return F;
 }
 
 int topk_fused_ctas(const FusedTopk &F, int n_q, int64_t n_max) {
   if (F.mode <= 0) return -1;
-  return (int)collect_ctas(current_device(), n_q, n_max) * n_q;
+  return (int)collect_ctas(current_device(), n_q, n_max, F.reserve) * n_q;
 }
 
 size_t topk_fused_bytes(int n_q, int64_t n_max, int k) {
   const FusedTopk F = topk_fused_plan(nullptr, n_q, n_max, k);
   if (F.mode == -1) return 0;
   if (F.mode == 0) return topk_workspace_bytes(n_q, n_max, k);
-  return (size_t)n_q * (size_t)F.W.sstride * 4;
+  size_t b = (size_t)n_q * (size_t)F.W.sstride * 4;
+  if (F.mode == 3) b = (b + 255) / 256 * 256 + (size_t)n_q * (size_t)F.W.gstride * 4;
+  return b;
 }
 
 cudaError_t launch_topk_fused(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max,
@@ -1166,7 +1467,7 @@ cudaError_t launch_topk_fused(const float *scores, int64_t stride, int n_q, cons
   S.q_seq = F.q_seq;
   S.n_seq = F.n_seq;
   const size_t dsm_collect = collect_smem_bytes();
-  const unsigned P = collect_ctas(current_device(), n_q, n_max);
+  const unsigned P = collect_ctas(current_device(), n_q, n_max, F.reserve);
   return launch_pdl(topk_collect_kernel, dim3(P, n_q), dim3(kCollectThreads), dsm_collect, st, P, S, F.sgi, F.parts,
                     k, F.W, out, status);
 }
