@@ -48,7 +48,8 @@ IDX_BYTES = 68
 # dram__bytes_read.sum + dram__bytes_write.sum of one index_score_tc_kernel launch inside
 # csa2_decode, from an ncu capture (--metrics dram__bytes_read.sum,dram__bytes_write.sum) of the
 # current kernel on the named workload; workloads without such a capture report null.
-INDEX_SCORE_TRAFFIC = {"long_full_decode_N1M_B8_zipf": 570_497_024 + 4_925_184}
+INDEX_SCORE_TRAFFIC = {"long_full_decode_N1M_B8_zipf": 570_499_840 + 5_160_448,
+                       "reindex_decode_N1M_B64": 84_263_680 + 2_083_072}
 
 
 def parse():
@@ -59,6 +60,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="with the default workload, skip the secondary 32 x 64K and Reindex lines")
     return ap.parse_args()
 
 
@@ -244,28 +247,30 @@ def run_ours(args, rank, world, local_rank):
     assert C.csa2_get_device_status() == 0
     ms = ranks.max_over_ranks(ms, device="cuda")
 
-    # end to end through the public API: the step's inputs (attention query,
-    # indexer query in bf16, head weights, per-query descriptors) packed in one
-    # pinned host buffer and copied in with one transfer; the bf16 output back
+    # end to end through the public API: csa2_decode_host takes the step's
+    # inputs (attention query, indexer query in bf16, head weights, per-query
+    # descriptors) in pinned host memory, copies each in, packs the indexer
+    # query, decodes and copies the bf16 output back, all on the stream
     from gen import inputs as G
     import numpy as np
     qidx_bits = np.concatenate([G.normal_block_bf16(wl.seed, G.S_QIDX, qi, 0, 32, 128) for qi in range(n_q)])
-    desc = torch.stack([dw.q_seq, dw.n_vis, dw.pos, dw.swa_first, dw.swa_cnt]).cpu()
-    stage_h, stage_d, (q_v, w_v, qidx_v, desc_v) = staged_inputs(
-        [dw.q.cpu(), dw.w.cpu(), torch.from_numpy(qidx_bits.view(np.int16)).view(torch.bfloat16), desc])
-    out_h = torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory()
-    dw.q, dw.w = q_v, w_v
-    dw.q_seq, dw.n_vis, dw.pos, dw.swa_first, dw.swa_cnt = desc_v[0], desc_v[1], desc_v[2], desc_v[3], desc_v[4]
+    h_q = dw.q.cpu().pin_memory()
+    h_qidx = torch.from_numpy(qidx_bits.view(np.int16)).pin_memory()
+    h_w = dw.w.cpu().pin_memory()
+    h_desc = torch.stack([dw.q_seq, dw.n_vis, dw.pos, dw.swa_first, dw.swa_cnt]).cpu().contiguous().pin_memory()
+    h_out = torch.empty(buf.out.shape, dtype=buf.out.dtype).pin_memory()
+    ws_h_bytes = C.csa2_workspace_size(C.CSA2_OP_DECODE_HOST, n_q, n_max, 512)
+    ws_h = torch.empty(ws_h_bytes, dtype=torch.uint8, device="cuda")
+    n_seq = dw.kv.shape[0]
 
     def e2e_step():
-        stage_d.copy_(stage_h, non_blocking=True)
-        C.csa2_fp4_pack(C.CSA2_IDX_MXFP4, qidx_v, n_q * 32, 1, None, dw.q_nib, dw.q_scale)
-        decode.fused_decode(dw, buf, None, stream)
-        out_h.copy_(buf.out, non_blocking=True)
+        C.csa2_decode_host(dw.key_nib, dw.key_scale, n_max, n_seq, dw.kv, dw.swa, dw.swa.shape[1], h_q, h_qidx, h_w,
+                           h_desc, n_q, None, h_out, C.CSA2_OUT_BF16, None, ws_h, ws_h_bytes, stream)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
     torch.cuda.synchronize()
+    assert C.csa2_get_device_status() == 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
@@ -274,8 +279,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = ranks.max_over_ranks(e2e_ms, device="cuda")
-    h2d = stage_h.numel()
-    d2h = out_h.numel() * out_h.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_qidx, h_w, h_desc))
+    d2h = h_out.numel() * h_out.element_size()
+    del ws_h
 
     if rank != 0:
         return None
@@ -314,10 +320,13 @@ def run_ours(args, rank, world, local_rank):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": INDEX_SCORE_TRAFFIC.get(wl.name),
                      "algorithmic_bytes_per_launch": score_bytes, "avg_launch_ms": score_ms,
-                     "measured_in": "K steps of the three-call chain after the timed region, same kernel"},
+                     "measured_in": "K launches of csa2_index_score (the three-call chain) after the timed "
+                                    "region: the kernel csa2_decode runs, without the 0.3 B per entry of "
+                                    "maxima its epilogue also writes there"},
         "clocks": clk,
         "e2e": {"value": units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "call": "csa2_decode_host (4 host-to-device copies, pack, decode, "
+                                                  "1 device-to-host copy per step)"},
         "gpu_launches": launches_per_step * args.steps,
         "impl": "ours",
     }
@@ -434,7 +443,7 @@ def run_rows(args, rank, world, local_rank, wl):
         hbm, hbm_kind = peaks()
         roof = {"kernel": "index_score (pool mode)", "bound": "hbm", "achieved": k_bytes / (k_ms / 1e3) / 1e9,
                 "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s",
-                "frac": k_bytes / (k_ms / 1e3) / 1e9 / hbm, "traffic": None,
+                "frac": k_bytes / (k_ms / 1e3) / 1e9 / hbm, "traffic": INDEX_SCORE_TRAFFIC.get(wl.name),
                 "algorithmic_bytes_per_launch": k_bytes, "avg_launch_ms": k_ms}
         dtype = "e2m1xe2m1->f32 (score), f16xf16 + bf16xbf16->f32 (attention)"
     else:
@@ -459,6 +468,7 @@ def run_rows(args, rank, world, local_rank, wl):
                    "m": wl.m, "pool_given": bool(wl.pool), "topk": 512, "swa": 128, "heads": 64, "latent": 512,
                    "parallelism": f"replicas x{world} (independent batches)"},
         "path_hbm_gbs": step_bytes / (ms / args.steps / 1e3) / 1e9,
+        "path_frac_of_measured_peak": (step_bytes / (ms / args.steps / 1e3) / 1e9 / peaks()[0]) if wl.pool else None,
         "roofline": roof, "clocks": clk,
         "e2e": {"value": units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -509,6 +519,27 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     line = run_ours(args, rank, world, local_rank)
+    if args.config == 4 and not args.no_extra:
+        # secondary workloads in the same run, as keys of the one line: the
+        # 32 x 65,536-entry decode batch and the 64 x 1,048,576 Reindex step
+        import copy
+        extra = {}
+        for c in (1, 3):
+            a2 = copy.copy(args)
+            a2.config, a2.no_cpu_baseline = c, True
+            a2.steps = max(3, min(args.steps, 50))
+            r = run_ours(a2, rank, world, local_rank)
+            if rank == 0:
+                extra[r["config"]["workload"]] = {
+                    k: r[k] for k in ("metric", "value", "unit", "ms_per_step", "path_hbm_gbs", "roofline", "e2e",
+                                      "clocks", "gpu_launches", "steps", "warmup")
+                    if k in r}
+                if "path_frac_of_measured_peak" in r:
+                    extra[r["config"]["workload"]]["path_frac_of_measured_peak"] = r["path_frac_of_measured_peak"]
+            import torch
+            torch.cuda.empty_cache()
+        if rank == 0:
+            line["secondary"] = extra
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -133,8 +133,35 @@ csa2_status csa2_index_score(const void *key_nib, const void *key_scale, int64_t
       scores, score_stride, st, (cudaStream_t)stream));
 }
 
+// csa2_decode_host's device staging, each part 256-B aligned, after the
+// decode workspace: q | indexer query bf16 | its packed nibbles | its scales |
+// w | descriptors [5][n_q] | sel | out (fp32-sized)
+struct HostStage {
+  size_t q, qidx, qnib, qsc, w, desc, sel, out, total;
+};
+static HostStage host_stage(int n_q) {
+  HostStage h;
+  size_t o = 0;
+  auto take = [&](size_t b) { const size_t at = o; o += round256(b); return at; };
+  h.q = take((size_t)n_q * kHeads * kDim * 2);
+  h.qidx = take((size_t)n_q * kIdxHeads * kIdxDim * 2);
+  h.qnib = take((size_t)n_q * kIdxHeads * kIdxNibBytes);
+  h.qsc = take((size_t)n_q * kIdxHeads * kIdxScaleBytes);
+  h.w = take((size_t)n_q * kIdxHeads * 4);
+  h.desc = take((size_t)n_q * 5 * 4);
+  h.sel = take((size_t)n_q * kTopK * 4);
+  h.out = take((size_t)n_q * kHeads * kDim * 4);
+  h.total = o;
+  return h;
+}
+
 csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t *bytes) {
   if (bytes == nullptr || n_q < 0 || n_items < 0) return CSA2_ERR_INVALID_ARG;
+  if (op == CSA2_OP_DECODE_HOST) {
+    if (n_items <= 0) return CSA2_ERR_INVALID_ARG;
+    *bytes = round256(decode_workspace_bytes(n_q, n_items)) + host_stage(n_q).total;
+    return CSA2_OK;
+  }
   if (op == CSA2_OP_TOPK) {
     if (k < 1 || k > 2048) return CSA2_ERR_UNSUPPORTED;
     *bytes = topk_workspace_bytes(n_q, n_items, k);
@@ -253,6 +280,47 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
   return from_cuda(launch_attn_tc(q, kv_cache, n_max, n_seq, sel, kTopK, swa_cache, swa_cap, q_seq, pos, swa_first,
                                   swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, ws_attn, st, s, true,
                                   topk_fused_ctas(F, n_q, n_max)));
+}
+
+csa2_status csa2_decode_host(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq, const void *kv_cache,
+                             const void *swa_cache, int swa_cap, const void *h_q, const void *h_qidx, const float *h_w,
+                             const int32_t *h_desc, int n_q, int32_t *h_sel, void *h_out, int out_dtype,
+                             const csa2_params *params, void *workspace, size_t workspace_bytes, csa2_stream_t stream) {
+  if (!params_ok(params)) return CSA2_ERR_UNSUPPORTED;
+  if (n_q < 0 || n_seq < 1 || n_max <= 0 || n_max % 128 != 0 || n_max > ((int64_t)1 << 31) - 128 || swa_cap < 0)
+    return CSA2_ERR_INVALID_ARG;
+  if (out_dtype != CSA2_OUT_BF16 && out_dtype != CSA2_OUT_F32) return CSA2_ERR_INVALID_ARG;
+  if (n_q > 65535) return CSA2_ERR_UNSUPPORTED;
+  if (n_q == 0) return CSA2_OK;
+  if (!h_q || !h_qidx || !h_w || !h_desc || !h_out) return CSA2_ERR_INVALID_ARG;
+  const size_t dec = round256(decode_workspace_bytes(n_q, n_max));
+  const HostStage H = host_stage(n_q);
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < dec + H.total) return CSA2_ERR_WORKSPACE;
+  const cudaStream_t s = (cudaStream_t)stream;
+  unsigned char *st = static_cast<unsigned char *>(workspace) + dec;
+  const size_t b_q = (size_t)n_q * kHeads * kDim * 2, b_qidx = (size_t)n_q * kIdxHeads * kIdxDim * 2;
+  const size_t b_w = (size_t)n_q * kIdxHeads * 4, b_desc = (size_t)n_q * 5 * 4;
+  const size_t b_out = (size_t)n_q * kHeads * kDim * (out_dtype == CSA2_OUT_F32 ? 4 : 2);
+  const size_t b_sel = (size_t)n_q * kTopK * 4;
+  // the step's inputs: one copy per host buffer
+  if (cudaMemcpyAsync(st + H.q, h_q, b_q, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(st + H.qidx, h_qidx, b_qidx, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(st + H.w, h_w, b_w, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(st + H.desc, h_desc, b_desc, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  csa2_status r = csa2_fp4_pack(CSA2_IDX_MXFP4, st + H.qidx, (int64_t)n_q * kIdxHeads, 1, nullptr, st + H.qnib,
+                                st + H.qsc, stream);
+  if (r != CSA2_OK) return r;
+  const int32_t *d = reinterpret_cast<const int32_t *>(st + H.desc);
+  r = csa2_decode(key_nib, key_scale, n_max, n_seq, st + H.qnib, st + H.qsc, reinterpret_cast<const float *>(st + H.w),
+                  d, d + n_q, n_q, st + H.q, kv_cache, swa_cache, swa_cap, d + 2 * n_q, d + 3 * n_q, d + 4 * n_q,
+                  reinterpret_cast<int32_t *>(st + H.sel), st + H.out, out_dtype, params, workspace, dec, stream);
+  if (r != CSA2_OK) return r;
+  // the step's outputs: one copy per host buffer
+  if (cudaMemcpyAsync(h_out, st + H.out, b_out, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (h_sel != nullptr && cudaMemcpyAsync(h_sel, st + H.sel, b_sel, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  return CSA2_OK;
 }
 
 csa2_status csa2_get_device_status(csa2_stream_t stream, csa2_status *out) {

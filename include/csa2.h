@@ -80,7 +80,7 @@ enum { CSA2_KV_NVFP4 = 0, CSA2_IDX_MXFP4 = 1, CSA2_SWA_MXFP8 = 2 };
 /* Output dtypes for csa2_sparse_attn. */
 enum { CSA2_OUT_BF16 = 0, CSA2_OUT_F32 = 1 };
 /* Operations for csa2_workspace_size. */
-enum { CSA2_OP_TOPK = 0, CSA2_OP_SPARSE_ATTN = 1, CSA2_OP_DECODE = 2 };
+enum { CSA2_OP_TOPK = 0, CSA2_OP_SPARSE_ATTN = 1, CSA2_OP_DECODE = 2, CSA2_OP_DECODE_HOST = 3 };
 
 /* Model constants.  The kernels are built for the pages' values only
  * (study, reading notes: 64 heads, 512-wide latent, RoPE on 64 of the 512
@@ -269,11 +269,44 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
                         const csa2_params *params, void *workspace, size_t workspace_bytes, csa2_stream_t stream);
 
 /*
+ * csa2_decode_host -- csa2_decode with the step's inputs and outputs in host
+ * memory: the end-to-end call of a decode step.  The caches (indexer keys,
+ * latents, window) stay resident in device memory; the per-step tensors
+ * travel with the call.  On `stream`, in order: one cudaMemcpyAsync per host
+ * input buffer into the workspace, csa2_fp4_pack of the indexer query,
+ * csa2_decode, one cudaMemcpyAsync per host output buffer.  Asynchronous:
+ * the host buffers must stay valid (and the outputs unread) until the stream
+ * has passed the call; pinned (page-locked) host memory makes the copies
+ * asynchronous and fast, pageable memory works but serialises them.
+ *
+ *   key_nib .. n_seq, kv_cache, swa_cache, swa_cap   (device) as csa2_decode.
+ *   h_q        (host) bf16 [n_q][64][512], the attention query (rotated).
+ *   h_qidx     (host) bf16 [n_q][32][128], the indexer query before packing.
+ *   h_w        (host) fp32 [n_q][32], the indexer head weights.
+ *   h_desc     (host) int32 [5][n_q]: rows q_seq, n_vis, pos, swa_first,
+ *              swa_cnt (meanings as csa2_decode).
+ *   h_sel      (host, may be NULL) int32 [n_q][512]: receives the selection.
+ *   h_out      (host) [n_q][64][512], bf16 or fp32 per out_dtype.
+ *   workspace  (device) >= csa2_workspace_size(CSA2_OP_DECODE_HOST, n_q,
+ *              n_max, 512) bytes, 256-B aligned; no initialisation.
+ * Argument checks and errors as csa2_decode; a failed copy returns
+ * CSA2_ERR_CUDA.
+ */
+csa2_status csa2_decode_host(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq, const void *kv_cache,
+                             const void *swa_cache, int swa_cap, const void *h_q, const void *h_qidx, const float *h_w,
+                             const int32_t *h_desc, int n_q, int32_t *h_sel, void *h_out, int out_dtype,
+                             const csa2_params *params, void *workspace, size_t workspace_bytes, csa2_stream_t stream);
+
+/*
  * csa2_workspace_size -- scratch bytes needed by an operation.
  *   op = CSA2_OP_TOPK:        n_q queries, n_items = items per row (entries,
  *                             blocks, or 16384 pool slots), k.
  *   op = CSA2_OP_SPARSE_ATTN: n_q queries, n_items = sel_stride + 128, k unused.
  *   op = CSA2_OP_DECODE:      n_q queries, n_items = n_max, k unused (512).
+ *   op = CSA2_OP_DECODE_HOST: as CSA2_OP_DECODE (the device copies of the
+ *                             step's inputs and outputs are included).
+ * Sizes are for the current device (the attention's split plan follows its
+ * SM count).
  */
 csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t *bytes);
 

@@ -71,10 +71,20 @@ def test_host_validation_rejects_before_launch(lib):
                               None, None, 0, None) == INVALID
     assert L.csa2_sparse_attn(fake, fake, 1024, 1, fake, 512, fake, 128, fake, fake, fake, fake, 8, fake, 0,
                               None, None, 0, None) == WS
+    # csa2_decode_host: a missing host buffer, a workspace without room for the staging
+    args = (fake, fake, 1024, 1, fake, fake, 128)
+    assert L.csa2_decode_host(*args, fake, fake, fake, None, 1, None, fake, 0, None, fake, 1 << 30, None) == INVALID
+    assert L.csa2_decode_host(*args, fake, fake, fake, fake, 1, None, fake, 0, None, fake, 1024, None) == WS
+    assert L.csa2_decode_host(*args, fake, fake, fake, fake, 1, None, fake, 7, None, fake, 1 << 30, None) == INVALID
     assert L.csa2_get_device_status(None, None) == INVALID
 
 
 def test_workspace_sizes(lib):
+    # the host-buffer decode stages the step's inputs and outputs after the decode workspace
+    dec = lib.csa2_workspace_size(lib.CSA2_OP_DECODE, 8, 1 << 20, 512)
+    host = lib.csa2_workspace_size(lib.CSA2_OP_DECODE_HOST, 8, 1 << 20, 512)
+    staged = 8 * (65536 + 8192 + 2048 + 128 + 128 + 20 + 2048 + 131072)
+    assert staged <= host - dec <= staged + 8 * 256
     assert lib.csa2_workspace_size(lib.CSA2_OP_TOPK, 8, 4096, 512) == 0          # one CTA per row
     # per row: the 2,048 maxima of 512-item supergroups (candidates stay on chip)
     assert lib.csa2_workspace_size(lib.CSA2_OP_TOPK, 8, 1 << 20, 512) == 8 * 2048 * 4

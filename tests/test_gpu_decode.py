@@ -366,3 +366,37 @@ def test_window_longer_than_ring_is_rejected(lib, oracle_lib):
     win = ring[(5 + np.arange(64)) % cap]
     ref = oracle_lib.sparse_attn(wl.q(1), kv_records(wl, 1, sel[1][sel[1] >= 0]), win, int(wl.pos()[1]))
     assert row_norm_err(got[1], ref) <= ATTN_TOL_F32
+
+
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_decode_host_equals_device_call(lib, out_f32):
+    """csa2_decode_host (inputs and outputs in pinned host memory, copied
+    inside the call) gives exactly csa2_decode's selection and output, on a
+    garbage-filled workspace and on a second call."""
+    import compressed_sparse_attention_index_gb300 as C
+    from gen import inputs as G
+    wl = small(n_seq=3, n_entries=20_000, seed=252)
+    dw = _dw(wl)
+    n_q = dw.q.shape[0]
+    dt = C.CSA2_OUT_F32 if out_f32 else C.CSA2_OUT_BF16
+    ref = _bufs(dw, out_dtype=dt)
+    from compressed_sparse_attention_index_gb300 import decode
+    decode.fused_decode(dw, ref)
+    qidx = np.concatenate([G.normal_block_bf16(wl.seed, G.S_QIDX, qi, 0, 32, 128) for qi in range(n_q)])
+    h_q = dw.q.cpu().pin_memory()
+    h_qidx = torch.from_numpy(qidx.view(np.int16)).pin_memory()
+    h_w = dw.w.cpu().pin_memory()
+    h_desc = torch.stack([dw.q_seq, dw.n_vis, dw.pos, dw.swa_first, dw.swa_cnt]).cpu().contiguous().pin_memory()
+    h_sel = torch.full((n_q, 512), -7, dtype=torch.int32).pin_memory()
+    h_out = torch.full(tuple(ref.out.shape), 7, dtype=ref.out.dtype).pin_memory()
+    wsb = C.csa2_workspace_size(C.CSA2_OP_DECODE_HOST, n_q, dw.n_max, 512)
+    ws = torch.full((wsb,), 0xA5, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        C.csa2_decode_host(dw.key_nib, dw.key_scale, dw.n_max, dw.kv.shape[0], dw.kv, dw.swa, dw.swa.shape[1], h_q,
+                           h_qidx, h_w, h_desc, n_q, h_sel, h_out, dt, None, ws, wsb)
+        torch.cuda.synchronize()
+        assert lib.csa2_get_device_status() == 0
+        assert torch.equal(h_sel, ref.sel.cpu())
+        assert torch.equal(h_out.view(torch.int16 if not out_f32 else torch.int32),
+                           ref.out.cpu().view(torch.int16 if not out_f32 else torch.int32))
+        h_out.fill_(7)
