@@ -477,6 +477,61 @@ def run_rows(args, rank, world, local_rank, wl):
     }
 
 
+def run_mq(args, rank, world, local_rank):
+    """Multi-query decode: five draft positions per sequence over the 8 x 1M
+    Zipf caches, decoded in one csa2_decode_mq step; the indexer reads each
+    sequence's keys once for its five queries."""
+    import torch
+    import compressed_sparse_attention_index_gb300 as C
+    from compressed_sparse_attention_index_gb300 import decode, ranks
+    from gen.device import build_device_workload
+    from gen.workloads import MQ_DECODE
+    wl = MQ_DECODE
+    dw = build_device_workload(wl)
+    n_q, n_max, G = dw.q.shape[0], dw.n_max, wl.q_per_seq
+    buf = decode.DecodeBuffers(n_q, n_max, out_dtype=C.CSA2_OUT_BF16, q_group=G)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        decode.mq_decode(dw, buf, None, stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert C.csa2_get_device_status() == 0
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = ranks.max_over_ranks(t0.elapsed_time(t1), device="cuda")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        C.csa2_index_score_mq(dw.key_nib, dw.key_scale, n_max, dw.kv.shape[0], dw.q_nib, dw.q_scale, dw.w, dw.q_seq,
+                              dw.n_vis, n_q, G, buf.scores, n_max, None, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    k_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    assert C.csa2_get_device_status() == 0
+    if rank != 0:
+        return None
+    peak, peak_kind = peaks()
+    key_bytes = wl.n_seq * wl.n_entries * IDX_BYTES
+    step_bytes = key_bytes + n_q * FIXED_BYTES_PER_QUERY
+    return {"metric": "multi-query decode query-tokens/s (5 draft positions per sequence, keys scored once per "
+                      "sequence)", "value": n_q * args.steps * world / (ms / 1e3), "unit": UNIT,
+            "ms_per_step": ms / args.steps, "steps": args.steps, "warmup": args.warmup,
+            "queries_per_step": n_q, "key_bytes_per_step": key_bytes,
+            "key_bytes_per_step_single_query_decode": wl.n_seq * wl.n_entries * IDX_BYTES,
+            "path_hbm_gbs": step_bytes / (ms / args.steps / 1e3) / 1e9,
+            "roofline": {"kernel": "index_score_mq (N = 160)", "bound": "hbm",
+                         "achieved": key_bytes / (k_ms / 1e3) / 1e9, "peak": peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": key_bytes / (k_ms / 1e3) / 1e9 / peak, "traffic": None,
+                         "algorithmic_bytes_per_launch": key_bytes, "avg_launch_ms": k_ms},
+            "gpu_launches": 4 * args.steps}
+
+
 def run_reference(args):
     from gen.workloads import CONFIGS
     import oracle
@@ -538,6 +593,11 @@ def main():
                     extra[r["config"]["workload"]]["path_frac_of_measured_peak"] = r["path_frac_of_measured_peak"]
             import torch
             torch.cuda.empty_cache()
+        a2 = copy.copy(args)
+        a2.steps = max(3, min(args.steps, 50))
+        r = run_mq(a2, rank, world, local_rank)
+        if rank == 0:
+            extra["mq_decode_N1M_B8_G5_zipf"] = r
         if rank == 0:
             line["secondary"] = extra
     if rank == 0:

@@ -16,13 +16,14 @@ LIB_PATH = os.path.join(HERE, "libcsa2.so")
 
 CSA2_KV_NVFP4, CSA2_IDX_MXFP4, CSA2_SWA_MXFP8 = 0, 1, 2
 CSA2_OUT_BF16, CSA2_OUT_F32 = 0, 1
-CSA2_OP_TOPK, CSA2_OP_SPARSE_ATTN, CSA2_OP_DECODE, CSA2_OP_DECODE_HOST = 0, 1, 2, 3
+CSA2_OP_TOPK, CSA2_OP_SPARSE_ATTN, CSA2_OP_DECODE, CSA2_OP_DECODE_HOST, CSA2_OP_DECODE_MQ = 0, 1, 2, 3, 4
 STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED", 3: "CSA2_ERR_CUDA",
           4: "CSA2_ERR_BOUNDS", 5: "CSA2_ERR_TIMEOUT", 6: "CSA2_ERR_WORKSPACE"}
 
 EXPORTS = ["csa2_default_params", "csa2_entry_bytes", "csa2_status_string", "csa2_fp4_pack",
            "csa2_index_score", "csa2_topk", "csa2_sparse_attn", "csa2_workspace_size",
-           "csa2_get_device_status", "csa2_topk_noalloc", "csa2_decode", "csa2_decode_host"]
+           "csa2_get_device_status", "csa2_topk_noalloc", "csa2_decode", "csa2_decode_host",
+           "csa2_index_score_mq", "csa2_decode_mq"]
 
 
 class CSA2Error(RuntimeError):
@@ -59,6 +60,9 @@ def load(path: str = LIB_PATH):
         "csa2_index_score": (i32, [P, P, i64, i32, P, P, P, P, P, i32, P, P, i64, PP, P]),
         "csa2_topk": (i32, [P, i64, i32, P, i64, i32, i32, P, P, P, sz, P]),
         "csa2_decode": (i32, [P, P, i64, i32, P, P, P, P, P, i32, P, P, P, i32, P, P, P, P, P, i32, PP, P, sz, P]),
+        "csa2_index_score_mq": (i32, [P, P, i64, i32, P, P, P, P, P, i32, i32, P, i64, PP, P]),
+        "csa2_decode_mq": (i32, [P, P, i64, i32, P, P, P, P, P, i32, i32, P, P, P, i32, P, P, P, P, P, i32, PP, P, sz,
+                                 P]),
         "csa2_decode_host": (i32, [P, P, i64, i32, P, P, i32, P, P, P, P, i32, P, P, i32, PP, P, sz, P]),
         "csa2_topk_noalloc": (i32, [P, i64, i32, P, i64, i32, i32, P, P, P]),
         "csa2_sparse_attn": (i32, [P, P, i64, i32, P, i32, P, i32, P, P, P, P, i32, P, i32, PP, P, sz, P]),
@@ -155,6 +159,25 @@ def csa2_decode(key_nib, key_scale, n_max, n_seq, q_nib, q_scale, w, q_seq, n_vi
         _ptr(n_vis), int(n_q), _ptr(q), _ptr(kv_cache), _ptr(swa_cache), int(swa_cap), _ptr(pos), _ptr(swa_first),
         _ptr(swa_cnt), _ptr(sel), _ptr(out), int(out_dtype), pp, _ptr(workspace), int(workspace_bytes),
         _stream(stream)))
+
+
+def csa2_index_score_mq(key_nib, key_scale, n_max, n_seq, q_nib, q_scale, w, q_seq, n_vis, n_q, q_group, scores,
+                        score_stride, params=None, stream=None):
+    pp = ctypes.byref(params) if params is not None else None
+    _check("csa2_index_score_mq", load().csa2_index_score_mq(
+        _ptr(key_nib), _ptr(key_scale), int(n_max), int(n_seq), _ptr(q_nib), _ptr(q_scale), _ptr(w), _ptr(q_seq),
+        _ptr(n_vis), int(n_q), int(q_group), _ptr(scores), int(score_stride), pp, _stream(stream)))
+
+
+def csa2_decode_mq(key_nib, key_scale, n_max, n_seq, q_nib, q_scale, w, q_seq, n_vis, n_q, q_group, q, kv_cache,
+                   swa_cache, swa_cap, pos, swa_first, swa_cnt, sel, out, out_dtype, params=None, workspace=None,
+                   workspace_bytes=0, stream=None):
+    pp = ctypes.byref(params) if params is not None else None
+    _check("csa2_decode_mq", load().csa2_decode_mq(
+        _ptr(key_nib), _ptr(key_scale), int(n_max), int(n_seq), _ptr(q_nib), _ptr(q_scale), _ptr(w), _ptr(q_seq),
+        _ptr(n_vis), int(n_q), int(q_group), _ptr(q), _ptr(kv_cache), _ptr(swa_cache), int(swa_cap), _ptr(pos),
+        _ptr(swa_first), _ptr(swa_cnt), _ptr(sel), _ptr(out), int(out_dtype), pp, _ptr(workspace),
+        int(workspace_bytes), _stream(stream)))
 
 
 def csa2_decode_host(key_nib, key_scale, n_max, n_seq, kv_cache, swa_cache, swa_cap, h_q, h_qidx, h_w, h_desc, n_q,

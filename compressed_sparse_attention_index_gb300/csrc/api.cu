@@ -155,8 +155,19 @@ static HostStage host_stage(int n_q) {
   return h;
 }
 
+// csa2_decode_mq's workspace: scores [n_q][n_max] | top-k scratch | attention partials
+static size_t decode_mq_workspace_bytes(int n_q, int64_t n_max) {
+  return round256((size_t)n_q * (size_t)n_max * 4) + round256(topk_workspace_bytes(n_q, n_max, kTopK)) +
+         round256(attn_workspace_bytes(n_q, kTopK));
+}
+
 csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t *bytes) {
   if (bytes == nullptr || n_q < 0 || n_items < 0) return CSA2_ERR_INVALID_ARG;
+  if (op == CSA2_OP_DECODE_MQ) {
+    if (n_items <= 0) return CSA2_ERR_INVALID_ARG;
+    *bytes = decode_mq_workspace_bytes(n_q, n_items);
+    return CSA2_OK;
+  }
   if (op == CSA2_OP_DECODE_HOST) {
     if (n_items <= 0) return CSA2_ERR_INVALID_ARG;
     *bytes = round256(decode_workspace_bytes(n_q, n_items)) + host_stage(n_q).total;
@@ -280,6 +291,74 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
   return from_cuda(launch_attn_tc(q, kv_cache, n_max, n_seq, sel, kTopK, swa_cache, swa_cap, q_seq, pos, swa_first,
                                   swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, ws_attn, st, s, true,
                                   topk_fused_ctas(F, n_q, n_max)));
+}
+
+csa2_status csa2_index_score_mq(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq,
+                                const void *q_nib, const void *q_scale, const float *w, const int32_t *q_seq,
+                                const int32_t *n_vis, int n_q, int q_group, float *scores, int64_t score_stride,
+                                const csa2_params *params, csa2_stream_t stream) {
+  if (!params_ok(params)) return CSA2_ERR_UNSUPPORTED;
+  if (n_q < 0 || n_seq < 1 || n_max <= 0 || n_max % 128 != 0 || n_max > ((int64_t)1 << 31) - 256)
+    return CSA2_ERR_INVALID_ARG;
+  if (q_group < 1 || q_group > kMaxQueryGroup) return CSA2_ERR_UNSUPPORTED;
+  if (n_q % q_group != 0) return CSA2_ERR_INVALID_ARG;
+  if (n_q > 65535) return CSA2_ERR_UNSUPPORTED;
+  if (score_stride < n_max) return CSA2_ERR_INVALID_ARG;
+  if (n_q == 0) return CSA2_OK;
+  if (!key_nib || !key_scale || !q_nib || !q_scale || !w || !q_seq || !n_vis || !scores) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(key_nib, 512) || !aligned(key_scale, 16) || !aligned(q_nib, 512) || !aligned(q_scale, 16) ||
+      !aligned(w, 16) || !aligned(scores, 4))
+    return CSA2_ERR_INVALID_ARG;
+  int *st = status_ptr();
+  if (st == nullptr) return CSA2_ERR_CUDA;
+  return from_cuda(launch_index_score_mq(static_cast<const uint8_t *>(key_nib), static_cast<const uint8_t *>(key_scale),
+                                         n_max, n_seq, static_cast<const uint8_t *>(q_nib),
+                                         static_cast<const uint8_t *>(q_scale), w, q_seq, n_vis, n_q, q_group, scores,
+                                         score_stride, st, (cudaStream_t)stream));
+}
+
+csa2_status csa2_decode_mq(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq, const void *q_nib,
+                           const void *q_scale, const float *w, const int32_t *q_seq, const int32_t *n_vis, int n_q,
+                           int q_group, const void *q, const void *kv_cache, const void *swa_cache, int swa_cap,
+                           const int32_t *pos, const int32_t *swa_first, const int32_t *swa_cnt, int32_t *sel,
+                           void *out, int out_dtype, const csa2_params *params, void *workspace,
+                           size_t workspace_bytes, csa2_stream_t stream) {
+  if (!params_ok(params)) return CSA2_ERR_UNSUPPORTED;
+  if (n_q < 0 || n_seq < 1 || n_max <= 0 || n_max % 128 != 0 || n_max > ((int64_t)1 << 31) - 256 || swa_cap < 0)
+    return CSA2_ERR_INVALID_ARG;
+  if (q_group < 1 || q_group > kMaxQueryGroup) return CSA2_ERR_UNSUPPORTED;
+  if (n_q % q_group != 0 || (out_dtype != CSA2_OUT_BF16 && out_dtype != CSA2_OUT_F32)) return CSA2_ERR_INVALID_ARG;
+  if (n_q > 65535) return CSA2_ERR_UNSUPPORTED;
+  if (n_q == 0) return CSA2_OK;
+  if (!key_nib || !key_scale || !q_nib || !q_scale || !w || !q_seq || !n_vis || !q || !kv_cache || !pos ||
+      !swa_first || !swa_cnt || !sel || !out)
+    return CSA2_ERR_INVALID_ARG;
+  if (swa_cap > 0 && swa_cache == nullptr) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(key_nib, 512) || !aligned(key_scale, 16) || !aligned(q_nib, 512) || !aligned(q_scale, 16) ||
+      !aligned(w, 16) || !aligned(q, 16) || !aligned(kv_cache, 16) || (swa_cache && !aligned(swa_cache, 16)) ||
+      !aligned(out, 16) || !aligned(sel, 4))
+    return CSA2_ERR_INVALID_ARG;
+  if (!topk_items_supported(n_max, kTopK)) return CSA2_ERR_UNSUPPORTED;
+  if (workspace_bytes < decode_mq_workspace_bytes(n_q, n_max) || workspace == nullptr || !aligned(workspace, 256))
+    return CSA2_ERR_WORKSPACE;
+  int *st = status_ptr();
+  if (st == nullptr) return CSA2_ERR_CUDA;
+  const cudaStream_t s = (cudaStream_t)stream;
+  unsigned char *base = static_cast<unsigned char *>(workspace);
+  float *scores = reinterpret_cast<float *>(base);
+  void *ws_topk = base + round256((size_t)n_q * (size_t)n_max * 4);
+  void *ws_attn = static_cast<unsigned char *>(ws_topk) + round256(topk_workspace_bytes(n_q, n_max, kTopK));
+  cudaError_t e = launch_index_score_mq(static_cast<const uint8_t *>(key_nib), static_cast<const uint8_t *>(key_scale),
+                                        n_max, n_seq, static_cast<const uint8_t *>(q_nib),
+                                        static_cast<const uint8_t *>(q_scale), w, q_seq, n_vis, n_q, q_group, scores,
+                                        n_max, st, s);
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  e = launch_topk(scores, n_max, n_q, n_vis, n_max, kTopK, 1, nullptr, sel, ws_topk, st, s);
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  const float sm_scale = params ? params->sm_scale : 1.0f / sqrtf((float)kDim);
+  const double rope_base = params ? params->rope_base : 10000.0;
+  return from_cuda(launch_attn_tc(q, kv_cache, n_max, n_seq, sel, kTopK, swa_cache, swa_cap, q_seq, pos, swa_first,
+                                  swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, ws_attn, st, s));
 }
 
 csa2_status csa2_decode_host(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq, const void *kv_cache,

@@ -116,6 +116,14 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
                                   const int32_t *n_vis, int n_q, const int32_t *pool, float *scores, int64_t stride,
                                   int *status, cudaStream_t st, const LongRowWs *W = nullptr, int smax_mode = 0);
 
+// Multi-query indexer: queries [g * group, g * group + group) share their
+// sequence and are scored in one pass over its keys (group 1 .. 6).
+constexpr int kMaxQueryGroup = 6;
+cudaError_t launch_index_score_mq(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
+                                  const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
+                                  const int32_t *n_vis, int n_q, int group, float *scores, int64_t stride,
+                                  int *status, cudaStream_t st);
+
 size_t topk_workspace_bytes(int n_q, int64_t n_items, int k);
 bool topk_items_supported(int64_t n_items, int k);
 cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max, int k,

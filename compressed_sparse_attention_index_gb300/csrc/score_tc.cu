@@ -68,17 +68,19 @@ constexpr uint32_t kColSFB = kColSFA + kScStages * kSub * 4;  // per query slot:
 static_assert(kColSFB + kQSlots * 4 <= kScTmemCols, "TMEM columns");
 static_assert(kScStages % kScAcc == 0, "a stage's done barrier also marks its accumulator full");
 
-// Instruction descriptor of kind::mxf4 block-scaled MMA, M=128, N=32, both
-// operands E2M1 and K-major, UE8M0 scales; sf_id picks the scale byte pair.
-__host__ __device__ constexpr uint32_t idesc_mxf4_m128n32(uint32_t sf_id) {
+// Instruction descriptor of kind::mxf4 block-scaled MMA, M=128, N=n (a
+// multiple of 16, <= 256), both operands E2M1 and K-major, UE8M0 scales;
+// sf_id picks the scale byte pair.
+__host__ __device__ constexpr uint32_t idesc_mxf4_m128(uint32_t sf_id, uint32_t n) {
   return (sf_id << 4)            // B scale-factor id
          | (1u << 7)             // A format: E2M1
          | (1u << 10)            // B format: E2M1
-         | ((32u >> 3) << 17)    // N / 8
+         | ((n >> 3) << 17)      // N / 8
          | (1u << 23)            // scale format UE8M0
          | ((128u >> 4) << 24)   // M / 16
          | (sf_id << 29);        // A scale-factor id
 }
+__host__ __device__ constexpr uint32_t idesc_mxf4_m128n32(uint32_t sf_id) { return idesc_mxf4_m128(sf_id, 32); }
 
 struct ScoreTcArgs {
   const uint8_t *key_nib;
@@ -122,11 +124,13 @@ struct ScoreTcArgs {
 constexpr int kRing = 16;
 constexpr uint32_t kDone = 0xFFFFFFFFu;
 
-// Bounded wait for the ring entry of iteration it; false on timeout or abort.
+// Bounded wait for the ring entry of iteration it (a ring of R entries); false
+// on timeout or abort.
+template <int R = kRing>
 __device__ __forceinline__ bool ring_get(const volatile unsigned long long *ring, uint32_t it, uint32_t &T,
                                          const volatile int &abort_flag) {
   for (long long n = 0; n < kSpinLimit; n++) {
-    const unsigned long long e = ring[it % kRing];
+    const unsigned long long e = ring[it % R];
     if ((uint32_t)(e >> 32) == it) { T = (uint32_t)e; return true; }
     if ((n & 63) == 63 && abort_flag) return false;
   }
@@ -161,27 +165,29 @@ struct QueryInfo {
 // units of one query (an epoch) takes the next slot round-robin; the slot's
 // previous user was the last unit of the epoch kQSlots earlier.  Registers
 // only: the ring of epoch starts is shifted, never indexed.
-struct QuerySlots {
+template <int NS>
+struct QuerySlotsT {
   int cur_q = -1;
-  uint32_t slot = kQSlots - 1;
-  int start[kQSlots];                    // first unit of the last kQSlots epochs, oldest first
-  __device__ QuerySlots() {
+  uint32_t slot = NS - 1;
+  int start[NS];                         // first unit of the last NS epochs, oldest first
+  __device__ QuerySlotsT() {
 #pragma unroll
-    for (int i = 0; i < kQSlots; i++) start[i] = -1;
+    for (int i = 0; i < NS; i++) start[i] = -1;
   }
   // call once per unit in schedule order; true when unit `it` starts an epoch
   __device__ bool step(int q, int it) {
     if (q == cur_q) return false;
     cur_q = q;
-    slot = slot + 1 == (uint32_t)kQSlots ? 0u : slot + 1;
+    slot = slot + 1 == (uint32_t)NS ? 0u : slot + 1;
 #pragma unroll
-    for (int i = 0; i + 1 < kQSlots; i++) start[i] = start[i + 1];
-    start[kQSlots - 1] = it;
+    for (int i = 0; i + 1 < NS; i++) start[i] = start[i + 1];
+    start[NS - 1] = it;
     return true;
   }
   // after step() returned true: the last unit that used this slot (< 0 if none)
   __device__ int prev_user() const { return start[0] - 1; }
 };
+using QuerySlots = QuerySlotsT<kQSlots>;
 
 // Pool mode: a unit is 64 gathered 8-entry blocks (512 B of nibbles + 32 B of
 // scales each).  Small bulk copies cost the copy engine more than their bytes,
@@ -535,6 +541,283 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   }
 }
 
+// ---------------------------------------------------------------- multi-query
+// Several queries of one sequence decoded together (draft positions of one
+// step: helix.ml, DeepSeek V4.1 Flash, section on DSpark, which proposes five
+// future positions at once) see the same keys, so a group of G consecutive
+// queries of one sequence is scored in one pass over the keys: the G queries'
+// 32 heads each are the MMA's N = 32 G columns, and every key unit is read once
+// per group instead of once per query.  The accumulators are G times wider, so
+// units are 128 entries, with two accumulators of 32 G <= 192 TMEM columns
+// (MMA and epilogue overlap) and 20 stages of 8.5 KB in flight.
+// Roles (384 threads): warp 0 producer, warp 1 MMA issuer (lane 0) and TMEM
+// owner, warp 2 scale factors, warp 3 idle, warps 4..11 epilogue in two groups
+// of four taking alternate units (warp w: TMEM lane quarter w % 4).  A query's
+// scale factors sit in TMEM as rows of B: head h of the group's query g (row
+// 32 g + h) at lane h, 32-bit word g (words 4..7 in the next four columns), as
+// the key rows of A do.
+constexpr int kMqUnit = 128;
+constexpr int kMqStages = 20;
+constexpr int kMqOffSFA = 8192;
+constexpr int kMqStageBytes = kMqOffSFA + 512;
+constexpr int kMqMaxG = 6;                                   // N = 32 G <= 192
+constexpr int kMqSlots = 2;
+constexpr int kMqQOffSFB = kMqMaxG * 2048;                    // then two 32 x 16-B scale blocks
+constexpr int kMqSlotBytes = kMqQOffSFB + 1024;
+constexpr int kMqSmem = kMqStages * kMqStageBytes + kMqSlots * kMqSlotBytes;
+constexpr int kMqThreads = 384;
+// ring of published units: the producer, gated by the MMA of the unit
+// kMqStages back, may run that far ahead of the MMA, and the epilogue trails
+// the MMA by up to two units, so the ring holds more than kMqStages + 2
+constexpr int kMqRing = 32;
+static_assert(kMqRing > kMqStages + 2, "ring of published units");
+constexpr uint32_t kMqColSFA = 2 * kMqMaxG * 32;              // after the two accumulators
+constexpr uint32_t kMqColSFB = kMqColSFA + kMqStages * 4;
+static_assert(kMqStageBytes % 512 == 0 && kMqSlotBytes % 512 == 0, "64B-swizzled tiles need 512-B alignment");
+static_assert(kMqColSFB + kMqSlots * 8 <= kScTmemCols, "TMEM columns");
+static_assert(kMqSmem + 1024 <= 227 * 1024, "shared memory");
+static_assert(kMqStages % 2 == 0, "a stage's done barrier also marks its accumulator full");
+static_assert(kMqMaxG == kMaxQueryGroup, "the query-group limit of the C ABI");
+
+// G (the queries of a group) is a template parameter so that the epilogue's
+// loops over the queries unroll into independent running sums.
+template <int G>
+__global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcArgs P) {
+  extern __shared__ __align__(1024) unsigned char mq_smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(mq_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char *qslots = smem + kMqStages * kMqStageBytes;
+  __shared__ __align__(8) uint64_t full_bar[kMqStages], sf_bar[kMqStages], done_bar[kMqStages];
+  __shared__ __align__(8) uint64_t acc_empty[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_flag;
+  __shared__ volatile unsigned long long unit_ring[kMqRing];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t N = 32u * (uint32_t)G;
+  griddep_wait();
+  griddep_launch();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMqStages; s++) {
+      ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&sf_bar[s], 1);
+      ptx::mbar_init(&done_bar[s], 1);
+    }
+    ptx::mbar_init(&acc_empty[0], 4);
+    ptx::mbar_init(&acc_empty[1], 4);
+    for (int i = 0; i < kMqRing; i++) unit_ring[i] = ~0ull;
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) ptx::tmem_alloc(&tmem_base_sh, kScTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  auto fail = [&]() {
+    record_error(P.status, CSA2_ERR_TIMEOUT);
+    abort_flag = 1;
+  };
+  const int n_groups = P.n_q / G;
+  const uint32_t total_units = (uint32_t)n_groups * (uint32_t)P.units_per_q;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t policy = ptx::policy_evict_first();
+    QuerySlotsT<kMqSlots> qs;
+    int cur_g = -1, seq = 0, nv_max = -1;
+    uint32_t T = blockIdx.x;
+    for (uint32_t it = 0;; it++) {
+      if (abort_flag) break;
+      int u = 0;
+      for (;;) {
+        if (T >= total_units) { T = kDone; break; }
+        const int gi = (int)(T / (uint32_t)P.units_per_q);
+        u = (int)(T - (uint32_t)gi * (uint32_t)P.units_per_q);
+        if (gi != cur_g) {
+          // the group's sequence (all G queries must share it) and its
+          // longest visible length; a group breaking this is skipped
+          cur_g = gi;
+          int sq = -1, nm = -1, ok = 1;
+          for (int g = 0; g < G; g++) {
+            const int q = gi * G + g, s_ = __ldg(P.q_seq + q), v = __ldg(P.n_vis + q);
+            if (g == 0) sq = s_;
+            if (s_ != sq || v < 0 || (int64_t)v > P.n_max) ok = 0;
+            nm = max(nm, v);
+          }
+          if (sq < 0 || sq >= P.n_seq) ok = 0;
+          if (!ok && lane == 0 && u == 0) record_error(P.status, CSA2_ERR_BOUNDS);
+          seq = sq;
+          nv_max = ok ? nm : -1;
+        }
+        if (nv_max >= 0 && u * kMqUnit < nv_max) break;
+        T += gridDim.x;
+      }
+      if (lane == 0) unit_ring[it % kMqRing] = ((unsigned long long)it << 32) | T;
+      if (T == kDone) break;
+      const uint32_t s = it % kMqStages, r = it / kMqStages;
+      const bool fresh = qs.step(cur_g, (int)it);
+      if (!ptx::mbar_wait(&done_bar[s], (r & 1) ^ 1)) { fail(); break; }
+      if (fresh) {
+        // the slot's previous user (MMAs complete in order: its last unit)
+        const int pu = qs.prev_user();
+        if (pu >= 0 && pu + kMqStages > (int)it &&
+            !ptx::mbar_wait(&done_bar[pu % kMqStages], (uint32_t)(pu / kMqStages) & 1)) { fail(); break; }
+      }
+      unsigned char *st = smem + s * kMqStageBytes;
+      unsigned char *qd = qslots + qs.slot * kMqSlotBytes;
+      if (lane == 0) {
+        const uint32_t qbytes = fresh ? (uint32_t)G * (2048 + 128) : 0u;
+        ptx::mbar_arrive_expect_tx(&full_bar[s], 8192u + 512u + qbytes);
+        if (fresh) {
+          const int64_t q0 = (int64_t)cur_g * G;
+          ptx::bulk_load(qd, P.q_nib + q0 * kIdxHeads * 64, (uint32_t)G * 2048, &full_bar[s]);
+          ptx::bulk_load(qd + kMqQOffSFB, P.q_scale + q0 * kIdxHeads * 4, (uint32_t)G * 128, &full_bar[s]);
+        }
+        // a unit that starts before n_vis ends within n_max (n_max % 128 == 0)
+        const int64_t r0 = (int64_t)seq * P.n_max + (int64_t)u * kMqUnit;
+        ptx::bulk_load_hint(st, P.key_nib + r0 * 64, 8192u, &full_bar[s], policy);
+        ptx::bulk_load(st + kMqOffSFA, P.key_scale + r0 * 4, 512u, &full_bar[s]);
+      }
+      __syncwarp();
+      T += gridDim.x;
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ scale-factor warp
+    QuerySlotsT<kMqSlots> qs;
+    for (uint32_t it = 0;; it++) {
+      if (abort_flag) break;
+      uint32_t T;
+      if (!ring_get<kMqRing>(unit_ring, it, T, abort_flag)) { fail(); break; }
+      if (T == kDone) break;
+      const uint32_t s = it % kMqStages, r = it / kMqStages;
+      const bool fresh = qs.step((int)(T / (uint32_t)P.units_per_q), (int)it);
+      if (!ptx::mbar_wait(&full_bar[s], r & 1)) { fail(); break; }
+      unsigned char *st = smem + s * kMqStageBytes;
+      unsigned char *qd = qslots + qs.slot * kMqSlotBytes;
+      if (fresh) {
+        // the queries' scales, [g][head] words as loaded -> block g / 4, line
+        // head, word g % 4 (zero for g >= G)
+        uint32_t *sfb = reinterpret_cast<uint32_t *>(qd + kMqQOffSFB);
+        uint32_t vb[8];
+#pragma unroll
+        for (int g = 0; g < 8; g++) vb[g] = g < G ? sfb[g * 32 + lane] : 0u;
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < 8; g++) sfb[(g >> 2) * 128 + lane * 4 + (g & 3)] = vb[g];
+      }
+      // key scales -> tcgen05.cp layout: 16-B line m0 holds rows m0, m0+32, m0+64, m0+96
+      uint32_t *sfa = reinterpret_cast<uint32_t *>(st + kMqOffSFA);
+      uint32_t va[4];
+#pragma unroll
+      for (int i = 0; i < 4; i++) va[i] = sfa[i * 32 + lane];
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; i++) sfa[lane * 4 + i] = va[i];
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tc_fence_after();
+        if (fresh) {
+          const uint32_t sb = ptx::smem_u32(qd + kMqQOffSFB);
+          ptx::tc_cp_32x128b_warpx4(tmem + kMqColSFB + qs.slot * 8, ptx::smem_desc(sb, 0, 128, 0));
+          if (G > 4) ptx::tc_cp_32x128b_warpx4(tmem + kMqColSFB + qs.slot * 8 + 4, ptx::smem_desc(sb + 512, 0, 128, 0));
+        }
+        ptx::tc_cp_32x128b_warpx4(tmem + kMqColSFA + s * 4, ptx::smem_desc(ptx::smem_u32(sfa), 0, 128, 0));
+        ptx::tc_commit(&sf_bar[s]);
+      }
+      __syncwarp();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (lane 0)
+    if (lane == 0) {
+      const uint32_t idesc0 = idesc_mxf4_m128(0, N), idesc1 = idesc_mxf4_m128(2, N);
+      QuerySlotsT<kMqSlots> qs;
+      for (uint32_t it = 0;; it++) {
+        if (abort_flag) break;
+        uint32_t T;
+        if (!ring_get<kMqRing>(unit_ring, it, T, abort_flag)) { fail(); break; }
+        if (T == kDone) break;
+        qs.step((int)(T / (uint32_t)P.units_per_q), (int)it);
+        const uint32_t s = it % kMqStages, r = it / kMqStages, a = it & 1, ra = it >> 1;
+        if (!ptx::mbar_wait(&sf_bar[s], r & 1) || !ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) { fail(); break; }
+        ptx::tc_fence_after();
+        const uint64_t ad = ptx::smem_desc(ptx::smem_u32(smem + s * kMqStageBytes), 16, 512, 4);
+        const uint64_t bd = ptx::smem_desc(ptx::smem_u32(qslots + qs.slot * kMqSlotBytes), 16, 512, 4);
+        const uint32_t t_sfa = tmem + kMqColSFA + s * 4, t_sfb = tmem + kMqColSFB + qs.slot * 8;
+        const uint32_t d = tmem + a * N;
+        ptx::tc_mma_mxf4(d, ad, bd, idesc0, t_sfa, t_sfb, 0u);
+        ptx::tc_mma_mxf4(d, ad + 2, bd + 2, idesc1, t_sfa, t_sfb, 1u);   // +32 B along K
+        ptx::tc_commit(&done_bar[s]);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    // group grp (warps 4+4 grp .. 7+4 grp) takes the units with it % 2 == grp
+    // and owns accumulator grp (see the single-query kernel for why waiting on
+    // done_bar is unambiguous)
+    const int quarter = warp & 3;
+    const uint32_t grp = (uint32_t)(warp - 4) >> 2;
+    for (uint32_t it = 0;; it++) {
+      if (abort_flag) break;
+      uint32_t T;
+      if (!ring_get<kMqRing>(unit_ring, it, T, abort_flag)) { fail(); break; }
+      if (T == kDone) break;
+      if ((it & 1) != grp) continue;
+      const int gi = (int)(T / (uint32_t)P.units_per_q), u = (int)(T % (uint32_t)P.units_per_q);
+      const uint32_t s = it % kMqStages, r = it / kMqStages;
+      if (!ptx::mbar_wait(&done_bar[s], r & 1)) { fail(); break; }
+      ptx::tc_fence_after();
+      const int64_t e = (int64_t)u * kMqUnit + quarter * 32 + lane;
+      const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + grp * N;
+      // up to three queries at a time: their 32 columns each in one load
+      // apiece and one wait (each TMEM round trip costs hundreds of cycles),
+      // then one running sum per query, heads in order
+#pragma unroll
+      for (int g0 = 0; g0 < G; g0 += 3) {
+        constexpr int kB = 3;
+        const int nb = G - g0 < kB ? G - g0 : kB;
+        uint32_t d[kB][32];
+#pragma unroll
+        for (int b = 0; b < kB; b++)
+          if (b < nb) ptx::tmem_ld_32x32b_x32(ta + (g0 + b) * 32, d[b]);
+        ptx::tmem_wait_ld();
+        float acc[kB] = {0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+#pragma unroll
+          for (int b = 0; b < kB; b++) {
+            if (b < nb) {
+              const float4 wv = __ldg(reinterpret_cast<const float4 *>(P.w + (int64_t)(gi * G + g0 + b) * kIdxHeads) + i);
+              acc[b] = fmaf(wv.x, fmaxf(__uint_as_float(d[b][4 * i]), 0.f), acc[b]);
+              acc[b] = fmaf(wv.y, fmaxf(__uint_as_float(d[b][4 * i + 1]), 0.f), acc[b]);
+              acc[b] = fmaf(wv.z, fmaxf(__uint_as_float(d[b][4 * i + 2]), 0.f), acc[b]);
+              acc[b] = fmaf(wv.w, fmaxf(__uint_as_float(d[b][4 * i + 3]), 0.f), acc[b]);
+            }
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < kB; b++) {
+          if (b < nb) {
+            const int q = gi * G + g0 + b;
+            if (e < __ldg(P.n_vis + q)) P.scores[(int64_t)q * P.stride + e] = acc[b];
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&acc_empty[grp]);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kScTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
                                   const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
@@ -573,6 +856,62 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
   const int n_sm = device_sm_count(dev);
   const int64_t grid = total_units < n_sm ? total_units : n_sm;
   return launch_pdl(index_score_tc_kernel, dim3((unsigned)grid), dim3(kScThreads), smem, st, 1u, P);
+}
+
+}  // namespace csa2
+
+namespace csa2 {
+
+cudaError_t launch_index_score_mq(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,
+                                  const uint8_t *q_nib, const uint8_t *q_scale, const float *w, const int32_t *q_seq,
+                                  const int32_t *n_vis, int n_q, int group, float *scores, int64_t stride,
+                                  int *status, cudaStream_t st) {
+  ScoreTcArgs P = {};
+  P.key_nib = key_nib;
+  P.q_nib = q_nib;
+  P.key_scale = key_scale;
+  P.q_scale = q_scale;
+  P.w = w;
+  P.q_seq = q_seq;
+  P.n_vis = n_vis;
+  P.pool = nullptr;
+  P.scores = scores;
+  P.stride = stride;
+  P.n_max = n_max;
+  P.n_seq = n_seq;
+  P.n_q = n_q;
+  P.units_per_q = (int)((n_max + kMqUnit - 1) / kMqUnit);
+  P.status = status;
+  const int64_t total_units = (int64_t)(n_q / group) * P.units_per_q;
+  const size_t smem = (size_t)kMqSmem + 1024;
+  const int dev = current_device();
+  static std::atomic<int> attr_done[kMaxDevices];
+  const cudaError_t e = once_per_device(attr_done, dev, [&] {
+    cudaError_t r = cudaSuccess, ri;
+    ri = cudaFuncSetAttribute(index_score_mq_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    r = r == cudaSuccess ? ri : r;
+    ri = cudaFuncSetAttribute(index_score_mq_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    r = r == cudaSuccess ? ri : r;
+    ri = cudaFuncSetAttribute(index_score_mq_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    r = r == cudaSuccess ? ri : r;
+    ri = cudaFuncSetAttribute(index_score_mq_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    r = r == cudaSuccess ? ri : r;
+    ri = cudaFuncSetAttribute(index_score_mq_kernel<5>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    r = r == cudaSuccess ? ri : r;
+    ri = cudaFuncSetAttribute(index_score_mq_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return r == cudaSuccess ? ri : r;
+  });
+  if (e != cudaSuccess) return e;
+  const int n_sm = device_sm_count(dev);
+  const dim3 grid((unsigned)(total_units < n_sm ? total_units : n_sm)), block(kMqThreads);
+  switch (group) {
+    case 1: return launch_pdl(index_score_mq_kernel<1>, grid, block, smem, st, 1u, P);
+    case 2: return launch_pdl(index_score_mq_kernel<2>, grid, block, smem, st, 1u, P);
+    case 3: return launch_pdl(index_score_mq_kernel<3>, grid, block, smem, st, 1u, P);
+    case 4: return launch_pdl(index_score_mq_kernel<4>, grid, block, smem, st, 1u, P);
+    case 5: return launch_pdl(index_score_mq_kernel<5>, grid, block, smem, st, 1u, P);
+    default: return launch_pdl(index_score_mq_kernel<6>, grid, block, smem, st, 1u, P);
+  }
 }
 
 }  // namespace csa2

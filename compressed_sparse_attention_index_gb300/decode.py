@@ -22,7 +22,8 @@ TOPK, POOL_BLOCKS, POOL_SLOTS, SWA = 512, 2048, 16384, 128
 class DecodeBuffers:
     """Device buffers of one decode step for n_q queries over caches of n_max entries."""
 
-    def __init__(self, n_q: int, n_max: int, pool: bool = False, out_dtype=L.CSA2_OUT_BF16, device="cuda"):
+    def __init__(self, n_q: int, n_max: int, pool: bool = False, out_dtype=L.CSA2_OUT_BF16, device="cuda",
+                 q_group: int = 1):
         self.n_q, self.n_max, self.pool, self.out_dtype = n_q, n_max, pool, out_dtype
         self.scores = torch.empty((n_q, n_max), dtype=torch.float32, device=device)
         self.sel = torch.empty((n_q, TOPK), dtype=torch.int32, device=device)
@@ -36,7 +37,9 @@ class DecodeBuffers:
                        L.csa2_workspace_size(L.CSA2_OP_TOPK, n_q, POOL_SLOTS, TOPK))
         self.ws_topk_bytes = ws_t
         self.ws_attn_bytes = L.csa2_workspace_size(L.CSA2_OP_SPARSE_ATTN, n_q, TOPK + SWA)
-        self.ws_decode_bytes = 0 if pool else L.csa2_workspace_size(L.CSA2_OP_DECODE, n_q, n_max, TOPK)
+        self.q_group = q_group
+        self.ws_decode_bytes = 0 if pool else L.csa2_workspace_size(
+            L.CSA2_OP_DECODE_MQ if q_group > 1 else L.CSA2_OP_DECODE, n_q, n_max, TOPK)
         self.ws = torch.empty(max(1, ws_t, self.ws_attn_bytes, self.ws_decode_bytes), dtype=torch.uint8,
                               device=device)
 
@@ -58,6 +61,16 @@ def fused_decode(dw, buf: DecodeBuffers, params=None, stream=None):
     L.csa2_decode(dw.key_nib, dw.key_scale, dw.n_max, dw.kv.shape[0], dw.q_nib, dw.q_scale, dw.w, dw.q_seq,
                   dw.n_vis, buf.n_q, dw.q, dw.kv, dw.swa, dw.swa.shape[1], dw.pos, dw.swa_first, dw.swa_cnt,
                   buf.sel, buf.out, buf.out_dtype, params, buf.ws, buf.ws_decode_bytes, stream)
+    return buf.out
+
+
+def mq_decode(dw, buf: DecodeBuffers, params=None, stream=None):
+    """Full-layer decode of groups of buf.q_group queries per sequence (draft
+    positions decoded together) as the single call csa2_decode_mq: each
+    sequence's keys are scored once for its whole group."""
+    L.csa2_decode_mq(dw.key_nib, dw.key_scale, dw.n_max, dw.kv.shape[0], dw.q_nib, dw.q_scale, dw.w, dw.q_seq,
+                     dw.n_vis, buf.n_q, buf.q_group, dw.q, dw.kv, dw.swa, dw.swa.shape[1], dw.pos, dw.swa_first,
+                     dw.swa_cnt, buf.sel, buf.out, buf.out_dtype, params, buf.ws, buf.ws_decode_bytes, stream)
     return buf.out
 
 

@@ -37,23 +37,33 @@ class Workload:
     pool: bool = False      # Reindex layer over a 16,384-position pool
     prefill: bool = False   # causal prefill: all queries on sequence 0
     swa_cap: int = SWA      # SWA ring capacity per sequence
+    q_per_seq: int = 1      # draft positions decoded together: queries [b*G, b*G + G) of sequence b
     extra: dict = field(default_factory=dict)
 
     # ---- per-query descriptors (host int32 arrays) ----
     def q_seq(self) -> np.ndarray:
         if self.prefill:
             return np.zeros(self.n_q, np.int32)
+        if self.q_per_seq > 1:
+            return (np.arange(self.n_q) // self.q_per_seq % self.n_seq).astype(np.int32)
         return (np.arange(self.n_q) % self.n_seq).astype(np.int32)
 
     def pos(self) -> np.ndarray:
         if self.prefill:
             return np.arange(self.n_q, dtype=np.int32)
+        if self.q_per_seq > 1:
+            # draft position t of G sits at n_entries - G + t: the cache holds
+            # the G drafted tokens' entries, each query sees up to its own
+            t = np.arange(self.n_q) % self.q_per_seq
+            return (self.n_entries - self.q_per_seq + t).astype(np.int32)
         return np.full(self.n_q, self.n_entries * self.m - 1, np.int32)
 
     def n_vis(self) -> np.ndarray:
         if self.prefill:   # entry j (tokens 2j, 2j+1) visible to query t iff 2j+1 <= t
             t = np.arange(self.n_q, dtype=np.int64)
             return ((t + 1) // self.m).astype(np.int32)
+        if self.q_per_seq > 1:
+            return (self.pos().astype(np.int64) + 1).astype(np.int32)
         return np.full(self.n_q, self.n_entries, np.int32)
 
     def swa_first(self) -> np.ndarray:
@@ -98,7 +108,12 @@ CONFIGS = {
     4: Workload("long_full_decode_N1M_B8_zipf", 4, 8, 1 << 20, 8, zipf=True),
 }
 
+# Multi-query decode (the next row after the five workloads above): the 8 x 1M
+# Zipf caches with five draft positions per sequence decoded in one step.
+MQ_DECODE = Workload("mq_decode_N1M_B8_G5_zipf", 4, 8, 1 << 20, 40, zipf=True, q_per_seq=5)
 
-def small(n_seq=2, n_entries=1000, zipf=False, pool=False, seed=100) -> Workload:
+
+def small(n_seq=2, n_entries=1000, zipf=False, pool=False, seed=100, q_per_seq=1) -> Workload:
     """A small decode workload for tests (ragged N allowed)."""
-    return Workload(f"small_N{n_entries}_B{n_seq}", seed, n_seq, n_entries, n_seq, zipf=zipf, pool=pool)
+    return Workload(f"small_N{n_entries}_B{n_seq}_G{q_per_seq}", seed, n_seq, n_entries, n_seq * q_per_seq,
+                    zipf=zipf, pool=pool, q_per_seq=q_per_seq)

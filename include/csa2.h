@@ -80,7 +80,7 @@ enum { CSA2_KV_NVFP4 = 0, CSA2_IDX_MXFP4 = 1, CSA2_SWA_MXFP8 = 2 };
 /* Output dtypes for csa2_sparse_attn. */
 enum { CSA2_OUT_BF16 = 0, CSA2_OUT_F32 = 1 };
 /* Operations for csa2_workspace_size. */
-enum { CSA2_OP_TOPK = 0, CSA2_OP_SPARSE_ATTN = 1, CSA2_OP_DECODE = 2, CSA2_OP_DECODE_HOST = 3 };
+enum { CSA2_OP_TOPK = 0, CSA2_OP_SPARSE_ATTN = 1, CSA2_OP_DECODE = 2, CSA2_OP_DECODE_HOST = 3, CSA2_OP_DECODE_MQ = 4 };
 
 /* Model constants.  The kernels are built for the pages' values only
  * (study, reading notes: 64 heads, 512-wide latent, RoPE on 64 of the 512
@@ -269,6 +269,41 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
                         const csa2_params *params, void *workspace, size_t workspace_bytes, csa2_stream_t stream);
 
 /*
+ * csa2_index_score_mq -- csa2_index_score (Full mode) for groups of queries
+ * that share a sequence, such as several draft positions of one sequence
+ * decoded in the same step (DeepSeek V4.1 Flash: Why Its Encoder, Engram and
+ * KV Cache Matter, section on DSpark: five future positions per step).  The
+ * queries [g * q_group, g * q_group + q_group) must all name the same
+ * sequence; each of its key units is read once for the whole group and
+ * multiplied with all 32 x q_group query heads at once.  Results as
+ * csa2_index_score for every query (scores[q][j] for j < n_vis[q]).
+ *
+ *   q_group    1 .. 6; n_q a multiple of q_group.  A group whose queries name
+ *              different sequences (or an out-of-range sequence or length) is
+ *              skipped and records CSA2_ERR_BOUNDS.
+ *   the rest   as csa2_index_score (no pool mode).
+ */
+csa2_status csa2_index_score_mq(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq,
+                                const void *q_nib, const void *q_scale, const float *w, const int32_t *q_seq,
+                                const int32_t *n_vis, int n_q, int q_group, float *scores, int64_t score_stride,
+                                const csa2_params *params, csa2_stream_t stream);
+
+/*
+ * csa2_decode_mq -- the decode step of csa2_decode for groups of q_group
+ * queries per sequence: csa2_index_score_mq, then the top-512 of every query
+ * (csa2_topk), then csa2_sparse_attn of every query; the results are those of
+ * that chain.  Arguments as csa2_decode, with q_group as in
+ * csa2_index_score_mq; workspace >= csa2_workspace_size(CSA2_OP_DECODE_MQ,
+ * n_q, n_max, 512) bytes, 256-B aligned, no initialisation.
+ */
+csa2_status csa2_decode_mq(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq, const void *q_nib,
+                           const void *q_scale, const float *w, const int32_t *q_seq, const int32_t *n_vis, int n_q,
+                           int q_group, const void *q, const void *kv_cache, const void *swa_cache, int swa_cap,
+                           const int32_t *pos, const int32_t *swa_first, const int32_t *swa_cnt, int32_t *sel,
+                           void *out, int out_dtype, const csa2_params *params, void *workspace,
+                           size_t workspace_bytes, csa2_stream_t stream);
+
+/*
  * csa2_decode_host -- csa2_decode with the step's inputs and outputs in host
  * memory: the end-to-end call of a decode step.  The caches (indexer keys,
  * latents, window) stay resident in device memory; the per-step tensors
@@ -305,6 +340,7 @@ csa2_status csa2_decode_host(const void *key_nib, const void *key_scale, int64_t
  *   op = CSA2_OP_DECODE:      n_q queries, n_items = n_max, k unused (512).
  *   op = CSA2_OP_DECODE_HOST: as CSA2_OP_DECODE (the device copies of the
  *                             step's inputs and outputs are included).
+ *   op = CSA2_OP_DECODE_MQ:   n_q queries, n_items = n_max, k unused (512).
  * Sizes are for the current device (the attention's split plan follows its
  * SM count).
  */
