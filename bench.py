@@ -532,6 +532,44 @@ def run_mq(args, rank, world, local_rank):
             "gpu_launches": 4 * args.steps}
 
 
+def run_layers(args, rank, world, local_rank):
+    """The decoder's twenty layers for one token of each sequence (one Full
+    layer, four Reindex layers, fifteen Reuse layers borrowing selections)
+    over the 8 x 1M Zipf caches, chained through the C ABI."""
+    import torch
+    import compressed_sparse_attention_index_gb300 as C
+    from compressed_sparse_attention_index_gb300 import decode, ranks
+    from gen.device import build_device_workload, build_decoder_layers
+    from gen.workloads import CONFIGS, DECODER_LAYERS
+    wl = CONFIGS[4]
+    dw = build_device_workload(wl)
+    dl = build_decoder_layers(wl, dw, DECODER_LAYERS)
+    n_q = dw.q.shape[0]
+    step = decode.DecoderStep(n_q, dw.n_max, DECODER_LAYERS, out_dtype=C.CSA2_OUT_BF16)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step.run(dw, dl, None, stream)
+    torch.cuda.synchronize()
+    assert C.csa2_get_device_status() == 0
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step.run(dw, dl, None, stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = ranks.max_over_ranks(t0.elapsed_time(t1), device="cuda")
+    assert C.csa2_get_device_status() == 0
+    if rank != 0:
+        return None
+    n_re = sum(1 for role, _ in DECODER_LAYERS if role == "reindex")
+    n_ru = sum(1 for role, _ in DECODER_LAYERS if role == "reuse")
+    return {"metric": "decoder-step query-tokens/s (20 layers: 1 Full, 4 Reindex, 15 Reuse)",
+            "value": n_q * args.steps * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms / args.steps,
+            "steps": args.steps, "warmup": args.warmup, "layers": len(DECODER_LAYERS),
+            "layer_mix": {"full": 1, "reindex": n_re, "reuse": n_ru},
+            "gpu_launches": args.steps * (4 + n_re * 2 + len(DECODER_LAYERS) * 2)}
+
+
 def run_reference(args):
     from gen.workloads import CONFIGS
     import oracle
@@ -598,6 +636,10 @@ def main():
         r = run_mq(a2, rank, world, local_rank)
         if rank == 0:
             extra["mq_decode_N1M_B8_G5_zipf"] = r
+        torch.cuda.empty_cache()
+        r = run_layers(a2, rank, world, local_rank)
+        if rank == 0:
+            extra["decoder_step_N1M_B8_zipf_20layers"] = r
         if rank == 0:
             line["secondary"] = extra
     if rank == 0:

@@ -96,3 +96,43 @@ def attend(dw, buf: DecodeBuffers, params=None, stream=None):
                        dw.pos, dw.swa_first, dw.swa_cnt, buf.n_q, buf.out, buf.out_dtype, params, buf.ws,
                        buf.ws_attn_bytes, stream)
     return buf.out
+
+
+class DecoderStep:
+    """The decoder's layers in one step over the C ABI (layers as in
+    gen.workloads.DECODER_LAYERS: (role, r) with role full / reindex / reuse):
+    the Full layer scores every visible entry, keeps the top-512 and picks the
+    pool of 2,048 blocks of 8 from the same scores; each Reindex layer r scores
+    the pool with its own indexer query and keeps its top-512; every layer
+    attends with its own query and window over the selection of the selecting
+    layer it names (Reuse layers borrow it).  One stream, no host sync."""
+
+    def __init__(self, n_q: int, n_max: int, layers, out_dtype=L.CSA2_OUT_F32, device="cuda"):
+        self.layers, self.n_q, self.n_max = list(layers), n_q, n_max
+        self.buf = DecodeBuffers(n_q, n_max, pool=True, out_dtype=out_dtype, device=device)
+        n_sel = 1 + max(r for _, r in self.layers)
+        self.sels = torch.empty((n_sel, n_q, TOPK), dtype=torch.int32, device=device)
+        odt = torch.bfloat16 if out_dtype == L.CSA2_OUT_BF16 else torch.float32
+        self.outs = torch.empty((len(self.layers), n_q, 64, 512), dtype=odt, device=device)
+        self.out_dtype = out_dtype
+
+    def run(self, dw, dl, params=None, stream=None):
+        b, n_q = self.buf, self.n_q
+        for l, (role, r) in enumerate(self.layers):
+            if role == "full":
+                L.csa2_index_score(dw.key_nib, dw.key_scale, dw.n_max, dw.kv.shape[0], dw.q_nib, dw.q_scale, dw.w,
+                                   dw.q_seq, dw.n_vis, n_q, None, b.scores, b.n_max, params, stream)
+                L.csa2_topk(b.scores, b.n_max, n_q, dw.n_vis, dw.n_max, TOPK, 1, None, self.sels[r], b.ws,
+                            b.ws_topk_bytes, stream)
+                L.csa2_topk(b.scores, b.n_max, n_q, dw.n_vis, dw.n_max, POOL_BLOCKS, 8, None, b.blocks, b.ws,
+                            b.ws_topk_bytes, stream)
+            elif role == "reindex":
+                L.csa2_index_score(dw.key_nib, dw.key_scale, dw.n_max, dw.kv.shape[0], dl.q_nib_re[r],
+                                   dl.q_scale_re[r], dl.w_re[r], dw.q_seq, dw.n_vis, n_q, b.blocks, b.pool_scores,
+                                   POOL_SLOTS, params, stream)
+                L.csa2_topk(b.pool_scores, POOL_SLOTS, n_q, dw.n_vis, dw.n_max, TOPK, 1, b.blocks, self.sels[r],
+                            b.ws, b.ws_topk_bytes, stream)
+            L.csa2_sparse_attn(dl.q[l], dw.kv, dw.n_max, dw.kv.shape[0], self.sels[r], TOPK, dl.swa[l],
+                               dl.swa.shape[2], dw.q_seq, dw.pos, dw.swa_first, dw.swa_cnt, n_q, self.outs[l],
+                               self.out_dtype, params, b.ws, b.ws_attn_bytes, stream)
+        return self.outs

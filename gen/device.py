@@ -181,3 +181,45 @@ def build_device_workload(wl: Workload, n_max: int | None = None, chunk: int = 1
     dw.swa_first, dw.swa_cnt = i32(wl.swa_first()), i32(wl.swa_cnt())
     assert int(g.walk_fail.item()) == 0
     return dw
+
+
+@dataclass
+class DecoderLayers:
+    """Device tensors of the decoder step's layers (see gen.workloads.DECODER_LAYERS):
+    per layer an attention query and a window cache (layer 0 shares the
+    workload's), per Reindex layer r an indexer query and weights."""
+    q: object           # bf16 [L, n_q, 64, 512]
+    swa: object         # uint8 [L, n_seq, swa_cap, 528]
+    q_nib_re: dict      # r -> uint8 [n_q * 32, 64]
+    q_scale_re: dict    # r -> uint8 [n_q * 32, 4]
+    w_re: dict          # r -> fp32 [n_q, 32]
+
+
+def build_decoder_layers(wl: Workload, dw: DeviceWorkload, layers) -> DecoderLayers:
+    import torch
+    from compressed_sparse_attention_index_gb300 import CSA2_IDX_MXFP4, CSA2_SWA_MXFP8
+    g = DeviceGen("cuda")
+    L, n_q = len(layers), dw.q.shape[0]
+    q = torch.empty((L, n_q, H, D), dtype=torch.bfloat16, device="cuda")
+    swa = torch.zeros((L, wl.n_seq, wl.swa_cap, 528), dtype=torch.uint8, device="cuda")
+    q[0].copy_(dw.q)
+    swa[0].copy_(dw.swa)
+    for l in range(1, L):
+        for qi in range(n_q):
+            g.normal_bf16(wl.seed, G.S_LQ, l * G.LAYER_SUB + qi, 0, H, D, out=q[l, qi])
+        for b in range(wl.n_seq):
+            rows = g.normal_bf16(wl.seed, G.S_LSWA, l * G.LAYER_SUB + b, 0, wl.swa_cap, D)
+            _pack(CSA2_SWA_MXFP8, rows, wl.swa_cap, 1, None, swa[l, b], None)
+    q_nib_re, q_scale_re, w_re = {}, {}, {}
+    for r in sorted({r for role, r in layers if role == "reindex"}):
+        qidx = torch.empty((n_q * HI, DI), dtype=torch.bfloat16, device="cuda")
+        w = torch.empty((n_q, HI), dtype=torch.float32, device="cuda")
+        for qi in range(n_q):
+            g.normal_bf16(wl.seed, G.S_QIDX_RE, r * G.LAYER_SUB + qi, 0, HI, DI, out=qidx[qi * HI:(qi + 1) * HI])
+            g.weights_f32(wl.seed, G.S_W_RE, r * G.LAYER_SUB + qi, 0, 1, out=w[qi:qi + 1])
+        q_nib_re[r] = torch.empty((n_q * HI, 64), dtype=torch.uint8, device="cuda")
+        q_scale_re[r] = torch.empty((n_q * HI, 4), dtype=torch.uint8, device="cuda")
+        _pack(CSA2_IDX_MXFP4, qidx, n_q * HI, 1, None, q_nib_re[r], q_scale_re[r])
+        w_re[r] = w
+    assert int(g.walk_fail.item()) == 0
+    return DecoderLayers(q, swa, q_nib_re, q_scale_re, w_re)

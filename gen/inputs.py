@@ -47,6 +47,9 @@ S_QIDX_RE = 9     # Reindex-layer indexer queries
 S_W_RE = 10       # Reindex-layer indexer weights
 S_SCORES = 11     # raw fp32 scores for top-k tests
 S_MISC = 12       # anything else a test needs
+S_LQ = 13         # attention queries of the decoder step's other layers (sub = layer * 65536 + query)
+S_LSWA = 14       # sliding-window entries of those layers (sub = layer * 65536 + sequence)
+LAYER_SUB = 65536  # sub-stream stride per layer (Reindex layer r: S_QIDX_RE / S_W_RE with sub r * 65536 + query)
 
 W_STD_F32 = np.float32(1.0 / np.sqrt(32.0))   # weights ~ N(0, variance 1/32)
 

@@ -99,6 +99,25 @@ class Workload:
     def w(self, qi: int, reindex: bool = False) -> np.ndarray:
         return G.weights_f32(self.seed, G.S_W_RE if reindex else G.S_W, qi, [0], HI)[0]
 
+    # ---- the decoder step's layers (see DECODER_LAYERS): layer 0 is the Full
+    # layer and uses the tensors above; layer l > 0 has its own attention query
+    # and window, Reindex layer r its own indexer query and weights
+    def q_layer(self, qi: int, layer: int) -> np.ndarray:
+        if layer == 0:
+            return self.q(qi)
+        return G.normal_block_bf16(self.seed, G.S_LQ, layer * G.LAYER_SUB + qi, 0, H, D)
+
+    def swa_rows_layer(self, seq: int, slots, layer: int) -> np.ndarray:
+        if layer == 0:
+            return self.swa_rows(seq, slots)
+        return G.normal_rows_bf16(self.seed, G.S_LSWA, layer * G.LAYER_SUB + seq, slots, D)
+
+    def qidx_reindex(self, qi: int, r: int) -> np.ndarray:
+        return G.normal_block_bf16(self.seed, G.S_QIDX_RE, r * G.LAYER_SUB + qi, 0, HI, DI)
+
+    def w_reindex(self, qi: int, r: int) -> np.ndarray:
+        return G.weights_f32(self.seed, G.S_W_RE, r * G.LAYER_SUB + qi, [0], HI)[0]
+
 
 CONFIGS = {
     0: Workload("tiny_full_decode_N4096_B1", 0, 1, 4096, 1),
@@ -107,6 +126,19 @@ CONFIGS = {
     3: Workload("reindex_decode_N1M_B64", 3, 64, 1 << 20, 64, pool=True),
     4: Workload("long_full_decode_N1M_B8_zipf", 4, 8, 1 << 20, 8, zipf=True),
 }
+
+# The decoder's twenty layers in one step (perchy.ai card "Full. Reindex.
+# Reuse."; the study's reading notes): the Full layer (layer 0: it scores the
+# whole cache, selects 512 entries and picks the 2,048-block pool), four
+# Reindex layers (each scores the pool with its own indexer query and selects
+# 512), and fifteen Reuse layers, each borrowing the selection of the nearest
+# Full or Reindex layer before it (20 decoder layers = 1 + 4 + 15; the order
+# within the decoder is not given on the pages: three Reuse layers follow each
+# selecting layer).  Entries: (role, r) with r the selecting layer's number
+# (0 = Full, 1..4 = Reindex r).
+DECODER_LAYERS = [("full", 0)] + [("reuse", 0)] * 3
+for _r in range(1, 5):
+    DECODER_LAYERS += [("reindex", _r)] + [("reuse", _r)] * 3
 
 # Multi-query decode (the next row after the five workloads above): the 8 x 1M
 # Zipf caches with five draft positions per sequence decoded in one step.

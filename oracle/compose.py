@@ -22,7 +22,7 @@ import numpy as np
 from gen.workloads import Workload, TOPK, SWA, BLOCK, POOL_BLOCKS
 
 __all__ = ["packed_keys", "kv_records", "swa_records", "query_inputs", "decode_query",
-           "full_scores", "reindex_query", "reindex_on_pool"]
+           "full_scores", "reindex_query", "reindex_on_pool", "decoder_step_query", "layer_attention"]
 
 
 def _o():
@@ -107,18 +107,23 @@ def decode_query(wl: Workload, qi: int, k: int = TOPK) -> dict:
     return {"scores": s, "sel": sel, "out": _attend(wl, qi, sel)}
 
 
-def reindex_on_pool(wl: Workload, qi: int, blocks, k: int = TOPK) -> dict:
+def reindex_on_pool(wl: Workload, qi: int, blocks, k: int = TOPK, layer: int = 0) -> dict:
     """The Reindex layer's own step for query qi over a given pool of 8-entry
     blocks (block ids, -1 = none): its indexer query scores the pool's visible
     positions, and the top-k of those scores (lower position first on ties,
-    positions ascending) is the selection."""
+    positions ascending) is the selection.  layer: which Reindex layer's query
+    and weights (0: the single Reindex layer of the Reindex workload; 1..4:
+    the decoder step's Reindex layers)."""
     o = _o()
     seq, n = int(wl.q_seq()[qi]), int(wl.n_vis()[qi])
     blocks = np.asarray(blocks)
     vb = np.sort(blocks[blocks >= 0].astype(np.int64))
     pos = (vb[:, None] * BLOCK + np.arange(BLOCK)[None, :]).reshape(-1)
     pos = pos[pos < n]
-    qidx, w = query_inputs(wl, qi, reindex=True)
+    if layer == 0:
+        qidx, w = query_inputs(wl, qi, reindex=True)
+    else:
+        qidx, w = o.pack_idx(wl.qidx_reindex(qi, layer)), wl.w_reindex(qi, layer)
     s_pool = o.index_score(packed_keys(wl, seq, n)[pos], qidx, w)
     loc = o.topk(s_pool, k)
     sel = np.where(loc >= 0, pos[np.maximum(loc, 0)], -1).astype(np.int32)
@@ -134,3 +139,43 @@ def reindex_query(wl: Workload, qi: int, k: int = TOPK) -> dict:
     r = reindex_on_pool(wl, qi, blocks, k)
     return {"scores_full": s_full, "blocks": blocks, "pool_pos": r["pool_pos"], "scores_pool": r["scores_pool"],
             "sel": r["sel"], "out": _attend(wl, qi, r["sel"])}
+
+
+def layer_attention(wl: Workload, qi: int, layer: int, sel) -> np.ndarray:
+    """Attention of decoder layer `layer` for query qi over the selection
+    `sel` (entry indices, -1 padding) and that layer's own window."""
+    o = _o()
+    seq = int(wl.q_seq()[qi])
+    sel = np.asarray(sel)
+    kv = kv_records(wl, seq, sel[sel >= 0])
+    first, cnt = int(wl.swa_first()[qi]), int(wl.swa_cnt()[qi])
+    slots = (first + np.arange(cnt, dtype=np.int64)) % wl.swa_cap
+    sw = o.pack_swa(wl.swa_rows_layer(seq, slots, layer)) if cnt else np.zeros((0, o.SWA_BYTES), np.uint8)
+    return o.sparse_attn(wl.q_layer(qi, layer), kv, sw, int(wl.pos()[qi]))
+
+
+def decoder_step_query(wl: Workload, qi: int, layers, pool=None, sels=None) -> dict:
+    """The decoder's layers for query qi in the pages' roles [perchy card
+    "Full. Reindex. Reuse."; study, reading notes]: the Full layer scores the
+    whole cache, keeps the top-512 and picks the pool of 2,048 blocks of 8;
+    each Reindex layer scores the pool with its own indexer query and keeps its
+    top-512; each Reuse layer attends over the selection of the selecting
+    layer it names.  Every layer attends with its own query and window.
+    pool / sels (optional): the pool and the selections to attend over (for
+    checking a GPU run's attention on its own selections); by default the
+    oracle's.  Returns the pool, the oracle's selections {r: sel} with their
+    scores, and the layers' outputs."""
+    o = _o()
+    s_full = full_scores(wl, qi)
+    osel = {0: o.topk(s_full, TOPK)}
+    opool = o.pool_blocks(s_full, BLOCK, POOL_BLOCKS)
+    use_pool = opool if pool is None else np.asarray(pool)
+    scores = {0: (np.arange(s_full.size), s_full)}
+    for role, r in layers:
+        if role == "reindex" and r not in osel:
+            rp = reindex_on_pool(wl, qi, use_pool, layer=r)
+            osel[r] = rp["sel"]
+            scores[r] = (rp["pool_pos"], rp["scores_pool"])
+    att = sels if sels is not None else osel
+    outs = [layer_attention(wl, qi, l, att[r]) for l, (role, r) in enumerate(layers)]
+    return {"pool": opool, "sel": osel, "scores": scores, "out": outs}

@@ -231,3 +231,28 @@ def test_attn_f64_is_sparse_attn_on_dequantised_records(oracle_lib):
     a = oracle_lib.sparse_attn(q, kv, sw, 321)
     b = oracle_lib.attn_f64(G.bf16_bits_to_f32(q).astype(np.float64), K, 321)
     assert np.array_equal(a, b)
+
+
+def test_decoder_step_roles(oracle_lib):
+    """The decoder step's composition: every Reindex selection lies inside the
+    Full layer's pool; a Reuse layer attending with its selecting layer's own
+    query reproduces that layer's output exactly; and when the cache fits the
+    pool (16,384 positions or fewer) a Reindex layer given the Full layer's
+    indexer query selects exactly the Full layer's entries."""
+    from gen.workloads import small, DECODER_LAYERS
+    wl = small(n_seq=1, n_entries=40_000, seed=61)
+    r = oracle_lib.decoder_step_query(wl, 0, DECODER_LAYERS)
+    pool = r["pool"][r["pool"] >= 0].astype(np.int64)
+    in_pool = set((pool[:, None] * 8 + np.arange(8)).reshape(-1).tolist())
+    for k in range(1, 5):
+        s = r["sel"][k]
+        assert set(s[s >= 0].tolist()) <= in_pool
+    # a Reuse layer (layer 1 borrows layer 0's selection) with layer 0's query
+    a = oracle_lib.layer_attention(wl, 0, 0, r["sel"][0])
+    assert np.array_equal(a, r["out"][0])
+    # pool = whole cache: Reindex with the Full layer's indexer query = Full selection
+    wl2 = small(n_seq=1, n_entries=12_000, seed=62)
+    wl2.qidx_reindex = lambda qi, layer: wl2.qidx(qi)
+    wl2.w_reindex = lambda qi, layer: wl2.w(qi)
+    r2 = oracle_lib.decoder_step_query(wl2, 0, DECODER_LAYERS[:5])
+    assert np.array_equal(r2["sel"][1], r2["sel"][0])
