@@ -23,7 +23,7 @@ STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED", 3:
 EXPORTS = ["csa2_default_params", "csa2_entry_bytes", "csa2_status_string", "csa2_fp4_pack",
            "csa2_index_score", "csa2_topk", "csa2_sparse_attn", "csa2_workspace_size",
            "csa2_get_device_status", "csa2_topk_noalloc", "csa2_decode", "csa2_decode_host",
-           "csa2_index_score_mq", "csa2_decode_mq"]
+           "csa2_index_score_mq", "csa2_decode_mq", "csa2_check_bounded_wait"]
 
 
 class CSA2Error(RuntimeError):
@@ -68,6 +68,7 @@ def load(path: str = LIB_PATH):
         "csa2_sparse_attn": (i32, [P, P, i64, i32, P, i32, P, i32, P, P, P, P, i32, P, i32, PP, P, sz, P]),
         "csa2_workspace_size": (i32, [i32, i32, i64, i32, ctypes.POINTER(sz)]),
         "csa2_get_device_status": (i32, [P, ctypes.POINTER(i32)]),
+        "csa2_check_bounded_wait": (i32, [ctypes.c_uint, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -189,6 +190,13 @@ def csa2_decode_host(key_nib, key_scale, n_max, n_seq, kv_cache, swa_cache, swa_
         _ptr(key_nib), _ptr(key_scale), int(n_max), int(n_seq), _ptr(kv_cache), _ptr(swa_cache), int(swa_cap),
         _ptr(h_q), _ptr(h_qidx), _ptr(h_w), _ptr(h_desc), int(n_q), _ptr(h_sel), _ptr(h_out), int(out_dtype), pp,
         _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def csa2_check_bounded_wait(limit_us, stream=None):
+    """Self-test of the bounded waits: a wait that cannot finish ends after
+    limit_us with CSA2_ERR_TIMEOUT in the device status (read it with
+    csa2_get_device_status)."""
+    _check("csa2_check_bounded_wait", load().csa2_check_bounded_wait(int(limit_us), _stream(stream)))
 
 
 def csa2_get_device_status(stream=None) -> int:

@@ -402,6 +402,13 @@ csa2_status csa2_decode_host(const void *key_nib, const void *key_scale, int64_t
   return CSA2_OK;
 }
 
+csa2_status csa2_check_bounded_wait(unsigned limit_us, csa2_stream_t stream) {
+  if (limit_us < 1 || limit_us > 2000000) return CSA2_ERR_INVALID_ARG;
+  int *st = status_ptr();
+  if (st == nullptr) return CSA2_ERR_CUDA;
+  return from_cuda(launch_bounded_wait_check(st, 1000ull * limit_us, (cudaStream_t)stream));
+}
+
 csa2_status csa2_get_device_status(csa2_stream_t stream, csa2_status *out) {
   if (out == nullptr) return CSA2_ERR_INVALID_ARG;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CSA2_ERR_CUDA;

@@ -59,7 +59,7 @@ constexpr int kSmMref = kSmOnes16 + 128;        // float[64] running maxima
 constexpr int kSmAlpha = kSmMref + 256;         // float[64] rescale factors
 constexpr int kSmValid = kSmAlpha + 256;        // uint8[128] slot validity
 constexpr int kSmBars = kSmValid + 128;         // 2 mbarriers, tmem base, flags
-constexpr int kSmTotal = kSmBars + 32;
+constexpr int kSmTotal = kSmBars + 48;            // + the drain barrier at kSmBars + 32
 constexpr int kSmAlloc = kSmTotal + 1024;       // + alignment slack (<= 227 KB)
 constexpr uint32_t kAttTmemCols = 512;
 constexpr uint32_t kColS = 0;                   // S^T, dims 0..255 of the dot products: 64 columns
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   float(*red)[kHeads] = reinterpret_cast<float(*)[kHeads]>(sm + kSmPhi);   // [4][64], during the max only
   uint8_t *valid_sh = sm + kSmValid;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kSmBars);
-  uint64_t &bar_s = bars[0], &bar_o = bars[1];
+  uint64_t &bar_s = bars[0], &bar_o = bars[1], &bar_drain = bars[4];
   uint32_t &tmem_sh = *reinterpret_cast<uint32_t *>(sm + kSmBars + 16);
   volatile int &bad_sh = *reinterpret_cast<volatile int *>(sm + kSmBars + 24);
 
@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   if (t == 0) {
     ptx::mbar_init(&bar_s, 2);                       // two S issuers
     ptx::mbar_init(&bar_o, 5);                       // five O issuers
+    ptx::mbar_init(&bar_drain, 5);                   // the MMA issuers, once each, after a wait ran out
     bad_sh = 0;
     ptx::fence_mbar_init();
   }
@@ -610,6 +611,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     if (bad_sh) break;
   }
 
+  if (bad_sh) {
+    // A wait ran out: before the tensor memory is read and given back, every
+    // MMA this CTA issued must have finished.  Each issuer commits once more
+    // (the commit completes when all of that thread's earlier MMAs have) and
+    // all threads wait on it, bounded.
+    if (lane == 0 && warp < 5) ptx::tc_commit(&bar_drain);
+    ptx::mbar_wait(&bar_drain, 0);
+    ptx::tc_fence_after();
+  }
   if (!waited) {
     griddep_wait();
     griddep_launch();

@@ -151,6 +151,8 @@ cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_s
                            float sm_scale, double rope_base, void *ws, int *status, cudaStream_t st,
                            bool inputs_settled = false, int ahead_ctas = -1);
 
+cudaError_t launch_bounded_wait_check(int *status, unsigned long long limit_ns, cudaStream_t st);
+
 int *status_word_ptr();
 
 }  // namespace csa2

@@ -241,8 +241,10 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   // may be refilled and the unit's accumulator may be read (one commit serves both)
   __shared__ __align__(8) uint64_t full_bar[kScStages], sf_bar[kScStages], done_bar[kScStages];
   __shared__ __align__(8) uint64_t acc_empty[kScAcc];
+  __shared__ __align__(8) uint64_t drain_bar;      // after a wait ran out: the tcgen05 issuers' last commits
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
+  __shared__ int armed_sh;                         // iterations whose copies the producer issued
   __shared__ volatile unsigned long long unit_ring[kRing];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -256,8 +258,10 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       ptx::mbar_init(&done_bar[s], 1);
     }
     for (int a = 0; a < kScAcc; a++) ptx::mbar_init(&acc_empty[a], 4);
+    ptx::mbar_init(&drain_bar, 3);                  // MMA issuers (warps 1, 11) and the scale-factor warp
     for (int i = 0; i < kRing; i++) unit_ring[i] = ~0ull;   // no iteration's tag
     abort_flag = 0;
+    armed_sh = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) ptx::tmem_alloc(&tmem_base_sh, kScTmemCols);
@@ -341,6 +345,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         pg.prefetch(P, 0, T + gridDim.x, sc, total_units);
       }
       __syncwarp();
+      if (lane == 0) armed_sh = (int)it + 1;
       T += gridDim.x;
     }
   } else if (warp == 2) {
@@ -533,6 +538,22 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       if (P.smax_mode == 3 && lane == 0) P.smax[(int64_t)sc.q * P.sstride + (int64_t)cur_u * 4 + quarter] = umax;
     }
   }
+  __syncthreads();
+  if (abort_flag) {
+    // A wait ran out.  Before the CTA gives its tensor memory back and exits,
+    // nothing it started may still be running: the copies of the last
+    // kScStages iterations the producer issued (waited on their barriers;
+    // pool mode: every gathering lane waits for its own asynchronous copies)
+    // and the MMAs and scale-factor copies (each issuer commits once more).
+    // All bounded.
+    if (warp == 0 && lane == 0) {
+      for (int i = max(0, armed_sh - kScStages); i < armed_sh; i++)
+        ptx::mbar_wait(&full_bar[i % kScStages], (uint32_t)(i / kScStages) & 1);
+    }
+    if (P.pool != nullptr && (warp == 0 || warp >= kScGather0)) asm volatile("cp.async.wait_all;" ::: "memory");
+    if (lane == 0 && (warp == 1 || warp == 2 || warp == kScMmaWarp2)) ptx::tc_commit(&drain_bar);
+    ptx::mbar_wait(&drain_bar, 0);
+  }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -589,8 +610,10 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
   unsigned char *qslots = smem + kMqStages * kMqStageBytes;
   __shared__ __align__(8) uint64_t full_bar[kMqStages], sf_bar[kMqStages], done_bar[kMqStages];
   __shared__ __align__(8) uint64_t acc_empty[2];
+  __shared__ __align__(8) uint64_t drain_bar;      // after a wait ran out: the tcgen05 issuers' last commits
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
+  __shared__ int armed_sh;                         // iterations whose copies the producer issued
   __shared__ volatile unsigned long long unit_ring[kMqRing];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -605,8 +628,10 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
     }
     ptx::mbar_init(&acc_empty[0], 4);
     ptx::mbar_init(&acc_empty[1], 4);
+    ptx::mbar_init(&drain_bar, 2);                  // the MMA issuer and the scale-factor warp
     for (int i = 0; i < kMqRing; i++) unit_ring[i] = ~0ull;
     abort_flag = 0;
+    armed_sh = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) ptx::tmem_alloc(&tmem_base_sh, kScTmemCols);
@@ -680,6 +705,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
         ptx::bulk_load(st + kMqOffSFA, P.key_scale + r0 * 4, 512u, &full_bar[s]);
       }
       __syncwarp();
+      if (lane == 0) armed_sh = (int)it + 1;
       T += gridDim.x;
     }
   } else if (warp == 2) {
@@ -810,12 +836,53 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
       if (lane == 0) ptx::mbar_arrive(&acc_empty[grp]);
     }
   }
+  __syncthreads();
+  if (abort_flag) {
+    // a wait ran out: as in the single-query kernel, the producer's last
+    // copies and the issuers' tcgen05 operations finish before TMEM goes back
+    if (warp == 0 && lane == 0) {
+      for (int i = max(0, armed_sh - kMqStages); i < armed_sh; i++)
+        ptx::mbar_wait(&full_bar[i % kMqStages], (uint32_t)(i / kMqStages) & 1);
+    }
+    if (lane == 0 && (warp == 1 || warp == 2)) ptx::tc_commit(&drain_bar);
+    ptx::mbar_wait(&drain_bar, 0);
+  }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kScTmemCols);
   }
+}
+
+// ---------------------------------------------------------------- bounded-wait check
+// One warp takes tensor memory, waits on a barrier that nothing completes with
+// a short wall-time limit, records CSA2_ERR_TIMEOUT, gives the memory back and
+// exits: the path every kernel here takes when a wait runs out, with nothing
+// asynchronous in flight.
+__global__ void __launch_bounds__(32, 1) bounded_wait_check_kernel(int *status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t never;
+  __shared__ uint32_t tmem_sh;
+  griddep_wait();
+  griddep_launch();
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&never, 1);                       // its one arrival never comes
+    ptx::fence_mbar_init();
+  }
+  ptx::tmem_alloc(&tmem_sh, 32);
+  ptx::tc_fence_before();
+  __syncwarp();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_sh;
+  if (!ptx::mbar_wait(&never, 0, limit_ns) && threadIdx.x == 0) record_error(status, CSA2_ERR_TIMEOUT);
+  ptx::tc_fence_before();
+  __syncwarp();
+  ptx::tc_fence_after();
+  ptx::tmem_dealloc(tmem, 32);
+}
+
+cudaError_t launch_bounded_wait_check(int *status, unsigned long long limit_ns, cudaStream_t st) {
+  return launch_pdl(bounded_wait_check_kernel, dim3(1), dim3(32), 0, st, 1u, status, limit_ns);
 }
 
 // ---------------------------------------------------------------- host side

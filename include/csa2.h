@@ -379,6 +379,18 @@ csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stride, int n_q
                               csa2_stream_t stream);
 
 /*
+ * csa2_check_bounded_wait -- self-test of the library's bounded waits (the
+ * pages have no counterpart).  Launches one warp that takes tensor memory,
+ * waits on a barrier that nothing will complete, gives up after limit_us
+ * microseconds (1 .. 2,000,000), records CSA2_ERR_TIMEOUT in the device
+ * status word, returns the tensor memory and exits: the path every kernel of
+ * this library takes when one of its waits runs out (each of them bounded by
+ * 2 s of wall time), with nothing asynchronous in flight.  Read the outcome
+ * with csa2_get_device_status; the context stays usable.
+ */
+csa2_status csa2_check_bounded_wait(unsigned limit_us, csa2_stream_t stream);
+
+/*
  * csa2_get_device_status -- synchronises `stream`, returns in *out the first
  * device-side error recorded by any kernel of this library on the current
  * device since the last call (CSA2_OK if none), and clears it.

@@ -76,6 +76,8 @@ def test_host_validation_rejects_before_launch(lib):
     assert L.csa2_decode_host(*args, fake, fake, fake, None, 1, None, fake, 0, None, fake, 1 << 30, None) == INVALID
     assert L.csa2_decode_host(*args, fake, fake, fake, fake, 1, None, fake, 0, None, fake, 1024, None) == WS
     assert L.csa2_decode_host(*args, fake, fake, fake, fake, 1, None, fake, 7, None, fake, 1 << 30, None) == INVALID
+    assert L.csa2_check_bounded_wait(0, None) == INVALID                                 # limit out of range
+    assert L.csa2_check_bounded_wait(2_000_001, None) == INVALID
     assert L.csa2_get_device_status(None, None) == INVALID
 
 

@@ -400,3 +400,24 @@ def test_decode_host_equals_device_call(lib, out_f32):
         assert torch.equal(h_out.view(torch.int16 if not out_f32 else torch.int32),
                            ref.out.cpu().view(torch.int16 if not out_f32 else torch.int32))
         h_out.fill_(7)
+
+
+def test_bounded_wait_runs_out_cleanly(lib):
+    """A wait that nothing completes ends after its limit with
+    CSA2_ERR_TIMEOUT in the status word (no trap, no hang), and the context
+    stays usable: a decode afterwards is exact."""
+    import time
+    t0 = time.time()
+    lib.csa2_check_bounded_wait(2000)                    # 2 ms
+    assert lib.csa2_get_device_status() == 5            # CSA2_ERR_TIMEOUT
+    assert time.time() - t0 < 5.0
+    assert lib.csa2_get_device_status() == 0            # read and cleared
+    from compressed_sparse_attention_index_gb300 import decode
+    wl = small(n_seq=2, n_entries=20_000, seed=253)
+    dw = _dw(wl)
+    chain, fused = _bufs(dw), _bufs(dw)
+    decode.full_decode(dw, chain)
+    decode.fused_decode(dw, fused)
+    assert lib.csa2_get_device_status() == 0
+    assert torch.equal(chain.sel, fused.sel)
+    assert torch.equal(chain.out.view(torch.int32), fused.out.view(torch.int32))
