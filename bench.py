@@ -48,8 +48,7 @@ IDX_BYTES = 68
 # dram__bytes_read.sum + dram__bytes_write.sum of one index_score_tc_kernel launch inside
 # csa2_decode, from an ncu capture (--metrics dram__bytes_read.sum,dram__bytes_write.sum) of the
 # current kernel on the named workload; workloads without such a capture report null.
-INDEX_SCORE_TRAFFIC = {"long_full_decode_N1M_B8_zipf": 570_499_840 + 5_160_448,
-                       "reindex_decode_N1M_B64": 84_263_680 + 2_083_072}
+INDEX_SCORE_TRAFFIC = {"long_full_decode_N1M_B8_zipf": 570_499_840 + 4_984_576}
 
 
 def parse():
@@ -61,7 +60,10 @@ def parse():
     ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
-                    help="with the default workload, skip the secondary 32 x 64K and Reindex lines")
+                    help="with the default workload, skip the secondary workloads")
+    ap.add_argument("--only", choices=["mq", "layers"], default=None,
+                    help="run and print only one secondary workload: the multi-query decode (mq) or the "
+                         "20-layer decoder step (layers)")
     return ap.parse_args()
 
 
@@ -611,6 +613,14 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
+    if args.only is not None:
+        r = (run_mq if args.only == "mq" else run_layers)(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(r))
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     line = run_ours(args, rank, world, local_rank)
     if args.config == 4 and not args.no_extra:
         # secondary workloads in the same run, as keys of the one line: the
