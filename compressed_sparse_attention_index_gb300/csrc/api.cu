@@ -46,9 +46,19 @@ static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 // csa2_decode's workspace, each part 256-B aligned:
 // scores [n_q][n_max] fp32 | top-k scratch | attention partials
+// csa2_decode's workspace: scores | top-k scratch | attention partials | the
+// candidate handoff (flags, then keys), where the selection hands its
+// candidates to the attention (the maxima come from the indexer and all
+// attention CTAs holding candidates fit one wave).
+static bool decode_handoff(int n_q, int64_t n_max) {
+  return topk_fused_plan(nullptr, n_q, n_max, kTopK).mode > 0 && attn_handoff_fits(n_q);
+}
 static size_t decode_workspace_bytes(int n_q, int64_t n_max) {
-  return round256((size_t)n_q * (size_t)n_max * 4) + round256(topk_fused_bytes(n_q, n_max, kTopK)) +
-         round256(attn_workspace_bytes(n_q, kTopK));
+  const bool hand = decode_handoff(n_q, n_max);
+  size_t b = round256((size_t)n_q * (size_t)n_max * 4) + round256(topk_fused_bytes(n_q, n_max, kTopK)) +
+             round256(attn_workspace_bytes(n_q, hand ? kHandCap : kTopK));
+  if (hand) b += round256((size_t)n_q * kHandWords * 4) + round256((size_t)n_q * kHandCtas * kHandSeg * 8);
+  return b;
 }
 
 }  // namespace csa2
@@ -133,16 +143,18 @@ csa2_status csa2_index_score(const void *key_nib, const void *key_scale, int64_t
       scores, score_stride, st, (cudaStream_t)stream));
 }
 
-// csa2_decode_host's device staging, each part 256-B aligned, after the
-// decode workspace: q | indexer query bf16 | its packed nibbles | its scales |
+// csa2_decode_host's device staging, after the decode workspace (from a
+// 512-B boundary on), each part 512-B aligned (csa2_decode wants its packed
+// indexer query so): q | indexer query bf16 | its packed nibbles | its scales |
 // w | descriptors [5][n_q] | sel | out (fp32-sized)
+static size_t round512(size_t b) { return (b + 511) / 512 * 512; }
 struct HostStage {
   size_t q, qidx, qnib, qsc, w, desc, sel, out, total;
 };
 static HostStage host_stage(int n_q) {
   HostStage h;
   size_t o = 0;
-  auto take = [&](size_t b) { const size_t at = o; o += round256(b); return at; };
+  auto take = [&](size_t b) { const size_t at = o; o += round512(b); return at; };
   h.q = take((size_t)n_q * kHeads * kDim * 2);
   h.qidx = take((size_t)n_q * kIdxHeads * kIdxDim * 2);
   h.qnib = take((size_t)n_q * kIdxHeads * kIdxNibBytes);
@@ -170,7 +182,7 @@ csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t 
   }
   if (op == CSA2_OP_DECODE_HOST) {
     if (n_items <= 0) return CSA2_ERR_INVALID_ARG;
-    *bytes = round256(decode_workspace_bytes(n_q, n_items)) + host_stage(n_q).total;
+    *bytes = round512(decode_workspace_bytes(n_q, n_items)) + host_stage(n_q).total;
     return CSA2_OK;
   }
   if (op == CSA2_OP_TOPK) {
@@ -275,8 +287,17 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
   F.kv = static_cast<const uint8_t *>(kv_cache);
   F.q_seq = q_seq;
   F.n_seq = n_seq;
-  F.reserve = attn_ctas(n_q, kTopK);
   const bool fused = F.mode > 0;
+  const bool hand = decode_handoff(n_q, n_max);
+  F.reserve = attn_ctas(n_q, hand ? kHandCap : kTopK);
+  Handoff H = {nullptr, nullptr, 0};
+  if (hand) {
+    unsigned char *hb = static_cast<unsigned char *>(ws_attn) + round256(attn_workspace_bytes(n_q, kHandCap));
+    H.flag = reinterpret_cast<uint32_t *>(hb);
+    H.cand = reinterpret_cast<uint64_t *>(hb + round256((size_t)n_q * kHandWords * 4));
+    H.parts = topk_fused_ctas(F, n_q, n_max) / n_q;   // the selection's cluster size
+    F.W.hand = H;
+  }
   cudaError_t e = launch_index_score_tc(static_cast<const uint8_t *>(key_nib), static_cast<const uint8_t *>(key_scale),
                                         n_max, n_seq, static_cast<const uint8_t *>(q_nib),
                                         static_cast<const uint8_t *>(q_scale), w, q_seq, n_vis, n_q, nullptr, scores,
@@ -290,7 +311,7 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
   // every earlier grid), so the attention may stage them during the top-k
   return from_cuda(launch_attn_tc(q, kv_cache, n_max, n_seq, sel, kTopK, swa_cache, swa_cap, q_seq, pos, swa_first,
                                   swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, ws_attn, st, s, true,
-                                  topk_fused_ctas(F, n_q, n_max)));
+                                  topk_fused_ctas(F, n_q, n_max), hand ? &H : nullptr));
 }
 
 csa2_status csa2_index_score_mq(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq,
@@ -372,7 +393,7 @@ csa2_status csa2_decode_host(const void *key_nib, const void *key_scale, int64_t
   if (n_q > 65535) return CSA2_ERR_UNSUPPORTED;
   if (n_q == 0) return CSA2_OK;
   if (!h_q || !h_qidx || !h_w || !h_desc || !h_out) return CSA2_ERR_INVALID_ARG;
-  const size_t dec = round256(decode_workspace_bytes(n_q, n_max));
+  const size_t dec = round512(decode_workspace_bytes(n_q, n_max));
   const HostStage H = host_stage(n_q);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < dec + H.total) return CSA2_ERR_WORKSPACE;
   const cudaStream_t s = (cudaStream_t)stream;

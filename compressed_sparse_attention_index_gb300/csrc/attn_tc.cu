@@ -135,6 +135,12 @@ struct AttnTcArgs {
   int n_seq;
   const int32_t *sel;
   int sel_stride;
+  // entry slots ahead of the window: sel_stride, or kHandCap with the handoff
+  int n_sel;
+  // optional: the selection grid ahead hands its candidates over (null: off)
+  const uint32_t *hflag;
+  const uint64_t *hcand;
+  int hparts;       // selection CTAs per query (each publishes one segment of candidates)
   const uint8_t *swa;
   int swa_cap;
   const int32_t *q_seq, *pos, *swa_first, *swa_cnt;
@@ -164,7 +170,8 @@ __device__ __forceinline__ void rope_cs(double inv_freq, int pos, float &c, floa
 
 // NH: the heads one CTA handles (64, or 32 when two CTAs share each chunk:
 // the gather is repeated, the MMAs, the softmax and the read-out are halved).
-template <int NH>
+// HAND: the selection grid ahead hands its candidates over (A.hflag set).
+template <int NH, bool HAND>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   static_assert(NH == 64 || NH == 32, "heads per CTA");
   constexpr int HS = kHeads / NH;                 // CTAs per chunk
@@ -189,8 +196,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   // wait is put off until the first chunk that holds selected entries: Q is
   // staged and window-only chunks run while the selection finishes.  (TMEM is
   // taken before the wait only then, when the grid ahead is the top-k, which
-  // holds no TMEM.)
+  // holds no TMEM.)  With the handoff, that chunk waits only for the
+  // candidates, and the softmax for the smallest selected key; the grid
+  // completion wait moves to the end (no data of the grid ahead is read after
+  // it), and the grid that follows may be placed at once.
+  __shared__ uint32_t hand_sh;
+  __shared__ uint64_t kth_sh;
+  __shared__ int hoff_sh[kHandCtas + 1];           // first candidate slot of each segment
   bool waited = false;
+  if (HAND) griddep_launch();
   if (!A.settled) {
     griddep_wait();
     griddep_launch();
@@ -201,7 +215,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   const bool bad = seq < 0 || seq >= A.n_seq || swa_cnt < 0 || swa_cnt > kSwa || swa_cnt > A.swa_cap ||
                    (swa_cnt > 0 && (swa_first < 0 || swa_first >= A.swa_cap));
   if (bad && t == 0 && split == 0 && h0 == 0) record_error(A.status, CSA2_ERR_BOUNDS);
-  const int n_slots = A.sel_stride + (bad ? 0 : swa_cnt);
+  const int n_slots = A.n_sel + (bad ? 0 : swa_cnt);
   const int c0 = split * A.chunks_per_split;
   const int c1 = bad ? c0 : min((n_slots + kTcChunk - 1) / kTcChunk, c0 + A.chunks_per_split);
 
@@ -219,11 +233,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     const int e = t >> 1, half = t & 1, slot = c0 * kTcChunk + e;
     const uint8_t *rec = nullptr;
     int bytes = 0;
-    if (slot < A.sel_stride) {
-      const int j = __ldg(A.sel + (int64_t)qi * A.sel_stride + slot);
+    if (slot < A.n_sel) {
+      const int j = slot < A.sel_stride ? __ldg(A.sel + (int64_t)qi * A.sel_stride + slot) : -1;
       if (j >= 0 && (int64_t)j < A.n_max) { rec = A.kv + ((int64_t)seq * A.n_max + j) * kKvBytes; bytes = kKvBytes; }
     } else if (slot < n_slots) {
-      const int ring = (swa_first + (slot - A.sel_stride)) % A.swa_cap;
+      const int ring = (swa_first + (slot - A.n_sel)) % A.swa_cap;
       rec = A.swa + ((int64_t)seq * A.swa_cap + ring) * kSwaBytes;
       bytes = kSwaBytes;
     }
@@ -284,8 +298,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     }
     return qscale;
   };
-  // the chunks of FP4 latents only (the first sel_stride / 128 ones) run in f16
-  auto chunk_f16 = [&](int c) { return (c + 1) * kTcChunk <= A.sel_stride; };
+  // the chunks of FP4 latents only (the first n_sel / 128 ones) run in f16
+  auto chunk_f16 = [&](int c) { return (c + 1) * kTcChunk <= A.n_sel; };
   bool q16 = c0 < c1 && chunk_f16(c0);
   float qscale = stage_q(q16);
   // all-ones A operands: one 8 x 16-B core matrix of 1.0 in bf16 and in f16,
@@ -311,13 +325,69 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   // discards the result (wp: the warm-up pass): the real pass then finds its
   // instructions in the SM's caches instead of fetching each phase's code as
   // it first runs.
-  const int warm = A.warm && !waited && c0 < c1 && c0 * kTcChunk < A.sel_stride ? 1 : 0;
+  const int warm = A.warm && !waited && c0 < c1 && c0 * kTcChunk < A.n_sel ? 1 : 0;
+  uint32_t hnc = 0;                                  // handoff: candidates + 1, or kHandFallback
+  bool got_sel = false;
   for (int c = c0, wp = warm; c < c1; c += 1 - wp, wp = 0) {
-    if (!waited && !wp && c * kTcChunk < A.sel_stride) {   // the chunk holds selected entries
-      griddep_wait();
-      griddep_launch();
-      waited = true;
+    const bool sel_chunk = !wp && c * kTcChunk < A.n_sel;   // the chunk holds selected entries (or candidates)
+    if (sel_chunk && !got_sel) {
+      got_sel = true;
+      if (!HAND) {
+        if (!waited) {
+          griddep_wait();
+          griddep_launch();
+          waited = true;
+        }
+      } else {
+        // every selection CTA of the query has published its segment: the
+        // segments' counts give each candidate slot; too many candidates, or a
+        // segment that could not be handed over, and the chunk waits for the
+        // final selection instead
+        const uint32_t *hf = A.hflag + (int64_t)qi * kHandWords;
+        if (t == 0) {
+          uint32_t v = 1u;                           // candidates + 1
+          if (!ptx::poll_at_least_u32(hf, (uint32_t)A.hparts)) {
+            record_error(A.status, CSA2_ERR_TIMEOUT);
+            bad_sh = 1;                              // (v = 1: no candidates)
+          } else {
+            uint32_t cnt[kHandCtas];                 // all counts in one round trip
+            const uint4 *c4 = reinterpret_cast<const uint4 *>(hf + 8);
+#pragma unroll
+            for (int v4 = 0; v4 < kHandCtas / 4; v4++) {
+              const uint4 x = __ldcg(c4 + v4);
+              cnt[4 * v4] = x.x;
+              cnt[4 * v4 + 1] = x.y;
+              cnt[4 * v4 + 2] = x.z;
+              cnt[4 * v4 + 3] = x.w;
+            }
+            int o = 0;
+            bool fb = false;
+#pragma unroll
+            for (int p = 0; p < kHandCtas; p++) {
+              if (p < A.hparts) {
+                hoff_sh[p] = o;
+                fb = fb || cnt[p] == kHandFallback;
+                o += fb ? 0 : (int)cnt[p];
+              }
+            }
+            hoff_sh[A.hparts] = o;
+            v = (fb || o > kHandCap) ? kHandFallback : (uint32_t)o + 1u;
+          }
+          if (v == kHandFallback && !ptx::poll_at_least_u32(hf + 1, 1u)) {   // the final selection
+            record_error(A.status, CSA2_ERR_TIMEOUT);
+            bad_sh = 1;
+            v = 1u;
+          }
+          hand_sh = v;
+        }
+        __syncthreads();
+        hnc = hand_sh;
+      }
     }
+    // handoff: candidates to be masked once the smallest selected key is out
+    const bool hand_live = HAND && sel_chunk && hnc != kHandFallback;
+    if (HAND && sel_chunk && c * kTcChunk >= (hand_live ? (int)hnc - 1 : A.sel_stride))
+      continue;                                      // uniform: the chunk holds no entry
     const bool f16c = chunk_f16(c);
     if (f16c != q16) {                                // the last chunk's MMAs are complete
       qscale = stage_q(f16c);
@@ -328,13 +398,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     const uint32_t id_qk = idesc_m128(0, f16c, NH), id_pv = idesc_m128(1, f16c, NH);
     const float sl2 = A.scale_log2 * (f16c ? qscale : 1.f);   // S was computed with Q x 2^-qs
     // ---------------------------------------------------------- gather + dequantise
+    uint64_t hk = 0ull;                              // handoff: this slot's candidate key
     {
       const int e = t >> 1, half = t & 1;             // entry slot e, dims [256*half, 256*half+256)
       const int slot = c * kTcChunk + e;
       const uint32_t rowbase = (e >> 3) * 8192;        // 8-entry group
       int ok = 0;
-      if (slot < A.sel_stride) {
-        const int j = wp ? ((int64_t)e < A.n_max ? e : -1) : __ldcg(A.sel + (int64_t)qi * A.sel_stride + slot);
+      if (slot < A.n_sel) {
+        int j = -1;
+        if (wp) {
+          j = (int64_t)e < A.n_max ? e : -1;
+        } else if (hand_live) {
+          if (slot < (int)hnc - 1) {                  // the key's low half is ~index
+            int p = 0;
+            while (slot >= hoff_sh[p + 1]) p++;
+            hk = __ldcg(A.hcand + ((int64_t)qi * kHandCtas + p) * kHandSeg + (slot - hoff_sh[p]));
+            j = (int)~(uint32_t)hk;
+          }
+        } else if (slot < A.sel_stride) {
+          j = __ldcg(A.sel + (int64_t)qi * A.sel_stride + slot);
+        }
         if (j >= 0 && (int64_t)j < A.n_max) {
           ok = 1;
           const uint8_t *rec = A.kv + ((int64_t)seq * A.n_max + j) * kKvBytes;
@@ -398,7 +481,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
         }
       } else if (slot < n_slots) {
         ok = 1;
-        const int ring = (swa_first + (slot - A.sel_stride)) % A.swa_cap;
+        const int ring = (swa_first + (slot - A.n_sel)) % A.swa_cap;
         const uint8_t *rec = A.swa + ((int64_t)seq * A.swa_cap + ring) * kSwaBytes;
         const uint2 scw = __ldg(reinterpret_cast<const uint2 *>(rec + 512 + half * 8));
         const uint32_t sc2[2] = {scw.x, scw.y};
@@ -454,6 +537,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
         ptx::tc_mma_bf16(tmem + col, ad, bd, id_qk, k2 > 0 ? 1u : 0u);
       }
       ptx::tc_commit(&bar_s);
+    }
+    // ---------------------------------------------------------- handoff mask
+    // while S is computed: candidates below the smallest selected key drop out
+    if (hand_live) {
+      if (t == 0) {
+        uint64_t K = 0ull;
+        if (!ptx::poll_nonzero_u64(reinterpret_cast<const uint64_t *>(A.hflag + (int64_t)qi * kHandWords + 2), K)) {
+          record_error(A.status, CSA2_ERR_TIMEOUT);
+          bad_sh = 1;
+          K = ~0ull;
+        }
+        kth_sh = K;
+      }
+      __syncthreads();
+      if ((t & 1) == 0 && valid_sh[t >> 1] != 0) valid_sh[t >> 1] = hk >= kth_sh ? 1 : 0;
+      __syncthreads();
     }
     // ---------------------------------------------------------- softmax (all 8 warps)
     int need_rescale = 0;
@@ -620,7 +719,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     ptx::mbar_wait(&bar_drain, 0);
     ptx::tc_fence_after();
   }
-  if (!waited) {
+  if (!waited && !HAND) {
     griddep_wait();
     griddep_launch();
   }
@@ -679,6 +778,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
       ml[h0 + t] = any_chunk ? m_ref[t] : -INFINITY;
     }
   }
+  // handoff: this grid completes after the selection grid ahead of it, as
+  // without it (the grids that follow rely on that)
+  if (HAND) griddep_wait();
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -788,6 +890,10 @@ int attn_ctas(int n_q, int sel_stride) {
   return n_q * p.nsplit * p.hs;
 }
 
+bool attn_handoff_fits(int n_q) {
+  return attn_plan(n_q, kHandCap, device_sm_count(current_device())).cps == 1;
+}
+
 size_t attn_workspace_bytes(int n_q, int sel_stride) {
   const AttnPlan p = attn_plan(n_q, sel_stride, device_sm_count(current_device()));
   if (p.nsplit == 1) return 0;
@@ -798,7 +904,7 @@ cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_s
                            const void *swa, int swa_cap, const int32_t *q_seq, const int32_t *pos,
                            const int32_t *swa_first, const int32_t *swa_cnt, int n_q, void *out, int out_dtype,
                            float sm_scale, double rope_base, void *ws, int *status, cudaStream_t st,
-                           bool inputs_settled, int ahead_ctas) {
+                           bool inputs_settled, int ahead_ctas, const Handoff *hand) {
   AttnTcArgs A;
   A.settled = inputs_settled ? 1 : 0;
   A.q = static_cast<const uint16_t *>(q);
@@ -807,6 +913,10 @@ cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_s
   A.n_seq = n_seq;
   A.sel = sel;
   A.sel_stride = sel_stride;
+  A.n_sel = hand != nullptr ? kHandCap : sel_stride;
+  A.hflag = hand != nullptr ? hand->flag : nullptr;
+  A.hcand = hand != nullptr ? hand->cand : nullptr;
+  A.hparts = hand != nullptr ? hand->parts : 0;
   A.swa = static_cast<const uint8_t *>(swa);
   A.swa_cap = swa_cap;
   A.q_seq = q_seq;
@@ -819,7 +929,7 @@ cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_s
   for (int i = 0; i < kRopeDim / 2; i++) A.inv_freq[i] = pow(rope_base, -2.0 * i / (double)kRopeDim);
   const int dev = current_device();
   const int n_sm = device_sm_count(dev);
-  const AttnPlan plan = attn_plan(n_q, sel_stride, n_sm);
+  const AttnPlan plan = attn_plan(n_q, A.n_sel, n_sm);
   A.nsplit = plan.nsplit;
   A.chunks_per_split = plan.cps;
   A.hsplit = plan.hs;
@@ -828,17 +938,25 @@ cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_s
   A.status = status;
   static std::atomic<int> attr_done[kMaxDevices];
   cudaError_t e = once_per_device(attr_done, dev, [&] {
-    cudaError_t e1 = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
-    cudaError_t e2 = cudaFuncSetAttribute(attn_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
-    return e1 != cudaSuccess ? e1 : e2;
+    const cudaError_t es[4] = {
+        cudaFuncSetAttribute(attn_tc_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc),
+        cudaFuncSetAttribute(attn_tc_kernel<32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc),
+        cudaFuncSetAttribute(attn_tc_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc),
+        cudaFuncSetAttribute(attn_tc_kernel<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc)};
+    for (cudaError_t x : es)
+      if (x != cudaSuccess) return x;
+    return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
   // the warm-up pays only where every CTA is resident while the grid ahead runs
   const int n_ctas = n_q * plan.nsplit * plan.hs;
   A.warm = inputs_settled && plan.cps == 1 && ahead_ctas >= 0 && ahead_ctas + n_ctas <= n_sm ? 1 : 0;
   const dim3 grid(n_q, A.nsplit * plan.hs);
-  e = plan.hs == 2 ? launch_pdl(attn_tc_kernel<32>, grid, dim3(kTcThreads), kSmAlloc, st, 1u, A)
-                   : launch_pdl(attn_tc_kernel<64>, grid, dim3(kTcThreads), kSmAlloc, st, 1u, A);
+  const bool h = A.hflag != nullptr;
+  e = plan.hs == 2 ? (h ? launch_pdl(attn_tc_kernel<32, true>, grid, dim3(kTcThreads), kSmAlloc, st, 1u, A)
+                        : launch_pdl(attn_tc_kernel<32, false>, grid, dim3(kTcThreads), kSmAlloc, st, 1u, A))
+                   : (h ? launch_pdl(attn_tc_kernel<64, true>, grid, dim3(kTcThreads), kSmAlloc, st, 1u, A)
+                        : launch_pdl(attn_tc_kernel<64, false>, grid, dim3(kTcThreads), kSmAlloc, st, 1u, A));
   if (e != cudaSuccess || A.nsplit == 1) return e;
   return launch_pdl(attn_tc_merge_kernel, dim3(kDim / 32, n_q), dim3(256), 0, st, 1u, A);
 }

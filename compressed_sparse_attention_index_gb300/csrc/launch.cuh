@@ -48,6 +48,30 @@ inline int current_device() {
   return dev;
 }
 
+// Candidate handoff inside csa2_decode.  Every CTA of a query's selection
+// cluster publishes its candidates (its entries reaching the threshold, in
+// ascending index order; together a superset of the selected entries) as soon
+// as it has them; CTA 0 publishes the smallest selected key the moment its
+// exact selection finds it.  The attention gathers and scores the candidates
+// meanwhile and masks those below that key.  Per query, flag holds kHandWords
+// words: [0] selection CTAs that have published (release); [1] nonzero once
+// the selection (sel) is final (release); [2..3] the smallest selected key
+// (never 0; it is the only datum read after it, so a plain store);
+// [8 + p] CTA p's candidate count, or kHandFallback where its list cannot be
+// handed over (the attention then reads the final selection).  Words 0-3 are
+// zeroed by the indexer of the same call.  cand holds
+// [n_q][kHandCtas][kHandSeg] keys, CTA p's in segment p.
+constexpr int kHandCap = 640;       // candidates the attention takes (5 chunks of 128)
+constexpr int kHandCtas = 16;       // selection CTAs per query, at most
+constexpr int kHandSeg = 256;       // candidates per CTA, at most
+constexpr int kHandWords = 32;
+constexpr uint32_t kHandFallback = 0xFFFFFFFFu;
+struct Handoff {
+  uint32_t *flag;
+  uint64_t *cand;
+  int parts;                        // selection CTAs per query
+};
+
 // Scratch of a long-row top-k: smax[q][sstride], the supergroup maxima (or
 // partial maxima) of row q.
 struct LongRowWs {
@@ -57,6 +81,8 @@ struct LongRowWs {
   // gmax[q][gstride] (entry j in group j / 32), or null
   uint32_t *gmax = nullptr;
   int64_t gstride = 0;
+  // optional (csa2_decode): the candidate handoff to the attention, or null
+  Handoff hand = {nullptr, nullptr, 0};
 };
 
 // Launch `kern` with programmatic stream serialisation (the kernel calls
@@ -145,11 +171,18 @@ int attn_ctas(int n_q, int sel_stride);
 // it waits for the selection.  ahead_ctas: the SMs the grid ahead holds while
 // it runs (one CTA each), or -1; when this grid fits beside it and a CTA has
 // one chunk, CTAs that wait for the selection run a warm-up pass meanwhile.
+// hand: the selection grid ahead hands its candidates over (csa2_decode, where
+// attn_handoff_fits(n_q)); the attention then runs kHandCap / 128 chunks of
+// candidates instead of sel_stride / 128 of selected entries, and reads sel only
+// where the selection fell back.
 cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_seq, const int32_t *sel,
                            int sel_stride, const void *swa, int swa_cap, const int32_t *q_seq, const int32_t *pos,
                            const int32_t *swa_first, const int32_t *swa_cnt, int n_q, void *out, int out_dtype,
                            float sm_scale, double rope_base, void *ws, int *status, cudaStream_t st,
-                           bool inputs_settled = false, int ahead_ctas = -1);
+                           bool inputs_settled = false, int ahead_ctas = -1, const Handoff *hand = nullptr);
+// The handoff pays where every CTA holding candidates fits one wave beside the
+// selection: one chunk per CTA for n_q queries.
+bool attn_handoff_fits(int n_q);
 
 cudaError_t launch_bounded_wait_check(int *status, unsigned long long limit_ns, cudaStream_t st);
 

@@ -109,6 +109,9 @@ struct ScoreTcArgs {
   uint32_t *gmax;
   int64_t gstride;
   int smax_mode;
+  // optional: the candidate-handoff flags of the selection and attention
+  // grids that follow ([n_q][kHandWords] words; words 0-3 zeroed here)
+  uint32_t *hflag;
 };
 
 // Work units are T = (query, unit) in query-major order, T < n_q * units_per_q;
@@ -251,6 +254,11 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   // everything below reads inputs or allocates TMEM: after the grid ahead
   griddep_wait();
   griddep_launch();
+  // (the previous call's attention, which read these flags, has completed:
+  // the grid ahead waited for it)
+  if (P.hflag != nullptr)
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 4 * P.n_q; i += gridDim.x * blockDim.x)
+      P.hflag[(i >> 2) * kHandWords + (i & 3)] = 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kScStages; s++) {
       ptx::mbar_init(&full_bar[s], P.pool != nullptr ? 1 + 32 * kPoolGatherWarps : 1);   // pool: see PoolGather
@@ -895,6 +903,7 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
   P.sstride = W ? W->sstride : 0;
   P.gmax = W ? W->gmax : nullptr;
   P.gstride = W ? W->gstride : 0;
+  P.hflag = W && pool == nullptr ? W->hand.flag : nullptr;
   P.smax_mode = pool == nullptr && W != nullptr && (smax_mode == 2 || (smax_mode == 3 && W->gmax != nullptr))
                     ? smax_mode : 0;
   P.key_nib = key_nib;

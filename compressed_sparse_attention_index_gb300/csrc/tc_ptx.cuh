@@ -73,6 +73,51 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
   return true;
 }
 
+// ------------------------------------------------------------------ flags in global memory
+// A flag published by one grid and read by a later grid of the same stream
+// that may already be running (programmatic dependent launch).  The writer
+// stores with release semantics at GPU scope after its data; the reader polls
+// with acquire loads, bounded by wall time, and sees the data after it.
+__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_release_u64(uint64_t *p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t *p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_add_u32(uint32_t *p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t *p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+// Poll until *p >= target; false after ~`limit_ns` of wall time.
+__device__ __forceinline__ bool poll_at_least_u32(const uint32_t *p, uint32_t target,
+                                                  uint64_t limit_ns = 2000000000ull) {
+  if (ld_acquire_u32(p) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  while (ld_acquire_u32(p) < target)
+    if (globaltimer() - t0 > limit_ns) return false;
+  return true;
+}
+// Poll until *p is nonzero; false (v = 0) after ~`limit_ns` of wall time.
+__device__ __forceinline__ bool poll_nonzero_u64(const uint64_t *p, uint64_t &v, uint64_t limit_ns = 2000000000ull) {
+  if ((v = ld_acquire_u64(p)) != 0ull) return true;
+  const uint64_t t0 = globaltimer();
+  while ((v = ld_acquire_u64(p)) == 0ull)
+    if (globaltimer() - t0 > limit_ns) return false;
+  return true;
+}
+
 // ------------------------------------------------------------------ copies
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int32_t x, int32_t y, uint64_t *bar) {
   asm volatile(

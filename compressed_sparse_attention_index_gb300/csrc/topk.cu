@@ -23,6 +23,7 @@
 
 #include "common.cuh"
 #include "launch.cuh"
+#include "tc_ptx.cuh"
 
 namespace csa2 {
 
@@ -505,13 +506,15 @@ __device__ __noinline__ uint32_t block_kth_bound12(const uint32_t *v, int n, int
 // of the k-th largest key is found by one 4,096-bin histogram of the 12 bits
 // below the common prefix of the score halves, the keys in that digit (at
 // most kBinCap) are ranked among themselves, and the selected keys are
-// written out by one order-keeping compaction: out[0..k) ascending indices.
+// written out by one order-keeping compaction: out[0..k) ascending indices,
+// and *kth (shared) = the smallest selected key, also stored to *pub (global,
+// optional) as soon as it is known.
 // Returns false, having written nothing, when that digit holds more than
 // kBinCap keys (many equal scores); the caller then runs select_block.
 // hist: kWideBins counters; bin_keys: kBinCap keys of scratch.
 constexpr int kBinCap = 256;
 __device__ __noinline__ bool select_small(const uint64_t *keys, int n, int k, int32_t *out, uint32_t *hist,
-                                          uint64_t *bin_keys) {
+                                          uint64_t *bin_keys, uint64_t *kth, uint64_t *pub) {
   __shared__ int n_bin;
   const int t = threadIdx.x;
   const uint64_t x = t < n ? keys[t] : 0ull;
@@ -539,6 +542,10 @@ __device__ __noinline__ bool select_small(const uint64_t *keys, int n, int k, in
       int r = 0;                                             // keys of digit D larger than this one
       for (int j = 0; j < in_d; j++) r += bin_keys[j] > x ? 1 : 0;
       selected = r < take_d;
+      if (r == take_d - 1) {                                 // exactly one key (1 <= take_d <= in_d)
+        *kth = x;
+        if (pub != nullptr) ptx::st_relaxed_u64(pub, x);
+      }
     }
   }
   int total;
@@ -556,9 +563,12 @@ __device__ __noinline__ bool select_small(const uint64_t *keys, int n, int k, in
 // by index (buckets of power-of-two width; a few indices per bucket).  keys
 // and sk are reused as scratch.  sel: >= k ints; bins: >= 4096 counters.
 // out[0..k): ascending indices, -1 padding.  by_index: keys[] is already in ascending index order; the selected keys are
-// then written out by one order-keeping compaction.
+// then written out by one order-keeping compaction.  kth (shared, optional):
+// receives K, the smallest key that is selected or 1 when all are; pub
+// (global, optional) too, at once.
 __device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t *out, int32_t *sel,
-                                          uint32_t *bins, bool by_index = false) {
+                                          uint32_t *bins, bool by_index = false, uint64_t *kth = nullptr,
+                                          uint64_t *pub = nullptr) {
   __shared__ int cnt_sh[2];
   __shared__ int n_sel;
   __shared__ uint32_t red_slots[2][32];
@@ -584,6 +594,10 @@ __device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t
       tlo = block_kth256(sk, n, need, 0, bins);
     }
     K = ((uint64_t)t32 << 32) | tlo;
+  }
+  if (kth != nullptr && threadIdx.x == 0) {
+    *kth = K;
+    if (pub != nullptr) ptx::st_relaxed_u64(pub, K);
   }
   __syncthreads();
   if (by_index) {
@@ -884,6 +898,27 @@ __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 constexpr int kMaxCluster = 16;
+static_assert(kMaxCluster <= kHandCtas && kHandSeg >= 256, "handoff segments");
+
+// Puts the n <= 256 unique keys lc[0..n) in ascending index order (rank = the
+// number of larger index halves, the index halves being ~index): tpe lanes of
+// a warp count for one key, each over every tpe-th key.  Block-wide
+// (blockDim.x == 1024); ends with lc written, not with a barrier.
+constexpr int kSortCap = 256;
+__device__ __noinline__ void sort_by_index(uint64_t *lc, int n) {
+  const int tpe = n <= 32 ? 32 : n <= 64 ? 16 : n <= 128 ? 8 : 4;
+  const int e = (int)threadIdx.x / tpe, sub = (int)threadIdx.x & (tpe - 1);
+  uint64_t mine = 0;
+  int r = 0;
+  if (e < n) {
+    mine = lc[e];
+    const uint32_t lo = (uint32_t)mine;
+    for (int j = sub; j < n; j += tpe) r += (uint32_t)lc[j] > lo ? 1 : 0;
+  }
+  for (int o = tpe >> 1; o > 0; o >>= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
+  __syncthreads();
+  if (e < n && sub == 0) lc[r] = mine;
+}
 
 // Pass 2: grid (P, n_q), clusters of P CTAs along x (P <= kMaxCluster): the
 // cluster rank of a CTA is blockIdx.x.  No thread returns before the second
@@ -901,6 +936,7 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
   __shared__ int n_vs, n_lc, lc_sorted, n_g;
   __shared__ int c_off[kMaxCluster + 1], c_bad, c_sorted;
   __shared__ int c_cnt[kMaxCluster], c_srt[kMaxCluster];   // (CTA 0) pushed by every CTA of the cluster
+  __shared__ uint64_t kth_sh;                                // (CTA 0) the smallest selected key
   griddep_wait();
   griddep_launch();
   const int q = blockIdx.y, P = gridDim.x, part = blockIdx.x;
@@ -1181,24 +1217,25 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
       }
     }
   }
-  // ---- a short list is put in index order (rank = number of larger index
-  // halves, the index halves being ~index): the lists of the CTAs, taken in
-  // cluster order, then run in index order
-  constexpr int kSortCap = 256;
+  // ---- a short list is put in index order: the lists of the CTAs, taken
+  // in cluster order, then run in index order
   __syncthreads();                                     // lc and n_lc are final
+  // L2 prefetch of the latent records of this CTA's candidates (a superset of
+  // the selected entries, which the attention gathers next), as soon as they
+  // are known: spread over the cluster
+  if (plain && pf_seq >= 0 && pf_seq < S.n_seq) {
+    const uint8_t *pf = S.kv_pf + (int64_t)pf_seq * S.n_max * kKvBytes;
+    const int nl = min(n_lc, kLocalCap);
+    for (int i = threadIdx.x; i < 4 * nl; i += blockDim.x) {   // a record spans at most four 128-B lines
+      const uint32_t idx = ~(uint32_t)lc[i >> 2];
+      if ((int64_t)idx >= S.n_max) continue;
+      const uint8_t *rec = pf + (int64_t)idx * kKvBytes;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + ((i & 3) == 3 ? kKvBytes - 1 : (i & 3) * 128)));
+    }
+  }
   {
     const int nl = n_lc;
-    if (nl <= kSortCap) {
-      uint64_t mine = 0;
-      int r = 0;
-      if ((int)threadIdx.x < nl) {
-        mine = lc[threadIdx.x];
-        const uint32_t lo = (uint32_t)mine;
-        for (int j = 0; j < nl; j++) r += (uint32_t)lc[j] > lo ? 1 : 0;
-      }
-      __syncthreads();
-      if ((int)threadIdx.x < nl) lc[r] = mine;
-    }
+    if (nl <= kSortCap) sort_by_index(lc, nl);
     if (threadIdx.x == 0) lc_sorted = nl <= kSortCap ? 1 : 0;
   }
   // ---- every CTA pushes its list into CTA 0's shared memory: slot `part`
@@ -1207,6 +1244,17 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
   // another CTA's shared memory, so the others may leave
   const int slot_cap = kCandCap / P;
   __syncthreads();                                     // the sorted lc is written
+  if (W.hand.flag != nullptr) {
+    // hand this CTA's candidates to the attention grid (already running): in
+    // index order or not at all; they are counted in after the cluster
+    // barrier, by when these stores have long landed
+    const int nl = n_lc;
+    const bool give = nl <= kSortCap && nl <= kHandSeg;
+    if (give)
+      for (int i = threadIdx.x; i < nl; i += blockDim.x)
+        W.hand.cand[((int64_t)q * kHandCtas + part) * kHandSeg + i] = lc[i];
+    if (threadIdx.x == 0) W.hand.flag[q * kHandWords + 8 + part] = give ? (uint32_t)nl : kHandFallback;
+  }
   {
     const int nl = n_lc;
     const int np = min(nl, min(kLocalCap, slot_cap));
@@ -1217,6 +1265,8 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
     }
   }
   cluster_barrier();                                   // the pushed lists are in CTA 0
+  if (W.hand.flag != nullptr && threadIdx.x == blockDim.x - 1)
+    ptx::red_release_add_u32(W.hand.flag + q * kHandWords, 1u);   // this CTA's candidates are out
   if (part == 0) {
     if (warp == 0) {
       const int c = lane < P ? c_cnt[lane] : 0;
@@ -1258,21 +1308,10 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
       }
     }
   }
-  // L2 prefetch of the latent records of this CTA's candidates (a superset of
-  // the selected entries, which the attention gathers next): spread over the
-  // cluster, and out of CTA 0's selection, which follows
-  if (plain && pf_seq >= 0 && pf_seq < S.n_seq) {
-    const uint8_t *pf = S.kv_pf + (int64_t)pf_seq * S.n_max * kKvBytes;
-    const int nl = min(n_lc, kLocalCap);
-    for (int i = threadIdx.x; i < 4 * nl; i += blockDim.x) {   // a record spans at most four 128-B lines
-      const uint32_t idx = ~(uint32_t)lc[i >> 2];
-      if ((int64_t)idx >= S.n_max) continue;
-      const uint8_t *rec = pf + (int64_t)idx * kKvBytes;
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + ((i & 3) == 3 ? kKvBytes - 1 : (i & 3) * 128)));
-    }
-  }
   if (part != 0) return;
   int32_t *oq = out + (int64_t)q * k;
+  if (threadIdx.x == 0) kth_sh = 1ull;                 // (overwritten by the exact selection)
+  uint64_t *kth_pub = W.hand.flag != nullptr ? reinterpret_cast<uint64_t *>(W.hand.flag + q * kHandWords + 2) : nullptr;
   if (!c_bad) {
     const int nc = c_off[P];
     __syncthreads();                                   // lc (over sv) is read above
@@ -1282,8 +1321,8 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
     // pool items run in slot order, not index order: only plain and block rows keep order
     const bool by_index = c_sorted != 0 && S.pool == nullptr;
     if (!(by_index && nc > k && nc <= (int)blockDim.x &&
-          select_small(keys, nc, k, oq, sh.whist, reinterpret_cast<uint64_t *>(sel))))
-      select_block(keys, sv, nc, k, oq, sel, sh.whist, by_index);
+          select_small(keys, nc, k, oq, sh.whist, reinterpret_cast<uint64_t *>(sel), &kth_sh, kth_pub)))
+      select_block(keys, sv, nc, k, oq, sel, sh.whist, by_index, &kth_sh, kth_pub);
   } else {
     // too many ties at T for the buffer: exact selection straight over the row
     __shared__ int nvi;
@@ -1298,6 +1337,14 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
     __syncthreads();
     auto get = [&](int64_t i, uint64_t &key) { return item_key(S, q, i, nv, key, status); };
     select_and_write(get, S.n_items, nvi, k, oq, sh, sel);
+  }
+  if (W.hand.flag != nullptr) {
+    // the selection (oq) is final
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      ptx::st_relaxed_u64(kth_pub, kth_sh);              // (again, where no exact pass ran)
+      ptx::st_release_u32(W.hand.flag + q * kHandWords + 1, 1u);
+    }
   }
 }
 

@@ -248,11 +248,18 @@ csa2_status csa2_sparse_attn(const void *q, const void *kv_cache, int64_t n_max,
  * csa2_decode -- one Full-layer decode step: csa2_index_score over every
  * visible entry, top-512 selection, csa2_sparse_attn over the selection and
  * the window, issued as one call.  The pages give no such call; it composes
- * the three steps above (same arguments, same meaning, same results as the
- * chain csa2_index_score -> csa2_topk(k = 512, block = 1) ->
+ * the three steps above (same arguments, same meaning, the same selection as
+ * the chain csa2_index_score -> csa2_topk(k = 512, block = 1) ->
  * csa2_sparse_attn(sel_stride = 512)), and lets the indexer's epilogue also
  * write the maxima the selection starts from, which saves the selection's
- * first pass over the scores.
+ * first pass over the scores.  For small batches (up to about 30 queries on
+ * 152 SMs) over long rows, the selection also hands its candidates (a superset
+ * of the selected entries, at most 640, in index order) to the attention before
+ * its exact pass, and the attention masks those below the smallest selected
+ * key: the output then attends to exactly the selected entries and the window,
+ * but groups them into other chunks than csa2_sparse_attn does, so it agrees
+ * with the chain's to rounding (relative 1e-3) rather than bit for bit.  The
+ * same inputs give the same bits on every call.
  *
  *   key_nib .. n_q      as csa2_index_score (Full mode; scores are kept in the
  *                       workspace).

@@ -150,9 +150,9 @@ def test_sparse_attn_query_scale_invariance(lib, oracle_lib, e):
         assert row_norm_err(out[qi], base[qi]) <= 1e-6
 
 
-def _check_full(lib, oracle_lib, wl, dw, buf, queries):
+def _check_full(lib, oracle_lib, wl, dw, buf, queries, fused=False):
     from compressed_sparse_attention_index_gb300 import decode
-    decode.full_decode(dw, buf)
+    (decode.fused_decode if fused else decode.full_decode)(dw, buf)
     sel = buf.sel.cpu().numpy()
     out = buf.out.float().cpu().numpy()
     assert lib.csa2_get_device_status() == 0
@@ -194,6 +194,17 @@ def test_full_decode_config4_full_size_sampled(lib, oracle_lib):
     wl = CONFIGS[4]
     dw = _dw(wl)
     _check_full(lib, oracle_lib, wl, dw, _bufs(dw), [0, 7])
+    # the one-call decode, whose attention starts from the candidate handoff
+    _check_full(lib, oracle_lib, wl, dw, _bufs(dw), [0, 3, 7], fused=True)
+
+
+def test_fused_decode_small_batch_of_64k_rows(lib, oracle_lib):
+    """Four queries over 65,536-entry caches: the one-call decode on the
+    32-entry group plan, whose attention takes the candidates when they fit
+    (and the final selection otherwise), against the oracle."""
+    wl = small(n_seq=4, n_entries=65536, zipf=True, seed=254)
+    dw = _dw(wl)
+    _check_full(lib, oracle_lib, wl, dw, _bufs(dw), [0, 1, 2, 3], fused=True)
 
 
 def _check_reindex(lib, oracle_lib, wl, blocks, sel, out, qi):
@@ -312,12 +323,42 @@ def test_empty_query_gives_zeros(lib):
     assert torch.count_nonzero(buf.out).item() == 0
 
 
+HAND_CAP = 640
+HAND_FALLBACK = 0xFFFFFFFF
+
+
+def _handoff(buf):
+    """What the selection handed to the attention in the last csa2_decode call
+    on buf, read from the workspace's last two regions (each 256-B aligned):
+    32 words per query (0: selection CTAs that published, P; 1: selection
+    final; 2-3: the smallest selected key; 8 + p: CTA p's candidate count or
+    0xFFFFFFFF), then 16 x 256 candidate keys per query.  Returns
+    [(counts, key)] per query."""
+    r256 = lambda b: (b + 255) // 256 * 256
+    n_q = buf.n_q
+    start = buf.ws_decode_bytes - r256(n_q * 16 * 256 * 8) - r256(n_q * 128)
+    w = buf.ws[start:start + n_q * 128].cpu().numpy().view(np.uint32).reshape(n_q, 32)
+    assert np.all(w[:, 1] == 1)
+    return [(w[qi, 8:8 + int(w[qi, 0])], int(w[qi, 2]) | (int(w[qi, 3]) << 32)) for qi in range(n_q)]
+
+
+def _order_key(x):
+    """The selection's order key of fp32 scores: unsigned order equals float order."""
+    b = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    return np.where(b >> np.uint64(31), b ^ np.uint64(0xFFFFFFFF), b | np.uint64(0x80000000))
+
+
 @pytest.mark.parametrize("case", ["small_direct", "ragged_standalone", "config1_groups", "config4_units"])
 def test_fused_decode_equals_call_chain(lib, case):
-    """csa2_decode (score epilogue feeds the selection) gives exactly the
-    results of csa2_index_score -> csa2_topk -> csa2_sparse_attn, for each of
-    its selection plans: one CTA per row, the standalone passes, 32-entry
-    groups and 512-entry units."""
+    """csa2_decode (score epilogue feeds the selection) selects exactly what
+    csa2_index_score -> csa2_topk selects, for each of its selection plans: one
+    CTA per row, the standalone passes, 32-entry groups and 512-entry units.
+    Where the attention takes the selection's candidates (8 x 1M: every query
+    hands over at most 640, and the smallest selected key published is the
+    512th largest key of the row), the entries sit in other chunks than in
+    csa2_sparse_attn, so the output agrees with the chain's to rounding;
+    elsewhere bit for bit.  Repeated calls and a garbage workspace give the
+    same bits."""
     from compressed_sparse_attention_index_gb300 import decode
     wl = {"small_direct": small(n_seq=2, n_entries=1000, seed=250),
           "ragged_standalone": small(n_seq=3, n_entries=20_000, seed=251),
@@ -330,7 +371,23 @@ def test_fused_decode_equals_call_chain(lib, case):
     decode.fused_decode(dw, fused)
     assert lib.csa2_get_device_status() == 0
     assert torch.equal(chain.sel, fused.sel)
-    assert torch.equal(chain.out.view(torch.int32), fused.out.view(torch.int32))
+    handoff = case == "config4_units"
+    if handoff:
+        hand = _handoff(fused)
+        sel = chain.sel.cpu().numpy()
+        scores = chain.scores.cpu().numpy()
+        for qi in range(fused.n_q):
+            counts, kth = hand[qi]
+            assert len(counts) >= 2 and np.all(counts != HAND_FALLBACK), counts
+            assert 512 <= counts.sum() <= HAND_CAP, counts
+            j = sel[qi][sel[qi] >= 0].astype(np.int64)
+            keys = (_order_key(scores[qi, j]) << np.uint64(32)) | (~j.astype(np.uint64) & np.uint64(0xFFFFFFFF))
+            assert kth == int(keys.min())
+        err = max(row_norm_err(fused.out[qi].cpu().numpy(), chain.out[qi].cpu().numpy()) for qi in range(fused.n_q))
+        assert err <= 1e-3, err
+    else:
+        assert torch.equal(chain.out.view(torch.int32), fused.out.view(torch.int32))
+    first = fused.out.clone()
     decode.fused_decode(dw, fused)                       # second call: nothing left over from the first
     assert torch.equal(chain.sel, fused.sel)
     fused.ws.fill_(0xA5)                                 # a workspace of garbage: nothing in it is
@@ -338,7 +395,37 @@ def test_fused_decode_equals_call_chain(lib, case):
     decode.fused_decode(dw, fused)
     assert lib.csa2_get_device_status() == 0
     assert torch.equal(chain.sel, fused.sel)
+    assert torch.equal(first.view(torch.int32), fused.out.view(torch.int32))
+
+
+def test_fused_decode_falls_back_to_the_final_selection(lib):
+    """Rows whose candidates cannot be handed over (all scores equal: every
+    entry reaches the threshold, the row is selected exactly from its scores)
+    are flagged so, and the attention reads the final selection: the output
+    is the chain's, bit for bit.  A query seeing fewer entries than k hands all
+    of them over with the key 1 (every candidate selected)."""
+    from compressed_sparse_attention_index_gb300 import decode
+    wl = small(n_seq=2, n_entries=65536, seed=255)
+    dw = _dw(wl)
+    dw.w.zero_()                                         # every score is +0
+    chain, fused = _bufs(dw), _bufs(dw)
+    decode.full_decode(dw, chain)
+    decode.fused_decode(dw, fused)
+    assert lib.csa2_get_device_status() == 0
+    assert torch.equal(chain.sel, fused.sel)
+    assert all(np.any(counts == HAND_FALLBACK) for counts, _ in _handoff(fused))
     assert torch.equal(chain.out.view(torch.int32), fused.out.view(torch.int32))
+    dw = _dw(wl)
+    dw.n_vis[1] = 300                                    # fewer entries than k
+    chain, fused = _bufs(dw), _bufs(dw)
+    decode.full_decode(dw, chain)
+    decode.fused_decode(dw, fused)
+    assert lib.csa2_get_device_status() == 0
+    assert torch.equal(chain.sel, fused.sel)
+    counts, kth = _handoff(fused)[1]
+    assert np.all(counts != HAND_FALLBACK) and counts.sum() == 300 and kth == 1, (counts, kth)
+    err = max(row_norm_err(fused.out[qi].cpu().numpy(), chain.out[qi].cpu().numpy()) for qi in range(2))
+    assert err <= 1e-3, err
 
 
 def test_window_longer_than_ring_is_rejected(lib, oracle_lib):
@@ -375,7 +462,7 @@ def test_decode_host_equals_device_call(lib, out_f32):
     garbage-filled workspace and on a second call."""
     import compressed_sparse_attention_index_gb300 as C
     from gen import inputs as G
-    wl = small(n_seq=3, n_entries=20_000, seed=252)
+    wl = small(n_seq=3, n_entries=65536, seed=252)
     dw = _dw(wl)
     n_q = dw.q.shape[0]
     dt = C.CSA2_OUT_F32 if out_f32 else C.CSA2_OUT_BF16
