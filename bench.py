@@ -61,10 +61,23 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="with the default workload, skip the secondary workloads")
+    ap.add_argument("--entries", type=int, default=None,
+                    help="shorten the workload's caches to this many entries per sequence (smaller device "
+                         "footprint, e.g. for profiler captures); the workload name records it")
     ap.add_argument("--only", choices=["mq", "layers"], default=None,
                     help="run and print only one secondary workload: the multi-query decode (mq) or the "
                          "20-layer decoder step (layers)")
     return ap.parse_args()
+
+
+def workload_of(args):
+    """The configuration's workload, its caches shortened to --entries if given."""
+    import dataclasses
+    from gen.workloads import CONFIGS
+    wl = CONFIGS[args.config]
+    if args.entries is not None and args.entries != wl.n_entries:
+        wl = dataclasses.replace(wl, n_entries=args.entries, name=f"{wl.name}_entries{args.entries}")
+    return wl
 
 
 def peaks():
@@ -192,7 +205,7 @@ def run_ours(args, rank, world, local_rank):
 
     from compressed_sparse_attention_index_gb300 import ranks
     torch.cuda.set_device(local_rank)
-    wl = ranks.rank_workload(CONFIGS[args.config], rank)    # each rank decodes its own batch
+    wl = ranks.rank_workload(workload_of(args), rank)       # each rank decodes its own batch
     if wl.pool or wl.prefill:
         return run_rows(args, rank, world, local_rank, wl)
     dw = build_device_workload(wl)
@@ -576,7 +589,7 @@ def run_reference(args):
     from gen.workloads import CONFIGS
     import oracle
     oracle.build()
-    wl = CONFIGS[args.config]
+    wl = workload_of(args)
     for _ in range(args.warmup):
         pass                       # the oracle has no state to warm; its packed keys are built once below
     t_total = 0.0

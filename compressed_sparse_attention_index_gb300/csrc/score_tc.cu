@@ -140,14 +140,17 @@ __device__ __forceinline__ bool ring_get(const volatile unsigned long long *ring
   return false;
 }
 
-// Sequence id and visible length of a query, re-read when the query changes;
-// nv = -1 marks a query whose values are out of range (recorded once, by the
-// producer of its unit 0).
+// Sequence id and visible length of a query, re-read when the query changes
+// (from the CTA's shared-memory copy of every query's pair when there is one:
+// qcache, for up to kQCache queries); nv = -1 marks a query whose values are
+// out of range (recorded once, by the producer of its unit 0).
+constexpr int kQCache = 256;
 struct QueryInfo {
   int q = -1, seq = 0, nv = -1;
   int pre_q = -1, pre_seq = 0, pre_nv = 0;   // values loaded ahead (prefetch)
+  const int2 *cache = nullptr;
   __device__ void prefetch(const ScoreTcArgs &P, int nq) {
-    if (nq == q || nq == pre_q) return;
+    if (cache != nullptr || nq == q || nq == pre_q) return;
     pre_q = nq;
     pre_seq = __ldg(P.q_seq + nq);
     pre_nv = __ldg(P.n_vis + nq);
@@ -155,8 +158,14 @@ struct QueryInfo {
   __device__ void set(const ScoreTcArgs &P, int nq, int u, bool record) {
     if (nq == q) return;
     q = nq;
-    seq = nq == pre_q ? pre_seq : __ldg(P.q_seq + q);
-    nv = nq == pre_q ? pre_nv : __ldg(P.n_vis + q);
+    if (cache != nullptr) {
+      const int2 c = cache[q];
+      seq = c.x;
+      nv = c.y;
+    } else {
+      seq = nq == pre_q ? pre_seq : __ldg(P.q_seq + q);
+      nv = nq == pre_q ? pre_nv : __ldg(P.n_vis + q);
+    }
     if (seq < 0 || seq >= P.n_seq || nv < 0 || (int64_t)nv > P.n_max) {
       if (record && u == 0) record_error(P.status, CSA2_ERR_BOUNDS);
       nv = -1;
@@ -193,31 +202,52 @@ struct QuerySlotsT {
 using QuerySlots = QuerySlotsT<kQSlots>;
 
 // Pool mode: a unit is 64 gathered 8-entry blocks (512 B of nibbles + 32 B of
-// scales each).  Small bulk copies cost the copy engine more than their bytes,
-// and one warp's plain asynchronous copies are limited by how many it may have
-// in flight, so four warps each move 16 blocks in 16-B pieces: one block's
-// nibbles per instruction (16 B per lane), then the 16 blocks' scales in one.
-// Each lane arrives on the stage's barrier when its copies have landed (the
-// barrier expects 1 + 32 x 4 arrivals: the producer's lane 0, with the query
-// data's bytes, and every gathering lane).  Each warp loads the block ids of
-// its next unit (T + gridDim.x, the usual next one) while this one's copies go
-// out.
+// scales each).  Small bulk copies cost the copy engine more than their bytes
+// (measured), and one warp's plain asynchronous copies are limited by how many
+// it may have in flight, so four warps each move 16 blocks in 16-B pieces: one
+// block's nibbles per instruction (16 B per lane), then the 16 blocks' scales
+// in one.  Each lane arrives on the stage's barrier when its copies have
+// landed (the barrier expects 1 + 32 x 4 arrivals: the producer's lane 0, with
+// the query data's bytes, and every gathering lane).  A CTA has few units in
+// pool mode (2,048 for 64 queries over 152 SMs), so the block ids are loaded
+// kPoolAhead units ahead (the CTA's units T, T + gridDim.x, ...): a unit's
+// copies then never wait for its ids to come back from memory.
+constexpr int kPoolAhead = 6;
 struct PoolGather {
-  uint32_t pre_T = kDone;
-  int pre_b = -1;
-  __device__ void prefetch(const ScoreTcArgs &P, int g, uint32_t Tn, QueryInfo &qi, uint32_t total_units) {
-    if (Tn >= total_units) return;
+  uint32_t pre_T[kPoolAhead];
+  int pre_b[kPoolAhead];
+  __device__ int load_b(const ScoreTcArgs &P, int g, uint32_t T) const {
     const int lane = threadIdx.x & 31;
-    const int qn = (int)(Tn / (uint32_t)P.units_per_q), un = (int)(Tn - (uint32_t)qn * (uint32_t)P.units_per_q);
-    pre_b = __ldg(P.pool + (int64_t)qn * kPoolBlocks + un * (kUnit / kBlock) + g * 16 + (lane & 15));
-    pre_T = Tn;
-    qi.prefetch(P, qn);
+    const int q = (int)(T / (uint32_t)P.units_per_q), u = (int)(T - (uint32_t)q * (uint32_t)P.units_per_q);
+    return __ldg(P.pool + (int64_t)q * kPoolBlocks + u * (kUnit / kBlock) + g * 16 + (lane & 15));
   }
-  __device__ void gather(const ScoreTcArgs &P, int g, uint32_t T, int q, int u, int64_t row0, unsigned char *st,
-                         uint64_t *full) {
+  // ids of the units T0, T0 + gridDim.x, ... (kPoolAhead of them)
+  __device__ void start(const ScoreTcArgs &P, int g, uint32_t T0, uint32_t total_units) {
+#pragma unroll
+    for (int d = 0; d < kPoolAhead; d++) {
+      const uint32_t T = T0 + (uint32_t)d * gridDim.x;
+      pre_T[d] = T < total_units ? T : kDone;
+      pre_b[d] = T < total_units ? load_b(P, g, T) : -1;
+    }
+  }
+  // the ids of unit T (normally the oldest prefetched); the ring then moves on
+  __device__ int take(const ScoreTcArgs &P, int g, uint32_t T, uint32_t total_units) {
+    if (pre_T[0] != T) start(P, g, T, total_units);   // a unit was skipped: restart the look-ahead at T
+    const int b = pre_b[0];
+#pragma unroll
+    for (int d = 0; d + 1 < kPoolAhead; d++) {
+      pre_T[d] = pre_T[d + 1];
+      pre_b[d] = pre_b[d + 1];
+    }
+    const uint32_t Tn = T + (uint32_t)kPoolAhead * gridDim.x;
+    pre_T[kPoolAhead - 1] = Tn < total_units ? Tn : kDone;
+    pre_b[kPoolAhead - 1] = Tn < total_units ? load_b(P, g, Tn) : -1;
+    return b;
+  }
+  __device__ void gather(const ScoreTcArgs &P, int g, uint32_t T, int64_t row0, unsigned char *st, uint64_t *full,
+                         uint32_t total_units) {
     const int lane = threadIdx.x & 31;
-    const int b = pre_T == T ? pre_b
-                             : __ldg(P.pool + (int64_t)q * kPoolBlocks + u * (kUnit / kBlock) + g * 16 + (lane & 15));
+    const int b = take(P, g, T, total_units);
     const bool ok = b >= 0 && (int64_t)b * kBlock < P.n_max;
     if (lane < 16 && b >= 0 && !ok) record_error(P.status, CSA2_ERR_BOUNDS);
 #pragma unroll 4
@@ -235,6 +265,8 @@ struct PoolGather {
   }
 };
 
+// POOL: pool mode (P.pool set: units of gathered 8-entry blocks).
+template <bool POOL>
 __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcArgs P) {
   extern __shared__ __align__(1024) unsigned char sc_smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -249,11 +281,17 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   __shared__ volatile int abort_flag;
   __shared__ int armed_sh;                         // iterations whose copies the producer issued
   __shared__ volatile unsigned long long unit_ring[kRing];
+  __shared__ int2 qcache[POOL ? kQCache : 1];      // pool mode: (q_seq, n_vis) of every query, when n_q <= kQCache
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // everything below reads inputs or allocates TMEM: after the grid ahead
   griddep_wait();
   griddep_launch();
+  // (pool mode only, where the query changes on every unit; elsewhere the
+  // first unit would wait for the table)
+  const int2 *qc = POOL && P.n_q <= kQCache ? qcache : nullptr;
+  if (qc != nullptr)
+    for (int i = threadIdx.x; i < P.n_q; i += blockDim.x) qcache[i] = make_int2(__ldg(P.q_seq + i), __ldg(P.n_vis + i));
   // (the previous call's attention, which read these flags, has completed:
   // the grid ahead waited for it)
   if (P.hflag != nullptr)
@@ -261,7 +299,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       P.hflag[(i >> 2) * kHandWords + (i & 3)] = 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kScStages; s++) {
-      ptx::mbar_init(&full_bar[s], P.pool != nullptr ? 1 + 32 * kPoolGatherWarps : 1);   // pool: see PoolGather
+      ptx::mbar_init(&full_bar[s], POOL ? 1 + 32 * kPoolGatherWarps : 1);   // pool: see PoolGather
       ptx::mbar_init(&sf_bar[s], 1);
       ptx::mbar_init(&done_bar[s], 1);
     }
@@ -289,9 +327,10 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     const uint64_t policy = ptx::policy_evict_first();
     QuerySlots qs;
     QueryInfo sc;
+    sc.cache = qc;
     uint32_t T = blockIdx.x;
     PoolGather pg;
-    if (P.pool != nullptr) pg.prefetch(P, 0, T, sc, total_units);
+    if (POOL) pg.start(P, 0, T, total_units);
     for (uint32_t it = 0;; it++) {
       if (abort_flag) break;
       // this iteration's unit: the next one inside its query's visible length
@@ -301,7 +340,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         const int q = (int)(T / (uint32_t)P.units_per_q);
         uq = (int)(T - (uint32_t)q * (uint32_t)P.units_per_q);
         sc.set(P, q, uq, lane == 0);
-        if (sc.nv >= 0 && (P.pool != nullptr || uq * kUnit < sc.nv)) break;
+        if (sc.nv >= 0 && (POOL || uq * kUnit < sc.nv)) break;
         T += gridDim.x;
       }
       if (lane == 0) unit_ring[it % kRing] = ((unsigned long long)it << 32) | T;
@@ -331,7 +370,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         ptx::bulk_load(qd + kQOffSFB, P.q_scale + (int64_t)sc.q * kIdxHeads * 4, 128, &full_bar[s]);
       };
       const int64_t row0 = (int64_t)sc.seq * P.n_max;
-      if (P.pool == nullptr) {
+      if (!POOL) {
         if (lane == 0) {
           // sub-tiles that start before n_vis end within n_max (n_max % 128 == 0)
           const int left = sc.nv - cur_u * kUnit;
@@ -349,8 +388,8 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
           ptx::mbar_arrive_expect_tx(&full_bar[s], qbytes);
           if (fresh) load_query();
         }
-        pg.gather(P, 0, T, sc.q, cur_u, row0, st, &full_bar[s]);
-        pg.prefetch(P, 0, T + gridDim.x, sc, total_units);
+        pg.gather(P, 0, T, row0, st, &full_bar[s], total_units);
+        if (T + gridDim.x < total_units) sc.prefetch(P, (int)((T + gridDim.x) / (uint32_t)P.units_per_q));
       }
       __syncwarp();
       if (lane == 0) armed_sh = (int)it + 1;
@@ -423,7 +462,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         if (!ptx::mbar_wait(&sf_bar[s], r & 1) || !ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) { fail(); break; }
         // pool mode: the stage was filled by ordinary asynchronous copies, which
         // the MMA (async proxy) reads only after a proxy fence
-        if (P.pool != nullptr) ptx::fence_proxy_async_smem();
+        if (POOL) ptx::fence_proxy_async_smem();
         ptx::tc_fence_after();
         const uint32_t sa = ptx::smem_u32(smem + s * kScStageBytes + kOffA);
         const uint64_t bd = ptx::smem_desc(ptx::smem_u32(qslots + qs.slot * kScQBytes + kQOffB), 16, 512, 4);
@@ -442,11 +481,12 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     __syncwarp();
   } else if (warp >= kScGather0) {
     // ------------------------------------------------------------ gathering warps (pool mode only)
-    if (P.pool != nullptr) {
+    if (POOL) {
       const int g = warp - kScGather0 + 1;
       QueryInfo gq;
+      gq.cache = qc;
       PoolGather pg;
-      pg.prefetch(P, g, blockIdx.x, gq, total_units);
+      pg.start(P, g, blockIdx.x, total_units);
       for (uint32_t it = 0;; it++) {
         if (abort_flag) break;
         uint32_t T;
@@ -456,8 +496,8 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         const int q = (int)(T / (uint32_t)P.units_per_q), u = (int)(T % (uint32_t)P.units_per_q);
         gq.set(P, q, u, false);                       // published units are valid
         if (!ptx::mbar_wait(&done_bar[s], (r & 1) ^ 1)) { fail(); break; }
-        pg.gather(P, g, T, q, u, (int64_t)gq.seq * P.n_max, smem + s * kScStageBytes, &full_bar[s]);
-        pg.prefetch(P, g, T + gridDim.x, gq, total_units);
+        pg.gather(P, g, T, (int64_t)gq.seq * P.n_max, smem + s * kScStageBytes, &full_bar[s], total_units);
+        if (T + gridDim.x < total_units) gq.prefetch(P, (int)((T + gridDim.x) / (uint32_t)P.units_per_q));
       }
     }
   } else {
@@ -472,17 +512,17 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     int cur_q = -1;
     float wv[kIdxHeads];
     QueryInfo sc;
+    sc.cache = qc;
     for (uint32_t it = 0;; it++) {
       if (abort_flag) break;
       uint32_t T;
       if (!ring_get(unit_ring, it, T, abort_flag)) { fail(); break; }   // every entry: the last may be either parity
       if (T == kDone) break;
       if ((it & 1) != group) continue;
-      const int cur_u = (int)(T % (uint32_t)P.units_per_q);
-      sc.set(P, (int)(T / (uint32_t)P.units_per_q), cur_u, false);
+      const int cur_u = (int)(T % (uint32_t)P.units_per_q), nq = (int)(T / (uint32_t)P.units_per_q);
       const uint32_t s = it % kScStages, r = it / kScStages;
-      if (sc.q != cur_q) {
-        const float4 *wp = reinterpret_cast<const float4 *>(P.w + (int64_t)sc.q * kIdxHeads);
+      auto load_w = [&]() {
+        const float4 *wp = reinterpret_cast<const float4 *>(P.w + (int64_t)nq * kIdxHeads);
 #pragma unroll
         for (int i = 0; i < 8; i++) {
           const float4 v = __ldg(wp + i);
@@ -491,18 +531,36 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
           wv[4 * i + 2] = v.z;
           wv[4 * i + 3] = v.w;
         }
-        cur_q = sc.q;
+        cur_q = nq;
+      };
+      int pb[kSub] = {};
+      if constexpr (POOL) {
+        // Pool mode changes query on every unit: every global load the unit's
+        // epilogue needs (the query's weights, the block id of each of this
+        // lane's four entries; its sequence and length are in shared memory)
+        // goes out before the wait for its MMA, so that their latencies
+        // overlap it and one another.
+        sc.prefetch(P, nq);
+        if (nq != cur_q) load_w();
+        const int32_t *pl = P.pool + (int64_t)nq * kPoolBlocks;
+#pragma unroll
+        for (int j = 0; j < kSub; j++) pb[j] = __ldg(pl + ((cur_u * kUnit + row + j * 128) >> 3));
+        if (!ptx::mbar_wait(&done_bar[s], r & 1)) { fail(); break; }
+        sc.set(P, nq, cur_u, false);
+      } else {
+        sc.set(P, nq, cur_u, false);
+        if (nq != cur_q) load_w();
+        if (!ptx::mbar_wait(&done_bar[s], r & 1)) { fail(); break; }
       }
-      if (!ptx::mbar_wait(&done_bar[s], r & 1)) { fail(); break; }
       ptx::tc_fence_after();
       const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + group * (kSub * 32);
       float *out = P.scores + (int64_t)sc.q * P.stride;
-      const int32_t *pl = P.pool + (int64_t)sc.q * kPoolBlocks;
-      auto store = [&](int64_t i, float v) {
-        if (P.pool == nullptr) {
+      // entry i = i0 + 128 j of the unit (j = 0..3)
+      auto store = [&](int64_t i, int j, float v) {
+        if (!POOL) {
           if (i < sc.nv) out[i] = v;
         } else {
-          const int b = __ldg(pl + (i >> 3));
+          const int b = j == 0 ? pb[0] : j == 1 ? pb[1] : j == 2 ? pb[2] : pb[3];   // (registers)
           const bool ok = b >= 0 && (int64_t)b * kBlock < P.n_max && (int64_t)b * kBlock + (i & 7) < sc.nv;
           out[i] = ok ? v : -INFINITY;
         }
@@ -526,8 +584,8 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
           s0 = fmaf(wv[h], fmaxf(__uint_as_float(d0[h]), 0.f), s0);
           s1 = fmaf(wv[h], fmaxf(__uint_as_float(d1[h]), 0.f), s1);
         }
-        store(i0 + h2 * 256, s0);
-        store(i0 + h2 * 256 + 128, s1);
+        store(i0 + h2 * 256, 2 * h2, s0);
+        store(i0 + h2 * 256 + 128, 2 * h2 + 1, s1);
         if (P.smax_mode != 0) {
           // order keys of this lane's two entries (0 if not visible)
           const uint32_t k0 = i0 + h2 * 256 < sc.nv ? order_key(s0) : 0u;
@@ -558,7 +616,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       for (int i = max(0, armed_sh - kScStages); i < armed_sh; i++)
         ptx::mbar_wait(&full_bar[i % kScStages], (uint32_t)(i / kScStages) & 1);
     }
-    if (P.pool != nullptr && (warp == 0 || warp >= kScGather0)) asm volatile("cp.async.wait_all;" ::: "memory");
+    if (POOL && (warp == 0 || warp >= kScGather0)) asm volatile("cp.async.wait_all;" ::: "memory");
     if (lane == 0 && (warp == 1 || warp == 2 || warp == kScMmaWarp2)) ptx::tc_commit(&drain_bar);
     ptx::mbar_wait(&drain_bar, 0);
   }
@@ -926,12 +984,18 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
   const int dev = current_device();
   static std::atomic<int> attr_done[kMaxDevices];
   const cudaError_t e = once_per_device(attr_done, dev, [&] {
-    return cudaFuncSetAttribute(index_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t e1 = cudaFuncSetAttribute(index_score_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)smem);
+    const cudaError_t e2 = cudaFuncSetAttribute(index_score_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)smem);
+    return e1 != cudaSuccess ? e1 : e2;
   });
   if (e != cudaSuccess) return e;
   const int n_sm = device_sm_count(dev);
   const int64_t grid = total_units < n_sm ? total_units : n_sm;
-  return launch_pdl(index_score_tc_kernel, dim3((unsigned)grid), dim3(kScThreads), smem, st, 1u, P);
+  return pool != nullptr
+             ? launch_pdl(index_score_tc_kernel<true>, dim3((unsigned)grid), dim3(kScThreads), smem, st, 1u, P)
+             : launch_pdl(index_score_tc_kernel<false>, dim3((unsigned)grid), dim3(kScThreads), smem, st, 1u, P);
 }
 
 }  // namespace csa2
