@@ -265,8 +265,9 @@ struct PoolGather {
   }
 };
 
-// POOL: pool mode (P.pool set: units of gathered 8-entry blocks).
-template <bool POOL>
+// POOL: pool mode (P.pool set: units of gathered 8-entry blocks); SMAX: the
+// maxima the epilogue writes (P.smax_mode: 0, 2 or 3, Full mode only).
+template <bool POOL, int SMAX>
 __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcArgs P) {
   extern __shared__ __align__(1024) unsigned char sc_smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -586,12 +587,12 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         }
         store(i0 + h2 * 256, 2 * h2, s0);
         store(i0 + h2 * 256 + 128, 2 * h2 + 1, s1);
-        if (P.smax_mode != 0) {
+        if constexpr (SMAX != 0) {
           // order keys of this lane's two entries (0 if not visible)
           const uint32_t k0 = i0 + h2 * 256 < sc.nv ? order_key(s0) : 0u;
           const uint32_t k1 = i0 + h2 * 256 + 128 < sc.nv ? order_key(s1) : 0u;
           // 32 consecutive entries per warp and sub-tile
-          uint32_t *gm = P.smax_mode == 2 ? P.smax + (int64_t)sc.q * P.sstride : P.gmax + (int64_t)sc.q * P.gstride;
+          uint32_t *gm = SMAX == 2 ? P.smax + (int64_t)sc.q * P.sstride : P.gmax + (int64_t)sc.q * P.gstride;
           const uint32_t g0 = __reduce_max_sync(0xFFFFFFFFu, k0), g1 = __reduce_max_sync(0xFFFFFFFFu, k1);
           if (lane == 0) {
             const int64_t e0 = (int64_t)cur_u * kUnit + h2 * 256 + quarter * 32;
@@ -601,7 +602,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
           umax = max(umax, max(g0, g1));
         }
       }
-      if (P.smax_mode == 3 && lane == 0) P.smax[(int64_t)sc.q * P.sstride + (int64_t)cur_u * 4 + quarter] = umax;
+      if (SMAX == 3 && lane == 0) P.smax[(int64_t)sc.q * P.sstride + (int64_t)cur_u * 4 + quarter] = umax;
     }
   }
   __syncthreads();
@@ -984,18 +985,23 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
   const int dev = current_device();
   static std::atomic<int> attr_done[kMaxDevices];
   const cudaError_t e = once_per_device(attr_done, dev, [&] {
-    const cudaError_t e1 = cudaFuncSetAttribute(index_score_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)smem);
-    const cudaError_t e2 = cudaFuncSetAttribute(index_score_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)smem);
-    return e1 != cudaSuccess ? e1 : e2;
+    const cudaError_t es[4] = {
+        cudaFuncSetAttribute(index_score_tc_kernel<false, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+        cudaFuncSetAttribute(index_score_tc_kernel<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+        cudaFuncSetAttribute(index_score_tc_kernel<false, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+        cudaFuncSetAttribute(index_score_tc_kernel<true, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)};
+    for (cudaError_t x : es)
+      if (x != cudaSuccess) return x;
+    return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
   const int n_sm = device_sm_count(dev);
   const int64_t grid = total_units < n_sm ? total_units : n_sm;
-  return pool != nullptr
-             ? launch_pdl(index_score_tc_kernel<true>, dim3((unsigned)grid), dim3(kScThreads), smem, st, 1u, P)
-             : launch_pdl(index_score_tc_kernel<false>, dim3((unsigned)grid), dim3(kScThreads), smem, st, 1u, P);
+  const dim3 g((unsigned)grid), b(kScThreads);
+  if (pool != nullptr) return launch_pdl(index_score_tc_kernel<true, 0>, g, b, smem, st, 1u, P);
+  if (P.smax_mode == 3) return launch_pdl(index_score_tc_kernel<false, 3>, g, b, smem, st, 1u, P);
+  if (P.smax_mode == 2) return launch_pdl(index_score_tc_kernel<false, 2>, g, b, smem, st, 1u, P);
+  return launch_pdl(index_score_tc_kernel<false, 0>, g, b, smem, st, 1u, P);
 }
 
 }  // namespace csa2

@@ -923,6 +923,11 @@ __device__ __noinline__ void sort_by_index(uint64_t *lc, int n) {
 // Pass 2: grid (P, n_q), clusters of P CTAs along x (P <= kMaxCluster): the
 // cluster rank of a CTA is blockIdx.x.  No thread returns before the second
 // cluster barrier.
+// GROUPS: plain rows with the indexer's unit partial maxima (parts == 4) and
+// 32-entry group maxima (csa2_decode's plan for 1M rows); compiled on its own,
+// without the code of the other paths, since it runs once per step with cold
+// instruction caches.
+template <bool GROUPS>
 __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S, int64_t sgi, int parts, int k,
                                                                        LongRowWs W, int32_t *__restrict__ out,
                                                                        int *status) {
@@ -941,7 +946,7 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
   griddep_launch();
   const int q = blockIdx.y, P = gridDim.x, part = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool plain = S.pool == nullptr && S.block == 1;
+  const bool plain = GROUPS || (S.pool == nullptr && S.block == 1);
   // Plain rows with the maxima of their 32-entry groups as well (written by
   // the indexer's epilogue, parts == 4): CTA p of the cluster takes the groups
   // [g_lo, g_hi) of the row and streams only those reaching T, about one per
@@ -949,7 +954,7 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
   // their entries.  Its groups' maxima are loaded up front, with the
   // supergroup maxima, before the row's length is known (slots past it hold
   // stale values and are masked once it is).
-  const bool by_groups = plain && parts == 4 && W.gmax != nullptr;
+  constexpr bool by_groups = GROUPS;
   const int gps = (int)(sgi >> 5);                                       // groups per supergroup
   const int64_t g_all = (W.sstride / 4) * gps;                           // group slots of a row
   const int64_t g_lo = part * g_all / P, g_hi = (part + 1) * g_all / P;
@@ -1378,8 +1383,10 @@ static unsigned collect_ctas(int dev, int n_q, int64_t n_items, int reserve = 0)
   if (dev < 0 || dev >= kMaxDevices) return 1;
   const size_t dsm = collect_smem_bytes();
   once_per_device(attr_done, dev, [&] {
-    cudaFuncSetAttribute(topk_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm);
-    cudaFuncSetAttribute(topk_collect_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaFuncSetAttribute(topk_collect_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm);
+    cudaFuncSetAttribute(topk_collect_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaFuncSetAttribute(topk_collect_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm);
+    cudaFuncSetAttribute(topk_collect_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaGetLastError();                                // a refused attribute leaves no error behind
     return cudaSuccess;
   });
@@ -1401,7 +1408,7 @@ static unsigned collect_ctas(int dev, int n_q, int64_t n_items, int reserve = 0)
       cfg.attrs = &at;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, topk_collect_kernel, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, topk_collect_kernel<false>, &cfg) != cudaSuccess) n = 0;
       cudaGetLastError();
       f = n + 1;
       fit[dev][p].store(f, std::memory_order_relaxed);
@@ -1446,7 +1453,7 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
                                      W, status);
   if (e != cudaSuccess) return e;
   const unsigned P = collect_ctas(dev, n_q, S.n_items);
-  return launch_pdl(topk_collect_kernel, dim3(P, n_q), dim3(kCollectThreads), dsm_collect, st, P, S, sgi, 1, k, W,
+  return launch_pdl(topk_collect_kernel<false>, dim3(P, n_q), dim3(kCollectThreads), dsm_collect, st, P, S, sgi, 1, k, W,
                     out, status);
 }
 
@@ -1515,8 +1522,11 @@ cudaError_t launch_topk_fused(const float *scores, int64_t stride, int n_q, cons
   S.n_seq = F.n_seq;
   const size_t dsm_collect = collect_smem_bytes();
   const unsigned P = collect_ctas(current_device(), n_q, n_max, F.reserve);
-  return launch_pdl(topk_collect_kernel, dim3(P, n_q), dim3(kCollectThreads), dsm_collect, st, P, S, F.sgi, F.parts,
-                    k, F.W, out, status);
+  if (F.parts == 4 && F.W.gmax != nullptr)
+    return launch_pdl(topk_collect_kernel<true>, dim3(P, n_q), dim3(kCollectThreads), dsm_collect, st, P, S, F.sgi,
+                      F.parts, k, F.W, out, status);
+  return launch_pdl(topk_collect_kernel<false>, dim3(P, n_q), dim3(kCollectThreads), dsm_collect, st, P, S, F.sgi,
+                    F.parts, k, F.W, out, status);
 }
 
 }  // namespace csa2
