@@ -47,6 +47,7 @@
 namespace csa2 {
 
 constexpr int kTcChunk = 128;
+static_assert(kHandCap > kTcChunk, "with the handoff a query always has several chunks (splits)");
 constexpr int kTcThreads = 256;
 // shared-memory layout (bytes; the big regions are 1024-aligned)
 constexpr int kSmK = 0;                         // 128 entries x 512 dims bf16  (128 KB)
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   __shared__ int hoff_sh[kHandCtas + 1];           // first candidate slot of each segment
   bool waited = false;
   if (HAND) griddep_launch();
-  if (!A.settled) {
+  if (!HAND && !A.settled) {                       // (the handoff runs inside csa2_decode: settled)
     griddep_wait();
     griddep_launch();
     waited = true;
@@ -725,13 +726,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   }
   // ---------------------------------------------------------- read-out
   {
+    // one split: the CTA finishes the output; else it writes its partials
+    // (always so with the handoff: a query's candidates take five chunks)
+    const bool one_split = !HAND && A.nsplit == 1;
     const int quarter = warp & 3;
     const int pos = __ldg(A.pos + qi);
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     for (int blk = warp >> 2; blk < 4; blk += 2) {
       const int d = blk * 128 + quarter * 32 + lane;   // TMEM lane = dim within block
       float rc = 1.f, rs = 0.f;                        // cos t, sin t of the pair holding d
-      if (d >= kRopeOff && A.nsplit == 1) rope_cs(A.inv_freq[(d - kRopeOff) >> 1], pos, rc, rs);
+      if (d >= kRopeOff && one_split) rope_cs(A.inv_freq[(d - kRopeOff) >> 1], pos, rc, rs);
 #pragma unroll
       for (int half = 0; half < NH / 32; half++) {
         uint32_t r[32], lr[32];
@@ -743,7 +747,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
 #pragma unroll
           for (int i = 0; i < 32; i++) r[i] = lr[i] = 0u;
         }
-        if (A.nsplit == 1) {
+        if (one_split) {
 #pragma unroll
           for (int i = 0; i < 32; i++) {
             const int h = h0 + half * 32 + i;
@@ -772,7 +776,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
         }
       }
     }
-    if (A.nsplit > 1 && t < NH) {
+    if (!one_split && t < NH) {
       // (the denominators, replicated over all 128 lanes, were written by lane 0 of warp 0)
       float *ml = A.part_ml + ((int64_t)qi * A.nsplit + split) * 2 * kHeads;
       ml[h0 + t] = any_chunk ? m_ref[t] : -INFINITY;
