@@ -469,7 +469,7 @@ __device__ int wide_find(const uint32_t *hist, int rem, uint32_t *above_out) {
 // 12 more when more than 64 values share the digit found, lower bits cleared.
 // Each step is one 4,096-bin histogram and a block-wide scan (blockDim.x ==
 // 1024).  hist: kWideBins counters.
-__device__ __noinline__ uint32_t block_kth_bound12(const uint32_t *v, int n, int rem, uint32_t *hist) {
+__device__ __forceinline__ uint32_t block_kth_bound12(const uint32_t *v, int n, int rem, uint32_t *hist) {
   const WideDigit wd = wide_digit([&](int i) { return v[i]; }, n, hist);
   if (wd.sh < 0) {
     __syncthreads();
@@ -513,7 +513,7 @@ __device__ __noinline__ uint32_t block_kth_bound12(const uint32_t *v, int n, int
 // kBinCap keys (many equal scores); the caller then runs select_block.
 // hist: kWideBins counters; bin_keys: kBinCap keys of scratch.
 constexpr int kBinCap = 256;
-__device__ __noinline__ bool select_small(const uint64_t *keys, int n, int k, int32_t *out, uint32_t *hist,
+__device__ __forceinline__ bool select_small(const uint64_t *keys, int n, int k, int32_t *out, uint32_t *hist,
                                           uint64_t *bin_keys, uint64_t *kth, uint64_t *pub) {
   __shared__ int n_bin;
   const int t = threadIdx.x;
@@ -905,7 +905,7 @@ static_assert(kMaxCluster <= kHandCtas && kHandSeg >= 256, "handoff segments");
 // a warp count for one key, each over every tpe-th key.  Block-wide
 // (blockDim.x == 1024); ends with lc written, not with a barrier.
 constexpr int kSortCap = 256;
-__device__ __noinline__ void sort_by_index(uint64_t *lc, int n) {
+__device__ __forceinline__ void sort_by_index(uint64_t *lc, int n) {
   const int tpe = n <= 32 ? 32 : n <= 64 ? 16 : n <= 128 ? 8 : 4;
   const int e = (int)threadIdx.x / tpe, sub = (int)threadIdx.x & (tpe - 1);
   uint64_t mine = 0;
