@@ -850,8 +850,15 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
     // group grp (warps 4+4 grp .. 7+4 grp) takes the units with it % 2 == grp
     // and owns accumulator grp (see the single-query kernel for why waiting on
     // done_bar is unambiguous)
+    // Each warp keeps its group's G x 32 weights in shared memory (read back
+    // four at a time, the same address in every lane) and the queries'
+    // visible lengths in registers, both reloaded when the group changes.
     const int quarter = warp & 3;
     const uint32_t grp = (uint32_t)(warp - 4) >> 2;
+    __shared__ __align__(16) float w_sm[8][kMqMaxG * 32];
+    float *wsm = w_sm[warp - 4];
+    int cur_gi = -1;
+    int nvq[G];
     for (uint32_t it = 0;; it++) {
       if (abort_flag) break;
       uint32_t T;
@@ -860,6 +867,13 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
       if ((it & 1) != grp) continue;
       const int gi = (int)(T / (uint32_t)P.units_per_q), u = (int)(T % (uint32_t)P.units_per_q);
       const uint32_t s = it % kMqStages, r = it / kMqStages;
+      if (gi != cur_gi) {
+        for (int i = lane; i < G * 32; i += 32) wsm[i] = __ldg(P.w + (int64_t)gi * G * kIdxHeads + i);
+#pragma unroll
+        for (int g = 0; g < G; g++) nvq[g] = __ldg(P.n_vis + gi * G + g);
+        __syncwarp();
+        cur_gi = gi;
+      }
       if (!ptx::mbar_wait(&done_bar[s], r & 1)) { fail(); break; }
       ptx::tc_fence_after();
       const int64_t e = (int64_t)u * kMqUnit + quarter * 32 + lane;
@@ -876,17 +890,18 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
         for (int b = 0; b < kB; b++)
           if (b < nb) ptx::tmem_ld_32x32b_x32(ta + (g0 + b) * 32, d[b]);
         ptx::tmem_wait_ld();
-        float acc[kB] = {0.f, 0.f, 0.f};
+        // two running sums per query (heads 4i, 4i+1 and 4i+2, 4i+3)
+        float acc[kB][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
         for (int i = 0; i < 8; i++) {
 #pragma unroll
           for (int b = 0; b < kB; b++) {
             if (b < nb) {
-              const float4 wv = __ldg(reinterpret_cast<const float4 *>(P.w + (int64_t)(gi * G + g0 + b) * kIdxHeads) + i);
-              acc[b] = fmaf(wv.x, fmaxf(__uint_as_float(d[b][4 * i]), 0.f), acc[b]);
-              acc[b] = fmaf(wv.y, fmaxf(__uint_as_float(d[b][4 * i + 1]), 0.f), acc[b]);
-              acc[b] = fmaf(wv.z, fmaxf(__uint_as_float(d[b][4 * i + 2]), 0.f), acc[b]);
-              acc[b] = fmaf(wv.w, fmaxf(__uint_as_float(d[b][4 * i + 3]), 0.f), acc[b]);
+              const float4 wv = reinterpret_cast<const float4 *>(wsm + (g0 + b) * kIdxHeads)[i];
+              acc[b][0] = fmaf(wv.x, fmaxf(__uint_as_float(d[b][4 * i]), 0.f), acc[b][0]);
+              acc[b][0] = fmaf(wv.y, fmaxf(__uint_as_float(d[b][4 * i + 1]), 0.f), acc[b][0]);
+              acc[b][1] = fmaf(wv.z, fmaxf(__uint_as_float(d[b][4 * i + 2]), 0.f), acc[b][1]);
+              acc[b][1] = fmaf(wv.w, fmaxf(__uint_as_float(d[b][4 * i + 3]), 0.f), acc[b][1]);
             }
           }
         }
@@ -894,7 +909,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
         for (int b = 0; b < kB; b++) {
           if (b < nb) {
             const int q = gi * G + g0 + b;
-            if (e < __ldg(P.n_vis + q)) P.scores[(int64_t)q * P.stride + e] = acc[b];
+            if (e < nvq[g0 + b]) P.scores[(int64_t)q * P.stride + e] = acc[b][0] + acc[b][1];
           }
         }
       }
