@@ -47,7 +47,8 @@ static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 // csa2_decode's workspace, each part 256-B aligned:
 // scores [n_q][n_max] fp32 | top-k scratch | attention partials
 // csa2_decode's workspace: scores | top-k scratch | attention partials | the
-// candidate handoff (flags, then keys), where the selection hands its
+// indexer's claim counter (256 B, where the maxima come from the indexer) |
+// the candidate handoff (flags, then keys), where the selection hands its
 // candidates to the attention (the maxima come from the indexer and all
 // attention CTAs holding candidates fit one wave).
 static bool decode_handoff(int n_q, int64_t n_max) {
@@ -57,6 +58,7 @@ static size_t decode_workspace_bytes(int n_q, int64_t n_max) {
   const bool hand = decode_handoff(n_q, n_max);
   size_t b = round256((size_t)n_q * (size_t)n_max * 4) + round256(topk_fused_bytes(n_q, n_max, kTopK)) +
              round256(attn_workspace_bytes(n_q, hand ? kHandCap : kTopK));
+  if (topk_fused_plan(nullptr, n_q, n_max, kTopK).mode > 0) b += 256;
   if (hand) b += round256((size_t)n_q * kHandWords * 4) + round256((size_t)n_q * kHandCtas * kHandSeg * 8);
   return b;
 }
@@ -290,9 +292,20 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
   const bool fused = F.mode > 0;
   const bool hand = decode_handoff(n_q, n_max);
   F.reserve = attn_ctas(n_q, hand ? kHandCap : kTopK);
+  unsigned char *after_attn = static_cast<unsigned char *>(ws_attn) +
+                              round256(attn_workspace_bytes(n_q, hand ? kHandCap : kTopK));
+  if (fused) {
+    // the indexer's claim counter, tagged per call (the tag is never 0)
+    static std::atomic<uint32_t> calls{0};
+    uint32_t id = calls.fetch_add(1, std::memory_order_relaxed) + 1u;
+    if (id == 0u) id = calls.fetch_add(1, std::memory_order_relaxed) + 1u;
+    F.W.steal = reinterpret_cast<unsigned long long *>(after_attn);
+    F.W.call_id = id;
+    after_attn += 256;
+  }
   Handoff H = {nullptr, nullptr, 0};
   if (hand) {
-    unsigned char *hb = static_cast<unsigned char *>(ws_attn) + round256(attn_workspace_bytes(n_q, kHandCap));
+    unsigned char *hb = after_attn;
     H.flag = reinterpret_cast<uint32_t *>(hb);
     H.cand = reinterpret_cast<uint64_t *>(hb + round256((size_t)n_q * kHandWords * 4));
     H.parts = topk_fused_ctas(F, n_q, n_max) / n_q;   // the selection's cluster size

@@ -83,6 +83,10 @@ struct LongRowWs {
   int64_t gstride = 0;
   // optional (csa2_decode): the candidate handoff to the attention, or null
   Handoff hand = {nullptr, nullptr, 0};
+  // optional (csa2_decode): the indexer's claim counter for its last rounds of
+  // units, and this call's tag (never 0; see index_score_tc_kernel)
+  unsigned long long *steal = nullptr;
+  uint32_t call_id = 0;
 };
 
 // Launch `kern` with programmatic stream serialisation (the kernel calls

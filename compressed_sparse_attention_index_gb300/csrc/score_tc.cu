@@ -112,7 +112,20 @@ struct ScoreTcArgs {
   // optional: the candidate-handoff flags of the selection and attention
   // grids that follow ([n_q][kHandWords] words; words 0-3 zeroed here)
   uint32_t *hflag;
+  // optional (Full mode): the claim counter of the last kStealRounds rounds of
+  // units, tagged with call_id in its upper 32 bits (see the producer)
+  unsigned long long *steal;
+  uint32_t call_id;
 };
+
+// Full mode inside csa2_decode: a CTA takes the units T = blockIdx.x + k gridDim.x
+// up to the last kStealRounds rounds, then claims units one at a time from a
+// counter, so that the SMs that stream faster take more of the tail.
+// Only where a CTA has many rounds (measured: 8 x 1M, 108 rounds, -2 us per
+// step; 32 x 64K, 27 rounds, +4.7 us: there a claimed unit is a fresh query
+// almost every time).
+constexpr int kStealRounds = 4;
+constexpr uint32_t kStealMinRounds = 32;
 
 // Work units are T = (query, unit) in query-major order, T < n_q * units_per_q;
 // a CTA takes T = blockIdx.x, blockIdx.x + gridDim.x, ...  The producer walks
@@ -285,19 +298,9 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   __shared__ int2 qcache[POOL ? kQCache : 1];      // pool mode: (q_seq, n_vis) of every query, when n_q <= kQCache
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // everything below reads inputs or allocates TMEM: after the grid ahead
-  griddep_wait();
-  griddep_launch();
-  // (pool mode only, where the query changes on every unit; elsewhere the
-  // first unit would wait for the table)
-  const int2 *qc = POOL && P.n_q <= kQCache ? qcache : nullptr;
-  if (qc != nullptr)
-    for (int i = threadIdx.x; i < P.n_q; i += blockDim.x) qcache[i] = make_int2(__ldg(P.q_seq + i), __ldg(P.n_vis + i));
-  // (the previous call's attention, which read these flags, has completed:
-  // the grid ahead waited for it)
-  if (P.hflag != nullptr)
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 4 * P.n_q; i += gridDim.x * blockDim.x)
-      P.hflag[(i >> 2) * kHandWords + (i & 3)] = 0u;
+  // The barriers and the tensor memory are set up before the wait for the
+  // grid ahead: neither touches memory that grid writes, and this CTA is
+  // placed only where no CTA holding tensor memory remains.
   if (threadIdx.x == 0) {
     for (int s = 0; s < kScStages; s++) {
       ptx::mbar_init(&full_bar[s], POOL ? 1 + 32 * kPoolGatherWarps : 1);   // pool: see PoolGather
@@ -315,6 +318,21 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // everything below reads inputs: after the grid ahead
+  griddep_wait();
+  griddep_launch();
+  // (pool mode only, where the query changes on every unit; elsewhere the
+  // first unit would wait for the table)
+  const int2 *qc = POOL && P.n_q <= kQCache ? qcache : nullptr;
+  if (qc != nullptr) {
+    for (int i = threadIdx.x; i < P.n_q; i += blockDim.x) qcache[i] = make_int2(__ldg(P.q_seq + i), __ldg(P.n_vis + i));
+    __syncthreads();
+  }
+  // (the previous call's attention, which read these flags, has completed:
+  // the grid ahead waited for it)
+  if (P.hflag != nullptr)
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 4 * P.n_q; i += gridDim.x * blockDim.x)
+      P.hflag[(i >> 2) * kHandWords + (i & 3)] = 0u;
   const uint32_t tmem = tmem_base_sh;
 
   auto fail = [&]() {
@@ -329,7 +347,48 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     QuerySlots qs;
     QueryInfo sc;
     sc.cache = qc;
+    // Claims (Full mode with a counter): the counter holds this call's tag
+    // in its upper half and the next claim index in its lower half.  A value
+    // with another tag is left from an earlier call (or is the workspace's
+    // initial contents).  Before its first claim each CTA makes sure the tag
+    // is this call's, by compare-and-swap alone (no CTA adds before it has
+    // seen the tag, so every failed swap means another CTA installed it).
+    // One claim is then always in flight (lane 0), issued a unit ahead of its
+    // use, so that the atomic's latency hides behind the unit's copies.
+    const bool steal = !POOL && P.steal != nullptr && total_units >= kStealMinRounds * gridDim.x;
+    const uint32_t s_static =
+        steal ? (uint32_t)max(0, (int)(total_units / gridDim.x) - kStealRounds) * gridDim.x : total_units;
+    unsigned long long claim_v = 0ull;
+    if (steal && lane == 0) {
+      unsigned long long v = *reinterpret_cast<volatile unsigned long long *>(P.steal);
+      int tries = 0;
+      for (; tries < 4096 && (uint32_t)(v >> 32) != P.call_id; tries++) {
+        const unsigned long long w = atomicCAS(P.steal, v, (unsigned long long)P.call_id << 32);
+        if (w == v) break;                                             // installed: index 0 is next
+        v = w;
+      }
+      if (tries == 4096) record_error(P.status, CSA2_ERR_TIMEOUT);   // (never seen)
+      claim_v = atomicAdd(P.steal, 1ull);
+    }
+    auto claim_next = [&]() -> uint32_t {
+      uint32_t idx = kDone;
+      if (lane == 0) {
+        if ((uint32_t)(claim_v >> 32) == P.call_id) idx = (uint32_t)claim_v;
+        claim_v = atomicAdd(P.steal, 1ull);                            // the next claim goes out now
+      }
+      return __shfl_sync(0xFFFFFFFFu, idx, 0);
+    };
+    // the unit after Tc in this CTA's sequence (total_units: none left)
+    auto advance = [&](uint32_t Tc) -> uint32_t {
+      if (!steal || Tc + gridDim.x < s_static) return Tc + gridDim.x;
+      const uint32_t i = claim_next();
+      return i < total_units - s_static ? s_static + i : total_units;
+    };
     uint32_t T = blockIdx.x;
+    if (steal && T >= s_static) {
+      const uint32_t i = claim_next();
+      T = i < total_units - s_static ? s_static + i : total_units;
+    }
     PoolGather pg;
     if (POOL) pg.start(P, 0, T, total_units);
     for (uint32_t it = 0;; it++) {
@@ -342,7 +401,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         uq = (int)(T - (uint32_t)q * (uint32_t)P.units_per_q);
         sc.set(P, q, uq, lane == 0);
         if (sc.nv >= 0 && (POOL || uq * kUnit < sc.nv)) break;
-        T += gridDim.x;
+        T = advance(T);
       }
       if (lane == 0) unit_ring[it % kRing] = ((unsigned long long)it << 32) | T;
       if (T == kDone) break;
@@ -394,7 +453,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       }
       __syncwarp();
       if (lane == 0) armed_sh = (int)it + 1;
-      T += gridDim.x;
+      T = advance(T);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ scale-factor warp
@@ -978,6 +1037,8 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
   P.gmax = W ? W->gmax : nullptr;
   P.gstride = W ? W->gstride : 0;
   P.hflag = W && pool == nullptr ? W->hand.flag : nullptr;
+  P.steal = W && pool == nullptr ? W->steal : nullptr;
+  P.call_id = W ? W->call_id : 0u;
   P.smax_mode = pool == nullptr && W != nullptr && (smax_mode == 2 || (smax_mode == 3 && W->gmax != nullptr))
                     ? smax_mode : 0;
   P.key_nib = key_nib;
