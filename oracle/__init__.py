@@ -62,6 +62,7 @@ def lib():
             "orc_e4m3_encode": (i32, [f64]), "orc_bf16_from_double": (ctypes.c_uint16, [f64]),
             "orc_pack_kv": (None, [P, i64, P]), "orc_pack_idx": (None, [P, i64, P]),
             "orc_pack_swa": (None, [P, i64, P]), "orc_pool_m2": (None, [P, P, i64, P]),
+            "orc_project_keys": (None, [P, i64, P, P]),
             "orc_dequant_kv": (None, [P, P]), "orc_dequant_idx": (None, [P, P]),
             "orc_dequant_swa": (None, [P, P]),
             "orc_index_score": (None, [P, i64, P, P, P]),
@@ -130,6 +131,16 @@ def pool_m2(x_bf16: np.ndarray, z: np.ndarray) -> np.ndarray:
     assert x.shape == z.shape and x.shape[0] % 2 == 0
     out = np.zeros((x.shape[0] // 2, D), np.uint16)
     lib().orc_pool_m2(_p(x), _p(z), out.shape[0], _p(out))
+    return out
+
+
+def project_keys(x_bf16: np.ndarray, w_bf16: np.ndarray) -> np.ndarray:
+    """The indexer keys of latents x ([rows][512] bf16 bits) under the 512 -> 128
+    projection w ([128][512] bf16 bits): [rows][128] bf16 bits."""
+    x = _c(x_bf16, np.uint16).reshape(-1, D)
+    w = _c(w_bf16, np.uint16).reshape(128, D)
+    out = np.zeros((x.shape[0], 128), np.uint16)
+    lib().orc_project_keys(_p(x), x.shape[0], _p(w), _p(out))
     return out
 
 

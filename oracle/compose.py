@@ -22,7 +22,7 @@ import numpy as np
 from gen.workloads import Workload, TOPK, SWA, BLOCK, POOL_BLOCKS
 
 __all__ = ["packed_keys", "kv_records", "swa_records", "query_inputs", "decode_query",
-           "full_scores", "reindex_query", "reindex_on_pool", "decoder_step_query", "layer_attention"]
+           "full_scores", "reindex_query", "reindex_on_pool", "decoder_step_query", "layer_attention", "build_cache"]
 
 
 def _o():
@@ -179,3 +179,18 @@ def decoder_step_query(wl: Workload, qi: int, layers, pool=None, sels=None) -> d
     att = sels if sels is not None else osel
     outs = [layer_attention(wl, qi, l, att[r]) for l, (role, r) in enumerate(layers)]
     return {"pool": opool, "sel": osel, "scores": scores, "out": outs}
+
+
+def build_cache(tokens_bf16: np.ndarray, gate_logits, w_idx_bf16: np.ndarray, m: int) -> dict:
+    """The cache a prompt's tokens leave (encoder entries: m = 2, two tokens
+    pooled into one entry by the learned softmax gate; decoder: m = 1), in the
+    pages' order ("An infra-oriented diagram of the DeepSeek-V4.1-Flash
+    architecture", reading notes on the Full layer's global KV and section "The
+    KV cache"): the entry's latent, its 288-B main-cache record, its indexer key
+    (the 512 -> 128 projection of the same latent) and that key's 68-B record."""
+    o = _o()
+    lat = np.asarray(tokens_bf16, np.uint16).reshape(-1, 512)
+    if m == 2:
+        lat = o.pool_m2(lat, gate_logits)
+    keys = o.project_keys(lat, w_idx_bf16)
+    return {"latent": lat, "kv": o.pack_kv(lat), "keys": keys, "idx": o.pack_idx(keys)}

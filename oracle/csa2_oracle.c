@@ -243,6 +243,25 @@ void orc_pool_m2(const uint16_t *x, const float *z, int64_t rows_out, uint16_t *
                         z + (2 * r + 1) * ORC_DIM, out + r * ORC_DIM);
 }
 
+/* Indexer-key projection: the indexer's 128-wide key is a 512 -> 128
+ * projection of the same latent the main cache stores [study, reading notes on
+ * the Full layer's global KV].  The weights are not on the pages (synthetic
+ * here).  Reading: out[r][n] = sum_c x[r][c] * w[n][c] over the bf16 latent
+ * (the m=2 pooled one for encoder entries) and bf16 weights, exact in fp64 and
+ * rounded once to bf16, the input of the key's FP4 packing.
+ * x: [rows][512], w: [128][512], out: [rows][128], all bf16 bits. */
+void orc_project_keys(const uint16_t *x, int64_t rows, const uint16_t *w, uint16_t *out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++) {
+        for (int n = 0; n < ORC_IDIM; n++) {
+            double acc = 0.0;
+            for (int c = 0; c < ORC_DIM; c++)
+                acc += orc_bf16_value(x[r * ORC_DIM + c]) * orc_bf16_value(w[(int64_t)n * ORC_DIM + c]);
+            out[r * ORC_IDIM + n] = orc_bf16_from_double(acc);
+        }
+    }
+}
+
 /* ---------------------------------------------------------------- dequant */
 void orc_dequant_kv(const uint8_t *rec, double *out) {
     for (int c = 0; c < ORC_DIM; c++) {
