@@ -17,13 +17,15 @@ LIB_PATH = os.path.join(HERE, "libcsa2.so")
 CSA2_KV_NVFP4, CSA2_IDX_MXFP4, CSA2_SWA_MXFP8 = 0, 1, 2
 CSA2_OUT_BF16, CSA2_OUT_F32 = 0, 1
 CSA2_OP_TOPK, CSA2_OP_SPARSE_ATTN, CSA2_OP_DECODE, CSA2_OP_DECODE_HOST, CSA2_OP_DECODE_MQ = 0, 1, 2, 3, 4
+CSA2_OP_BUILD_CACHE = 5
 STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED", 3: "CSA2_ERR_CUDA",
           4: "CSA2_ERR_BOUNDS", 5: "CSA2_ERR_TIMEOUT", 6: "CSA2_ERR_WORKSPACE"}
 
 EXPORTS = ["csa2_default_params", "csa2_entry_bytes", "csa2_status_string", "csa2_fp4_pack",
            "csa2_index_score", "csa2_topk", "csa2_sparse_attn", "csa2_workspace_size",
            "csa2_get_device_status", "csa2_topk_noalloc", "csa2_decode", "csa2_decode_host",
-           "csa2_index_score_mq", "csa2_decode_mq", "csa2_check_bounded_wait"]
+           "csa2_index_score_mq", "csa2_decode_mq", "csa2_check_bounded_wait", "csa2_index_key_proj",
+           "csa2_build_cache"]
 
 
 class CSA2Error(RuntimeError):
@@ -69,6 +71,8 @@ def load(path: str = LIB_PATH):
         "csa2_workspace_size": (i32, [i32, i32, i64, i32, ctypes.POINTER(sz)]),
         "csa2_get_device_status": (i32, [P, ctypes.POINTER(i32)]),
         "csa2_check_bounded_wait": (i32, [ctypes.c_uint, P]),
+        "csa2_index_key_proj": (i32, [P, i64, P, P, P]),
+        "csa2_build_cache": (i32, [P, i64, i32, P, P, P, P, P, P, sz, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -203,3 +207,15 @@ def csa2_get_device_status(stream=None) -> int:
     v = ctypes.c_int(0)
     _check("csa2_get_device_status", load().csa2_get_device_status(_stream(stream), ctypes.byref(v)))
     return int(v.value)
+
+
+def csa2_index_key_proj(latent, rows, w_idx, keys, stream=None):
+    _check("csa2_index_key_proj", load().csa2_index_key_proj(_ptr(latent), int(rows), _ptr(w_idx), _ptr(keys),
+                                                               _stream(stream)))
+
+
+def csa2_build_cache(tokens, n_tokens, m, gate_logits, w_idx, kv, idx_nib, idx_scale, workspace, workspace_bytes,
+                     stream=None):
+    _check("csa2_build_cache", load().csa2_build_cache(_ptr(tokens), int(n_tokens), int(m), _ptr(gate_logits),
+                                                         _ptr(w_idx), _ptr(kv), _ptr(idx_nib), _ptr(idx_scale),
+                                                         _ptr(workspace), int(workspace_bytes), _stream(stream)))

@@ -169,6 +169,15 @@ static HostStage host_stage(int n_q) {
   return h;
 }
 
+// csa2_build_cache's workspace for one chunk of entries: the keys (bf16
+// [chunk][128]) and, for m = 2, the pooled latents (bf16 [chunk][512]).
+constexpr int64_t kBuildChunk = 32768;
+static size_t build_cache_workspace_bytes(int64_t n_tokens, int m) {
+  const int64_t entries = n_tokens / m;
+  const int64_t c = entries < kBuildChunk ? entries : kBuildChunk;
+  return round256((size_t)c * kIdxDim * 2) + (m == 2 ? round256((size_t)c * kDim * 2) : 0);
+}
+
 // csa2_decode_mq's workspace: scores [n_q][n_max] | top-k scratch | attention partials
 static size_t decode_mq_workspace_bytes(int n_q, int64_t n_max) {
   return round256((size_t)n_q * (size_t)n_max * 4) + round256(topk_workspace_bytes(n_q, n_max, kTopK)) +
@@ -177,6 +186,11 @@ static size_t decode_mq_workspace_bytes(int n_q, int64_t n_max) {
 
 csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t *bytes) {
   if (bytes == nullptr || n_q < 0 || n_items < 0) return CSA2_ERR_INVALID_ARG;
+  if (op == CSA2_OP_BUILD_CACHE) {
+    if (n_items < 0 || (k != 1 && k != 2)) return CSA2_ERR_INVALID_ARG;
+    *bytes = build_cache_workspace_bytes(n_items, k);
+    return CSA2_OK;
+  }
   if (op == CSA2_OP_DECODE_MQ) {
     if (n_items <= 0) return CSA2_ERR_INVALID_ARG;
     *bytes = decode_mq_workspace_bytes(n_q, n_items);
@@ -433,6 +447,56 @@ csa2_status csa2_decode_host(const void *key_nib, const void *key_scale, int64_t
   if (cudaMemcpyAsync(h_out, st + H.out, b_out, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CSA2_ERR_CUDA;
   if (h_sel != nullptr && cudaMemcpyAsync(h_sel, st + H.sel, b_sel, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return CSA2_ERR_CUDA;
+  return CSA2_OK;
+}
+
+csa2_status csa2_index_key_proj(const void *latent, int64_t rows, const void *w_idx, void *keys,
+                                csa2_stream_t stream) {
+  if (rows < 0 || rows > ((int64_t)1 << 40)) return CSA2_ERR_INVALID_ARG;
+  if (rows == 0) return CSA2_OK;
+  if (!latent || !w_idx || !keys) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(latent, 16) || !aligned(w_idx, 16) || !aligned(keys, 16)) return CSA2_ERR_INVALID_ARG;
+  int *st = status_ptr();
+  if (st == nullptr) return CSA2_ERR_CUDA;
+  return from_cuda(launch_proj_keys(latent, rows, w_idx, keys, st, (cudaStream_t)stream));
+}
+
+csa2_status csa2_build_cache(const void *tokens, int64_t n_tokens, int m, const float *gate_logits,
+                             const void *w_idx, void *kv, void *idx_nib, void *idx_scale, void *workspace,
+                             size_t workspace_bytes, csa2_stream_t stream) {
+  if (n_tokens < 0 || (m != 1 && m != 2) || n_tokens % (8 * m) != 0 || n_tokens > ((int64_t)1 << 40))
+    return CSA2_ERR_INVALID_ARG;
+  if ((m == 2) != (gate_logits != nullptr)) return CSA2_ERR_INVALID_ARG;
+  if (n_tokens == 0) return CSA2_OK;
+  if (!tokens || !w_idx || !kv || !idx_nib || !idx_scale) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(tokens, 16) || !aligned(w_idx, 16) || !aligned(kv, 16) || !aligned(idx_nib, 512) ||
+      !aligned(idx_scale, 4) || (gate_logits && !aligned(gate_logits, 16)))
+    return CSA2_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < build_cache_workspace_bytes(n_tokens, m))
+    return CSA2_ERR_WORKSPACE;
+  int *st = status_ptr();
+  if (st == nullptr) return CSA2_ERR_CUDA;
+  const cudaStream_t s = (cudaStream_t)stream;
+  const int64_t entries = n_tokens / m;
+  uint16_t *keys = static_cast<uint16_t *>(workspace);
+  uint16_t *pooled = m == 2 ? reinterpret_cast<uint16_t *>(static_cast<unsigned char *>(workspace) +
+                                                           round256((size_t)kBuildChunk * kIdxDim * 2))
+                            : nullptr;
+  const uint16_t *tok = static_cast<const uint16_t *>(tokens);
+  for (int64_t e0 = 0; e0 < entries; e0 += kBuildChunk) {
+    const int64_t ne = entries - e0 < kBuildChunk ? entries - e0 : kBuildChunk;
+    // the chunk's latents (m = 2: pooled into the workspace) and main-cache records
+    cudaError_t e = launch_pack(CSA2_KV_NVFP4, tok + e0 * m * kDim, ne * m, m, m == 2 ? gate_logits + e0 * 2 * kDim : nullptr,
+                                static_cast<uint8_t *>(kv) + e0 * kKvBytes, nullptr, s, pooled);
+    if (e != cudaSuccess) return CSA2_ERR_CUDA;
+    // their keys, then the keys' records (e0 is a multiple of 8: the key plane's swizzle holds per chunk)
+    e = launch_proj_keys(m == 2 ? static_cast<const void *>(pooled) : static_cast<const void *>(tok + e0 * kDim), ne,
+                         w_idx, keys, st, s);
+    if (e != cudaSuccess) return CSA2_ERR_CUDA;
+    e = launch_pack(CSA2_IDX_MXFP4, keys, ne, 1, nullptr, static_cast<uint8_t *>(idx_nib) + e0 * (kIdxDim / 2),
+                    static_cast<uint8_t *>(idx_scale) + e0 * 4, s);
+    if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  }
   return CSA2_OK;
 }
 

@@ -137,8 +137,13 @@ struct FusedTopk {
   int reserve;
 };
 
+// pooled (KV, m = 2, optional): also write the pooled bf16 latents, [rows / 2][512]
 cudaError_t launch_pack(int kind, const void *src, int64_t rows, int m, const float *gate, void *dst,
-                        void *dst_scales, cudaStream_t st);
+                        void *dst_scales, cudaStream_t st, void *pooled = nullptr);
+
+// The indexer keys of rows bf16 latents under the 512 -> 128 bf16 weights
+// w ([128][512]): out [rows][128] bf16 (tcgen05, fp32 accumulation).
+cudaError_t launch_proj_keys(const void *x, int64_t rows, const void *w, void *out, int *status, cudaStream_t st);
 
 // W / smax_mode: maxima for a fused top-k (smax_mode 0: none).
 cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_scale, int64_t n_max, int n_seq,

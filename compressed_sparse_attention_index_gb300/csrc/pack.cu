@@ -65,11 +65,12 @@ __device__ __forceinline__ uint32_t bf16_from_f64(double v) {
 }
 
 // ------------------------------------------------------------------ KV (S1)
-// One warp per output row; lane g packs channels [16g, 16g+16).
+// One warp per output row; lane g packs channels [16g, 16g+16).  pooled
+// (M = 2, optional): the pooled bf16 latents as well, [rows_out][512].
 template <int M>
 __global__ void __launch_bounds__(256) pack_kv_kernel(const uint16_t *__restrict__ src,
                                                        const float *__restrict__ gate, int64_t rows_out,
-                                                       uint8_t *__restrict__ dst) {
+                                                       uint8_t *__restrict__ dst, uint16_t *__restrict__ pooled) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= rows_out) return;
@@ -98,6 +99,14 @@ __global__ void __launch_bounds__(256) pack_kv_kernel(const uint16_t *__restrict
       double ea = exp(za - mz), eb = exp(zb - mz);
       double v = (ea * (double)t0 + eb * (double)t1) / (ea + eb);
       x[i] = __uint_as_float(bf16_from_f64(v) << 16);
+    }
+    if (pooled != nullptr) {
+      uint32_t b[8];
+#pragma unroll
+      for (int i = 0; i < 8; i++) b[i] = (__float_as_uint(x[2 * i]) >> 16) | (__float_as_uint(x[2 * i + 1]) & 0xFFFF0000u);
+      uint4 *po = reinterpret_cast<uint4 *>(pooled + row * kDim + lane * 16);
+      po[0] = make_uint4(b[0], b[1], b[2], b[3]);
+      po[1] = make_uint4(b[4], b[5], b[6], b[7]);
     }
   }
   float amax = 0.f;
@@ -211,15 +220,16 @@ __global__ void __launch_bounds__(256) pack_swa_kernel(const uint16_t *__restric
 
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_pack(int kind, const void *src, int64_t rows, int m, const float *gate, void *dst,
-                        void *dst_scales, cudaStream_t st) {
+                        void *dst_scales, cudaStream_t st, void *pooled) {
   const uint16_t *s = static_cast<const uint16_t *>(src);
   if (kind == CSA2_KV_NVFP4) {
     const int64_t out_rows = rows / m;
     const int64_t blocks = (out_rows + 7) / 8;
     if (m == 1)
-      pack_kv_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(s, nullptr, out_rows, (uint8_t *)dst);
+      pack_kv_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(s, nullptr, out_rows, (uint8_t *)dst, nullptr);
     else
-      pack_kv_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(s, gate, out_rows, (uint8_t *)dst);
+      pack_kv_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(s, gate, out_rows, (uint8_t *)dst,
+                                                          static_cast<uint16_t *>(pooled));
   } else if (kind == CSA2_IDX_MXFP4) {
     const int64_t blocks = (rows * 8 + 255) / 256;
     pack_idx_kernel<<<(unsigned)blocks, 256, 0, st>>>(s, rows, (uint8_t *)dst, (uint8_t *)dst_scales);

@@ -80,7 +80,8 @@ enum { CSA2_KV_NVFP4 = 0, CSA2_IDX_MXFP4 = 1, CSA2_SWA_MXFP8 = 2 };
 /* Output dtypes for csa2_sparse_attn. */
 enum { CSA2_OUT_BF16 = 0, CSA2_OUT_F32 = 1 };
 /* Operations for csa2_workspace_size. */
-enum { CSA2_OP_TOPK = 0, CSA2_OP_SPARSE_ATTN = 1, CSA2_OP_DECODE = 2, CSA2_OP_DECODE_HOST = 3, CSA2_OP_DECODE_MQ = 4 };
+enum { CSA2_OP_TOPK = 0, CSA2_OP_SPARSE_ATTN = 1, CSA2_OP_DECODE = 2, CSA2_OP_DECODE_HOST = 3, CSA2_OP_DECODE_MQ = 4,
+       CSA2_OP_BUILD_CACHE = 5 };
 
 /* Model constants.  The kernels are built for the pages' values only
  * (study, reading notes: 64 heads, 512-wide latent, RoPE on 64 of the 512
@@ -340,6 +341,49 @@ csa2_status csa2_decode_host(const void *key_nib, const void *key_scale, int64_t
                              const csa2_params *params, void *workspace, size_t workspace_bytes, csa2_stream_t stream);
 
 /*
+ * csa2_index_key_proj -- the indexer keys of cache entries: the 512 -> 128
+ * projection of each entry's latent ("An infra-oriented diagram of the
+ * DeepSeek-V4.1-Flash architecture", reading notes on the Full layer's global
+ * KV: the indexer's key is a 512 -> 128 projection of the same latent).  The
+ * pages give no weights; the caller supplies them.
+ *   keys[r][n] = bf16( sum_c latent[r][c] * w_idx[n][c] ), fp32 accumulation on
+ *   the tensor cores, rounded to nearest even.
+ *   latent  (device) bf16 [rows][512], 16-B aligned.
+ *   w_idx   (device) bf16 [128][512], 16-B aligned.
+ *   keys    (device) bf16 [rows][128], 16-B aligned; the input of
+ *           csa2_fp4_pack(CSA2_IDX_MXFP4, ...).
+ */
+csa2_status csa2_index_key_proj(const void *latent, int64_t rows, const void *w_idx, void *keys,
+                                csa2_stream_t stream);
+
+/*
+ * csa2_build_cache -- the cache entries of a prompt (the study's reading
+ * notes: encoder caches pool two tokens into one entry with a learned softmax
+ * gate, m = 2; the decoder's Full layer keeps one entry per token, m = 1; the
+ * indexer's key is a 512 -> 128 projection of the entry's latent): per entry,
+ * the latent (gated pooling for m = 2), its 288-B main-cache record, its key
+ * (csa2_index_key_proj) and the key's two-plane 68-B record -- the same bytes
+ * as csa2_fp4_pack(CSA2_KV_NVFP4, m), csa2_index_key_proj and
+ * csa2_fp4_pack(CSA2_IDX_MXFP4) on the pooled latents.  Prompts of any length
+ * (1,048,576 tokens and more) are built in chunks of 32,768 entries, so the
+ * scratch stays bounded.
+ *   tokens       (device) bf16 [n_tokens][512], 16-B aligned.
+ *   n_tokens     a multiple of 8 m (so that chunks start on 8-row boundaries
+ *                of the key plane).
+ *   m, gate_logits   as csa2_fp4_pack (gate_logits [n_tokens][512] for m = 2,
+ *                NULL for m = 1).
+ *   w_idx        (device) bf16 [128][512].
+ *   kv           (device) [n_tokens / m][288]; idx_nib [n_tokens / m][64]
+ *                (512-B aligned, the swizzled key plane); idx_scale
+ *                [n_tokens / m][4].  Entry e of the prompt is row e of each.
+ *   workspace    (device) >= csa2_workspace_size(CSA2_OP_BUILD_CACHE, 0,
+ *                n_tokens, m) bytes, 256-B aligned; no initialisation.
+ */
+csa2_status csa2_build_cache(const void *tokens, int64_t n_tokens, int m, const float *gate_logits,
+                             const void *w_idx, void *kv, void *idx_nib, void *idx_scale, void *workspace,
+                             size_t workspace_bytes, csa2_stream_t stream);
+
+/*
  * csa2_workspace_size -- scratch bytes needed by an operation.
  *   op = CSA2_OP_TOPK:        n_q queries, n_items = items per row (entries,
  *                             blocks, or 16384 pool slots), k.
@@ -348,6 +392,7 @@ csa2_status csa2_decode_host(const void *key_nib, const void *key_scale, int64_t
  *   op = CSA2_OP_DECODE_HOST: as CSA2_OP_DECODE (the device copies of the
  *                             step's inputs and outputs are included).
  *   op = CSA2_OP_DECODE_MQ:   n_q queries, n_items = n_max, k unused (512).
+ *   op = CSA2_OP_BUILD_CACHE: n_q unused, n_items = tokens, k = m (1 or 2).
  * Sizes are for the current device (the attention's split plan follows its
  * SM count).
  */

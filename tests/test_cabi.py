@@ -76,6 +76,17 @@ def test_host_validation_rejects_before_launch(lib):
     assert L.csa2_decode_host(*args, fake, fake, fake, None, 1, None, fake, 0, None, fake, 1 << 30, None) == INVALID
     assert L.csa2_decode_host(*args, fake, fake, fake, fake, 1, None, fake, 0, None, fake, 1024, None) == WS
     assert L.csa2_decode_host(*args, fake, fake, fake, fake, 1, None, fake, 7, None, fake, 1 << 30, None) == INVALID
+    # csa2_index_key_proj / csa2_build_cache: negative or ragged sizes, a gate
+    # that does not match m, an unaligned key plane, a short workspace
+    assert L.csa2_index_key_proj(fake, -1, fake, fake, None) == INVALID
+    assert L.csa2_index_key_proj(fake, 0, None, None, None) == 0                         # nothing to do
+    assert L.csa2_index_key_proj(fake + 8, 4, fake, fake, None) == INVALID
+    assert L.csa2_build_cache(fake, 24, 2, fake, fake, fake, fake, fake, fake, 1 << 30, None) == INVALID
+    assert L.csa2_build_cache(fake, 32, 2, None, fake, fake, fake, fake, fake, 1 << 30, None) == INVALID
+    assert L.csa2_build_cache(fake, 32, 1, fake, fake, fake, fake, fake, fake, 1 << 30, None) == INVALID
+    assert L.csa2_build_cache(fake, 32, 1, None, fake, fake, fake + 256, fake, fake,
+                              1 << 30, None) == INVALID
+    assert L.csa2_build_cache(fake, 32, 2, fake, fake, fake, fake, fake, fake, 1024, None) == WS
     assert L.csa2_check_bounded_wait(0, None) == INVALID                                 # limit out of range
     assert L.csa2_check_bounded_wait(2_000_001, None) == INVALID
     assert L.csa2_get_device_status(None, None) == INVALID
@@ -91,5 +102,11 @@ def test_workspace_sizes(lib):
     # per row: the 2,048 maxima of 512-item supergroups (candidates stay on chip)
     assert lib.csa2_workspace_size(lib.CSA2_OP_TOPK, 8, 1 << 20, 512) == 8 * 2048 * 4
     assert lib.csa2_workspace_size(lib.CSA2_OP_SPARSE_ATTN, 8192, 640) == 0      # no split for big batches
+    # the cache build's scratch: one chunk of at most 32,768 entries (keys; pooled latents for m = 2)
+    assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 1 << 20, 2) == 32768 * (128 + 512) * 2
+    assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 1 << 20, 1) == 32768 * 128 * 2
+    assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 64, 2) == 32 * (128 + 512) * 2
+    with pytest.raises(lib.CSA2Error):
+        lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 64, 3)
     with pytest.raises(lib.CSA2Error):
         lib.csa2_workspace_size(lib.CSA2_OP_SPARSE_ATTN, 8, 100)
