@@ -65,9 +65,9 @@ def parse():
     ap.add_argument("--entries", type=int, default=None,
                     help="shorten the workload's caches to this many entries per sequence (smaller device "
                          "footprint, e.g. for profiler captures); the workload name records it")
-    ap.add_argument("--only", choices=["mq", "layers"], default=None,
-                    help="run and print only one secondary workload: the multi-query decode (mq) or the "
-                         "20-layer decoder step (layers)")
+    ap.add_argument("--only", choices=["mq", "layers", "build"], default=None,
+                    help="run and print only one secondary workload: the multi-query decode (mq), the "
+                         "20-layer decoder step (layers) or the cache build of a 1M-token prompt (build)")
     return ap.parse_args()
 
 
@@ -586,6 +586,71 @@ def run_layers(args, rank, world, local_rank):
             "gpu_launches": args.steps * (4 + n_re * 2 + len(DECODER_LAYERS) * 2)}
 
 
+def run_build(args, rank, world, local_rank):
+    """The cache a 1,048,576-token encoder prompt leaves (m = 2: 524,288 entries):
+    csa2_build_cache from bf16 tokens and fp32 gate logits in HBM to the main-cache
+    records and the indexer keys' records; and the key projection alone
+    (csa2_index_key_proj over the pooled latents), the tensor-core kernel of the
+    build."""
+    import torch
+    import compressed_sparse_attention_index_gb300 as C
+    from compressed_sparse_attention_index_gb300 import ranks
+    n_tok, m = 1 << 20, 2
+    n_e = n_tok // m
+    g = torch.Generator(device="cuda").manual_seed(91 + rank)
+    toks = torch.randn((n_tok, 512), generator=g, device="cuda").to(torch.bfloat16)
+    z = torch.randn((n_tok, 512), generator=g, device="cuda")
+    w = (torch.randn((128, 512), generator=g, device="cuda") / 512 ** 0.5).to(torch.bfloat16)
+    kv = torch.empty((n_e, 288), dtype=torch.uint8, device="cuda")
+    nib = torch.empty((n_e, 64), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((n_e, 4), dtype=torch.uint8, device="cuda")
+    wsb = C.csa2_workspace_size(C.CSA2_OP_BUILD_CACHE, 0, n_tok, m)
+    ws = torch.empty((wsb,), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        C.csa2_build_cache(toks, n_tok, m, z, w, kv, nib, sc, ws, wsb, stream)
+    steps = max(3, min(args.steps, 20))
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert C.csa2_get_device_status() == 0
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = ranks.max_over_ranks(t0.elapsed_time(t1), device="cuda") / steps
+    # the projection alone over the prompt's pooled latents (here: its first n_e tokens)
+    lat = toks[:n_e]
+    keys = torch.empty((n_e, 128), dtype=torch.bfloat16, device="cuda")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        C.csa2_index_key_proj(lat, n_e, w, keys, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    p_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    assert C.csa2_get_device_status() == 0
+    if rank != 0:
+        return None
+    peak, peak_kind = peaks()
+    io_bytes = n_tok * (512 * 2 + 512 * 4) + n_e * (288 + 68)          # tokens + gates in, records out
+    p_bytes = n_e * (512 * 2 + 128 * 2)                                  # latents in, bf16 keys out
+    return {"metric": "cache-build prompt tokens/s (1,048,576-token encoder prompt, m = 2: pooling, main-cache "
+                      "records, 512 -> 128 key projection, key records)",
+            "value": n_tok * world / (ms / 1e3), "unit": "prompt-tokens/s", "ms_per_step": ms, "steps": steps,
+            "warmup": args.warmup, "io_bytes_per_step": io_bytes,
+            "path_hbm_gbs": io_bytes / (ms / 1e3) / 1e9, "path_frac_of_measured_peak": io_bytes / (ms / 1e3) / 1e9 / peak,
+            "roofline": {"kernel": "proj_keys (csa2_index_key_proj)", "bound": "hbm",
+                         "achieved": p_bytes / (p_ms / 1e3) / 1e9, "peak": peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": p_bytes / (p_ms / 1e3) / 1e9 / peak, "traffic": None,
+                         "algorithmic_bytes_per_launch": p_bytes, "avg_launch_ms": p_ms,
+                         "tflops": 2.0 * n_e * 128 * 512 / (p_ms / 1e3) / 1e12},
+            "gpu_launches": steps * 3 * ((n_e + 131071) // 131072)}
+
+
 def run_reference(args):
     from gen.workloads import CONFIGS
     import oracle
@@ -628,7 +693,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     if args.only is not None:
-        r = (run_mq if args.only == "mq" else run_layers)(args, rank, world, local_rank)
+        r = {"mq": run_mq, "layers": run_layers, "build": run_build}[args.only](args, rank, world, local_rank)
         if rank == 0:
             print(json.dumps(r))
         if world > 1:
@@ -664,6 +729,10 @@ def main():
         r = run_layers(a2, rank, world, local_rank)
         if rank == 0:
             extra["decoder_step_N1M_B8_zipf_20layers"] = r
+        torch.cuda.empty_cache()
+        r = run_build(a2, rank, world, local_rank)
+        if rank == 0:
+            extra["cache_build_prompt_1M_m2"] = r
         if rank == 0:
             line["secondary"] = extra
     if rank == 0:

@@ -171,7 +171,7 @@ static HostStage host_stage(int n_q) {
 
 // csa2_build_cache's workspace for one chunk of entries: the keys (bf16
 // [chunk][128]) and, for m = 2, the pooled latents (bf16 [chunk][512]).
-constexpr int64_t kBuildChunk = 32768;
+constexpr int64_t kBuildChunk = 131072;
 static size_t build_cache_workspace_bytes(int64_t n_tokens, int m) {
   const int64_t entries = n_tokens / m;
   const int64_t c = entries < kBuildChunk ? entries : kBuildChunk;

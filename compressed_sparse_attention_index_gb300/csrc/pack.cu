@@ -16,6 +16,8 @@
 //
 // All three kernels are HBM-bound streams: one warp per row (KV, SWA) or eight
 // lanes per row (IDX), 16-B vector loads of the bf16 row, 8- or 16-B stores.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "launch.cuh"
 
@@ -82,7 +84,17 @@ __global__ void __launch_bounds__(256) pack_kv_kernel(const uint16_t *__restrict
 #pragma unroll
     for (int i = 0; i < 8; i++) { x[2 * i] = bf16_lo(w[i]); x[2 * i + 1] = bf16_hi(w[i]); }
   } else {
-    // gated pooling of tokens 2*row and 2*row+1, in fp64, rounded once to bf16
+    // gated pooling of tokens 2*row and 2*row+1, rounded once to bf16: the
+    // exact value's rounding.  With the larger logit's token t_m, the other
+    // t_o, e = exp(-|z_a - z_b|) and s = e / (1 + e), the value is
+    // t_m + (t_o - t_m) s.  fp32 first, one FMA: expf is within 2 ulps, the
+    // argument, 1 + e, the quotient and t_o - t_m round once each, so its error
+    // is below |t_o - t_m| (1.75 s 2^-22 + 0.28 2^-24) + 2^-24 |v| (s |dz| <=
+    // 0.28); with d twice that or more, when v - d and v + d round to the same
+    // bf16 so does the exact value.  The rest (about one element in a
+    // thousand, near a rounding boundary) are recomputed in fp64 afterwards as
+    // (e_a t_a + e_b t_b) / (e_a + e_b), all lanes of the warp together, each
+    // taking its next such element.
     const uint4 *p0 = reinterpret_cast<const uint4 *>(src + (2 * row) * kDim + lane * 16);
     const uint4 *p1 = reinterpret_cast<const uint4 *>(src + (2 * row + 1) * kDim + lane * 16);
     const float *z0 = gate + (2 * row) * kDim + lane * 16;
@@ -90,15 +102,48 @@ __global__ void __launch_bounds__(256) pack_kv_kernel(const uint16_t *__restrict
     uint4 a0 = __ldg(p0), b0 = __ldg(p0 + 1), a1 = __ldg(p1), b1 = __ldg(p1 + 1);
     uint32_t w0[8] = {a0.x, a0.y, a0.z, a0.w, b0.x, b0.y, b0.z, b0.w};
     uint32_t w1[8] = {a1.x, a1.y, a1.z, a1.w, b1.x, b1.y, b1.z, b1.w};
+    float za4[16], zb4[16];                           // the logits, 16-B loads
+#pragma unroll
+    for (int v = 0; v < 4; v++) {
+      const float4 ga = __ldg(reinterpret_cast<const float4 *>(z0) + v);
+      const float4 gb = __ldg(reinterpret_cast<const float4 *>(z1) + v);
+      za4[4 * v] = ga.x; za4[4 * v + 1] = ga.y; za4[4 * v + 2] = ga.z; za4[4 * v + 3] = ga.w;
+      zb4[4 * v] = gb.x; zb4[4 * v + 1] = gb.y; zb4[4 * v + 2] = gb.z; zb4[4 * v + 3] = gb.w;
+    }
+    float t0v[16], t1v[16];
+    uint32_t redo = 0u;                               // channels this lane recomputes in fp64
 #pragma unroll
     for (int i = 0; i < 16; i++) {
-      float t0 = (i & 1) ? bf16_hi(w0[i >> 1]) : bf16_lo(w0[i >> 1]);
-      float t1 = (i & 1) ? bf16_hi(w1[i >> 1]) : bf16_lo(w1[i >> 1]);
-      double za = (double)__ldg(z0 + i), zb = (double)__ldg(z1 + i);
-      double mz = za > zb ? za : zb;
-      double ea = exp(za - mz), eb = exp(zb - mz);
-      double v = (ea * (double)t0 + eb * (double)t1) / (ea + eb);
-      x[i] = __uint_as_float(bf16_from_f64(v) << 16);
+      t0v[i] = (i & 1) ? bf16_hi(w0[i >> 1]) : bf16_lo(w0[i >> 1]);
+      t1v[i] = (i & 1) ? bf16_hi(w1[i >> 1]) : bf16_lo(w1[i >> 1]);
+      const float fa = za4[i], fb = zb4[i];
+      const float tm = fa >= fb ? t0v[i] : t1v[i], to = fa >= fb ? t1v[i] : t0v[i];
+      const float e = expf(-fabsf(fa - fb));
+      const float sg = e / (1.0f + e);
+      const float dl = to - tm;
+      const float vf = fmaf(dl, sg, tm);
+      const float d = fabsf(dl) * fmaf(sg, 0x1p-20f, 0x1p-24f) + fabsf(vf) * 0x1p-23f;
+      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(vf - d));
+      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(vf + d));
+      x[i] = __uint_as_float(lo << 16);
+      redo |= (lo != hi ? 1u : 0u) << i;
+    }
+    while (__any_sync(0xFFFFFFFFu, redo != 0u)) {
+      if (redo != 0u) {
+        const int c = __ffs(redo) - 1;
+        redo &= redo - 1u;
+        float t0 = 0.f, t1 = 0.f, fa = 0.f, fb = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; i++)
+          if (i == c) { t0 = t0v[i]; t1 = t1v[i]; fa = za4[i]; fb = zb4[i]; }
+        const double za = (double)fa, zb = (double)fb;
+        const double e = exp(-fabs(za - zb));
+        const double v = za >= zb ? ((double)t0 + e * (double)t1) / (1.0 + e) : (e * (double)t0 + (double)t1) / (e + 1.0);
+        const float xv = __uint_as_float(bf16_from_f64(v) << 16);
+#pragma unroll
+        for (int i = 0; i < 16; i++)
+          if (i == c) x[i] = xv;
+      }
     }
     if (pooled != nullptr) {
       uint32_t b[8];

@@ -365,8 +365,8 @@ csa2_status csa2_index_key_proj(const void *latent, int64_t rows, const void *w_
  * (csa2_index_key_proj) and the key's two-plane 68-B record -- the same bytes
  * as csa2_fp4_pack(CSA2_KV_NVFP4, m), csa2_index_key_proj and
  * csa2_fp4_pack(CSA2_IDX_MXFP4) on the pooled latents.  Prompts of any length
- * (1,048,576 tokens and more) are built in chunks of 32,768 entries, so the
- * scratch stays bounded.
+ * (1,048,576 tokens and more) are built in chunks of 131,072 entries, so the
+ * scratch stays bounded (168 MB for m = 2, 34 MB for m = 1).
  *   tokens       (device) bf16 [n_tokens][512], 16-B aligned.
  *   n_tokens     a multiple of 8 m (so that chunks start on 8-row boundaries
  *                of the key plane).

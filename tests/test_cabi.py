@@ -102,9 +102,9 @@ def test_workspace_sizes(lib):
     # per row: the 2,048 maxima of 512-item supergroups (candidates stay on chip)
     assert lib.csa2_workspace_size(lib.CSA2_OP_TOPK, 8, 1 << 20, 512) == 8 * 2048 * 4
     assert lib.csa2_workspace_size(lib.CSA2_OP_SPARSE_ATTN, 8192, 640) == 0      # no split for big batches
-    # the cache build's scratch: one chunk of at most 32,768 entries (keys; pooled latents for m = 2)
-    assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 1 << 20, 2) == 32768 * (128 + 512) * 2
-    assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 1 << 20, 1) == 32768 * 128 * 2
+    # the cache build's scratch: one chunk of at most 131,072 entries (keys; pooled latents for m = 2)
+    assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 1 << 20, 2) == 131072 * (128 + 512) * 2
+    assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 1 << 20, 1) == 131072 * 128 * 2
     assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 64, 2) == 32 * (128 + 512) * 2
     with pytest.raises(lib.CSA2Error):
         lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 64, 3)

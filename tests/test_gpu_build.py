@@ -95,11 +95,11 @@ def _build(lib, toks, z, w, m):
 
 @pytest.mark.parametrize("m", [1, 2])
 def test_build_cache_parity(lib, oracle_lib, m):
-    """A prompt of 2 x 40,008 / 40,008 tokens: two chunks of entries, the second
-    ragged.  Main-cache records bit for bit against the oracle; keys within one
+    """A prompt of 2 x 140,008 / 140,008 tokens: two chunks of entries, the
+    second ragged.  Main-cache records bit for bit against the oracle; keys within one
     bf16 step of the oracle's, and their records exactly the packing of the
     keys this GPU computes for the same latents."""
-    n_e = 40_008
+    n_e = 140_008
     n_tok = n_e * m
     toks = G.normal_rows_bf16(83, 1, 0, np.arange(n_tok), 512)
     z = G.gate_logits_f32(83, 0, np.arange(n_tok)) if m == 2 else None
@@ -115,7 +115,7 @@ def test_build_cache_parity(lib, oracle_lib, m):
 
 
 def test_build_cache_of_a_million_token_prompt_sampled(lib, oracle_lib):
-    """A 1,048,576-token encoder prompt (m = 2: 524,288 entries, 16 chunks) on
+    """A 1,048,576-token encoder prompt (m = 2: 524,288 entries, 4 chunks) on
     the device; entries sampled across the chunks and at both ends checked
     against the oracle's composition of their own tokens."""
     n_tok = 1 << 20
@@ -131,7 +131,7 @@ def test_build_cache_of_a_million_token_prompt_sampled(lib, oracle_lib):
     ws = torch.empty((wsb,), dtype=torch.uint8, device="cuda")
     lib.csa2_build_cache(toks, n_tok, 2, z, _dev(w), kv, nib, sc, ws, wsb)
     assert lib.csa2_get_device_status() == 0
-    ents = np.unique(np.concatenate([[0, 1, 7, 8, 32767, 32768, 32775, n_e - 8, n_e - 1],
+    ents = np.unique(np.concatenate([[0, 1, 7, 8, 131071, 131072, 131079, 262144, n_e - 8, n_e - 1],
                                      np.random.default_rng(84).integers(0, n_e, 48)]))
     # whole 8-row groups of the key plane, so that the swizzle undoes exactly
     groups = np.unique(ents // 8)
