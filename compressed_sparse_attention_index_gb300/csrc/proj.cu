@@ -10,13 +10,13 @@
 // GPU's FLOP/byte ridge: it is bound by HBM.  Persistent CTAs, one per SM,
 // take tiles of 128 entries (the MMA's M); the 128 x 512 weights (128 KB) stay
 // in shared memory as the B operand for the whole kernel, and a tile's
-// latents stream through a 4-stage ring of 64-wide K slices (16 KB: 128 rows
+// latents stream through a 6-stage ring of 64-wide K slices (16 KB: 128 rows
 // x 128 B), each slice four MMAs of K = 16 into the tile's TMEM accumulator
 // (128 lanes x 128 columns, two accumulators so that the epilogue of one tile
 // overlaps the MMAs of the next).  Both operands are K-major with the 128-byte
 // swizzle: 8-row groups of 128-B rows, the 16-B chunk c of row r at c ^ (r & 7).
 // Roles (384 threads): warps 0-3 load the slices (warp p: rows 32p..32p+31,
-// one row per lane, 16-B asynchronous copies), lane 0 of warp 4 issues the
+// 16-B asynchronous copies, eight lanes per 128-B slice), lane 0 of warp 4 issues the
 // MMAs (warp 4 owns the tensor memory), warps 8-11 read the accumulator (one
 // row per thread), round to bf16 and store.  Every wait is bounded.
 #include <cuda_bf16.h>
@@ -30,7 +30,7 @@ namespace csa2 {
 constexpr int kPjRows = 128;                       // entries per tile (MMA M)
 constexpr int kPjIn = 512, kPjOut = 128;           // K, N
 constexpr int kPjAtoms = kPjIn / 64;               // 64-wide (128-B) K slices
-constexpr int kPjStages = 4;
+constexpr int kPjStages = 6;
 constexpr int kPjStageBytes = kPjRows * 128;       // 16 KB
 constexpr int kPjSmW = 0;                          // weights: [n/8][atom][n%8][128 B]  (128 KB)
 constexpr int kPjSmA = kPjOut * kPjIn * 2;         // slices: [stage][row/8][row%8][128 B]
@@ -89,18 +89,22 @@ __global__ void __launch_bounds__(kPjThreads, 1)
 
   if (warp < 4) {
     // ------------------------------------------------------------ loaders
+    // eight lanes per 128-B row slice, so that each instruction moves four
+    // whole slices (lane: row 4j + lane / 8 of the warp's 32, chunk lane % 8)
     uint32_t it = 0;
+    const int c = lane & 7;
     for (int64_t t = blockIdx.x; t < n_tiles && !abort_flag; t += gridDim.x) {
-      const int r = warp * 32 + lane;
-      const int64_t row = t * kPjRows + r;
-      const unsigned char *src = reinterpret_cast<const unsigned char *>(x + row * kPjIn);
       for (int a = 0; a < kPjAtoms; a++, it++) {
         const uint32_t s = it % kPjStages, ph = (it / kPjStages) & 1;
         if (!ptx::mbar_wait(&empty_bar[s], ph ^ 1)) { fail(); break; }
-        unsigned char *dst = sm + kPjSmA + s * kPjStageBytes + (r >> 3) * 1024;
-        if (row < rows) {
+        unsigned char *dst = sm + kPjSmA + s * kPjStageBytes;
 #pragma unroll
-          for (int c = 0; c < 8; c++) ptx::cp_async16(dst + pj_sw128(r & 7, c), src + a * 128 + c * 16);
+        for (int j = 0; j < 8; j++) {
+          const int r = warp * 32 + j * 4 + (lane >> 3);
+          const int64_t row = t * kPjRows + r;
+          if (row < rows)
+            ptx::cp_async16(dst + (r >> 3) * 1024 + pj_sw128(r & 7, c),
+                            reinterpret_cast<const unsigned char *>(x + row * kPjIn) + a * 128 + c * 16);
         }
         ptx::cp_async_arrive_noinc(&full_bar[s]);
       }
