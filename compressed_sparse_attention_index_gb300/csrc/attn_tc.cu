@@ -213,6 +213,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   }
   const int seq = __ldg(A.q_seq + qi);
   const int swa_cnt = __ldg(A.swa_cnt + qi), swa_first = __ldg(A.swa_first + qi);
+  // the position is needed only by the read-out: loaded now, kept in shared
+  // memory once Q is staged
+  __shared__ int pos_sh;
+  const int pos0 = t == 0 ? __ldg(A.pos + qi) : 0;
   const bool bad = seq < 0 || seq >= A.n_seq || swa_cnt < 0 || swa_cnt > kSwa || swa_cnt > A.swa_cap ||
                    (swa_cnt > 0 && (swa_first < 0 || swa_first >= A.swa_cap));
   if (bad && t == 0 && split == 0 && h0 == 0) record_error(A.status, CSA2_ERR_BOUNDS);
@@ -310,6 +314,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   else if (t < 16)
     *reinterpret_cast<uint4 *>(sm + kSmOnes16 + (t - 8) * 16) =
         make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+  if (t == 0) pos_sh = pos0;
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
@@ -329,6 +334,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   const int warm = A.warm && !waited && c0 < c1 && c0 * kTcChunk < A.n_sel ? 1 : 0;
   uint32_t hnc = 0;                                  // handoff: candidates + 1, or kHandFallback
   bool got_sel = false;
+  // A CTA with several chunks of selected entries reads the records of the
+  // next one into registers while the current one runs its MMAs and softmax
+  // (pre_c: the chunk whose records rec_sc / rec_nb hold; the gather of a
+  // chunk without them loads them itself)
+  int pre_c = -1, pre_j = -1;
+  uint32_t rec_sc[4];                                // this thread's half-record: 16 E4M3 scales
+  uint4 rec_nb[8];                                   //   and 256 E2M1 latents
+  auto load_rec = [&](int j) {
+    const int half = t & 1;
+    const uint8_t *rec = A.kv + ((int64_t)seq * A.n_max + j) * kKvBytes;
+#pragma unroll
+    for (int k = 0; k < 4; k++) rec_sc[k] = __ldg(reinterpret_cast<const uint32_t *>(rec + 256 + half * 16 + 4 * k));
+#pragma unroll
+    for (int v = 0; v < 8; v++) rec_nb[v] = __ldg(reinterpret_cast<const uint4 *>(rec + half * 128 + v * 16));
+  };
   for (int c = c0, wp = warm; c < c1; c += 1 - wp, wp = 0) {
     const bool sel_chunk = !wp && c * kTcChunk < A.n_sel;   // the chunk holds selected entries (or candidates)
     if (sel_chunk && !got_sel) {
@@ -416,19 +436,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
             hk = __ldcg(A.hcand + ((int64_t)qi * kHandCtas + p) * kHandSeg + (slot - hoff_sh[p]));
             j = (int)~(uint32_t)hk;
           }
+        } else if (pre_c == c) {
+          j = pre_j;
         } else if (slot < A.sel_stride) {
           j = __ldcg(A.sel + (int64_t)qi * A.sel_stride + slot);
         }
         if (j >= 0 && (int64_t)j < A.n_max) {
           ok = 1;
-          const uint8_t *rec = A.kv + ((int64_t)seq * A.n_max + j) * kKvBytes;
-          const uint32_t sc4[4] = {__ldg(reinterpret_cast<const uint32_t *>(rec + 256 + half * 16)),
-                                   __ldg(reinterpret_cast<const uint32_t *>(rec + 256 + half * 16 + 4)),
-                                   __ldg(reinterpret_cast<const uint32_t *>(rec + 256 + half * 16 + 8)),
-                                   __ldg(reinterpret_cast<const uint32_t *>(rec + 256 + half * 16 + 12))};
-          uint4 nbv[8];
-#pragma unroll
-          for (int v = 0; v < 8; v++) nbv[v] = __ldg(reinterpret_cast<const uint4 *>(rec + half * 128 + v * 16));
+          if (pre_c != c) load_rec(j);
+          const uint32_t(&sc4)[4] = rec_sc;
+          const uint4(&nbv)[8] = rec_nb;
           if (f16c) {
             // f16: E2M1 pairs and E4M3 scale pairs by the hardware converter
             uint32_t sh[8];                           // the half-row's 16 scales as f16x2 pairs
@@ -538,6 +555,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
         ptx::tc_mma_bf16(tmem + col, ad, bd, id_qk, k2 > 0 ? 1u : 0u);
       }
       ptx::tc_commit(&bar_s);
+    }
+    // the next chunk's records, if it holds selected entries only (its smem
+    // stores wait for this chunk's PV)
+    if (!HAND && got_sel && !wp && c + 1 < c1 && chunk_f16(c + 1)) {
+      const int slot = (c + 1) * kTcChunk + (t >> 1);
+      pre_c = c + 1;
+      pre_j = slot < A.sel_stride ? __ldcg(A.sel + (int64_t)qi * A.sel_stride + slot) : -1;
+      if (pre_j >= 0 && (int64_t)pre_j < A.n_max) load_rec(pre_j);
     }
     // ---------------------------------------------------------- handoff mask
     // while S is computed: candidates below the smallest selected key drop out
@@ -730,7 +755,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     // (always so with the handoff: a query's candidates take five chunks)
     const bool one_split = !HAND && A.nsplit == 1;
     const int quarter = warp & 3;
-    const int pos = __ldg(A.pos + qi);
+    const int pos = pos_sh;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     for (int blk = warp >> 2; blk < 4; blk += 2) {
       const int d = blk * 128 + quarter * 32 + lane;   // TMEM lane = dim within block
@@ -752,7 +777,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
           for (int i = 0; i < 32; i++) {
             const int h = h0 + half * 32 + i;
             const float l = __uint_as_float(lr[i]);
-            float x = l > 0.f ? __uint_as_float(r[i]) / l : 0.f;
+            float x = l > 0.f ? __fdividef(__uint_as_float(r[i]), l) : 0.f;   // (within 2 ulp)
             if (d >= kRopeOff) {
               // rotate the pair (a, b) = (o[d & ~1], o[d | 1]) by -pos:
               // a' = a c + b s,  b' = -a s + b c; the partner lives in the next lane

@@ -18,12 +18,13 @@
 // so the design keeps those per byte low: big units, one commit per unit, and
 // two MMA issuers.  Warp roles (480 threads):
 //   warp 0      producer: one bulk copy (cp.async.bulk) of the unit's 32 KB of
-//               nibbles and one of its 2 KB of E8M0 scales (pool mode: 16 of
-//               the 64 gathered 8-entry blocks of 512 B + 32 B, by 16-B
-//               asynchronous copies; warps 12..14 gather the other 48); with the first unit
-//               of each run of one query, its 2 KB of nibbles and 128 B of
-//               scales into the next of six query slots (so a CTA may switch
-//               query on every unit without a stall).  The nibble planes are stored
+//               nibbles, and its 2 KB of E8M0 scales by the lanes' 16-B
+//               asynchronous copies (pool mode: 16 of the 64 gathered 8-entry
+//               blocks of 512 B + 32 B, by 16-B asynchronous copies; warps
+//               12..14 gather the other 48); with the first unit of each run
+//               of one query, its 2 KB of nibbles and 128 B of scales (lanes'
+//               copies too) into the next of six query slots (so a CTA may
+//               switch query on every unit without a stall).  The nibble planes are stored
 //               64B-swizzled, so a plain contiguous copy lands in the layout the
 //               MMA reads;
 //   warp 2      scale-factor warp: rearranges the unit's key scales in shared
@@ -36,8 +37,9 @@
 //   warps 3..10 epilogue, two groups of four warps taking alternate units: one
 //               TMEM lane (= one entry of each sub-tile) per thread, 32 columns
 //               (= heads) per sub-tile, ReLU + weighted sum, coalesced store.
-// The producer walks the CTA's units (a fixed stride over all of them) and
-// hands each to the other roles through a small shared-memory ring; the
+// The producer walks the CTA's units (a fixed stride over all of them, or
+// over runs of consecutive units) and hands each to the other roles through
+// a small shared-memory ring; the
 // per-query sequence id / visible length are cached.  Every wait is bounded (CSA2_ERR_TIMEOUT
 // instead of a hang).
 #include "common.cuh"
@@ -116,6 +118,7 @@ struct ScoreTcArgs {
   // units, tagged with call_id in its upper 32 bits (see the producer)
   unsigned long long *steal;
   uint32_t call_id;
+  int run;          // Full mode without claims: consecutive units a CTA takes at a time (set by the launch)
 };
 
 // Full mode inside csa2_decode: a CTA takes the units T = blockIdx.x + k gridDim.x
@@ -125,18 +128,20 @@ struct ScoreTcArgs {
 // step; 32 x 64K, 27 rounds, +4.7 us: there a claimed unit is a fresh query
 // almost every time).
 constexpr int kStealRounds = 4;
+constexpr int kMaxRun = 16;
 constexpr uint32_t kStealMinRounds = 32;
 
 // Work units are T = (query, unit) in query-major order, T < n_q * units_per_q;
-// a CTA takes T = blockIdx.x, blockIdx.x + gridDim.x, ...  The producer walks
-// that sequence, skips units past a query's visible length, and publishes the
-// unit of each of its iterations `it` in a ring of shared-memory words
-// (it << 32 | T; T = kDone after the last unit); every other role reads the
-// ring in iteration order instead of walking the sequence itself.  A slot is
+// a CTA takes T = blockIdx.x, blockIdx.x + gridDim.x, ... (or runs of P.run
+// consecutive units at a stride of gridDim.x runs; inside csa2_decode the last
+// rounds may be claimed, see kStealRounds).  The producer walks that sequence,
+// skips units past a query's visible length, and publishes the unit of each
+// of its iterations `it` in a ring of shared-memory words (it << 32 | T;
+// T = kDone after the last unit); every other role reads the ring in
+// iteration order instead of walking the sequence itself.  A slot is
 // rewritten 16 iterations later, which needs the MMA of iteration it + 10
-// done, so every role has read it by then.  (Units claimed from a global
-// counter, so that faster SMs take more, measured slower: the counter's
-// atomics queue up.)
+// done, so every role has read it by then.  (Claiming every unit from a
+// global counter measured slower: its atomics queue up.)
 constexpr int kRing = 16;
 constexpr uint32_t kDone = 0xFFFFFFFFu;
 
@@ -378,13 +383,26 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       }
       return __shfl_sync(0xFFFFFFFFu, idx, 0);
     };
+    // Full mode without claims: the CTA takes runs of P.run consecutive units
+    // at a stride of gridDim.x runs, so that where queries have few units
+    // each (many short sequences, or a prefill's queries) a new query's data
+    // and bookkeeping come once per run instead of on nearly every unit (the
+    // launch picks the run length, never more units for the busiest CTA)
+    const uint32_t run = !POOL && !steal && P.run > 1 ? (uint32_t)P.run : 1u;
+    uint32_t grp = blockIdx.x, rin = 0;            // the current unit: grp * run + rin
     // the unit after Tc in this CTA's sequence (total_units: none left)
     auto advance = [&](uint32_t Tc) -> uint32_t {
+      if (run > 1) {
+        if (++rin < run && Tc + 1 < total_units) return Tc + 1;
+        rin = 0;
+        grp += gridDim.x;
+        return (uint64_t)grp * run < total_units ? grp * run : total_units;
+      }
       if (!steal || Tc + gridDim.x < s_static) return Tc + gridDim.x;
       const uint32_t i = claim_next();
       return i < total_units - s_static ? s_static + i : total_units;
     };
-    uint32_t T = blockIdx.x;
+    uint32_t T = (uint64_t)blockIdx.x * run < total_units ? blockIdx.x * run : total_units;
     if (steal && T >= s_static) {
       const uint32_t i = claim_next();
       T = i < total_units - s_static ? s_static + i : total_units;
@@ -423,31 +441,47 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       }
       unsigned char *st = smem + s * kScStageBytes;
       // a new run of units of one query: its data travel with this unit
-      const uint32_t qbytes = fresh ? 2048 + 128 : 0;
       unsigned char *qd = qslots + qs.slot * kScQBytes;
-      auto load_query = [&]() {
-        ptx::bulk_load(qd + kQOffB, P.q_nib + (int64_t)sc.q * kIdxHeads * 64, 2048, &full_bar[s]);
-        ptx::bulk_load(qd + kQOffSFB, P.q_scale + (int64_t)sc.q * kIdxHeads * 4, 128, &full_bar[s]);
-      };
       const int64_t row0 = (int64_t)sc.seq * P.n_max;
       if (!POOL) {
+        // A new query's 2 KB of nibbles and 128 B of scales, and the unit's
+        // key scales, go as 16-B asynchronous copies of the warp's lanes, each
+        // lane counted into the stage's barrier (before the expected bytes of
+        // the nibbles' bulk copy), not as more bulk copies: the bulk-copy unit
+        // spends a fixed time per instruction (measured: -1.5 us per step at
+        // 32 x 64K, where the query changes on nearly every unit).
+        // Sub-tiles that start before n_vis end within n_max (n_max % 128 == 0).
+        const int left = sc.nv - cur_u * kUnit;
+        const int nsub = left >= kUnit ? kSub : (left + 127) >> 7;
+        const int64_t r0 = row0 + (int64_t)cur_u * kUnit;
+        if (fresh) {
+          const unsigned char *qn = P.q_nib + (int64_t)sc.q * kIdxHeads * 64;
+#pragma unroll
+          for (int k = 0; k < 4; k++) ptx::cp_async16(qd + kQOffB + (k * 32 + lane) * 16, qn + (k * 32 + lane) * 16);
+          if (lane < 8) ptx::cp_async16(qd + kQOffSFB + lane * 16, P.q_scale + (int64_t)sc.q * kIdxHeads * 4 + lane * 16);
+        }
+        // the unit's key scales (nsub x 512 B) the same way
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          if (k * 32 + lane < nsub * 32)
+            ptx::cp_async16(st + kOffSFA + (k * 32 + lane) * 16, P.key_scale + r0 * 4 + (k * 32 + lane) * 16);
+        ptx::cp_async_arrive(&full_bar[s]);
+        __syncwarp();
         if (lane == 0) {
-          // sub-tiles that start before n_vis end within n_max (n_max % 128 == 0)
-          const int left = sc.nv - cur_u * kUnit;
-          const int nsub = left >= kUnit ? kSub : (left + 127) >> 7;
-          ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)nsub * (8192 + 512) + qbytes);
-          if (fresh) load_query();
-          const int64_t r0 = row0 + (int64_t)cur_u * kUnit;
+          ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)nsub * 8192);
           ptx::bulk_load_hint(st + kOffA, P.key_nib + r0 * 64, (uint32_t)nsub * 8192, &full_bar[s], policy);
-          ptx::bulk_load(st + kOffSFA, P.key_scale + r0 * 4, (uint32_t)nsub * 512, &full_bar[s]);
         }
       } else {
         // pool: this warp gathers blocks 0..15 of the unit, warps 12..14 the
-        // rest (see PoolGather); lane 0 also brings the query data, if any
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&full_bar[s], qbytes);
-          if (fresh) load_query();
+        // rest (see PoolGather); its lanes also bring the query data, if any,
+        // as asynchronous copies that the gather's arrivals cover
+        if (fresh) {
+          const unsigned char *qn = P.q_nib + (int64_t)sc.q * kIdxHeads * 64;
+#pragma unroll
+          for (int k = 0; k < 4; k++) ptx::cp_async16(qd + kQOffB + (k * 32 + lane) * 16, qn + (k * 32 + lane) * 16);
+          if (lane < 8) ptx::cp_async16(qd + kQOffSFB + lane * 16, P.q_scale + (int64_t)sc.q * kIdxHeads * 4 + lane * 16);
         }
+        if (lane == 0) ptx::mbar_arrive(&full_bar[s]);
         pg.gather(P, 0, T, row0, st, &full_bar[s], total_units);
         if (T + gridDim.x < total_units) sc.prefetch(P, (int)((T + gridDim.x) / (uint32_t)P.units_per_q));
       }
@@ -520,9 +554,10 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         if ((it & 1) != par) continue;
         const uint32_t s = it % kScStages, r = it / kScStages, a = it % kScAcc, ra = it / kScAcc;
         if (!ptx::mbar_wait(&sf_bar[s], r & 1) || !ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) { fail(); break; }
-        // pool mode: the stage was filled by ordinary asynchronous copies, which
-        // the MMA (async proxy) reads only after a proxy fence
-        if (POOL) ptx::fence_proxy_async_smem();
+        // the query data (and, in pool mode, the stage) came by ordinary
+        // asynchronous copies, which the MMA (async proxy) reads only after a
+        // proxy fence
+        ptx::fence_proxy_async_smem();
         ptx::tc_fence_after();
         const uint32_t sa = ptx::smem_u32(smem + s * kScStageBytes + kOffA);
         const uint64_t bd = ptx::smem_desc(ptx::smem_u32(qslots + qs.slot * kScQBytes + kQOffB), 16, 512, 4);
@@ -676,7 +711,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       for (int i = max(0, armed_sh - kScStages); i < armed_sh; i++)
         ptx::mbar_wait(&full_bar[i % kScStages], (uint32_t)(i / kScStages) & 1);
     }
-    if (POOL && (warp == 0 || warp >= kScGather0)) asm volatile("cp.async.wait_all;" ::: "memory");
+    if (warp == 0 || (POOL && warp >= kScGather0)) asm volatile("cp.async.wait_all;" ::: "memory");
     if (lane == 0 && (warp == 1 || warp == 2 || warp == kScMmaWarp2)) ptx::tc_commit(&drain_bar);
     ptx::mbar_wait(&drain_bar, 0);
   }
@@ -1073,6 +1108,21 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
   if (e != cudaSuccess) return e;
   const int n_sm = device_sm_count(dev);
   const int64_t grid = total_units < n_sm ? total_units : n_sm;
+  // runs of consecutive units (Full mode without claims): the longest run,
+  // up to kMaxRun, that leaves the busiest CTA no more units than a stride of
+  // single units would
+  P.run = 1;
+  const bool steal = pool == nullptr && P.steal != nullptr && total_units >= (int64_t)kStealMinRounds * grid;
+  if (pool == nullptr && !steal && grid > 0) {
+    const int64_t most = (total_units + grid - 1) / grid;
+    for (int r = kMaxRun; r > 1; r--) {
+      const int64_t groups = (total_units + r - 1) / r;
+      if ((groups + grid - 1) / grid * r <= most) {
+        P.run = r;
+        break;
+      }
+    }
+  }
   const dim3 g((unsigned)grid), b(kScThreads);
   if (pool != nullptr) return launch_pdl(index_score_tc_kernel<true, 0>, g, b, smem, st, 1u, P);
   if (P.smax_mode == 3) return launch_pdl(index_score_tc_kernel<false, 3>, g, b, smem, st, 1u, P);
