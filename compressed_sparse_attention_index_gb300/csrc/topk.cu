@@ -661,11 +661,21 @@ __device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t
 }
 
 // ---------------------------------------------------------------- direct path
+// Shared memory of the direct path for rows of up to `cap` items (a multiple
+// of 4, <= kDirectCap): keys [cap] | sel [kMaxK] | 32 warp histograms [32][256]
+// | score halves sk [max(min(cap, kCandCap), 4096)] (rows of n <= cap keys, or
+// their group maxima, or the candidates above their threshold).  Short rows
+// (a prefill's) so take less of it, and two CTAs share an SM.
+__host__ __device__ constexpr int direct_sk_cap(int cap) { return (cap < kCandCap ? cap : kCandCap) > 4096 ? (cap < kCandCap ? cap : kCandCap) : 4096; }
+__host__ __device__ constexpr size_t direct_smem_bytes(int cap) {
+  return (size_t)cap * 8 + (size_t)kMaxK * 4 + 32 * 256 * 4 + (size_t)direct_sk_cap(cap) * 4;
+}
+
 __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, int k, int32_t *__restrict__ out,
-                                                                    int *status) {
+                                                                    int *status, int cap) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  uint64_t *keys = reinterpret_cast<uint64_t *>(smem_raw);                       // [kDirectCap]
-  int32_t *sel = reinterpret_cast<int32_t *>(keys + kDirectCap);                 // [kMaxK]
+  uint64_t *keys = reinterpret_cast<uint64_t *>(smem_raw);                       // [cap]
+  int32_t *sel = reinterpret_cast<int32_t *>(keys + cap);                        // [kMaxK]
   __shared__ SelectShared sh;
   sh.whist = reinterpret_cast<uint32_t *>(sel + kMaxK);                          // [32][256]
   __shared__ int n_keys;
@@ -688,20 +698,21 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
   __syncthreads();
   const int n = n_keys;
   int32_t *oq = out + (int64_t)q * k;
-  uint32_t *sk = sh.whist + 32 * 256;                                            // [kCandCap]
+  uint32_t *sk = sh.whist + 32 * 256;                                            // [direct_sk_cap(cap)]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  if (n <= 2048) {
+  // Larger sets: a threshold from the maxima of groups of gsz keys (the
+  // largest power of two <= 32 leaving >= 4k groups): at least k groups reach
+  // the k-th largest maximum T, so the top-k keys all have scores >= T; those
+  // candidates go to select_block.  Sets too small for groups of two (fewer
+  // than 8k keys) go to select_block whole, as do sets of <= 2,048.
+  int gsz = 32;
+  while (gsz > 1 && n / gsz < 4 * k) gsz >>= 1;
+  if (n <= 2048 || (gsz < 2 && n <= direct_sk_cap(cap))) {
     for (int i = threadIdx.x; i < ((n + 3) & ~3); i += blockDim.x) sk[i] = i < n ? (uint32_t)(keys[i] >> 32) : 0u;
     __syncthreads();
     select_block(keys, sk, n, k, oq, sel, sh.whist);
     return;
   }
-  // Larger sets: a threshold from the maxima of groups of gsz keys (the
-  // largest power of two <= 32 leaving >= 4k groups): at least k groups reach
-  // the k-th largest maximum T, so the top-k keys all have scores >= T; those
-  // candidates go to select_warp.
-  int gsz = 32;
-  while (gsz > 1 && n / gsz < 4 * k) gsz >>= 1;
   bool done = false;
   if (gsz >= 2) {
     __shared__ uint32_t T_sh;
@@ -1431,7 +1442,7 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
   S.kv_pf = nullptr;
   S.q_seq = nullptr;
   S.n_seq = 0;
-  const size_t dsm_direct = (size_t)kDirectCap * 8 + (size_t)kMaxK * 4 + 32 * 256 * 4 + (size_t)kCandCap * 4;
+  const size_t dsm_direct = direct_smem_bytes(kDirectCap);
   const size_t dsm_collect = collect_smem_bytes();
   const int dev = current_device();
   static std::atomic<int> attr_done[kMaxDevices];
@@ -1439,8 +1450,11 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
     return cudaFuncSetAttribute(topk_direct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm_direct);
   });
   if (ea != cudaSuccess) return ea;
-  if (S.n_items <= kDirectCap)
-    return launch_pdl(topk_direct_kernel, dim3(n_q), dim3(kTopkThreads), dsm_direct, st, 1u, S, k, out, status);
+  if (S.n_items <= kDirectCap) {
+    const int cap = (int)((S.n_items + 3) / 4 * 4);
+    return launch_pdl(topk_direct_kernel, dim3(n_q), dim3(kTopkThreads), direct_smem_bytes(cap), st, 1u, S, k, out,
+                      status, cap);
+  }
   const int64_t sgi = long_row_sgi(S.n_items, k);
   const LongRowWs W = long_row_ws(ws, n_q, S.n_items, k);
   const bool plain = pool == nullptr && block == 1;

@@ -105,6 +105,7 @@ def _run_topk(lib, s_rows, n_valid, k, block=1, pool=None, n_max=None):
 
 
 @pytest.mark.parametrize("n,levels,k", [(4096, 0, 512), (5000, 7, 512), (300, 3, 512), (16384, 0, 512),
+                                        (3000, 5, 512), (7000, 0, 1024),
                                         (100_000, 0, 512), (100_000, 50, 512), (1 << 20, 0, 512),
                                         (70_000, 0, 2048), (20_000, 1000, 1)])
 def test_topk_bit_exact(lib, oracle_lib, n, levels, k):
