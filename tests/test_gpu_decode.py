@@ -41,6 +41,24 @@ def test_index_score_full_parity(lib, oracle_lib, zipf):
         check_scores(s[qi, :1000], oracle_lib.full_scores(wl, qi))
 
 
+def test_index_score_runs_of_units_across_queries(lib, oracle_lib):
+    """More units than SMs and nothing claimed: each CTA takes runs of
+    consecutive units (here 40 queries x 10 units over at most 152 CTAs, runs
+    of 3 that cross from one query into the next), with ragged visible
+    lengths (the last unit of every query partly visible)."""
+    wl = small(n_seq=4, n_entries=5000, seed=207, q_per_seq=10)
+    dw = _dw(wl)
+    buf = _bufs(dw)
+    n_q = dw.q.shape[0]
+    lib.csa2_index_score(dw.key_nib, dw.key_scale, dw.n_max, 4, dw.q_nib, dw.q_scale, dw.w, dw.q_seq, dw.n_vis, n_q,
+                         None, buf.scores, dw.n_max)
+    s = buf.scores.cpu().numpy()
+    assert lib.csa2_get_device_status() == 0
+    nv = wl.n_vis()
+    for qi in range(n_q):
+        check_scores(s[qi, :nv[qi]], oracle_lib.full_scores(wl, qi))
+
+
 def test_index_score_pool_mode_gather(lib, oracle_lib):
     """Pool mode: each 512-entry unit is 64 gathered 8-entry blocks, moved by
     four warps of 16 blocks each.  Empty slots (-1) fall in every warp's share,
