@@ -49,24 +49,30 @@ struct TopkSrc {
 };
 
 // Key of item i of query q; false if the item is not valid.
-__device__ __forceinline__ bool item_key(const TopkSrc &S, int q, int64_t i, int nv, uint64_t &key, int *status) {
-  const float *row = S.scores + (int64_t)q * S.stride;
+// The key of item i from its score and (pool mode) its block id, already
+// loaded (pool mode or S.block == 1).
+__device__ __forceinline__ bool item_key_of(const TopkSrc &S, int64_t i, int nv, float score, int blk, uint64_t &key,
+                                            int *status) {
   if (S.pool != nullptr) {
-    const int blk = __ldg(S.pool + (int64_t)q * kPoolBlocks + (i >> 3));
     if (blk < 0) return false;
     const int64_t j = (int64_t)blk * kBlock + (i & 7);
     if (j >= nv) {
       if ((int64_t)blk * kBlock >= S.n_max) record_error(status, CSA2_ERR_BOUNDS);
       return false;
     }
-    key = ((uint64_t)order_key(__ldg(row + i)) << 32) | (uint32_t)(~(uint32_t)j);
+    key = ((uint64_t)order_key(score) << 32) | (uint32_t)(~(uint32_t)j);
     return true;
   }
-  if (S.block == 1) {
-    if (i >= nv) return false;
-    key = ((uint64_t)order_key(__ldg(row + i)) << 32) | (uint32_t)(~(uint32_t)i);
-    return true;
-  }
+  if (i >= nv) return false;
+  key = ((uint64_t)order_key(score) << 32) | (uint32_t)(~(uint32_t)i);
+  return true;
+}
+
+__device__ __forceinline__ bool item_key(const TopkSrc &S, int q, int64_t i, int nv, uint64_t &key, int *status) {
+  const float *row = S.scores + (int64_t)q * S.stride;
+  if (S.pool != nullptr || S.block == 1)
+    return item_key_of(S, i, nv, __ldg(row + i), S.pool != nullptr ? __ldg(S.pool + (int64_t)q * kPoolBlocks + (i >> 3)) : 0,
+                       key, status);
   const int64_t j0 = i * kBlock;
   if (j0 >= nv) return false;
   uint32_t m = 0;
@@ -685,15 +691,43 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
   const int nv = query_nv(S, q, status);
   if (threadIdx.x == 0) n_keys = 0;
   __syncthreads();
-  for (int64_t b0 = 0; b0 < S.n_items; b0 += blockDim.x) {   // uniform trip count: ballots see full warps
-    const int64_t i = b0 + threadIdx.x;
-    uint64_t key = 0;
-    const bool v = i < S.n_items && item_key(S, q, i, nv, key, status);
+  // the row's keys, compacted into shared memory (uniform trip counts:
+  // ballots see full warps)
+  auto put = [&](bool v, uint64_t key) {
     const unsigned ballot = __ballot_sync(0xFFFFFFFFu, v);
     int base = 0;
     if ((threadIdx.x & 31) == 0 && ballot) base = atomicAdd(&n_keys, __popc(ballot));
     base = __shfl_sync(0xFFFFFFFFu, base, 0);
     if (v) keys[base + __popc(ballot & ((1u << (threadIdx.x & 31)) - 1u))] = key;
+  };
+  if (S.pool != nullptr || S.block == 1) {
+    // scores (and pool block ids) kBatch rounds at a time, all loads out
+    // before the first ballot: one round trip per batch instead of per round
+    constexpr int kBatch = 8;
+    const float *row = S.scores + (int64_t)q * S.stride;
+    for (int64_t b0 = 0; b0 < S.n_items; b0 += (int64_t)kBatch * blockDim.x) {
+      float sv[kBatch];
+      int bv[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; u++) {
+        const int64_t i = b0 + (int64_t)u * blockDim.x + threadIdx.x;
+        sv[u] = i < S.n_items ? __ldg(row + i) : 0.f;
+        bv[u] = i < S.n_items && S.pool != nullptr ? __ldg(S.pool + (int64_t)q * kPoolBlocks + (i >> 3)) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; u++) {
+        if (b0 + (int64_t)u * blockDim.x >= S.n_items) break;
+        const int64_t i = b0 + (int64_t)u * blockDim.x + threadIdx.x;
+        uint64_t key = 0;
+        put(i < S.n_items && item_key_of(S, i, nv, sv[u], bv[u], key, status), key);
+      }
+    }
+  } else {
+    for (int64_t b0 = 0; b0 < S.n_items; b0 += blockDim.x) {
+      const int64_t i = b0 + threadIdx.x;
+      uint64_t key = 0;
+      put(i < S.n_items && item_key(S, q, i, nv, key, status), key);
+    }
   }
   __syncthreads();
   const int n = n_keys;
