@@ -670,8 +670,8 @@ __device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t
 // Shared memory of the direct path for rows of up to `cap` items (a multiple
 // of 4, <= kDirectCap): keys [cap] | sel [kMaxK] | 32 warp histograms [32][256]
 // | score halves sk [max(min(cap, kCandCap), 4096)] (rows of n <= cap keys, or
-// their group maxima, or the candidates above their threshold).  Short rows
-// (a prefill's) so take less of it, and two CTAs share an SM.
+// their group maxima, or the candidates above their threshold): short rows
+// (a prefill's) take less of it.
 __host__ __device__ constexpr int direct_sk_cap(int cap) { return (cap < kCandCap ? cap : kCandCap) > 4096 ? (cap < kCandCap ? cap : kCandCap) : 4096; }
 __host__ __device__ constexpr size_t direct_smem_bytes(int cap) {
   return (size_t)cap * 8 + (size_t)kMaxK * 4 + 32 * 256 * 4 + (size_t)direct_sk_cap(cap) * 4;
@@ -700,9 +700,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
     base = __shfl_sync(0xFFFFFFFFu, base, 0);
     if (v) keys[base + __popc(ballot & ((1u << (threadIdx.x & 31)) - 1u))] = key;
   };
-  if (S.pool != nullptr || S.block == 1) {
-    // scores (and pool block ids) kBatch rounds at a time, all loads out
-    // before the first ballot: one round trip per batch instead of per round
+  if (S.pool != nullptr) {
+    // pool mode (rows of 16,384 items): scores and block ids kBatch rounds
+    // at a time, all loads out before the first ballot: one round trip per
+    // batch instead of per round (measured: no gain for a prefill's shorter
+    // rows, whose items past the visible length are not read at all)
     constexpr int kBatch = 8;
     const float *row = S.scores + (int64_t)q * S.stride;
     for (int64_t b0 = 0; b0 < S.n_items; b0 += (int64_t)kBatch * blockDim.x) {
