@@ -369,7 +369,7 @@ def run_rows(args, rank, world, local_rank, wl):
         decode.reindex_decode(dw, buf, None, stream, build_pool=True)     # the pool the step is given
 
         def step():
-            decode.reindex_decode(dw, buf, None, stream, build_pool=False)
+            decode.fused_reindex_decode(dw, buf, None, stream)
     else:
         def step():
             decode.fused_decode(dw, buf, None, stream)

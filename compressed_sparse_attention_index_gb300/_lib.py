@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(HERE, "libcsa2.so")
 CSA2_KV_NVFP4, CSA2_IDX_MXFP4, CSA2_SWA_MXFP8 = 0, 1, 2
 CSA2_OUT_BF16, CSA2_OUT_F32 = 0, 1
 CSA2_OP_TOPK, CSA2_OP_SPARSE_ATTN, CSA2_OP_DECODE, CSA2_OP_DECODE_HOST, CSA2_OP_DECODE_MQ = 0, 1, 2, 3, 4
-CSA2_OP_BUILD_CACHE = 5
+CSA2_OP_BUILD_CACHE, CSA2_OP_DECODE_REINDEX = 5, 6
 STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED", 3: "CSA2_ERR_CUDA",
           4: "CSA2_ERR_BOUNDS", 5: "CSA2_ERR_TIMEOUT", 6: "CSA2_ERR_WORKSPACE"}
 
@@ -25,7 +25,7 @@ EXPORTS = ["csa2_default_params", "csa2_entry_bytes", "csa2_status_string", "csa
            "csa2_index_score", "csa2_topk", "csa2_sparse_attn", "csa2_workspace_size",
            "csa2_get_device_status", "csa2_topk_noalloc", "csa2_decode", "csa2_decode_host",
            "csa2_index_score_mq", "csa2_decode_mq", "csa2_check_bounded_wait", "csa2_index_key_proj",
-           "csa2_build_cache"]
+           "csa2_build_cache", "csa2_decode_reindex"]
 
 
 class CSA2Error(RuntimeError):
@@ -62,6 +62,8 @@ def load(path: str = LIB_PATH):
         "csa2_index_score": (i32, [P, P, i64, i32, P, P, P, P, P, i32, P, P, i64, PP, P]),
         "csa2_topk": (i32, [P, i64, i32, P, i64, i32, i32, P, P, P, sz, P]),
         "csa2_decode": (i32, [P, P, i64, i32, P, P, P, P, P, i32, P, P, P, i32, P, P, P, P, P, i32, PP, P, sz, P]),
+        "csa2_decode_reindex": (i32, [P, P, i64, i32, P, P, P, P, P, i32, P, P, P, P, i32, P, P, P, P, P, i32, PP, P,
+                                      sz, P]),
         "csa2_index_score_mq": (i32, [P, P, i64, i32, P, P, P, P, P, i32, i32, P, i64, PP, P]),
         "csa2_decode_mq": (i32, [P, P, i64, i32, P, P, P, P, P, i32, i32, P, P, P, i32, P, P, P, P, P, i32, PP, P, sz,
                                  P]),
@@ -164,6 +166,17 @@ def csa2_decode(key_nib, key_scale, n_max, n_seq, q_nib, q_scale, w, q_seq, n_vi
         _ptr(n_vis), int(n_q), _ptr(q), _ptr(kv_cache), _ptr(swa_cache), int(swa_cap), _ptr(pos), _ptr(swa_first),
         _ptr(swa_cnt), _ptr(sel), _ptr(out), int(out_dtype), pp, _ptr(workspace), int(workspace_bytes),
         _stream(stream)))
+
+
+def csa2_decode_reindex(key_nib, key_scale, n_max, n_seq, q_nib, q_scale, w, q_seq, n_vis, n_q, pool_blocks, q,
+                        kv_cache, swa_cache, swa_cap, pos, swa_first, swa_cnt, sel, out, out_dtype, params=None,
+                        workspace=None, workspace_bytes=0, stream=None):
+    pp = ctypes.byref(params) if params is not None else None
+    _check("csa2_decode_reindex", load().csa2_decode_reindex(
+        _ptr(key_nib), _ptr(key_scale), int(n_max), int(n_seq), _ptr(q_nib), _ptr(q_scale), _ptr(w), _ptr(q_seq),
+        _ptr(n_vis), int(n_q), _ptr(pool_blocks), _ptr(q), _ptr(kv_cache), _ptr(swa_cache), int(swa_cap), _ptr(pos),
+        _ptr(swa_first), _ptr(swa_cnt), _ptr(sel), _ptr(out), int(out_dtype), pp, _ptr(workspace),
+        int(workspace_bytes), _stream(stream)))
 
 
 def csa2_index_score_mq(key_nib, key_scale, n_max, n_seq, q_nib, q_scale, w, q_seq, n_vis, n_q, q_group, scores,

@@ -178,6 +178,13 @@ static size_t build_cache_workspace_bytes(int64_t n_tokens, int m) {
   return round256((size_t)c * kIdxDim * 2) + (m == 2 ? round256((size_t)c * kDim * 2) : 0);
 }
 
+// csa2_decode_reindex's workspace: pool scores [n_q][16384] fp32 | block
+// maxima [n_q][2048] | top-k scratch | attention partials
+static size_t decode_reindex_workspace_bytes(int n_q) {
+  return round256((size_t)n_q * kPoolSlots * 4) + round256((size_t)n_q * kPoolBlocks * 4) +
+         round256(topk_workspace_bytes(n_q, kPoolSlots, kTopK)) + round256(attn_workspace_bytes(n_q, kTopK));
+}
+
 // csa2_decode_mq's workspace: scores [n_q][n_max] | top-k scratch | attention partials
 static size_t decode_mq_workspace_bytes(int n_q, int64_t n_max) {
   return round256((size_t)n_q * (size_t)n_max * 4) + round256(topk_workspace_bytes(n_q, n_max, kTopK)) +
@@ -194,6 +201,11 @@ csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t 
   if (op == CSA2_OP_DECODE_MQ) {
     if (n_items <= 0) return CSA2_ERR_INVALID_ARG;
     *bytes = decode_mq_workspace_bytes(n_q, n_items);
+    return CSA2_OK;
+  }
+  if (op == CSA2_OP_DECODE_REINDEX) {
+    if (n_items <= 0) return CSA2_ERR_INVALID_ARG;
+    *bytes = decode_reindex_workspace_bytes(n_q);
     return CSA2_OK;
   }
   if (op == CSA2_OP_DECODE_HOST) {
@@ -339,6 +351,60 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
   return from_cuda(launch_attn_tc(q, kv_cache, n_max, n_seq, sel, kTopK, swa_cache, swa_cap, q_seq, pos, swa_first,
                                   swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, ws_attn, st, s, true,
                                   topk_fused_ctas(F, n_q, n_max), hand ? &H : nullptr));
+}
+
+csa2_status csa2_decode_reindex(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq,
+                                const void *q_nib, const void *q_scale, const float *w, const int32_t *q_seq,
+                                const int32_t *n_vis, int n_q, const int32_t *pool_blocks, const void *q,
+                                const void *kv_cache, const void *swa_cache, int swa_cap, const int32_t *pos,
+                                const int32_t *swa_first, const int32_t *swa_cnt, int32_t *sel, void *out,
+                                int out_dtype, const csa2_params *params, void *workspace, size_t workspace_bytes,
+                                csa2_stream_t stream) {
+  if (!params_ok(params)) return CSA2_ERR_UNSUPPORTED;
+  if (n_q < 0 || n_seq < 1 || n_max <= 0 || n_max % 128 != 0 || n_max > ((int64_t)1 << 31) - 128 || swa_cap < 0)
+    return CSA2_ERR_INVALID_ARG;
+  if (out_dtype != CSA2_OUT_BF16 && out_dtype != CSA2_OUT_F32) return CSA2_ERR_INVALID_ARG;
+  if (n_q > 65535) return CSA2_ERR_UNSUPPORTED;
+  if (n_q == 0) return CSA2_OK;
+  if (!key_nib || !key_scale || !q_nib || !q_scale || !w || !q_seq || !n_vis || !pool_blocks || !q || !kv_cache ||
+      !pos || !swa_first || !swa_cnt || !sel || !out)
+    return CSA2_ERR_INVALID_ARG;
+  if (swa_cap > 0 && swa_cache == nullptr) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(key_nib, 512) || !aligned(key_scale, 16) || !aligned(q_nib, 512) || !aligned(q_scale, 16) ||
+      !aligned(w, 16) || !aligned(pool_blocks, 4) || !aligned(q, 16) || !aligned(kv_cache, 16) ||
+      (swa_cache && !aligned(swa_cache, 16)) || !aligned(out, 16) || !aligned(sel, 4))
+    return CSA2_ERR_INVALID_ARG;
+  if (workspace_bytes < decode_reindex_workspace_bytes(n_q) || workspace == nullptr || !aligned(workspace, 256))
+    return CSA2_ERR_WORKSPACE;
+  int *st = status_ptr();
+  if (st == nullptr) return CSA2_ERR_CUDA;
+  const cudaStream_t s = (cudaStream_t)stream;
+  unsigned char *base = static_cast<unsigned char *>(workspace);
+  float *scores = reinterpret_cast<float *>(base);
+  uint32_t *bmax = reinterpret_cast<uint32_t *>(base + round256((size_t)n_q * kPoolSlots * 4));
+  void *ws_topk = reinterpret_cast<unsigned char *>(bmax) + round256((size_t)n_q * kPoolBlocks * 4);
+  void *ws_attn = static_cast<unsigned char *>(ws_topk) + round256(topk_workspace_bytes(n_q, kPoolSlots, kTopK));
+  // the pool-mode indexer also writes every block's largest order key
+  LongRowWs W;
+  W.smax = nullptr;
+  W.sstride = 0;
+  W.gmax = bmax;
+  W.gstride = kPoolBlocks;
+  cudaError_t e = launch_index_score_tc(static_cast<const uint8_t *>(key_nib), static_cast<const uint8_t *>(key_scale),
+                                        n_max, n_seq, static_cast<const uint8_t *>(q_nib),
+                                        static_cast<const uint8_t *>(q_scale), w, q_seq, n_vis, n_q, pool_blocks, scores,
+                                        kPoolSlots, st, s, &W, 1);
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  e = launch_topk(scores, kPoolSlots, n_q, n_vis, n_max, kTopK, 1, pool_blocks, sel, ws_topk, st, s, bmax,
+                  kPoolBlocks);
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  const float sm_scale = params ? params->sm_scale : 1.0f / sqrtf((float)kDim);
+  const double rope_base = params ? params->rope_base : 10000.0;
+  // the attention inputs were final before the indexer started, so the
+  // attention may stage them during the selection (one CTA per pool row)
+  return from_cuda(launch_attn_tc(q, kv_cache, n_max, n_seq, sel, kTopK, swa_cache, swa_cap, q_seq, pos, swa_first,
+                                  swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, ws_attn, st, s, true, n_q,
+                                  nullptr));
 }
 
 csa2_status csa2_index_score_mq(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq,

@@ -78,7 +78,8 @@ struct LongRowWs {
   uint32_t *smax;
   int64_t sstride;
   // optional (plain rows): the maxima of every 32 consecutive entries,
-  // gmax[q][gstride] (entry j in group j / 32), or null
+  // gmax[q][gstride] (entry j in group j / 32), or null; (pool rows, the
+  // indexer's smax_mode 1) the maxima of the pool's 8-entry blocks
   uint32_t *gmax = nullptr;
   int64_t gstride = 0;
   // optional (csa2_decode): the candidate handoff to the attention, or null
@@ -161,8 +162,11 @@ cudaError_t launch_index_score_mq(const uint8_t *key_nib, const uint8_t *key_sca
 
 size_t topk_workspace_bytes(int n_q, int64_t n_items, int k);
 bool topk_items_supported(int64_t n_items, int k);
+// bmax (pool rows, optional): the pool-mode indexer's block maxima,
+// [n_q][bstride] order keys (see csa2_decode_reindex)
 cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max, int k,
-                        int block, const int32_t *pool, int32_t *out, void *ws, int *status, cudaStream_t st);
+                        int block, const int32_t *pool, int32_t *out, void *ws, int *status, cudaStream_t st,
+                        const uint32_t *bmax = nullptr, int64_t bstride = 0);
 FusedTopk topk_fused_plan(void *ws, int n_q, int64_t n_max, int k);
 size_t topk_fused_bytes(int n_q, int64_t n_max, int k);
 cudaError_t launch_topk_fused(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max,

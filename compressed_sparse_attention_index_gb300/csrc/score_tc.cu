@@ -100,12 +100,13 @@ struct ScoreTcArgs {
   int n_q;
   int units_per_q;
   int *status;
-  // optional, Full mode only: maxima of the order keys of the scores, for the
-  // top-k that follows.  smax_mode 2: per 32 consecutive entries at
+  // optional: maxima of the order keys of the scores, for the top-k that
+  // follows.  Full mode: smax_mode 2: per 32 consecutive entries at
   // smax[q * sstride + entry / 32]; smax_mode 3: per work unit u, four partial
   // maxima (one per TMEM lane quarter, over its rows of the four sub-tiles) at
   // smax[q * sstride + 4u + quarter], and per 32 consecutive entries at
-  // gmax[q * gstride + entry / 32].  Invalid entries count as key 0.
+  // gmax[q * gstride + entry / 32].  Pool mode: smax_mode 1: per gathered
+  // 8-entry block b at gmax[q * gstride + b].  Invalid entries count as key 0.
   uint32_t *smax;
   int64_t sstride;
   uint32_t *gmax;
@@ -284,7 +285,8 @@ struct PoolGather {
 };
 
 // POOL: pool mode (P.pool set: units of gathered 8-entry blocks); SMAX: the
-// maxima the epilogue writes (P.smax_mode: 0, 2 or 3, Full mode only).
+// maxima the epilogue writes (P.smax_mode: 0, 2 or 3 in Full mode, 0 or 1 in
+// pool mode).
 template <bool POOL, int SMAX>
 __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcArgs P) {
   extern __shared__ __align__(1024) unsigned char sc_smem_raw[];
@@ -651,13 +653,16 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + group * (kSub * 32);
       float *out = P.scores + (int64_t)sc.q * P.stride;
       // entry i = i0 + 128 j of the unit (j = 0..3)
-      auto store = [&](int64_t i, int j, float v) {
+      // stores the score of entry i (sub-tile j); true if the entry is valid
+      auto store = [&](int64_t i, int j, float v) -> bool {
         if (!POOL) {
           if (i < sc.nv) out[i] = v;
+          return i < sc.nv;
         } else {
           const int b = j == 0 ? pb[0] : j == 1 ? pb[1] : j == 2 ? pb[2] : pb[3];   // (registers)
           const bool ok = b >= 0 && (int64_t)b * kBlock < P.n_max && (int64_t)b * kBlock + (i & 7) < sc.nv;
           out[i] = ok ? v : -INFINITY;
+          return ok;
         }
       };
       const int64_t i0 = (int64_t)cur_u * kUnit + row;
@@ -679,9 +684,24 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
           s0 = fmaf(wv[h], fmaxf(__uint_as_float(d0[h]), 0.f), s0);
           s1 = fmaf(wv[h], fmaxf(__uint_as_float(d1[h]), 0.f), s1);
         }
-        store(i0 + h2 * 256, 2 * h2, s0);
-        store(i0 + h2 * 256 + 128, 2 * h2 + 1, s1);
-        if constexpr (SMAX != 0) {
+        const bool ok0 = store(i0 + h2 * 256, 2 * h2, s0);
+        const bool ok1 = store(i0 + h2 * 256 + 128, 2 * h2 + 1, s1);
+        if constexpr (POOL && SMAX == 1) {
+          // pool mode: the maximum order key of each gathered 8-entry block
+          // (8 consecutive TMEM lanes; 0 when none of its entries is valid),
+          // for the selection in the pool that follows
+          uint32_t k0 = ok0 ? order_key(s0) : 0u, k1 = ok1 ? order_key(s1) : 0u;
+#pragma unroll
+          for (int o = 1; o < kBlock; o <<= 1) {
+            k0 = max(k0, __shfl_xor_sync(0xFFFFFFFFu, k0, o));
+            k1 = max(k1, __shfl_xor_sync(0xFFFFFFFFu, k1, o));
+          }
+          if ((lane & (kBlock - 1)) == 0) {
+            uint32_t *bm = P.gmax + (int64_t)sc.q * P.gstride + (int64_t)cur_u * (kUnit / kBlock);
+            bm[(2 * h2) * (128 / kBlock) + quarter * (32 / kBlock) + lane / kBlock] = k0;
+            bm[(2 * h2 + 1) * (128 / kBlock) + quarter * (32 / kBlock) + lane / kBlock] = k1;
+          }
+        } else if constexpr (SMAX != 0) {
           // order keys of this lane's two entries (0 if not visible)
           const uint32_t k0 = i0 + h2 * 256 < sc.nv ? order_key(s0) : 0u;
           const uint32_t k1 = i0 + h2 * 256 + 128 < sc.nv ? order_key(s1) : 0u;
@@ -1076,6 +1096,7 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
   P.call_id = W ? W->call_id : 0u;
   P.smax_mode = pool == nullptr && W != nullptr && (smax_mode == 2 || (smax_mode == 3 && W->gmax != nullptr))
                     ? smax_mode : 0;
+  if (pool != nullptr && W != nullptr && smax_mode == 1 && W->gmax != nullptr) P.smax_mode = 1;   // block maxima
   P.key_nib = key_nib;
   P.q_nib = q_nib;
   P.key_scale = key_scale;
@@ -1096,11 +1117,12 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
   const int dev = current_device();
   static std::atomic<int> attr_done[kMaxDevices];
   const cudaError_t e = once_per_device(attr_done, dev, [&] {
-    const cudaError_t es[4] = {
+    const cudaError_t es[5] = {
         cudaFuncSetAttribute(index_score_tc_kernel<false, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
         cudaFuncSetAttribute(index_score_tc_kernel<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
         cudaFuncSetAttribute(index_score_tc_kernel<false, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
-        cudaFuncSetAttribute(index_score_tc_kernel<true, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)};
+        cudaFuncSetAttribute(index_score_tc_kernel<true, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+        cudaFuncSetAttribute(index_score_tc_kernel<true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)};
     for (cudaError_t x : es)
       if (x != cudaSuccess) return x;
     return cudaSuccess;
@@ -1124,6 +1146,7 @@ cudaError_t launch_index_score_tc(const uint8_t *key_nib, const uint8_t *key_sca
     }
   }
   const dim3 g((unsigned)grid), b(kScThreads);
+  if (pool != nullptr && P.smax_mode == 1) return launch_pdl(index_score_tc_kernel<true, 1>, g, b, smem, st, 1u, P);
   if (pool != nullptr) return launch_pdl(index_score_tc_kernel<true, 0>, g, b, smem, st, 1u, P);
   if (P.smax_mode == 3) return launch_pdl(index_score_tc_kernel<false, 3>, g, b, smem, st, 1u, P);
   if (P.smax_mode == 2) return launch_pdl(index_score_tc_kernel<false, 2>, g, b, smem, st, 1u, P);

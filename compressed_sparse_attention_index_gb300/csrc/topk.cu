@@ -46,6 +46,11 @@ struct TopkSrc {
   const uint8_t *kv_pf;
   const int32_t *q_seq;
   int n_seq;
+  // optional (pool rows): the maximum order key of each 8-entry block's
+  // valid entries, 0 for none, [n_q][bstride] (written by the pool-mode
+  // indexer inside csa2_decode_reindex)
+  const uint32_t *bmax;
+  int64_t bstride;
 };
 
 // Key of item i of query q; false if the item is not valid.
@@ -700,6 +705,69 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
     base = __shfl_sync(0xFFFFFFFFu, base, 0);
     if (v) keys[base + __popc(ballot & ((1u << (threadIdx.x & 31)) - 1u))] = key;
   };
+  if (S.pool != nullptr && S.bmax != nullptr) {
+    // Pool rows with the indexer's block maxima: the k-th largest block
+    // maximum T is a lower bound of the k-th largest item (at least k blocks
+    // reach it, each with an item at its maximum), so only the blocks
+    // reaching T are read, item by item, and the exact selection runs on
+    // their items.  Where they hold more items than the selection's buffer,
+    // the whole row is read as below.
+    uint32_t *bm = sh.whist + 32 * 256;                                          // [kPoolBlocks]
+    int32_t *cb = reinterpret_cast<int32_t *>(keys + cap) ;                      // (sel) [kPoolBlocks]
+    __shared__ int n_cb;
+    __shared__ uint32_t T_bm;
+    const uint32_t *src = S.bmax + (int64_t)q * S.bstride;
+    for (int i = threadIdx.x; i < kPoolBlocks; i += blockDim.x) bm[i] = __ldg(src + i);
+    if (threadIdx.x == 0) n_cb = 0;
+    __syncthreads();
+    const uint32_t t = block_kth256(bm, kPoolBlocks, k < kPoolBlocks ? k : kPoolBlocks, 0, sh.whist);
+    if (threadIdx.x == 0) T_bm = t;
+    __syncthreads();
+    const uint32_t T = T_bm;
+    for (int b0 = 0; b0 < kPoolBlocks; b0 += blockDim.x) {
+      const int b = b0 + threadIdx.x;
+      const bool c = b < kPoolBlocks && bm[b] != 0u && bm[b] >= T;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, c);
+      int base = 0;
+      if ((threadIdx.x & 31) == 0 && bal) base = atomicAdd(&n_cb, __popc(bal));
+      base = __shfl_sync(0xFFFFFFFFu, base, 0);
+      if (c) cb[base + __popc(bal & ((1u << (threadIdx.x & 31)) - 1u))] = b;
+    }
+    __syncthreads();
+    const int ncb = n_cb, total = ncb * kBlock;
+    if (total <= direct_sk_cap(cap) && total <= 8 * (int)blockDim.x) {
+      // the candidate blocks' items: all loads out before the first ballot
+      constexpr int kBatch = 8;
+      const float *row = S.scores + (int64_t)q * S.stride;
+      float sv[kBatch];
+      int bv[kBatch], iv[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; u++) {
+        const int idx = u * blockDim.x + threadIdx.x;
+        const int b = idx < total ? cb[idx >> 3] : 0;
+        iv[u] = b * kBlock + (idx & 7);
+        sv[u] = idx < total ? __ldg(row + iv[u]) : 0.f;
+        bv[u] = idx < total ? __ldg(S.pool + (int64_t)q * kPoolBlocks + b) : -1;
+      }
+      __syncthreads();                                   // cb (in sel) is read: the selection may reuse it
+#pragma unroll
+      for (int u = 0; u < kBatch; u++) {
+        if (u * (int)blockDim.x >= total) break;
+        const int idx = u * blockDim.x + threadIdx.x;
+        uint64_t key = 0;
+        put(idx < total && item_key_of(S, iv[u], nv, sv[u], bv[u], key, status), key);
+      }
+      __syncthreads();
+      const int n = n_keys;
+      uint32_t *sk = bm;                                 // (the block maxima are no longer read)
+      for (int i = threadIdx.x; i < ((n + 3) & ~3); i += blockDim.x) sk[i] = i < n ? (uint32_t)(keys[i] >> 32) : 0u;
+      __syncthreads();
+      select_block(keys, sk, n, k, out + (int64_t)q * k, sel, sh.whist);
+      return;
+    }
+    if (threadIdx.x == 0) n_keys = 0;
+    __syncthreads();
+  }
   if (S.pool != nullptr) {
     // pool mode (rows of 16,384 items): scores and block ids kBatch rounds
     // at a time, all loads out before the first ballot: one round trip per
@@ -1466,8 +1534,11 @@ static unsigned collect_ctas(int dev, int n_q, int64_t n_items, int reserve = 0)
 }
 
 cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int32_t *n_valid, int64_t n_max, int k,
-                        int block, const int32_t *pool, int32_t *out, void *ws, int *status, cudaStream_t st) {
+                        int block, const int32_t *pool, int32_t *out, void *ws, int *status, cudaStream_t st,
+                        const uint32_t *bmax, int64_t bstride) {
   TopkSrc S;
+  S.bmax = pool != nullptr ? bmax : nullptr;
+  S.bstride = bstride;
   S.scores = scores;
   S.stride = stride;
   S.n_valid = n_valid;
@@ -1560,6 +1631,8 @@ cudaError_t launch_topk_fused(const float *scores, int64_t stride, int n_q, cons
                               int k, const FusedTopk &F, int32_t *out, void *ws, int *status, cudaStream_t st) {
   if (F.mode <= 0) return launch_topk(scores, stride, n_q, n_valid, n_max, k, 1, nullptr, out, ws, status, st);
   TopkSrc S;
+  S.bmax = nullptr;
+  S.bstride = 0;
   S.scores = scores;
   S.stride = stride;
   S.n_valid = n_valid;

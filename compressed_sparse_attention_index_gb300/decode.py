@@ -38,8 +38,8 @@ class DecodeBuffers:
         self.ws_topk_bytes = ws_t
         self.ws_attn_bytes = L.csa2_workspace_size(L.CSA2_OP_SPARSE_ATTN, n_q, TOPK + SWA)
         self.q_group = q_group
-        self.ws_decode_bytes = 0 if pool else L.csa2_workspace_size(
-            L.CSA2_OP_DECODE_MQ if q_group > 1 else L.CSA2_OP_DECODE, n_q, n_max, TOPK)
+        self.ws_decode_bytes = L.csa2_workspace_size(L.CSA2_OP_DECODE_REINDEX, n_q, n_max, TOPK) if pool else \
+            L.csa2_workspace_size(L.CSA2_OP_DECODE_MQ if q_group > 1 else L.CSA2_OP_DECODE, n_q, n_max, TOPK)
         self.ws = torch.empty(max(1, ws_t, self.ws_attn_bytes, self.ws_decode_bytes), dtype=torch.uint8,
                               device=device)
 
@@ -91,6 +91,18 @@ def reindex_decode(dw, buf: DecodeBuffers, params=None, stream=None, build_pool:
     return buf.out
 
 
+def fused_reindex_decode(dw, buf: DecodeBuffers, params=None, stream=None):
+    """The Reindex-layer step over the pool in buf.blocks (chosen earlier by
+    the Full layer) as the single call csa2_decode_reindex: the same selection
+    and output as reindex_decode(build_pool=False); buf.sel and buf.out are
+    written, the pool's scores stay in the workspace."""
+    L.csa2_decode_reindex(dw.key_nib, dw.key_scale, dw.n_max, dw.kv.shape[0], dw.q_nib_re, dw.q_scale_re, dw.w_re,
+                          dw.q_seq, dw.n_vis, buf.n_q, buf.blocks, dw.q, dw.kv, dw.swa, dw.swa.shape[1], dw.pos,
+                          dw.swa_first, dw.swa_cnt, buf.sel, buf.out, buf.out_dtype, params, buf.ws,
+                          buf.ws_decode_bytes, stream)
+    return buf.out
+
+
 def attend(dw, buf: DecodeBuffers, params=None, stream=None):
     L.csa2_sparse_attn(dw.q, dw.kv, dw.n_max, dw.kv.shape[0], buf.sel, TOPK, dw.swa, dw.swa.shape[1], dw.q_seq,
                        dw.pos, dw.swa_first, dw.swa_cnt, buf.n_q, buf.out, buf.out_dtype, params, buf.ws,
@@ -127,11 +139,12 @@ class DecoderStep:
                 L.csa2_topk(b.scores, b.n_max, n_q, dw.n_vis, dw.n_max, POOL_BLOCKS, 8, None, b.blocks, b.ws,
                             b.ws_topk_bytes, stream)
             elif role == "reindex":
-                L.csa2_index_score(dw.key_nib, dw.key_scale, dw.n_max, dw.kv.shape[0], dl.q_nib_re[r],
-                                   dl.q_scale_re[r], dl.w_re[r], dw.q_seq, dw.n_vis, n_q, b.blocks, b.pool_scores,
-                                   POOL_SLOTS, params, stream)
-                L.csa2_topk(b.pool_scores, POOL_SLOTS, n_q, dw.n_vis, dw.n_max, TOPK, 1, b.blocks, self.sels[r],
-                            b.ws, b.ws_topk_bytes, stream)
+                # scoring the pool, its top-512 and the attention: one call
+                L.csa2_decode_reindex(dw.key_nib, dw.key_scale, dw.n_max, dw.kv.shape[0], dl.q_nib_re[r],
+                                      dl.q_scale_re[r], dl.w_re[r], dw.q_seq, dw.n_vis, n_q, b.blocks, dl.q[l], dw.kv,
+                                      dl.swa[l], dl.swa.shape[2], dw.pos, dw.swa_first, dw.swa_cnt, self.sels[r],
+                                      self.outs[l], self.out_dtype, params, b.ws, b.ws_decode_bytes, stream)
+                continue
             L.csa2_sparse_attn(dl.q[l], dw.kv, dw.n_max, dw.kv.shape[0], self.sels[r], TOPK, dl.swa[l],
                                dl.swa.shape[2], dw.q_seq, dw.pos, dw.swa_first, dw.swa_cnt, n_q, self.outs[l],
                                self.out_dtype, params, b.ws, b.ws_attn_bytes, stream)

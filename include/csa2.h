@@ -81,7 +81,7 @@ enum { CSA2_KV_NVFP4 = 0, CSA2_IDX_MXFP4 = 1, CSA2_SWA_MXFP8 = 2 };
 enum { CSA2_OUT_BF16 = 0, CSA2_OUT_F32 = 1 };
 /* Operations for csa2_workspace_size. */
 enum { CSA2_OP_TOPK = 0, CSA2_OP_SPARSE_ATTN = 1, CSA2_OP_DECODE = 2, CSA2_OP_DECODE_HOST = 3, CSA2_OP_DECODE_MQ = 4,
-       CSA2_OP_BUILD_CACHE = 5 };
+       CSA2_OP_BUILD_CACHE = 5, CSA2_OP_DECODE_REINDEX = 6 };
 
 /* Model constants.  The kernels are built for the pages' values only
  * (study, reading notes: 64 heads, 512-wide latent, RoPE on 64 of the 512
@@ -277,6 +277,39 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
                         const csa2_params *params, void *workspace, size_t workspace_bytes, csa2_stream_t stream);
 
 /*
+ * csa2_decode_reindex -- the decode step of a Reindex layer ("An
+ * infra-oriented diagram of the DeepSeek-V4.1-Flash architecture", reading
+ * notes on the Full / Reindex / Reuse roles; perchy.ai card "Full. Reindex.
+ * Reuse."): the layer's own indexer query scores the 16,384 positions of the
+ * candidate pool the Full layer chose (2,048 blocks of 8), the top-512 of the
+ * pool is selected, and the attention runs over it and the window, as one
+ * call.  The results are those of the chain csa2_index_score (pool mode) ->
+ * csa2_topk(k = 512, block = 1, pool_blocks) -> csa2_sparse_attn(sel_stride =
+ * 512), bit for bit (selection and output).  Inside the call the indexer also
+ * writes the largest order key of every 8-entry block of the pool, so that
+ * the selection reads only the blocks that can hold one of the 512, and the
+ * attention, whose inputs are final before the call starts, stages them while
+ * the selection runs.
+ *
+ *   key_nib .. n_q      as csa2_index_score; q_nib, q_scale, w are the
+ *                       Reindex layer's indexer query and weights.
+ *   pool_blocks         (device) int32 [n_q][2048]: the pool's block ids, as
+ *                       csa2_topk(block = 8) writes them (-1: none).
+ *   q .. swa_cnt, out, out_dtype, params   as csa2_sparse_attn.
+ *   sel                 (device) int32 [n_q][512]: the selected entries
+ *                       (ascending, -1 padding), as csa2_topk writes them.
+ *   workspace           (device) >= csa2_workspace_size(CSA2_OP_DECODE_REINDEX,
+ *                       n_q, n_max, 512) bytes, 256-B aligned; no initialisation.
+ */
+csa2_status csa2_decode_reindex(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq,
+                                const void *q_nib, const void *q_scale, const float *w, const int32_t *q_seq,
+                                const int32_t *n_vis, int n_q, const int32_t *pool_blocks, const void *q,
+                                const void *kv_cache, const void *swa_cache, int swa_cap, const int32_t *pos,
+                                const int32_t *swa_first, const int32_t *swa_cnt, int32_t *sel, void *out,
+                                int out_dtype, const csa2_params *params, void *workspace, size_t workspace_bytes,
+                                csa2_stream_t stream);
+
+/*
  * csa2_index_score_mq -- csa2_index_score (Full mode) for groups of queries
  * that share a sequence, such as several draft positions of one sequence
  * decoded in the same step (DeepSeek V4.1 Flash: Why Its Encoder, Engram and
@@ -393,6 +426,7 @@ csa2_status csa2_build_cache(const void *tokens, int64_t n_tokens, int m, const 
  *                             step's inputs and outputs are included).
  *   op = CSA2_OP_DECODE_MQ:   n_q queries, n_items = n_max, k unused (512).
  *   op = CSA2_OP_BUILD_CACHE: n_q unused, n_items = tokens, k = m (1 or 2).
+ *   op = CSA2_OP_DECODE_REINDEX: n_q queries, n_items = n_max, k unused (512).
  * Sizes are for the current device (the attention's split plan follows its
  * SM count).
  */

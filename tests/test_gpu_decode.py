@@ -305,6 +305,42 @@ def test_reindex_decode_config3_full_size_sampled(lib, oracle_lib):
         _check_reindex(lib, oracle_lib, wl, blocks[qi], sel[qi], out[qi], qi)
 
 
+@pytest.mark.parametrize("case", ["pool_40k", "short_3000", "equal_scores", "config3"])
+def test_fused_reindex_equals_chain(lib, oracle_lib, case):
+    """csa2_decode_reindex (the pool-mode indexer writing block maxima, the
+    selection reading only the blocks that reach the 512th largest of them,
+    the attention staged during the selection) against the chain
+    csa2_index_score -> csa2_topk -> csa2_sparse_attn on the same pool:
+    selection and output bit for bit.  short_3000: a pool of 375 valid blocks
+    (fewer than 512 blocks: every valid block is read); equal_scores: zero
+    head weights, every score equal, all 2,048 block maxima tie (more items
+    than the candidate buffer: the whole row is read); config3: 64 x 1M, with
+    sampled queries also against the oracle."""
+    from compressed_sparse_attention_index_gb300 import decode
+    wl = {"pool_40k": small(n_seq=2, n_entries=40_000, pool=True, seed=232),
+          "short_3000": small(n_seq=2, n_entries=3000, pool=True, seed=233),
+          "equal_scores": small(n_seq=2, n_entries=40_000, pool=True, seed=234),
+          "config3": CONFIGS[3]}[case]
+    dw = _dw(wl)
+    if case == "equal_scores":
+        dw.w_re.zero_()
+    buf = _bufs(dw, pool=True)
+    decode.reindex_decode(dw, buf)                      # the pool, then the chain on it
+    sel_c, out_c = buf.sel.clone(), buf.out.clone()
+    buf.sel.fill_(-7)
+    buf.out.fill_(7.0)
+    decode.fused_reindex_decode(dw, buf)
+    assert lib.csa2_get_device_status() == 0
+    assert torch.equal(buf.sel, sel_c)
+    assert torch.equal(buf.out, out_c)
+    if case == "equal_scores":                          # ties: the lowest pool positions win
+        assert (buf.sel >= 0).sum().item() == 2 * 512
+    if case == "config3":
+        blocks, sel, out = buf.blocks.cpu().numpy(), buf.sel.cpu().numpy(), buf.out.float().cpu().numpy()
+        for qi in (7, 40):
+            _check_reindex(lib, oracle_lib, wl, blocks[qi], sel[qi], out[qi], qi)
+
+
 def test_prefill_m2_config2_sampled(lib, oracle_lib):
     wl = CONFIGS[2]
     dw = _dw(wl)
