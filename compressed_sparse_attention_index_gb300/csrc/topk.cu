@@ -706,12 +706,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
     if (v) keys[base + __popc(ballot & ((1u << (threadIdx.x & 31)) - 1u))] = key;
   };
   if (S.pool != nullptr && S.bmax != nullptr) {
-    // Pool rows with the indexer's block maxima: the k-th largest block
-    // maximum T is a lower bound of the k-th largest item (at least k blocks
-    // reach it, each with an item at its maximum), so only the blocks
+    // Pool rows with the indexer's block maxima: a lower bound T of the k-th
+    // largest block maximum is one of the k-th largest item too (at least k
+    // blocks reach it, each with an item at its maximum), so only the blocks
     // reaching T are read, item by item, and the exact selection runs on
-    // their items.  Where they hold more items than the selection's buffer,
-    // the whole row is read as below.
+    // their items that reach T.  T is taken two radix steps deep (16 bits
+    // below the bits all maxima share), which is enough to leave few more
+    // candidates than k.  Where the blocks hold more items than the
+    // selection's buffer, the whole row is read as below.
     uint32_t *bm = sh.whist + 32 * 256;                                          // [kPoolBlocks]
     int32_t *cb = reinterpret_cast<int32_t *>(keys + cap) ;                      // (sel) [kPoolBlocks]
     __shared__ int n_cb;
@@ -720,7 +722,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
     for (int i = threadIdx.x; i < kPoolBlocks; i += blockDim.x) bm[i] = __ldg(src + i);
     if (threadIdx.x == 0) n_cb = 0;
     __syncthreads();
-    const uint32_t t = block_kth256(bm, kPoolBlocks, k < kPoolBlocks ? k : kPoolBlocks, 0, sh.whist);
+    const uint32_t t = block_kth256(bm, kPoolBlocks, k < kPoolBlocks ? k : kPoolBlocks, 0, sh.whist, 2);
     if (threadIdx.x == 0) T_bm = t;
     __syncthreads();
     const uint32_t T = T_bm;
@@ -755,7 +757,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
         if (u * (int)blockDim.x >= total) break;
         const int idx = u * blockDim.x + threadIdx.x;
         uint64_t key = 0;
-        put(idx < total && item_key_of(S, iv[u], nv, sv[u], bv[u], key, status), key);
+        const bool v = idx < total && item_key_of(S, iv[u], nv, sv[u], bv[u], key, status);
+        put(v && (uint32_t)(key >> 32) >= T, key);
       }
       __syncthreads();
       const int n = n_keys;
