@@ -19,9 +19,9 @@
 // two MMA issuers.  Warp roles (480 threads):
 //   warp 0      producer: one bulk copy (cp.async.bulk) of the unit's 32 KB of
 //               nibbles, and its 2 KB of E8M0 scales by the lanes' 16-B
-//               asynchronous copies (pool mode: 16 of the 64 gathered 8-entry
+//               asynchronous copies (pool mode: 8 of the 64 gathered 8-entry
 //               blocks of 512 B + 32 B, by 16-B asynchronous copies; warps
-//               12..14 gather the other 48); with the first unit of each run
+//               12..14 and 7..10 gather the other 56); with the first unit of each run
 //               of one query, its 2 KB of nibbles and 128 B of scales (lanes'
 //               copies too) into the next of six query slots (so a CTA may
 //               switch query on every unit without a stall).  The nibble planes are stored
@@ -34,7 +34,8 @@
 //               units: eight MMAs per unit into the unit's accumulator, then one
 //               commit to the stage's done barrier, which both frees the stage
 //               and marks the accumulator full;
-//   warps 3..10 epilogue, two groups of four warps taking alternate units: one
+//   warps 3..10 epilogue, two groups of four warps taking alternate units (pool
+//               mode: warps 3..6 take every unit, warps 7..10 gather): one
 //               TMEM lane (= one entry of each sub-tile) per thread, 32 columns
 //               (= heads) per sub-tile, ReLU + weighted sum, coalesced store.
 // The producer walks the CTA's units (a fixed stride over all of them, or
@@ -60,7 +61,9 @@ constexpr int kQOffB = 0, kQOffSFB = 2048;
 constexpr int kScSmem = kScStages * kScStageBytes + kQSlots * kScQBytes;
 static_assert(kScStageBytes % 1024 == 0, "64B-swizzled tiles need 512-B aligned stages and slots");
 constexpr int kScGather0 = 12;            // warps 12..14: extra gathering warps (pool mode)
-constexpr int kPoolGatherWarps = 4;       // warp 0 and warps 12..14, 16 of a unit's 64 blocks each
+constexpr int kScGather1 = 7;             // warps 7..10: gathering warps too in pool mode (one epilogue group there)
+constexpr int kPoolGatherWarps = 8;       // warp 0, warps 12..14 and 7..10, 8 of a unit's 64 blocks each
+constexpr int kPoolWarpBlocks = 64 / kPoolGatherWarps;
 constexpr int kScThreads = 480;
 constexpr int kScMmaWarp2 = 11;          // second MMA issuer (odd units)
 constexpr int kScAcc = 2;                 // TMEM accumulators (kSub x 32 columns each), one per epilogue group
@@ -222,12 +225,12 @@ using QuerySlots = QuerySlotsT<kQSlots>;
 
 // Pool mode: a unit is 64 gathered 8-entry blocks (512 B of nibbles + 32 B of
 // scales each).  Small bulk copies cost the copy engine more than their bytes
-// (measured), and one warp's plain asynchronous copies are limited by how many
-// it may have in flight, so four warps each move 16 blocks in 16-B pieces: one
-// block's nibbles per instruction (16 B per lane), then the 16 blocks' scales
-// in one.  Each lane arrives on the stage's barrier when its copies have
-// landed (the barrier expects 1 + 32 x 4 arrivals: the producer's lane 0, with
-// the query data's bytes, and every gathering lane).  A CTA has few units in
+// (measured, also as tile::gather4 tensor copies), and a warp takes a
+// microsecond or more to issue a unit's asynchronous copies, so eight warps
+// each move 8 blocks in 16-B pieces: one block's nibbles per instruction (16 B
+// per lane), then the 8 blocks' scales in one.  Each lane arrives on the
+// stage's barrier when its copies have landed (the barrier expects 1 + 32 x 8
+// arrivals: the producer's lane 0 and every gathering lane).  A CTA has few units in
 // pool mode (2,048 for 64 queries over 152 SMs), so the block ids are loaded
 // kPoolAhead units ahead (the CTA's units T, T + gridDim.x, ...): a unit's
 // copies then never wait for its ids to come back from memory.
@@ -238,7 +241,8 @@ struct PoolGather {
   __device__ int load_b(const ScoreTcArgs &P, int g, uint32_t T) const {
     const int lane = threadIdx.x & 31;
     const int q = (int)(T / (uint32_t)P.units_per_q), u = (int)(T - (uint32_t)q * (uint32_t)P.units_per_q);
-    return __ldg(P.pool + (int64_t)q * kPoolBlocks + u * (kUnit / kBlock) + g * 16 + (lane & 15));
+    return __ldg(P.pool + (int64_t)q * kPoolBlocks + u * (kUnit / kBlock) + g * kPoolWarpBlocks +
+                 (lane & (kPoolWarpBlocks - 1)));
   }
   // ids of the units T0, T0 + gridDim.x, ... (kPoolAhead of them)
   __device__ void start(const ScoreTcArgs &P, int g, uint32_t T0, uint32_t total_units) {
@@ -268,17 +272,17 @@ struct PoolGather {
     const int lane = threadIdx.x & 31;
     const int b = take(P, g, T, total_units);
     const bool ok = b >= 0 && (int64_t)b * kBlock < P.n_max;
-    if (lane < 16 && b >= 0 && !ok) record_error(P.status, CSA2_ERR_BOUNDS);
-#pragma unroll 4
-    for (int j = 0; j < 16; j++) {
+    if (lane < kPoolWarpBlocks && b >= 0 && !ok) record_error(P.status, CSA2_ERR_BOUNDS);
+#pragma unroll
+    for (int j = 0; j < kPoolWarpBlocks; j++) {
       const int bj = __shfl_sync(0xFFFFFFFFu, b, j);
       if (bj >= 0 && (int64_t)bj * kBlock < P.n_max)
-        ptx::cp_async16(st + kOffA + (g * 16 + j) * 512 + lane * 16,
+        ptx::cp_async16(st + kOffA + (g * kPoolWarpBlocks + j) * 512 + lane * 16,
                         P.key_nib + (row0 + (int64_t)bj * kBlock) * 64 + lane * 16);
     }
-    const int bs = __shfl_sync(0xFFFFFFFFu, b, lane >> 1);
-    if (bs >= 0 && (int64_t)bs * kBlock < P.n_max)
-      ptx::cp_async16(st + kOffSFA + (g * 16 + (lane >> 1)) * 32 + (lane & 1) * 16,
+    const int bs = __shfl_sync(0xFFFFFFFFu, b, (lane >> 1) & (kPoolWarpBlocks - 1));
+    if (lane < 2 * kPoolWarpBlocks && bs >= 0 && (int64_t)bs * kBlock < P.n_max)
+      ptx::cp_async16(st + kOffSFA + (g * kPoolWarpBlocks + (lane >> 1)) * 32 + (lane & 1) * 16,
                       P.key_scale + (row0 + (int64_t)bs * kBlock) * 4 + (lane & 1) * 16);
     ptx::cp_async_arrive_noinc(full);
   }
@@ -576,10 +580,10 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       }
     }
     __syncwarp();
-  } else if (warp >= kScGather0) {
+  } else if (warp >= kScGather0 || (POOL && warp >= kScGather1 && warp < kScGather1 + 4)) {
     // ------------------------------------------------------------ gathering warps (pool mode only)
     if (POOL) {
-      const int g = warp - kScGather0 + 1;
+      const int g = warp >= kScGather0 ? warp - kScGather0 + 1 : warp - kScGather1 + 4;
       QueryInfo gq;
       gq.cache = qc;
       PoolGather pg;
@@ -600,9 +604,11 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
   } else {
     // ------------------------------------------------------------ epilogue
     // group g (warps 3+4g .. 6+4g) takes the units with it % 2 == g and owns
-    // accumulator g.  Waiting on done_bar is unambiguous: the stage's next
-    // phase needs the MMA of unit it+kScStages, which needs this group to have
-    // released unit it+kScStages-2, i.e. to have passed unit it.
+    // accumulator g; in pool mode, whose units are few and gathered by more
+    // warps, group 0 alone takes every unit, accumulator it % 2 (warps 7..10
+    // gather).  Waiting on done_bar is unambiguous: the stage's next phase
+    // needs the MMA of unit it+kScStages, which needs the unit it+kScStages-2
+    // (same accumulator) released, i.e. this group to have passed unit it.
     const int quarter = warp & 3;
     const uint32_t group = (uint32_t)(warp - 3) >> 2;     // warps 3..6 -> 0, 7..10 -> 1
     const int row = quarter * 32 + lane;
@@ -615,7 +621,8 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       uint32_t T;
       if (!ring_get(unit_ring, it, T, abort_flag)) { fail(); break; }   // every entry: the last may be either parity
       if (T == kDone) break;
-      if ((it & 1) != group) continue;
+      if (!POOL && (it & 1) != group) continue;
+      const uint32_t acc = POOL ? (it & 1) : group;
       const int cur_u = (int)(T % (uint32_t)P.units_per_q), nq = (int)(T / (uint32_t)P.units_per_q);
       const uint32_t s = it % kScStages, r = it / kScStages;
       auto load_w = [&]() {
@@ -650,7 +657,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         if (!ptx::mbar_wait(&done_bar[s], r & 1)) { fail(); break; }
       }
       ptx::tc_fence_after();
-      const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + group * (kSub * 32);
+      const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + acc * (kSub * 32);
       float *out = P.scores + (int64_t)sc.q * P.stride;
       // entry i = i0 + 128 j of the unit (j = 0..3)
       // stores the score of entry i (sub-tile j); true if the entry is valid
@@ -676,7 +683,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         if (h2 == kSub / 2 - 1) {
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&acc_empty[group]);
+          if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
         }
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -731,7 +738,8 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       for (int i = max(0, armed_sh - kScStages); i < armed_sh; i++)
         ptx::mbar_wait(&full_bar[i % kScStages], (uint32_t)(i / kScStages) & 1);
     }
-    if (warp == 0 || (POOL && warp >= kScGather0)) asm volatile("cp.async.wait_all;" ::: "memory");
+    if (warp == 0 || (POOL && (warp >= kScGather0 || (warp >= kScGather1 && warp < kScGather1 + 4))))
+      asm volatile("cp.async.wait_all;" ::: "memory");
     if (lane == 0 && (warp == 1 || warp == 2 || warp == kScMmaWarp2)) ptx::tc_commit(&drain_bar);
     ptx::mbar_wait(&drain_bar, 0);
   }
