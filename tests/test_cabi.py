@@ -87,6 +87,14 @@ def test_host_validation_rejects_before_launch(lib):
     assert L.csa2_build_cache(fake, 32, 1, None, fake, fake, fake + 256, fake, fake,
                               1 << 30, None) == INVALID
     assert L.csa2_build_cache(fake, 32, 2, fake, fake, fake, fake, fake, fake, 1024, None) == WS
+    # csa2_decode_reindex: no pool, a misaligned pool, n_max not a multiple of 128, a short workspace
+    def reindex(n_max, pool, ws_bytes):
+        return L.csa2_decode_reindex(fake, fake, n_max, 1, fake, fake, fake, fake, fake, 8, pool, fake, fake, fake,
+                                     128, fake, fake, fake, fake, fake, 0, None, fake, ws_bytes, None)
+    assert reindex(1024, None, 1 << 30) == INVALID
+    assert reindex(1024, fake + 2, 1 << 30) == INVALID
+    assert reindex(1000, fake, 1 << 30) == INVALID
+    assert reindex(1024, fake, 1024) == WS
     assert L.csa2_check_bounded_wait(0, None) == INVALID                                 # limit out of range
     assert L.csa2_check_bounded_wait(2_000_001, None) == INVALID
     assert L.csa2_get_device_status(None, None) == INVALID
@@ -102,6 +110,8 @@ def test_workspace_sizes(lib):
     # per row: the 2,048 maxima of 512-item supergroups (candidates stay on chip)
     assert lib.csa2_workspace_size(lib.CSA2_OP_TOPK, 8, 1 << 20, 512) == 8 * 2048 * 4
     assert lib.csa2_workspace_size(lib.CSA2_OP_SPARSE_ATTN, 8192, 640) == 0      # no split for big batches
+    # the Reindex step: the pool's scores and block maxima come first
+    assert lib.csa2_workspace_size(lib.CSA2_OP_DECODE_REINDEX, 8, 1 << 20, 512) >= 8 * (16384 + 2048) * 4
     # the cache build's scratch: one chunk of at most 131,072 entries (keys; pooled latents for m = 2)
     assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 1 << 20, 2) == 131072 * (128 + 512) * 2
     assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 1 << 20, 1) == 131072 * 128 * 2
