@@ -50,7 +50,7 @@ IDX_BYTES = 68
 # current kernel on the named workload; workloads without such a capture report null.
 INDEX_SCORE_TRAFFIC = {"long_full_decode_N1M_B8_zipf": 570_489_344 + 5_250_304,
                        "full_decode_N65536_B32": 142_722_048 + 4_186_880,
-                       "reindex_decode_N1M_B64": 84_273_152 + 1_938_432}
+                       "reindex_decode_N1M_B64": 84_276_736 + 1_779_200}
 
 
 def parse():
