@@ -409,6 +409,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
     const bool hand_live = HAND && sel_chunk && hnc != kHandFallback;
     if (HAND && sel_chunk && c * kTcChunk >= (hand_live ? (int)hnc - 1 : A.sel_stride))
       continue;                                      // uniform: the chunk holds no entry
+    // a chunk of selected entries only whose 128 slots are all empty (a query
+    // with fewer visible entries than k: a prefill's early positions) is
+    // skipped; the slot indices read here serve its gather too
+    int sel_j = -1;
+    if (sel_chunk && !hand_live) {                   // (the handoff's fallback reads the selection too)
+      const int slot = c * kTcChunk + (t >> 1);
+      sel_j = pre_c == c ? pre_j : (slot < A.sel_stride ? __ldcg(A.sel + (int64_t)qi * A.sel_stride + slot) : -1);
+      if (!__syncthreads_or(sel_j >= 0) && (c + 1) * kTcChunk <= A.n_sel) continue;
+    }
     const bool f16c = chunk_f16(c);
     if (f16c != q16) {                                // the last chunk's MMAs are complete
       qscale = stage_q(f16c);
@@ -436,10 +445,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
             hk = __ldcg(A.hcand + ((int64_t)qi * kHandCtas + p) * kHandSeg + (slot - hoff_sh[p]));
             j = (int)~(uint32_t)hk;
           }
-        } else if (pre_c == c) {
-          j = pre_j;
-        } else if (slot < A.sel_stride) {
-          j = __ldcg(A.sel + (int64_t)qi * A.sel_stride + slot);
+        } else {
+          j = sel_j;                                  // (read above)
         }
         if (j >= 0 && (int64_t)j < A.n_max) {
           ok = 1;
