@@ -97,7 +97,7 @@ __device__ __forceinline__ int query_nv(const TopkSrc &S, int q, int *status) {
   return nv;
 }
 
-// ---- block-wide pieces (blockDim.x == kTopkThreads) ----
+// ---- block-wide pieces (blockDim.x a multiple of 32, <= kTopkThreads) ----
 struct SelectShared {
   uint32_t hist[256];
   uint32_t *whist;   // [32 warps][256] private histograms (dynamic shared memory)
@@ -112,7 +112,8 @@ struct SelectShared {
 template <class F>
 __device__ void block_hist(SelectShared &sh, int64_t n, F digit_of) {
   uint32_t *wh = sh.whist + (threadIdx.x >> 5) * 256;
-  for (int i = threadIdx.x; i < 32 * 256; i += blockDim.x) sh.whist[i] = 0;
+  const int nw = blockDim.x >> 5;
+  for (int i = threadIdx.x; i < nw * 256; i += blockDim.x) sh.whist[i] = 0;
   __syncthreads();
   for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
     uint32_t d;
@@ -122,7 +123,7 @@ __device__ void block_hist(SelectShared &sh, int64_t n, F digit_of) {
   for (int b = threadIdx.x; b < 256; b += blockDim.x) {
     uint32_t c = 0;
 #pragma unroll 8
-    for (int w = 0; w < 32; w++) c += sh.whist[w * 256 + b];
+    for (int w = 0; w < nw; w++) c += sh.whist[w * 256 + b];
     sh.hist[b] = c;
   }
   __syncthreads();
@@ -678,9 +679,17 @@ __device__ void select_block(uint64_t *keys, uint32_t *sk, int n, int k, int32_t
 // their group maxima, or the candidates above their threshold): short rows
 // (a prefill's) take less of it.
 __host__ __device__ constexpr int direct_sk_cap(int cap) { return (cap < kCandCap ? cap : kCandCap) > 4096 ? (cap < kCandCap ? cap : kCandCap) : 4096; }
-__host__ __device__ constexpr size_t direct_smem_bytes(int cap) {
-  return (size_t)cap * 8 + (size_t)kMaxK * 4 + 32 * 256 * 4 + (size_t)direct_sk_cap(cap) * 4;
+// the warp histograms' region in words (also the exact selection's 4,096
+// bucket counters, and the candidates of the group-maxima path as 64-bit keys)
+__host__ __device__ constexpr int direct_whist_words(int threads) {
+  return (threads / 32) * 256 > 4096 ? (threads / 32) * 256 : 4096;
 }
+__host__ __device__ constexpr size_t direct_smem_bytes(int cap, int threads) {
+  return (size_t)cap * 8 + (size_t)kMaxK * 4 + (size_t)direct_whist_words(threads) * 4 + (size_t)direct_sk_cap(cap) * 4;
+}
+// rows of up to this many items take a CTA of 256 threads (three per SM),
+// longer ones 1,024
+constexpr int kDirectSmallItems = 4096;
 
 __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, int k, int32_t *__restrict__ out,
                                                                     int *status, int cap) {
@@ -714,7 +723,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
     // below the bits all maxima share), which is enough to leave few more
     // candidates than k.  Where the blocks hold more items than the
     // selection's buffer, the whole row is read as below.
-    uint32_t *bm = sh.whist + 32 * 256;                                          // [kPoolBlocks]
+    uint32_t *bm = sh.whist + direct_whist_words(blockDim.x);                   // [kPoolBlocks]
     int32_t *cb = reinterpret_cast<int32_t *>(keys + cap) ;                      // (sel) [kPoolBlocks]
     __shared__ int n_cb;
     __shared__ uint32_t T_bm;
@@ -805,7 +814,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
   __syncthreads();
   const int n = n_keys;
   int32_t *oq = out + (int64_t)q * k;
-  uint32_t *sk = sh.whist + 32 * 256;                                            // [direct_sk_cap(cap)]
+  uint32_t *sk = sh.whist + direct_whist_words(blockDim.x);                     // [direct_sk_cap(cap)]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   // Larger sets: a threshold from the maxima of groups of gsz keys (the
   // largest power of two <= 32 leaving >= 4k groups): at least k groups reach
@@ -841,8 +850,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_direct_kernel(TopkSrc S, in
     }
     __syncthreads();
     const uint32_t T = T_sh;
-    uint64_t *cand = reinterpret_cast<uint64_t *>(sh.whist);                     // [kCandCap / 2]
-    constexpr int kDirCand = kCandCap / 2;
+    uint64_t *cand = reinterpret_cast<uint64_t *>(sh.whist);                     // [kDirCand]
+    const int kDirCand = direct_whist_words(blockDim.x) / 2;
     for (int b0 = 0; b0 < n; b0 += blockDim.x) {
       const int i = b0 + threadIdx.x;
       const uint64_t x = i < n ? keys[i] : 0ull;
@@ -1552,7 +1561,7 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
   S.kv_pf = nullptr;
   S.q_seq = nullptr;
   S.n_seq = 0;
-  const size_t dsm_direct = direct_smem_bytes(kDirectCap);
+  const size_t dsm_direct = direct_smem_bytes(kDirectCap, kTopkThreads);
   const size_t dsm_collect = collect_smem_bytes();
   const int dev = current_device();
   static std::atomic<int> attr_done[kMaxDevices];
@@ -1562,8 +1571,9 @@ cudaError_t launch_topk(const float *scores, int64_t stride, int n_q, const int3
   if (ea != cudaSuccess) return ea;
   if (S.n_items <= kDirectCap) {
     const int cap = (int)((S.n_items + 3) / 4 * 4);
-    return launch_pdl(topk_direct_kernel, dim3(n_q), dim3(kTopkThreads), direct_smem_bytes(cap), st, 1u, S, k, out,
-                      status, cap);
+    const int threads = S.n_items <= kDirectSmallItems ? 256 : kTopkThreads;
+    return launch_pdl(topk_direct_kernel, dim3(n_q), dim3(threads), direct_smem_bytes(cap, threads), st, 1u, S, k,
+                      out, status, cap);
   }
   const int64_t sgi = long_row_sgi(S.n_items, k);
   const LongRowWs W = long_row_ws(ws, n_q, S.n_items, k);
