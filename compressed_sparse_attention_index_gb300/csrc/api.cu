@@ -57,7 +57,7 @@ static bool decode_handoff(int n_q, int64_t n_max) {
 static size_t decode_workspace_bytes(int n_q, int64_t n_max) {
   const bool hand = decode_handoff(n_q, n_max);
   size_t b = round256((size_t)n_q * (size_t)n_max * 4) + round256(topk_fused_bytes(n_q, n_max, kTopK)) +
-             round256(attn_workspace_bytes(n_q, hand ? kHandCap : kTopK));
+             round256(attn_workspace_bytes(n_q, hand ? kHandCap : kTopK, true));
   if (topk_fused_plan(nullptr, n_q, n_max, kTopK).mode > 0) b += 256;
   if (hand) b += round256((size_t)n_q * kHandWords * 4) + round256((size_t)n_q * kHandCtas * kHandSeg * 8);
   return b;
@@ -182,7 +182,7 @@ static size_t build_cache_workspace_bytes(int64_t n_tokens, int m) {
 // maxima [n_q][2048] | top-k scratch | attention partials
 static size_t decode_reindex_workspace_bytes(int n_q) {
   return round256((size_t)n_q * kPoolSlots * 4) + round256((size_t)n_q * kPoolBlocks * 4) +
-         round256(topk_workspace_bytes(n_q, kPoolSlots, kTopK)) + round256(attn_workspace_bytes(n_q, kTopK));
+         round256(topk_workspace_bytes(n_q, kPoolSlots, kTopK)) + round256(attn_workspace_bytes(n_q, kTopK, true));
 }
 
 // csa2_decode_mq's workspace: scores [n_q][n_max] | top-k scratch | attention partials
@@ -317,9 +317,9 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
   F.n_seq = n_seq;
   const bool fused = F.mode > 0;
   const bool hand = decode_handoff(n_q, n_max);
-  F.reserve = attn_ctas(n_q, hand ? kHandCap : kTopK);
+  F.reserve = attn_ctas(n_q, hand ? kHandCap : kTopK, true);
   unsigned char *after_attn = static_cast<unsigned char *>(ws_attn) +
-                              round256(attn_workspace_bytes(n_q, hand ? kHandCap : kTopK));
+                              round256(attn_workspace_bytes(n_q, hand ? kHandCap : kTopK, true));
   if (fused) {
     // the indexer's claim counter, tagged per call (the tag is never 0)
     static std::atomic<uint32_t> calls{0};

@@ -150,6 +150,7 @@ struct AttnTcArgs {
   float scale_log2;
   double inv_freq[kRopeDim / 2];   // rope_base^(-2i/64)
   int nsplit, chunks_per_split;
+  int merge_tail;   // the last split also runs the window-only chunks, first (settled inputs: during the selection)
   int hsplit;       // CTAs sharing a chunk, each with 64 / hsplit of the heads
   float *part;      // [n_q][nsplit][64][512]: unnormalised O
   float *part_ml;   // [n_q][nsplit][2][64]
@@ -221,8 +222,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
                    (swa_cnt > 0 && (swa_first < 0 || swa_first >= A.swa_cap));
   if (bad && t == 0 && split == 0 && h0 == 0) record_error(A.status, CSA2_ERR_BOUNDS);
   const int n_slots = A.n_sel + (bad ? 0 : swa_cnt);
+  // A merged last split (settled inputs) runs the window-only chunks first,
+  // while the selection finishes, then its chunks of selected entries
+  const bool merged = A.merge_tail && split == A.nsplit - 1;
   const int c0 = split * A.chunks_per_split;
-  const int c1 = bad ? c0 : min((n_slots + kTcChunk - 1) / kTcChunk, c0 + A.chunks_per_split);
+  const int c1 = bad ? c0 : min((n_slots + kTcChunk - 1) / kTcChunk, merged ? 1 << 20 : c0 + A.chunks_per_split);
+  const int sel_end = (A.n_sel + kTcChunk - 1) / kTcChunk;      // the first window-only chunk
+  const int n_w = merged ? max(0, c1 - max(c0, sel_end)) : 0;  // window-only chunks run first
 
   if (t == 0) {
     ptx::mbar_init(&bar_s, 2);                       // two S issuers
@@ -305,7 +311,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
   };
   // the chunks of FP4 latents only (the first n_sel / 128 ones) run in f16
   auto chunk_f16 = [&](int c) { return (c + 1) * kTcChunk <= A.n_sel; };
-  bool q16 = c0 < c1 && chunk_f16(c0);
+  bool q16 = c0 < c1 && chunk_f16(n_w > 0 ? c1 - n_w : c0);   // the type of the first chunk run
   float qscale = stage_q(q16);
   // all-ones A operands: one 8 x 16-B core matrix of 1.0 in bf16 and in f16,
   // read for every row group and K chunk (both descriptor strides 0)
@@ -349,7 +355,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(AttnTcArgs A) {
 #pragma unroll
     for (int v = 0; v < 8; v++) rec_nb[v] = __ldg(reinterpret_cast<const uint4 *>(rec + half * 128 + v * 16));
   };
-  for (int c = c0, wp = warm; c < c1; c += 1 - wp, wp = 0) {
+  for (int kc = c0, wp = warm; kc < c1; kc += 1 - wp, wp = 0) {
+    const int c = kc - c0 < n_w ? c1 - n_w + (kc - c0) : kc - n_w;   // (merged: window-only chunks first)
     const bool sel_chunk = !wp && c * kTcChunk < A.n_sel;   // the chunk holds selected entries (or candidates)
     if (sel_chunk && !got_sel) {
       got_sel = true;
@@ -904,25 +911,35 @@ static int attn_chunks(int sel_stride) { return (sel_stride + kSwa + kTcChunk - 
 // per CTA while the CTAs whose chunks hold selected entries fit one wave on the
 // current device's n_sm SMs (the window-only chunks are placed first and run
 // while the selection finishes); else contiguous runs of chunks, at least one
-// CTA per query.
+// CTA per query.  With settled inputs, where the chunks of selected entries
+// alone, in runs of fewer chunks, fit one wave (64 queries: two runs of two
+// instead of a run of three beside one of two), the last split also takes the
+// window-only chunk and runs it first, while the selection finishes.
 struct AttnPlan {
   int nsplit, cps, hs;   // splits of a query's chunks, chunks per split, CTAs per chunk (head halves)
+  int merge;             // the last split also runs the window-only chunks (first)
 };
-static AttnPlan attn_plan(int n_q, int sel_stride, int n_sm) {
+static AttnPlan attn_plan(int n_q, int sel_stride, int n_sm, bool settled = false) {
   const int chunks = attn_chunks(sel_stride);
   const int sel_ch = (sel_stride + kTcChunk - 1) / kTcChunk;
   if (n_q * sel_ch <= n_sm) {
     // one chunk per CTA; two CTAs per chunk (32 heads each) while all of them
     // fit one wave: the gather is repeated, the rest of the chunk is halved
-    return AttnPlan{chunks, 1, n_q * chunks * 2 <= n_sm ? 2 : 1};
+    return AttnPlan{chunks, 1, n_q * chunks * 2 <= n_sm ? 2 : 1, 0};
   }
   const int ns = std::max(1, std::min(chunks, n_sm / n_q));
   const int cps = (chunks + ns - 1) / ns;
-  return AttnPlan{(chunks + cps - 1) / cps, cps, 1};
+  if (settled && sel_stride % kTcChunk == 0 && chunks > sel_ch) {
+    const int ns_s = std::max(1, std::min(sel_ch, n_sm / n_q));
+    const int cps_s = (sel_ch + ns_s - 1) / ns_s;
+    const int nsp = (sel_ch + cps_s - 1) / cps_s;
+    if (cps_s < cps && n_q * nsp <= n_sm) return AttnPlan{nsp, cps_s, 1, 1};
+  }
+  return AttnPlan{(chunks + cps - 1) / cps, cps, 1, 0};
 }
 
-int attn_ctas(int n_q, int sel_stride) {
-  const AttnPlan p = attn_plan(n_q, sel_stride, device_sm_count(current_device()));
+int attn_ctas(int n_q, int sel_stride, bool settled) {
+  const AttnPlan p = attn_plan(n_q, sel_stride, device_sm_count(current_device()), settled);
   return n_q * p.nsplit * p.hs;
 }
 
@@ -930,8 +947,8 @@ bool attn_handoff_fits(int n_q) {
   return attn_plan(n_q, kHandCap, device_sm_count(current_device())).cps == 1;
 }
 
-size_t attn_workspace_bytes(int n_q, int sel_stride) {
-  const AttnPlan p = attn_plan(n_q, sel_stride, device_sm_count(current_device()));
+size_t attn_workspace_bytes(int n_q, int sel_stride, bool settled) {
+  const AttnPlan p = attn_plan(n_q, sel_stride, device_sm_count(current_device()), settled);
   if (p.nsplit == 1) return 0;
   return (size_t)n_q * p.nsplit * (kHeads * kDim + 2 * kHeads) * sizeof(float);
 }
@@ -965,9 +982,10 @@ cudaError_t launch_attn_tc(const void *q, const void *kv, int64_t n_max, int n_s
   for (int i = 0; i < kRopeDim / 2; i++) A.inv_freq[i] = pow(rope_base, -2.0 * i / (double)kRopeDim);
   const int dev = current_device();
   const int n_sm = device_sm_count(dev);
-  const AttnPlan plan = attn_plan(n_q, A.n_sel, n_sm);
+  const AttnPlan plan = attn_plan(n_q, A.n_sel, n_sm, inputs_settled);
   A.nsplit = plan.nsplit;
   A.chunks_per_split = plan.cps;
+  A.merge_tail = plan.merge;
   A.hsplit = plan.hs;
   A.part = static_cast<float *>(ws);
   A.part_ml = A.part + (size_t)n_q * A.nsplit * kHeads * kDim;

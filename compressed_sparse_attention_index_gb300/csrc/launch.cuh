@@ -175,9 +175,10 @@ cudaError_t launch_topk_fused(const float *scores, int64_t stride, int n_q, cons
 // or -1 where that is not known (modes -1 and 0).
 int topk_fused_ctas(const FusedTopk &F, int n_q, int64_t n_max);
 
-size_t attn_workspace_bytes(int n_q, int sel_stride);
+// settled: the plan of a launch with inputs_settled (below)
+size_t attn_workspace_bytes(int n_q, int sel_stride, bool settled = false);
 // CTAs of the attention grid (one per SM) for n_q queries
-int attn_ctas(int n_q, int sel_stride);
+int attn_ctas(int n_q, int sel_stride, bool settled = false);
 // inputs_settled: q, the window cache and the per-query arrays were final
 // before the grid ahead of this one on the stream started (so inside
 // csa2_decode): the kernel then stages Q and runs its window-only chunks before

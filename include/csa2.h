@@ -259,8 +259,10 @@ csa2_status csa2_sparse_attn(const void *q, const void *kv_cache, int64_t n_max,
  * its exact pass, and the attention masks those below the smallest selected
  * key: the output then attends to exactly the selected entries and the window,
  * but groups them into other chunks than csa2_sparse_attn does, so it agrees
- * with the chain's to rounding (relative 1e-3) rather than bit for bit.  The
- * same inputs give the same bits on every call.
+ * with the chain's to rounding (relative 1e-3) rather than bit for bit; the
+ * same holds for batches (about 39 to 76 queries on 152 SMs) where the
+ * attention runs a query's window chunk first in its last split, while the
+ * selection finishes.  The same inputs give the same bits on every call.
  *
  *   key_nib .. n_q      as csa2_index_score (Full mode; scores are kept in the
  *                       workspace).
@@ -285,7 +287,10 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
  * pool is selected, and the attention runs over it and the window, as one
  * call.  The results are those of the chain csa2_index_score (pool mode) ->
  * csa2_topk(k = 512, block = 1, pool_blocks) -> csa2_sparse_attn(sel_stride =
- * 512), bit for bit (selection and output).  Inside the call the indexer also
+ * 512): the selection bit for bit, the output bit for bit where the attention
+ * splits a query's chunks as csa2_sparse_attn does, else to rounding (relative
+ * 1e-3; for some batch sizes the call runs a query's window chunk first in its
+ * last split, while the selection finishes).  Inside the call the indexer also
  * writes the largest order key of every 8-entry block of the pool, so that
  * the selection reads only the blocks that can hold one of the 512, and the
  * attention, whose inputs are final before the call starts, stages them while
