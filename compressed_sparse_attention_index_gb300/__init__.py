@@ -8,6 +8,7 @@ library is not built, importing the binding raises.
 from ._lib import (  # noqa: F401
     CSA2_IDX_MXFP4, CSA2_KV_NVFP4, CSA2_OP_BUILD_CACHE, CSA2_OP_DECODE, CSA2_OP_DECODE_HOST, CSA2_OP_DECODE_MQ,
     CSA2_OP_DECODE_REINDEX, CSA2_OP_SPARSE_ATTN, csa2_build_cache, csa2_decode_reindex, csa2_index_key_proj,
+    csa2_profile_events,
     CSA2_OP_TOPK, CSA2_OUT_BF16, CSA2_OUT_F32, CSA2_SWA_MXFP8, CSA2Error, EXPORTS, LIB_PATH, csa2_check_bounded_wait,
     csa2_decode,
     csa2_decode_host, csa2_decode_mq, csa2_entry_bytes, csa2_fp4_pack, csa2_get_device_status, csa2_index_score,

@@ -25,7 +25,7 @@ EXPORTS = ["csa2_default_params", "csa2_entry_bytes", "csa2_status_string", "csa
            "csa2_index_score", "csa2_topk", "csa2_sparse_attn", "csa2_workspace_size",
            "csa2_get_device_status", "csa2_topk_noalloc", "csa2_decode", "csa2_decode_host",
            "csa2_index_score_mq", "csa2_decode_mq", "csa2_check_bounded_wait", "csa2_index_key_proj",
-           "csa2_build_cache", "csa2_decode_reindex"]
+           "csa2_build_cache", "csa2_decode_reindex", "csa2_profile_events"]
 
 
 class CSA2Error(RuntimeError):
@@ -72,6 +72,7 @@ def load(path: str = LIB_PATH):
         "csa2_sparse_attn": (i32, [P, P, i64, i32, P, i32, P, i32, P, P, P, P, i32, P, i32, PP, P, sz, P]),
         "csa2_workspace_size": (i32, [i32, i32, i64, i32, ctypes.POINTER(sz)]),
         "csa2_get_device_status": (i32, [P, ctypes.POINTER(i32)]),
+        "csa2_profile_events": (i32, [P, P]),
         "csa2_check_bounded_wait": (i32, [ctypes.c_uint, P]),
         "csa2_index_key_proj": (i32, [P, i64, P, P, P]),
         "csa2_build_cache": (i32, [P, i64, i32, P, P, P, P, P, P, sz, P]),
@@ -166,6 +167,14 @@ def csa2_decode(key_nib, key_scale, n_max, n_seq, q_nib, q_scale, w, q_seq, n_vi
         _ptr(n_vis), int(n_q), _ptr(q), _ptr(kv_cache), _ptr(swa_cache), int(swa_cap), _ptr(pos), _ptr(swa_first),
         _ptr(swa_cnt), _ptr(sel), _ptr(out), int(out_dtype), pp, _ptr(workspace), int(workspace_bytes),
         _stream(stream)))
+
+
+def csa2_profile_events(begin=None, end=None):
+    """Events (torch.cuda.Event, already recorded once so that they exist)
+    that csa2_decode / csa2_decode_reindex record around their indexer launch
+    on this host thread; both None: off."""
+    ptr = lambda e: None if e is None else int(e.cuda_event)
+    _check("csa2_profile_events", load().csa2_profile_events(ptr(begin), ptr(end)))
 
 
 def csa2_decode_reindex(key_nib, key_scale, n_max, n_seq, q_nib, q_scale, w, q_seq, n_vis, n_q, pool_blocks, q,

@@ -44,6 +44,11 @@ static csa2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA2_OK 
 
 static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
+// csa2_profile_events: events recorded around the indexer launch of the
+// decode steps, per host thread (null: off)
+static thread_local cudaEvent_t g_prof_begin = nullptr, g_prof_end = nullptr;
+static cudaError_t prof_mark(cudaEvent_t e, cudaStream_t s) { return e != nullptr ? cudaEventRecord(e, s) : cudaSuccess; }
+
 // csa2_decode's workspace, each part 256-B aligned:
 // scores [n_q][n_max] fp32 | top-k scratch | attention partials
 // csa2_decode's workspace: scores | top-k scratch | attention partials | the
@@ -189,6 +194,13 @@ static size_t decode_reindex_workspace_bytes(int n_q) {
 static size_t decode_mq_workspace_bytes(int n_q, int64_t n_max) {
   return round256((size_t)n_q * (size_t)n_max * 4) + round256(topk_workspace_bytes(n_q, n_max, kTopK)) +
          round256(attn_workspace_bytes(n_q, kTopK));
+}
+
+csa2_status csa2_profile_events(void *begin, void *end) {
+  if ((begin == nullptr) != (end == nullptr)) return CSA2_ERR_INVALID_ARG;
+  g_prof_begin = static_cast<cudaEvent_t>(begin);
+  g_prof_end = static_cast<cudaEvent_t>(end);
+  return CSA2_OK;
 }
 
 csa2_status csa2_workspace_size(int op, int n_q, int64_t n_items, int k, size_t *bytes) {
@@ -337,11 +349,12 @@ csa2_status csa2_decode(const void *key_nib, const void *key_scale, int64_t n_ma
     H.parts = topk_fused_ctas(F, n_q, n_max) / n_q;   // the selection's cluster size
     F.W.hand = H;
   }
+  if (prof_mark(g_prof_begin, s) != cudaSuccess) return CSA2_ERR_CUDA;
   cudaError_t e = launch_index_score_tc(static_cast<const uint8_t *>(key_nib), static_cast<const uint8_t *>(key_scale),
                                         n_max, n_seq, static_cast<const uint8_t *>(q_nib),
                                         static_cast<const uint8_t *>(q_scale), w, q_seq, n_vis, n_q, nullptr, scores,
                                         n_max, st, s, fused ? &F.W : nullptr, fused ? F.mode : 0);
-  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  if (e != cudaSuccess || prof_mark(g_prof_end, s) != cudaSuccess) return CSA2_ERR_CUDA;
   e = launch_topk_fused(scores, n_max, n_q, n_vis, n_max, kTopK, F, sel, ws_topk, st, s);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
   const float sm_scale = params ? params->sm_scale : 1.0f / sqrtf((float)kDim);
@@ -390,11 +403,12 @@ csa2_status csa2_decode_reindex(const void *key_nib, const void *key_scale, int6
   W.sstride = 0;
   W.gmax = bmax;
   W.gstride = kPoolBlocks;
+  if (prof_mark(g_prof_begin, s) != cudaSuccess) return CSA2_ERR_CUDA;
   cudaError_t e = launch_index_score_tc(static_cast<const uint8_t *>(key_nib), static_cast<const uint8_t *>(key_scale),
                                         n_max, n_seq, static_cast<const uint8_t *>(q_nib),
                                         static_cast<const uint8_t *>(q_scale), w, q_seq, n_vis, n_q, pool_blocks, scores,
                                         kPoolSlots, st, s, &W, 1);
-  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  if (e != cudaSuccess || prof_mark(g_prof_end, s) != cudaSuccess) return CSA2_ERR_CUDA;
   e = launch_topk(scores, kPoolSlots, n_q, n_vis, n_max, kTopK, 1, pool_blocks, sel, ws_topk, st, s, bmax,
                   kPoolBlocks);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;

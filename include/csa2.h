@@ -422,6 +422,20 @@ csa2_status csa2_build_cache(const void *tokens, int64_t n_tokens, int m, const 
                              size_t workspace_bytes, csa2_stream_t stream);
 
 /*
+ * csa2_profile_events -- measurement hook: while set, csa2_decode and
+ * csa2_decode_reindex record `begin` on their stream just before they launch
+ * the indexer and `end` just after it, so that the indexer kernel of the step
+ * itself (the instantiation that also writes the selection's maxima) can be
+ * timed with cudaEventElapsedTime.  Recording between the step's kernels keeps
+ * the next kernel from starting early beside the indexer, so a step timed this
+ * way runs a little slower than one that is not.  Both null: off.  The setting
+ * is per host thread.
+ *
+ *   begin, end   cudaEvent_t (created by the caller), or both null.
+ */
+csa2_status csa2_profile_events(void *begin, void *end);
+
+/*
  * csa2_workspace_size -- scratch bytes needed by an operation.
  *   op = CSA2_OP_TOPK:        n_q queries, n_items = items per row (entries,
  *                             blocks, or 16384 pool slots), k.

@@ -95,6 +95,8 @@ def test_host_validation_rejects_before_launch(lib):
     assert reindex(1024, fake + 2, 1 << 30) == INVALID
     assert reindex(1000, fake, 1 << 30) == INVALID
     assert reindex(1024, fake, 1024) == WS
+    assert L.csa2_profile_events(fake, None) == INVALID                                  # both or neither
+    assert L.csa2_profile_events(None, None) == 0
     assert L.csa2_check_bounded_wait(0, None) == INVALID                                 # limit out of range
     assert L.csa2_check_bounded_wait(2_000_001, None) == INVALID
     assert L.csa2_get_device_status(None, None) == INVALID
