@@ -759,17 +759,20 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
 // 32 heads each are the MMA's N = 32 G columns, and every key unit is read once
 // per group instead of once per query.  The accumulators are G times wider, so
 // units are 128 entries, with two accumulators of 32 G <= 192 TMEM columns
-// (MMA and epilogue overlap) and 20 stages of 8.5 KB in flight.
+// (MMA and epilogue overlap) and 20 stages of 8.5 KB in flight; a CTA takes
+// its units in adjacent pairs, each pair one bulk copy.
 // Roles (384 threads): warp 0 producer, warp 1 MMA issuer (lane 0) and TMEM
 // owner, warp 2 scale factors, warp 3 idle, warps 4..11 epilogue in two groups
-// of four taking alternate units (warp w: TMEM lane quarter w % 4).  A query's
+// of four taking alternate units (warp w: TMEM lane quarter w % 4), each group
+// reading only its own units' entries of the ring.  A query's
 // scale factors sit in TMEM as rows of B: head h of the group's query g (row
 // 32 g + h) at lane h, 32-bit word g (words 4..7 in the next four columns), as
 // the key rows of A do.
 constexpr int kMqUnit = 128;
 constexpr int kMqStages = 20;
-constexpr int kMqOffSFA = 8192;
-constexpr int kMqStageBytes = kMqOffSFA + 512;
+constexpr int kMqNibBytes = 8192;                             // a stage's nibbles: [stage][8 KB]
+constexpr int kMqStageBytes = kMqNibBytes + 512;               // and its key scales, after all nibbles
+constexpr int kMqSfaBase = kMqStages * kMqNibBytes;
 constexpr int kMqMaxG = 6;                                   // N = 32 G <= 192
 constexpr int kMqSlots = 2;
 constexpr int kMqQOffSFB = kMqMaxG * 2048;                    // then two 32 x 16-B scale blocks
@@ -780,14 +783,32 @@ constexpr int kMqThreads = 384;
 // kMqStages back, may run that far ahead of the MMA, and the epilogue trails
 // the MMA by up to two units, so the ring holds more than kMqStages + 2
 constexpr int kMqRing = 32;
-static_assert(kMqRing > kMqStages + 2, "ring of published units");
+static_assert(kMqRing > kMqStages + 3, "ring of published units (and the second end mark)");
 constexpr uint32_t kMqColSFA = 2 * kMqMaxG * 32;              // after the two accumulators
 constexpr uint32_t kMqColSFB = kMqColSFA + kMqStages * 4;
-static_assert(kMqStageBytes % 512 == 0 && kMqSlotBytes % 512 == 0, "64B-swizzled tiles need 512-B alignment");
+static_assert(kMqNibBytes % 512 == 0 && kMqSlotBytes % 512 == 0, "64B-swizzled tiles need 512-B alignment");
+static_assert(kMqStages % 2 == 0, "unit pairs take stages s, s + 1 with s even");
 static_assert(kMqColSFB + kMqSlots * 8 <= kScTmemCols, "TMEM columns");
 static_assert(kMqSmem + 1024 <= 227 * 1024, "shared memory");
 static_assert(kMqStages % 2 == 0, "a stage's done barrier also marks its accumulator full");
 static_assert(kMqMaxG == kMaxQueryGroup, "the query-group limit of the C ABI");
+
+// The group and unit of a schedule position T, for positions that only grow:
+// the division runs only when T leaves the current group (every role runs
+// this per unit, on sub-partitions shared with the epilogue's arithmetic).
+struct GroupOf {
+  uint32_t upq, base = 0;
+  int g = -1;
+  __device__ explicit GroupOf(uint32_t units_per_q) : upq(units_per_q) {}
+  __device__ int group(uint32_t T) {
+    if (g < 0 || T - base >= upq) {
+      g = (int)(T / upq);
+      base = (uint32_t)g * upq;
+    }
+    return g;
+  }
+  __device__ int unit(uint32_t T) const { return (int)(T - base); }
+};
 
 // G (the queries of a group) is a template parameter so that the epilogue's
 // loops over the queries unroll into independent running sums.
@@ -837,17 +858,32 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // The CTA's units come in adjacent pairs (2b, 2b + 1 for b = blockIdx.x,
+    // blockIdx.x + gridDim.x, ...), so that one bulk copy (16 KB) and one
+    // 16-B asynchronous copy per lane bring both, into stages s, s + 1 (s
+    // even), counted on stage s's barrier; the second stage's barrier then
+    // takes a plain arrival (its consumers wait on stage s's first, in order).
+    // The producer shares its sub-partition with two epilogue warps, and its
+    // instructions per unit set the kernel's pace when they are many (units of
+    // one at a time, a division per unit and two bulk copies: 312 us per
+    // 8 x 1M x 5 launch, against 261 us with the pairs and the steps below
+    // together), so it looks one unit ahead and does little per unit.
     const uint64_t policy = ptx::policy_evict_first();
     QuerySlotsT<kMqSlots> qs;
-    int cur_g = -1, seq = 0, nv_max = -1;
-    uint32_t T = blockIdx.x;
-    for (uint32_t it = 0;; it++) {
-      if (abort_flag) break;
-      int u = 0;
+    GroupOf go((uint32_t)P.units_per_q);
+    int cur_g = -1;
+    int64_t row_g = 0;                             // the looked-at group's first key row
+    int nv_max = -1;
+    struct Found {
+      uint32_t T;
+      int g;
+      int64_t r0;                                  // the unit's first key row
+    };
+    // the first valid unit at or after schedule position T
+    auto find = [&](uint32_t T) -> Found {
       for (;;) {
-        if (T >= total_units) { T = kDone; break; }
-        const int gi = (int)(T / (uint32_t)P.units_per_q);
-        u = (int)(T - (uint32_t)gi * (uint32_t)P.units_per_q);
+        if (T >= total_units) return Found{kDone, -1, 0};
+        const int gi = go.group(T), u = go.unit(T);
         if (gi != cur_g) {
           // the group's sequence (all G queries must share it) and its
           // longest visible length; a group breaking this is skipped
@@ -861,54 +897,83 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
           }
           if (sq < 0 || sq >= P.n_seq) ok = 0;
           if (!ok && lane == 0 && u == 0) record_error(P.status, CSA2_ERR_BOUNDS);
-          seq = sq;
+          row_g = (int64_t)sq * P.n_max;
           nv_max = ok ? nm : -1;
         }
-        if (nv_max >= 0 && u * kMqUnit < nv_max) break;
-        T += gridDim.x;
+        // a unit that starts before n_vis ends within n_max (n_max % 128 == 0)
+        if (nv_max >= 0 && u * kMqUnit < nv_max) return Found{T, gi, row_g + (int64_t)u * kMqUnit};
+        T = (T & 1u) ? T + 2u * gridDim.x - 1u : T + 1u;
       }
-      if (lane == 0) unit_ring[it % kMqRing] = ((unsigned long long)it << 32) | T;
-      if (T == kDone) break;
+    };
+    Found nx = find(2u * blockIdx.x);
+    bool second = false;                           // this unit's data came with the previous one's
+    for (uint32_t it = 0;; it++) {
+      if (abort_flag) break;
+      const Found cu = nx;
+      if (lane == 0) unit_ring[it % kMqRing] = ((unsigned long long)it << 32) | cu.T;
+      if (cu.T == kDone) {
+        // the end, also for the epilogue group that reads only the other entries
+        if (lane == 0) unit_ring[(it + 1) % kMqRing] = ((unsigned long long)(it + 1) << 32) | kDone;
+        break;
+      }
+      nx = find((cu.T & 1u) ? cu.T + 2u * gridDim.x - 1u : cu.T + 1u);
       const uint32_t s = it % kMqStages, r = it / kMqStages;
-      const bool fresh = qs.step(cur_g, (int)it);
-      if (!ptx::mbar_wait(&done_bar[s], (r & 1) ^ 1)) { fail(); break; }
+      const bool fresh = qs.step(cu.g, (int)it);
+      if (second) {
+        second = false;
+        if (lane == 0) {
+          ptx::mbar_arrive(&full_bar[s]);
+          armed_sh = (int)it + 1;
+        }
+        __syncwarp();
+        continue;
+      }
+      // a pair: the next unit is adjacent, in the same group (so not a fresh one)
+      const bool pair = (s & 1u) == 0u && nx.T == cu.T + 1u && nx.g == cu.g;
+      // stage s (and s + 1) free: MMAs complete in order, so the later suffices
+      if (!ptx::mbar_wait(&done_bar[pair ? s + 1 : s], (r & 1) ^ 1)) { fail(); break; }
       if (fresh) {
         // the slot's previous user (MMAs complete in order: its last unit)
         const int pu = qs.prev_user();
         if (pu >= 0 && pu + kMqStages > (int)it &&
             !ptx::mbar_wait(&done_bar[pu % kMqStages], (uint32_t)(pu / kMqStages) & 1)) { fail(); break; }
       }
-      unsigned char *st = smem + s * kMqStageBytes;
       unsigned char *qd = qslots + qs.slot * kMqSlotBytes;
+      // the units' key scales (512 B each) come as the lanes' 16-B asynchronous
+      // copies, each lane counted into the stage's barrier, not as more bulk
+      // copies: the bulk-copy unit spends a fixed time per instruction
+      const unsigned char *ks = P.key_scale + cu.r0 * 4;
+      ptx::cp_async16(smem + kMqSfaBase + s * 512 + lane * 16, ks + lane * 16);
+      if (pair) ptx::cp_async16(smem + kMqSfaBase + s * 512 + 512 + lane * 16, ks + 512 + lane * 16);
+      ptx::cp_async_arrive(&full_bar[s]);
+      __syncwarp();
       if (lane == 0) {
+        const uint32_t nbytes = pair ? 16384u : 8192u;
         const uint32_t qbytes = fresh ? (uint32_t)G * (2048 + 128) : 0u;
-        ptx::mbar_arrive_expect_tx(&full_bar[s], 8192u + 512u + qbytes);
+        ptx::mbar_arrive_expect_tx(&full_bar[s], nbytes + qbytes);
         if (fresh) {
-          const int64_t q0 = (int64_t)cur_g * G;
+          const int64_t q0 = (int64_t)cu.g * G;
           ptx::bulk_load(qd, P.q_nib + q0 * kIdxHeads * 64, (uint32_t)G * 2048, &full_bar[s]);
           ptx::bulk_load(qd + kMqQOffSFB, P.q_scale + q0 * kIdxHeads * 4, (uint32_t)G * 128, &full_bar[s]);
         }
-        // a unit that starts before n_vis ends within n_max (n_max % 128 == 0)
-        const int64_t r0 = (int64_t)seq * P.n_max + (int64_t)u * kMqUnit;
-        ptx::bulk_load_hint(st, P.key_nib + r0 * 64, 8192u, &full_bar[s], policy);
-        ptx::bulk_load(st + kMqOffSFA, P.key_scale + r0 * 4, 512u, &full_bar[s]);
+        ptx::bulk_load_hint(smem + s * kMqNibBytes, P.key_nib + cu.r0 * 64, nbytes, &full_bar[s], policy);
+        armed_sh = (int)it + 1;
       }
       __syncwarp();
-      if (lane == 0) armed_sh = (int)it + 1;
-      T += gridDim.x;
+      second = pair;
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ scale-factor warp
     QuerySlotsT<kMqSlots> qs;
+    GroupOf go((uint32_t)P.units_per_q);
     for (uint32_t it = 0;; it++) {
       if (abort_flag) break;
       uint32_t T;
       if (!ring_get<kMqRing>(unit_ring, it, T, abort_flag)) { fail(); break; }
       if (T == kDone) break;
       const uint32_t s = it % kMqStages, r = it / kMqStages;
-      const bool fresh = qs.step((int)(T / (uint32_t)P.units_per_q), (int)it);
+      const bool fresh = qs.step(go.group(T), (int)it);
       if (!ptx::mbar_wait(&full_bar[s], r & 1)) { fail(); break; }
-      unsigned char *st = smem + s * kMqStageBytes;
       unsigned char *qd = qslots + qs.slot * kMqSlotBytes;
       if (fresh) {
         // the queries' scales, [g][head] words as loaded -> block g / 4, line
@@ -922,7 +987,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
         for (int g = 0; g < 8; g++) sfb[(g >> 2) * 128 + lane * 4 + (g & 3)] = vb[g];
       }
       // key scales -> tcgen05.cp layout: 16-B line m0 holds rows m0, m0+32, m0+64, m0+96
-      uint32_t *sfa = reinterpret_cast<uint32_t *>(st + kMqOffSFA);
+      uint32_t *sfa = reinterpret_cast<uint32_t *>(smem + kMqSfaBase + s * 512);
       uint32_t va[4];
 #pragma unroll
       for (int i = 0; i < 4; i++) va[i] = sfa[i * 32 + lane];
@@ -948,16 +1013,17 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
     if (lane == 0) {
       const uint32_t idesc0 = idesc_mxf4_m128(0, N), idesc1 = idesc_mxf4_m128(2, N);
       QuerySlotsT<kMqSlots> qs;
+      GroupOf go((uint32_t)P.units_per_q);
       for (uint32_t it = 0;; it++) {
         if (abort_flag) break;
         uint32_t T;
         if (!ring_get<kMqRing>(unit_ring, it, T, abort_flag)) { fail(); break; }
         if (T == kDone) break;
-        qs.step((int)(T / (uint32_t)P.units_per_q), (int)it);
+        qs.step(go.group(T), (int)it);
         const uint32_t s = it % kMqStages, r = it / kMqStages, a = it & 1, ra = it >> 1;
         if (!ptx::mbar_wait(&sf_bar[s], r & 1) || !ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) { fail(); break; }
         ptx::tc_fence_after();
-        const uint64_t ad = ptx::smem_desc(ptx::smem_u32(smem + s * kMqStageBytes), 16, 512, 4);
+        const uint64_t ad = ptx::smem_desc(ptx::smem_u32(smem + s * kMqNibBytes), 16, 512, 4);
         const uint64_t bd = ptx::smem_desc(ptx::smem_u32(qslots + qs.slot * kMqSlotBytes), 16, 512, 4);
         const uint32_t t_sfa = tmem + kMqColSFA + s * 4, t_sfb = tmem + kMqColSFB + qs.slot * 8;
         const uint32_t d = tmem + a * N;
@@ -981,13 +1047,13 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
     float *wsm = w_sm[warp - 4];
     int cur_gi = -1;
     int nvq[G];
-    for (uint32_t it = 0;; it++) {
+    GroupOf go((uint32_t)P.units_per_q);
+    for (uint32_t it = grp;; it += 2) {             // this group's units only
       if (abort_flag) break;
       uint32_t T;
       if (!ring_get<kMqRing>(unit_ring, it, T, abort_flag)) { fail(); break; }
       if (T == kDone) break;
-      if ((it & 1) != grp) continue;
-      const int gi = (int)(T / (uint32_t)P.units_per_q), u = (int)(T % (uint32_t)P.units_per_q);
+      const int gi = go.group(T), u = go.unit(T);
       const uint32_t s = it % kMqStages, r = it / kMqStages;
       if (gi != cur_gi) {
         for (int i = lane; i < G * 32; i += 32) wsm[i] = __ldg(P.w + (int64_t)gi * G * kIdxHeads + i);
@@ -1002,7 +1068,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
       const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + grp * N;
       // up to three queries at a time: their 32 columns each in one load
       // apiece and one wait (each TMEM round trip costs hundreds of cycles),
-      // then one running sum per query, heads in order
+      // then four running sums per query
 #pragma unroll
       for (int g0 = 0; g0 < G; g0 += 3) {
         constexpr int kB = 3;
@@ -1012,18 +1078,25 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
         for (int b = 0; b < kB; b++)
           if (b < nb) ptx::tmem_ld_32x32b_x32(ta + (g0 + b) * 32, d[b]);
         ptx::tmem_wait_ld();
-        // two running sums per query (heads 4i, 4i+1 and 4i+2, 4i+3)
-        float acc[kB][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+        // four running sums per query (heads i mod 4), as two pairs: the
+        // packed two-lane FMA halves the FMA instructions (the epilogue's
+        // arithmetic, 160 ReLU-weight-add steps per entry at G = 5, is what
+        // the units wait on once the producer keeps ahead)
+        float2 acc[kB][2];
+#pragma unroll
+        for (int b = 0; b < kB; b++) acc[b][0] = acc[b][1] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 8; i++) {
 #pragma unroll
           for (int b = 0; b < kB; b++) {
             if (b < nb) {
               const float4 wv = reinterpret_cast<const float4 *>(wsm + (g0 + b) * kIdxHeads)[i];
-              acc[b][0] = fmaf(wv.x, fmaxf(__uint_as_float(d[b][4 * i]), 0.f), acc[b][0]);
-              acc[b][0] = fmaf(wv.y, fmaxf(__uint_as_float(d[b][4 * i + 1]), 0.f), acc[b][0]);
-              acc[b][1] = fmaf(wv.z, fmaxf(__uint_as_float(d[b][4 * i + 2]), 0.f), acc[b][1]);
-              acc[b][1] = fmaf(wv.w, fmaxf(__uint_as_float(d[b][4 * i + 3]), 0.f), acc[b][1]);
+              const float2 r01 = make_float2(fmaxf(__uint_as_float(d[b][4 * i]), 0.f),
+                                             fmaxf(__uint_as_float(d[b][4 * i + 1]), 0.f));
+              const float2 r23 = make_float2(fmaxf(__uint_as_float(d[b][4 * i + 2]), 0.f),
+                                             fmaxf(__uint_as_float(d[b][4 * i + 3]), 0.f));
+              acc[b][0] = __ffma2_rn(make_float2(wv.x, wv.y), r01, acc[b][0]);
+              acc[b][1] = __ffma2_rn(make_float2(wv.z, wv.w), r23, acc[b][1]);
             }
           }
         }
@@ -1031,7 +1104,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
         for (int b = 0; b < kB; b++) {
           if (b < nb) {
             const int q = gi * G + g0 + b;
-            if (e < nvq[g0 + b]) P.scores[(int64_t)q * P.stride + e] = acc[b][0] + acc[b][1];
+            if (e < nvq[g0 + b]) P.scores[(int64_t)q * P.stride + e] = (acc[b][0].x + acc[b][0].y) + (acc[b][1].x + acc[b][1].y);
           }
         }
       }
@@ -1044,6 +1117,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
   if (abort_flag) {
     // a wait ran out: as in the single-query kernel, the producer's last
     // copies and the issuers' tcgen05 operations finish before TMEM goes back
+    if (warp == 0) asm volatile("cp.async.wait_all;" ::: "memory");
     if (warp == 0 && lane == 0) {
       for (int i = max(0, armed_sh - kMqStages); i < armed_sh; i++)
         ptx::mbar_wait(&full_bar[i % kMqStages], (uint32_t)(i / kMqStages) & 1);
