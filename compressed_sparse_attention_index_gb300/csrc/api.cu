@@ -489,6 +489,20 @@ csa2_status csa2_decode_mq(const void *key_nib, const void *key_scale, int64_t n
                                   swa_cnt, n_q, out, out_dtype, sm_scale, rope_base, ws_attn, st, s));
 }
 
+// The device address of page-locked host memory (under unified addressing
+// the same as the host's, for memory from cudaHostAlloc / cudaMallocHost or
+// registered with cudaHostRegister); false for pageable memory.
+static bool device_accessible_host(const void *h, const void **d) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+    (void)cudaGetLastError();                      // (an unknown pointer: not an error of the call)
+    return false;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return false;
+  *d = a.devicePointer;
+  return true;
+}
+
 csa2_status csa2_decode_host(const void *key_nib, const void *key_scale, int64_t n_max, int n_seq, const void *kv_cache,
                              const void *swa_cache, int swa_cap, const void *h_q, const void *h_qidx, const float *h_w,
                              const int32_t *h_desc, int n_q, int32_t *h_sel, void *h_out, int out_dtype,
@@ -509,22 +523,52 @@ csa2_status csa2_decode_host(const void *key_nib, const void *key_scale, int64_t
   const size_t b_w = (size_t)n_q * kIdxHeads * 4, b_desc = (size_t)n_q * 5 * 4;
   const size_t b_out = (size_t)n_q * kHeads * kDim * (out_dtype == CSA2_OUT_F32 ? 4 : 2);
   const size_t b_sel = (size_t)n_q * kTopK * 4;
-  // the step's inputs: one copy per host buffer
-  if (cudaMemcpyAsync(st + H.q, h_q, b_q, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(st + H.qidx, h_qidx, b_qidx, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(st + H.w, h_w, b_w, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(st + H.desc, h_desc, b_desc, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return CSA2_ERR_CUDA;
-  csa2_status r = csa2_fp4_pack(CSA2_IDX_MXFP4, st + H.qidx, (int64_t)n_q * kIdxHeads, 1, nullptr, st + H.qnib,
-                                st + H.qsc, stream);
-  if (r != CSA2_OK) return r;
+  // the step's inputs: from page-locked host memory, read by one grid that
+  // also packs the indexer query (no copy engine round trip per buffer);
+  // from pageable memory, one copy per host buffer and the packing kernel
+  const void *dq = nullptr, *dqidx = nullptr, *dw = nullptr, *ddesc = nullptr;
+  if (device_accessible_host(h_q, &dq) && device_accessible_host(h_qidx, &dqidx) &&
+      device_accessible_host(h_w, &dw) && device_accessible_host(h_desc, &ddesc) && aligned(dqidx, 16) &&
+      aligned(dq, 4) && aligned(dw, 4) && aligned(ddesc, 4)) {
+    StageIn S;
+    S.qidx = static_cast<const uint16_t *>(dqidx);
+    S.qidx_rows = (int64_t)n_q * kIdxHeads;
+    S.qnib = st + H.qnib;
+    S.qsc = st + H.qsc;
+    const void *src[3] = {dq, dw, ddesc};
+    void *dst[3] = {st + H.q, st + H.w, st + H.desc};
+    const size_t bytes[3] = {b_q, b_w, b_desc};
+    for (int k = 0; k < 3; k++) {
+      S.src[k] = src[k];
+      S.dst[k] = dst[k];
+      S.wide[k] = aligned(src[k], 16) && bytes[k] % 16 == 0 ? 1 : 0;
+      S.units[k] = (int64_t)(bytes[k] / (S.wide[k] ? 16 : 4));
+    }
+    if (launch_stage_host_inputs(S, s) != cudaSuccess) return CSA2_ERR_CUDA;
+  } else {
+    if (cudaMemcpyAsync(st + H.q, h_q, b_q, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(st + H.qidx, h_qidx, b_qidx, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(st + H.w, h_w, b_w, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(st + H.desc, h_desc, b_desc, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return CSA2_ERR_CUDA;
+    const csa2_status r = csa2_fp4_pack(CSA2_IDX_MXFP4, st + H.qidx, (int64_t)n_q * kIdxHeads, 1, nullptr,
+                                        st + H.qnib, st + H.qsc, stream);
+    if (r != CSA2_OK) return r;
+  }
   const int32_t *d = reinterpret_cast<const int32_t *>(st + H.desc);
-  r = csa2_decode(key_nib, key_scale, n_max, n_seq, st + H.qnib, st + H.qsc, reinterpret_cast<const float *>(st + H.w),
+  // a page-locked output buffer takes the output straight from the grid that
+  // finishes it; otherwise the output goes through the staging and a copy
+  const void *dout = nullptr;
+  const bool out_direct = device_accessible_host(h_out, &dout) && aligned(dout, 16);
+  const csa2_status r =
+      csa2_decode(key_nib, key_scale, n_max, n_seq, st + H.qnib, st + H.qsc, reinterpret_cast<const float *>(st + H.w),
                   d, d + n_q, n_q, st + H.q, kv_cache, swa_cache, swa_cap, d + 2 * n_q, d + 3 * n_q, d + 4 * n_q,
-                  reinterpret_cast<int32_t *>(st + H.sel), st + H.out, out_dtype, params, workspace, dec, stream);
+                  reinterpret_cast<int32_t *>(st + H.sel), out_direct ? const_cast<void *>(dout) : st + H.out,
+                  out_dtype, params, workspace, dec, stream);
   if (r != CSA2_OK) return r;
-  // the step's outputs: one copy per host buffer
-  if (cudaMemcpyAsync(h_out, st + H.out, b_out, cudaMemcpyDeviceToHost, s) != cudaSuccess) return CSA2_ERR_CUDA;
+  // the step's other outputs: one copy per host buffer
+  if (!out_direct && cudaMemcpyAsync(h_out, st + H.out, b_out, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return CSA2_ERR_CUDA;
   if (h_sel != nullptr && cudaMemcpyAsync(h_sel, st + H.sel, b_sel, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return CSA2_ERR_CUDA;
   return CSA2_OK;

@@ -142,6 +142,23 @@ struct FusedTopk {
 cudaError_t launch_pack(int kind, const void *src, int64_t rows, int m, const float *gate, void *dst,
                         void *dst_scales, cudaStream_t st, void *pooled = nullptr);
 
+// csa2_decode_host's inputs from page-locked host memory (device-accessible
+// addresses): the indexer query rows (bf16 [qidx_rows][128]) packed into qnib
+// / qsc, and up to three segments copied (units[k] units of 16 B when wide[k],
+// else of 4 B; src and dst aligned to the unit).  One grid; pack_ctas is set
+// by the launch.
+struct StageIn {
+  const uint16_t *qidx;
+  int64_t qidx_rows;
+  uint8_t *qnib, *qsc;
+  const void *src[3];
+  void *dst[3];
+  int64_t units[3];
+  int wide[3];
+  int pack_ctas;
+};
+cudaError_t launch_stage_host_inputs(StageIn S, cudaStream_t st);
+
 // The indexer keys of rows bf16 latents under the 512 -> 128 bf16 weights
 // w ([128][512]): out [rows][128] bf16 (tcgen05, fp32 accumulation).
 cudaError_t launch_proj_keys(const void *x, int64_t rows, const void *w, void *out, int *status, cudaStream_t st);

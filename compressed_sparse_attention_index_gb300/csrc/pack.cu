@@ -193,10 +193,11 @@ __device__ __forceinline__ int pow2_exp_fp8(float amax) {   // lim = 448 = 1.75 
 // lane pair (2g, 2g+1) shares E8M0 group g.  The nibble row is stored in the
 // 64-byte swizzled order (see include/csa2.h) so that the indexer can move
 // whole tiles with one bulk copy.
-__global__ void __launch_bounds__(256) pack_idx_kernel(const uint16_t *__restrict__ src, int64_t rows,
-                                                        uint8_t *__restrict__ nib_out,
-                                                        uint8_t *__restrict__ sc_out) {
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+// The part of one thread t (row t / 8, channels 16 (t % 8) ..): HOST reads
+// the row from page-locked host memory (fetched anew, not from a cache).
+template <bool HOST>
+__device__ __forceinline__ void pack_idx_part(const uint16_t *__restrict__ src, int64_t rows, int64_t t,
+                                              uint8_t *__restrict__ nib_out, uint8_t *__restrict__ sc_out) {
   const int64_t row = t >> 3;
   const int part = (int)(t & 7);
   const bool live = row < rows;
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(256) pack_idx_kernel(const uint16_t *__restric
   float amax = 0.f;
   if (live) {
     const uint4 *p = reinterpret_cast<const uint4 *>(src + row * kIdxDim + part * 16);
-    uint4 a = __ldg(p), b = __ldg(p + 1);
+    uint4 a = HOST ? __ldcv(p) : __ldg(p), b = HOST ? __ldcv(p + 1) : __ldg(p + 1);
     uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int i = 0; i < 8; i++) { x[2 * i] = bf16_lo(w[i]); x[2 * i + 1] = bf16_hi(w[i]); }
@@ -229,6 +230,59 @@ __global__ void __launch_bounds__(256) pack_idx_kernel(const uint16_t *__restric
   const uint32_t chunk = ((uint32_t)part >> 1) ^ (uint32_t)((reinterpret_cast<uintptr_t>(rowp) >> 7) & 3u);
   *reinterpret_cast<uint2 *>(rowp + chunk * 16 + (part & 1) * 8) = make_uint2(nib[0], nib[1]);
   if ((part & 1) == 0) sc_out[row * kIdxScaleBytes + (part >> 1)] = (uint8_t)scale_byte;
+}
+
+__global__ void __launch_bounds__(256) pack_idx_kernel(const uint16_t *__restrict__ src, int64_t rows,
+                                                        uint8_t *__restrict__ nib_out,
+                                                        uint8_t *__restrict__ sc_out) {
+  pack_idx_part<false>(src, rows, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, nib_out, sc_out);
+}
+
+// ------------------------------------------------------------------ host-input staging
+// csa2_decode_host's per-step inputs read straight from page-locked host
+// memory (device-accessible at the same address under unified addressing),
+// in one grid instead of one copy per buffer plus the packing kernel: the
+// first pack_ctas CTAs pack the indexer query (as pack_idx_kernel), the rest
+// copy the other segments (16-B units; 4-B units where a segment's size or
+// address is not a multiple of 16).  Every thread loads its first unit before
+// the grid-dependency wait and stores it after.
+__global__ void __launch_bounds__(256) stage_host_inputs_kernel(StageIn S) {
+  if ((int)blockIdx.x < S.pack_ctas) {
+    griddep_wait();
+    pack_idx_part<true>(S.qidx, S.qidx_rows, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, S.qnib, S.qsc);
+    return;
+  }
+  const int64_t total = S.units[0] + S.units[1] + S.units[2];
+  const int64_t stride = (int64_t)(gridDim.x - S.pack_ctas) * blockDim.x;
+  auto locate = [&](int64_t i, int &k, int64_t &u) {
+    k = 0;
+    u = i;
+    while (k < 2 && u >= S.units[k]) { u -= S.units[k]; k++; }
+  };
+  auto load = [&](int k, int64_t u) -> uint4 {
+    if (S.wide[k]) return __ldcv(static_cast<const uint4 *>(S.src[k]) + u);
+    return make_uint4(__ldcv(static_cast<const unsigned int *>(S.src[k]) + u), 0u, 0u, 0u);
+  };
+  auto store = [&](int k, int64_t u, uint4 v) {
+    if (S.wide[k]) static_cast<uint4 *>(S.dst[k])[u] = v;
+    else static_cast<unsigned int *>(S.dst[k])[u] = v.x;
+  };
+  int64_t i = (int64_t)(blockIdx.x - S.pack_ctas) * blockDim.x + threadIdx.x;
+  int k0 = 0;
+  int64_t u0 = 0;
+  uint4 v0 = make_uint4(0u, 0u, 0u, 0u);
+  if (i < total) {
+    locate(i, k0, u0);
+    v0 = load(k0, u0);
+  }
+  griddep_wait();
+  if (i < total) store(k0, u0, v0);
+  for (i += stride; i < total; i += stride) {
+    int k;
+    int64_t u;
+    locate(i, k, u);
+    store(k, u, load(k, u));
+  }
 }
 
 // ------------------------------------------------------------------ SWA (S3)
@@ -283,6 +337,16 @@ cudaError_t launch_pack(int kind, const void *src, int64_t rows, int m, const fl
     pack_swa_kernel<<<(unsigned)blocks, 256, 0, st>>>(s, rows, (uint8_t *)dst);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_stage_host_inputs(StageIn S, cudaStream_t st) {
+  S.pack_ctas = (int)((S.qidx_rows * 8 + 255) / 256);
+  int64_t units = 0;
+  for (int k = 0; k < 3; k++) units += S.units[k];
+  const int64_t copy_ctas = (units + 255) / 256;
+  const int64_t cap = 8 * (int64_t)device_sm_count(current_device());
+  const int64_t grid = S.pack_ctas + (copy_ctas < cap ? copy_ctas : cap);
+  return launch_pdl(stage_host_inputs_kernel, dim3((unsigned)grid), dim3(256), 0, st, 1u, S);
 }
 
 }  // namespace csa2

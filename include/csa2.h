@@ -353,12 +353,17 @@ csa2_status csa2_decode_mq(const void *key_nib, const void *key_scale, int64_t n
  * csa2_decode_host -- csa2_decode with the step's inputs and outputs in host
  * memory: the end-to-end call of a decode step.  The caches (indexer keys,
  * latents, window) stay resident in device memory; the per-step tensors
- * travel with the call.  On `stream`, in order: one cudaMemcpyAsync per host
- * input buffer into the workspace, csa2_fp4_pack of the indexer query,
- * csa2_decode, one cudaMemcpyAsync per host output buffer.  Asynchronous:
- * the host buffers must stay valid (and the outputs unread) until the stream
- * has passed the call; pinned (page-locked) host memory makes the copies
- * asynchronous and fast, pageable memory works but serialises them.
+ * travel with the call.  On `stream`, in order: the inputs into the
+ * workspace -- where all four input buffers are page-locked (cudaHostAlloc,
+ * cudaMallocHost, cudaHostRegister: device-accessible under unified
+ * addressing), one kernel reads them in place and packs the indexer query;
+ * otherwise one cudaMemcpyAsync per buffer and csa2_fp4_pack --, then
+ * csa2_decode, whose last grid writes the output straight into h_out where
+ * that is page-locked (else into the workspace, then one cudaMemcpyAsync),
+ * then one cudaMemcpyAsync into h_sel, if given.  Either way the results are
+ * the same.  Asynchronous: the host buffers must stay valid
+ * and unchanged (and the outputs unread) until the stream has passed the
+ * call; pageable memory works but serialises the copies.
  *
  *   key_nib .. n_seq, kv_cache, swa_cache, swa_cap   (device) as csa2_decode.
  *   h_q        (host) bf16 [n_q][64][512], the attention query (rotated).

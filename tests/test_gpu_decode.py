@@ -519,10 +519,12 @@ def test_window_longer_than_ring_is_rejected(lib, oracle_lib):
 
 
 @pytest.mark.parametrize("out_f32", [False, True])
-def test_decode_host_equals_device_call(lib, out_f32):
-    """csa2_decode_host (inputs and outputs in pinned host memory, copied
-    inside the call) gives exactly csa2_decode's selection and output, on a
-    garbage-filled workspace and on a second call."""
+@pytest.mark.parametrize("pinned", [True, False])
+def test_decode_host_equals_device_call(lib, out_f32, pinned):
+    """csa2_decode_host (inputs and outputs in host memory: page-locked,
+    read in place by the staging kernel, or pageable, copied) gives exactly
+    csa2_decode's selection and output, on a garbage-filled workspace and on a
+    second call with changed inputs."""
     import compressed_sparse_attention_index_gb300 as C
     from gen import inputs as G
     wl = small(n_seq=3, n_entries=65536, seed=252)
@@ -533,22 +535,29 @@ def test_decode_host_equals_device_call(lib, out_f32):
     from compressed_sparse_attention_index_gb300 import decode
     decode.fused_decode(dw, ref)
     qidx = np.concatenate([G.normal_block_bf16(wl.seed, G.S_QIDX, qi, 0, 32, 128) for qi in range(n_q)])
-    h_q = dw.q.cpu().pin_memory()
-    h_qidx = torch.from_numpy(qidx.view(np.int16)).pin_memory()
-    h_w = dw.w.cpu().pin_memory()
-    h_desc = torch.stack([dw.q_seq, dw.n_vis, dw.pos, dw.swa_first, dw.swa_cnt]).cpu().contiguous().pin_memory()
-    h_sel = torch.full((n_q, 512), -7, dtype=torch.int32).pin_memory()
-    h_out = torch.full(tuple(ref.out.shape), 7, dtype=ref.out.dtype).pin_memory()
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
+    h_q = pin(dw.q.cpu())
+    h_qidx = pin(torch.from_numpy(qidx.view(np.int16)))
+    h_w = pin(dw.w.cpu())
+    h_desc = pin(torch.stack([dw.q_seq, dw.n_vis, dw.pos, dw.swa_first, dw.swa_cnt]).cpu().contiguous())
+    h_sel = pin(torch.full((n_q, 512), -7, dtype=torch.int32))
+    h_out = pin(torch.full(tuple(ref.out.shape), 7, dtype=ref.out.dtype))
     wsb = C.csa2_workspace_size(C.CSA2_OP_DECODE_HOST, n_q, dw.n_max, 512)
     ws = torch.full((wsb,), 0xA5, dtype=torch.uint8, device="cuda")
-    for _ in range(2):
+    q_true = h_q.clone()
+    for it in range(3):
+        # the first call sees a zero attention query (its output is not
+        # compared); the later ones the true one, so that a stale read of the
+        # host buffer would show
+        h_q.copy_(torch.zeros_like(q_true) if it == 0 else q_true)
         C.csa2_decode_host(dw.key_nib, dw.key_scale, dw.n_max, dw.kv.shape[0], dw.kv, dw.swa, dw.swa.shape[1], h_q,
                            h_qidx, h_w, h_desc, n_q, h_sel, h_out, dt, None, ws, wsb)
         torch.cuda.synchronize()
         assert lib.csa2_get_device_status() == 0
         assert torch.equal(h_sel, ref.sel.cpu())
-        assert torch.equal(h_out.view(torch.int16 if not out_f32 else torch.int32),
-                           ref.out.cpu().view(torch.int16 if not out_f32 else torch.int32))
+        if it > 0:
+            assert torch.equal(h_out.view(torch.int16 if not out_f32 else torch.int32),
+                               ref.out.cpu().view(torch.int16 if not out_f32 else torch.int32))
         h_out.fill_(7)
 
 
