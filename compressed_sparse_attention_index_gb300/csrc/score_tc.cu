@@ -1104,7 +1104,8 @@ __global__ void __launch_bounds__(kMqThreads, 1) index_score_mq_kernel(ScoreTcAr
         for (int b = 0; b < kB; b++) {
           if (b < nb) {
             const int q = gi * G + g0 + b;
-            if (e < nvq[g0 + b]) P.scores[(int64_t)q * P.stride + e] = (acc[b][0].x + acc[b][0].y) + (acc[b][1].x + acc[b][1].y);
+            if (e < nvq[g0 + b])
+              P.scores[(int64_t)q * P.stride + e] = (acc[b][0].x + acc[b][0].y) + (acc[b][1].x + acc[b][1].y);
           }
         }
       }
