@@ -175,12 +175,16 @@ static HostStage host_stage(int n_q) {
 }
 
 // csa2_build_cache's workspace for one chunk of entries: the keys (bf16
-// [chunk][128]) and, for m = 2, the pooled latents (bf16 [chunk][512]).
+// [chunk][128]) and, for m = 2, the pooled latents (bf16 [chunk][512]), two
+// counts (256 B) and the pooling's fix-up list (uint32 [chunk * 4]: up to
+// four of an entry's 32 channel blocks on average).
 constexpr int64_t kBuildChunk = 131072;
+constexpr int kBuildFixPerEntry = 4;
 static size_t build_cache_workspace_bytes(int64_t n_tokens, int m) {
   const int64_t entries = n_tokens / m;
   const int64_t c = entries < kBuildChunk ? entries : kBuildChunk;
-  return round256((size_t)c * kIdxDim * 2) + (m == 2 ? round256((size_t)c * kDim * 2) : 0);
+  return round256((size_t)c * kIdxDim * 2) +
+         (m == 2 ? round256((size_t)c * kDim * 2) + 256 + round256((size_t)c * kBuildFixPerEntry * 4) : 0);
 }
 
 // csa2_decode_reindex's workspace: pool scores [n_q][16384] fp32 | block
@@ -603,15 +607,24 @@ csa2_status csa2_build_cache(const void *tokens, int64_t n_tokens, int m, const 
   const cudaStream_t s = (cudaStream_t)stream;
   const int64_t entries = n_tokens / m;
   uint16_t *keys = static_cast<uint16_t *>(workspace);
+  const int64_t c = entries < kBuildChunk ? entries : kBuildChunk;   // (the workspace's chunk)
   uint16_t *pooled = m == 2 ? reinterpret_cast<uint16_t *>(static_cast<unsigned char *>(workspace) +
-                                                           round256((size_t)kBuildChunk * kIdxDim * 2))
+                                                           round256((size_t)c * kIdxDim * 2))
                             : nullptr;
+  // m = 2: the pooling's fix-up list and its two counts (one per parity of the
+  // chunk; each chunk's fix-up grid zeroes the next chunk's)
+  uint32_t *fix_cnt = m == 2 ? reinterpret_cast<uint32_t *>(pooled + (size_t)round256((size_t)c * kDim * 2) / 2)
+                             : nullptr;
+  uint32_t *fix_list = m == 2 ? fix_cnt + 64 : nullptr;
+  if (m == 2 && cudaMemsetAsync(fix_cnt, 0, 2 * sizeof(uint32_t), s) != cudaSuccess) return CSA2_ERR_CUDA;
   const uint16_t *tok = static_cast<const uint16_t *>(tokens);
-  for (int64_t e0 = 0; e0 < entries; e0 += kBuildChunk) {
+  for (int64_t e0 = 0, k = 0; e0 < entries; e0 += kBuildChunk, k++) {
     const int64_t ne = entries - e0 < kBuildChunk ? entries - e0 : kBuildChunk;
     // the chunk's latents (m = 2: pooled into the workspace) and main-cache records
-    cudaError_t e = launch_pack(CSA2_KV_NVFP4, tok + e0 * m * kDim, ne * m, m, m == 2 ? gate_logits + e0 * 2 * kDim : nullptr,
-                                static_cast<uint8_t *>(kv) + e0 * kKvBytes, nullptr, s, pooled);
+    const KvFix fix = {fix_cnt + (k & 1), fix_list, (uint32_t)(c * kBuildFixPerEntry), fix_cnt + ((k + 1) & 1)};
+    cudaError_t e = launch_pack(CSA2_KV_NVFP4, tok + e0 * m * kDim, ne * m, m,
+                                m == 2 ? gate_logits + e0 * 2 * kDim : nullptr,
+                                static_cast<uint8_t *>(kv) + e0 * kKvBytes, nullptr, s, pooled, m == 2 ? &fix : nullptr);
     if (e != cudaSuccess) return CSA2_ERR_CUDA;
     // their keys, then the keys' records (e0 is a multiple of 8: the key plane's swizzle holds per chunk)
     e = launch_proj_keys(m == 2 ? static_cast<const void *>(pooled) : static_cast<const void *>(tok + e0 * kDim), ne,

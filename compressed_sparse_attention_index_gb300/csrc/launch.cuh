@@ -138,9 +138,19 @@ struct FusedTopk {
   int reserve;
 };
 
-// pooled (KV, m = 2, optional): also write the pooled bf16 latents, [rows / 2][512]
+// The KV pack's fix-up list (m = 2): the (row, lane block) pairs, row * 32 +
+// block, whose fp64 recomputation a second grid does; cnt zero on entry;
+// next_cnt (optional) zeroed by that grid, for the next launch.
+struct KvFix {
+  uint32_t *cnt;
+  uint32_t *list;
+  uint32_t cap;
+  uint32_t *next_cnt;
+};
+// pooled (KV, m = 2, optional): also write the pooled bf16 latents, [rows / 2][512];
+// fix (KV, m = 2, optional): defer the fp64 recomputations to a fix-up grid
 cudaError_t launch_pack(int kind, const void *src, int64_t rows, int m, const float *gate, void *dst,
-                        void *dst_scales, cudaStream_t st, void *pooled = nullptr);
+                        void *dst_scales, cudaStream_t st, void *pooled = nullptr, const KvFix *fix = nullptr);
 
 // csa2_decode_host's inputs from page-locked host memory (device-accessible
 // addresses): the indexer query rows (bf16 [qidx_rows][128]) packed into qnib

@@ -69,91 +69,93 @@ __device__ __forceinline__ uint32_t bf16_from_f64(double v) {
 // ------------------------------------------------------------------ KV (S1)
 // One warp per output row; lane g packs channels [16g, 16g+16).  pooled
 // (M = 2, optional): the pooled bf16 latents as well, [rows_out][512].
-template <int M>
-__global__ void __launch_bounds__(256) pack_kv_kernel(const uint16_t *__restrict__ src,
-                                                       const float *__restrict__ gate, int64_t rows_out,
-                                                       uint8_t *__restrict__ dst, uint16_t *__restrict__ pooled) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= rows_out) return;
-  float x[16];
-  if (M == 1) {
-    const uint4 *p = reinterpret_cast<const uint4 *>(src + row * kDim + lane * 16);
-    uint4 a = __ldg(p), b = __ldg(p + 1);
-    uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+//
+// M = 2: gated pooling of tokens 2*row and 2*row+1, rounded once to bf16: the
+// exact value's rounding.  With the larger logit's token t_m, the other t_o,
+// e = exp(-|z_a - z_b|) and s = e / (1 + e), the value is t_m + (t_o - t_m) s.
+// fp32 first, one FMA: expf is within 2 ulps, the argument, 1 + e, the
+// quotient and t_o - t_m round once each, so its error is below
+// |t_o - t_m| (1.75 s 2^-22 + 0.28 2^-24) + 2^-24 |v| (s |dz| <= 0.28); with d
+// twice that or more, when v - d and v + d round to the same bf16 so does the
+// exact value.  The rest (about one element in a thousand, near a rounding
+// boundary) are recomputed in fp64 as (e_a t_a + e_b t_b) / (e_a + e_b).  fp64
+// is slow on this part, and a warp recomputing an element stalls its row: with
+// a fix-up list (csa2_build_cache), a lane with such elements appends its
+// (row, lane) and leaves, and a second grid recomputes those 16-channel blocks
+// densely, one per thread; without one (or once the list is full), the warp's
+// lanes recompute theirs together, each taking its next element.
+
+// The 16 channels of lane block g of output row `row`: the fp32 values (x,
+// rounded down where ambiguous) and the mask of channels to recompute, with
+// the inputs the recomputation needs.
+struct Kv2Block {
+  float x[16], t0[16], t1[16], za[16], zb[16];
+  uint32_t redo;
+};
+__device__ __forceinline__ void kv2_block(const uint16_t *__restrict__ src, const float *__restrict__ gate,
+                                          int64_t row, int g, Kv2Block &B) {
+  const uint4 *p0 = reinterpret_cast<const uint4 *>(src + (2 * row) * kDim + g * 16);
+  const uint4 *p1 = reinterpret_cast<const uint4 *>(src + (2 * row + 1) * kDim + g * 16);
+  const float *z0 = gate + (2 * row) * kDim + g * 16;
+  const float *z1 = gate + (2 * row + 1) * kDim + g * 16;
+  uint4 a0 = __ldg(p0), b0 = __ldg(p0 + 1), a1 = __ldg(p1), b1 = __ldg(p1 + 1);
+  uint32_t w0[8] = {a0.x, a0.y, a0.z, a0.w, b0.x, b0.y, b0.z, b0.w};
+  uint32_t w1[8] = {a1.x, a1.y, a1.z, a1.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-    for (int i = 0; i < 8; i++) { x[2 * i] = bf16_lo(w[i]); x[2 * i + 1] = bf16_hi(w[i]); }
-  } else {
-    // gated pooling of tokens 2*row and 2*row+1, rounded once to bf16: the
-    // exact value's rounding.  With the larger logit's token t_m, the other
-    // t_o, e = exp(-|z_a - z_b|) and s = e / (1 + e), the value is
-    // t_m + (t_o - t_m) s.  fp32 first, one FMA: expf is within 2 ulps, the
-    // argument, 1 + e, the quotient and t_o - t_m round once each, so its error
-    // is below |t_o - t_m| (1.75 s 2^-22 + 0.28 2^-24) + 2^-24 |v| (s |dz| <=
-    // 0.28); with d twice that or more, when v - d and v + d round to the same
-    // bf16 so does the exact value.  The rest (about one element in a
-    // thousand, near a rounding boundary) are recomputed in fp64 afterwards as
-    // (e_a t_a + e_b t_b) / (e_a + e_b), all lanes of the warp together, each
-    // taking its next such element.
-    const uint4 *p0 = reinterpret_cast<const uint4 *>(src + (2 * row) * kDim + lane * 16);
-    const uint4 *p1 = reinterpret_cast<const uint4 *>(src + (2 * row + 1) * kDim + lane * 16);
-    const float *z0 = gate + (2 * row) * kDim + lane * 16;
-    const float *z1 = gate + (2 * row + 1) * kDim + lane * 16;
-    uint4 a0 = __ldg(p0), b0 = __ldg(p0 + 1), a1 = __ldg(p1), b1 = __ldg(p1 + 1);
-    uint32_t w0[8] = {a0.x, a0.y, a0.z, a0.w, b0.x, b0.y, b0.z, b0.w};
-    uint32_t w1[8] = {a1.x, a1.y, a1.z, a1.w, b1.x, b1.y, b1.z, b1.w};
-    float za4[16], zb4[16];                           // the logits, 16-B loads
-#pragma unroll
-    for (int v = 0; v < 4; v++) {
-      const float4 ga = __ldg(reinterpret_cast<const float4 *>(z0) + v);
-      const float4 gb = __ldg(reinterpret_cast<const float4 *>(z1) + v);
-      za4[4 * v] = ga.x; za4[4 * v + 1] = ga.y; za4[4 * v + 2] = ga.z; za4[4 * v + 3] = ga.w;
-      zb4[4 * v] = gb.x; zb4[4 * v + 1] = gb.y; zb4[4 * v + 2] = gb.z; zb4[4 * v + 3] = gb.w;
-    }
-    float t0v[16], t1v[16];
-    uint32_t redo = 0u;                               // channels this lane recomputes in fp64
-#pragma unroll
-    for (int i = 0; i < 16; i++) {
-      t0v[i] = (i & 1) ? bf16_hi(w0[i >> 1]) : bf16_lo(w0[i >> 1]);
-      t1v[i] = (i & 1) ? bf16_hi(w1[i >> 1]) : bf16_lo(w1[i >> 1]);
-      const float fa = za4[i], fb = zb4[i];
-      const float tm = fa >= fb ? t0v[i] : t1v[i], to = fa >= fb ? t1v[i] : t0v[i];
-      const float e = expf(-fabsf(fa - fb));
-      const float sg = e / (1.0f + e);
-      const float dl = to - tm;
-      const float vf = fmaf(dl, sg, tm);
-      const float d = fabsf(dl) * fmaf(sg, 0x1p-20f, 0x1p-24f) + fabsf(vf) * 0x1p-23f;
-      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(vf - d));
-      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(vf + d));
-      x[i] = __uint_as_float(lo << 16);
-      redo |= (lo != hi ? 1u : 0u) << i;
-    }
-    while (__any_sync(0xFFFFFFFFu, redo != 0u)) {
-      if (redo != 0u) {
-        const int c = __ffs(redo) - 1;
-        redo &= redo - 1u;
-        float t0 = 0.f, t1 = 0.f, fa = 0.f, fb = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; i++)
-          if (i == c) { t0 = t0v[i]; t1 = t1v[i]; fa = za4[i]; fb = zb4[i]; }
-        const double za = (double)fa, zb = (double)fb;
-        const double e = exp(-fabs(za - zb));
-        const double v = za >= zb ? ((double)t0 + e * (double)t1) / (1.0 + e) : (e * (double)t0 + (double)t1) / (e + 1.0);
-        const float xv = __uint_as_float(bf16_from_f64(v) << 16);
-#pragma unroll
-        for (int i = 0; i < 16; i++)
-          if (i == c) x[i] = xv;
-      }
-    }
-    if (pooled != nullptr) {
-      uint32_t b[8];
-#pragma unroll
-      for (int i = 0; i < 8; i++) b[i] = (__float_as_uint(x[2 * i]) >> 16) | (__float_as_uint(x[2 * i + 1]) & 0xFFFF0000u);
-      uint4 *po = reinterpret_cast<uint4 *>(pooled + row * kDim + lane * 16);
-      po[0] = make_uint4(b[0], b[1], b[2], b[3]);
-      po[1] = make_uint4(b[4], b[5], b[6], b[7]);
-    }
+  for (int v = 0; v < 4; v++) {                     // the logits, 16-B loads
+    const float4 ga = __ldg(reinterpret_cast<const float4 *>(z0) + v);
+    const float4 gb = __ldg(reinterpret_cast<const float4 *>(z1) + v);
+    B.za[4 * v] = ga.x; B.za[4 * v + 1] = ga.y; B.za[4 * v + 2] = ga.z; B.za[4 * v + 3] = ga.w;
+    B.zb[4 * v] = gb.x; B.zb[4 * v + 1] = gb.y; B.zb[4 * v + 2] = gb.z; B.zb[4 * v + 3] = gb.w;
   }
+  B.redo = 0u;
+#pragma unroll
+  for (int i = 0; i < 16; i++) {
+    B.t0[i] = (i & 1) ? bf16_hi(w0[i >> 1]) : bf16_lo(w0[i >> 1]);
+    B.t1[i] = (i & 1) ? bf16_hi(w1[i >> 1]) : bf16_lo(w1[i >> 1]);
+    const float fa = B.za[i], fb = B.zb[i];
+    const float tm = fa >= fb ? B.t0[i] : B.t1[i], to = fa >= fb ? B.t1[i] : B.t0[i];
+    const float e = expf(-fabsf(fa - fb));
+    const float sg = e / (1.0f + e);
+    const float dl = to - tm;
+    const float vf = fmaf(dl, sg, tm);
+    const float d = fabsf(dl) * fmaf(sg, 0x1p-20f, 0x1p-24f) + fabsf(vf) * 0x1p-23f;
+    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(vf - d));
+    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(vf + d));
+    B.x[i] = __uint_as_float(lo << 16);
+    B.redo |= (lo != hi ? 1u : 0u) << i;
+  }
+}
+
+// channel c of the block, recomputed in fp64 and rounded once to bf16
+__device__ __forceinline__ void kv2_recompute(Kv2Block &B, int c) {
+  float t0 = 0.f, t1 = 0.f, fa = 0.f, fb = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; i++)
+    if (i == c) { t0 = B.t0[i]; t1 = B.t1[i]; fa = B.za[i]; fb = B.zb[i]; }
+  const double za = (double)fa, zb = (double)fb;
+  const double e = exp(-fabs(za - zb));
+  const double v = za >= zb ? ((double)t0 + e * (double)t1) / (1.0 + e) : (e * (double)t0 + (double)t1) / (e + 1.0);
+  const float xv = __uint_as_float(bf16_from_f64(v) << 16);
+#pragma unroll
+  for (int i = 0; i < 16; i++)
+    if (i == c) B.x[i] = xv;
+}
+
+// the pooled latents of the block (bf16, 32 B)
+__device__ __forceinline__ void kv2_store_pooled(const float (&x)[16], uint16_t *__restrict__ pooled, int64_t row,
+                                                 int g) {
+  uint32_t b[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) b[i] = (__float_as_uint(x[2 * i]) >> 16) | (__float_as_uint(x[2 * i + 1]) & 0xFFFF0000u);
+  uint4 *po = reinterpret_cast<uint4 *>(pooled + row * kDim + g * 16);
+  po[0] = make_uint4(b[0], b[1], b[2], b[3]);
+  po[1] = make_uint4(b[4], b[5], b[6], b[7]);
+}
+
+// the block's 16 channels -> one E4M3 scale and 8 bytes of E2M1 codes of the
+// record of `row`
+__device__ __forceinline__ void kv_store_record(const float (&x)[16], uint8_t *__restrict__ dst, int64_t row, int g) {
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; i++) amax = fmaxf(amax, fabsf(x[i]));
@@ -168,8 +170,72 @@ __global__ void __launch_bounds__(256) pack_kv_kernel(const uint16_t *__restrict
     nib[1] = cvt_e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
   }
   uint8_t *rec = dst + row * kKvBytes;
-  *reinterpret_cast<uint2 *>(rec + lane * 8) = make_uint2(nib[0], nib[1]);
-  rec[256 + lane] = (uint8_t)sc;
+  *reinterpret_cast<uint2 *>(rec + g * 8) = make_uint2(nib[0], nib[1]);
+  rec[256 + g] = (uint8_t)sc;
+}
+
+template <int M>
+__global__ void __launch_bounds__(256) pack_kv_kernel(const uint16_t *__restrict__ src,
+                                                       const float *__restrict__ gate, int64_t rows_out,
+                                                       uint8_t *__restrict__ dst, uint16_t *__restrict__ pooled,
+                                                       KvFix F) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows_out) return;
+  if (M == 1) {
+    float x[16];
+    const uint4 *p = reinterpret_cast<const uint4 *>(src + row * kDim + lane * 16);
+    uint4 a = __ldg(p), b = __ldg(p + 1);
+    uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; i++) { x[2 * i] = bf16_lo(w[i]); x[2 * i + 1] = bf16_hi(w[i]); }
+    kv_store_record(x, dst, row, lane);
+  } else {
+    Kv2Block B;
+    kv2_block(src, gate, row, lane, B);
+    bool deferred = false;
+    if (F.list != nullptr && B.redo != 0u) {
+      const uint32_t i = atomicAdd(F.cnt, 1u);
+      if (i < F.cap) {
+        F.list[i] = (uint32_t)row * 32u + (uint32_t)lane;
+        deferred = true;
+        B.redo = 0u;
+      }
+    }
+    while (__any_sync(0xFFFFFFFFu, B.redo != 0u)) {
+      if (B.redo != 0u) {
+        const int c = __ffs(B.redo) - 1;
+        B.redo &= B.redo - 1u;
+        kv2_recompute(B, c);
+      }
+    }
+    if (deferred) return;                            // (the fix-up grid writes this block)
+    if (pooled != nullptr) kv2_store_pooled(B.x, pooled, row, lane);
+    kv_store_record(B.x, dst, row, lane);
+  }
+}
+
+// The deferred blocks of one pack_kv_kernel<2> launch, one per thread; then
+// the next launch's list count is zeroed (none of this grid reads it).
+__global__ void __launch_bounds__(256) pack_kv2_fix_kernel(const uint16_t *__restrict__ src,
+                                                            const float *__restrict__ gate, uint8_t *__restrict__ dst,
+                                                            uint16_t *__restrict__ pooled, KvFix F) {
+  const uint32_t n = min(*F.cnt, F.cap);
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const uint32_t e = F.list[i];
+    const int64_t row = e >> 5;
+    const int g = (int)(e & 31u);
+    Kv2Block B;
+    kv2_block(src, gate, row, g, B);
+    while (B.redo != 0u) {
+      const int c = __ffs(B.redo) - 1;
+      B.redo &= B.redo - 1u;
+      kv2_recompute(B, c);
+    }
+    if (pooled != nullptr) kv2_store_pooled(B.x, pooled, row, g);
+    kv_store_record(B.x, dst, row, g);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0 && F.next_cnt != nullptr) *F.next_cnt = 0u;
 }
 
 // smallest e with lim * 2^e >= amax (amax > 0), for lim = 1.5 * 2^p, 1.75 * 2^p
@@ -319,16 +385,25 @@ __global__ void __launch_bounds__(256) pack_swa_kernel(const uint16_t *__restric
 
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_pack(int kind, const void *src, int64_t rows, int m, const float *gate, void *dst,
-                        void *dst_scales, cudaStream_t st, void *pooled) {
+                        void *dst_scales, cudaStream_t st, void *pooled, const KvFix *fix) {
   const uint16_t *s = static_cast<const uint16_t *>(src);
   if (kind == CSA2_KV_NVFP4) {
     const int64_t out_rows = rows / m;
     const int64_t blocks = (out_rows + 7) / 8;
-    if (m == 1)
-      pack_kv_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(s, nullptr, out_rows, (uint8_t *)dst, nullptr);
-    else
+    const KvFix none = {nullptr, nullptr, 0u, nullptr};
+    if (m == 1) {
+      pack_kv_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(s, nullptr, out_rows, (uint8_t *)dst, nullptr, none);
+    } else {
+      const KvFix F = fix != nullptr && out_rows * 32 < ((int64_t)1 << 32) ? *fix : none;
       pack_kv_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(s, gate, out_rows, (uint8_t *)dst,
-                                                          static_cast<uint16_t *>(pooled));
+                                                          static_cast<uint16_t *>(pooled), F);
+      if (F.list != nullptr) {
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        pack_kv2_fix_kernel<<<(unsigned)(2 * device_sm_count(current_device())), 256, 0, st>>>(
+            s, gate, (uint8_t *)dst, static_cast<uint16_t *>(pooled), F);
+      }
+    }
   } else if (kind == CSA2_IDX_MXFP4) {
     const int64_t blocks = (rows * 8 + 255) / 256;
     pack_idx_kernel<<<(unsigned)blocks, 256, 0, st>>>(s, rows, (uint8_t *)dst, (uint8_t *)dst_scales);

@@ -114,10 +114,12 @@ def test_workspace_sizes(lib):
     assert lib.csa2_workspace_size(lib.CSA2_OP_SPARSE_ATTN, 8192, 640) == 0      # no split for big batches
     # the Reindex step: the pool's scores and block maxima come first
     assert lib.csa2_workspace_size(lib.CSA2_OP_DECODE_REINDEX, 8, 1 << 20, 512) >= 8 * (16384 + 2048) * 4
-    # the cache build's scratch: one chunk of at most 131,072 entries (keys; pooled latents for m = 2)
-    assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 1 << 20, 2) == 131072 * (128 + 512) * 2
+    # the cache build's scratch: one chunk of at most 131,072 entries (keys; for m = 2 the pooled
+    # latents, two counts and the pooling's fix-up list of four words per entry)
+    assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 1 << 20, 2) == \
+        131072 * (128 + 512) * 2 + 256 + 131072 * 4 * 4
     assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 1 << 20, 1) == 131072 * 128 * 2
-    assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 64, 2) == 32 * (128 + 512) * 2
+    assert lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 64, 2) == 32 * (128 + 512) * 2 + 256 + 512
     with pytest.raises(lib.CSA2Error):
         lib.csa2_workspace_size(lib.CSA2_OP_BUILD_CACHE, 0, 64, 3)
     with pytest.raises(lib.CSA2Error):
