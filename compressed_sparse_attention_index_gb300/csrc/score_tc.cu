@@ -240,7 +240,8 @@ struct PoolGather {
   int pre_b[kPoolAhead];
   __device__ int load_b(const ScoreTcArgs &P, int g, uint32_t T) const {
     const int lane = threadIdx.x & 31;
-    const int q = (int)(T / (uint32_t)P.units_per_q), u = (int)(T - (uint32_t)q * (uint32_t)P.units_per_q);
+    constexpr uint32_t upq = kPoolSlots / kUnit;   // (pool mode: a power of two)
+    const int q = (int)(T / upq), u = (int)(T - (uint32_t)q * upq);
     return __ldg(P.pool + (int64_t)q * kPoolBlocks + u * (kUnit / kBlock) + g * kPoolWarpBlocks +
                  (lane & (kPoolWarpBlocks - 1)));
   }
@@ -351,7 +352,11 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
     abort_flag = 1;
   };
 
-  const uint32_t total_units = (uint32_t)P.n_q * (uint32_t)P.units_per_q;
+  // units per query: in pool mode a compile-time power of two (the divisions
+  // below become shifts; each role divides on every unit, the query changing
+  // on nearly every one there)
+  const uint32_t upq = POOL ? (uint32_t)(kPoolSlots / kUnit) : (uint32_t)P.units_per_q;
+  const uint32_t total_units = (uint32_t)P.n_q * upq;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = ptx::policy_evict_first();
@@ -421,8 +426,8 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       int uq = 0;
       for (;;) {
         if (T >= total_units) { T = kDone; break; }
-        const int q = (int)(T / (uint32_t)P.units_per_q);
-        uq = (int)(T - (uint32_t)q * (uint32_t)P.units_per_q);
+        const int q = (int)(T / upq);
+        uq = (int)(T - (uint32_t)q * upq);
         sc.set(P, q, uq, lane == 0);
         if (sc.nv >= 0 && (POOL || uq * kUnit < sc.nv)) break;
         T = advance(T);
@@ -489,7 +494,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         }
         if (lane == 0) ptx::mbar_arrive(&full_bar[s]);
         pg.gather(P, 0, T, row0, st, &full_bar[s], total_units);
-        if (T + gridDim.x < total_units) sc.prefetch(P, (int)((T + gridDim.x) / (uint32_t)P.units_per_q));
+        if (T + gridDim.x < total_units) sc.prefetch(P, (int)((T + gridDim.x) / upq));
       }
       __syncwarp();
       if (lane == 0) armed_sh = (int)it + 1;
@@ -504,7 +509,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       if (!ring_get(unit_ring, it, T, abort_flag)) { fail(); break; }
       if (T == kDone) break;
       const uint32_t s = it % kScStages, r = it / kScStages;
-      const bool fresh = qs.step((int)(T / (uint32_t)P.units_per_q), (int)it);
+      const bool fresh = qs.step((int)(T / upq), (int)it);
       if (!ptx::mbar_wait(&full_bar[s], r & 1)) { fail(); break; }
       unsigned char *st = smem + s * kScStageBytes;
       unsigned char *qd = qslots + qs.slot * kScQBytes;
@@ -556,7 +561,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         uint32_t T;
         if (!ring_get(unit_ring, it, T, abort_flag)) { fail(); break; }
         if (T == kDone) break;
-        qs.step((int)(T / (uint32_t)P.units_per_q), (int)it);
+        qs.step((int)(T / upq), (int)it);
         if ((it & 1) != par) continue;
         const uint32_t s = it % kScStages, r = it / kScStages, a = it % kScAcc, ra = it / kScAcc;
         if (!ptx::mbar_wait(&sf_bar[s], r & 1) || !ptx::mbar_wait(&acc_empty[a], (ra & 1) ^ 1)) { fail(); break; }
@@ -594,11 +599,11 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
         if (!ring_get(unit_ring, it, T, abort_flag)) { fail(); break; }
         if (T == kDone) break;
         const uint32_t s = it % kScStages, r = it / kScStages;
-        const int q = (int)(T / (uint32_t)P.units_per_q), u = (int)(T % (uint32_t)P.units_per_q);
+        const int q = (int)(T / upq), u = (int)(T % upq);
         gq.set(P, q, u, false);                       // published units are valid
         if (!ptx::mbar_wait(&done_bar[s], (r & 1) ^ 1)) { fail(); break; }
         pg.gather(P, g, T, (int64_t)gq.seq * P.n_max, smem + s * kScStageBytes, &full_bar[s], total_units);
-        if (T + gridDim.x < total_units) gq.prefetch(P, (int)((T + gridDim.x) / (uint32_t)P.units_per_q));
+        if (T + gridDim.x < total_units) gq.prefetch(P, (int)((T + gridDim.x) / upq));
       }
     }
   } else {
@@ -623,7 +628,7 @@ __global__ void __launch_bounds__(kScThreads, 1) index_score_tc_kernel(ScoreTcAr
       if (T == kDone) break;
       if (!POOL && (it & 1) != group) continue;
       const uint32_t acc = POOL ? (it & 1) : group;
-      const int cur_u = (int)(T % (uint32_t)P.units_per_q), nq = (int)(T / (uint32_t)P.units_per_q);
+      const int cur_u = (int)(T % upq), nq = (int)(T / upq);
       const uint32_t s = it % kScStages, r = it / kScStages;
       auto load_w = [&]() {
         const float4 *wp = reinterpret_cast<const float4 *>(P.w + (int64_t)nq * kIdxHeads);
