@@ -48,9 +48,9 @@ IDX_BYTES = 68
 # dram__bytes_read.sum + dram__bytes_write.sum of one index_score_tc_kernel launch inside
 # csa2_decode, from an ncu capture (--metrics dram__bytes_read.sum,dram__bytes_write.sum) of the
 # current kernel on the named workload; workloads without such a capture report null.
-INDEX_SCORE_TRAFFIC = {"long_full_decode_N1M_B8_zipf": 570_489_344 + 5_250_304,
+INDEX_SCORE_TRAFFIC = {"long_full_decode_N1M_B8_zipf": 570_488_832 + 4_995_328,
                        "full_decode_N65536_B32": 142_722_048 + 4_186_880,
-                       "reindex_decode_N1M_B64": 84_276_736 + 1_779_200}
+                       "reindex_decode_N1M_B64": 84_265_984 + 1_812_480}
 
 
 def parse():
