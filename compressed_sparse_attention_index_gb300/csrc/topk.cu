@@ -1184,7 +1184,7 @@ __global__ void __launch_bounds__(kCollectThreads) topk_collect_kernel(TopkSrc S
       const int64_t g_valid = (int64_t)ns * gps;                 // groups of the supergroups holding valid entries
       for (int64_t b0 = g_lo, j = 0; b0 < g_hi; b0 += blockDim.x, j++) {   // uniform trip count
         const int64_t gid = b0 + threadIdx.x;
-        const uint32_t m0 = gpre[0];                             // this round's prefetched maximum
+        const uint32_t m0 = gpre[0];                             // this pass's prefetched maximum
 #pragma unroll
         for (int t = 0; t + 1 < kGPre; t++) gpre[t] = gpre[t + 1];
         gpre[kGPre - 1] = 0u;
